@@ -1,0 +1,71 @@
+"""The pins must be sensitive: plant plausible mistakes in a copy of the
+oracle's C source, build it, and check that at least one pin fails for each.
+
+The mistakes are planted on the CPU, in a temporary copy; the committed
+oracle is untouched.
+"""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "oracle.c")
+
+# (name, text in oracle.c, replacement)
+MUTANTS = [
+    ("dropped 1/sqrt2 in phi", "x[a] * x[b] * inv_sqrt2", "x[a] * x[b]"),
+    ("column-major quadratic block", "phi[1 + dfeat + a * dfeat + b] = x[a] * x[b] * inv_sqrt2",
+     "phi[1 + dfeat + a * dfeat + b] = x[a] * x[(b + 1) % dfeat] * inv_sqrt2"),
+    ("normaliser not accumulated", "z[r] += phk[r];", "z[r] = phk[r];"),
+    ("eps forced to one", "y[c] = nm / (dn + j->eps);", "y[c] = nm / (dn + 1.0);"),
+    ("delta-rule sign flipped", "al * (S[i * dk + a] - be * Sk[i] * kt[a])", "al * (S[i * dk + a] + be * Sk[i] * kt[a])"),
+    ("write decayed by alpha", "+ be * vt[i] * kt[a];", "+ al * be * vt[i] * kt[a];"),
+    ("beta dropped from erase", "al * (S[i * dk + a] - be * Sk[i] * kt[a])", "al * (S[i * dk + a] - Sk[i] * kt[a])"),
+    ("query read with the key", "acc += S[i * dk + a] * qt[a];", "acc += S[i * dk + a] * kt[a];"),
+    ("state_in ignored", "S[i] = j->s_in ? j->s_in[bh * dv * dk + i] : 0.0;", "S[i] = 0.0;"),
+]
+
+PIN_FUNCS = [
+    lambda: pins.test_feature_inner_product_is_closed_form_kernel(4),
+    pins.test_feature_layout_row_major_and_constant_term,
+    lambda: pins.test_taylor_equals_quadratic_form(4, 5, 37),
+    pins.test_taylor_state_invariants,
+    pins.test_taylor_zero_query_is_running_mean,
+    lambda: pins.test_gdn_equals_dense_matrix_form(6, 5, 23),
+    pins.test_gdn_reduces_to_additive_for_orthogonal_keys,
+    pins.test_gdn_beta_zero_pure_decay,
+    pins.test_gdn_overwrite_property_unit_keys,
+    pins.test_gdn_q_scale_split_and_samples,
+]
+
+
+def _caught(fn) -> bool:
+    try:
+        fn()
+    except AssertionError:
+        return True
+    return False
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    text = open(SRC).read()
+    assert old in text, f"mutation anchor for '{name}' not found in oracle.c"
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(old, new, 1))
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-std=c11", "-o", str(so), str(src), "-lm"],
+                   check=True)
+    oracle._load()
+    prev = oracle.load_library(str(so))
+    try:
+        caught = [_caught(f) for f in PIN_FUNCS]
+    finally:
+        oracle.restore_library(prev)
+    assert any(caught), f"no pin caught the planted mistake '{name}'"

@@ -1,0 +1,347 @@
+"""Pins for the fp64 oracle, checked against things other than the oracle itself.
+
+Each test states what fixes the expected value: a closed form the pages give,
+brute force of a different formula (the quadratic/attention form, the dense
+matrix form of the recurrence), exact rational arithmetic, invariants and
+special cases that reduce to textbook results, or dimension facts the pages
+print (tests/golden/).  CPU only.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+rng = np.random.default_rng(12345)
+
+
+def rel_err(x, ref):
+    return float(np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-300))
+
+
+def taylor_kernel(q, k):
+    """K(q,k) = 1 + q.k + (q.k)^2/2 (BASED notes Sec. 2.3, paper Eq. (4))."""
+    t = float(np.dot(q, k))
+    return 1.0 + t + 0.5 * t * t
+
+
+def f32(shape, scale=1.0):
+    return (rng.standard_normal(shape) * scale).astype(np.float32)
+
+
+# --------------------------------------------------------------------------
+# Feature map: closed form and dimensions
+
+
+@pytest.mark.parametrize("df", [1, 2, 4, 16])
+def test_feature_inner_product_is_closed_form_kernel(df):
+    for _ in range(20):
+        q = rng.standard_normal(df)
+        k = rng.standard_normal(df)
+        got = float(np.dot(oracle.taylor_feature(q), oracle.taylor_feature(k)))
+        assert got == pytest.approx(taylor_kernel(q, k), rel=1e-13, abs=1e-13)
+
+
+def test_feature_dims_match_pages():
+    g = json.load(open(os.path.join(GOLDEN, "taylor_feature_dims.json")))
+    assert oracle.taylor_dim(16) == g["full_outer_product"]["16"]
+    phi = oracle.taylor_feature(rng.standard_normal(16))
+    assert phi.size == 273
+    assert 273 <= g["hardware_padded_multiple_of_64"]["16"] and g["hardware_padded_multiple_of_64"]["16"] % 64 == 0
+    # The full map repeats each cross term twice; the number of distinct
+    # monomials is the compact dimension the pages print.
+    for df_s, compact in g["compact_symmetric"].items():
+        if not df_s.isdigit():
+            continue
+        df = int(df_s)
+        x = rng.standard_normal(df) + 3.0  # generic point: distinct monomials have distinct values
+        phi = oracle.taylor_feature(x)
+        assert phi.size == 1 + df + df * df
+        assert len(np.unique(np.round(phi, 12))) == compact
+
+
+def test_feature_layout_row_major_and_constant_term():
+    x = np.arange(1, 5, dtype=np.float64)
+    phi = oracle.taylor_feature(x)
+    assert phi[0] == 1.0
+    assert np.array_equal(phi[1:5], x)
+    quad = phi[5:].reshape(4, 4)
+    assert np.allclose(quad, np.outer(x, x) / math.sqrt(2.0), rtol=0, atol=1e-15)
+
+
+def test_denominator_positivity_identity():
+    # 1 + t + t^2/2 = ((t+1)^2 + 1)/2 >= 1/2  (BASED notes Sec. 2.3)
+    for t in np.linspace(-10, 10, 101):
+        assert 1 + t + t * t / 2 == pytest.approx(((t + 1) ** 2 + 1) / 2, rel=1e-14)
+        assert 1 + t + t * t / 2 >= 0.5
+
+
+# --------------------------------------------------------------------------
+# Taylor recurrence vs the quadratic (attention) form
+
+
+def quadratic_form(q, k, v):
+    """y_i = sum_{j<=i} K(q_i,k_j) v_j / sum_{j<=i} K(q_i,k_j), by brute force."""
+    B, H, N, _ = q.shape
+    y = np.zeros(v.shape, dtype=np.float64)
+    den = np.zeros((B, H, N))
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                w = np.array([taylor_kernel(q[b, h, i].astype(np.float64), k[b, h, j].astype(np.float64))
+                              for j in range(i + 1)])
+                y[b, h, i] = w @ v[b, h, : i + 1].astype(np.float64) / w.sum()
+                den[b, h, i] = w.sum()
+    return y, den
+
+
+@pytest.mark.parametrize("df,dv,N", [(4, 5, 37), (16, 8, 40)])
+def test_taylor_equals_quadratic_form(df, dv, N):
+    q = f32((1, 2, N, df), 1 / math.sqrt(df))
+    k = f32((1, 2, N, df), 1 / math.sqrt(df))
+    v = f32((1, 2, N, dv))
+    out = oracle.taylor(q, k, v, want_den=True, nthreads=2)
+    y_ref, den_ref = quadratic_form(q, k, v)
+    assert rel_err(out["y"], y_ref) < 1e-12
+    assert rel_err(out["den"], den_ref) < 1e-12
+
+
+def test_taylor_exact_rational_example():
+    """Dyadic inputs, exact Fraction arithmetic of the quadratic form."""
+    q = np.array([[0.5, -0.25], [1.0, 0.75], [-0.5, 0.5], [0.25, 0.125]], dtype=np.float32)
+    k = np.array([[0.25, 0.5], [-1.0, 0.5], [0.75, -0.25], [0.5, 0.5]], dtype=np.float32)
+    v = np.array([[1.0, -2.0], [0.5, 3.0], [-1.5, 0.25], [2.0, 1.0]], dtype=np.float32)
+    out = oracle.taylor(q[None, None], k[None, None], v[None, None])
+
+    def K(a, b):
+        t = sum(Fraction(float(x)) * Fraction(float(y)) for x, y in zip(a, b))
+        return 1 + t + t * t / 2
+
+    for i in range(4):
+        w = [K(q[i], k[j]) for j in range(i + 1)]
+        for c in range(2):
+            exact = sum(wj * Fraction(float(v[j, c])) for j, wj in enumerate(w)) / sum(w)
+            assert out["y"][0, 0, i, c] == pytest.approx(float(exact), rel=1e-15, abs=1e-15)
+
+
+def test_taylor_state_invariants():
+    df, dv, N = 16, 8, 50
+    q = f32((2, 2, N, df), 0.25)
+    k = f32((2, 2, N, df), 0.25)
+    v = f32((2, 2, N, dv))
+    out = oracle.taylor(q, k, v, want_den=True)
+    s, z = out["s"], out["z"]
+    kd, vd = k.astype(np.float64), v.astype(np.float64)
+    # constant row: z[0] = N, s[0] = sum v
+    assert np.all(z[..., 0] == N)
+    assert np.allclose(s[..., 0, :], vd.sum(axis=2), rtol=1e-13, atol=1e-12)
+    # linear rows: sum k v^T
+    assert np.allclose(s[..., 1:1 + df, :], np.einsum("bhna,bhnc->bhac", kd, vd), rtol=1e-12, atol=1e-12)
+    # quadratic rows, row-major (a,b): sum k_a k_b v / sqrt 2 ; symmetric bit-for-bit
+    quad = s[..., 1 + df:, :].reshape(2, 2, df, df, dv)
+    ref = np.einsum("xhna,xhnm,xhnc->xhamc", kd, kd, vd) / math.sqrt(2.0)
+    assert np.allclose(quad, ref, rtol=1e-12, atol=1e-12)
+    assert np.array_equal(quad, np.swapaxes(quad, 2, 3))
+    # z rows: sum of features
+    assert np.allclose(z[..., 1:1 + df], kd.sum(axis=2), rtol=1e-12, atol=1e-12)
+    # denominator >= i/2 for the 1-based prefix length i
+    i = np.arange(1, N + 1)
+    assert np.all(out["den"] >= i / 2 - 1e-12)
+
+
+def test_taylor_zero_query_is_running_mean():
+    df, dv, N = 16, 6, 30
+    q = np.zeros((1, 1, N, df), np.float32)
+    k = f32((1, 1, N, df), 0.25)
+    v = f32((1, 1, N, dv))
+    y = oracle.taylor(q, k, v)["y"][0, 0]
+    ref = np.cumsum(v[0, 0].astype(np.float64), axis=0) / np.arange(1, N + 1)[:, None]
+    assert rel_err(y, ref) < 1e-13
+
+
+def test_taylor_split_resume_and_samples():
+    df, dv, N = 16, 8, 45
+    q = f32((1, 3, N, df), 0.25)
+    k = f32((1, 3, N, df), 0.25)
+    v = f32((1, 3, N, dv))
+    full = oracle.taylor(q, k, v)
+    a = oracle.taylor(q[:, :, :17], k[:, :, :17], v[:, :, :17])
+    b = oracle.taylor(q[:, :, 17:], k[:, :, 17:], v[:, :, 17:], s_in=a["s"], z_in=a["z"])
+    assert rel_err(np.concatenate([a["y"], b["y"]], axis=2), full["y"]) < 1e-13
+    assert rel_err(b["s"], full["s"]) < 1e-13 and rel_err(b["z"], full["z"]) < 1e-13
+    t = [0, 5, 17, 44]
+    smp = oracle.taylor(q, k, v, t_samples=t)
+    assert np.array_equal(smp["y"], full["y"][:, :, t])
+
+
+def test_bf16_bits_decode_like_float32():
+    x = f32((1, 1, 20, 16), 0.25)
+    bits = (x.view(np.uint32) >> 16).astype(np.uint16)           # truncate to bf16
+    xr = (bits.astype(np.uint32) << 16).view(np.float32)          # the same values as fp32
+    v = f32((1, 1, 20, 4))
+    vbits = (v.view(np.uint32) >> 16).astype(np.uint16)
+    vr = (vbits.astype(np.uint32) << 16).view(np.float32)
+    a = oracle.taylor(bits, bits, vbits)
+    b = oracle.taylor(xr, xr, vr)
+    assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["s"], b["s"])
+
+
+# --------------------------------------------------------------------------
+# Gated delta rule
+
+
+def dense_eq1(q, k, v, alpha, beta, S0):
+    """S_t = S_{t-1} A_t + beta_t v_t k_t^T with A_t = alpha_t (I - beta_t k_t k_t^T)
+    formed as a dense d_k x d_k matrix; o_t = S_t q_t (NoteBank Sec. 2 Eq. (1))."""
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, H, N, dv))
+    S_out = np.zeros((B, H, dv, dk))
+    I = np.eye(dk)
+    for b in range(B):
+        for h in range(H):
+            S = S0[b, h].copy()
+            for t in range(N):
+                kt = k[b, h, t].astype(np.float64)
+                A = float(alpha[b, h, t]) * (I - float(beta[b, h, t]) * np.outer(kt, kt))
+                S = S @ A + float(beta[b, h, t]) * np.outer(v[b, h, t].astype(np.float64), kt)
+                o[b, h, t] = S @ q[b, h, t].astype(np.float64)
+            S_out[b, h] = S
+    return o, S_out
+
+
+def gdn_rand(B, H, N, dk, dv):
+    q = f32((B, H, N, dk))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = f32((B, H, N, dk))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = f32((B, H, N, dv))
+    beta = (1 / (1 + np.exp(-rng.standard_normal((B, H, N))))).astype(np.float32)
+    alpha = np.exp(-rng.uniform(0.001, 0.1, (B, H, N))).astype(np.float32)
+    return q.astype(np.float32), k.astype(np.float32), v, alpha, beta
+
+
+@pytest.mark.parametrize("dk,dv,N", [(6, 5, 23), (8, 8, 31)])
+def test_gdn_equals_dense_matrix_form(dk, dv, N):
+    q, k, v, alpha, beta = gdn_rand(2, 2, N, dk, dv)
+    S0 = rng.standard_normal((2, 2, dv, dk))
+    out = oracle.gdn(q, k, v, alpha, beta, S_in=S0)
+    o_ref, S_ref = dense_eq1(q, k, v, alpha, beta, S0)
+    assert rel_err(out["o"], o_ref) < 1e-12
+    assert rel_err(out["S"], S_ref) < 1e-12
+
+
+def test_gdn_reduces_to_additive_for_orthogonal_keys():
+    """alpha = 1, beta = 1 and each key orthogonal to all earlier keys:
+    A_t acts as I on the state, so S_t = sum_{j<=t} v_j k_j^T (additive
+    linear attention, NoteBank Sec. 2)."""
+    dk, dv, N = 16, 7, 12
+    # rows of a 16x16 Sylvester Hadamard matrix / 4: entries +-1/4, exactly
+    # orthonormal in binary floating point; random order and signs
+    had = np.array([[1.0]])
+    while had.shape[0] < dk:
+        had = np.block([[had, had], [had, -had]])
+    rows = rng.permutation(dk)[:N]
+    signs = rng.choice([-1.0, 1.0], N)
+    k = (had[rows] * signs[:, None] / 4.0).astype(np.float32)[None, None]
+    q = f32((1, 1, N, dk))
+    v = f32((1, 1, N, dv))
+    ones = np.ones((1, 1, N), np.float32)
+    out = oracle.gdn(q, k, v, ones, ones)
+    kd, vd, qd = k[0, 0].astype(np.float64), v[0, 0].astype(np.float64), q[0, 0].astype(np.float64)
+    S = np.zeros((dv, dk))
+    for t in range(N):
+        S = S + np.outer(vd[t], kd[t])
+        assert np.allclose(out["o"][0, 0, t], S @ qd[t], rtol=1e-10, atol=1e-10)
+    assert np.allclose(out["S"][0, 0], S, rtol=1e-10, atol=1e-10)
+
+
+def test_gdn_beta_zero_pure_decay():
+    dk, dv, N = 8, 4, 20
+    q, k, v, alpha, _ = gdn_rand(1, 2, N, dk, dv)
+    S0 = rng.standard_normal((1, 2, dv, dk))
+    out = oracle.gdn(q, k, v, alpha, np.zeros_like(alpha), S_in=S0)
+    g = np.cumprod(alpha.astype(np.float64), axis=-1)
+    for h in range(2):
+        for t in range(N):
+            assert np.allclose(out["o"][0, h, t], g[0, h, t] * (S0[0, h] @ q[0, h, t]), rtol=1e-12, atol=1e-12)
+        assert np.allclose(out["S"][0, h], g[0, h, -1] * S0[0, h], rtol=1e-12, atol=1e-14)
+    # alpha = 1, beta = 0: the state never changes
+    one = np.ones_like(alpha)
+    out = oracle.gdn(q, k, v, one, np.zeros_like(alpha), S_in=S0)
+    assert np.array_equal(out["S"], S0)
+
+
+def test_gdn_overwrite_property_unit_keys():
+    """||k_t|| = 1 exactly => S_t k_t = alpha_t (1 - beta_t) S_{t-1} k_t + beta_t v_t;
+    with beta = 1 the key reads back exactly its value (delta-rule overwrite)."""
+    dk, dv, N = 16, 5, 25
+    k = np.zeros((1, 1, N, dk), np.float32)
+    for t in range(N):  # four entries of +-1/2: unit norm in exact arithmetic
+        idx = rng.choice(dk, 4, replace=False)
+        k[0, 0, t, idx] = rng.choice([-0.5, 0.5], 4)
+    q = f32((1, 1, N, dk))
+    v = f32((1, 1, N, dv))
+    alpha = np.exp(-rng.uniform(0.001, 0.1, (1, 1, N))).astype(np.float32)
+    beta = (1 / (1 + np.exp(-rng.standard_normal((1, 1, N))))).astype(np.float32)
+    S_prev = np.zeros((dv, dk))
+    for t in range(N):
+        o = oracle.gdn(q[:, :, : t + 1], k[:, :, : t + 1], v[:, :, : t + 1], alpha[:, :, : t + 1], beta[:, :, : t + 1])
+        S_t = o["S"][0, 0]
+        kt = k[0, 0, t].astype(np.float64)
+        lhs = S_t @ kt
+        rhs = float(alpha[0, 0, t]) * (1 - float(beta[0, 0, t])) * (S_prev @ kt) + float(beta[0, 0, t]) * v[0, 0, t].astype(np.float64)
+        assert np.allclose(lhs, rhs, rtol=1e-12, atol=1e-12)
+        S_prev = S_t
+    ones = np.ones((1, 1, N), np.float32)
+    o = oracle.gdn(q, k, v, ones, ones)
+    # last key reads back the last value exactly
+    assert np.allclose(o["S"][0, 0] @ k[0, 0, -1].astype(np.float64), v[0, 0, -1], rtol=1e-13, atol=1e-13)
+
+
+def test_gdn_q_scale_split_and_samples():
+    dk, dv, N = 8, 6, 40
+    q, k, v, alpha, beta = gdn_rand(1, 3, N, dk, dv)
+    full = oracle.gdn(q, k, v, alpha, beta)
+    half = oracle.gdn(q, k, v, alpha, beta, q_scale=0.5)
+    assert rel_err(half["o"], 0.5 * full["o"]) < 1e-14
+    a = oracle.gdn(q[:, :, :13], k[:, :, :13], v[:, :, :13], alpha[:, :, :13], beta[:, :, :13])
+    b = oracle.gdn(q[:, :, 13:], k[:, :, 13:], v[:, :, 13:], alpha[:, :, 13:], beta[:, :, 13:], S_in=a["S"])
+    assert rel_err(np.concatenate([a["o"], b["o"]], axis=2), full["o"]) < 1e-13
+    assert rel_err(b["S"], full["S"]) < 1e-13
+    t = [3, 13, 39]
+    smp = oracle.gdn(q, k, v, alpha, beta, t_samples=t)
+    assert np.array_equal(smp["o"], full["o"][:, :, t])
+
+
+def test_gdn_state_size_arithmetic():
+    g = json.load(open(os.path.join(GOLDEN, "state_size.json")))
+    q, k, v, alpha, beta = gdn_rand(1, 1, 2, 4, 3)
+    S = oracle.gdn(q, k, v, alpha, beta)["S"]
+    assert S.shape[-2:] == (3, 4)  # d_v x d_k
+    assert g["J"] * g["d_v"] * g["d_k"] * g["bytes_per_element"] == g["MiB"] * 2 ** 20
+
+
+def test_rejects_bad_samples():
+    q, k, v, alpha, beta = gdn_rand(1, 1, 5, 4, 3)
+    with pytest.raises(ValueError):
+        oracle.gdn(q, k, v, alpha, beta, t_samples=[3, 1])
+    with pytest.raises(ValueError):
+        oracle.taylor(q, k, v[..., :3], t_samples=[7])
+
+
+def test_empty_sequence_passes_state_through():
+    q = np.zeros((1, 2, 0, 16), np.float32)
+    v = np.zeros((1, 2, 0, 8), np.float32)
+    s0 = rng.standard_normal((1, 2, 273, 8))
+    z0 = rng.standard_normal((1, 2, 273))
+    out = oracle.taylor(q, q, v, s_in=s0, z_in=z0)
+    assert np.array_equal(out["s"], s0) and np.array_equal(out["z"], z0)
+    S0 = rng.standard_normal((1, 2, 8, 16))
+    out = oracle.gdn(q, q, v, np.zeros((1, 2, 0), np.float32), np.zeros((1, 2, 0), np.float32), S_in=S0)
+    assert np.array_equal(out["S"], S0)
