@@ -1,0 +1,461 @@
+"""Benchmark of the causal linear-attention hot path on GB300.
+
+One step = one pass of every hot-path row on synthetic inputs resident in
+HBM.  The headline line (``value``) is the BASED Taylor prefill,
+B=8, H=16, N=4096, d'=16, d_v=64, bf16 in / fp32 state, in tokens/s (B*N per
+step).  The same run also times, under ``paths``:
+  gdn_prefill       Gated DeltaNet prefill B=4, H=16, N=16384, d=128
+  gdn_prefill_long  Gated DeltaNet prefill B=1, H=16, N=1,048,576, d=128
+  decode_gdn        1000 decode steps, 256 seqs x 16 heads, 128x128 state
+  decode_taylor     1000 decode steps, 256 seqs x 16 heads, 273x64 state + z
+each with its own tokens/s and roofline.
+
+Timing: W untimed warm-up steps, then K steps; each launch is bracketed by
+CUDA events on its own stream and an L2 flush (a 512 MiB write, outside the
+events) separates timed steps.  Multi-GPU (torchrun): each rank runs its own
+copy of the workload (weak scaling, no collective on the data path); the
+per-rank times are max-reduced.  ``--impl reference`` times the fp64 CPU
+oracle (the only reference there is for this method) on the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synthetic  # noqa: E402
+
+L2_FLUSH_BYTES = 512 << 20
+HEADLINE = "based_prefill"
+METRIC = "prefill & decode tokens/s on 1 GB300; % of tensor-core / HBM roofline (ncu)"
+
+# Algorithmic HBM bytes per token-head (inputs read once, outputs written once):
+#  Taylor prefill  q,k (2*16*2 B) + v (64*2 B) + y (64*2 B)                    = 320 B
+#  GDN prefill     q,k,v (3*128*2 B) + o (128*2 B) + alpha,beta (2*4 B)        = 1032 B
+#  GDN decode      state read+write 2*128*128*4 + q,k,v,o 4*128*2 + alpha,beta = 132,104 B
+#  Taylor decode   (s,z) read+write 2*(273*64+273)*4 + q,k 2*16*2 + v,y 2*64*2  = 142,248 B
+# plus, for prefill, the final fp32 state written once per (b,h).
+BYTES_PER_TOKEN_HEAD = {"taylor_prefill": 320, "gdn_prefill": 1032,
+                        "gdn_decode": 2 * 128 * 128 * 4 + 4 * 128 * 2 + 8,
+                        "taylor_decode": 2 * (273 * 64 + 273) * 4 + 2 * 16 * 2 + 2 * 64 * 2}
+STATE_BYTES = {"taylor": (273 * 64 + 273) * 4, "gdn": 128 * 128 * 4}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def kernel_sources_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "linear_attention_recurrence_chunked_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(key):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel
+    sources are unchanged since it was taken; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(key)
+    if not d:
+        return None
+    if d.get("source_sha") != kernel_sources_sha(d.get("sources", [])):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during timing."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower().startswith("active"):
+                    reasons.add(name)
+        loaded = [x for x in sm if x > 0.5 * (max(sm) if sm else 0)]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+
+
+class Timer:
+    """Per-launch CUDA-event timing on one stream, L2 flushed between launches."""
+
+    def __init__(self, stream, flush_buf):
+        self.stream = stream
+        self.flush_buf = flush_buf
+        self.events = []
+
+    def run(self, fn, flush=True):
+        with torch.cuda.stream(self.stream):
+            if flush:
+                self.flush_buf.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+        self.events.append((a, b))
+
+    def total_ms(self):
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in self.events)
+
+    def reset(self):
+        self.events = []
+
+
+def max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def roofline(bytes_per_launch, ms_per_launch, peak_gbs, traffic):
+    ach = bytes_per_launch / (ms_per_launch * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": peak_gbs, "unit": "GB/s",
+            "frac": round(ach / peak_gbs, 4), "traffic": traffic,
+            "algorithmic_bytes": int(bytes_per_launch)}
+
+
+def gpu_arm(args, ws, rank, local):
+    import linear_attention_recurrence_chunked_gb300 as la
+    from linear_attention_recurrence_chunked_gb300 import _build
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _build.build()
+    la.load_library()
+    pk = peaks()
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    seed_off = 1000 * rank
+    launches = 0
+
+    # --- headline: BASED prefill --------------------------------------------
+    w = synthetic.WORKLOADS[HEADLINE]
+    x = synthetic.workload_inputs(HEADLINE, device=dev, seed=w.seed + seed_off)
+    q, k, v = x["q"], x["k"], x["v"]
+    y = torch.empty((w.B, w.H, w.N, 64), dtype=torch.bfloat16, device=dev)
+    s = torch.empty((w.B, w.H, la.TAYLOR_D, 64), dtype=torch.float32, device=dev)
+    z = torch.empty((w.B, w.H, la.TAYLOR_D), dtype=torch.float32, device=dev)
+
+    def based_step():
+        la.la_based_prefill(q, k, v, y=y, s_out=s, z_out=z, stream=stream)
+
+    timer = Timer(stream, flush)
+    for _ in range(args.warmup):
+        timer.run(based_step)
+    timer.reset()
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(ws)
+    for _ in range(args.steps):
+        timer.run(based_step)
+    ms_total = timer.total_ms()
+    barrier(ws)
+    launches += args.steps * KERNELS_PER_CALL["based_prefill"]
+    ms_total = max_over_ranks(ms_total, ws)
+    ms_step = ms_total / args.steps
+    tokens = w.B * w.N
+    value = ws * tokens * args.steps / (ms_total * 1e-3)
+    bytes_launch = BYTES_PER_TOKEN_HEAD["taylor_prefill"] * w.B * w.H * w.N + STATE_BYTES["taylor"] * w.B * w.H
+    roof = roofline(bytes_launch, ms_step, pk["hbm_gbs"], ncu_traffic("taylor_prefill"))
+    roof["peak_source"] = pk["source"]
+
+    # --- e2e through the C ABI with host buffers ----------------------------
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    hs = torch.empty(s.shape, dtype=s.dtype).pin_memory()
+    hz = torch.empty(z.shape, dtype=z.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        la.la_based_prefill(q, k, v, y=y, s_out=s, z_out=z, stream=stream)
+        hy.copy_(y, non_blocking=True)
+        hs.copy_(s, non_blocking=True)
+        hz.copy_(z, non_blocking=True)
+
+    et = Timer(stream, flush)
+    for _ in range(args.warmup):
+        et.run(e2e_step)
+    et.reset()
+    barrier(ws)
+    for _ in range(args.steps):
+        et.run(e2e_step)
+    e2e_ms = max_over_ranks(et.total_ms(), ws)
+    barrier(ws)
+    launches += args.steps * KERNELS_PER_CALL["based_prefill"]
+    e2e = {"value": ws * tokens * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+           "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (hq, hk, hv))),
+           "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (hy, hs, hz)))}
+    del hq, hk, hv, hy, hs, hz
+
+    paths = {}
+    if not args.headline_only:
+        paths, extra_launches = other_paths(args, la, dev, stream, flush, pk, seed_off, ws)
+        launches += extra_launches
+    clk = clocks.stop()
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.description, "B": w.B, "H": w.H, "N": w.N, "d_feat": 16, "d_v": 64,
+                       "tokens_per_step": tokens, "seed": w.seed, "l2": "flushed between timed steps (512 MiB write)",
+                       "parallelism": f"replicas{ws}" if ws > 1 else "single"},
+            "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clk, "paths": paths}
+    return line
+
+
+KERNELS_PER_CALL = {"based_prefill": 1, "gdn_prefill": 1, "decode": 1}
+
+
+def other_paths(args, la, dev, stream, flush, pk, seed_off, ws):
+    out = {}
+    launches = 0
+    steps = max(1, args.steps)
+    for name in ("gdn_prefill", "gdn_prefill_long"):
+        w = synthetic.WORKLOADS[name]
+        reps = steps if name == "gdn_prefill" else max(1, min(steps, args.long_steps))
+        x = synthetic.workload_inputs(name, device=dev, seed=w.seed + seed_off)
+        o = torch.empty((w.B, w.H, w.N, 128), dtype=torch.bfloat16, device=dev)
+        S = torch.empty((w.B, w.H, 128, 128), dtype=torch.float32, device=dev)
+        ws_t = torch.empty(max(1, la.la_gdn_prefill_workspace_size(x["q"], x["k"], x["v"], x["alpha"], x["beta"])),
+                           dtype=torch.uint8, device=dev)
+
+        def step():
+            la.la_gdn_prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], o=o, S_out=S, workspace=ws_t,
+                              stream=stream)
+
+        t = Timer(stream, flush)
+        for _ in range(min(args.warmup, 3) if name == "gdn_prefill_long" else args.warmup):
+            t.run(step)
+        t.reset()
+        barrier(ws)
+        for _ in range(reps):
+            t.run(step)
+        ms = max_over_ranks(t.total_ms(), ws) / reps
+        launches += reps * KERNELS_PER_CALL["gdn_prefill"]
+        byts = BYTES_PER_TOKEN_HEAD["gdn_prefill"] * w.B * w.H * w.N + STATE_BYTES["gdn"] * w.B * w.H
+        r = roofline(byts, ms, pk["hbm_gbs"], ncu_traffic(name))
+        out[name] = {"workload": w.description, "tokens_per_s": round(ws * w.B * w.N / (ms * 1e-3), 1),
+                     "ms": round(ms, 4), "roofline": r}
+        del x, o, S, ws_t
+        torch.cuda.empty_cache()
+
+    w = synthetic.WORKLOADS["decode"]
+    S_, H_, n_steps = w.B, w.H, w.N
+    for variant in ("gdn", "taylor"):
+        n_inputs = 16  # distinct per-step inputs, cycled (each step still reads its own q, k, v)
+        xs = [synthetic.decode_step_inputs(S_, H_, i, seed=w.seed + seed_off, device=dev)[variant]
+              for i in range(n_inputs)]
+        if variant == "gdn":
+            state = torch.zeros((S_, H_, 128, 128), device=dev)
+            z = None
+        else:
+            state = torch.zeros((S_, H_, la.TAYLOR_D, 64), device=dev)
+            z = torch.zeros((S_, H_, la.TAYLOR_D), device=dev)
+        outb = torch.empty((S_, H_, 128 if variant == "gdn" else 64), dtype=torch.bfloat16, device=dev)
+
+        def run_steps(count):
+            for i in range(count):
+                xi = xs[i % n_inputs]
+                if variant == "gdn":
+                    la.la_decode_step(la.LA_VARIANT_GDN, xi["q"], xi["k"], xi["v"], state, alpha=xi["alpha"],
+                                      beta=xi["beta"], out=outb, stream=stream)
+                else:
+                    la.la_decode_step(la.LA_VARIANT_TAYLOR, xi["q"], xi["k"], xi["v"], state, z=z, out=outb,
+                                      stream=stream)
+
+        t = Timer(stream, flush)
+        t.run(lambda: run_steps(min(n_steps, 50)))  # warm-up
+        t.reset()
+        barrier(ws)
+        t.run(lambda: run_steps(n_steps))  # the state (>L2) is streamed every step
+        ms = max_over_ranks(t.total_ms(), ws)
+        launches += n_steps * KERNELS_PER_CALL["decode"]
+        per_step = ms / n_steps
+        key = f"{variant}_decode"
+        byts = BYTES_PER_TOKEN_HEAD[key] * S_ * H_
+        r = roofline(byts, per_step, pk["hbm_gbs"], ncu_traffic(key))
+        out[f"decode_{variant}"] = {"workload": f"{variant} decode {S_} seqs x {H_} heads x {n_steps} steps",
+                                    "tokens_per_s": round(ws * S_ / (per_step * 1e-3), 1),
+                                    "ms_per_step": round(per_step, 5), "roofline": r}
+        del xs, state, z, outb
+        torch.cuda.empty_cache()
+    return out, launches
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle arm (cpu_baseline and --impl reference)
+
+
+def oracle_taylor_sample(heads=32):
+    """Oracle on a bounded sample of the headline workload: `heads` of its
+    128 (batch, head) pairs over the full N=4096 tokens (seeded on the CPU)."""
+    w = synthetic.WORKLOADS[HEADLINE]
+    B = max(1, heads // w.H)
+    return synthetic.taylor_inputs(B, w.H, w.N, dtype=w.dtype, seed=w.seed), B * w.N
+
+
+def time_oracle_once(inp):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.taylor(*(synthetic.to_oracle(inp[n]) for n in ("q", "k", "v")))
+    return time.perf_counter() - t0
+
+
+def cpu_baseline():
+    import oracle
+    oracle.build()
+    inp, tokens = oracle_taylor_sample()
+    dt = time_oracle_once(inp)
+    return {"value": round(tokens / dt, 1), "unit": "tokens/s", "cores": oracle.default_threads(), "kind": "oracle",
+            "sample": f"fp64 C oracle, 2 of 8 sequences (32 of 128 heads) x N=4096 of the headline workload; "
+                      f"{dt:.2f} s wall"}
+
+
+def reference_arm(args, ws, rank):
+    import oracle
+    if rank != 0:
+        return None
+    oracle.build()
+    inp, tokens = oracle_taylor_sample()
+    for _ in range(args.warmup):
+        time_oracle_once(inp)
+    total = sum(time_oracle_once(inp) for _ in range(args.steps))
+    value = tokens * args.steps / total
+    w = synthetic.WORKLOADS[HEADLINE]
+    cores = oracle.default_threads()
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.description, "B": w.B, "H": w.H, "N": w.N, "d_feat": 16, "d_v": 64,
+                       "tokens_per_step": tokens, "sample": "32 of 128 heads, all 4096 tokens"},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "fp64 C oracle on 2 sequences x 16 heads x 4096 tokens per step"},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--long-steps", type=int, default=3, help="timed passes of the 1M-token prefill")
+    ap.add_argument("--headline-only", action="store_true", help="skip the secondary paths")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        line = reference_arm(args, ws, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    line = gpu_arm(args, ws, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

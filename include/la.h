@@ -1,0 +1,174 @@
+/*
+ * la.h -- C ABI of the GB300 (sm_103a) causal linear-attention library.
+ *
+ * The library computes the generalised linear-attention recurrence
+ *
+ *     S_t = S_{t-1} A_t + beta_t v_t k_t^T ,      o_t = S_t q_t
+ *
+ * ("History Replays Itself: Unleashing Long-Context Capability in Linear
+ * Attention" (NoteBank), Sec. 2, Eq. (1)) in two instantiations:
+ *
+ *   Taylor / BASED   A_t = I, beta_t = 1 on the feature-mapped keys
+ *                    phi(x) = [1, x, vec(x x^T)/sqrt(2)], with the
+ *                    normaliser  y_i = s_i^T phi(q_i) / (z_i^T phi(q_i) + eps),
+ *                    s_i = s_{i-1} + phi(k_i) v_i^T, z_i = z_{i-1} + phi(k_i)
+ *                    ("BASED：简单线性注意力如何平衡召回能力与生成吞吐", reading
+ *                    notes of "Simple linear attention language models balance
+ *                    the recall-throughput tradeoff", Sec. 2.2 = paper
+ *                    Eqs. (1)-(3); Sec. 2.3 = paper Eq. (4)).
+ *   Gated DeltaNet   A_t = alpha_t (I - beta_t k_t k_t^T), i.e.
+ *                    S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T
+ *                    (the delta-rule family named in NoteBank Sec. 2; its
+ *                    per-token cost J(7 d_k d_v + d_k + 2 d_v) in App. C.6,
+ *                    Eq. (11) counts exactly this update).
+ *
+ * Both run as a chunked prefill that returns the final state (the state is
+ * carried across chunk boundaries, NoteBank Sec. 3.2) and as a one-token
+ * decode step that updates the state in place.  Outputs are read after the
+ * token's own write (o_t = S_t q_t with S_t already holding token t).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  The
+ *     library never allocates or frees memory; scratch space comes from the
+ *     caller's workspace buffer, sized by the *_workspace_size queries.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream).  Argument validation happens on the
+ *     host before anything is launched; a rejected call launches nothing.
+ *   - Element strides are given per tensor for the batch, head and token
+ *     axes; the last (feature) axis must be contiguous.  Base pointers and
+ *     token strides must be 16-byte aligned (in bytes), as the tile loaders
+ *     move 16-byte vectors and TMA boxes.
+ *   - States are fp32, contiguous, and may alias (state_in == state_out is
+ *     an in-place update, the copy-and-branch use of NoteBank Alg. 1).
+ *   - No exception crosses the ABI; every failure is a la_status.
+ */
+#ifndef LA_H
+#define LA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LA_ABI_VERSION 1
+
+typedef enum la_status {
+  LA_OK = 0,
+  LA_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size, stride or alignment */
+  LA_ERR_UNSUPPORTED = 2,      /* well-formed but outside the built kernels   */
+  LA_ERR_WORKSPACE = 3,        /* workspace missing or too small              */
+  LA_ERR_CUDA = 4,             /* a CUDA runtime/driver call failed           */
+  LA_ERR_TIMEOUT = 5           /* a bounded device-side wait gave up          */
+} la_status;
+
+typedef enum la_dtype { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
+
+typedef enum la_variant { LA_VARIANT_TAYLOR = 0, LA_VARIANT_GDN = 1 } la_variant;
+
+/* A strided [B, H, N, d] view; strides in ELEMENTS; the d axis is contiguous. */
+typedef struct la_tensor {
+  void* ptr;
+  int64_t stride_b, stride_h, stride_t;
+} la_tensor;
+
+/* Taylor (BASED) prefill.
+ *   q, k : [B, H, N, d_feat]   in_dtype      (d_feat = d' = 16)
+ *   v    : [B, H, N, d_v]      in_dtype      (d_v = 64)
+ *   y    : [B, H, N, d_v]      out_dtype     y_i = s_i^T phi(q_i) / (z_i^T phi(q_i) + eps)
+ *   s_in : [B, H, D, d_v] fp32 contiguous, D = 1 + d' + d'^2 = 273, rows in
+ *          the order [1, x_0..x_{d'-1}, x_a x_b/sqrt2 for a, then b]; NULL = zero.
+ *   z_in : [B, H, D] fp32 contiguous; NULL = zero.
+ *   s_out, z_out : final state after token N-1 (required; may alias s_in/z_in).
+ *   eps  : added to the denominator (0 reproduces the pages' definition). */
+typedef struct la_based_prefill_args {
+  int64_t B, H, N, d_feat, d_v;
+  la_dtype in_dtype, out_dtype;
+  la_tensor q, k, v, y;
+  const float* s_in;
+  const float* z_in;
+  float* s_out;
+  float* z_out;
+  float eps;
+} la_based_prefill_args;
+
+/* Gated DeltaNet prefill.
+ *   q, k : [B, H, N, d_k]  in_dtype;  v, o : [B, H, N, d_v] in/out_dtype
+ *          (d_k = d_v = 128)
+ *   alpha, beta : [B, H, N] fp32 strided views (their feature axis is absent;
+ *          stride_t must be 1)
+ *   q_scale : multiplies q (1 = the pages' parametrisation: input scaling is
+ *          absorbed into q, NoteBank Sec. 2)
+ *   S_in : [B, H, d_v, d_k] fp32 contiguous (row i = value index); NULL = zero
+ *   S_out: final state (required; may alias S_in). */
+typedef struct la_gdn_prefill_args {
+  int64_t B, H, N, d_k, d_v;
+  la_dtype in_dtype, out_dtype;
+  la_tensor q, k, v, o;
+  la_tensor alpha, beta;
+  float q_scale;
+  const float* S_in;
+  float* S_out;
+} la_gdn_prefill_args;
+
+/* One decode step for S sequences x H heads, state updated in place.
+ *   q, k : [S, H, d_k] contiguous in_dtype (Taylor: d_k means d' = 16)
+ *   v    : [S, H, d_v] contiguous in_dtype
+ *   alpha, beta : [S, H] fp32 contiguous (GDN only; ignored for Taylor)
+ *   out  : [S, H, d_v] contiguous out_dtype
+ *   state: GDN [S, H, d_v, d_k] fp32; Taylor [S, H, D, d_v] fp32 (s)
+ *   z    : Taylor [S, H, D] fp32 (ignored for GDN)
+ *   eps  : Taylor denominator term; q_scale: GDN query scale. */
+typedef struct la_decode_args {
+  la_variant variant;
+  int64_t S, H, d_k, d_v;
+  la_dtype in_dtype, out_dtype;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* alpha;
+  const float* beta;
+  void* out;
+  float* state;
+  float* z;
+  float eps;
+  float q_scale;
+} la_decode_args;
+
+/* Bytes of device workspace the matching prefill call needs for `args`
+ * (0 = none; a NULL workspace is then accepted).  Pure host function. */
+size_t la_based_prefill_workspace_size(const la_based_prefill_args* args);
+size_t la_gdn_prefill_workspace_size(const la_gdn_prefill_args* args);
+
+/* Chunked Taylor prefill (BASED notes Sec. 2.2 and Sec. 2.5: the block
+ * decomposition U_b = (M_b . Phi_Qb Phi_Kb^T) V_b + Phi_Qb S_{<b}). */
+la_status la_based_prefill(const la_based_prefill_args* args, void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/* Chunked gated-delta-rule prefill (NoteBank Sec. 2 Eq. (1); chunks carry
+ * the state across boundaries as in NoteBank Sec. 3.2). */
+la_status la_gdn_prefill(const la_gdn_prefill_args* args, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* One recurrent decode step (NoteBank Eq. (1) for one token; BASED notes
+ * Sec. 2.5: the decode step fuses the outer-product write with the query
+ * readout and still reads and writes the whole persistent state). */
+la_status la_decode_step(const la_decode_args* args, void* stream);
+
+/* Synchronises `stream`, then reports (and clears when `clear` != 0) the
+ * device-side status word that bounded waits set on expiry:
+ * LA_OK or LA_ERR_TIMEOUT; LA_ERR_CUDA if the synchronisation failed. */
+la_status la_device_status(void* stream, int clear);
+
+/* Static description of a status code; never NULL. */
+const char* la_status_string(la_status status);
+
+/* LA_ABI_VERSION of the built library. */
+int la_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_H */

@@ -1,0 +1,292 @@
+"""Thin Python binding of the GB300 causal linear-attention library.
+
+Every function here marshals torch tensors into the C ABI of ``include/la.h``
+and calls it; all arithmetic runs in the library's CUDA kernels.  There is no
+CPU or PyTorch fallback: if the compiled library is missing, importing the
+binding's functions raises.
+
+Names follow the C entry points: ``la_based_prefill``, ``la_gdn_prefill``,
+``la_decode_step`` (plus the workspace queries and status helpers).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+LA_OK = 0
+LA_ERR_INVALID_ARGUMENT = 1
+LA_ERR_UNSUPPORTED = 2
+LA_ERR_WORKSPACE = 3
+LA_ERR_CUDA = 4
+LA_ERR_TIMEOUT = 5
+
+LA_DTYPE_F32 = 0
+LA_DTYPE_BF16 = 1
+LA_VARIANT_TAYLOR = 0
+LA_VARIANT_GDN = 1
+
+TAYLOR_DFEAT = 16
+TAYLOR_DV = 64
+TAYLOR_D = 1 + TAYLOR_DFEAT + TAYLOR_DFEAT * TAYLOR_DFEAT
+GDN_D = 128
+
+_i64 = ctypes.c_int64
+
+
+class LATensor(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("stride_b", _i64), ("stride_h", _i64), ("stride_t", _i64)]
+
+
+class BasedPrefillArgs(ctypes.Structure):
+    _fields_ = [("B", _i64), ("H", _i64), ("N", _i64), ("d_feat", _i64), ("d_v", _i64),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("q", LATensor), ("k", LATensor), ("v", LATensor), ("y", LATensor),
+                ("s_in", ctypes.c_void_p), ("z_in", ctypes.c_void_p),
+                ("s_out", ctypes.c_void_p), ("z_out", ctypes.c_void_p),
+                ("eps", ctypes.c_float)]
+
+
+class GdnPrefillArgs(ctypes.Structure):
+    _fields_ = [("B", _i64), ("H", _i64), ("N", _i64), ("d_k", _i64), ("d_v", _i64),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("q", LATensor), ("k", LATensor), ("v", LATensor), ("o", LATensor),
+                ("alpha", LATensor), ("beta", LATensor),
+                ("q_scale", ctypes.c_float),
+                ("S_in", ctypes.c_void_p), ("S_out", ctypes.c_void_p)]
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("S", _i64), ("H", _i64), ("d_k", _i64), ("d_v", _i64),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("alpha", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("state", ctypes.c_void_p), ("z", ctypes.c_void_p),
+                ("eps", ctypes.c_float), ("q_scale", ctypes.c_float)]
+
+
+EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_decode_step", "la_based_prefill_workspace_size",
+            "la_gdn_prefill_workspace_size", "la_device_status", "la_status_string", "la_abi_version")
+
+
+class LAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {la_status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load the compiled library (build it first with ``_build.build()``)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or _build.LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library not built ({p} missing); run __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    vp = ctypes.c_void_p
+    lib.la_based_prefill.restype = ctypes.c_int
+    lib.la_based_prefill.argtypes = [ctypes.POINTER(BasedPrefillArgs), vp, ctypes.c_size_t, vp]
+    lib.la_gdn_prefill.restype = ctypes.c_int
+    lib.la_gdn_prefill.argtypes = [ctypes.POINTER(GdnPrefillArgs), vp, ctypes.c_size_t, vp]
+    lib.la_decode_step.restype = ctypes.c_int
+    lib.la_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), vp]
+    lib.la_based_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.la_based_prefill_workspace_size.argtypes = [ctypes.POINTER(BasedPrefillArgs)]
+    lib.la_gdn_prefill_workspace_size.restype = ctypes.c_size_t
+    lib.la_gdn_prefill_workspace_size.argtypes = [ctypes.POINTER(GdnPrefillArgs)]
+    lib.la_device_status.restype = ctypes.c_int
+    lib.la_device_status.argtypes = [vp, ctypes.c_int]
+    lib.la_status_string.restype = ctypes.c_char_p
+    lib.la_status_string.argtypes = [ctypes.c_int]
+    lib.la_abi_version.restype = ctypes.c_int
+    lib.la_abi_version.argtypes = []
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def la_status_string(status: int) -> str:
+    return load_library().la_status_string(int(status)).decode()
+
+
+def la_abi_version() -> int:
+    return int(load_library().la_abi_version())
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return LA_DTYPE_F32
+    if t == torch.bfloat16:
+        return LA_DTYPE_BF16
+    raise TypeError(f"unsupported dtype {t}; use float32 or bfloat16")
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _view4(t: torch.Tensor) -> LATensor:
+    """[B,H,N,d] tensor -> strided view (the d axis must be contiguous)."""
+    if t.dim() != 4:
+        raise ValueError(f"expected a [B,H,N,d] tensor, got shape {tuple(t.shape)}")
+    if t.shape[-1] > 1 and t.stride(-1) != 1:
+        raise ValueError("the feature axis must be contiguous")
+    return LATensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
+
+
+def _gate3(t: torch.Tensor) -> LATensor:
+    """[B,H,N] fp32 gate -> view with its N axis as the token axis."""
+    if t.dim() != 3 or t.dtype != torch.float32:
+        raise ValueError("alpha/beta must be float32 [B,H,N]")
+    return LATensor(t.data_ptr(), t.stride(0), t.stride(1), t.stride(2))
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must live on a CUDA device")
+
+
+def _workspace(nbytes: int, workspace, device):
+    if nbytes == 0:
+        return None, 0
+    if workspace is not None:
+        return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return ws, nbytes
+
+
+# ---------------------------------------------------------------------------
+# entry points
+
+
+def _based_args(q, k, v, y, s_in, z_in, s_out, z_out, eps):
+    B, H, N, F = q.shape
+    return BasedPrefillArgs(B, H, N, F, v.shape[-1], _dtype_code(q.dtype), _dtype_code(y.dtype),
+                            _view4(q), _view4(k), _view4(v), _view4(y),
+                            _ptr(s_in), _ptr(z_in), _ptr(s_out), _ptr(z_out), float(eps))
+
+
+def la_based_prefill_workspace_size(q, k, v, y=None) -> int:
+    y = y if y is not None else v
+    a = _based_args(q, k, v, y, None, None, None, None, 0.0)
+    return int(load_library().la_based_prefill_workspace_size(ctypes.byref(a)))
+
+
+def la_based_prefill(q, k, v, y=None, s_in=None, z_in=None, s_out=None, z_out=None, eps: float = 0.0,
+                     out_dtype=None, workspace=None, stream=None):
+    """Chunked Taylor (BASED) prefill.  Returns (y, s_out, z_out).
+
+    q, k: [B,H,N,16], v: [B,H,N,64] (fp32 or bf16); states fp32
+    s: [B,H,273,64], z: [B,H,273]."""
+    lib = load_library()
+    _check_cuda(q, k, v, y, s_in, z_in, s_out, z_out)
+    B, H, N, _ = q.shape
+    dv = v.shape[-1]
+    if y is None:
+        y = torch.empty((B, H, N, dv), dtype=out_dtype or q.dtype, device=q.device)
+    if s_out is None:
+        s_out = torch.empty((B, H, TAYLOR_D, dv), dtype=torch.float32, device=q.device)
+    if z_out is None:
+        z_out = torch.empty((B, H, TAYLOR_D), dtype=torch.float32, device=q.device)
+    for name, t in (("s_in", s_in), ("z_in", z_in), ("s_out", s_out), ("z_out", z_out)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 tensor")
+    a = _based_args(q, k, v, y, s_in, z_in, s_out, z_out, eps)
+    need = int(lib.la_based_prefill_workspace_size(ctypes.byref(a)))
+    ws, ws_bytes = _workspace(need, workspace, q.device)
+    st = lib.la_based_prefill(ctypes.byref(a), _ptr(ws) if isinstance(ws, torch.Tensor) else ws, ws_bytes,
+                              _stream_handle(stream))
+    if st != LA_OK:
+        raise LAError(st, "la_based_prefill")
+    return y, s_out, z_out
+
+
+def _gdn_args(q, k, v, o, alpha, beta, S_in, S_out, q_scale):
+    B, H, N, dk = q.shape
+    return GdnPrefillArgs(B, H, N, dk, v.shape[-1], _dtype_code(q.dtype), _dtype_code(o.dtype),
+                          _view4(q), _view4(k), _view4(v), _view4(o), _gate3(alpha), _gate3(beta),
+                          float(q_scale), _ptr(S_in), _ptr(S_out))
+
+
+def la_gdn_prefill_workspace_size(q, k, v, alpha, beta, o=None) -> int:
+    o = o if o is not None else v
+    a = _gdn_args(q, k, v, o, alpha, beta, None, None, 1.0)
+    return int(load_library().la_gdn_prefill_workspace_size(ctypes.byref(a)))
+
+
+def la_gdn_prefill(q, k, v, alpha, beta, o=None, S_in=None, S_out=None, q_scale: float = 1.0,
+                   out_dtype=None, workspace=None, stream=None):
+    """Chunked gated-delta-rule prefill.  Returns (o, S_out).
+
+    q, k, v: [B,H,N,128] (fp32 or bf16); alpha, beta: fp32 [B,H,N];
+    S: fp32 [B,H,128,128] (row = value index)."""
+    lib = load_library()
+    _check_cuda(q, k, v, alpha, beta, o, S_in, S_out)
+    B, H, N, _ = q.shape
+    dv = v.shape[-1]
+    if o is None:
+        o = torch.empty((B, H, N, dv), dtype=out_dtype or q.dtype, device=q.device)
+    if S_out is None:
+        S_out = torch.empty((B, H, dv, q.shape[-1]), dtype=torch.float32, device=q.device)
+    for name, t in (("S_in", S_in), ("S_out", S_out)):
+        if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 tensor")
+    a = _gdn_args(q, k, v, o, alpha, beta, S_in, S_out, q_scale)
+    need = int(lib.la_gdn_prefill_workspace_size(ctypes.byref(a)))
+    ws, ws_bytes = _workspace(need, workspace, q.device)
+    st = lib.la_gdn_prefill(ctypes.byref(a), _ptr(ws) if isinstance(ws, torch.Tensor) else ws, ws_bytes,
+                            _stream_handle(stream))
+    if st != LA_OK:
+        raise LAError(st, "la_gdn_prefill")
+    return o, S_out
+
+
+def la_decode_step(variant: int, q, k, v, state, z=None, alpha=None, beta=None, out=None,
+                   eps: float = 0.0, q_scale: float = 1.0, out_dtype=None, stream=None):
+    """One decode step, state (and z) updated in place.  Returns out [S,H,d_v].
+
+    GDN: q, k, v [S,H,128], alpha, beta fp32 [S,H], state fp32 [S,H,128,128].
+    Taylor: q, k [S,H,16], v [S,H,64], state fp32 [S,H,273,64], z fp32 [S,H,273]."""
+    lib = load_library()
+    _check_cuda(q, k, v, state, z, alpha, beta, out)
+    for name, t in (("q", q), ("k", k), ("v", v), ("state", state), ("z", z), ("alpha", alpha),
+                    ("beta", beta), ("out", out)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    S, H, dk = q.shape
+    dv = v.shape[-1]
+    if out is None:
+        out = torch.empty((S, H, dv), dtype=out_dtype or q.dtype, device=q.device)
+    a = DecodeArgs(int(variant), S, H, dk, dv, _dtype_code(q.dtype), _dtype_code(out.dtype),
+                   _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(out), _ptr(state), _ptr(z),
+                   float(eps), float(q_scale))
+    st = lib.la_decode_step(ctypes.byref(a), _stream_handle(stream))
+    if st != LA_OK:
+        raise LAError(st, "la_decode_step")
+    return out
+
+
+def la_device_status(stream=None, clear: bool = True) -> int:
+    return int(load_library().la_device_status(_stream_handle(stream), 1 if clear else 0))

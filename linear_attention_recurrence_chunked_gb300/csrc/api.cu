@@ -1,0 +1,219 @@
+// api.cu -- the extern "C" entry points declared in include/la.h.
+//
+// Host side only: argument validation (before anything is launched), the
+// N == 0 state pass-through, and dispatch to the kernel launchers.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "la.h"
+
+namespace {
+
+// Device status word set by bounded waits that expire (LA_ERR_TIMEOUT).
+__device__ unsigned g_la_device_status = 0;
+
+unsigned* device_status_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_la_device_status) != cudaSuccess) return nullptr;
+  return static_cast<unsigned*>(p);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes(la_dtype t) { return t == LA_DTYPE_BF16 ? 2 : 4; }
+
+bool valid_dtype(la_dtype t) { return t == LA_DTYPE_F32 || t == LA_DTYPE_BF16; }
+
+// A [B,H,N,d] view: non-null (unless empty), 16-byte aligned base and token
+// stride, non-negative strides, and rows that do not overlap along t.
+bool valid_view(const la_tensor& x, int64_t B, int64_t H, int64_t N, int64_t d, la_dtype dt) {
+  if (B * H * N == 0) return true;
+  if (x.ptr == nullptr || !aligned16(x.ptr)) return false;
+  if (x.stride_b < 0 || x.stride_h < 0 || x.stride_t < 0) return false;
+  if (N > 1 && x.stride_t < d) return false;
+  if ((x.stride_t * elem_bytes(dt)) % 16 != 0) return false;
+  if ((x.stride_h * elem_bytes(dt)) % 16 != 0 || (x.stride_b * elem_bytes(dt)) % 16 != 0) return false;
+  return true;
+}
+
+bool valid_gate(const la_tensor& x, int64_t B, int64_t H, int64_t N) {
+  if (B * H * N == 0) return true;
+  if (x.ptr == nullptr || (reinterpret_cast<uintptr_t>(x.ptr) & 3u) != 0) return false;
+  if (x.stride_b < 0 || x.stride_h < 0) return false;
+  return x.stride_t == 1;
+}
+
+la::View4 view(const la_tensor& x) { return la::View4{x.ptr, x.stride_b, x.stride_h, x.stride_t}; }
+
+la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+// N == 0: the final state is the initial state (or zero).
+la_status pass_state(float* out, const float* in, size_t n_floats, cudaStream_t s) {
+  if (n_floats == 0) return LA_OK;
+  if (in == out) return LA_OK;
+  const size_t bytes = n_floats * sizeof(float);
+  if (in) return from_cuda(cudaMemcpyAsync(out, in, bytes, cudaMemcpyDeviceToDevice, s));
+  return from_cuda(cudaMemsetAsync(out, 0, bytes, s));
+}
+
+constexpr int64_t kTaylorF = 16, kTaylorDv = 64, kTaylorD = 1 + 16 + 16 * 16;
+constexpr int64_t kGdnD = 128;
+constexpr int64_t kMaxDim = int64_t(1) << 40;
+
+la_status check_based(const la_based_prefill_args* a) {
+  if (!a) return LA_ERR_INVALID_ARGUMENT;
+  if (a->B < 0 || a->H < 0 || a->N < 0 || a->B > kMaxDim || a->H > kMaxDim || a->N > kMaxDim)
+    return LA_ERR_INVALID_ARGUMENT;
+  if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return LA_ERR_INVALID_ARGUMENT;
+  if (a->d_feat != kTaylorF || a->d_v != kTaylorDv) return LA_ERR_UNSUPPORTED;
+  if (a->B * a->H > (int64_t(1) << 31) - 1) return LA_ERR_UNSUPPORTED;
+  const int64_t B = a->B, H = a->H, N = a->N;
+  if (!valid_view(a->q, B, H, N, kTaylorF, a->in_dtype) || !valid_view(a->k, B, H, N, kTaylorF, a->in_dtype) ||
+      !valid_view(a->v, B, H, N, kTaylorDv, a->in_dtype) || !valid_view(a->y, B, H, N, kTaylorDv, a->out_dtype))
+    return LA_ERR_INVALID_ARGUMENT;
+  if (B * H > 0) {
+    if (!a->s_out || !a->z_out) return LA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(a->s_out) || !aligned16(a->s_in) || (reinterpret_cast<uintptr_t>(a->z_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(a->z_in) & 3u))
+      return LA_ERR_INVALID_ARGUMENT;
+  }
+  return LA_OK;
+}
+
+la_status check_gdn(const la_gdn_prefill_args* a) {
+  if (!a) return LA_ERR_INVALID_ARGUMENT;
+  if (a->B < 0 || a->H < 0 || a->N < 0 || a->B > kMaxDim || a->H > kMaxDim || a->N > kMaxDim)
+    return LA_ERR_INVALID_ARGUMENT;
+  if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return LA_ERR_INVALID_ARGUMENT;
+  if (a->d_k != kGdnD || a->d_v != kGdnD) return LA_ERR_UNSUPPORTED;
+  if (a->B * a->H > (int64_t(1) << 28)) return LA_ERR_UNSUPPORTED;
+  const int64_t B = a->B, H = a->H, N = a->N;
+  if (!valid_view(a->q, B, H, N, kGdnD, a->in_dtype) || !valid_view(a->k, B, H, N, kGdnD, a->in_dtype) ||
+      !valid_view(a->v, B, H, N, kGdnD, a->in_dtype) || !valid_view(a->o, B, H, N, kGdnD, a->out_dtype))
+    return LA_ERR_INVALID_ARGUMENT;
+  if (!valid_gate(a->alpha, B, H, N) || !valid_gate(a->beta, B, H, N)) return LA_ERR_INVALID_ARGUMENT;
+  if (B * H > 0) {
+    if (!a->S_out || !aligned16(a->S_out) || !aligned16(a->S_in)) return LA_ERR_INVALID_ARGUMENT;
+  }
+  return LA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int la_abi_version(void) { return LA_ABI_VERSION; }
+
+const char* la_status_string(la_status s) {
+  switch (s) {
+    case LA_OK: return "ok";
+    case LA_ERR_INVALID_ARGUMENT: return "invalid argument (null pointer, size, stride or alignment)";
+    case LA_ERR_UNSUPPORTED: return "unsupported shape or dtype for the built kernels";
+    case LA_ERR_WORKSPACE: return "workspace missing or too small";
+    case LA_ERR_CUDA: return "CUDA call failed";
+    case LA_ERR_TIMEOUT: return "a bounded device-side wait expired";
+  }
+  return "unknown status";
+}
+
+size_t la_based_prefill_workspace_size(const la_based_prefill_args* a) {
+  if (check_based(a) != LA_OK) return 0;
+  return la::taylor_prefill_workspace(a->B, a->H, a->N);
+}
+
+size_t la_gdn_prefill_workspace_size(const la_gdn_prefill_args* a) {
+  if (check_gdn(a) != LA_OK) return 0;
+  return la::gdn_prefill_workspace(a->B, a->H, a->N);
+}
+
+la_status la_based_prefill(const la_based_prefill_args* a, void* ws, size_t ws_bytes, void* stream) {
+  const la_status st = check_based(a);
+  if (st != LA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t BH = a->B * a->H;
+  if (BH == 0) return LA_OK;
+  if (a->N == 0) {
+    la_status r = pass_state(a->s_out, a->s_in, (size_t)(BH * kTaylorD * kTaylorDv), s);
+    if (r != LA_OK) return r;
+    return pass_state(a->z_out, a->z_in, (size_t)(BH * kTaylorD), s);
+  }
+  const size_t need = la::taylor_prefill_workspace(a->B, a->H, a->N);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned16(ws))) return LA_ERR_WORKSPACE;
+  la::TaylorPrefillLaunch L{};
+  L.B = a->B; L.H = a->H; L.N = a->N;
+  L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
+  L.out_bf16 = a->out_dtype == LA_DTYPE_BF16;
+  L.q = view(a->q); L.k = view(a->k); L.v = view(a->v);
+  L.y = a->y.ptr; L.y_sb = a->y.stride_b; L.y_sh = a->y.stride_h; L.y_st = a->y.stride_t;
+  L.s_in = a->s_in; L.z_in = a->z_in; L.s_out = a->s_out; L.z_out = a->z_out;
+  L.eps = a->eps;
+  unsigned* status = device_status_ptr();
+  if (!status) return LA_ERR_CUDA;
+  return from_cuda(la::launch_taylor_prefill(L, ws, ws_bytes, status, s));
+}
+
+la_status la_gdn_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes, void* stream) {
+  const la_status st = check_gdn(a);
+  if (st != LA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t BH = a->B * a->H;
+  if (BH == 0) return LA_OK;
+  if (a->N == 0) return pass_state(a->S_out, a->S_in, (size_t)(BH * kGdnD * kGdnD), s);
+  const size_t need = la::gdn_prefill_workspace(a->B, a->H, a->N);
+  if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned16(ws))) return LA_ERR_WORKSPACE;
+  la::GdnPrefillLaunch L{};
+  L.B = a->B; L.H = a->H; L.N = a->N;
+  L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
+  L.out_bf16 = a->out_dtype == LA_DTYPE_BF16;
+  L.q = view(a->q); L.k = view(a->k); L.v = view(a->v);
+  L.o = a->o.ptr; L.o_sb = a->o.stride_b; L.o_sh = a->o.stride_h; L.o_st = a->o.stride_t;
+  L.alpha = static_cast<const float*>(a->alpha.ptr); L.a_sb = a->alpha.stride_b; L.a_sh = a->alpha.stride_h;
+  L.beta = static_cast<const float*>(a->beta.ptr); L.b_sb = a->beta.stride_b; L.b_sh = a->beta.stride_h;
+  L.q_scale = a->q_scale;
+  L.S_in = a->S_in; L.S_out = a->S_out;
+  unsigned* status = device_status_ptr();
+  if (!status) return LA_ERR_CUDA;
+  return from_cuda(la::launch_gdn_prefill(L, ws, ws_bytes, status, s));
+}
+
+la_status la_decode_step(const la_decode_args* a, void* stream) {
+  if (!a) return LA_ERR_INVALID_ARGUMENT;
+  if (a->S < 0 || a->H < 0 || a->S > kMaxDim || a->H > kMaxDim) return LA_ERR_INVALID_ARGUMENT;
+  if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return LA_ERR_INVALID_ARGUMENT;
+  if (a->variant != LA_VARIANT_TAYLOR && a->variant != LA_VARIANT_GDN) return LA_ERR_INVALID_ARGUMENT;
+  if (a->variant == LA_VARIANT_GDN && (a->d_k != kGdnD || a->d_v != kGdnD)) return LA_ERR_UNSUPPORTED;
+  if (a->variant == LA_VARIANT_TAYLOR && (a->d_k != kTaylorF || a->d_v != kTaylorDv)) return LA_ERR_UNSUPPORTED;
+  const int64_t SH = a->S * a->H;
+  if (SH == 0) return LA_OK;
+  if (SH > (int64_t(1) << 31) - 1) return LA_ERR_UNSUPPORTED;
+  if (!a->q || !a->k || !a->v || !a->out || !a->state) return LA_ERR_INVALID_ARGUMENT;
+  const int in_align = a->in_dtype == LA_DTYPE_BF16 ? 8 : 16;
+  if ((reinterpret_cast<uintptr_t>(a->q) % in_align) || (reinterpret_cast<uintptr_t>(a->k) % in_align) ||
+      (reinterpret_cast<uintptr_t>(a->v) % in_align) || !aligned16(a->state))
+    return LA_ERR_INVALID_ARGUMENT;
+  if (a->variant == LA_VARIANT_GDN && (!a->alpha || !a->beta)) return LA_ERR_INVALID_ARGUMENT;
+  if (a->variant == LA_VARIANT_TAYLOR && (!a->z || (reinterpret_cast<uintptr_t>(a->z) & 3u)))
+    return LA_ERR_INVALID_ARGUMENT;
+  la::DecodeLaunch L{};
+  L.S = a->S; L.H = a->H;
+  L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
+  L.out_bf16 = a->out_dtype == LA_DTYPE_BF16;
+  L.q = a->q; L.k = a->k; L.v = a->v; L.alpha = a->alpha; L.beta = a->beta;
+  L.out = a->out; L.state = a->state; L.z = a->z; L.eps = a->eps; L.q_scale = a->q_scale;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return from_cuda(a->variant == LA_VARIANT_GDN ? la::launch_gdn_decode(L, s) : la::launch_taylor_decode(L, s));
+}
+
+la_status la_device_status(void* stream, int clear) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_la_device_status, sizeof v) != cudaSuccess) return LA_ERR_CUDA;
+  if (clear && v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_la_device_status, &zero, sizeof zero) != cudaSuccess) return LA_ERR_CUDA;
+  }
+  return v ? LA_ERR_TIMEOUT : LA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,67 @@
+// common.cuh -- small device helpers shared by the kernels of this library.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace la {
+
+constexpr unsigned kFullMask = 0xffffffffu;
+
+// Loads of 4 consecutive elements (16-byte aligned for fp32, 8-byte for bf16).
+__device__ __forceinline__ float4 load4(const float* p) {
+  return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 raw = *reinterpret_cast<const uint2*>(p);
+  float4 r;
+  r.x = __uint_as_float(raw.x << 16);
+  r.y = __uint_as_float(raw.x & 0xffff0000u);
+  r.z = __uint_as_float(raw.y << 16);
+  r.w = __uint_as_float(raw.y & 0xffff0000u);
+  return r;
+}
+
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ void store1(float* p, float x) { *p = x; }
+__device__ __forceinline__ void store1(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float dot4(float4 a, float4 b) {
+  return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, a.w * b.w)));
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(kFullMask, x, off);
+  return x;
+}
+
+// Reduce-scatter of NV per-lane partial values across the 32 lanes of a warp.
+// On return, v[0] of lane l holds the warp-wide sum of value index
+// (l >> (5 - log2 NV)).  Uses 31 shuffles for NV = 32 instead of 160.
+template <int NV>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV]) {
+  static_assert(NV >= 1 && NV <= 32 && (NV & (NV - 1)) == 0, "NV must be a power of two <= 32");
+  const int lane = threadIdx.x & 31;
+  int off = 16;
+#pragma unroll
+  for (int n = NV; n > 1; n >>= 1, off >>= 1) {
+    const int half = n >> 1;
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFullMask, send, off);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (; off >= 1; off >>= 1) r += __shfl_xor_sync(kFullMask, r, off);
+  return r;
+}
+
+}  // namespace la

@@ -1,0 +1,63 @@
+// kernels.h -- internal launch descriptors shared by the C ABI layer and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace la {
+
+struct View4 {        // strided [B, H, N, d] view, element strides
+  const void* ptr;
+  int64_t sb, sh, st;
+};
+
+struct DecodeLaunch {
+  int64_t S, H;
+  bool in_bf16, out_bf16;
+  const void *q, *k, *v;
+  const float *alpha, *beta;
+  void* out;
+  float* state;
+  float* z;
+  float eps, q_scale;
+};
+
+struct TaylorPrefillLaunch {
+  int64_t B, H, N;
+  bool in_bf16, out_bf16;
+  View4 q, k, v;
+  void* y;
+  int64_t y_sb, y_sh, y_st;
+  const float* s_in;
+  const float* z_in;
+  float* s_out;
+  float* z_out;
+  float eps;
+};
+
+struct GdnPrefillLaunch {
+  int64_t B, H, N;
+  bool in_bf16, out_bf16;
+  View4 q, k, v;
+  void* o;
+  int64_t o_sb, o_sh, o_st;
+  const float* alpha;
+  int64_t a_sb, a_sh;
+  const float* beta;
+  int64_t b_sb, b_sh;
+  float q_scale;
+  const float* S_in;
+  float* S_out;
+};
+
+cudaError_t launch_gdn_decode(const DecodeLaunch& a, cudaStream_t stream);
+cudaError_t launch_taylor_decode(const DecodeLaunch& a, cudaStream_t stream);
+cudaError_t launch_taylor_prefill(const TaylorPrefillLaunch& a, void* ws, size_t ws_bytes,
+                                  unsigned* dev_status, cudaStream_t stream);
+cudaError_t launch_gdn_prefill(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes,
+                               unsigned* dev_status, cudaStream_t stream);
+size_t taylor_prefill_workspace(int64_t B, int64_t H, int64_t N);
+size_t gdn_prefill_workspace(int64_t B, int64_t H, int64_t N);
+
+}  // namespace la

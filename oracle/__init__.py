@@ -36,13 +36,13 @@ IN_BF16 = 1
 
 
 def build(force: bool = False) -> str:
-    """Compile oracle.c into a shared library (gcc, -O2, no arch flags)."""
+    """Compile oracle.c into a shared library (gcc, -O3, no arch flags)."""
     os.makedirs(_OUT_DIR, exist_ok=True)
     fresh = os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)
     if fresh and not force:
         return _LIB_PATH
     tmp = _LIB_PATH + f".{os.getpid()}.tmp"
-    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-std=c11", "-o", tmp, _SRC, "-lm"]
+    cmd = ["gcc", "-O3", "-fPIC", "-shared", "-pthread", "-std=c11", "-o", tmp, _SRC, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH

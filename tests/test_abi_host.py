@@ -1,0 +1,141 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports
+every entry point include/la.h declares, and rejects malformed arguments with
+status codes before any CUDA call (only argument validation runs here)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import linear_attention_recurrence_chunked_gb300 as la
+from linear_attention_recurrence_chunked_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return la.load_library()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b(la_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"la_based_prefill", "la_gdn_prefill", "la_decode_step"} <= names
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT (la_[a-z0-9_]+)\b", out))
+    assert names <= exported, f"missing exports: {names - exported}"
+    for n in names:
+        assert hasattr(lib, n)
+    assert set(la.EXPORTED) <= names
+
+
+def test_abi_version_and_status_strings(lib):
+    assert la.la_abi_version() == 1
+    for code in range(6):
+        assert la.la_status_string(code)
+    assert la.la_status_string(99) == "unknown status"
+
+
+def _tensor(ptr, sb=0, sh=0, st=0):
+    return la.LATensor(ptr, sb, sh, st)
+
+
+def gdn_args(**kw):
+    B, H, N = kw.get("B", 1), kw.get("H", 1), kw.get("N", 64)
+    base = kw.get("base", 0x10000)
+    t = lambda off: _tensor(base + off, H * N * 128, N * 128, 128)
+    g = lambda off: _tensor(base + off, H * N, N, 1)
+    a = la.GdnPrefillArgs(B, H, N, kw.get("dk", 128), kw.get("dv", 128), la.LA_DTYPE_BF16, la.LA_DTYPE_BF16,
+                          t(0), t(1 << 20), t(2 << 20), t(3 << 20), g(4 << 20), g(5 << 20), 1.0,
+                          None, base + (6 << 20))
+    for k, v in kw.get("set", {}).items():
+        setattr(a, k, v)
+    return a
+
+
+def based_args(**kw):
+    B, H, N = kw.get("B", 1), kw.get("H", 1), kw.get("N", 64)
+    base = 0x10000
+    tq = lambda off: _tensor(base + off, H * N * 16, N * 16, 16)
+    tv = lambda off: _tensor(base + off, H * N * 64, N * 64, 64)
+    a = la.BasedPrefillArgs(B, H, N, kw.get("df", 16), kw.get("dv", 64), la.LA_DTYPE_BF16, la.LA_DTYPE_BF16,
+                            tq(0), tq(1 << 20), tv(2 << 20), tv(3 << 20), None, None,
+                            base + (4 << 20), base + (5 << 20), 0.0)
+    for k, v in kw.get("set", {}).items():
+        setattr(a, k, v)
+    return a
+
+
+def call_gdn(lib, a):
+    return lib.la_gdn_prefill(ctypes.byref(a), None, 0, None)
+
+
+def call_based(lib, a):
+    return lib.la_based_prefill(ctypes.byref(a), None, 0, None)
+
+
+def test_gdn_rejections(lib):
+    assert lib.la_gdn_prefill(None, None, 0, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert call_gdn(lib, gdn_args(dk=64, dv=64)) == la.LA_ERR_UNSUPPORTED
+    assert call_gdn(lib, gdn_args(N=-1)) == la.LA_ERR_INVALID_ARGUMENT
+    a = gdn_args()
+    a.q = _tensor(None, 128 * 64, 128 * 64, 128)
+    assert call_gdn(lib, a) == la.LA_ERR_INVALID_ARGUMENT            # null q
+    a = gdn_args()
+    a.k = _tensor(0x10000 + 2, 128 * 64, 128 * 64, 128)
+    assert call_gdn(lib, a) == la.LA_ERR_INVALID_ARGUMENT            # misaligned base
+    a = gdn_args()
+    a.v = _tensor(0x10000, 128 * 64, 128 * 64, 100)
+    assert call_gdn(lib, a) == la.LA_ERR_INVALID_ARGUMENT            # token stride < d and unaligned
+    a = gdn_args()
+    a.alpha = _tensor(0x20000, 64, 64, 2)
+    assert call_gdn(lib, a) == la.LA_ERR_INVALID_ARGUMENT            # gate not contiguous along t
+    a = gdn_args(set={"S_out": None})
+    assert call_gdn(lib, a) == la.LA_ERR_INVALID_ARGUMENT            # missing final state
+    a = gdn_args(set={"in_dtype": 7})
+    assert call_gdn(lib, a) == la.LA_ERR_INVALID_ARGUMENT
+    assert lib.la_gdn_prefill_workspace_size(ctypes.byref(gdn_args(dk=64, dv=64))) == 0
+    # empty batch: nothing to do, no CUDA call
+    assert call_gdn(lib, gdn_args(B=0)) == la.LA_OK
+
+
+def test_based_rejections(lib):
+    assert lib.la_based_prefill(None, None, 0, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert call_based(lib, based_args(df=8)) == la.LA_ERR_UNSUPPORTED
+    assert call_based(lib, based_args(dv=32)) == la.LA_ERR_UNSUPPORTED
+    assert call_based(lib, based_args(set={"z_out": None})) == la.LA_ERR_INVALID_ARGUMENT
+    assert call_based(lib, based_args(set={"s_out": 0x10004})) == la.LA_ERR_INVALID_ARGUMENT
+    a = based_args()
+    a.q = _tensor(0x10000, 16 * 64, 16 * 64, 12)
+    assert call_based(lib, a) == la.LA_ERR_INVALID_ARGUMENT
+    assert call_based(lib, based_args(H=0)) == la.LA_OK
+
+
+def test_decode_rejections(lib):
+    mk = lambda **kw: la.DecodeArgs(kw.get("variant", la.LA_VARIANT_GDN), kw.get("S", 2), 2, kw.get("dk", 128),
+                                    kw.get("dv", 128), la.LA_DTYPE_BF16, la.LA_DTYPE_BF16,
+                                    kw.get("q", 0x10000), 0x20000, 0x30000, kw.get("alpha", 0x40000), 0x50000,
+                                    0x60000, kw.get("state", 0x70000), kw.get("z", None), 0.0, 1.0)
+    call = lambda a: lib.la_decode_step(ctypes.byref(a), None)
+    assert lib.la_decode_step(None, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert call(mk(variant=5)) == la.LA_ERR_INVALID_ARGUMENT
+    assert call(mk(dk=64)) == la.LA_ERR_UNSUPPORTED
+    assert call(mk(variant=la.LA_VARIANT_TAYLOR)) == la.LA_ERR_UNSUPPORTED  # 128 != 16
+    assert call(mk(variant=la.LA_VARIANT_TAYLOR, dk=16, dv=64)) == la.LA_ERR_INVALID_ARGUMENT  # z missing
+    assert call(mk(q=None)) == la.LA_ERR_INVALID_ARGUMENT
+    assert call(mk(alpha=None)) == la.LA_ERR_INVALID_ARGUMENT
+    assert call(mk(state=0x70004)) == la.LA_ERR_INVALID_ARGUMENT
+    assert call(mk(S=0)) == la.LA_OK

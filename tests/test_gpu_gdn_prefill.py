@@ -1,0 +1,137 @@
+"""GPU parity of the gated-delta-rule prefill against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import linear_attention_recurrence_chunked_gb300 as la
+import oracle
+import synthetic
+from tests.helpers import TOL, cuda_device, rel_err, to_np
+
+pytestmark = pytest.mark.gpu
+NAMES = ("q", "k", "v", "alpha", "beta")
+
+
+def oracle_ref(inp, S_in=None, q_scale=1.0, t_samples=None):
+    return oracle.gdn(*(synthetic.to_oracle(inp[n]) for n in ("q", "k", "v")), inp["alpha"].cpu().numpy(),
+                      inp["beta"].cpu().numpy(), S_in=None if S_in is None else S_in.double().cpu().numpy(),
+                      q_scale=q_scale, t_samples=t_samples)
+
+
+def run(inp, dev, **kw):
+    o, S = la.la_gdn_prefill(*(inp[n].to(dev) for n in NAMES), **kw)
+    torch.cuda.synchronize()
+    return to_np(o), to_np(S)
+
+
+def test_gdn_fp32_small_with_state_in():
+    dev = cuda_device()
+    inp = synthetic.gdn_inputs(1, 2, 200, dtype=torch.float32, seed=41)
+    S_in = torch.randn((1, 2, 128, 128), generator=torch.Generator().manual_seed(4)) * 0.1
+    o, S = run(inp, dev, S_in=S_in.to(dev))
+    ref = oracle_ref(inp, S_in=S_in)
+    assert rel_err(o, ref["o"]) < TOL[torch.float32]
+    assert rel_err(S, ref["S"]) < TOL[torch.float32]
+
+
+@pytest.mark.parametrize("N", [1, 15, 63, 64, 65, 127, 128, 129, 257, 1000])
+def test_gdn_bf16_ragged_lengths(N):
+    dev = cuda_device()
+    inp = synthetic.gdn_inputs(1, 3, N, dtype=torch.bfloat16, seed=200 + N)
+    o, S = run(inp, dev)
+    ref = oracle_ref(inp)
+    assert rel_err(o, ref["o"]) < TOL[torch.bfloat16]
+    assert rel_err(S, ref["S"]) < TOL[torch.bfloat16]
+
+
+def test_gdn_q_scale_strided_views_fp32_output():
+    dev = cuda_device()
+    B, H, N = 2, 2, 150
+    inp = synthetic.gdn_inputs(B, H, N, dtype=torch.bfloat16, seed=42)
+    packed = torch.cat([inp["q"], inp["k"], inp["v"]], dim=-1).permute(0, 2, 1, 3).contiguous().to(dev)
+    qv, kv, vv = (packed[..., i * 128:(i + 1) * 128].permute(0, 2, 1, 3) for i in range(3))
+    gates = torch.stack([inp["alpha"], inp["beta"]], dim=0).to(dev)  # [2, B, H, N]
+    obuf = torch.empty((B, N, H, 128), dtype=torch.float32, device=dev)
+    o = obuf.permute(0, 2, 1, 3)
+    _, S = la.la_gdn_prefill(qv, kv, vv, gates[0], gates[1], o=o, q_scale=0.5)
+    torch.cuda.synchronize()
+    ref = oracle_ref(inp, q_scale=0.5)
+    assert rel_err(to_np(o), ref["o"]) < TOL[torch.bfloat16]
+    assert rel_err(to_np(S), ref["S"]) < TOL[torch.bfloat16]
+
+
+def test_gdn_split_resume_and_inplace_state():
+    dev = cuda_device()
+    inp = synthetic.gdn_inputs(1, 2, 300, dtype=torch.bfloat16, seed=43)
+    x = {n: inp[n].to(dev) for n in NAMES}
+    o, S = la.la_gdn_prefill(*(x[n] for n in NAMES), out_dtype=torch.float32)
+    first = {n: x[n][:, :, :111] for n in NAMES}
+    rest = {n: x[n][:, :, 111:] for n in NAMES}
+    o1, S1 = la.la_gdn_prefill(*(first[n] for n in NAMES), out_dtype=torch.float32)
+    o2, S2 = la.la_gdn_prefill(*(rest[n] for n in NAMES), S_in=S1, S_out=S1, out_dtype=torch.float32)  # in place
+    assert S2.data_ptr() == S1.data_ptr()
+    assert rel_err(to_np(torch.cat([o1, o2], dim=2)), to_np(o)) < 1e-3
+    assert rel_err(to_np(S2), to_np(S)) < 1e-3
+
+
+def test_gdn_prefill_then_decode_matches_longer_prefill():
+    dev = cuda_device()
+    inp = synthetic.gdn_inputs(2, 2, 129, dtype=torch.bfloat16, seed=44)
+    x = {n: inp[n].to(dev) for n in NAMES}
+    _, S = la.la_gdn_prefill(*(x[n][:, :, :128] for n in NAMES))
+    o_dec = la.la_decode_step(la.LA_VARIANT_GDN, *(x[n][:, :, 128].contiguous() for n in ("q", "k", "v")), S,
+                              alpha=x["alpha"][:, :, 128].contiguous(), beta=x["beta"][:, :, 128].contiguous())
+    ref = oracle_ref(inp, t_samples=[128])
+    assert rel_err(to_np(o_dec), ref["o"][:, :, 0]) < TOL[torch.bfloat16]
+    assert rel_err(to_np(S), ref["S"]) < TOL[torch.bfloat16]
+
+
+def test_gdn_empty_sequence_passes_state():
+    dev = cuda_device()
+    z = torch.zeros((1, 2, 0, 128), dtype=torch.bfloat16, device=dev)
+    g = torch.zeros((1, 2, 0), dtype=torch.float32, device=dev)
+    S_in = torch.randn((1, 2, 128, 128), device=dev)
+    _, S = la.la_gdn_prefill(z, z, z, g, g, S_in=S_in)
+    assert torch.equal(S, S_in)
+
+
+def test_gdn_prefill_full_size():
+    """Gated DeltaNet prefill bf16/fp32-state: B=4, H=16, N=16384, the launch
+    the benchmark times; 8 sampled heads checked on every token and state."""
+    dev = cuda_device()
+    w = synthetic.WORKLOADS["gdn_prefill"]
+    inp = synthetic.workload_inputs("gdn_prefill", device=dev)
+    o, S = la.la_gdn_prefill(*(inp[n] for n in NAMES))
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(7)
+    heads = sorted(rng.choice(w.B * w.H, 8, replace=False).tolist())
+    bi = torch.tensor([h // w.H for h in heads], device=dev)
+    hi = torch.tensor([h % w.H for h in heads], device=dev)
+    sub = {n: inp[n][bi, hi].unsqueeze(0).cpu() for n in NAMES}
+    ref = oracle_ref(sub)
+    tol = TOL[torch.bfloat16]
+    assert rel_err(to_np(o[bi, hi]), ref["o"][0]) < tol
+    assert rel_err(to_np(S[bi, hi]), ref["S"][0]) < tol
+    assert la.la_device_status() == la.LA_OK
+
+
+def test_gdn_prefill_long_context_full_size():
+    """Long-context Gated DeltaNet prefill: B=1, H=16, N=1,048,576.  The whole
+    launch runs on the GPU; two heads are recomputed by the oracle over all
+    1M tokens and compared on 64 sampled output positions and the final state."""
+    dev = cuda_device()
+    w = synthetic.WORKLOADS["gdn_prefill_long"]
+    inp = synthetic.workload_inputs("gdn_prefill_long", device=dev)
+    o, S = la.la_gdn_prefill(*(inp[n] for n in NAMES))
+    torch.cuda.synchronize()
+    heads = [3, 12]
+    rng = np.random.default_rng(8)
+    t_samples = np.unique(np.concatenate([rng.choice(w.N, 60, replace=False), [0, 1, w.N - 2, w.N - 1]]))
+    sub = {n: inp[n][:, heads].cpu() for n in NAMES}
+    ref = oracle_ref(sub, t_samples=t_samples)
+    tol = TOL[torch.bfloat16]
+    ts = torch.tensor(t_samples, device=dev)
+    assert rel_err(to_np(o[:, heads][:, :, ts]), ref["o"]) < tol
+    assert rel_err(to_np(S[:, heads]), ref["S"]) < tol
+    del inp, o
+    assert la.la_device_status() == la.LA_OK
