@@ -296,11 +296,16 @@ def gpu_arm(args, ws, rank, local):
 KERNELS_PER_CALL = {"based_prefill": 1, "gdn_prefill": 1, "decode": 1}
 
 
-def other_paths(args, la, dev, stream, flush, pk, seed_off, ws):
+PATH_NAMES = ("gdn_prefill", "gdn_prefill_long", "decode_gdn", "decode_taylor")
+
+
+def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
     out = {}
     launches = 0
     steps = max(1, args.steps)
     for name in ("gdn_prefill", "gdn_prefill_long"):
+        if only is not None and name != only:
+            continue
         w = synthetic.WORKLOADS[name]
         reps = steps if name == "gdn_prefill" else max(1, min(steps, args.long_steps))
         x = synthetic.workload_inputs(name, device=dev, seed=w.seed + seed_off)
@@ -331,7 +336,11 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws):
 
     w = synthetic.WORKLOADS["decode"]
     S_, H_, n_steps = w.B, w.H, w.N
+    if only is not None:
+        n_steps = max(1, args.steps)
     for variant in ("gdn", "taylor"):
+        if only is not None and f"decode_{variant}" != only:
+            continue
         n_inputs = 16  # distinct per-step inputs, cycled (each step still reads its own q, k, v)
         xs = [synthetic.decode_step_inputs(S_, H_, i, seed=w.seed + seed_off, device=dev)[variant]
               for i in range(n_inputs)]
@@ -354,7 +363,7 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws):
                                       stream=stream)
 
         t = Timer(stream, flush)
-        t.run(lambda: run_steps(min(n_steps, 50)))  # warm-up
+        t.run(lambda: run_steps(min(n_steps, 50) if only is None else max(1, args.warmup)))  # warm-up
         t.reset()
         barrier(ws)
         t.run(lambda: run_steps(n_steps))  # the state (>L2) is streamed every step
@@ -376,9 +385,10 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws):
 # CPU oracle arm (cpu_baseline and --impl reference)
 
 
-def oracle_taylor_sample(heads=32):
+def oracle_taylor_sample(heads=128):
     """Oracle on a bounded sample of the headline workload: `heads` of its
-    128 (batch, head) pairs over the full N=4096 tokens (seeded on the CPU)."""
+    128 (batch, head) pairs over the full N=4096 tokens (seeded on the CPU;
+    the default is the whole workload, about a second of host time)."""
     w = synthetic.WORKLOADS[HEADLINE]
     B = max(1, heads // w.H)
     return synthetic.taylor_inputs(B, w.H, w.N, dtype=w.dtype, seed=w.seed), B * w.N
@@ -397,8 +407,8 @@ def cpu_baseline():
     inp, tokens = oracle_taylor_sample()
     dt = time_oracle_once(inp)
     return {"value": round(tokens / dt, 1), "unit": "tokens/s", "cores": oracle.default_threads(), "kind": "oracle",
-            "sample": f"fp64 C oracle, 2 of 8 sequences (32 of 128 heads) x N=4096 of the headline workload; "
-                      f"{dt:.2f} s wall"}
+            "sample": f"fp64 C oracle on the whole headline workload (8 sequences x 16 heads x 4096 tokens, "
+                      f"CPU-seeded inputs); {dt:.2f} s wall"}
 
 
 def reference_arm(args, ws, rank):
@@ -417,9 +427,9 @@ def reference_arm(args, ws, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.description, "B": w.B, "H": w.H, "N": w.N, "d_feat": 16, "d_v": 64,
-                       "tokens_per_step": tokens, "sample": "32 of 128 heads, all 4096 tokens"},
+                       "tokens_per_step": tokens, "sample": "all 128 heads, all 4096 tokens"},
             "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": "fp64 C oracle on 2 sequences x 16 heads x 4096 tokens per step"},
+                             "sample": "fp64 C oracle on 8 sequences x 16 heads x 4096 tokens per step"},
             "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
@@ -433,6 +443,8 @@ def main():
     ap.add_argument("--long-steps", type=int, default=3, help="timed passes of the 1M-token prefill")
     ap.add_argument("--headline-only", action="store_true", help="skip the secondary paths")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=PATH_NAMES, default=None,
+                    help="time one secondary path alone (K timed launches or decode steps), for profiling")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -446,9 +458,23 @@ def main():
         import torch.distributed as dist
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if args.only is not None:
+        import linear_attention_recurrence_chunked_gb300 as la
+        from linear_attention_recurrence_chunked_gb300 import _build
+        dev = torch.device("cuda", local)
+        torch.cuda.set_device(dev)
+        _build.build()
+        la.load_library()
+        stream = torch.cuda.Stream(device=dev)
+        flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        paths, launches = other_paths(args, la, dev, stream, flush, peaks(), 1000 * rank, ws, only=args.only)
+        if rank == 0:
+            print(json.dumps({"only": args.only, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+                              "gpu_launches": launches, **paths[args.only]}), flush=True)
+        return
     line = gpu_arm(args, ws, rank, local)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and ws == 1:
             line["cpu_baseline"] = cpu_baseline()
         print(json.dumps(line), flush=True)
     if ws > 1:
