@@ -88,6 +88,7 @@ la_status check_gdn(const la_gdn_prefill_args* a) {
   if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return LA_ERR_INVALID_ARGUMENT;
   if (a->d_k != kGdnD || a->d_v != kGdnD) return LA_ERR_UNSUPPORTED;
   if (a->B * a->H > (int64_t(1) << 28)) return LA_ERR_UNSUPPORTED;
+  if (a->N > INT32_MAX - 128) return LA_ERR_UNSUPPORTED;  // tile coordinates are 32-bit
   const int64_t B = a->B, H = a->H, N = a->N;
   if (!valid_view(a->q, B, H, N, kGdnD, a->in_dtype) || !valid_view(a->k, B, H, N, kGdnD, a->in_dtype) ||
       !valid_view(a->v, B, H, N, kGdnD, a->in_dtype) || !valid_view(a->o, B, H, N, kGdnD, a->out_dtype))
@@ -119,12 +120,12 @@ const char* la_status_string(la_status s) {
 
 size_t la_based_prefill_workspace_size(const la_based_prefill_args* a) {
   if (check_based(a) != LA_OK) return 0;
-  return la::taylor_prefill_workspace(a->B, a->H, a->N);
+  return 0;
 }
 
 size_t la_gdn_prefill_workspace_size(const la_gdn_prefill_args* a) {
   if (check_gdn(a) != LA_OK) return 0;
-  return la::gdn_prefill_workspace(a->B, a->H, a->N);
+  return 0;
 }
 
 la_status la_based_prefill(const la_based_prefill_args* a, void* ws, size_t ws_bytes, void* stream) {
@@ -138,8 +139,8 @@ la_status la_based_prefill(const la_based_prefill_args* a, void* ws, size_t ws_b
     if (r != LA_OK) return r;
     return pass_state(a->z_out, a->z_in, (size_t)(BH * kTaylorD), s);
   }
-  const size_t need = la::taylor_prefill_workspace(a->B, a->H, a->N);
-  if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned16(ws))) return LA_ERR_WORKSPACE;
+  (void)ws;
+  (void)ws_bytes;
   la::TaylorPrefillLaunch L{};
   L.B = a->B; L.H = a->H; L.N = a->N;
   L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
@@ -148,9 +149,7 @@ la_status la_based_prefill(const la_based_prefill_args* a, void* ws, size_t ws_b
   L.y = a->y.ptr; L.y_sb = a->y.stride_b; L.y_sh = a->y.stride_h; L.y_st = a->y.stride_t;
   L.s_in = a->s_in; L.z_in = a->z_in; L.s_out = a->s_out; L.z_out = a->z_out;
   L.eps = a->eps;
-  unsigned* status = device_status_ptr();
-  if (!status) return LA_ERR_CUDA;
-  return from_cuda(la::launch_taylor_prefill(L, ws, ws_bytes, status, s));
+  return from_cuda(la::launch_taylor_prefill_recurrent(L, s));
 }
 
 la_status la_gdn_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes, void* stream) {
@@ -160,8 +159,8 @@ la_status la_gdn_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes
   const int64_t BH = a->B * a->H;
   if (BH == 0) return LA_OK;
   if (a->N == 0) return pass_state(a->S_out, a->S_in, (size_t)(BH * kGdnD * kGdnD), s);
-  const size_t need = la::gdn_prefill_workspace(a->B, a->H, a->N);
-  if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned16(ws))) return LA_ERR_WORKSPACE;
+  (void)ws;
+  (void)ws_bytes;
   la::GdnPrefillLaunch L{};
   L.B = a->B; L.H = a->H; L.N = a->N;
   L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
@@ -172,9 +171,12 @@ la_status la_gdn_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes
   L.beta = static_cast<const float*>(a->beta.ptr); L.b_sb = a->beta.stride_b; L.b_sh = a->beta.stride_h;
   L.q_scale = a->q_scale;
   L.S_in = a->S_in; L.S_out = a->S_out;
+  if (!L.in_bf16) return from_cuda(la::launch_gdn_prefill_recurrent(L, s));
   unsigned* status = device_status_ptr();
   if (!status) return LA_ERR_CUDA;
-  return from_cuda(la::launch_gdn_prefill(L, ws, ws_bytes, status, s));
+  const cudaError_t e = la::launch_gdn_prefill_chunked(L, status, s);
+  if (e == cudaErrorInvalidValue) return LA_ERR_UNSUPPORTED;  // strides TMA cannot describe
+  return from_cuda(e);
 }
 
 la_status la_decode_step(const la_decode_args* a, void* stream) {

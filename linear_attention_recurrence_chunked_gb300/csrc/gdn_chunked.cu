@@ -1,0 +1,495 @@
+// gdn_chunked.cu -- chunked gated-delta-rule prefill on the tcgen05 tensor cores.
+//
+// Recurrence (NoteBank Sec. 2 Eq. (1) with A_t = alpha_t (I - beta_t k_t k_t^T)):
+//   S_t = alpha_t S_{t-1} + beta_t (v_t - alpha_t S_{t-1} k_t) k_t^T,  o_t = S_t q_t.
+// Chunk form for a chunk of C tokens with incoming state S0 (an exact
+// re-association of the recurrence; the state is carried across chunk
+// boundaries as in NoteBank Sec. 3.2):
+//   g_r = sum_{j<=r} log alpha_j,  gamma_r = e^{g_r},  Gamma_rj = e^{g_r - g_j}
+//   L   = strict_lower(diag(beta) (Gamma . K K^T)),   T = (I + L)^{-1}
+//   W   = T diag(beta gamma) K,   U~ = T diag(beta) V,   U = U~ - W S0^T
+//   O   = diag(gamma) Q S0^T + (tril(Gamma) . Q K^T) U     (times q_scale: O is linear in Q)
+//   S_C = gamma_C S0 + U^T diag(gamma_C / gamma) K
+//
+// One CTA per (batch, head) walks the chunks in order with the fp32 state S
+// resident in tensor memory.  Every product is issued as a tcgen05 MMA with
+// M = 128 by putting the 128-wide head dimension on M (the transposed
+// products W^T, U~^T, (S0 W^T), (S0 Q^T), (P U)^T), except [K;Q] K^T where
+// the K and Q tiles of the chunk are stacked into one 128-row operand.
+// Tiles arrive by TMA into a two-stage ring; the next chunk's tiles load
+// while the current one is processed.  T is solved column by column on the
+// CUDA cores (each of 64 threads solves one unit-lower-triangular system).
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace la {
+namespace {
+using namespace tc;
+
+constexpr int kC = 64;        // tokens per chunk
+constexpr int kD = 128;       // d_k = d_v
+constexpr int kThreads = 128;
+
+// shared memory map, offsets from a 1024-byte aligned base
+constexpr uint32_t kStageBytes = 49152;   // [K;Q] tile [128][128] bf16 (32 KB) + V [64][128] (16 KB)
+constexpr uint32_t kOffKQ = 0;            // within a stage
+constexpr uint32_t kOffV = 32768;         // within a stage
+constexpr uint32_t kOffS0 = 2 * kStageBytes;      // bf16 S0 [128 i][128 k], K-major
+constexpr uint32_t kOffW = kOffS0 + 32768;        // bf16 W [64 r][128 k], K-major
+constexpr uint32_t kOffT1 = kOffW + 16384;        // bf16 T diag(beta gamma) [64 r][64 j]
+constexpr uint32_t kOffT2 = kOffT1 + 8192;        // bf16 T diag(beta)       [64 r][64 j]
+constexpr uint32_t kOffPo = kOffT2 + 8192;        // bf16 tril(Gamma) . Q K^T [64 r][64 j]
+constexpr uint32_t kOffU = kOffPo + 8192;         // bf16 U^T [128 i][64 j]
+constexpr uint32_t kOffUD = kOffU + 16384;        // bf16 U^T diag(gamma_C/gamma) [128 i][64 j]
+constexpr uint32_t kOffL = kOffU;                 // fp32 L [64][65], lives only before U is formed
+constexpr uint32_t kOffGate = kOffUD + 16384;     // fp32 g[64], beta[64]
+constexpr uint32_t kSmemUsed = kOffGate + 512;
+constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
+constexpr int kLStride = 65;
+static_assert(kOffL + 64 * kLStride * 4 <= kOffGate, "L scratch overlaps the gates");
+
+// tensor-memory columns (fp32, lane = row of the M = 128 accumulator)
+constexpr uint32_t kColS = 0;     // S [i][k], 128 columns
+constexpr uint32_t kColKQ = 128;  // lanes 0..63: K K^T, lanes 64..127: Q K^T (64 columns)
+constexpr uint32_t kColW = 192;   // W^T [k][r]
+constexpr uint32_t kColUt = 256;  // U~^T [i][r]
+constexpr uint32_t kColX = 320;   // (W S0^T)^T [i][r]
+constexpr uint32_t kColY = 384;   // (Q S0^T)^T [i][r]
+constexpr uint32_t kColPU = 448;  // (P_o U)^T [i][r]
+constexpr uint32_t kTmemCols = 512;
+
+__device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sw128_desc(addr, 0, 1024); }
+
+__device__ __forceinline__ void ld64(uint32_t taddr, float* v) {
+  float a[16], b[16], c[16], d[16];
+  tmem_ld16(taddr, a);
+  tmem_ld16(taddr + 16, b);
+  tmem_ld16(taddr + 32, c);
+  tmem_ld16(taddr + 48, d);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[i] = a[i];
+    v[16 + i] = b[i];
+    v[32 + i] = c[i];
+    v[48 + i] = d[i];
+  }
+}
+
+__device__ __forceinline__ void st_bf16(uint8_t* p, float x) {
+  *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
+}
+
+template <typename TOut>
+__global__ void __launch_bounds__(kThreads, 1)
+gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const GdnPrefillLaunch a, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_tma[2];
+  __shared__ uint64_t bar_mma;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ float warp0_total;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t bh = blockIdx.x;
+  const int b = (int)(bh / a.H), h = (int)(bh % a.H);
+  const int64_t N = a.N;
+  const int nchunks = (int)((N + kC - 1) / kC);
+  float* gsm = reinterpret_cast<float*>(sm + kOffGate);
+  float* bsm = gsm + kC;
+  float* Lsm = reinterpret_cast<float*>(sm + kOffL);
+  const uint32_t sbase = smem_u32(sm);
+  const float* al_p = a.alpha + b * a.a_sb + h * a.a_sh;
+  const float* be_p = a.beta + b * a.b_sb + h * a.b_sh;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar_tma[0]), 1);
+    mbar_init(smem_u32(&bar_tma[1]), 1);
+    mbar_init(smem_u32(&bar_mma), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_v);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lane quarter
+
+  auto issue_tma = [&](int c) {
+    const uint32_t st = sbase + (uint32_t)(c & 1) * kStageBytes;
+    const uint32_t bar = smem_u32(&bar_tma[c & 1]);
+    const int t0 = c * kC;
+    mbar_arrive_expect_tx(bar, kStageBytes);
+    tma_load_4d(st + kOffKQ + 0, &tmap_k, 0, t0, h, b, bar);
+    tma_load_4d(st + kOffKQ + 16384, &tmap_k, 64, t0, h, b, bar);
+    tma_load_4d(st + kOffKQ + 8192, &tmap_q, 0, t0, h, b, bar);
+    tma_load_4d(st + kOffKQ + 24576, &tmap_q, 64, t0, h, b, bar);
+    tma_load_4d(st + kOffV + 0, &tmap_v, 0, t0, h, b, bar);
+    tma_load_4d(st + kOffV + 8192, &tmap_v, 64, t0, h, b, bar);
+  };
+  int tma_issued = 0;  // chunks whose loads have been issued (meaningful in thread 0)
+  if (tid == 0) {
+    issue_tma(0);
+    tma_issued = 1;
+    if (nchunks > 1) {
+      issue_tma(1);
+      tma_issued = 2;
+    }
+  }
+
+  // Initial state: thread i owns row i of S (TMEM lane i) and of the bf16 copy.
+  {
+    const float* src = a.S_in ? a.S_in + bh * kD * kD + (int64_t)tid * kD : nullptr;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kD; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; j += 4) {
+        const float4 x = src ? *reinterpret_cast<const float4*>(src + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
+      }
+      tmem_st16(tlane + kColS + c0, v);
+      *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(tid, c0, 128)) = pack8_bf16(v);
+      *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(tid, c0 + 8, 128)) = pack8_bf16(v + 8);
+    }
+    tmem_st_wait();
+  }
+
+  auto load_gates = [&](int c, float& lg, float& bt) {
+    const int64_t t = (int64_t)c * kC + tid;
+    if (tid < kC && t < N) {
+      lg = logf(al_p[t]);
+      bt = be_p[t];
+    } else {
+      lg = 0.f;
+      bt = 0.f;
+    }
+  };
+  float lg_next = 0.f, bt_next = 0.f;
+  load_gates(0, lg_next, bt_next);
+
+  uint32_t mma_phase = 0;
+  bool ok = true;
+  bool mma_pending = false;
+  int c = 0;
+  for (; c < nchunks; ++c) {
+    const int64_t t0 = (int64_t)c * kC;
+    const int nvalid = (N - t0 < kC) ? (int)(N - t0) : kC;
+    const uint32_t st = sbase + (uint32_t)(c & 1) * kStageBytes;
+    const float lg = lg_next, bt = bt_next;
+    if (c + 1 < nchunks) load_gates(c + 1, lg_next, bt_next);
+
+    // ---- gates: inclusive scan of log alpha over the chunk (threads 0..63)
+    float gx = lg;
+    if (tid < kC) {
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float y = __shfl_up_sync(kFullMask, gx, off);
+        if (lane >= off) gx += y;
+      }
+      if (tid == 31) warp0_total = gx;
+    }
+    __syncthreads();
+    if (tid < kC) {
+      if (warp == 1) gx += warp0_total;
+      gsm[tid] = gx;
+      bsm[tid] = bt;
+    }
+    ok = ok && mbar_wait(smem_u32(&bar_tma[c & 1]), (uint32_t)((c >> 1) & 1), status);
+    if (__syncthreads_or(!ok)) break;
+
+    // ---- MMA 1: [K;Q] K^T -> KQ, S0 Q^T -> Y
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        mma_bf16(tmem + kColKQ, kmaj(st + kOffKQ + koff), kmaj(st + kOffKQ + koff), id, ks > 0);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        mma_bf16(tmem + kColY, kmaj(sbase + kOffS0 + koff), kmaj(st + kOffKQ + 8192 + koff), id, ks > 0);
+      }
+      mma_commit(smem_u32(&bar_mma));
+    }
+    mma_pending = true;
+    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
+    mma_phase ^= 1;
+    mma_pending = !ok;
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+
+    // ---- L (lanes 0..63: rows of K K^T) and P_o (lanes 64..127: rows of Q K^T)
+    {
+      float v[64];
+      ld64(tlane + kColKQ, v);
+      if (tid < kC) {
+        const int r = tid;
+        const float gr = gsm[r], br = bsm[r];
+        float* Lrow = Lsm + r * kLStride;
+#pragma unroll
+        for (int j = 0; j < kC; ++j) Lrow[j] = (j < r) ? br * __expf(gr - gsm[j]) * v[j] : 0.f;
+      } else {
+        const int r = tid - kC;
+        const float gr = gsm[r];
+#pragma unroll
+        for (int j = 0; j < kC; ++j) v[j] = (j <= r) ? __expf(gr - gsm[j]) * v[j] : 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(sm + kOffPo + sw128_off(r, 8 * q, 64)) = pack8_bf16(v + 8 * q);
+      }
+    }
+    __syncthreads();
+
+    // ---- T = (I + L)^{-1}: thread c solves column c; writes T diag(beta gamma), T diag(beta)
+    if (tid < kC) {
+      const int cc = tid;
+      float x[kC];
+#pragma unroll
+      for (int r = 0; r < kC; ++r) {
+        float acc0 = 0.f, acc1 = 0.f;
+        const float* Lr = Lsm + r * kLStride;
+#pragma unroll
+        for (int j = 0; j + 1 < r; j += 2) {
+          acc0 = fmaf(Lr[j], x[j], acc0);
+          acc1 = fmaf(Lr[j + 1], x[j + 1], acc1);
+        }
+        if (r & 1) acc0 = fmaf(Lr[r - 1], x[r - 1], acc0);
+        x[r] = (r < cc) ? 0.f : ((r == cc) ? 1.f : -(acc0 + acc1));
+      }
+      const float bc = bsm[cc];
+      const float bgc = bc * __expf(gsm[cc]);
+#pragma unroll
+      for (int r = 0; r < kC; ++r) {
+        st_bf16(sm + kOffT1 + sw128_off(r, cc, 64), x[r] * bgc);
+        st_bf16(sm + kOffT2 + sw128_off(r, cc, 64), x[r] * bc);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // ---- MMA 2: W^T = K^T (T diag(beta gamma))^T, U~^T = V^T (T diag(beta))^T
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t id = idesc_bf16(128, 64, 1, 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + kColW, sw128_desc(st + kOffKQ + ks * 2048, 16384, 1024), kmaj(sbase + kOffT1 + ks * 32),
+                 id, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + kColUt, sw128_desc(st + kOffV + ks * 2048, 8192, 1024), kmaj(sbase + kOffT2 + ks * 32),
+                 id, ks > 0);
+      mma_commit(smem_u32(&bar_mma));
+    }
+    mma_pending = true;
+    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
+    mma_phase ^= 1;
+    mma_pending = !ok;
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+
+    // ---- W tile (bf16, [r][k]): thread k writes column k
+    {
+      float w[64];
+      ld64(tlane + kColW, w);
+#pragma unroll
+      for (int r = 0; r < kC; ++r) st_bf16(sm + kOffW + sw128_off(r, tid, 64), w[r]);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- MMA 3: X = S0 W^T ; meanwhile S <- gamma_C S in tensor memory
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        const uint32_t woff = (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u;
+        mma_bf16(tmem + kColX, kmaj(sbase + kOffS0 + koff), kmaj(sbase + kOffW + woff), id, ks > 0);
+      }
+      mma_commit(smem_u32(&bar_mma));
+    }
+    mma_pending = true;
+    {
+      const float gamC = __expf(gsm[kC - 1]);
+#pragma unroll 1
+      for (int c0 = 0; c0 < kD; c0 += 16) {
+        float v[16];
+        tmem_ld16(tlane + kColS + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] *= gamC;
+        tmem_st16(tlane + kColS + c0, v);
+      }
+      tmem_st_wait();
+    }
+    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
+    mma_phase ^= 1;
+    mma_pending = !ok;
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+
+    // ---- U^T = U~^T - X (thread i owns row i); also U^T diag(gamma_C / gamma)
+    {
+      float u[64], x[64];
+      ld64(tlane + kColUt, u);
+      ld64(tlane + kColX, x);
+      const float gC = gsm[kC - 1];
+      float ud[64];
+#pragma unroll
+      for (int j = 0; j < kC; ++j) {
+        u[j] -= x[j];
+        ud[j] = u[j] * __expf(gC - gsm[j]);
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        *reinterpret_cast<uint4*>(sm + kOffU + sw128_off(tid, 8 * q, 128)) = pack8_bf16(u + 8 * q);
+        *reinterpret_cast<uint4*>(sm + kOffUD + sw128_off(tid, 8 * q, 128)) = pack8_bf16(ud + 8 * q);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- MMA 4: (P_o U)^T = U^T P_o^T ; S += U^T diag(gamma_C/gamma) K
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, 64, 0, 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + kColPU, kmaj(sbase + kOffU + ks * 32), kmaj(sbase + kOffPo + ks * 32), id, ks > 0);
+      const uint32_t id2 = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        mma_bf16(tmem + kColS, kmaj(sbase + kOffUD + ks * 32), sw128_desc(st + kOffKQ + ks * 2048, 16384, 1024),
+                 id2, 1u);
+      mma_commit(smem_u32(&bar_mma));
+    }
+    mma_pending = true;
+    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
+    mma_phase ^= 1;
+    mma_pending = !ok;
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+
+    // ---- outputs o[t0 + r][i] = gamma_r Y[i][r] + PU[i][r]; next bf16 S0 row i
+    {
+      float y[64], p[64];
+      ld64(tlane + kColY, y);
+      ld64(tlane + kColPU, p);
+      TOut* obase = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + t0 * a.o_st + tid;
+#pragma unroll
+      for (int r = 0; r < kC; ++r)
+        if (r < nvalid) store1(obase + r * a.o_st, a.q_scale * fmaf(__expf(gsm[r]), y[r], p[r]));
+#pragma unroll 1
+      for (int c0 = 0; c0 < kD; c0 += 16) {
+        float v[16];
+        tmem_ld16(tlane + kColS + c0, v);
+        tmem_ld_wait();
+        *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(tid, c0, 128)) = pack8_bf16(v);
+        *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(tid, c0 + 8, 128)) = pack8_bf16(v + 8);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && c + 2 < nchunks) {
+      issue_tma(c + 2);
+      tma_issued = c + 3;
+    }
+  }
+
+  if (ok) {
+    // final state, row i from lane i
+    float* dst = a.S_out + bh * kD * kD + (int64_t)tid * kD;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kD; c0 += 16) {
+      float v[16];
+      tmem_ld16(tlane + kColS + c0, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    }
+  } else if (tid == 0) {
+    // a wait expired: let this CTA's own copies and MMAs drain (bounded) before freeing TMEM
+    for (int k = c; k < tma_issued; ++k) mbar_wait(smem_u32(&bar_tma[k & 1]), (uint32_t)((k >> 1) & 1), status);
+    if (mma_pending) mbar_wait(smem_u32(&bar_mma), mma_phase, status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ----------------------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 [B, H, N, 128] view -> 4-D tensor map with a (64 features x 64 tokens) box, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const View4& x, int64_t B, int64_t H, int64_t N) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)(x.st * 2), (cuuint64_t)(x.sh * 2), (cuuint64_t)(x.sb * 2)};
+  const cuuint32_t box[4] = {64, (cuuint32_t)kC, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(x.ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename TOut>
+cudaError_t launch_typed(const GdnPrefillLaunch& a, unsigned* status, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  // strides of 0 (broadcast views) or not multiples of 16 bytes cannot be described
+  if (!make_map(&mq, a.q, a.B, a.H, a.N) || !make_map(&mk, a.k, a.B, a.H, a.N) || !make_map(&mv, a.v, a.B, a.H, a.N))
+    return cudaErrorInvalidValue;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(gdn_chunked_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemAlloc);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  gdn_chunked_kernel<TOut><<<(unsigned)(a.B * a.H), kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gdn_prefill_chunked(const GdnPrefillLaunch& a, unsigned* status, cudaStream_t stream) {
+  if (a.B * a.H == 0 || a.N == 0) return cudaSuccess;
+  return a.out_bf16 ? launch_typed<__nv_bfloat16>(a, status, stream) : launch_typed<float>(a, status, stream);
+}
+
+}  // namespace la

@@ -53,11 +53,10 @@ struct GdnPrefillLaunch {
 
 cudaError_t launch_gdn_decode(const DecodeLaunch& a, cudaStream_t stream);
 cudaError_t launch_taylor_decode(const DecodeLaunch& a, cudaStream_t stream);
-cudaError_t launch_taylor_prefill(const TaylorPrefillLaunch& a, void* ws, size_t ws_bytes,
-                                  unsigned* dev_status, cudaStream_t stream);
-cudaError_t launch_gdn_prefill(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes,
-                               unsigned* dev_status, cudaStream_t stream);
-size_t taylor_prefill_workspace(int64_t B, int64_t H, int64_t N);
-size_t gdn_prefill_workspace(int64_t B, int64_t H, int64_t N);
+// fp32 inputs: token-serial CUDA-core kernels (fp32 arithmetic throughout).
+cudaError_t launch_taylor_prefill_recurrent(const TaylorPrefillLaunch& a, cudaStream_t stream);
+cudaError_t launch_gdn_prefill_recurrent(const GdnPrefillLaunch& a, cudaStream_t stream);
+// bf16 inputs: chunked tcgen05 kernels.
+cudaError_t launch_gdn_prefill_chunked(const GdnPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
 
 }  // namespace la

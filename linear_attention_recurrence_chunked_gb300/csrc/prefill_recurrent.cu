@@ -2,7 +2,9 @@
 //
 // Each CTA walks the sequence one token at a time with its slice of the
 // state held in registers, exactly as the recurrence reads
-// (NoteBank Sec. 2 Eq. (1); BASED reading notes Sec. 2.2).
+// (NoteBank Sec. 2 Eq. (1); BASED reading notes Sec. 2.2).  These serve fp32
+// inputs, whose 1e-4 accuracy contract the bf16 tensor-core chunk kernels
+// cannot meet; bf16 inputs take the chunked kernels.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -200,10 +202,7 @@ taylor_prefill_recurrent_kernel(TaylorPrefillLaunch a) {
 
 }  // namespace
 
-size_t taylor_prefill_workspace(int64_t, int64_t, int64_t) { return 0; }
-size_t gdn_prefill_workspace(int64_t, int64_t, int64_t) { return 0; }
-
-cudaError_t launch_gdn_prefill(const GdnPrefillLaunch& a, void*, size_t, unsigned*, cudaStream_t stream) {
+cudaError_t launch_gdn_prefill_recurrent(const GdnPrefillLaunch& a, cudaStream_t stream) {
   const int64_t grid = a.B * a.H * (kD / kSlab);
   if (grid == 0) return cudaSuccess;
 #define LA_GDN_PF(TI, TO) gdn_prefill_recurrent_kernel<TI, TO><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(a)
@@ -215,7 +214,7 @@ cudaError_t launch_gdn_prefill(const GdnPrefillLaunch& a, void*, size_t, unsigne
   return cudaGetLastError();
 }
 
-cudaError_t launch_taylor_prefill(const TaylorPrefillLaunch& a, void*, size_t, unsigned*, cudaStream_t stream) {
+cudaError_t launch_taylor_prefill_recurrent(const TaylorPrefillLaunch& a, cudaStream_t stream) {
   const int64_t grid = a.B * a.H;
   if (grid == 0) return cudaSuccess;
 #define LA_TAY_PF(TI, TO) taylor_prefill_recurrent_kernel<TI, TO><<<(unsigned)grid, kTThreads, 0, stream>>>(a)

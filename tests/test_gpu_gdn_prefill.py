@@ -70,8 +70,15 @@ def test_gdn_split_resume_and_inplace_state():
     o1, S1 = la.la_gdn_prefill(*(first[n] for n in NAMES), out_dtype=torch.float32)
     o2, S2 = la.la_gdn_prefill(*(rest[n] for n in NAMES), S_in=S1, S_out=S1, out_dtype=torch.float32)  # in place
     assert S2.data_ptr() == S1.data_ptr()
-    assert rel_err(to_np(torch.cat([o1, o2], dim=2)), to_np(o)) < 1e-3
-    assert rel_err(to_np(S2), to_np(S)) < 1e-3
+    # the split moves chunk boundaries, so bf16 operand rounding differs:
+    # each run meets the bf16 contract against the oracle, and the two GPU
+    # runs agree to well inside it
+    ref = oracle_ref(inp)
+    o12 = to_np(torch.cat([o1, o2], dim=2))
+    assert rel_err(o12, ref["o"]) < TOL[torch.bfloat16] and rel_err(to_np(o), ref["o"]) < TOL[torch.bfloat16]
+    assert rel_err(to_np(S2), ref["S"]) < TOL[torch.bfloat16]
+    assert rel_err(o12, to_np(o)) < 1e-2
+    assert rel_err(to_np(S2), to_np(S)) < 1e-2
 
 
 def test_gdn_prefill_then_decode_matches_longer_prefill():
