@@ -68,6 +68,7 @@ la_status check_based(const la_based_prefill_args* a) {
   if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return LA_ERR_INVALID_ARGUMENT;
   if (a->d_feat != kTaylorF || a->d_v != kTaylorDv) return LA_ERR_UNSUPPORTED;
   if (a->B * a->H > (int64_t(1) << 31) - 1) return LA_ERR_UNSUPPORTED;
+  if (a->N > INT32_MAX - 128) return LA_ERR_UNSUPPORTED;  // tile coordinates are 32-bit
   const int64_t B = a->B, H = a->H, N = a->N;
   if (!valid_view(a->q, B, H, N, kTaylorF, a->in_dtype) || !valid_view(a->k, B, H, N, kTaylorF, a->in_dtype) ||
       !valid_view(a->v, B, H, N, kTaylorDv, a->in_dtype) || !valid_view(a->y, B, H, N, kTaylorDv, a->out_dtype))
@@ -149,7 +150,12 @@ la_status la_based_prefill(const la_based_prefill_args* a, void* ws, size_t ws_b
   L.y = a->y.ptr; L.y_sb = a->y.stride_b; L.y_sh = a->y.stride_h; L.y_st = a->y.stride_t;
   L.s_in = a->s_in; L.z_in = a->z_in; L.s_out = a->s_out; L.z_out = a->z_out;
   L.eps = a->eps;
-  return from_cuda(la::launch_taylor_prefill_recurrent(L, s));
+  if (!L.in_bf16) return from_cuda(la::launch_taylor_prefill_recurrent(L, s));
+  unsigned* status = device_status_ptr();
+  if (!status) return LA_ERR_CUDA;
+  const cudaError_t e = la::launch_taylor_prefill_chunked(L, status, s);
+  if (e == cudaErrorInvalidValue) return LA_ERR_UNSUPPORTED;  // strides TMA cannot describe
+  return from_cuda(e);
 }
 
 la_status la_gdn_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes, void* stream) {

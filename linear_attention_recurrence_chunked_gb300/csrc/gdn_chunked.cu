@@ -17,8 +17,9 @@
 // products W^T, U~^T, (S0 W^T), (S0 Q^T), (P U)^T), except [K;Q] K^T where
 // the K and Q tiles of the chunk are stacked into one 128-row operand.
 // Tiles arrive by TMA into a two-stage ring; the next chunk's tiles load
-// while the current one is processed.  T is solved column by column on the
-// CUDA cores (each of 64 threads solves one unit-lower-triangular system).
+// while the current one is processed.  T is inverted on the CUDA cores in
+// 16x16 blocks: diagonal blocks by forward substitution, the blocks below
+// them by block forward substitution.
 #include <mutex>
 
 #include "common.cuh"
@@ -45,11 +46,14 @@ constexpr uint32_t kOffPo = kOffT2 + 8192;        // bf16 tril(Gamma) . Q K^T [6
 constexpr uint32_t kOffU = kOffPo + 8192;         // bf16 U^T [128 i][64 j]
 constexpr uint32_t kOffUD = kOffU + 16384;        // bf16 U^T diag(gamma_C/gamma) [128 i][64 j]
 constexpr uint32_t kOffL = kOffU;                 // fp32 L [64][65], lives only before U is formed
-constexpr uint32_t kOffGate = kOffUD + 16384;     // fp32 g[64], beta[64]
-constexpr uint32_t kSmemUsed = kOffGate + 512;
+constexpr uint32_t kOffZ = kOffL + 64 * 65 * 4;   // fp32 3 x [16][16] block products (same lifetime)
+constexpr uint32_t kOffGate = kOffUD + 16384;     // fp32 g[64], beta[64], gamma[64]
+constexpr uint32_t kSmemUsed = kOffGate + 768;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
 constexpr int kLStride = 65;
-static_assert(kOffL + 64 * kLStride * 4 <= kOffGate, "L scratch overlaps the gates");
+constexpr int kTStride = 64;                      // fp32 T [64][64] reuses the W tile space
+static_assert(kOffZ + 3 * 256 * 4 <= kOffGate, "L/Z scratch overlaps the gates");
+static_assert(64 * kTStride * 4 <= 16384, "T scratch exceeds the W tile");
 
 // tensor-memory columns (fp32, lane = row of the M = 128 accumulator)
 constexpr uint32_t kColS = 0;     // S [i][k], 128 columns
@@ -101,6 +105,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   const int nchunks = (int)((N + kC - 1) / kC);
   float* gsm = reinterpret_cast<float*>(sm + kOffGate);
   float* bsm = gsm + kC;
+  float* gam = gsm + 2 * kC;
   float* Lsm = reinterpret_cast<float*>(sm + kOffL);
   const uint32_t sbase = smem_u32(sm);
   const float* al_p = a.alpha + b * a.a_sb + h * a.a_sh;
@@ -204,6 +209,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       if (warp == 1) gx += warp0_total;
       gsm[tid] = gx;
       bsm[tid] = bt;
+      gam[tid] = __expf(gx);
     }
     ok = ok && mbar_wait(smem_u32(&bar_tma[c & 1]), (uint32_t)((c >> 1) & 1), status);
     if (__syncthreads_or(!ok)) break;
@@ -253,28 +259,73 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     }
     __syncthreads();
 
-    // ---- T = (I + L)^{-1}: thread c solves column c; writes T diag(beta gamma), T diag(beta)
-    if (tid < kC) {
-      const int cc = tid;
-      float x[kC];
+    // ---- T = (I + L)^{-1} in 16x16 blocks (fp32, in the dead W tile space):
+    // diagonal blocks by forward substitution (one thread per block column),
+    // then block row i: T_ij = -T_ii sum_{m=j}^{i-1} L_im T_mj for j < i.
+    {
+      float* Tsm = reinterpret_cast<float*>(sm + kOffW);
+      float* Zsm = reinterpret_cast<float*>(sm + kOffZ);
+      if (tid < kC) {
+        const int base = (tid >> 4) * 16, col = tid & 15;
+        float x[16];
 #pragma unroll
-      for (int r = 0; r < kC; ++r) {
-        float acc0 = 0.f, acc1 = 0.f;
-        const float* Lr = Lsm + r * kLStride;
+        for (int r = 0; r < 16; ++r) {
+          float acc = 0.f;
 #pragma unroll
-        for (int j = 0; j + 1 < r; j += 2) {
-          acc0 = fmaf(Lr[j], x[j], acc0);
-          acc1 = fmaf(Lr[j + 1], x[j + 1], acc1);
+          for (int j = 0; j < r; ++j) acc = fmaf(Lsm[(base + r) * kLStride + base + j], x[j], acc);
+          x[r] = (r < col) ? 0.f : ((r == col) ? 1.f : -acc);
         }
-        if (r & 1) acc0 = fmaf(Lr[r - 1], x[r - 1], acc0);
-        x[r] = (r < cc) ? 0.f : ((r == cc) ? 1.f : -(acc0 + acc1));
-      }
-      const float bc = bsm[cc];
-      const float bgc = bc * __expf(gsm[cc]);
 #pragma unroll
-      for (int r = 0; r < kC; ++r) {
-        st_bf16(sm + kOffT1 + sw128_off(r, cc, 64), x[r] * bgc);
-        st_bf16(sm + kOffT2 + sw128_off(r, cc, 64), x[r] * bc);
+        for (int r = 0; r < 16; ++r) Tsm[(base + r) * kTStride + base + col] = x[r];
+      } else {
+        // zero the six blocks above the block diagonal
+        for (int e = tid - kC; e < 6 * 256; e += kC) {
+          const int pr = e >> 8, w = e & 255;
+          const int bi = pr < 3 ? 0 : (pr < 5 ? 1 : 2);
+          const int bj = pr < 3 ? pr + 1 : (pr < 5 ? pr - 1 : 3);
+          Tsm[(bi * 16 + (w >> 4)) * kTStride + bj * 16 + (w & 15)] = 0.f;
+        }
+      }
+      __syncthreads();
+#pragma unroll 1
+      for (int i = 1; i < 4; ++i) {
+        for (int e = tid; e < i * 256; e += kThreads) {
+          const int j = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+          const float* Lr = Lsm + (16 * i + r) * kLStride;
+          float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 4
+          for (int q = 16 * j; q < 16 * i; q += 2) {
+            acc0 = fmaf(Lr[q], Tsm[q * kTStride + 16 * j + cc], acc0);
+            acc1 = fmaf(Lr[q + 1], Tsm[(q + 1) * kTStride + 16 * j + cc], acc1);
+          }
+          Zsm[e] = acc0 + acc1;
+        }
+        __syncthreads();
+        for (int e = tid; e < i * 256; e += kThreads) {
+          const int j = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+          const float* Tr = Tsm + (16 * i + r) * kTStride + 16 * i;
+          float acc = 0.f;
+#pragma unroll
+          for (int p2 = 0; p2 < 16; ++p2) acc = fmaf(Tr[p2], Zsm[(j << 8) + p2 * 16 + cc], acc);
+          Tsm[(16 * i + r) * kTStride + 16 * j + cc] = -acc;
+        }
+        __syncthreads();
+      }
+      // bf16 tiles T diag(beta gamma) and T diag(beta): thread -> half a row
+      {
+        const int r = tid >> 1, c0 = (tid & 1) * 32;
+        float t1[32], t2[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float t = Tsm[r * kTStride + c0 + j];
+          t2[j] = t * bsm[c0 + j];
+          t1[j] = t2[j] * gam[c0 + j];
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          *reinterpret_cast<uint4*>(sm + kOffT1 + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t1 + 8 * q);
+          *reinterpret_cast<uint4*>(sm + kOffT2 + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t2 + 8 * q);
+        }
       }
     }
     fence_proxy_async_smem();

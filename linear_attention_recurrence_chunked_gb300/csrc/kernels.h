@@ -58,5 +58,6 @@ cudaError_t launch_taylor_prefill_recurrent(const TaylorPrefillLaunch& a, cudaSt
 cudaError_t launch_gdn_prefill_recurrent(const GdnPrefillLaunch& a, cudaStream_t stream);
 // bf16 inputs: chunked tcgen05 kernels.
 cudaError_t launch_gdn_prefill_chunked(const GdnPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
+cudaError_t launch_taylor_prefill_chunked(const TaylorPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
 
 }  // namespace la

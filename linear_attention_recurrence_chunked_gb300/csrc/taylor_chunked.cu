@@ -1,0 +1,506 @@
+// taylor_chunked.cu -- chunked Taylor (BASED) linear-attention prefill on tcgen05.
+//
+// Definition (BASED reading notes Sec. 2.2-2.3, paper Eqs. (1)-(4)):
+//   phi(x) = [1, x, vec(x x^T)/sqrt(2)],  s_i = s_{i-1} + phi(k_i) v_i^T,
+//   z_i = z_{i-1} + phi(k_i),  y_i = s_i^T phi(q_i) / (z_i^T phi(q_i) + eps).
+// Block decomposition (BASED notes Sec. 2.5): for a chunk b of C tokens
+//   num = (M . (1 + Q K^T + (Q K^T)^2 / 2)) V + Phi_Q s_{<b}
+//   den = rowsum(M . (1 + Q K^T + (Q K^T)^2 / 2)) + Phi_Q z_{<b}
+//   s_{<b+1} = s_{<b} + Phi_K^T V,   z_{<b+1} = z_{<b} + Phi_K^T 1
+// with M the inclusive causal mask; the intra-chunk block uses the closed
+// form kernel 1 + a + a^2/2 (paper Eq. (4)), so the C x D feature product
+// is never formed for it.
+//
+// Inside the kernel the state is kept in the compact symmetric feature basis
+// (the pages' 153-wide count, padded to 160): c = [1, x_a, x_a^2/sqrt2,
+// x_a x_b (a<b)] gives the same kernel value as phi with half the width.  The
+// 273-row state of the interface relates to it by c_(a,a) = s_(a,a) and
+// c_(a,b) = (s_(a,b) + s_(b,a))/sqrt2 for a < b; only this symmetric part
+// enters any readout, and the final state is returned as s_in + the
+// accumulated update expanded back to 273 rows, so the result is exact for
+// any incoming state.
+//
+// One CTA (128 threads, thread r = token r of the chunk) per (batch, head);
+// V tiles arrive by TMA (two stages), q and k by plain loads (the features
+// are formed from them in registers).  Tensor-memory state: c[0:128) as an
+// M = 128 accumulator and c[128:192) as an M = 64 accumulator, 64 columns each.
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace la {
+namespace {
+using namespace tc;
+
+constexpr int kC = 128;      // tokens per chunk
+constexpr int kF = 16;       // d'
+constexpr int kDv = 64;      // d_v
+constexpr int kDc = 160;     // compact features, padded (153 used)
+constexpr int kDcUsed = 1 + kF + kF + kF * (kF - 1) / 2;  // 153
+constexpr int kDfull = 1 + kF + kF * kF;                  // 273
+constexpr int kThreads = 128;
+constexpr float kInvSqrt2 = 0.70710678118654752f;
+
+// shared memory (offsets from a 1024-byte aligned base)
+constexpr uint32_t kOffV = 0;                    // 2 stages x bf16 V [128 tokens][64] (16 KB each)
+constexpr uint32_t kOffQK = 32768;               // bf16 [128 tokens][64]: cols 0..15 q, 16..31 k
+constexpr uint32_t kOffPhiQ = kOffQK + 16384;    // bf16 [128 tokens][192] (3 blocks of 16 KB)
+constexpr uint32_t kOffPhiK = kOffPhiQ + 49152;  // bf16 [128 tokens][192]
+constexpr uint32_t kOffP = kOffPhiK + 49152;     // bf16 [128 r][128 j] (2 blocks of 16 KB)
+constexpr uint32_t kOffCt = kOffP + 32768;       // bf16 c [192 features][64 v] (24 KB)
+constexpr uint32_t kOffZ = kOffCt + 24576;       // fp32 z[160]
+constexpr uint32_t kSmemUsed = kOffZ + kDc * 4;
+constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
+
+// tensor memory columns
+constexpr uint32_t kColC0 = 0;     // features 0..127  (M = 128: lane = feature), 64 cols
+constexpr uint32_t kColC1 = 64;    // features 128..191 (M = 64 layout), 64 cols
+constexpr uint32_t kColAcc = 128;  // numerator [token][v], 64 cols
+constexpr uint32_t kColQK = 256;   // Q K^T [r][j], 128 cols
+constexpr uint32_t kTmemCols = 512;
+
+__device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sw128_desc(addr, 0, 1024); }
+
+// Compact feature j of x (j < 160): 1 | x_a | x_a^2/sqrt2 | x_a x_b (a<b, row-major) | 0.
+// Pair index p in 0..119 enumerates (0,1),(0,2),...,(0,15),(1,2),...,(14,15).
+__device__ __forceinline__ void compact_features(const float* x, float* f) {
+  f[0] = 1.f;
+#pragma unroll
+  for (int a = 0; a < kF; ++a) f[1 + a] = x[a];
+#pragma unroll
+  for (int a = 0; a < kF; ++a) f[1 + kF + a] = x[a] * x[a] * kInvSqrt2;
+  int p = 1 + 2 * kF;
+#pragma unroll
+  for (int a = 0; a < kF; ++a)
+#pragma unroll
+    for (int b = a + 1; b < kF; ++b) f[p++] = x[a] * x[b];
+#pragma unroll
+  for (int j = kDcUsed; j < kDc; ++j) f[j] = 0.f;
+}
+
+// (a, b) of compact pair feature j (33 <= j < 153), computed by counting.
+__device__ __forceinline__ void pair_of(int j, int& a, int& b) {
+  int p = j - (1 + 2 * kF);
+  a = 0;
+  while (p >= kF - 1 - a) {
+    p -= kF - 1 - a;
+    ++a;
+  }
+  b = a + 1 + p;
+}
+
+// Full-basis state rows of compact feature j; returns how many (1 or 2).
+__device__ __forceinline__ int full_rows_of(int j, int& r0, int& r1, float& scale) {
+  if (j < 1 + kF) { r0 = j; r1 = -1; scale = 1.f; return 1; }
+  if (j < 1 + 2 * kF) { const int a = j - 1 - kF; r0 = 1 + kF + a * kF + a; r1 = -1; scale = 1.f; return 1; }
+  int a, b;
+  pair_of(j, a, b);
+  r0 = 1 + kF + a * kF + b;
+  r1 = 1 + kF + b * kF + a;
+  scale = kInvSqrt2;
+  return 2;
+}
+
+// Tensor-memory lane and column base holding compact feature j (j < 192).
+// Features 0..127: the M = 128 accumulator, lane j.  Features 128..191: the
+// M = 64 accumulator, whose row m lives in lane (m % 16) + 32 (m / 16).
+__device__ __forceinline__ int feature_of_lane(int lane) {
+  // inverse map for the M = 64 accumulator (-1 for unused lanes)
+  const int q = lane >> 5, w = lane & 31;
+  return w < 16 ? 128 + q * 16 + w : -1;
+}
+
+template <typename TOut>
+__global__ void __launch_bounds__(kThreads, 1)
+taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPrefillLaunch a, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_tma[2];
+  __shared__ uint64_t bar_mma;
+  __shared__ uint32_t tmem_base_sh;
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int64_t bh = blockIdx.x;
+  const int b = (int)(bh / a.H), h = (int)(bh % a.H);
+  const int64_t N = a.N;
+  const int nchunks = (int)((N + kC - 1) / kC);
+  const uint32_t sbase = smem_u32(sm);
+  float* zsm = reinterpret_cast<float*>(sm + kOffZ);
+  const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q.ptr) + b * a.q.sb + h * a.q.sh;
+  const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(a.k.ptr) + b * a.k.sb + h * a.k.sh;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar_tma[0]), 1);
+    mbar_init(smem_u32(&bar_tma[1]), 1);
+    mbar_init(smem_u32(&bar_mma), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_v);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+
+  auto issue_tma = [&](int c) {
+    const uint32_t bar = smem_u32(&bar_tma[c & 1]);
+    mbar_arrive_expect_tx(bar, 16384);
+    tma_load_4d(sbase + kOffV + (uint32_t)(c & 1) * 16384u, &tmap_v, 0, c * kC, h, b, bar);
+  };
+  int tma_issued = 0;
+  if (tid == 0) {
+    issue_tma(0);
+    tma_issued = 1;
+    if (nchunks > 1) {
+      issue_tma(1);
+      tma_issued = 2;
+    }
+  }
+
+  // ---- initial compact state c_in (fp32 in TMEM, bf16 tile) and z
+  // thread t handles feature t of the M=128 accumulator and, if its lane is
+  // one of the M=64 accumulator's, feature feature_of_lane(t).
+  const float* s_in = a.s_in ? a.s_in + bh * kDfull * kDv : nullptr;
+  const float* z_in = a.z_in ? a.z_in + bh * kDfull : nullptr;
+  auto compact_row = [&](int j, float* row /*64*/) {
+    if (!s_in || j >= kDcUsed) {
+#pragma unroll
+      for (int c = 0; c < kDv; ++c) row[c] = 0.f;
+      return;
+    }
+    int r0, r1;
+    float sc;
+    const int n = full_rows_of(j, r0, r1, sc);
+#pragma unroll
+    for (int c = 0; c < kDv; c += 4) {
+      float4 x = *reinterpret_cast<const float4*>(s_in + r0 * kDv + c);
+      if (n == 2) {
+        const float4 y = *reinterpret_cast<const float4*>(s_in + r1 * kDv + c);
+        x.x = (x.x + y.x) * sc; x.y = (x.y + y.y) * sc; x.z = (x.z + y.z) * sc; x.w = (x.w + y.w) * sc;
+      }
+      row[c] = x.x; row[c + 1] = x.y; row[c + 2] = x.z; row[c + 3] = x.w;
+    }
+  };
+  auto compact_z = [&](int j) -> float {
+    if (!z_in || j >= kDcUsed) return 0.f;
+    int r0, r1;
+    float sc;
+    const int n = full_rows_of(j, r0, r1, sc);
+    return n == 2 ? (z_in[r0] + z_in[r1]) * sc : z_in[r0];
+  };
+  {
+    float row[kDv];
+    compact_row(tid, row);
+#pragma unroll
+    for (int c = 0; c < kDv; c += 16) tmem_st16(tlane + kColC0 + c, *reinterpret_cast<float(*)[16]>(row + c));
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(tid, 8 * q, 192)) = pack8_bf16(row + 8 * q);
+    const int f1 = feature_of_lane(tid);
+    compact_row(f1 < 0 ? kDc : f1, row);
+#pragma unroll
+    for (int c = 0; c < kDv; c += 16) tmem_st16(tlane + kColC1 + c, *reinterpret_cast<float(*)[16]>(row + c));
+    if (f1 >= 0) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(f1, 8 * q, 192)) = pack8_bf16(row + 8 * q);
+    }
+    zsm[tid] = compact_z(tid);
+    if (tid < kDc - 128) zsm[128 + tid] = compact_z(128 + tid);
+    tmem_st_wait();
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  uint32_t mma_phase = 0;
+  bool ok = true;
+  bool mma_pending = false;
+  int c = 0;
+  for (; c < nchunks; ++c) {
+    const int64_t t0 = (int64_t)c * kC;
+    const int64_t t = t0 + tid;
+    const bool valid = t < N;
+    // ---- this token's q, k; compact features into the Phi tiles; q|k into the QK tile
+    float xq[kF], xk[kF];
+    {
+      if (valid) {
+        const uint4* q4 = reinterpret_cast<const uint4*>(qp + t * a.q.st);
+        const uint4* k4 = reinterpret_cast<const uint4*>(kp + t * a.k.st);
+        uint4 raw[4] = {q4[0], q4[1], k4[0], k4[1]};
+        *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(tid, 0, kC)) = raw[0];
+        *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(tid, 8, kC)) = raw[1];
+        *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(tid, 16, kC)) = raw[2];
+        *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(tid, 24, kC)) = raw[3];
+        const __nv_bfloat16* hq = reinterpret_cast<const __nv_bfloat16*>(&raw[0]);
+        const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(&raw[2]);
+#pragma unroll
+        for (int i = 0; i < kF; ++i) {
+          xq[i] = __bfloat162float(hq[i]);
+          xk[i] = __bfloat162float(hk[i]);
+        }
+      } else {
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(tid, 8 * q, kC)) = zero;
+#pragma unroll
+        for (int i = 0; i < kF; ++i) xq[i] = xk[i] = 0.f;
+      }
+      float f[kDc];
+      compact_features(xq, f);
+#pragma unroll
+      for (int q = 0; q < kDc / 8; ++q)
+        *reinterpret_cast<uint4*>(sm + kOffPhiQ + sw128_off(tid, 8 * q, kC)) = pack8_bf16(f + 8 * q);
+      compact_features(xk, f);
+      if (!valid) f[0] = 0.f;  // padded tokens contribute nothing to the state
+#pragma unroll
+      for (int q = 0; q < kDc / 8; ++q)
+        *reinterpret_cast<uint4*>(sm + kOffPhiK + sw128_off(tid, 8 * q, kC)) = pack8_bf16(f + 8 * q);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    // ---- MMA 1: Q K^T -> QK ; Phi_Q c_{<b} -> Acc
+    if (tid == 0) {
+      mma_bf16(tmem + kColQK, kmaj(sbase + kOffQK), kmaj(sbase + kOffQK + 32), idesc_bf16(128, 128, 0, 0), 0u);
+      const uint32_t id = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+      for (int ks = 0; ks < kDc / 16; ++ks) {
+        const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        mma_bf16(tmem + kColAcc, kmaj(sbase + kOffPhiQ + aoff), sw128_desc(sbase + kOffCt + ks * 2048, 0, 1024), id,
+                 ks > 0);
+      }
+      mma_commit(smem_u32(&bar_mma));
+    }
+    mma_pending = true;
+    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
+    mma_phase ^= 1;
+    mma_pending = !ok;
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+
+    // ---- P = tril(1 + A + A^2/2) (row r = tid), row sums; denominator
+    float den;
+    {
+      float p[kC];
+#pragma unroll
+      for (int c0 = 0; c0 < kC; c0 += 16) {
+        float v[16];
+        tmem_ld16(tlane + kColQK + c0, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float x = v[j];
+          p[c0 + j] = (c0 + j <= tid && valid) ? fmaf(0.5f * x, x, 1.f + x) : 0.f;
+        }
+      }
+      float rs = 0.f;
+#pragma unroll
+      for (int j = 0; j < kC; ++j) rs += p[j];
+#pragma unroll
+      for (int q = 0; q < kC / 8; ++q)
+        *reinterpret_cast<uint4*>(sm + kOffP + sw128_off(tid, 8 * q, kC)) = pack8_bf16(p + 8 * q);
+      // phi_c(q) . z_{<b} in fp32
+      float fq[kDc];
+      compact_features(xq, fq);
+      float dz = 0.f;
+#pragma unroll
+      for (int j = 0; j < kDcUsed; ++j) dz = fmaf(fq[j], zsm[j], dz);
+      den = rs + dz;
+    }
+    ok = ok && mbar_wait(smem_u32(&bar_tma[c & 1]), (uint32_t)((c >> 1) & 1), status);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+
+    // ---- MMA 2: Acc += P V ; c0 += Phi_K[:, 0:128]^T V ; c1 += Phi_K[:, 128:192]^T V
+    const uint32_t vt = sbase + kOffV + (uint32_t)(c & 1) * 16384u;
+    if (tid == 0) {
+      const uint32_t id = idesc_bf16(128, 64, 0, 1);
+#pragma unroll
+      for (int ks = 0; ks < kC / 16; ++ks) {
+        const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        mma_bf16(tmem + kColAcc, kmaj(sbase + kOffP + aoff), sw128_desc(vt + ks * 2048, 0, 1024), id, 1u);
+      }
+      const uint32_t id0 = idesc_bf16(128, 64, 1, 1);
+      const uint32_t id1 = idesc_bf16(64, 64, 1, 1);
+#pragma unroll
+      for (int ks = 0; ks < kC / 16; ++ks) {
+        mma_bf16(tmem + kColC0, sw128_desc(sbase + kOffPhiK + ks * 2048, 16384, 1024), sw128_desc(vt + ks * 2048, 0, 1024),
+                 id0, 1u);
+        mma_bf16(tmem + kColC1, sw128_desc(sbase + kOffPhiK + 2 * 16384 + ks * 2048, 16384, 1024),
+                 sw128_desc(vt + ks * 2048, 0, 1024), id1, 1u);
+      }
+      mma_commit(smem_u32(&bar_mma));
+    }
+    mma_pending = true;
+    // normaliser update while the MMAs run: z_f += sum_r Phi_K[r][f] (fp32 sums of the bf16 features)
+    float znew0, znew1 = 0.f;
+    {
+      float acc = 0.f;
+      for (int r = 0; r < kC; ++r)
+        acc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + kOffPhiK + sw128_off(r, tid, kC)));
+      znew0 = zsm[tid] + acc;
+      if (tid < kDc - 128) {
+        float acc1 = 0.f;
+        for (int r = 0; r < kC; ++r)
+          acc1 += __bfloat162float(
+              *reinterpret_cast<const __nv_bfloat16*>(sm + kOffPhiK + sw128_off(r, 128 + tid, kC)));
+        znew1 = zsm[128 + tid] + acc1;
+      }
+    }
+    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
+    mma_phase ^= 1;
+    mma_pending = !ok;
+    if (__syncthreads_or(!ok)) break;
+    tc_fence_after();
+    zsm[tid] = znew0;
+    if (tid < kDc - 128) zsm[128 + tid] = znew1;
+
+    // ---- outputs y_r = Acc[r] / (den_r + eps); next bf16 state tile
+    {
+      float y[kDv];
+#pragma unroll
+      for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + kColAcc + c0, *reinterpret_cast<float(*)[16]>(y + c0));
+      tmem_ld_wait();
+      if (valid) {
+        const float inv = 1.f / (den + a.eps);
+        TOut* yrow = reinterpret_cast<TOut*>(a.y) + b * a.y_sb + h * a.y_sh + t * a.y_st;
+#pragma unroll
+        for (int j = 0; j < kDv; ++j) store1(yrow + j, y[j] * inv);
+      }
+      float row[kDv];
+#pragma unroll
+      for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + kColC0 + c0, *reinterpret_cast<float(*)[16]>(row + c0));
+      tmem_ld_wait();
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(tid, 8 * q, 192)) = pack8_bf16(row + 8 * q);
+#pragma unroll
+      for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + kColC1 + c0, *reinterpret_cast<float(*)[16]>(row + c0));
+      tmem_ld_wait();
+      const int f1 = feature_of_lane(tid);
+      if (f1 >= 0) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(f1, 8 * q, 192)) = pack8_bf16(row + 8 * q);
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && c + 2 < nchunks) {
+      issue_tma(c + 2);
+      tma_issued = c + 3;
+    }
+  }
+
+  if (ok) {
+    // ---- final state in the 273-row basis: s_out = s_in + expand(c - c_in)
+    float* s_out = a.s_out + bh * kDfull * kDv;
+    float* z_out = a.z_out + bh * kDfull;
+    auto emit = [&](int j, const float* cur) {
+      if (j >= kDcUsed) return;
+      float prev[kDv];
+      compact_row(j, prev);
+      int r0, r1;
+      float sc;
+      const int n = full_rows_of(j, r0, r1, sc);
+      for (int k = 0; k < n; ++k) {
+        const int r = k == 0 ? r0 : r1;
+#pragma unroll
+        for (int cc = 0; cc < kDv; cc += 4) {
+          float4 o;
+          const float base0 = s_in ? s_in[r * kDv + cc] : 0.f, base1 = s_in ? s_in[r * kDv + cc + 1] : 0.f;
+          const float base2 = s_in ? s_in[r * kDv + cc + 2] : 0.f, base3 = s_in ? s_in[r * kDv + cc + 3] : 0.f;
+          o.x = base0 + (cur[cc] - prev[cc]) * sc;
+          o.y = base1 + (cur[cc + 1] - prev[cc + 1]) * sc;
+          o.z = base2 + (cur[cc + 2] - prev[cc + 2]) * sc;
+          o.w = base3 + (cur[cc + 3] - prev[cc + 3]) * sc;
+          *reinterpret_cast<float4*>(s_out + r * kDv + cc) = o;
+        }
+        const float zb = z_in ? z_in[r] : 0.f;
+        z_out[r] = zb + (zsm[j] - compact_z(j)) * sc;
+      }
+    };
+    // Every 273-basis row belongs to exactly one compact feature, and emit()
+    // reads a row of s_in / z_in before it writes the same row of s_out /
+    // z_out, so the update may run in place (s_out == s_in).
+    float cur0[kDv], cur1[kDv];
+#pragma unroll
+    for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + kColC0 + c0, *reinterpret_cast<float(*)[16]>(cur0 + c0));
+#pragma unroll
+    for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + kColC1 + c0, *reinterpret_cast<float(*)[16]>(cur1 + c0));
+    tmem_ld_wait();
+    emit(tid, cur0);
+    const int f1 = feature_of_lane(tid);
+    if (f1 >= 0) emit(f1, cur1);
+  } else if (tid == 0) {
+    for (int k = c; k < tma_issued; ++k) mbar_wait(smem_u32(&bar_tma[k & 1]), (uint32_t)((k >> 1) & 1), status);
+    if (mma_pending) mbar_wait(smem_u32(&bar_mma), mma_phase, status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+template <typename TOut>
+cudaError_t launch_typed(const TaylorPrefillLaunch& a, unsigned* status, cudaStream_t stream) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorInvalidValue;
+  CUtensorMap mv;
+  const cuuint64_t dims[4] = {(cuuint64_t)kDv, (cuuint64_t)a.N, (cuuint64_t)a.H, (cuuint64_t)a.B};
+  const cuuint64_t strides[3] = {(cuuint64_t)(a.v.st * 2), (cuuint64_t)(a.v.sh * 2), (cuuint64_t)(a.v.sb * 2)};
+  const cuuint32_t box[4] = {64, (cuuint32_t)kC, 1, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  if (fn(&mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(a.v.ptr), dims, strides, box, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(taylor_chunked_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemAlloc);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  taylor_chunked_kernel<TOut><<<(unsigned)(a.B * a.H), kThreads, kSmemAlloc, stream>>>(mv, a, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_taylor_prefill_chunked(const TaylorPrefillLaunch& a, unsigned* status, cudaStream_t stream) {
+  if (a.B * a.H == 0 || a.N == 0) return cudaSuccess;
+  return a.out_bf16 ? launch_typed<__nv_bfloat16>(a, status, stream) : launch_typed<float>(a, status, stream);
+}
+
+}  // namespace la
