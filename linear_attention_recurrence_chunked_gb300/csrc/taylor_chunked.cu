@@ -20,10 +20,14 @@
 // accumulated update expanded back to 273 rows, so the result is exact for
 // any incoming state.
 //
-// One CTA (128 threads, thread r = token r of the chunk) per (batch, head);
-// V tiles arrive by TMA (two stages), q and k by plain loads (the features
-// are formed from them in registers).  Tensor-memory state: c[0:128) as an
-// M = 128 accumulator and c[128:192) as an M = 64 accumulator, 64 columns each.
+// One CTA per (batch, head), two threads per token row of a 128-token chunk
+// (each takes half of the row's columns).  V tiles arrive by TMA (two
+// stages); q and k rows by plain loads, prefetched a chunk ahead, from which
+// the features are formed in registers.  Tensor-memory state: c[0:128) as an
+// M = 128 accumulator and c[128:192) as an M = 64 accumulator, 64 columns
+// each.  The normaliser z and the denominators run through the tensor cores
+// too: a constant tile whose first row is ones gives z += Phi_K^T 1 and the
+// row sums of P, and a tile whose first row is z gives Phi_Q z.
 #include <mutex>
 
 #include "common.cuh"
@@ -40,7 +44,7 @@ constexpr int kDv = 64;      // d_v
 constexpr int kDc = 160;     // compact features, padded (153 used)
 constexpr int kDcUsed = 1 + kF + kF + kF * (kF - 1) / 2;  // 153
 constexpr int kDfull = 1 + kF + kF * kF;                  // 273
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // two threads per token row of the chunk
 constexpr float kInvSqrt2 = 0.70710678118654752f;
 
 // shared memory (offsets from a 1024-byte aligned base)
@@ -50,14 +54,18 @@ constexpr uint32_t kOffPhiQ = kOffQK + 16384;    // bf16 [128 tokens][192] (3 bl
 constexpr uint32_t kOffPhiK = kOffPhiQ + 49152;  // bf16 [128 tokens][192]
 constexpr uint32_t kOffP = kOffPhiK + 49152;     // bf16 [128 r][128 j] (2 blocks of 16 KB)
 constexpr uint32_t kOffCt = kOffP + 32768;       // bf16 c [192 features][64 v] (24 KB)
-constexpr uint32_t kOffZ = kOffCt + 24576;       // fp32 z[160]
-constexpr uint32_t kSmemUsed = kOffZ + kDc * 4;
+constexpr uint32_t kOffOnes = kOffCt + 24576;    // bf16 [16][128 tokens], row 0 = 1 (4 KB)
+constexpr uint32_t kOffZt = kOffOnes + 4096;     // bf16 [16][192 features], row 0 = z (6 KB)
+constexpr uint32_t kSmemUsed = kOffZt + 6144;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
 
 // tensor memory columns
-constexpr uint32_t kColC0 = 0;     // features 0..127  (M = 128: lane = feature), 64 cols
-constexpr uint32_t kColC1 = 64;    // features 128..191 (M = 64 layout), 64 cols
+constexpr uint32_t kColC0 = 0;     // c, features 0..127 (M = 128: lane = feature), 64 cols
+constexpr uint32_t kColC1 = 64;    // c, features 128..191 (M = 64 layout), 64 cols
 constexpr uint32_t kColAcc = 128;  // numerator [token][v], 64 cols
+constexpr uint32_t kColZ0 = 192;   // z, features 0..127, column 0 of 16
+constexpr uint32_t kColZ1 = 208;   // z, features 128..191 (M = 64), column 0 of 16
+constexpr uint32_t kColDen = 224;  // denominator [token], column 0 of 16
 constexpr uint32_t kColQK = 256;   // Q K^T [r][j], 128 cols
 constexpr uint32_t kTmemCols = 512;
 
@@ -103,13 +111,26 @@ __device__ __forceinline__ int full_rows_of(int j, int& r0, int& r1, float& scal
   return 2;
 }
 
-// Tensor-memory lane and column base holding compact feature j (j < 192).
-// Features 0..127: the M = 128 accumulator, lane j.  Features 128..191: the
-// M = 64 accumulator, whose row m lives in lane (m % 16) + 32 (m / 16).
+// Features 0..127 live in the M = 128 accumulators (lane = feature);
+// features 128..191 in the M = 64 accumulators, whose row m sits in lane
+// (m % 16) + 32 (m / 16).  Inverse map for the latter (-1: lane unused).
 __device__ __forceinline__ int feature_of_lane(int lane) {
-  // inverse map for the M = 64 accumulator (-1 for unused lanes)
   const int q = lane >> 5, w = lane & 31;
   return w < 16 ? 128 + q * 16 + w : -1;
+}
+
+template <typename T>
+__device__ __forceinline__ void store_row32(T* dst, const float* v);
+template <>
+__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(dst)[q] = pack8_bf16(v + 8 * q);
+}
+template <>
+__device__ __forceinline__ void store_row32<float>(float* dst, const float* v) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
 template <typename TOut>
@@ -122,14 +143,16 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   __shared__ uint32_t tmem_base_sh;
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int row = tid & (kC - 1);   // token row of the chunk == TMEM lane
+  const int half = tid >> 7;        // which half of a row's columns this thread takes
   const int64_t bh = blockIdx.x;
   const int b = (int)(bh / a.H), h = (int)(bh % a.H);
   const int64_t N = a.N;
   const int nchunks = (int)((N + kC - 1) / kC);
   const uint32_t sbase = smem_u32(sm);
-  float* zsm = reinterpret_cast<float*>(sm + kOffZ);
   const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q.ptr) + b * a.q.sb + h * a.q.sh;
   const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(a.k.ptr) + b * a.k.sb + h * a.k.sh;
+  const int f1 = feature_of_lane(row);  // feature of this lane in the M = 64 accumulators
 
   if (tid == 0) {
     mbar_init(smem_u32(&bar_tma[0]), 1);
@@ -146,7 +169,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);
+  const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 
   auto issue_tma = [&](int c) {
     const uint32_t bar = smem_u32(&bar_tma[c & 1]);
@@ -163,15 +186,19 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     }
   }
 
-  // ---- initial compact state c_in (fp32 in TMEM, bf16 tile) and z
-  // thread t handles feature t of the M=128 accumulator and, if its lane is
-  // one of the M=64 accumulator's, feature feature_of_lane(t).
+  // ---- constant tiles: ones (row 0 = 1) and the z tile (row 0 = z), zeroed first
+  for (int i = tid; i < (4096 + 6144) / 16; i += kThreads)
+    reinterpret_cast<uint4*>(sm + kOffOnes)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  if (tid < kC) *reinterpret_cast<__nv_bfloat16*>(sm + kOffOnes + sw128_off(0, tid, 16)) = __float2bfloat16_rn(1.f);
+
+  // ---- initial compact state c_in (fp32 in TMEM, bf16 tile) and z_in
   const float* s_in = a.s_in ? a.s_in + bh * kDfull * kDv : nullptr;
   const float* z_in = a.z_in ? a.z_in + bh * kDfull : nullptr;
-  auto compact_row = [&](int j, float* row /*64*/) {
-    if (!s_in || j >= kDcUsed) {
+  auto compact_row = [&](int j, float* out /*64*/) {
+    if (!s_in || j < 0 || j >= kDcUsed) {
 #pragma unroll
-      for (int c = 0; c < kDv; ++c) row[c] = 0.f;
+      for (int c = 0; c < kDv; ++c) out[c] = 0.f;
       return;
     }
     int r0, r1;
@@ -184,100 +211,114 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         const float4 y = *reinterpret_cast<const float4*>(s_in + r1 * kDv + c);
         x.x = (x.x + y.x) * sc; x.y = (x.y + y.y) * sc; x.z = (x.z + y.z) * sc; x.w = (x.w + y.w) * sc;
       }
-      row[c] = x.x; row[c + 1] = x.y; row[c + 2] = x.z; row[c + 3] = x.w;
+      out[c] = x.x; out[c + 1] = x.y; out[c + 2] = x.z; out[c + 3] = x.w;
     }
   };
   auto compact_z = [&](int j) -> float {
-    if (!z_in || j >= kDcUsed) return 0.f;
+    if (!z_in || j < 0 || j >= kDcUsed) return 0.f;
     int r0, r1;
     float sc;
     const int n = full_rows_of(j, r0, r1, sc);
     return n == 2 ? (z_in[r0] + z_in[r1]) * sc : z_in[r0];
   };
   {
-    float row[kDv];
-    compact_row(tid, row);
+    // half 0 owns feature `row` (M = 128 accumulators), half 1 owns feature f1 (M = 64)
+    const int j = half == 0 ? row : f1;
+    const uint32_t colc = half == 0 ? kColC0 : kColC1;
+    const uint32_t colz = half == 0 ? kColZ0 : kColZ1;
+    float v[kDv];
+    compact_row(j, v);
 #pragma unroll
-    for (int c = 0; c < kDv; c += 16) tmem_st16(tlane + kColC0 + c, *reinterpret_cast<float(*)[16]>(row + c));
+    for (int c = 0; c < kDv; c += 16) tmem_st16(tlane + colc + c, *reinterpret_cast<float(*)[16]>(v + c));
+    float zz[16];
+    zz[0] = compact_z(j);
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(tid, 8 * q, 192)) = pack8_bf16(row + 8 * q);
-    const int f1 = feature_of_lane(tid);
-    compact_row(f1 < 0 ? kDc : f1, row);
-#pragma unroll
-    for (int c = 0; c < kDv; c += 16) tmem_st16(tlane + kColC1 + c, *reinterpret_cast<float(*)[16]>(row + c));
-    if (f1 >= 0) {
+    for (int i = 1; i < 16; ++i) zz[i] = 0.f;
+    tmem_st16(tlane + colz, zz);
+    if (j >= 0) {
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(f1, 8 * q, 192)) = pack8_bf16(row + 8 * q);
+        *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(j, 8 * q, 192)) = pack8_bf16(v + 8 * q);
+      *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, j, 16)) = __float2bfloat16_rn(zz[0]);
     }
-    zsm[tid] = compact_z(tid);
-    if (tid < kDc - 128) zsm[128 + tid] = compact_z(128 + tid);
     tmem_st_wait();
   }
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
+
+  // this thread's q (half 0) or k (half 1) row for the next chunk, prefetched
+  auto load_row = [&](int c, uint4& r0v, uint4& r1v) {
+    const int64_t t = (int64_t)c * kC + row;
+    if (c < nchunks && t < N) {
+      const uint4* src = reinterpret_cast<const uint4*>((half == 0 ? qp + t * a.q.st : kp + t * a.k.st));
+      r0v = src[0];
+      r1v = src[1];
+    } else {
+      r0v = r1v = make_uint4(0, 0, 0, 0);
+    }
+  };
+  uint4 nx0, nx1;
+  load_row(0, nx0, nx1);
 
   uint32_t mma_phase = 0;
   bool ok = true;
   bool mma_pending = false;
   int c = 0;
   for (; c < nchunks; ++c) {
-    const int64_t t0 = (int64_t)c * kC;
-    const int64_t t = t0 + tid;
+    const int64_t t = (int64_t)c * kC + row;
     const bool valid = t < N;
-    // ---- this token's q, k; compact features into the Phi tiles; q|k into the QK tile
-    float xq[kF], xk[kF];
+    // ---- q|k into the QK tile (half 0: q at cols 0..15, half 1: k at cols 16..31)
+    const uint4 x0 = nx0, x1 = nx1;
+    load_row(c + 1, nx0, nx1);
+    *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(row, 16 * half, kC)) = x0;
+    *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(row, 16 * half + 8, kC)) = x1;
+    __syncthreads();
+    // ---- compact features of q and k for this row; this thread stores columns [80 half, 80 half + 80)
     {
-      if (valid) {
-        const uint4* q4 = reinterpret_cast<const uint4*>(qp + t * a.q.st);
-        const uint4* k4 = reinterpret_cast<const uint4*>(kp + t * a.k.st);
-        uint4 raw[4] = {q4[0], q4[1], k4[0], k4[1]};
-        *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(tid, 0, kC)) = raw[0];
-        *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(tid, 8, kC)) = raw[1];
-        *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(tid, 16, kC)) = raw[2];
-        *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(tid, 24, kC)) = raw[3];
-        const __nv_bfloat16* hq = reinterpret_cast<const __nv_bfloat16*>(&raw[0]);
-        const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(&raw[2]);
+      float xq[kF], xk[kF];
+      const __nv_bfloat16* hq = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 0, kC));
+      const __nv_bfloat16* hq2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 8, kC));
+      const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 16, kC));
+      const __nv_bfloat16* hk2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 24, kC));
 #pragma unroll
-        for (int i = 0; i < kF; ++i) {
-          xq[i] = __bfloat162float(hq[i]);
-          xk[i] = __bfloat162float(hk[i]);
-        }
-      } else {
-        const uint4 zero = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(tid, 8 * q, kC)) = zero;
-#pragma unroll
-        for (int i = 0; i < kF; ++i) xq[i] = xk[i] = 0.f;
+      for (int i = 0; i < 8; ++i) {
+        xq[i] = __bfloat162float(hq[i]);
+        xq[8 + i] = __bfloat162float(hq2[i]);
+        xk[i] = __bfloat162float(hk[i]);
+        xk[8 + i] = __bfloat162float(hk2[i]);
       }
       float f[kDc];
       compact_features(xq, f);
 #pragma unroll
-      for (int q = 0; q < kDc / 8; ++q)
-        *reinterpret_cast<uint4*>(sm + kOffPhiQ + sw128_off(tid, 8 * q, kC)) = pack8_bf16(f + 8 * q);
+      for (int q = 0; q < 10; ++q) {
+        const int col = 80 * half + 8 * q;
+        *reinterpret_cast<uint4*>(sm + kOffPhiQ + sw128_off(row, col, kC)) =
+            pack8_bf16(f + (half == 0 ? 8 * q : 80 + 8 * q));
+      }
       compact_features(xk, f);
       if (!valid) f[0] = 0.f;  // padded tokens contribute nothing to the state
 #pragma unroll
-      for (int q = 0; q < kDc / 8; ++q)
-        *reinterpret_cast<uint4*>(sm + kOffPhiK + sw128_off(tid, 8 * q, kC)) = pack8_bf16(f + 8 * q);
+      for (int q = 0; q < 10; ++q) {
+        const int col = 80 * half + 8 * q;
+        *reinterpret_cast<uint4*>(sm + kOffPhiK + sw128_off(row, col, kC)) =
+            pack8_bf16(f + (half == 0 ? 8 * q : 80 + 8 * q));
+      }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
-    // ---- MMA 1: Q K^T -> QK ; Phi_Q c_{<b} -> Acc
+    // ---- MMA 1: Q K^T -> QK ; Phi_Q c_{<b} -> Acc ; Phi_Q z_{<b} -> Den
     if (tid == 0) {
       mma_bf16(tmem + kColQK, kmaj(sbase + kOffQK), kmaj(sbase + kOffQK + 32), idesc_bf16(128, 128, 0, 0), 0u);
       const uint32_t id = idesc_bf16(128, 64, 0, 1);
+      const uint32_t idz = idesc_bf16(128, 16, 0, 0);
 #pragma unroll
       for (int ks = 0; ks < kDc / 16; ++ks) {
         const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        const uint32_t zoff = (uint32_t)(ks >> 2) * 2048u + (uint32_t)(ks & 3) * 32u;
         mma_bf16(tmem + kColAcc, kmaj(sbase + kOffPhiQ + aoff), sw128_desc(sbase + kOffCt + ks * 2048, 0, 1024), id,
                  ks > 0);
+        mma_bf16(tmem + kColDen, kmaj(sbase + kOffPhiQ + aoff), kmaj(sbase + kOffZt + zoff), idz, ks > 0);
       }
       mma_commit(smem_u32(&bar_mma));
     }
@@ -288,34 +329,23 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // ---- P = tril(1 + A + A^2/2) (row r = tid), row sums; denominator
-    float den;
+    // ---- P = tril(1 + A + A^2/2) for row `row`, columns [64 half, 64 half + 64)
     {
-      float p[kC];
+      float p[64];
 #pragma unroll
-      for (int c0 = 0; c0 < kC; c0 += 16) {
+      for (int c0 = 0; c0 < 64; c0 += 16) {
         float v[16];
-        tmem_ld16(tlane + kColQK + c0, v);
+        tmem_ld16(tlane + kColQK + 64 * half + c0, v);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const float x = v[j];
-          p[c0 + j] = (c0 + j <= tid && valid) ? fmaf(0.5f * x, x, 1.f + x) : 0.f;
+          p[c0 + j] = (64 * half + c0 + j <= row && valid) ? fmaf(0.5f * x, x, 1.f + x) : 0.f;
         }
       }
-      float rs = 0.f;
 #pragma unroll
-      for (int j = 0; j < kC; ++j) rs += p[j];
-#pragma unroll
-      for (int q = 0; q < kC / 8; ++q)
-        *reinterpret_cast<uint4*>(sm + kOffP + sw128_off(tid, 8 * q, kC)) = pack8_bf16(p + 8 * q);
-      // phi_c(q) . z_{<b} in fp32
-      float fq[kDc];
-      compact_features(xq, fq);
-      float dz = 0.f;
-#pragma unroll
-      for (int j = 0; j < kDcUsed; ++j) dz = fmaf(fq[j], zsm[j], dz);
-      den = rs + dz;
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(sm + kOffP + sw128_off(row, 64 * half + 8 * q, kC)) = pack8_bf16(p + 8 * q);
     }
     ok = ok && mbar_wait(smem_u32(&bar_tma[c & 1]), (uint32_t)((c >> 1) & 1), status);
     fence_proxy_async_smem();
@@ -323,77 +353,66 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // ---- MMA 2: Acc += P V ; c0 += Phi_K[:, 0:128]^T V ; c1 += Phi_K[:, 128:192]^T V
+    // ---- MMA 2: Acc += P V, Den += P 1 ; c += Phi_K^T V, z += Phi_K^T 1
     const uint32_t vt = sbase + kOffV + (uint32_t)(c & 1) * 16384u;
     if (tid == 0) {
       const uint32_t id = idesc_bf16(128, 64, 0, 1);
+      const uint32_t idz = idesc_bf16(128, 16, 0, 0);
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks) {
         const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        const uint32_t ooff = (uint32_t)(ks >> 2) * 2048u + (uint32_t)(ks & 3) * 32u;
         mma_bf16(tmem + kColAcc, kmaj(sbase + kOffP + aoff), sw128_desc(vt + ks * 2048, 0, 1024), id, 1u);
+        mma_bf16(tmem + kColDen, kmaj(sbase + kOffP + aoff), kmaj(sbase + kOffOnes + ooff), idz, 1u);
       }
-      const uint32_t id0 = idesc_bf16(128, 64, 1, 1);
-      const uint32_t id1 = idesc_bf16(64, 64, 1, 1);
+      const uint32_t id0 = idesc_bf16(128, 64, 1, 1), id1 = idesc_bf16(64, 64, 1, 1);
+      const uint32_t iz0 = idesc_bf16(128, 16, 1, 0), iz1 = idesc_bf16(64, 16, 1, 0);
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks) {
-        mma_bf16(tmem + kColC0, sw128_desc(sbase + kOffPhiK + ks * 2048, 16384, 1024), sw128_desc(vt + ks * 2048, 0, 1024),
-                 id0, 1u);
-        mma_bf16(tmem + kColC1, sw128_desc(sbase + kOffPhiK + 2 * 16384 + ks * 2048, 16384, 1024),
-                 sw128_desc(vt + ks * 2048, 0, 1024), id1, 1u);
+        const uint64_t a0 = sw128_desc(sbase + kOffPhiK + ks * 2048, 16384, 1024);
+        const uint64_t a1 = sw128_desc(sbase + kOffPhiK + 2 * 16384 + ks * 2048, 16384, 1024);
+        const uint64_t bv = sw128_desc(vt + ks * 2048, 0, 1024);
+        const uint64_t bo = kmaj(sbase + kOffOnes + (uint32_t)(ks >> 2) * 2048u + (uint32_t)(ks & 3) * 32u);
+        mma_bf16(tmem + kColC0, a0, bv, id0, 1u);
+        mma_bf16(tmem + kColC1, a1, bv, id1, 1u);
+        mma_bf16(tmem + kColZ0, a0, bo, iz0, 1u);
+        mma_bf16(tmem + kColZ1, a1, bo, iz1, 1u);
       }
       mma_commit(smem_u32(&bar_mma));
     }
     mma_pending = true;
-    // normaliser update while the MMAs run: z_f += sum_r Phi_K[r][f] (fp32 sums of the bf16 features)
-    float znew0, znew1 = 0.f;
-    {
-      float acc = 0.f;
-      for (int r = 0; r < kC; ++r)
-        acc += __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + kOffPhiK + sw128_off(r, tid, kC)));
-      znew0 = zsm[tid] + acc;
-      if (tid < kDc - 128) {
-        float acc1 = 0.f;
-        for (int r = 0; r < kC; ++r)
-          acc1 += __bfloat162float(
-              *reinterpret_cast<const __nv_bfloat16*>(sm + kOffPhiK + sw128_off(r, 128 + tid, kC)));
-        znew1 = zsm[128 + tid] + acc1;
-      }
-    }
     ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
     mma_phase ^= 1;
     mma_pending = !ok;
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
-    zsm[tid] = znew0;
-    if (tid < kDc - 128) zsm[128 + tid] = znew1;
 
-    // ---- outputs y_r = Acc[r] / (den_r + eps); next bf16 state tile
+    // ---- outputs y = Acc / (Den + eps) (this thread: 32 columns); refresh the bf16 c and z tiles
     {
-      float y[kDv];
-#pragma unroll
-      for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + kColAcc + c0, *reinterpret_cast<float(*)[16]>(y + c0));
+      float d[16], y[32];
+      tmem_ld16(tlane + kColDen, d);
+      tmem_ld16(tlane + kColAcc + 32 * half, *reinterpret_cast<float(*)[16]>(y));
+      tmem_ld16(tlane + kColAcc + 32 * half + 16, *reinterpret_cast<float(*)[16]>(y + 16));
       tmem_ld_wait();
       if (valid) {
-        const float inv = 1.f / (den + a.eps);
-        TOut* yrow = reinterpret_cast<TOut*>(a.y) + b * a.y_sb + h * a.y_sh + t * a.y_st;
+        const float inv = 1.f / (d[0] + a.eps);
 #pragma unroll
-        for (int j = 0; j < kDv; ++j) store1(yrow + j, y[j] * inv);
+        for (int j = 0; j < 32; ++j) y[j] *= inv;
+        TOut* yrow = reinterpret_cast<TOut*>(a.y) + b * a.y_sb + h * a.y_sh + t * a.y_st + 32 * half;
+        store_row32<TOut>(yrow, y);
       }
-      float row[kDv];
+      const int j = half == 0 ? row : f1;
+      float v[kDv], zz[16];
+      const uint32_t colc = half == 0 ? kColC0 : kColC1;
 #pragma unroll
-      for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + kColC0 + c0, *reinterpret_cast<float(*)[16]>(row + c0));
+      for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + colc + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+      tmem_ld16(tlane + (half == 0 ? kColZ0 : kColZ1), zz);
       tmem_ld_wait();
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(tid, 8 * q, 192)) = pack8_bf16(row + 8 * q);
-#pragma unroll
-      for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + kColC1 + c0, *reinterpret_cast<float(*)[16]>(row + c0));
-      tmem_ld_wait();
-      const int f1 = feature_of_lane(tid);
-      if (f1 >= 0) {
+      if (j >= 0) {
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(f1, 8 * q, 192)) = pack8_bf16(row + 8 * q);
+          *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(j, 8 * q, 192)) = pack8_bf16(v + 8 * q);
+        *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, j, 16)) = __float2bfloat16_rn(zz[0]);
       }
     }
     fence_proxy_async_smem();
@@ -407,13 +426,23 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   }
 
   if (ok) {
-    // ---- final state in the 273-row basis: s_out = s_in + expand(c - c_in)
+    // ---- final state in the 273-row basis: s_out = s_in + expand(c - c_in).
+    // Every 273-basis row belongs to exactly one compact feature, and a row of
+    // s_in / z_in is read before the same row of s_out / z_out is written, so
+    // the update may run in place (s_out == s_in).
     float* s_out = a.s_out + bh * kDfull * kDv;
     float* z_out = a.z_out + bh * kDfull;
-    auto emit = [&](int j, const float* cur) {
-      if (j >= kDcUsed) return;
+    const int j = half == 0 ? row : f1;
+    float cur[kDv], zz[16];
+    const uint32_t colc = half == 0 ? kColC0 : kColC1;
+#pragma unroll
+    for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + colc + c0, *reinterpret_cast<float(*)[16]>(cur + c0));
+    tmem_ld16(tlane + (half == 0 ? kColZ0 : kColZ1), zz);
+    tmem_ld_wait();
+    if (j >= 0 && j < kDcUsed) {
       float prev[kDv];
       compact_row(j, prev);
+      const float zprev = compact_z(j);
       int r0, r1;
       float sc;
       const int n = full_rows_of(j, r0, r1, sc);
@@ -421,31 +450,17 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         const int r = k == 0 ? r0 : r1;
 #pragma unroll
         for (int cc = 0; cc < kDv; cc += 4) {
-          float4 o;
-          const float base0 = s_in ? s_in[r * kDv + cc] : 0.f, base1 = s_in ? s_in[r * kDv + cc + 1] : 0.f;
-          const float base2 = s_in ? s_in[r * kDv + cc + 2] : 0.f, base3 = s_in ? s_in[r * kDv + cc + 3] : 0.f;
-          o.x = base0 + (cur[cc] - prev[cc]) * sc;
-          o.y = base1 + (cur[cc + 1] - prev[cc + 1]) * sc;
-          o.z = base2 + (cur[cc + 2] - prev[cc + 2]) * sc;
-          o.w = base3 + (cur[cc + 3] - prev[cc + 3]) * sc;
-          *reinterpret_cast<float4*>(s_out + r * kDv + cc) = o;
+          float4 base = s_in ? *reinterpret_cast<const float4*>(s_in + r * kDv + cc) : make_float4(0.f, 0.f, 0.f, 0.f);
+          base.x += (cur[cc] - prev[cc]) * sc;
+          base.y += (cur[cc + 1] - prev[cc + 1]) * sc;
+          base.z += (cur[cc + 2] - prev[cc + 2]) * sc;
+          base.w += (cur[cc + 3] - prev[cc + 3]) * sc;
+          *reinterpret_cast<float4*>(s_out + r * kDv + cc) = base;
         }
         const float zb = z_in ? z_in[r] : 0.f;
-        z_out[r] = zb + (zsm[j] - compact_z(j)) * sc;
+        z_out[r] = zb + (zz[0] - zprev) * sc;
       }
-    };
-    // Every 273-basis row belongs to exactly one compact feature, and emit()
-    // reads a row of s_in / z_in before it writes the same row of s_out /
-    // z_out, so the update may run in place (s_out == s_in).
-    float cur0[kDv], cur1[kDv];
-#pragma unroll
-    for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + kColC0 + c0, *reinterpret_cast<float(*)[16]>(cur0 + c0));
-#pragma unroll
-    for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + kColC1 + c0, *reinterpret_cast<float(*)[16]>(cur1 + c0));
-    tmem_ld_wait();
-    emit(tid, cur0);
-    const int f1 = feature_of_lane(tid);
-    if (f1 >= 0) emit(f1, cur1);
+    }
   } else if (tid == 0) {
     for (int k = c; k < tma_issued; ++k) mbar_wait(smem_u32(&bar_tma[k & 1]), (uint32_t)((k >> 1) & 1), status);
     if (mma_pending) mbar_wait(smem_u32(&bar_mma), mma_phase, status);
