@@ -21,13 +21,15 @@
 // any incoming state.
 //
 // One CTA per (batch, head), two threads per token row of a 128-token chunk
-// (each takes half of the row's columns).  V tiles arrive by TMA (two
-// stages); q and k rows by plain loads, prefetched a chunk ahead, from which
-// the features are formed in registers.  Tensor-memory state: c[0:128) as an
-// M = 128 accumulator and c[128:192) as an M = 64 accumulator, 64 columns
-// each.  The normaliser z and the denominators run through the tensor cores
-// too: a constant tile whose first row is ones gives z += Phi_K^T 1 and the
-// row sums of P, and a tile whose first row is z gives Phi_Q z.
+// (each takes half of the row's columns and features).  V tiles arrive by TMA
+// (two stages); q and k rows by cp.async, issued a chunk ahead, from which the
+// features are formed in registers.  Tensor-memory state: [c | z] for
+// features 0..127 as an M = 128 accumulator and for features 128..191 as an
+// M = 64 accumulator.  The normaliser runs through the tensor cores with the
+// state: the B operand is [V | 1] (a constant block whose first column is
+// ones), so z += Phi_K^T 1 lands in column 64 of the state accumulators and
+// the row sums of P in column 64 of the numerator; a tile whose first row
+// is z supplies Phi_Q z.
 #include <mutex>
 
 #include "common.cuh"
@@ -48,71 +50,87 @@ constexpr int kThreads = 256;  // two threads per token row of the chunk
 constexpr float kInvSqrt2 = 0.70710678118654752f;
 
 // shared memory (offsets from a 1024-byte aligned base)
-constexpr uint32_t kOffV = 0;                    // 2 stages x bf16 V [128 tokens][64] (16 KB each)
-constexpr uint32_t kOffQK = 32768;               // bf16 [128 tokens][64]: cols 0..15 q, 16..31 k
-constexpr uint32_t kOffPhiQ = kOffQK + 16384;    // bf16 [128 tokens][192] (3 blocks of 16 KB)
-constexpr uint32_t kOffPhiK = kOffPhiQ + 49152;  // bf16 [128 tokens][192]
-constexpr uint32_t kOffP = kOffPhiK + 49152;     // bf16 [128 r][128 j] (2 blocks of 16 KB)
-constexpr uint32_t kOffCt = kOffP + 32768;       // bf16 c [192 features][64 v] (24 KB)
-constexpr uint32_t kOffOnes = kOffCt + 24576;    // bf16 [16][128 tokens], row 0 = 1 (4 KB)
-constexpr uint32_t kOffZt = kOffOnes + 4096;     // bf16 [16][192 features], row 0 = z (6 KB)
+constexpr uint32_t kOffV = 0;                      // 2 stages x bf16 V [128 tokens][64] (16 KB each)
+constexpr uint32_t kOffOnes = 32768;               // bf16 [128 tokens][64], column 0 = 1: the "1" of [V | 1]
+constexpr uint32_t kOffQK = kOffOnes + 16384;      // bf16 [128 tokens][64]: cols 0..15 q, 16..31 k
+constexpr uint32_t kOffPhiQ = kOffQK + 16384;      // bf16 [128 tokens][192] (3 blocks of 16 KB)
+constexpr uint32_t kOffPhiK = kOffPhiQ + 49152;    // bf16 [128 tokens][192]
+constexpr uint32_t kOffP = kOffPhiK + 49152;       // bf16 [128 r][128 j] (2 blocks of 16 KB)
+constexpr uint32_t kOffCt = kOffP + 32768;         // bf16 c [192 features][64 v] (24 KB)
+constexpr uint32_t kOffZt = kOffCt + 24576;        // bf16 [16][192 features], row 0 = z (6 KB)
 constexpr uint32_t kSmemUsed = kOffZt + 6144;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
+static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
-// tensor memory columns
-constexpr uint32_t kColC0 = 0;     // c, features 0..127 (M = 128: lane = feature), 64 cols
-constexpr uint32_t kColC1 = 64;    // c, features 128..191 (M = 64 layout), 64 cols
-constexpr uint32_t kColAcc = 128;  // numerator [token][v], 64 cols
-constexpr uint32_t kColZ0 = 192;   // z, features 0..127, column 0 of 16
-constexpr uint32_t kColZ1 = 208;   // z, features 128..191 (M = 64), column 0 of 16
-constexpr uint32_t kColDen = 224;  // denominator [token], column 0 of 16
-constexpr uint32_t kColQK = 256;   // Q K^T [r][j], 128 cols
+// tensor memory columns; N = 80 accumulators: columns 0..63 = v, column 64 = the "1" column
+constexpr uint32_t kColC0 = 0;     // [c | z], features 0..127 (M = 128: lane = feature)
+constexpr uint32_t kColC1 = 96;    // [c | z], features 128..191 (M = 64 layout)
+constexpr uint32_t kColAcc = 192;  // [numerator | denominator] per token
+constexpr uint32_t kColQK = 320;   // Q K^T [r][j], 128 cols
 constexpr uint32_t kTmemCols = 512;
 
 __device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sw128_desc(addr, 0, 1024); }
 
-// Compact feature j of x (j < 160): 1 | x_a | x_a^2/sqrt2 | x_a x_b (a<b, row-major) | 0.
-// Pair index p in 0..119 enumerates (0,1),(0,2),...,(0,15),(1,2),...,(14,15).
-__device__ __forceinline__ void compact_features(const float* x, float* f) {
-  f[0] = 1.f;
-#pragma unroll
-  for (int a = 0; a < kF; ++a) f[1 + a] = x[a];
-#pragma unroll
-  for (int a = 0; a < kF; ++a) f[1 + kF + a] = x[a] * x[a] * kInvSqrt2;
-  int p = 1 + 2 * kF;
-#pragma unroll
-  for (int a = 0; a < kF; ++a)
-#pragma unroll
-    for (int b = a + 1; b < kF; ++b) f[p++] = x[a] * x[b];
-#pragma unroll
-  for (int j = kDcUsed; j < kDc; ++j) f[j] = 0.f;
+// Compact feature basis: j = 0: 1 | 1..16: x_a | 17..32: x_a^2/sqrt2 |
+// 33..152: x_a x_b for a < b in the order (0,1),(0,2),...,(0,15),(1,2),...,(14,15) | 153..159: 0.
+__host__ __device__ constexpr int feat_kind(int j) { return j == 0 ? 0 : (j <= kF ? 1 : (j <= 2 * kF ? 2 : (j < kDcUsed ? 3 : 4))); }
+__host__ __device__ constexpr int feat_a(int j) {
+  if (j <= kF) return j - 1;
+  if (j <= 2 * kF) return j - 1 - kF;
+  int p = j - (1 + 2 * kF), a = 0;
+  while (p >= kF - 1 - a) { p -= kF - 1 - a; ++a; }
+  return a;
 }
-
-// (a, b) of compact pair feature j (33 <= j < 153), computed by counting.
-__device__ __forceinline__ void pair_of(int j, int& a, int& b) {
-  int p = j - (1 + 2 * kF);
-  a = 0;
-  while (p >= kF - 1 - a) {
-    p -= kF - 1 - a;
-    ++a;
-  }
-  b = a + 1 + p;
+__host__ __device__ constexpr int feat_b(int j) {
+  int p = j - (1 + 2 * kF), a = 0;
+  while (p >= kF - 1 - a) { p -= kF - 1 - a; ++a; }
+  return a + 1 + p;
+}
+template <int J>
+__device__ __forceinline__ float feature(const float* x) {
+  constexpr int kind = feat_kind(J);
+  if constexpr (kind == 0) return 1.f;
+  else if constexpr (kind == 1) return x[feat_a(J)];
+  else if constexpr (kind == 2) return x[feat_a(J)] * x[feat_a(J)] * kInvSqrt2;
+  else if constexpr (kind == 3) return x[feat_a(J)] * x[feat_b(J)];
+  else return 0.f;
+}
+// Features [BEGIN, BEGIN + 8) of x as one 16-byte bf16 vector.
+template <int BEGIN>
+__device__ __forceinline__ uint4 feature8(const float* x) {
+  const float f[8] = {feature<BEGIN>(x), feature<BEGIN + 1>(x), feature<BEGIN + 2>(x), feature<BEGIN + 3>(x),
+                      feature<BEGIN + 4>(x), feature<BEGIN + 5>(x), feature<BEGIN + 6>(x), feature<BEGIN + 7>(x)};
+  return pack8_bf16(f);
+}
+// Row `row` of a [128][192] feature tile, features [BEGIN, BEGIN + 80).
+template <int BEGIN>
+__device__ __forceinline__ void store_features80(uint8_t* tile, int row, const float* x) {
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 0, kC)) = feature8<BEGIN + 0>(x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 8, kC)) = feature8<BEGIN + 8>(x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 16, kC)) = feature8<BEGIN + 16>(x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 24, kC)) = feature8<BEGIN + 24>(x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 32, kC)) = feature8<BEGIN + 32>(x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 40, kC)) = feature8<BEGIN + 40>(x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 48, kC)) = feature8<BEGIN + 48>(x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 56, kC)) = feature8<BEGIN + 56>(x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 64, kC)) = feature8<BEGIN + 64>(x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 72, kC)) = feature8<BEGIN + 72>(x);
 }
 
 // Full-basis state rows of compact feature j; returns how many (1 or 2).
 __device__ __forceinline__ int full_rows_of(int j, int& r0, int& r1, float& scale) {
-  if (j < 1 + kF) { r0 = j; r1 = -1; scale = 1.f; return 1; }
-  if (j < 1 + 2 * kF) { const int a = j - 1 - kF; r0 = 1 + kF + a * kF + a; r1 = -1; scale = 1.f; return 1; }
-  int a, b;
-  pair_of(j, a, b);
+  const int kind = feat_kind(j);
+  if (kind == 0 || kind == 1) { r0 = j; r1 = -1; scale = 1.f; return 1; }
+  if (kind == 2) { const int a = feat_a(j); r0 = 1 + kF + a * kF + a; r1 = -1; scale = 1.f; return 1; }
+  const int a = feat_a(j), b = feat_b(j);
   r0 = 1 + kF + a * kF + b;
   r1 = 1 + kF + b * kF + a;
   scale = kInvSqrt2;
   return 2;
 }
 
-// Features 0..127 live in the M = 128 accumulators (lane = feature);
-// features 128..191 in the M = 64 accumulators, whose row m sits in lane
+// Features 0..127 live in the M = 128 accumulator (lane = feature);
+// features 128..191 in the M = 64 accumulator, whose row m sits in lane
 // (m % 16) + 32 (m / 16).  Inverse map for the latter (-1: lane unused).
 __device__ __forceinline__ int feature_of_lane(int lane) {
   const int q = lane >> 5, w = lane & 31;
@@ -152,7 +170,9 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   const uint32_t sbase = smem_u32(sm);
   const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q.ptr) + b * a.q.sb + h * a.q.sh;
   const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(a.k.ptr) + b * a.k.sb + h * a.k.sh;
-  const int f1 = feature_of_lane(row);  // feature of this lane in the M = 64 accumulators
+  const int f1 = feature_of_lane(row);  // feature of this lane in the M = 64 accumulator
+  const int my_feature = half == 0 ? row : f1;
+  const uint32_t my_colc = half == 0 ? kColC0 : kColC1;
 
   if (tid == 0) {
     mbar_init(smem_u32(&bar_tma[0]), 1);
@@ -185,12 +205,22 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       tma_issued = 2;
     }
   }
+  // q (half 0) or k (half 1) row of chunk c into the QK tile, asynchronously
+  auto fetch_qk = [&](int cc) {
+    const int64_t t = (int64_t)cc * kC + row;
+    const bool in = cc < nchunks && t < N;
+    const __nv_bfloat16* src = half == 0 ? qp + (in ? t : 0) * a.q.st : kp + (in ? t : 0) * a.k.st;
+    cp_async16(sbase + kOffQK + sw128_off(row, 16 * half, kC), src, in ? 16u : 0u);
+    cp_async16(sbase + kOffQK + sw128_off(row, 16 * half + 8, kC), src + 8, in ? 16u : 0u);
+    cp_async_commit();
+  };
+  fetch_qk(0);
 
-  // ---- constant tiles: ones (row 0 = 1) and the z tile (row 0 = z), zeroed first
-  for (int i = tid; i < (4096 + 6144) / 16; i += kThreads)
-    reinterpret_cast<uint4*>(sm + kOffOnes)[i] = make_uint4(0, 0, 0, 0);
+  // ---- constant tiles: [.. | 1] block (column 0 = 1) and the z tile, zeroed first
+  for (int i = tid; i < 16384 / 16; i += kThreads) reinterpret_cast<uint4*>(sm + kOffOnes)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < 6144 / 16; i += kThreads) reinterpret_cast<uint4*>(sm + kOffZt)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  if (tid < kC) *reinterpret_cast<__nv_bfloat16*>(sm + kOffOnes + sw128_off(0, tid, 16)) = __float2bfloat16_rn(1.f);
+  if (tid < kC) *reinterpret_cast<__nv_bfloat16*>(sm + kOffOnes + sw128_off(tid, 0, kC)) = __float2bfloat16_rn(1.f);
 
   // ---- initial compact state c_in (fp32 in TMEM, bf16 tile) and z_in
   const float* s_in = a.s_in ? a.s_in + bh * kDfull * kDv : nullptr;
@@ -222,41 +252,21 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     return n == 2 ? (z_in[r0] + z_in[r1]) * sc : z_in[r0];
   };
   {
-    // half 0 owns feature `row` (M = 128 accumulators), half 1 owns feature f1 (M = 64)
-    const int j = half == 0 ? row : f1;
-    const uint32_t colc = half == 0 ? kColC0 : kColC1;
-    const uint32_t colz = half == 0 ? kColZ0 : kColZ1;
-    float v[kDv];
-    compact_row(j, v);
+    float v[kDv + 16];
+    compact_row(my_feature, v);
+    v[kDv] = compact_z(my_feature);
 #pragma unroll
-    for (int c = 0; c < kDv; c += 16) tmem_st16(tlane + colc + c, *reinterpret_cast<float(*)[16]>(v + c));
-    float zz[16];
-    zz[0] = compact_z(j);
+    for (int i = 1; i < 16; ++i) v[kDv + i] = 0.f;
 #pragma unroll
-    for (int i = 1; i < 16; ++i) zz[i] = 0.f;
-    tmem_st16(tlane + colz, zz);
-    if (j >= 0) {
+    for (int c = 0; c < kDv + 16; c += 16) tmem_st16(tlane + my_colc + c, *reinterpret_cast<float(*)[16]>(v + c));
+    if (my_feature >= 0) {
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(j, 8 * q, 192)) = pack8_bf16(v + 8 * q);
-      *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, j, 16)) = __float2bfloat16_rn(zz[0]);
+        *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(my_feature, 8 * q, 192)) = pack8_bf16(v + 8 * q);
+      *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(v[kDv]);
     }
     tmem_st_wait();
   }
-
-  // this thread's q (half 0) or k (half 1) row for the next chunk, prefetched
-  auto load_row = [&](int c, uint4& r0v, uint4& r1v) {
-    const int64_t t = (int64_t)c * kC + row;
-    if (c < nchunks && t < N) {
-      const uint4* src = reinterpret_cast<const uint4*>((half == 0 ? qp + t * a.q.st : kp + t * a.k.st));
-      r0v = src[0];
-      r1v = src[1];
-    } else {
-      r0v = r1v = make_uint4(0, 0, 0, 0);
-    }
-  };
-  uint4 nx0, nx1;
-  load_row(0, nx0, nx1);
 
   uint32_t mma_phase = 0;
   bool ok = true;
@@ -265,13 +275,9 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   for (; c < nchunks; ++c) {
     const int64_t t = (int64_t)c * kC + row;
     const bool valid = t < N;
-    // ---- q|k into the QK tile (half 0: q at cols 0..15, half 1: k at cols 16..31)
-    const uint4 x0 = nx0, x1 = nx1;
-    load_row(c + 1, nx0, nx1);
-    *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(row, 16 * half, kC)) = x0;
-    *reinterpret_cast<uint4*>(sm + kOffQK + sw128_off(row, 16 * half + 8, kC)) = x1;
+    cp_async_wait_all();
     __syncthreads();
-    // ---- compact features of q and k for this row; this thread stores columns [80 half, 80 half + 80)
+    // ---- compact features of this row's q and k; this thread writes features [80 half, 80 half + 80)
     {
       float xq[kF], xk[kF];
       const __nv_bfloat16* hq = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 0, kC));
@@ -285,21 +291,14 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         xk[i] = __bfloat162float(hk[i]);
         xk[8 + i] = __bfloat162float(hk2[i]);
       }
-      float f[kDc];
-      compact_features(xq, f);
-#pragma unroll
-      for (int q = 0; q < 10; ++q) {
-        const int col = 80 * half + 8 * q;
-        *reinterpret_cast<uint4*>(sm + kOffPhiQ + sw128_off(row, col, kC)) =
-            pack8_bf16(f + (half == 0 ? 8 * q : 80 + 8 * q));
-      }
-      compact_features(xk, f);
-      if (!valid) f[0] = 0.f;  // padded tokens contribute nothing to the state
-#pragma unroll
-      for (int q = 0; q < 10; ++q) {
-        const int col = 80 * half + 8 * q;
-        *reinterpret_cast<uint4*>(sm + kOffPhiK + sw128_off(row, col, kC)) =
-            pack8_bf16(f + (half == 0 ? 8 * q : 80 + 8 * q));
+      if (half == 0) {
+        store_features80<0>(sm + kOffPhiQ, row, xq);
+        store_features80<0>(sm + kOffPhiK, row, xk);
+        // a padded token must not add its constant feature to the state
+        if (!valid) *reinterpret_cast<__nv_bfloat16*>(sm + kOffPhiK + sw128_off(row, 0, kC)) = __float2bfloat16_rn(0.f);
+      } else {
+        store_features80<80>(sm + kOffPhiQ, row, xq);
+        store_features80<80>(sm + kOffPhiK, row, xk);
       }
     }
     fence_proxy_async_smem();
@@ -307,7 +306,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     __syncthreads();
     tc_fence_after();
 
-    // ---- MMA 1: Q K^T -> QK ; Phi_Q c_{<b} -> Acc ; Phi_Q z_{<b} -> Den
+    // ---- MMA 1: Q K^T -> QK ; Phi_Q c_{<b} -> Acc[0:64) ; Phi_Q z_{<b} -> Acc[64:80)
     if (tid == 0) {
       mma_bf16(tmem + kColQK, kmaj(sbase + kOffQK), kmaj(sbase + kOffQK + 32), idesc_bf16(128, 128, 0, 0), 0u);
       const uint32_t id = idesc_bf16(128, 64, 0, 1);
@@ -318,7 +317,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         const uint32_t zoff = (uint32_t)(ks >> 2) * 2048u + (uint32_t)(ks & 3) * 32u;
         mma_bf16(tmem + kColAcc, kmaj(sbase + kOffPhiQ + aoff), sw128_desc(sbase + kOffCt + ks * 2048, 0, 1024), id,
                  ks > 0);
-        mma_bf16(tmem + kColDen, kmaj(sbase + kOffPhiQ + aoff), kmaj(sbase + kOffZt + zoff), idz, ks > 0);
+        mma_bf16(tmem + kColAcc + 64, kmaj(sbase + kOffPhiQ + aoff), kmaj(sbase + kOffZt + zoff), idz, ks > 0);
       }
       mma_commit(smem_u32(&bar_mma));
     }
@@ -328,20 +327,18 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     mma_pending = !ok;
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
+    fetch_qk(c + 1);  // the QK tile is free again: next chunk's rows load behind this one
 
     // ---- P = tril(1 + A + A^2/2) for row `row`, columns [64 half, 64 half + 64)
     {
       float p[64];
 #pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) {
-        float v[16];
-        tmem_ld16(tlane + kColQK + 64 * half + c0, v);
-        tmem_ld_wait();
+      for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tlane + kColQK + 64 * half + c0, *reinterpret_cast<float(*)[16]>(p + c0));
+      tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float x = v[j];
-          p[c0 + j] = (64 * half + c0 + j <= row && valid) ? fmaf(0.5f * x, x, 1.f + x) : 0.f;
-        }
+      for (int j = 0; j < 64; ++j) {
+        const float x = p[j];
+        p[j] = (64 * half + j <= row && valid) ? fmaf(0.5f * x, x, 1.f + x) : 0.f;
       }
 #pragma unroll
       for (int q = 0; q < 8; ++q)
@@ -353,30 +350,19 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // ---- MMA 2: Acc += P V, Den += P 1 ; c += Phi_K^T V, z += Phi_K^T 1
+    // ---- MMA 2: Acc += P [V | 1] ; [c | z] += Phi_K^T [V | 1]
     const uint32_t vt = sbase + kOffV + (uint32_t)(c & 1) * 16384u;
+    const uint32_t lbo = sbase + kOffOnes - vt;  // distance from the V block to the [.. | 1] block
     if (tid == 0) {
-      const uint32_t id = idesc_bf16(128, 64, 0, 1);
-      const uint32_t idz = idesc_bf16(128, 16, 0, 0);
+      const uint32_t id = idesc_bf16(128, 80, 0, 1);
+      const uint32_t id0 = idesc_bf16(128, 80, 1, 1), id1 = idesc_bf16(64, 80, 1, 1);
 #pragma unroll
       for (int ks = 0; ks < kC / 16; ++ks) {
         const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-        const uint32_t ooff = (uint32_t)(ks >> 2) * 2048u + (uint32_t)(ks & 3) * 32u;
-        mma_bf16(tmem + kColAcc, kmaj(sbase + kOffP + aoff), sw128_desc(vt + ks * 2048, 0, 1024), id, 1u);
-        mma_bf16(tmem + kColDen, kmaj(sbase + kOffP + aoff), kmaj(sbase + kOffOnes + ooff), idz, 1u);
-      }
-      const uint32_t id0 = idesc_bf16(128, 64, 1, 1), id1 = idesc_bf16(64, 64, 1, 1);
-      const uint32_t iz0 = idesc_bf16(128, 16, 1, 0), iz1 = idesc_bf16(64, 16, 1, 0);
-#pragma unroll
-      for (int ks = 0; ks < kC / 16; ++ks) {
-        const uint64_t a0 = sw128_desc(sbase + kOffPhiK + ks * 2048, 16384, 1024);
-        const uint64_t a1 = sw128_desc(sbase + kOffPhiK + 2 * 16384 + ks * 2048, 16384, 1024);
-        const uint64_t bv = sw128_desc(vt + ks * 2048, 0, 1024);
-        const uint64_t bo = kmaj(sbase + kOffOnes + (uint32_t)(ks >> 2) * 2048u + (uint32_t)(ks & 3) * 32u);
-        mma_bf16(tmem + kColC0, a0, bv, id0, 1u);
-        mma_bf16(tmem + kColC1, a1, bv, id1, 1u);
-        mma_bf16(tmem + kColZ0, a0, bo, iz0, 1u);
-        mma_bf16(tmem + kColZ1, a1, bo, iz1, 1u);
+        const uint64_t bv = sw128_desc(vt + ks * 2048, lbo, 1024);
+        mma_bf16(tmem + kColAcc, kmaj(sbase + kOffP + aoff), bv, id, 1u);
+        mma_bf16(tmem + kColC0, sw128_desc(sbase + kOffPhiK + ks * 2048, 16384, 1024), bv, id0, 1u);
+        mma_bf16(tmem + kColC1, sw128_desc(sbase + kOffPhiK + 2 * 16384 + ks * 2048, 16384, 1024), bv, id1, 1u);
       }
       mma_commit(smem_u32(&bar_mma));
     }
@@ -387,12 +373,15 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // ---- outputs y = Acc / (Den + eps) (this thread: 32 columns); refresh the bf16 c and z tiles
+    // ---- outputs y = Acc / (Acc[64] + eps) (this thread: 32 columns); refresh the bf16 c and z tiles
     {
-      float d[16], y[32];
-      tmem_ld16(tlane + kColDen, d);
+      float d[16], y[32], v[kDv], zz[16];
+      tmem_ld16(tlane + kColAcc + 64, d);
       tmem_ld16(tlane + kColAcc + 32 * half, *reinterpret_cast<float(*)[16]>(y));
       tmem_ld16(tlane + kColAcc + 32 * half + 16, *reinterpret_cast<float(*)[16]>(y + 16));
+#pragma unroll
+      for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + my_colc + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+      tmem_ld16(tlane + my_colc + kDv, zz);
       tmem_ld_wait();
       if (valid) {
         const float inv = 1.f / (d[0] + a.eps);
@@ -401,18 +390,11 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         TOut* yrow = reinterpret_cast<TOut*>(a.y) + b * a.y_sb + h * a.y_sh + t * a.y_st + 32 * half;
         store_row32<TOut>(yrow, y);
       }
-      const int j = half == 0 ? row : f1;
-      float v[kDv], zz[16];
-      const uint32_t colc = half == 0 ? kColC0 : kColC1;
-#pragma unroll
-      for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + colc + c0, *reinterpret_cast<float(*)[16]>(v + c0));
-      tmem_ld16(tlane + (half == 0 ? kColZ0 : kColZ1), zz);
-      tmem_ld_wait();
-      if (j >= 0) {
+      if (my_feature >= 0) {
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(j, 8 * q, 192)) = pack8_bf16(v + 8 * q);
-        *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, j, 16)) = __float2bfloat16_rn(zz[0]);
+          *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(my_feature, 8 * q, 192)) = pack8_bf16(v + 8 * q);
+        *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(zz[0]);
       }
     }
     fence_proxy_async_smem();
@@ -424,6 +406,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       tma_issued = c + 3;
     }
   }
+  cp_async_wait_all();
 
   if (ok) {
     // ---- final state in the 273-row basis: s_out = s_in + expand(c - c_in).
@@ -432,12 +415,11 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     // the update may run in place (s_out == s_in).
     float* s_out = a.s_out + bh * kDfull * kDv;
     float* z_out = a.z_out + bh * kDfull;
-    const int j = half == 0 ? row : f1;
+    const int j = my_feature;
     float cur[kDv], zz[16];
-    const uint32_t colc = half == 0 ? kColC0 : kColC1;
 #pragma unroll
-    for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + colc + c0, *reinterpret_cast<float(*)[16]>(cur + c0));
-    tmem_ld16(tlane + (half == 0 ? kColZ0 : kColZ1), zz);
+    for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + my_colc + c0, *reinterpret_cast<float(*)[16]>(cur + c0));
+    tmem_ld16(tlane + my_colc + kDv, zz);
     tmem_ld_wait();
     if (j >= 0 && j < kDcUsed) {
       float prev[kDv];

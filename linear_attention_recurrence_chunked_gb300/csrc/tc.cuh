@@ -92,6 +92,13 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* map, int c
       : "memory");
 }
 
+// 16-byte asynchronous global->shared copy (zero-filled when src_bytes is 0).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMEM
 // Allocation is warp-wide; the base address is written to shared memory.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
