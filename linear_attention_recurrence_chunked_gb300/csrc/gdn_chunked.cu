@@ -17,9 +17,10 @@
 // products W^T, U~^T, (S0 W^T), (S0 Q^T), (P U)^T), except [K;Q] K^T where
 // the K and Q tiles of the chunk are stacked into one 128-row operand.
 // Tiles arrive by TMA into a two-stage ring; the next chunk's tiles load
-// while the current one is processed.  T is inverted on the CUDA cores in
-// 16x16 blocks: diagonal blocks by forward substitution, the blocks below
-// them by block forward substitution.
+// while the current one is processed.  T is inverted on the CUDA cores by
+// doubling: 16x16 diagonal blocks by forward substitution, then 32x32 and
+// 64x64 blocks from [[A,0],[C,B]]^-1 = [[A^-1,0],[-B^-1 C A^-1, B^-1]].
+// Two threads share each tensor-memory lane and split its columns.
 #include <mutex>
 
 #include "common.cuh"
@@ -32,7 +33,7 @@ using namespace tc;
 
 constexpr int kC = 64;        // tokens per chunk
 constexpr int kD = 128;       // d_k = d_v
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;  // two threads per tensor-memory lane, splitting its columns
 
 // shared memory map, offsets from a 1024-byte aligned base
 constexpr uint32_t kStageBytes = 49152;   // [K;Q] tile [128][128] bf16 (32 KB) + V [64][128] (16 KB)
@@ -46,14 +47,15 @@ constexpr uint32_t kOffPo = kOffT2 + 8192;        // bf16 tril(Gamma) . Q K^T [6
 constexpr uint32_t kOffU = kOffPo + 8192;         // bf16 U^T [128 i][64 j]
 constexpr uint32_t kOffUD = kOffU + 16384;        // bf16 U^T diag(gamma_C/gamma) [128 i][64 j]
 constexpr uint32_t kOffL = kOffU;                 // fp32 L [64][65], lives only before U is formed
-constexpr uint32_t kOffZ = kOffL + 64 * 65 * 4;   // fp32 3 x [16][16] block products (same lifetime)
-constexpr uint32_t kOffGate = kOffUD + 16384;     // fp32 g[64], beta[64], gamma[64]
-constexpr uint32_t kSmemUsed = kOffGate + 768;
+constexpr uint32_t kOffZ = kOffL + 64 * 65 * 4;   // fp32 block products for the inversion (4 KB, same lifetime)
+constexpr uint32_t kOffGate = kOffUD + 16384;     // fp32 g, beta, gamma, 1/gamma [64] each
+constexpr uint32_t kSmemUsed = kOffGate + 1024;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
 constexpr int kLStride = 65;
 constexpr int kTStride = 64;                      // fp32 T [64][64] reuses the W tile space
-static_assert(kOffZ + 3 * 256 * 4 <= kOffGate, "L/Z scratch overlaps the gates");
+static_assert(kOffZ + 1024 * 4 <= kOffGate, "L/Z scratch overlaps the gates");
 static_assert(64 * kTStride * 4 <= 16384, "T scratch exceeds the W tile");
+static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 // tensor-memory columns (fp32, lane = row of the M = 128 accumulator)
 constexpr uint32_t kColS = 0;     // S [i][k], 128 columns
@@ -67,20 +69,11 @@ constexpr uint32_t kTmemCols = 512;
 
 __device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sw128_desc(addr, 0, 1024); }
 
-__device__ __forceinline__ void ld64(uint32_t taddr, float* v) {
-  float a[16], b[16], c[16], d[16];
-  tmem_ld16(taddr, a);
-  tmem_ld16(taddr + 16, b);
-  tmem_ld16(taddr + 32, c);
-  tmem_ld16(taddr + 48, d);
+// 32 consecutive TMEM columns of this thread's lane, one wait.
+__device__ __forceinline__ void ld32(uint32_t taddr, float* v) {
+  tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(v));
+  tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(v + 16));
   tmem_ld_wait();
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    v[i] = a[i];
-    v[16 + i] = b[i];
-    v[32 + i] = c[i];
-    v[48 + i] = d[i];
-  }
 }
 
 __device__ __forceinline__ void st_bf16(uint8_t* p, float x) {
@@ -99,14 +92,19 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   __shared__ float warp0_total;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int row = tid & 127;   // tensor-memory lane owned with the partner thread
+  const int half = tid >> 7;   // which half of the lane's columns
   const int64_t bh = blockIdx.x;
   const int b = (int)(bh / a.H), h = (int)(bh % a.H);
   const int64_t N = a.N;
   const int nchunks = (int)((N + kC - 1) / kC);
-  float* gsm = reinterpret_cast<float*>(sm + kOffGate);
-  float* bsm = gsm + kC;
-  float* gam = gsm + 2 * kC;
+  float* gsm = reinterpret_cast<float*>(sm + kOffGate);  // g_r = sum_{j<=r} log alpha_j
+  float* bsm = gsm + kC;                                  // beta_r
+  float* gam = gsm + 2 * kC;                              // gamma_r = e^{g_r}
+  float* gin = gsm + 3 * kC;                              // 1 / gamma_r
   float* Lsm = reinterpret_cast<float*>(sm + kOffL);
+  float* Tsm = reinterpret_cast<float*>(sm + kOffW);
+  float* Zsm = reinterpret_cast<float*>(sm + kOffZ);
   const uint32_t sbase = smem_u32(sm);
   const float* al_p = a.alpha + b * a.a_sb + h * a.a_sh;
   const float* be_p = a.beta + b * a.b_sb + h * a.b_sh;
@@ -128,7 +126,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const uint32_t tlane = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lane quarter
+  const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lane quarter
 
   auto issue_tma = [&](int c) {
     const uint32_t st = sbase + (uint32_t)(c & 1) * kStageBytes;
@@ -152,21 +150,20 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     }
   }
 
-  // Initial state: thread i owns row i of S (TMEM lane i) and of the bf16 copy.
+  // Initial state: lane i holds row i of S; this thread columns [64 half, 64 half + 64).
   {
-    const float* src = a.S_in ? a.S_in + bh * kD * kD + (int64_t)tid * kD : nullptr;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kD; c0 += 16) {
-      float v[16];
+    const float* src = a.S_in ? a.S_in + bh * kD * kD + (int64_t)row * kD + 64 * half : nullptr;
+    float v[64];
 #pragma unroll
-      for (int j = 0; j < 16; j += 4) {
-        const float4 x = src ? *reinterpret_cast<const float4*>(src + c0 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
-      }
-      tmem_st16(tlane + kColS + c0, v);
-      *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(tid, c0, 128)) = pack8_bf16(v);
-      *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(tid, c0 + 8, 128)) = pack8_bf16(v + 8);
+    for (int j = 0; j < 64; j += 4) {
+      const float4 x = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
     }
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) tmem_st16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(row, 64 * half + 8 * q, 128)) = pack8_bf16(v + 8 * q);
     tmem_st_wait();
   }
 
@@ -210,6 +207,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       gsm[tid] = gx;
       bsm[tid] = bt;
       gam[tid] = __expf(gx);
+      gin[tid] = __expf(-gx);
     }
     ok = ok && mbar_wait(smem_u32(&bar_tma[c & 1]), (uint32_t)((c >> 1) & 1), status);
     if (__syncthreads_or(!ok)) break;
@@ -237,95 +235,115 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // ---- L (lanes 0..63: rows of K K^T) and P_o (lanes 64..127: rows of Q K^T)
+    // ---- L (lanes 0..63: rows of K K^T) and P_o (lanes 64..127: rows of Q K^T); columns [32 half, 32 half + 32)
     {
-      float v[64];
-      ld64(tlane + kColKQ, v);
-      if (tid < kC) {
-        const int r = tid;
-        const float gr = gsm[r], br = bsm[r];
-        float* Lrow = Lsm + r * kLStride;
+      float v[32];
+      ld32(tlane + kColKQ + 32 * half, v);
+      const int j0 = 32 * half;
+      if (row < kC) {
+        const int r = row;
+        const float f = bsm[r] * gam[r];
+        float* Lrow = Lsm + r * kLStride + j0;
 #pragma unroll
-        for (int j = 0; j < kC; ++j) Lrow[j] = (j < r) ? br * __expf(gr - gsm[j]) * v[j] : 0.f;
+        for (int j = 0; j < 32; ++j) Lrow[j] = (j0 + j < r) ? f * gin[j0 + j] * v[j] : 0.f;
       } else {
-        const int r = tid - kC;
-        const float gr = gsm[r];
+        const int r = row - kC;
+        const float f = gam[r];
 #pragma unroll
-        for (int j = 0; j < kC; ++j) v[j] = (j <= r) ? __expf(gr - gsm[j]) * v[j] : 0.f;
+        for (int j = 0; j < 32; ++j) v[j] = (j0 + j <= r) ? f * gin[j0 + j] * v[j] : 0.f;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<uint4*>(sm + kOffPo + sw128_off(r, 8 * q, 64)) = pack8_bf16(v + 8 * q);
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(sm + kOffPo + sw128_off(r, j0 + 8 * q, 64)) = pack8_bf16(v + 8 * q);
       }
     }
     __syncthreads();
 
-    // ---- T = (I + L)^{-1} in 16x16 blocks (fp32, in the dead W tile space):
-    // diagonal blocks by forward substitution (one thread per block column),
-    // then block row i: T_ij = -T_ii sum_{m=j}^{i-1} L_im T_mj for j < i.
+    // ---- T = (I + L)^{-1} by doubling: 16x16 diagonal blocks by forward
+    // substitution, then the 32x32 and 64x64 levels with
+    //   [[A, 0], [C, B]]^{-1} = [[A^-1, 0], [-B^-1 C A^-1, B^-1]].
+    if (tid < kC) {
+      const int base = (tid >> 4) * 16, col = tid & 15;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < r; ++j) acc = fmaf(Lsm[(base + r) * kLStride + base + j], x[j], acc);
+        x[r] = (r < col) ? 0.f : ((r == col) ? 1.f : -acc);
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) Tsm[(base + r) * kTStride + base + col] = x[r];
+    } else {
+      // zero the six 16x16 blocks above the block diagonal
+      for (int e = tid - kC; e < 6 * 256; e += kThreads - kC) {
+        const int pr = e >> 8, w = e & 255;
+        const int bi = pr < 3 ? 0 : (pr < 5 ? 1 : 2);
+        const int bj = pr < 3 ? pr + 1 : (pr < 5 ? pr - 1 : 3);
+        Tsm[(bi * 16 + (w >> 4)) * kTStride + bj * 16 + (w & 15)] = 0.f;
+      }
+    }
+    __syncthreads();
     {
-      float* Tsm = reinterpret_cast<float*>(sm + kOffW);
-      float* Zsm = reinterpret_cast<float*>(sm + kOffZ);
-      if (tid < kC) {
-        const int base = (tid >> 4) * 16, col = tid & 15;
-        float x[16];
+      // level 32: blocks k = 0, 1 at rows 32k+16.., columns 32k..; thread: 2 columns of one row
+      const int k = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+      const int R = 32 * k + 16, Cb = 32 * k;
+      float z0 = 0.f, z1 = 0.f;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          float acc = 0.f;
-#pragma unroll
-          for (int j = 0; j < r; ++j) acc = fmaf(Lsm[(base + r) * kLStride + base + j], x[j], acc);
-          x[r] = (r < col) ? 0.f : ((r == col) ? 1.f : -acc);
-        }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) Tsm[(base + r) * kTStride + base + col] = x[r];
-      } else {
-        // zero the six blocks above the block diagonal
-        for (int e = tid - kC; e < 6 * 256; e += kC) {
-          const int pr = e >> 8, w = e & 255;
-          const int bi = pr < 3 ? 0 : (pr < 5 ? 1 : 2);
-          const int bj = pr < 3 ? pr + 1 : (pr < 5 ? pr - 1 : 3);
-          Tsm[(bi * 16 + (w >> 4)) * kTStride + bj * 16 + (w & 15)] = 0.f;
-        }
+      for (int m = 0; m < 16; ++m) {
+        const float l = Lsm[(R + r) * kLStride + Cb + m];
+        z0 = fmaf(l, Tsm[(Cb + m) * kTStride + Cb + c0], z0);
+        z1 = fmaf(l, Tsm[(Cb + m) * kTStride + Cb + c0 + 1], z1);
       }
+      Zsm[k * 256 + r * 16 + c0] = z0;
+      Zsm[k * 256 + r * 16 + c0 + 1] = z1;
       __syncthreads();
-#pragma unroll 1
-      for (int i = 1; i < 4; ++i) {
-        for (int e = tid; e < i * 256; e += kThreads) {
-          const int j = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-          const float* Lr = Lsm + (16 * i + r) * kLStride;
-          float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 4
-          for (int q = 16 * j; q < 16 * i; q += 2) {
-            acc0 = fmaf(Lr[q], Tsm[q * kTStride + 16 * j + cc], acc0);
-            acc1 = fmaf(Lr[q + 1], Tsm[(q + 1) * kTStride + 16 * j + cc], acc1);
-          }
-          Zsm[e] = acc0 + acc1;
-        }
-        __syncthreads();
-        for (int e = tid; e < i * 256; e += kThreads) {
-          const int j = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-          const float* Tr = Tsm + (16 * i + r) * kTStride + 16 * i;
-          float acc = 0.f;
+      float t0v = 0.f, t1v = 0.f;
 #pragma unroll
-          for (int p2 = 0; p2 < 16; ++p2) acc = fmaf(Tr[p2], Zsm[(j << 8) + p2 * 16 + cc], acc);
-          Tsm[(16 * i + r) * kTStride + 16 * j + cc] = -acc;
-        }
-        __syncthreads();
+      for (int p2 = 0; p2 < 16; ++p2) {
+        const float tv = Tsm[(R + r) * kTStride + R + p2];
+        t0v = fmaf(tv, Zsm[k * 256 + p2 * 16 + c0], t0v);
+        t1v = fmaf(tv, Zsm[k * 256 + p2 * 16 + c0 + 1], t1v);
       }
-      // bf16 tiles T diag(beta gamma) and T diag(beta): thread -> half a row
-      {
-        const int r = tid >> 1, c0 = (tid & 1) * 32;
-        float t1[32], t2[32];
+      Tsm[(R + r) * kTStride + Cb + c0] = -t0v;
+      Tsm[(R + r) * kTStride + Cb + c0 + 1] = -t1v;
+    }
+    __syncthreads();
+    {
+      // level 64: rows 32.., columns 0..31; thread: 4 columns of one row
+      const int r = tid >> 3, c0 = (tid & 7) * 4;
+      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int m = 0; m < 32; ++m) {
+        const float l = Lsm[(32 + r) * kLStride + m];
+        const float4 tv = *reinterpret_cast<const float4*>(Tsm + m * kTStride + c0);
+        z.x = fmaf(l, tv.x, z.x); z.y = fmaf(l, tv.y, z.y); z.z = fmaf(l, tv.z, z.z); z.w = fmaf(l, tv.w, z.w);
+      }
+      *reinterpret_cast<float4*>(Zsm + r * 32 + c0) = z;
+      __syncthreads();
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+      for (int p2 = 0; p2 < 32; ++p2) {
+        const float tv = Tsm[(32 + r) * kTStride + 32 + p2];
+        const float4 zz = *reinterpret_cast<const float4*>(Zsm + p2 * 32 + c0);
+        o.x = fmaf(tv, zz.x, o.x); o.y = fmaf(tv, zz.y, o.y); o.z = fmaf(tv, zz.z, o.z); o.w = fmaf(tv, zz.w, o.w);
+      }
+      *reinterpret_cast<float4*>(Tsm + (32 + r) * kTStride + c0) = make_float4(-o.x, -o.y, -o.z, -o.w);
+    }
+    __syncthreads();
+    {
+      // bf16 tiles T diag(beta gamma) and T diag(beta): thread -> 16 columns of one row
+      const int r = tid >> 2, c0 = (tid & 3) * 16;
+      float t1[16], t2[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float t = Tsm[r * kTStride + c0 + j];
-          t2[j] = t * bsm[c0 + j];
-          t1[j] = t2[j] * gam[c0 + j];
-        }
+      for (int j = 0; j < 16; ++j) {
+        const float tv = Tsm[r * kTStride + c0 + j];
+        t2[j] = tv * bsm[c0 + j];
+        t1[j] = t2[j] * gam[c0 + j];
+      }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          *reinterpret_cast<uint4*>(sm + kOffT1 + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t1 + 8 * q);
-          *reinterpret_cast<uint4*>(sm + kOffT2 + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t2 + 8 * q);
-        }
+      for (int q = 0; q < 2; ++q) {
+        *reinterpret_cast<uint4*>(sm + kOffT1 + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t1 + 8 * q);
+        *reinterpret_cast<uint4*>(sm + kOffT2 + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t2 + 8 * q);
       }
     }
     fence_proxy_async_smem();
@@ -352,12 +370,12 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // ---- W tile (bf16, [r][k]): thread k writes column k
+    // ---- W tile (bf16, [r][k]): lane k, rows r in [32 half, 32 half + 32)
     {
-      float w[64];
-      ld64(tlane + kColW, w);
+      float w[32];
+      ld32(tlane + kColW + 32 * half, w);
 #pragma unroll
-      for (int r = 0; r < kC; ++r) st_bf16(sm + kOffW + sw128_off(r, tid, 64), w[r]);
+      for (int r = 0; r < 32; ++r) st_bf16(sm + kOffW + sw128_off(32 * half + r, row, 64), w[r]);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -377,16 +395,15 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     }
     mma_pending = true;
     {
-      const float gamC = __expf(gsm[kC - 1]);
-#pragma unroll 1
-      for (int c0 = 0; c0 < kD; c0 += 16) {
-        float v[16];
-        tmem_ld16(tlane + kColS + c0, v);
-        tmem_ld_wait();
+      const float gamC = gam[kC - 1];
+      float v[64];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] *= gamC;
-        tmem_st16(tlane + kColS + c0, v);
-      }
+      for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 64; ++j) v[j] *= gamC;
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 16) tmem_st16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
       tmem_st_wait();
     }
     ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
@@ -395,22 +412,26 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // ---- U^T = U~^T - X (thread i owns row i); also U^T diag(gamma_C / gamma)
+    // ---- U^T = U~^T - X (lane i, columns j in [32 half, 32 half + 32)); also U^T diag(gamma_C / gamma)
     {
-      float u[64], x[64];
-      ld64(tlane + kColUt, u);
-      ld64(tlane + kColX, x);
-      const float gC = gsm[kC - 1];
-      float ud[64];
+      float u[32], x[32];
+      tmem_ld16(tlane + kColUt + 32 * half, *reinterpret_cast<float(*)[16]>(u));
+      tmem_ld16(tlane + kColUt + 32 * half + 16, *reinterpret_cast<float(*)[16]>(u + 16));
+      tmem_ld16(tlane + kColX + 32 * half, *reinterpret_cast<float(*)[16]>(x));
+      tmem_ld16(tlane + kColX + 32 * half + 16, *reinterpret_cast<float(*)[16]>(x + 16));
+      tmem_ld_wait();
+      const float gamC = gam[kC - 1];
+      const int j0 = 32 * half;
+      float ud[32];
 #pragma unroll
-      for (int j = 0; j < kC; ++j) {
+      for (int j = 0; j < 32; ++j) {
         u[j] -= x[j];
-        ud[j] = u[j] * __expf(gC - gsm[j]);
+        ud[j] = u[j] * (gamC * gin[j0 + j]);
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        *reinterpret_cast<uint4*>(sm + kOffU + sw128_off(tid, 8 * q, 128)) = pack8_bf16(u + 8 * q);
-        *reinterpret_cast<uint4*>(sm + kOffUD + sw128_off(tid, 8 * q, 128)) = pack8_bf16(ud + 8 * q);
+      for (int q = 0; q < 4; ++q) {
+        *reinterpret_cast<uint4*>(sm + kOffU + sw128_off(row, j0 + 8 * q, 128)) = pack8_bf16(u + 8 * q);
+        *reinterpret_cast<uint4*>(sm + kOffUD + sw128_off(row, j0 + 8 * q, 128)) = pack8_bf16(ud + 8 * q);
       }
     }
     fence_proxy_async_smem();
@@ -438,23 +459,25 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // ---- outputs o[t0 + r][i] = gamma_r Y[i][r] + PU[i][r]; next bf16 S0 row i
+    // ---- outputs o[t0 + r][i] = q_scale (gamma_r Y[i][r] + PU[i][r]), r in [32 half, 32 half + 32);
+    //      next bf16 S0 row i, columns [64 half, 64 half + 64)
     {
-      float y[64], p[64];
-      ld64(tlane + kColY, y);
-      ld64(tlane + kColPU, p);
-      TOut* obase = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + t0 * a.o_st + tid;
+      float y[32], p[32], v[64];
+      tmem_ld16(tlane + kColY + 32 * half, *reinterpret_cast<float(*)[16]>(y));
+      tmem_ld16(tlane + kColY + 32 * half + 16, *reinterpret_cast<float(*)[16]>(y + 16));
+      tmem_ld16(tlane + kColPU + 32 * half, *reinterpret_cast<float(*)[16]>(p));
+      tmem_ld16(tlane + kColPU + 32 * half + 16, *reinterpret_cast<float(*)[16]>(p + 16));
 #pragma unroll
-      for (int r = 0; r < kC; ++r)
-        if (r < nvalid) store1(obase + r * a.o_st, a.q_scale * fmaf(__expf(gsm[r]), y[r], p[r]));
-#pragma unroll 1
-      for (int c0 = 0; c0 < kD; c0 += 16) {
-        float v[16];
-        tmem_ld16(tlane + kColS + c0, v);
-        tmem_ld_wait();
-        *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(tid, c0, 128)) = pack8_bf16(v);
-        *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(tid, c0 + 8, 128)) = pack8_bf16(v + 8);
-      }
+      for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+      tmem_ld_wait();
+      const int r0 = 32 * half;
+      TOut* obase = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + (t0 + r0) * a.o_st + row;
+#pragma unroll
+      for (int r = 0; r < 32; ++r)
+        if (r0 + r < nvalid) store1(obase + r * a.o_st, a.q_scale * fmaf(gam[r0 + r], y[r], p[r]));
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(row, 64 * half + 8 * q, 128)) = pack8_bf16(v + 8 * q);
     }
     fence_proxy_async_smem();
     tc_fence_before();
@@ -467,16 +490,14 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   }
 
   if (ok) {
-    // final state, row i from lane i
-    float* dst = a.S_out + bh * kD * kD + (int64_t)tid * kD;
-#pragma unroll 1
-    for (int c0 = 0; c0 < kD; c0 += 16) {
-      float v[16];
-      tmem_ld16(tlane + kColS + c0, v);
-      tmem_ld_wait();
+    // final state: lane i row i, this thread columns [64 half, 64 half + 64)
+    float* dst = a.S_out + bh * kD * kD + (int64_t)row * kD + 64 * half;
+    float v[64];
 #pragma unroll
-      for (int j = 0; j < 16; j += 4) *reinterpret_cast<float4*>(dst + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-    }
+    for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
   } else if (tid == 0) {
     // a wait expired: let this CTA's own copies and MMAs drain (bounded) before freeing TMEM
     for (int k = c; k < tma_issued; ++k) mbar_wait(smem_u32(&bar_tma[k & 1]), (uint32_t)((k >> 1) & 1), status);
