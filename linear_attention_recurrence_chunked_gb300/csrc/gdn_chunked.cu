@@ -43,17 +43,20 @@ constexpr uint32_t kOffS0 = 2 * kStageBytes;      // bf16 S0 [128 i][128 k], K-m
 constexpr uint32_t kOffW = kOffS0 + 32768;        // bf16 W [64 r][128 k], K-major
 constexpr uint32_t kOffT1 = kOffW + 16384;        // bf16 T diag(beta gamma) [64 r][64 j]
 constexpr uint32_t kOffT2 = kOffT1 + 8192;        // bf16 T diag(beta)       [64 r][64 j]
-constexpr uint32_t kOffPo = kOffT2 + 8192;        // bf16 tril(Gamma) . Q K^T [64 r][64 j]
-constexpr uint32_t kOffU = kOffPo + 8192;         // bf16 U^T [128 i][64 j]
+constexpr uint32_t kOffPo = kOffT2 + 8192;        // 2 x bf16 tril(Gamma) . Q K^T [64 r][64 j]
+constexpr uint32_t kOffU = kOffPo + 16384;        // bf16 U^T [128 i][64 j]
 constexpr uint32_t kOffUD = kOffU + 16384;        // bf16 U^T diag(gamma_C/gamma) [128 i][64 j]
-constexpr uint32_t kOffL = kOffU;                 // fp32 L [64][65], lives only before U is formed
-constexpr uint32_t kOffZ = kOffL + 64 * 65 * 4;   // fp32 block products for the inversion (4 KB, same lifetime)
-constexpr uint32_t kOffGate = kOffUD + 16384;     // fp32 g, beta, gamma, 1/gamma [64] each
-constexpr uint32_t kSmemUsed = kOffGate + 1024;
+constexpr uint32_t kOffGate = kOffUD + 16384;     // 2 x fp32 {g, beta, gamma, 1/gamma}[64]
+constexpr uint32_t kSmemUsed = kOffGate + 2048;
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
+// Scratch of the inversion of the NEXT chunk, in tiles that are dead meanwhile:
+// L and the block products live in the S0 tile (read by MMA 3 before, rewritten
+// after), T in fp32 in the W tile (read by MMA 3 before, rewritten after).
+constexpr uint32_t kOffL = kOffS0;                // fp32 L [64][65]
+constexpr uint32_t kOffZ = kOffL + 64 * 65 * 4;   // fp32 block products (4 KB)
 constexpr int kLStride = 65;
-constexpr int kTStride = 64;                      // fp32 T [64][64] reuses the W tile space
-static_assert(kOffZ + 1024 * 4 <= kOffGate, "L/Z scratch overlaps the gates");
+constexpr int kTStride = 64;
+static_assert(64 * 65 * 4 + 1024 * 4 <= 32768, "L/Z scratch exceeds the S0 tile");
 static_assert(64 * kTStride * 4 <= 16384, "T scratch exceeds the W tile");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
@@ -98,16 +101,19 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   const int b = (int)(bh / a.H), h = (int)(bh % a.H);
   const int64_t N = a.N;
   const int nchunks = (int)((N + kC - 1) / kC);
-  float* gsm = reinterpret_cast<float*>(sm + kOffGate);  // g_r = sum_{j<=r} log alpha_j
-  float* bsm = gsm + kC;                                  // beta_r
-  float* gam = gsm + 2 * kC;                              // gamma_r = e^{g_r}
-  float* gin = gsm + 3 * kC;                              // 1 / gamma_r
   float* Lsm = reinterpret_cast<float*>(sm + kOffL);
   float* Tsm = reinterpret_cast<float*>(sm + kOffW);
   float* Zsm = reinterpret_cast<float*>(sm + kOffZ);
   const uint32_t sbase = smem_u32(sm);
   const float* al_p = a.alpha + b * a.a_sb + h * a.a_sh;
   const float* be_p = a.beta + b * a.b_sb + h * a.b_sh;
+  // per-chunk gate tables, double-buffered by chunk parity
+  auto gsm = [&](int c) { return reinterpret_cast<float*>(sm + kOffGate + (c & 1) * 1024); };  // g_r
+  auto bsm = [&](int c) { return gsm(c) + kC; };      // beta_r
+  auto gam = [&](int c) { return gsm(c) + 2 * kC; };  // gamma_r = e^{g_r}
+  auto gin = [&](int c) { return gsm(c) + 3 * kC; };  // 1 / gamma_r
+  auto stage = [&](int c) { return sbase + (uint32_t)(c & 1) * kStageBytes; };
+  auto po = [&](int c) { return (uint32_t)kOffPo + (uint32_t)(c & 1) * 8192u; };
 
   if (tid == 0) {
     mbar_init(smem_u32(&bar_tma[0]), 1);
@@ -129,7 +135,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lane quarter
 
   auto issue_tma = [&](int c) {
-    const uint32_t st = sbase + (uint32_t)(c & 1) * kStageBytes;
+    const uint32_t st = stage(c);
     const uint32_t bar = smem_u32(&bar_tma[c & 1]);
     const int t0 = c * kC;
     mbar_arrive_expect_tx(bar, kStageBytes);
@@ -140,7 +146,8 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     tma_load_4d(st + kOffV + 0, &tmap_v, 0, t0, h, b, bar);
     tma_load_4d(st + kOffV + 8192, &tmap_v, 64, t0, h, b, bar);
   };
-  int tma_issued = 0;  // chunks whose loads have been issued (meaningful in thread 0)
+  int tma_issued = 0;   // chunks whose loads have been issued (meaningful in thread 0)
+  int tma_waited = 0;   // chunks whose loads have been waited for
   if (tid == 0) {
     issue_tma(0);
     tma_issued = 1;
@@ -161,15 +168,12 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     }
 #pragma unroll
     for (int c0 = 0; c0 < 64; c0 += 16) tmem_st16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(row, 64 * half + 8 * q, 128)) = pack8_bf16(v + 8 * q);
     tmem_st_wait();
   }
 
   auto load_gates = [&](int c, float& lg, float& bt) {
     const int64_t t = (int64_t)c * kC + tid;
-    if (tid < kC && t < N) {
+    if (tid < kC && c < nchunks && t < N) {
       lg = logf(al_p[t]);
       bt = be_p[t];
     } else {
@@ -183,15 +187,12 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   uint32_t mma_phase = 0;
   bool ok = true;
   bool mma_pending = false;
-  int c = 0;
-  for (; c < nchunks; ++c) {
-    const int64_t t0 = (int64_t)c * kC;
-    const int nvalid = (N - t0 < kC) ? (int)(N - t0) : kC;
-    const uint32_t st = sbase + (uint32_t)(c & 1) * kStageBytes;
-    const float lg = lg_next, bt = bt_next;
-    if (c + 1 < nchunks) load_gates(c + 1, lg_next, bt_next);
 
-    // ---- gates: inclusive scan of log alpha over the chunk (threads 0..63)
+  // ---------------------------------------------------------------- phases
+  // gates of chunk cc: inclusive scan of log alpha (threads 0..63); ends with a barrier
+  auto phase_gates = [&](int cc) {
+    const float lg = lg_next, bt = bt_next;
+    load_gates(cc + 1, lg_next, bt_next);
     float gx = lg;
     if (tid < kC) {
 #pragma unroll
@@ -204,72 +205,66 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     __syncthreads();
     if (tid < kC) {
       if (warp == 1) gx += warp0_total;
-      gsm[tid] = gx;
-      bsm[tid] = bt;
-      gam[tid] = __expf(gx);
-      gin[tid] = __expf(-gx);
+      gsm(cc)[tid] = gx;
+      bsm(cc)[tid] = bt;
+      gam(cc)[tid] = __expf(gx);
+      gin(cc)[tid] = __expf(-gx);
     }
-    ok = ok && mbar_wait(smem_u32(&bar_tma[c & 1]), (uint32_t)((c >> 1) & 1), status);
-    if (__syncthreads_or(!ok)) break;
-
-    // ---- MMA 1: [K;Q] K^T -> KQ, S0 Q^T -> Y
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-        mma_bf16(tmem + kColKQ, kmaj(st + kOffKQ + koff), kmaj(st + kOffKQ + koff), id, ks > 0);
-      }
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-        mma_bf16(tmem + kColY, kmaj(sbase + kOffS0 + koff), kmaj(st + kOffKQ + 8192 + koff), id, ks > 0);
-      }
-      mma_commit(smem_u32(&bar_mma));
-    }
-    mma_pending = true;
+  };
+  auto wait_tma = [&](int cc) {
+    ok = ok && mbar_wait(smem_u32(&bar_tma[cc & 1]), (uint32_t)((cc >> 1) & 1), status);
+    tma_waited = cc + 1;
+  };
+  auto wait_mma = [&]() {
     ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
     mma_phase ^= 1;
     mma_pending = !ok;
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-
-    // ---- L (lanes 0..63: rows of K K^T) and P_o (lanes 64..127: rows of Q K^T); columns [32 half, 32 half + 32)
-    {
-      float v[32];
-      ld32(tlane + kColKQ + 32 * half, v);
-      const int j0 = 32 * half;
-      if (row < kC) {
-        const int r = row;
-        const float f = bsm[r] * gam[r];
-        float* Lrow = Lsm + r * kLStride + j0;
+  };
+  auto mma_kq = [&](int cc) {  // [K;Q] K^T of chunk cc -> KQ
+    const uint32_t st = stage(cc);
+    const uint32_t id = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) Lrow[j] = (j0 + j < r) ? f * gin[j0 + j] * v[j] : 0.f;
-      } else {
-        const int r = row - kC;
-        const float f = gam[r];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = (j0 + j <= r) ? f * gin[j0 + j] * v[j] : 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(sm + kOffPo + sw128_off(r, j0 + 8 * q, 64)) = pack8_bf16(v + 8 * q);
-      }
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+      mma_bf16(tmem + kColKQ, kmaj(st + kOffKQ + koff), kmaj(st + kOffKQ + koff), id, ks > 0);
     }
-    __syncthreads();
-
-    // ---- T = (I + L)^{-1} by doubling: 16x16 diagonal blocks by forward
-    // substitution, then the 32x32 and 64x64 levels with
-    //   [[A, 0], [C, B]]^{-1} = [[A^-1, 0], [-B^-1 C A^-1, B^-1]].
+  };
+  // L (into the S0-tile scratch) and P_o of chunk cc from KQ
+  auto phase_L_Po = [&](int cc) {
+    float v[32];
+    ld32(tlane + kColKQ + 32 * half, v);
+    const int j0 = 32 * half;
+    const float* gm = gam(cc);
+    const float* gi = gin(cc);
+    if (row < kC) {
+      const int r = row;
+      const float f = bsm(cc)[r] * gm[r];
+      float* Lrow = Lsm + r * kLStride + j0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) Lrow[j] = (j0 + j < r) ? f * gi[j0 + j] * v[j] : 0.f;
+    } else {
+      const int r = row - kC;
+      const float f = gm[r];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = (j0 + j <= r) ? f * gi[j0 + j] * v[j] : 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(sm + po(cc) + sw128_off(r, j0 + 8 * q, 64)) = pack8_bf16(v + 8 * q);
+    }
+  };
+  // T = (I + L)^{-1} of chunk cc by doubling, then the bf16 tiles T diag(beta gamma), T diag(beta)
+  auto phase_T = [&](int cc) {
     if (tid < kC) {
+      // 16x16 diagonal blocks, right-looking substitution: one thread per block column
       const int base = (tid >> 4) * 16, col = tid & 15;
       float x[16];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float acc = 0.f;
+      for (int r = 0; r < 16; ++r) x[r] = (r == col) ? 1.f : 0.f;
 #pragma unroll
-        for (int j = 0; j < r; ++j) acc = fmaf(Lsm[(base + r) * kLStride + base + j], x[j], acc);
-        x[r] = (r < col) ? 0.f : ((r == col) ? 1.f : -acc);
+      for (int j = 0; j < 15; ++j) {
+        const float* Lc = Lsm + (base + j + 1) * kLStride + base + j;
+#pragma unroll
+        for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-Lc[(r - j - 1) * kLStride], x[j], x[r]);
       }
 #pragma unroll
       for (int r = 0; r < 16; ++r) Tsm[(base + r) * kTStride + base + col] = x[r];
@@ -284,7 +279,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     }
     __syncthreads();
     {
-      // level 32: blocks k = 0, 1 at rows 32k+16.., columns 32k..; thread: 2 columns of one row
+      // level 32: [[A,0],[C,B]]^-1 lower-left block = -B^-1 (C A^-1); blocks k = 0, 1
       const int k = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
       const int R = 32 * k + 16, Cb = 32 * k;
       float z0 = 0.f, z1 = 0.f;
@@ -331,14 +326,15 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     }
     __syncthreads();
     {
-      // bf16 tiles T diag(beta gamma) and T diag(beta): thread -> 16 columns of one row
       const int r = tid >> 2, c0 = (tid & 3) * 16;
+      const float* bt = bsm(cc);
+      const float* gm = gam(cc);
       float t1[16], t2[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
         const float tv = Tsm[r * kTStride + c0 + j];
-        t2[j] = tv * bsm[c0 + j];
-        t1[j] = t2[j] * gam[c0 + j];
+        t2[j] = tv * bt[c0 + j];
+        t1[j] = t2[j] * gm[c0 + j];
       }
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
@@ -346,44 +342,83 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         *reinterpret_cast<uint4*>(sm + kOffT2 + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t2 + 8 * q);
       }
     }
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    // ---- MMA 2: W^T = K^T (T diag(beta gamma))^T, U~^T = V^T (T diag(beta))^T
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t id = idesc_bf16(128, 64, 1, 0);
+  };
+  auto mma_wu = [&](int cc) {  // W^T = K^T (T diag(beta gamma))^T, U~^T = V^T (T diag(beta))^T
+    const uint32_t st = stage(cc);
+    const uint32_t id = idesc_bf16(128, 64, 1, 0);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kColW, sw128_desc(st + kOffKQ + ks * 2048, 16384, 1024), kmaj(sbase + kOffT1 + ks * 32),
-                 id, ks > 0);
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem + kColW, sw128_desc(st + kOffKQ + ks * 2048, 16384, 1024), kmaj(sbase + kOffT1 + ks * 32), id,
+               ks > 0);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kColUt, sw128_desc(st + kOffV + ks * 2048, 8192, 1024), kmaj(sbase + kOffT2 + ks * 32),
-                 id, ks > 0);
-      mma_commit(smem_u32(&bar_mma));
-    }
-    mma_pending = true;
-    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
-    mma_phase ^= 1;
-    mma_pending = !ok;
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-
-    // ---- W tile (bf16, [r][k]): lane k, rows r in [32 half, 32 half + 32)
-    {
-      float w[32];
-      ld32(tlane + kColW + 32 * half, w);
+    for (int ks = 0; ks < 4; ++ks)
+      mma_bf16(tmem + kColUt, sw128_desc(st + kOffV + ks * 2048, 8192, 1024), kmaj(sbase + kOffT2 + ks * 32), id,
+               ks > 0);
+  };
+  auto phase_Wtile = [&]() {  // lane k, rows r in [32 half, 32 half + 32)
+    float w[32];
+    ld32(tlane + kColW + 32 * half, w);
 #pragma unroll
-      for (int r = 0; r < 32; ++r) st_bf16(sm + kOffW + sw128_off(32 * half + r, row, 64), w[r]);
-    }
+    for (int r = 0; r < 32; ++r) st_bf16(sm + kOffW + sw128_off(32 * half + r, row, 64), w[r]);
+  };
+  auto sync_for_mma = [&]() {  // generic-proxy tile writes -> visible to the tensor cores
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+  };
 
-    // ---- MMA 3: X = S0 W^T ; meanwhile S <- gamma_C S in tensor memory
+  // ---------------------------------------------------------------- prologue: intra-chunk work of chunk 0
+  phase_gates(0);
+  if (tid == 0) wait_tma(0);
+  if (__syncthreads_or(!ok)) goto done;
+  if (tid == 0) {
+    tc_fence_after();
+    mma_kq(0);
+    mma_commit(smem_u32(&bar_mma));
+  }
+  mma_pending = true;
+  wait_mma();
+  if (__syncthreads_or(!ok)) goto done;
+  tc_fence_after();
+  phase_L_Po(0);
+  __syncthreads();
+  phase_T(0);
+  sync_for_mma();
+  if (tid == 0) {
+    mma_wu(0);
+    mma_commit(smem_u32(&bar_mma));
+  }
+  mma_pending = true;
+  // the S0 tile (its region held the inversion scratch) gets the initial state now
+  {
+    float v[64];
+#pragma unroll
+    for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(row, 64 * half + 8 * q, 128)) = pack8_bf16(v + 8 * q);
+  }
+  wait_mma();
+  if (__syncthreads_or(!ok)) goto done;
+  tc_fence_after();
+  phase_Wtile();
+  sync_for_mma();
+
+  // ---------------------------------------------------------------- main loop: chain of chunk c, intra of c+1
+  for (int c = 0; c < nchunks; ++c) {
+    const bool has_next = c + 1 < nchunks;
+    const int64_t t0 = (int64_t)c * kC;
+    const int nvalid = (N - t0 < kC) ? (int)(N - t0) : kC;
+    if (has_next) phase_gates(c + 1);
+    if (tid == 0 && has_next) wait_tma(c + 1);
+    if (__syncthreads_or(!ok)) break;
+
+    // ---- MMA 3: X = S0 W^T, Y = S0 Q^T of chunk c; [K;Q] K^T of chunk c+1
     if (tid == 0) {
+      tc_fence_after();
+      const uint32_t st = stage(c);
       const uint32_t id = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
@@ -391,11 +426,18 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const uint32_t woff = (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u;
         mma_bf16(tmem + kColX, kmaj(sbase + kOffS0 + koff), kmaj(sbase + kOffW + woff), id, ks > 0);
       }
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+        mma_bf16(tmem + kColY, kmaj(sbase + kOffS0 + koff), kmaj(st + kOffKQ + 8192 + koff), id, ks > 0);
+      }
+      if (has_next) mma_kq(c + 1);
       mma_commit(smem_u32(&bar_mma));
     }
     mma_pending = true;
     {
-      const float gamC = gam[kC - 1];
+      // S <- gamma_C S while the MMAs run (S itself is not an operand of this round)
+      const float gamC = gam(c)[kC - 1];
       float v[64];
 #pragma unroll
       for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
@@ -406,13 +448,12 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       for (int c0 = 0; c0 < 64; c0 += 16) tmem_st16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
       tmem_st_wait();
     }
-    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
-    mma_phase ^= 1;
-    mma_pending = !ok;
+    wait_mma();
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // ---- U^T = U~^T - X (lane i, columns j in [32 half, 32 half + 32)); also U^T diag(gamma_C / gamma)
+    // ---- U^T = U~^T - X of chunk c (lane i, columns j in [32 half, 32 half + 32)), U^T diag(gamma_C/gamma);
+    //      L and P_o of chunk c+1
     {
       float u[32], x[32];
       tmem_ld16(tlane + kColUt + 32 * half, *reinterpret_cast<float(*)[16]>(u));
@@ -420,13 +461,14 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       tmem_ld16(tlane + kColX + 32 * half, *reinterpret_cast<float(*)[16]>(x));
       tmem_ld16(tlane + kColX + 32 * half + 16, *reinterpret_cast<float(*)[16]>(x + 16));
       tmem_ld_wait();
-      const float gamC = gam[kC - 1];
+      const float gamC = gam(c)[kC - 1];
+      const float* gi = gin(c);
       const int j0 = 32 * half;
       float ud[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         u[j] -= x[j];
-        ud[j] = u[j] * (gamC * gin[j0 + j]);
+        ud[j] = u[j] * (gamC * gi[j0 + j]);
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -434,17 +476,16 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         *reinterpret_cast<uint4*>(sm + kOffUD + sw128_off(row, j0 + 8 * q, 128)) = pack8_bf16(ud + 8 * q);
       }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    if (has_next) phase_L_Po(c + 1);
+    sync_for_mma();
 
-    // ---- MMA 4: (P_o U)^T = U^T P_o^T ; S += U^T diag(gamma_C/gamma) K
+    // ---- MMA 4: (P_o U)^T = U^T P_o^T ; S += U^T diag(gamma_C/gamma) K  (chunk c)
     if (tid == 0) {
+      const uint32_t st = stage(c);
       const uint32_t id = idesc_bf16(128, 64, 0, 0);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        mma_bf16(tmem + kColPU, kmaj(sbase + kOffU + ks * 32), kmaj(sbase + kOffPo + ks * 32), id, ks > 0);
+        mma_bf16(tmem + kColPU, kmaj(sbase + kOffU + ks * 32), kmaj(sbase + po(c) + ks * 32), id, ks > 0);
       const uint32_t id2 = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
@@ -453,14 +494,18 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       mma_commit(smem_u32(&bar_mma));
     }
     mma_pending = true;
-    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
-    mma_phase ^= 1;
-    mma_pending = !ok;
+    if (has_next) phase_T(c + 1);  // overlaps MMA 4; its tiles are not operands of MMA 4
+    sync_for_mma();
+    wait_mma();
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
 
-    // ---- outputs o[t0 + r][i] = q_scale (gamma_r Y[i][r] + PU[i][r]), r in [32 half, 32 half + 32);
-    //      next bf16 S0 row i, columns [64 half, 64 half + 64)
+    // ---- MMA 2 of chunk c+1 (W^T, U~^T), overlapped with chunk c's outputs and the next S0 tile
+    if (tid == 0 && has_next) {
+      mma_wu(c + 1);
+      mma_commit(smem_u32(&bar_mma));
+    }
+    if (has_next) mma_pending = true;
     {
       float y[32], p[32], v[64];
       tmem_ld16(tlane + kColY + 32 * half, *reinterpret_cast<float(*)[16]>(y));
@@ -471,24 +516,33 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
       tmem_ld_wait();
       const int r0 = 32 * half;
-      TOut* obase = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + (t0 + r0) * a.o_st + row;
+      const float* gm = gam(c);
+      TOut* optr = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + (t0 + r0) * a.o_st + row;
 #pragma unroll
-      for (int r = 0; r < 32; ++r)
-        if (r0 + r < nvalid) store1(obase + r * a.o_st, a.q_scale * fmaf(gam[r0 + r], y[r], p[r]));
+      for (int r = 0; r < 32; ++r) {
+        if (r0 + r < nvalid) store1(optr, a.q_scale * fmaf(gm[r0 + r], y[r], p[r]));
+        optr += a.o_st;
+      }
+      if (has_next) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(row, 64 * half + 8 * q, 128)) = pack8_bf16(v + 8 * q);
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(sm + kOffS0 + sw128_off(row, 64 * half + 8 * q, 128)) = pack8_bf16(v + 8 * q);
+      }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    if (has_next) {
+      wait_mma();
+      if (__syncthreads_or(!ok)) break;
+      tc_fence_after();
+      phase_Wtile();
+    }
+    sync_for_mma();
     if (tid == 0 && c + 2 < nchunks) {
-      issue_tma(c + 2);
+      issue_tma(c + 2);  // stage c is free: every MMA that read it has completed
       tma_issued = c + 3;
     }
   }
 
+done:
   if (ok) {
     // final state: lane i row i, this thread columns [64 half, 64 half + 64)
     float* dst = a.S_out + bh * kD * kD + (int64_t)row * kD + 64 * half;
@@ -500,7 +554,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
   } else if (tid == 0) {
     // a wait expired: let this CTA's own copies and MMAs drain (bounded) before freeing TMEM
-    for (int k = c; k < tma_issued; ++k) mbar_wait(smem_u32(&bar_tma[k & 1]), (uint32_t)((k >> 1) & 1), status);
+    for (int k = tma_waited; k < tma_issued; ++k) mbar_wait(smem_u32(&bar_tma[k & 1]), (uint32_t)((k >> 1) & 1), status);
     if (mma_pending) mbar_wait(smem_u32(&bar_mma), mma_phase, status);
   }
   tc_fence_before();
