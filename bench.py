@@ -179,20 +179,34 @@ class Timer:
         self.events = []
 
 
+def rank_seed_offset(rank: int) -> int:
+    """Each rank runs its own replica of the workload on its own seeded inputs
+    (independent problems: weak scaling, no collective on the data path)."""
+    return 1000 * int(rank)
+
+
 def max_over_ranks(x: float, ws: int) -> float:
+    """Slowest rank's time (the job is done when the last replica is)."""
     if ws == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, ws: int, max_seconds: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time."""
+    return ws * units_per_rank / max_seconds
 
 
 def barrier(ws):
     if ws > 1:
         import torch.distributed as dist
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 def roofline(bytes_per_launch, ms_per_launch, peak_gbs, traffic):
@@ -213,7 +227,7 @@ def gpu_arm(args, ws, rank, local):
     pk = peaks()
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    seed_off = 1000 * rank
+    seed_off = rank_seed_offset(rank)
     launches = 0
 
     # --- headline: BASED prefill --------------------------------------------
@@ -242,7 +256,7 @@ def gpu_arm(args, ws, rank, local):
     ms_total = max_over_ranks(ms_total, ws)
     ms_step = ms_total / args.steps
     tokens = w.B * w.N
-    value = ws * tokens * args.steps / (ms_total * 1e-3)
+    value = whole_job_rate(tokens * args.steps, ws, ms_total * 1e-3)
     bytes_launch = BYTES_PER_TOKEN_HEAD["taylor_prefill"] * w.B * w.H * w.N + STATE_BYTES["taylor"] * w.B * w.H
     roof = roofline(bytes_launch, ms_step, pk["hbm_gbs"], ncu_traffic("taylor_prefill"))
     roof["peak_source"] = pk["source"]
@@ -272,7 +286,7 @@ def gpu_arm(args, ws, rank, local):
     e2e_ms = max_over_ranks(et.total_ms(), ws)
     barrier(ws)
     launches += args.steps * KERNELS_PER_CALL["based_prefill"]
-    e2e = {"value": ws * tokens * args.steps / (e2e_ms * 1e-3), "unit": "tokens/s",
+    e2e = {"value": whole_job_rate(tokens * args.steps, ws, e2e_ms * 1e-3), "unit": "tokens/s",
            "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (hq, hk, hv))),
            "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in (hy, hs, hz)))}
     del hq, hk, hv, hy, hs, hz
@@ -329,7 +343,7 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         launches += reps * KERNELS_PER_CALL["gdn_prefill"]
         byts = BYTES_PER_TOKEN_HEAD["gdn_prefill"] * w.B * w.H * w.N + STATE_BYTES["gdn"] * w.B * w.H
         r = roofline(byts, ms, pk["hbm_gbs"], ncu_traffic(name))
-        out[name] = {"workload": w.description, "tokens_per_s": round(ws * w.B * w.N / (ms * 1e-3), 1),
+        out[name] = {"workload": w.description, "tokens_per_s": round(whole_job_rate(w.B * w.N, ws, ms * 1e-3), 1),
                      "ms": round(ms, 4), "roofline": r}
         del x, o, S, ws_t
         torch.cuda.empty_cache()
@@ -374,7 +388,7 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         byts = BYTES_PER_TOKEN_HEAD[key] * S_ * H_
         r = roofline(byts, per_step, pk["hbm_gbs"], ncu_traffic(key))
         out[f"decode_{variant}"] = {"workload": f"{variant} decode {S_} seqs x {H_} heads x {n_steps} steps",
-                                    "tokens_per_s": round(ws * S_ / (per_step * 1e-3), 1),
+                                    "tokens_per_s": round(whole_job_rate(S_, ws, per_step * 1e-3), 1),
                                     "ms_per_step": round(per_step, 5), "roofline": r}
         del xs, state, z, outb
         torch.cuda.empty_cache()
@@ -467,7 +481,7 @@ def main():
         la.load_library()
         stream = torch.cuda.Stream(device=dev)
         flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-        paths, launches = other_paths(args, la, dev, stream, flush, peaks(), 1000 * rank, ws, only=args.only)
+        paths, launches = other_paths(args, la, dev, stream, flush, peaks(), rank_seed_offset(rank), ws, only=args.only)
         if rank == 0:
             print(json.dumps({"only": args.only, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
                               "gpu_launches": launches, **paths[args.only]}), flush=True)

@@ -161,6 +161,17 @@ la_status la_decode_step(const la_decode_args* args, void* stream);
  * LA_OK or LA_ERR_TIMEOUT; LA_ERR_CUDA if the synchronisation failed. */
 la_status la_device_status(void* stream, int clear);
 
+/* Self-test of the bounded-wait error path (infrastructure; the pages have no
+ * counterpart).  Launches one thread on `stream` that waits on a shared-memory
+ * barrier with the same bounded wait the tensor-core kernels use.  With
+ * arrive == 0 nothing ever arrives, so the wait gives up after limit_ns and
+ * sets the device status word (la_device_status then reports
+ * LA_ERR_TIMEOUT); with arrive != 0 the thread arrives itself and the wait
+ * completes at once.  No fault, trap or unbounded wait is involved, and the
+ * context stays usable.  limit_ns must lie in [1e6, 2e9]; otherwise
+ * LA_ERR_INVALID_ARGUMENT and nothing is launched. */
+la_status la_selftest_bounded_wait(int arrive, int64_t limit_ns, void* stream);
+
 /* Static description of a status code; never NULL. */
 const char* la_status_string(la_status status);
 

@@ -69,7 +69,8 @@ class DecodeArgs(ctypes.Structure):
 
 
 EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_decode_step", "la_based_prefill_workspace_size",
-            "la_gdn_prefill_workspace_size", "la_device_status", "la_status_string", "la_abi_version")
+            "la_gdn_prefill_workspace_size", "la_device_status", "la_selftest_bounded_wait", "la_status_string",
+            "la_abi_version")
 
 
 class LAError(RuntimeError):
@@ -107,6 +108,8 @@ def load_library(path: str | None = None):
     lib.la_gdn_prefill_workspace_size.argtypes = [ctypes.POINTER(GdnPrefillArgs)]
     lib.la_device_status.restype = ctypes.c_int
     lib.la_device_status.argtypes = [vp, ctypes.c_int]
+    lib.la_selftest_bounded_wait.restype = ctypes.c_int
+    lib.la_selftest_bounded_wait.argtypes = [ctypes.c_int, ctypes.c_int64, vp]
     lib.la_status_string.restype = ctypes.c_char_p
     lib.la_status_string.argtypes = [ctypes.c_int]
     lib.la_abi_version.restype = ctypes.c_int
@@ -290,3 +293,8 @@ def la_decode_step(variant: int, q, k, v, state, z=None, alpha=None, beta=None, 
 
 def la_device_status(stream=None, clear: bool = True) -> int:
     return int(load_library().la_device_status(_stream_handle(stream), 1 if clear else 0))
+
+
+def la_selftest_bounded_wait(arrive: bool, limit_ns: int, stream=None) -> int:
+    """Launch the bounded-wait self-test (see include/la.h); returns the launch status."""
+    return int(load_library().la_selftest_bounded_wait(1 if arrive else 0, int(limit_ns), _stream_handle(stream)))

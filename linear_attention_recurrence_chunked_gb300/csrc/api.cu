@@ -213,6 +213,13 @@ la_status la_decode_step(const la_decode_args* a, void* stream) {
   return from_cuda(a->variant == LA_VARIANT_GDN ? la::launch_gdn_decode(L, s) : la::launch_taylor_decode(L, s));
 }
 
+la_status la_selftest_bounded_wait(int arrive, int64_t limit_ns, void* stream) {
+  if (limit_ns < 1000000 || limit_ns > 2000000000) return LA_ERR_INVALID_ARGUMENT;
+  unsigned* status = device_status_ptr();
+  if (!status) return LA_ERR_CUDA;
+  return from_cuda(la::launch_bounded_wait_selftest(arrive, (uint64_t)limit_ns, status, static_cast<cudaStream_t>(stream)));
+}
+
 la_status la_device_status(void* stream, int clear) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
   unsigned v = 0;

@@ -59,5 +59,6 @@ cudaError_t launch_gdn_prefill_recurrent(const GdnPrefillLaunch& a, cudaStream_t
 // bf16 inputs: chunked tcgen05 kernels.
 cudaError_t launch_gdn_prefill_chunked(const GdnPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
 cudaError_t launch_taylor_prefill_chunked(const TaylorPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
+cudaError_t launch_bounded_wait_selftest(int arrive, uint64_t limit_ns, unsigned* dev_status, cudaStream_t stream);
 
 }  // namespace la

@@ -53,17 +53,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 // Waits for phase `parity` of the barrier to complete; gives up after
-// kWaitLimitNs, ORs kStatusTimeout into *status and returns false.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status) {
+// limit_ns, ORs kStatusTimeout into *status and returns false.
+__device__ __forceinline__ bool mbar_wait_ns(uint32_t bar, uint32_t parity, unsigned* status, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
       atomicOr(status, kStatusTimeout);
       return false;
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status) {
+  return mbar_wait_ns(bar, parity, status, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------- fences
