@@ -340,7 +340,9 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         for _ in range(reps):
             t.run(step)
         ms = max_over_ranks(t.total_ms(), ws) / reps
-        launches += reps * KERNELS_PER_CALL["gdn_prefill"]
+        # a call that splits the sequence into segments runs three kernels (maps, combine, outputs)
+        per_call = 3 if ws_t.numel() > 1 else KERNELS_PER_CALL["gdn_prefill"]
+        launches += reps * per_call
         byts = BYTES_PER_TOKEN_HEAD["gdn_prefill"] * w.B * w.H * w.N + STATE_BYTES["gdn"] * w.B * w.H
         r = roofline(byts, ms, pk["hbm_gbs"], ncu_traffic(name))
         out[name] = {"workload": w.description, "tokens_per_s": round(whole_job_rate(w.B * w.N, ws, ms * 1e-3), 1),

@@ -137,7 +137,14 @@ typedef struct la_decode_args {
 } la_decode_args;
 
 /* Bytes of device workspace the matching prefill call needs for `args`
- * (0 = none; a NULL workspace is then accepted).  Pure host function. */
+ * (0 = none; a NULL workspace is then accepted).  Pure host function of the
+ * sizes and dtypes in `args` (no pointer is read), so it can be asked before
+ * any buffer is allocated.  The gated-delta-rule prefill needs scratch when
+ * it splits long sequences of few (b,h) pairs into segments: one 64 KiB fp32
+ * map pair per segment but the last, and one 64 KiB entry state per segment.
+ * The workspace must be 16-byte aligned; a short one yields
+ * LA_ERR_WORKSPACE.  Its contents need no initialisation and are dead when
+ * the call's work on the stream has finished. */
 size_t la_based_prefill_workspace_size(const la_based_prefill_args* args);
 size_t la_gdn_prefill_workspace_size(const la_gdn_prefill_args* args);
 

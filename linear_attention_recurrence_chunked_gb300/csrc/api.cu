@@ -119,14 +119,17 @@ const char* la_status_string(la_status s) {
   return "unknown status";
 }
 
+// The workspace queries depend on the problem's sizes and dtypes only (no
+// pointer is inspected), so they may be asked before any buffer exists.
 size_t la_based_prefill_workspace_size(const la_based_prefill_args* a) {
-  if (check_based(a) != LA_OK) return 0;
+  (void)a;
   return 0;
 }
 
 size_t la_gdn_prefill_workspace_size(const la_gdn_prefill_args* a) {
-  if (check_gdn(a) != LA_OK) return 0;
-  return 0;
+  if (!a || a->B <= 0 || a->H <= 0 || a->N <= 0 || a->B > kMaxDim || a->H > kMaxDim || a->N > kMaxDim) return 0;
+  if (a->d_k != kGdnD || a->d_v != kGdnD || a->in_dtype != LA_DTYPE_BF16) return 0;  // fp32 path: no scratch
+  return la::gdn_segment_plan(a->B, a->H, a->N).ws_bytes;
 }
 
 la_status la_based_prefill(const la_based_prefill_args* a, void* ws, size_t ws_bytes, void* stream) {
@@ -165,8 +168,10 @@ la_status la_gdn_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes
   const int64_t BH = a->B * a->H;
   if (BH == 0) return LA_OK;
   if (a->N == 0) return pass_state(a->S_out, a->S_in, (size_t)(BH * kGdnD * kGdnD), s);
-  (void)ws;
-  (void)ws_bytes;
+  if (a->in_dtype == LA_DTYPE_BF16) {
+    const size_t need = la::gdn_segment_plan(a->B, a->H, a->N).ws_bytes;
+    if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned16(ws))) return LA_ERR_WORKSPACE;
+  }
   la::GdnPrefillLaunch L{};
   L.B = a->B; L.H = a->H; L.N = a->N;
   L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
@@ -180,7 +185,7 @@ la_status la_gdn_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes
   if (!L.in_bf16) return from_cuda(la::launch_gdn_prefill_recurrent(L, s));
   unsigned* status = device_status_ptr();
   if (!status) return LA_ERR_CUDA;
-  const cudaError_t e = la::launch_gdn_prefill_chunked(L, status, s);
+  const cudaError_t e = la::launch_gdn_prefill_chunked(L, ws, ws_bytes, status, s);
   if (e == cudaErrorInvalidValue) return LA_ERR_UNSUPPORTED;  // strides TMA cannot describe
   return from_cuda(e);
 }

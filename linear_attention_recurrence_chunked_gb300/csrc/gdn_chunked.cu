@@ -21,6 +21,15 @@
 // doubling: 16x16 diagonal blocks by forward substitution, then 32x32 and
 // 64x64 blocks from [[A,0],[C,B]]^-1 = [[A^-1,0],[-B^-1 C A^-1, B^-1]].
 // Two threads share each tensor-memory lane and split its columns.
+//
+// Sequence segments (few (b,h) pairs, long N).  With d_v = d_k a segment
+// acts on the incoming state as an affine map S_end = S_start M + B.  Pass 1
+// runs the same chunk scan over every segment but the last twice, writing no
+// outputs: from S = 0 (its final state is B_g) and from S = I with V taken
+// as zero (the recurrence is then linear in S, so the final state is M_g).
+// A small fp32 kernel chains E_{g+1} = E_g M_g + B_g into every segment's
+// entry state; pass 2 reruns each segment from its entry state and writes
+// the outputs, and the last segment the final state.
 #include <mutex>
 
 #include "common.cuh"
@@ -83,10 +92,22 @@ __device__ __forceinline__ void st_bf16(uint8_t* p, float x) {
   *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
 }
 
+// What one launch computes (see the segment scheme in the file header).
+struct GdnTask {
+  int mode;                 // kWhole, kSegmentMaps or kSegmentOutputs
+  int G;                    // segments per (b,h)
+  int64_t seg_len;          // tokens per segment (a multiple of the chunk)
+  float* maps;              // kSegmentMaps: [BH][G-1][2][128][128]  (B_g, then M_g)
+  const float* states;      // kSegmentOutputs: [BH][G][128][128] entry states
+};
+constexpr int kWhole = 0, kSegmentMaps = 1, kSegmentOutputs = 2;
+constexpr int64_t kStateElems = (int64_t)kD * kD;
+
 template <typename TOut>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                   const __grid_constant__ CUtensorMap tmap_v, const GdnPrefillLaunch a, unsigned* status) {
+                   const __grid_constant__ CUtensorMap tmap_v, const GdnPrefillLaunch a, const GdnTask task,
+                   unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_tma[2];
@@ -97,10 +118,34 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = tid & 127;   // tensor-memory lane owned with the partner thread
   const int half = tid >> 7;   // which half of the lane's columns
-  const int64_t bh = blockIdx.x;
+  // ---- this CTA's (b,h), token range, incoming state, outputs and final state
+  int64_t bh;
+  int seg = 0, which = 0;
+  if (task.mode == kWhole) {
+    bh = blockIdx.x;
+  } else if (task.mode == kSegmentMaps) {
+    const int per = 2 * (task.G - 1);
+    bh = blockIdx.x / per;
+    seg = (int)(blockIdx.x % per) >> 1;
+    which = (int)(blockIdx.x % per) & 1;  // 0: B_g (zero entry state), 1: M_g (identity entry, V taken as 0)
+  } else {
+    bh = blockIdx.x / task.G;
+    seg = (int)(blockIdx.x % task.G);
+  }
   const int b = (int)(bh / a.H), h = (int)(bh % a.H);
-  const int64_t N = a.N;
-  const int nchunks = (int)((N + kC - 1) / kC);
+  const int64_t t_begin = task.mode == kWhole ? 0 : (int64_t)seg * task.seg_len;
+  const int64_t t_end = task.mode == kWhole ? a.N : min(a.N, t_begin + task.seg_len);
+  const int64_t N = t_end;
+  const int nchunks = (int)((t_end - t_begin + kC - 1) / kC);
+  const bool zero_v = task.mode == kSegmentMaps && which == 1;
+  const bool write_out = task.mode != kSegmentMaps;
+  const float* s_entry = task.mode == kWhole ? (a.S_in ? a.S_in + bh * kStateElems : nullptr)
+                         : task.mode == kSegmentOutputs ? task.states + (bh * task.G + seg) * kStateElems
+                                                        : nullptr;
+  float* s_exit = task.mode == kWhole ? a.S_out + bh * kStateElems
+                  : task.mode == kSegmentMaps
+                      ? task.maps + ((bh * (task.G - 1) + seg) * 2 + which) * kStateElems
+                      : (seg == task.G - 1 ? a.S_out + bh * kStateElems : nullptr);
   float* Lsm = reinterpret_cast<float*>(sm + kOffL);
   float* Tsm = reinterpret_cast<float*>(sm + kOffW);
   float* Zsm = reinterpret_cast<float*>(sm + kOffZ);
@@ -137,7 +182,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   auto issue_tma = [&](int c) {
     const uint32_t st = stage(c);
     const uint32_t bar = smem_u32(&bar_tma[c & 1]);
-    const int t0 = c * kC;
+    const int t0 = (int)(t_begin + (int64_t)c * kC);
     mbar_arrive_expect_tx(bar, kStageBytes);
     tma_load_4d(st + kOffKQ + 0, &tmap_k, 0, t0, h, b, bar);
     tma_load_4d(st + kOffKQ + 16384, &tmap_k, 64, t0, h, b, bar);
@@ -159,12 +204,16 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 
   // Initial state: lane i holds row i of S; this thread columns [64 half, 64 half + 64).
   {
-    const float* src = a.S_in ? a.S_in + bh * kD * kD + (int64_t)row * kD + 64 * half : nullptr;
+    const float* src = s_entry ? s_entry + (int64_t)row * kD + 64 * half : nullptr;
     float v[64];
 #pragma unroll
     for (int j = 0; j < 64; j += 4) {
       const float4 x = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
+    }
+    if (zero_v) {  // identity entry state: the run then yields the segment's linear map M_g
+#pragma unroll
+      for (int j = 0; j < 64; ++j) v[j] = (64 * half + j == row) ? 1.f : 0.f;
     }
 #pragma unroll
     for (int c0 = 0; c0 < 64; c0 += 16) tmem_st16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
@@ -172,8 +221,8 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   }
 
   auto load_gates = [&](int c, float& lg, float& bt) {
-    const int64_t t = (int64_t)c * kC + tid;
-    if (tid < kC && c < nchunks && t < N) {
+    const int64_t t = t_begin + (int64_t)c * kC + tid;
+    if (tid < kC && c < nchunks && t < t_end) {
       lg = logf(al_p[t]);
       bt = be_p[t];
     } else {
@@ -336,6 +385,10 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         t2[j] = tv * bt[c0 + j];
         t1[j] = t2[j] * gm[c0 + j];
       }
+      if (zero_v) {  // V taken as zero: U~ = T diag(beta) V = 0
+#pragma unroll
+        for (int j = 0; j < 16; ++j) t2[j] = 0.f;
+      }
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         *reinterpret_cast<uint4*>(sm + kOffT1 + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t1 + 8 * q);
@@ -409,8 +462,8 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   // ---------------------------------------------------------------- main loop: chain of chunk c, intra of c+1
   for (int c = 0; c < nchunks; ++c) {
     const bool has_next = c + 1 < nchunks;
-    const int64_t t0 = (int64_t)c * kC;
-    const int nvalid = (N - t0 < kC) ? (int)(N - t0) : kC;
+    const int64_t t0 = t_begin + (int64_t)c * kC;
+    const int nvalid = (N - t0 < kC) ? (int)(N - t0) : kC;  // tokens of this chunk inside [t_begin, t_end)
     if (has_next) phase_gates(c + 1);
     if (tid == 0 && has_next) wait_tma(c + 1);
     if (__syncthreads_or(!ok)) break;
@@ -517,11 +570,13 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       tmem_ld_wait();
       const int r0 = 32 * half;
       const float* gm = gam(c);
-      TOut* optr = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + (t0 + r0) * a.o_st + row;
+      if (write_out) {
+        TOut* optr = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + (t0 + r0) * a.o_st + row;
 #pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        if (r0 + r < nvalid) store1(optr, a.q_scale * fmaf(gm[r0 + r], y[r], p[r]));
-        optr += a.o_st;
+        for (int r = 0; r < 32; ++r) {
+          if (r0 + r < nvalid) store1(optr, a.q_scale * fmaf(gm[r0 + r], y[r], p[r]));
+          optr += a.o_st;
+        }
       }
       if (has_next) {
 #pragma unroll
@@ -543,16 +598,16 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   }
 
 done:
-  if (ok) {
+  if (ok && s_exit) {
     // final state: lane i row i, this thread columns [64 half, 64 half + 64)
-    float* dst = a.S_out + bh * kD * kD + (int64_t)row * kD + 64 * half;
+    float* dst = s_exit + (int64_t)row * kD + 64 * half;
     float v[64];
 #pragma unroll
     for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tlane + kColS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
     tmem_ld_wait();
 #pragma unroll
     for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-  } else if (tid == 0) {
+  } else if (!ok && tid == 0) {
     // a wait expired: let this CTA's own copies and MMAs drain (bounded) before freeing TMEM
     for (int k = tma_waited; k < tma_issued; ++k) mbar_wait(smem_u32(&bar_tma[k & 1]), (uint32_t)((k >> 1) & 1), status);
     if (mma_pending) mbar_wait(smem_u32(&bar_mma), mma_phase, status);
@@ -560,6 +615,61 @@ done:
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ----------------------------------------------------------------------------- segment combine
+// Entry states of the segments of one (b,h): E_0 = S_in (or 0),
+// E_{g+1} = E_g M_g + B_g, in fp32 on the CUDA cores.  M_g and E_g are staged
+// in shared memory; thread t owns 64 columns of row t/2.
+constexpr int kCombineThreads = 256;
+constexpr int kEStride = kD + 1;  // padded rows: conflict-free column reads
+constexpr size_t kCombineSmem = (size_t)kD * kEStride * 4 + (size_t)kD * kD * 4;
+
+__global__ void __launch_bounds__(kCombineThreads)
+gdn_segment_combine_kernel(const float* S_in, const float* maps, float* states, int G) {
+  extern __shared__ float cs[];
+  float* E = cs;                    // [128][129]
+  float* M = cs + kD * kEStride;    // [128][128]
+  const int64_t bh = blockIdx.x;
+  const int tid = threadIdx.x, i = tid >> 1, k0 = (tid & 1) * 64;
+  float* out0 = states + bh * G * kStateElems;
+  for (int e = tid; e < kD * kD; e += kCombineThreads) {
+    const float x = S_in ? S_in[bh * kStateElems + e] : 0.f;
+    E[(e >> 7) * kEStride + (e & 127)] = x;
+    out0[e] = x;
+  }
+  for (int g = 0; g + 1 < G; ++g) {
+    const float* Bg = maps + ((bh * (G - 1) + g) * 2 + 0) * kStateElems;
+    const float* Mg = maps + ((bh * (G - 1) + g) * 2 + 1) * kStateElems;
+    __syncthreads();
+    for (int e = tid * 4; e < kD * kD; e += kCombineThreads * 4)
+      *reinterpret_cast<float4*>(M + e) = *reinterpret_cast<const float4*>(Mg + e);
+    __syncthreads();
+    float acc[64];
+#pragma unroll
+    for (int j = 0; j < 64; j += 4) {
+      const float4 bb = *reinterpret_cast<const float4*>(Bg + i * kD + k0 + j);
+      acc[j] = bb.x; acc[j + 1] = bb.y; acc[j + 2] = bb.z; acc[j + 3] = bb.w;
+    }
+#pragma unroll 2
+    for (int m = 0; m < kD; ++m) {
+      const float e = E[i * kEStride + m];
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        const float4 mm = *reinterpret_cast<const float4*>(M + m * kD + k0 + j);
+        acc[j] = fmaf(e, mm.x, acc[j]);
+        acc[j + 1] = fmaf(e, mm.y, acc[j + 1]);
+        acc[j + 2] = fmaf(e, mm.z, acc[j + 2]);
+        acc[j + 3] = fmaf(e, mm.w, acc[j + 3]);
+      }
+    }
+    __syncthreads();
+    float* outg = states + (bh * G + g + 1) * kStateElems + i * kD + k0;
+#pragma unroll
+    for (int j = 0; j < 64; ++j) E[i * kEStride + k0 + j] = acc[j];
+#pragma unroll
+    for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(outg + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+  }
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -595,7 +705,7 @@ bool make_map(CUtensorMap* m, const View4& x, int64_t B, int64_t H, int64_t N) {
 }
 
 template <typename TOut>
-cudaError_t launch_typed(const GdnPrefillLaunch& a, unsigned* status, cudaStream_t stream) {
+cudaError_t launch_typed(const GdnPrefillLaunch& a, void* ws, unsigned* status, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   // strides of 0 (broadcast views) or not multiples of 16 bytes cannot be described
   if (!make_map(&mq, a.q, a.B, a.H, a.N) || !make_map(&mk, a.k, a.B, a.H, a.N) || !make_map(&mv, a.v, a.B, a.H, a.N))
@@ -605,17 +715,72 @@ cudaError_t launch_typed(const GdnPrefillLaunch& a, unsigned* status, cudaStream
   std::call_once(attr_once, [] {
     attr_err = cudaFuncSetAttribute(gdn_chunked_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kSmemAlloc);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(gdn_segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kCombineSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  gdn_chunked_kernel<TOut><<<(unsigned)(a.B * a.H), kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, status);
+  const GdnSegPlan plan = gdn_segment_plan(a.B, a.H, a.N);
+  const int64_t BH = a.B * a.H;
+  if (plan.G == 1) {
+    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr};
+    gdn_chunked_kernel<TOut><<<(unsigned)BH, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, task, status);
+    return cudaGetLastError();
+  }
+  float* maps = static_cast<float*>(ws);
+  float* states = maps + BH * (plan.G - 1) * 2 * kStateElems;
+  const GdnTask t1{kSegmentMaps, plan.G, plan.seg_len, maps, nullptr};
+  gdn_chunked_kernel<TOut><<<(unsigned)(BH * (plan.G - 1) * 2), kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, t1,
+                                                                                               status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  gdn_segment_combine_kernel<<<(unsigned)BH, kCombineThreads, kCombineSmem, stream>>>(a.S_in, maps, states, plan.G);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const GdnTask t2{kSegmentOutputs, plan.G, plan.seg_len, nullptr, states};
+  gdn_chunked_kernel<TOut><<<(unsigned)(BH * plan.G), kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, t2, status);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gdn_prefill_chunked(const GdnPrefillLaunch& a, unsigned* status, cudaStream_t stream) {
+// Number of sequence segments per (b,h).  With one CTA per SM, the three
+// launches cost about ceil(2 (G-1) BH / P) + ceil(G BH / P) waves of a
+// segment's length (P = 148 SMs assumed, so the plan does not depend on the
+// device), against ceil(BH / P) waves of the whole sequence for G = 1;
+// segments are used when they save at least 20 %, keep at least 32 chunks
+// each, and G stays <= 16 (the combine is sequential in G).
+GdnSegPlan gdn_segment_plan(int64_t B, int64_t H, int64_t N) {
+  GdnSegPlan p{1, N, 0};
+  const int64_t BH = B * H;
+  const int64_t nchunks = (N + kC - 1) / kC;
+  if (BH <= 0 || N <= 0) return p;
+  constexpr int64_t P = 148, kMinSegChunks = 32, kMaxG = 16;
+  auto waves = [&](int64_t ctas) { return (ctas + P - 1) / P; };
+  double best = (double)waves(BH);
+  int64_t bestG = 1;
+  for (int64_t G = 2; G <= kMaxG && G * kMinSegChunks <= nchunks; ++G) {
+    const double cost = (double)(waves(2 * (G - 1) * BH) + waves(G * BH)) / (double)G;
+    if (cost < 0.8 * best && (bestG == 1 || cost < best)) {
+      best = cost;
+      bestG = G;
+    }
+  }
+  if (bestG == 1) return p;
+  const int64_t seg_chunks = (nchunks + bestG - 1) / bestG;
+  p.G = (int)((nchunks + seg_chunks - 1) / seg_chunks);
+  p.seg_len = seg_chunks * kC;
+  p.ws_bytes = (size_t)(BH * (p.G - 1) * 2 + BH * p.G) * kStateElems * sizeof(float);
+  if (p.G == 1) p.ws_bytes = 0;
+  return p;
+}
+
+cudaError_t launch_gdn_prefill_chunked(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* status,
+                                       cudaStream_t stream) {
   if (a.B * a.H == 0 || a.N == 0) return cudaSuccess;
-  return a.out_bf16 ? launch_typed<__nv_bfloat16>(a, status, stream) : launch_typed<float>(a, status, stream);
+  const GdnSegPlan plan = gdn_segment_plan(a.B, a.H, a.N);
+  if (plan.G > 1 && (ws == nullptr || ws_bytes < plan.ws_bytes)) return cudaErrorInvalidValue;
+  return a.out_bf16 ? launch_typed<__nv_bfloat16>(a, ws, status, stream) : launch_typed<float>(a, ws, status, stream);
 }
 
 }  // namespace la

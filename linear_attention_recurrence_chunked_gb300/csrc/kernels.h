@@ -51,13 +51,23 @@ struct GdnPrefillLaunch {
   float* S_out;
 };
 
+// Sequence-segment plan of the gated-delta-rule prefill (see gdn_chunked.cu):
+// G segments of seg_len tokens per (b,h); G == 1 runs the plain chunk scan.
+struct GdnSegPlan {
+  int G;
+  int64_t seg_len;
+  size_t ws_bytes;  // workspace: segment maps then segment entry states
+};
+GdnSegPlan gdn_segment_plan(int64_t B, int64_t H, int64_t N);
+
 cudaError_t launch_gdn_decode(const DecodeLaunch& a, cudaStream_t stream);
 cudaError_t launch_taylor_decode(const DecodeLaunch& a, cudaStream_t stream);
 // fp32 inputs: token-serial CUDA-core kernels (fp32 arithmetic throughout).
 cudaError_t launch_taylor_prefill_recurrent(const TaylorPrefillLaunch& a, cudaStream_t stream);
 cudaError_t launch_gdn_prefill_recurrent(const GdnPrefillLaunch& a, cudaStream_t stream);
 // bf16 inputs: chunked tcgen05 kernels.
-cudaError_t launch_gdn_prefill_chunked(const GdnPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
+cudaError_t launch_gdn_prefill_chunked(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* dev_status,
+                                       cudaStream_t stream);
 cudaError_t launch_taylor_prefill_chunked(const TaylorPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(int arrive, uint64_t limit_ns, unsigned* dev_status, cudaStream_t stream);
 

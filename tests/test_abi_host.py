@@ -139,3 +139,16 @@ def test_decode_rejections(lib):
     assert call(mk(alpha=None)) == la.LA_ERR_INVALID_ARGUMENT
     assert call(mk(state=0x70004)) == la.LA_ERR_INVALID_ARGUMENT
     assert call(mk(S=0)) == la.LA_OK
+
+
+def test_gdn_segment_workspace_query_and_rejection(lib):
+    # few heads and a long sequence plan sequence segments, which need scratch
+    a = gdn_args(B=1, H=16, N=1 << 20)
+    need = lib.la_gdn_prefill_workspace_size(ctypes.byref(a))
+    assert need > 0
+    # short sequences or many heads need none
+    assert lib.la_gdn_prefill_workspace_size(ctypes.byref(gdn_args(B=4, H=16, N=16384))) == 0
+    assert lib.la_gdn_prefill_workspace_size(ctypes.byref(gdn_args(B=1, H=2, N=64))) == 0
+    # a missing or short workspace is rejected on the host, before any launch
+    assert lib.la_gdn_prefill(ctypes.byref(a), None, 0, None) == la.LA_ERR_WORKSPACE
+    assert lib.la_gdn_prefill(ctypes.byref(a), ctypes.c_void_p(0x100000), need - 16, None) == la.LA_ERR_WORKSPACE

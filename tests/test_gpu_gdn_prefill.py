@@ -142,3 +142,32 @@ def test_gdn_prefill_long_context_full_size():
     assert rel_err(to_np(S[:, heads]), ref["S"]) < tol
     del inp, o
     assert la.la_device_status() == la.LA_OK
+
+
+def _slow_decay(inp, seed):
+    """alpha close to 1 (exp(-U(0.001, 0.002))): a 2048-token segment keeps a
+    sizeable part of its entry state, so the segment maps are far from zero."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.rand(inp["alpha"].shape, generator=g)
+    inp = dict(inp)
+    inp["alpha"] = torch.exp(-(0.001 + 0.001 * u)).contiguous()
+    return inp
+
+
+@pytest.mark.parametrize("N,inplace", [(6144, False), (7990, True)])
+def test_gdn_sequence_segments_match_oracle(N, inplace):
+    """Few heads and a long sequence take the segment path (maps per segment,
+    a combine, then all segments in parallel); results must match the oracle."""
+    dev = cuda_device()
+    inp = _slow_decay(synthetic.gdn_inputs(1, 2, N, dtype=torch.bfloat16, seed=300 + N), seed=N)
+    x = {n: inp[n].to(dev) for n in NAMES}
+    assert la.la_gdn_prefill_workspace_size(*(x[n] for n in NAMES)) > 0, "expected the segment path"
+    S_in = (torch.randn((1, 2, 128, 128), generator=torch.Generator().manual_seed(9)) * 0.1)
+    S_dev = S_in.to(dev).contiguous()
+    o, S = la.la_gdn_prefill(*(x[n] for n in NAMES), S_in=S_dev, S_out=S_dev if inplace else None)
+    torch.cuda.synchronize()
+    ref = oracle_ref(inp, S_in=S_in)
+    tol = TOL[torch.bfloat16]
+    assert rel_err(to_np(o), ref["o"]) < tol
+    assert rel_err(to_np(S), ref["S"]) < tol
+    assert la.la_device_status() == la.LA_OK
