@@ -158,6 +158,29 @@ la_status la_based_prefill(const la_based_prefill_args* args, void* workspace,
 la_status la_gdn_prefill(const la_gdn_prefill_args* args, void* workspace,
                          size_t workspace_bytes, void* stream);
 
+/* la_gdn_prefill for callers that cannot allocate device memory (the pages
+ * have no counterpart; this is an interface convenience).  Some callers have
+ * no workspace to hand over: a plug-in inside a host framework that owns all
+ * device memory and forbids its plug-ins to allocate, an engine that reserved
+ * its whole memory budget up front, or a latency-critical loop that must not
+ * pay the implicit device-wide synchronisation of cudaMalloc/cudaFree.  This
+ * entry point computes exactly what la_gdn_prefill computes, but takes its
+ * scratch from a fixed 16 MiB array in the library's own device memory, so it
+ * calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Limit: problems whose la_gdn_prefill_workspace_size exceeds 16 MiB
+ *     (16777216 bytes) are refused with LA_ERR_WORKSPACE before anything is
+ *     launched; problems that need no scratch always run.
+ *   - Every GPU that loads the library holds the 16 MiB array until the
+ *     process exits.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it needs to start at zero).  Calls whose GPU work overlaps,
+ *     e.g. on two streams at once, race on it: serialise them.
+ * Arguments, validation and other errors as for la_gdn_prefill. */
+la_status la_gdn_prefill_noalloc(const la_gdn_prefill_args* args, void* stream);
+
 /* One recurrent decode step (NoteBank Eq. (1) for one token; BASED notes
  * Sec. 2.5: the decode step fuses the outer-product write with the query
  * readout and still reads and writes the whole persistent state). */

@@ -69,8 +69,8 @@ class DecodeArgs(ctypes.Structure):
 
 
 EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_decode_step", "la_based_prefill_workspace_size",
-            "la_gdn_prefill_workspace_size", "la_device_status", "la_selftest_bounded_wait", "la_status_string",
-            "la_abi_version")
+            "la_gdn_prefill_workspace_size", "la_gdn_prefill_noalloc", "la_device_status",
+            "la_selftest_bounded_wait", "la_status_string", "la_abi_version")
 
 
 class LAError(RuntimeError):
@@ -100,6 +100,8 @@ def load_library(path: str | None = None):
     lib.la_based_prefill.argtypes = [ctypes.POINTER(BasedPrefillArgs), vp, ctypes.c_size_t, vp]
     lib.la_gdn_prefill.restype = ctypes.c_int
     lib.la_gdn_prefill.argtypes = [ctypes.POINTER(GdnPrefillArgs), vp, ctypes.c_size_t, vp]
+    lib.la_gdn_prefill_noalloc.restype = ctypes.c_int
+    lib.la_gdn_prefill_noalloc.argtypes = [ctypes.POINTER(GdnPrefillArgs), vp]
     lib.la_decode_step.restype = ctypes.c_int
     lib.la_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), vp]
     lib.la_based_prefill_workspace_size.restype = ctypes.c_size_t
@@ -263,6 +265,20 @@ def la_gdn_prefill(q, k, v, alpha, beta, o=None, S_in=None, S_out=None, q_scale:
                             _stream_handle(stream))
     if st != LA_OK:
         raise LAError(st, "la_gdn_prefill")
+    return o, S_out
+
+
+def la_gdn_prefill_noalloc(q, k, v, alpha, beta, o, S_out, S_in=None, q_scale: float = 1.0, stream=None):
+    """la_gdn_prefill without a workspace, for callers that cannot allocate:
+    the library's fixed 16 MiB device array serves as scratch (see
+    include/la.h).  o and S_out must be preallocated by the caller.
+    Returns (o, S_out)."""
+    lib = load_library()
+    _check_cuda(q, k, v, alpha, beta, o, S_in, S_out)
+    a = _gdn_args(q, k, v, o, alpha, beta, S_in, S_out, q_scale)
+    st = lib.la_gdn_prefill_noalloc(ctypes.byref(a), _stream_handle(stream))
+    if st != LA_OK:
+        raise LAError(st, "la_gdn_prefill_noalloc")
     return o, S_out
 
 
