@@ -307,7 +307,7 @@ def gpu_arm(args, ws, rank, local):
     return line
 
 
-KERNELS_PER_CALL = {"based_prefill": 1, "gdn_prefill": 1, "decode": 1}
+KERNELS_PER_CALL = {"based_prefill": 1, "gdn_prefill": 2, "decode": 1}
 
 
 PATH_NAMES = ("gdn_prefill", "gdn_prefill_long", "decode_gdn", "decode_taylor")
@@ -340,8 +340,10 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         for _ in range(reps):
             t.run(step)
         ms = max_over_ranks(t.total_ms(), ws) / reps
-        # a call that splits the sequence into segments runs three kernels (maps, combine, outputs)
-        per_call = 3 if ws_t.numel() > 1 else KERNELS_PER_CALL["gdn_prefill"]
+        # the chunk-local kernel, then the chain; sequences split into segments run the chain as
+        # three kernels (maps, combine, outputs)
+        segments = la.la_gdn_prefill_workspace_size_min(x["q"], x["k"], x["v"], x["alpha"], x["beta"]) > 0
+        per_call = 4 if segments else KERNELS_PER_CALL["gdn_prefill"]
         launches += reps * per_call
         byts = BYTES_PER_TOKEN_HEAD["gdn_prefill"] * w.B * w.H * w.N + STATE_BYTES["gdn"] * w.B * w.H
         r = roofline(byts, ms, pk["hbm_gbs"], ncu_traffic(name))

@@ -137,16 +137,30 @@ typedef struct la_decode_args {
 } la_decode_args;
 
 /* Bytes of device workspace the matching prefill call needs for `args`
- * (0 = none; a NULL workspace is then accepted).  Pure host function of the
- * sizes and dtypes in `args` (no pointer is read), so it can be asked before
- * any buffer is allocated.  The gated-delta-rule prefill needs scratch when
- * it splits long sequences of few (b,h) pairs into segments: one 64 KiB fp32
- * map pair per segment but the last, and one 64 KiB entry state per segment.
- * The workspace must be 16-byte aligned; a short one yields
- * LA_ERR_WORKSPACE.  Its contents need no initialisation and are dead when
- * the call's work on the stream has finished. */
+ * (0 = none; a NULL workspace is then accepted).  Pure host functions of the
+ * sizes and dtypes in `args` (no pointer is read), so they can be asked
+ * before any buffer is allocated.  The workspace must be 16-byte aligned;
+ * its contents need no initialisation and are dead when the call's work on
+ * the stream has finished.
+ *
+ * Gated-delta-rule prefill (bf16 inputs) has two schedules:
+ *   - two kernels (the fastest): a chunk-parallel kernel leaves one record
+ *     of 74,240 bytes per 64-token chunk of every (b,h) (W, the decayed
+ *     queries, P_o, the decay tables and U~ of the chunk), then a sequential
+ *     chain per (b,h) consumes them; la_gdn_prefill_workspace_size returns
+ *     what it needs;
+ *   - one kernel that walks the chunks of each (b,h) itself; it needs scratch
+ *     only when it splits long sequences of few (b,h) pairs into segments
+ *     (one 64 KiB fp32 map pair per segment but the last, one 64 KiB entry
+ *     state per segment); la_gdn_prefill_workspace_size_min returns that
+ *     (often 0).
+ * la_gdn_prefill runs the two-kernel schedule when the workspace holds at
+ * least la_gdn_prefill_workspace_size bytes, else the one-kernel schedule
+ * when it holds at least la_gdn_prefill_workspace_size_min bytes, else fails
+ * with LA_ERR_WORKSPACE.  Both compute the same result up to rounding. */
 size_t la_based_prefill_workspace_size(const la_based_prefill_args* args);
 size_t la_gdn_prefill_workspace_size(const la_gdn_prefill_args* args);
+size_t la_gdn_prefill_workspace_size_min(const la_gdn_prefill_args* args);
 
 /* Chunked Taylor prefill (BASED notes Sec. 2.2 and Sec. 2.5: the block
  * decomposition U_b = (M_b . Phi_Qb Phi_Kb^T) V_b + Phi_Qb S_{<b}). */
@@ -167,9 +181,11 @@ la_status la_gdn_prefill(const la_gdn_prefill_args* args, void* workspace,
  * entry point computes exactly what la_gdn_prefill computes, but takes its
  * scratch from a fixed 16 MiB array in the library's own device memory, so it
  * calls no cudaMalloc, cudaFree or other allocating routine.
- *   - Limit: problems whose la_gdn_prefill_workspace_size exceeds 16 MiB
- *     (16777216 bytes) are refused with LA_ERR_WORKSPACE before anything is
- *     launched; problems that need no scratch always run.
+ *   - Limit: problems whose la_gdn_prefill_workspace_size_min exceeds
+ *     16 MiB (16777216 bytes) are refused with LA_ERR_WORKSPACE before
+ *     anything is launched; problems that need no scratch always run.  The
+ *     two-kernel schedule runs when its records fit the array, otherwise
+ *     the one-kernel schedule.
  *   - Every GPU that loads the library holds the 16 MiB array until the
  *     process exits.
  *   - The first call on each device looks up the array's device address

@@ -69,7 +69,7 @@ class DecodeArgs(ctypes.Structure):
 
 
 EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_decode_step", "la_based_prefill_workspace_size",
-            "la_gdn_prefill_workspace_size", "la_gdn_prefill_noalloc", "la_device_status",
+            "la_gdn_prefill_workspace_size", "la_gdn_prefill_workspace_size_min", "la_gdn_prefill_noalloc", "la_device_status",
             "la_selftest_bounded_wait", "la_status_string", "la_abi_version")
 
 
@@ -108,6 +108,8 @@ def load_library(path: str | None = None):
     lib.la_based_prefill_workspace_size.argtypes = [ctypes.POINTER(BasedPrefillArgs)]
     lib.la_gdn_prefill_workspace_size.restype = ctypes.c_size_t
     lib.la_gdn_prefill_workspace_size.argtypes = [ctypes.POINTER(GdnPrefillArgs)]
+    lib.la_gdn_prefill_workspace_size_min.restype = ctypes.c_size_t
+    lib.la_gdn_prefill_workspace_size_min.argtypes = [ctypes.POINTER(GdnPrefillArgs)]
     lib.la_device_status.restype = ctypes.c_int
     lib.la_device_status.argtypes = [vp, ctypes.c_int]
     lib.la_selftest_bounded_wait.restype = ctypes.c_int
@@ -241,12 +243,22 @@ def la_gdn_prefill_workspace_size(q, k, v, alpha, beta, o=None) -> int:
     return int(load_library().la_gdn_prefill_workspace_size(ctypes.byref(a)))
 
 
+def la_gdn_prefill_workspace_size_min(q, k, v, alpha, beta, o=None) -> int:
+    """Smallest workspace la_gdn_prefill accepts (selects the one-kernel schedule)."""
+    o = o if o is not None else v
+    a = _gdn_args(q, k, v, o, alpha, beta, None, None, 1.0)
+    return int(load_library().la_gdn_prefill_workspace_size_min(ctypes.byref(a)))
+
+
 def la_gdn_prefill(q, k, v, alpha, beta, o=None, S_in=None, S_out=None, q_scale: float = 1.0,
                    out_dtype=None, workspace=None, stream=None):
     """Chunked gated-delta-rule prefill.  Returns (o, S_out).
 
     q, k, v: [B,H,N,128] (fp32 or bf16); alpha, beta: fp32 [B,H,N];
-    S: fp32 [B,H,128,128] (row = value index)."""
+    S: fp32 [B,H,128,128] (row = value index).  workspace: optional uint8
+    device tensor; by default la_gdn_prefill_workspace_size bytes are
+    allocated (two-kernel schedule); a smaller one of at least
+    la_gdn_prefill_workspace_size_min bytes selects the one-kernel schedule."""
     lib = load_library()
     _check_cuda(q, k, v, alpha, beta, o, S_in, S_out)
     B, H, N, _ = q.shape

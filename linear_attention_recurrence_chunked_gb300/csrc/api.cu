@@ -126,10 +126,18 @@ size_t la_based_prefill_workspace_size(const la_based_prefill_args* a) {
   return 0;
 }
 
+// bf16 GDN problems the chunked kernels take (the fp32 path needs no scratch)
+static bool gdn_chunked_shape(const la_gdn_prefill_args* a) {
+  if (!a || a->B <= 0 || a->H <= 0 || a->N <= 0 || a->B > kMaxDim || a->H > kMaxDim || a->N > kMaxDim) return false;
+  return a->d_k == kGdnD && a->d_v == kGdnD && a->in_dtype == LA_DTYPE_BF16;
+}
+
 size_t la_gdn_prefill_workspace_size(const la_gdn_prefill_args* a) {
-  if (!a || a->B <= 0 || a->H <= 0 || a->N <= 0 || a->B > kMaxDim || a->H > kMaxDim || a->N > kMaxDim) return 0;
-  if (a->d_k != kGdnD || a->d_v != kGdnD || a->in_dtype != LA_DTYPE_BF16) return 0;  // fp32 path: no scratch
-  return la::gdn_segment_plan(a->B, a->H, a->N).ws_bytes;
+  return gdn_chunked_shape(a) ? la::gdn_split_workspace_bytes(a->B, a->H, a->N) : 0;
+}
+
+size_t la_gdn_prefill_workspace_size_min(const la_gdn_prefill_args* a) {
+  return gdn_chunked_shape(a) ? la::gdn_segment_plan(a->B, a->H, a->N).ws_bytes : 0;
 }
 
 la_status la_based_prefill(const la_based_prefill_args* a, void* ws, size_t ws_bytes, void* stream) {
@@ -168,9 +176,15 @@ la_status la_gdn_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes
   const int64_t BH = a->B * a->H;
   if (BH == 0) return LA_OK;
   if (a->N == 0) return pass_state(a->S_out, a->S_in, (size_t)(BH * kGdnD * kGdnD), s);
+  // bf16: the two-kernel split when the workspace holds its chunk records,
+  // else the single-kernel scan, which needs the segment scratch only
+  bool split = false;
   if (a->in_dtype == LA_DTYPE_BF16) {
-    const size_t need = la::gdn_segment_plan(a->B, a->H, a->N).ws_bytes;
-    if (need > 0 && (ws == nullptr || ws_bytes < need || !aligned16(ws))) return LA_ERR_WORKSPACE;
+    if (ws != nullptr && !aligned16(ws)) return LA_ERR_WORKSPACE;
+    const int64_t nch = (a->N + 63) / 64;
+    split = ws != nullptr && ws_bytes >= la::gdn_split_workspace_bytes(a->B, a->H, a->N) && BH * nch <= INT32_MAX;
+    const size_t need_min = la::gdn_segment_plan(a->B, a->H, a->N).ws_bytes;
+    if (!split && need_min > 0 && (ws == nullptr || ws_bytes < need_min)) return LA_ERR_WORKSPACE;
   }
   la::GdnPrefillLaunch L{};
   L.B = a->B; L.H = a->H; L.N = a->N;
@@ -185,7 +199,8 @@ la_status la_gdn_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes
   if (!L.in_bf16) return from_cuda(la::launch_gdn_prefill_recurrent(L, s));
   unsigned* status = device_status_ptr();
   if (!status) return LA_ERR_CUDA;
-  const cudaError_t e = la::launch_gdn_prefill_chunked(L, ws, ws_bytes, status, s);
+  const cudaError_t e = split ? la::launch_gdn_prefill_split(L, ws, ws_bytes, status, s)
+                              : la::launch_gdn_prefill_chunked(L, ws, ws_bytes, status, s);
   if (e == cudaErrorInvalidValue) return LA_ERR_UNSUPPORTED;  // strides TMA cannot describe
   return from_cuda(e);
 }

@@ -32,17 +32,12 @@
 // the outputs, and the last segment the final state.
 #include <mutex>
 
-#include "common.cuh"
-#include "kernels.h"
-#include "tc.cuh"
+#include "gdn_common.cuh"
 
 namespace la {
 namespace {
 using namespace tc;
-
-constexpr int kC = 64;        // tokens per chunk
-constexpr int kD = 128;       // d_k = d_v
-constexpr int kThreads = 256;  // two threads per tensor-memory lane, splitting its columns
+using namespace gdn;
 
 // shared memory map, offsets from a 1024-byte aligned base
 constexpr uint32_t kStageBytes = 49152;   // [K;Q] tile [128][128] bf16 (32 KB) + V [64][128] (16 KB)
@@ -63,8 +58,6 @@ constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
 // after), T in fp32 in the W tile (read by MMA 3 before, rewritten after).
 constexpr uint32_t kOffL = kOffS0;                // fp32 L [64][65]
 constexpr uint32_t kOffZ = kOffL + 64 * 65 * 4;   // fp32 block products (4 KB)
-constexpr int kLStride = 65;
-constexpr int kTStride = 64;
 static_assert(64 * 65 * 4 + 1024 * 4 <= 32768, "L/Z scratch exceeds the S0 tile");
 static_assert(64 * kTStride * 4 <= 16384, "T scratch exceeds the W tile");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
@@ -79,30 +72,6 @@ constexpr uint32_t kColY = 384;   // (Q S0^T)^T [i][r]
 constexpr uint32_t kColPU = 448;  // (P_o U)^T [i][r]
 constexpr uint32_t kTmemCols = 512;
 
-__device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sw128_desc(addr, 0, 1024); }
-
-// 32 consecutive TMEM columns of this thread's lane, one wait.
-__device__ __forceinline__ void ld32(uint32_t taddr, float* v) {
-  tmem_ld16(taddr, *reinterpret_cast<float(*)[16]>(v));
-  tmem_ld16(taddr + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-  tmem_ld_wait();
-}
-
-__device__ __forceinline__ void st_bf16(uint8_t* p, float x) {
-  *reinterpret_cast<__nv_bfloat16*>(p) = __float2bfloat16_rn(x);
-}
-
-// What one launch computes (see the segment scheme in the file header).
-struct GdnTask {
-  int mode;                 // kWhole, kSegmentMaps or kSegmentOutputs
-  int G;                    // segments per (b,h)
-  int64_t seg_len;          // tokens per segment (a multiple of the chunk)
-  float* maps;              // kSegmentMaps: [BH][G-1][2][128][128]  (B_g, then M_g)
-  const float* states;      // kSegmentOutputs: [BH][G][128][128] entry states
-};
-constexpr int kWhole = 0, kSegmentMaps = 1, kSegmentOutputs = 2;
-constexpr int64_t kStateElems = (int64_t)kD * kD;
-
 template <typename TOut>
 __global__ void __launch_bounds__(kThreads, 1)
 gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -115,37 +84,17 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   __shared__ uint32_t tmem_base_sh;
   __shared__ float warp0_total;
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int row = tid & 127;   // tensor-memory lane owned with the partner thread
   const int half = tid >> 7;   // which half of the lane's columns
-  // ---- this CTA's (b,h), token range, incoming state, outputs and final state
-  int64_t bh;
-  int seg = 0, which = 0;
-  if (task.mode == kWhole) {
-    bh = blockIdx.x;
-  } else if (task.mode == kSegmentMaps) {
-    const int per = 2 * (task.G - 1);
-    bh = blockIdx.x / per;
-    seg = (int)(blockIdx.x % per) >> 1;
-    which = (int)(blockIdx.x % per) & 1;  // 0: B_g (zero entry state), 1: M_g (identity entry, V taken as 0)
-  } else {
-    bh = blockIdx.x / task.G;
-    seg = (int)(blockIdx.x % task.G);
-  }
-  const int b = (int)(bh / a.H), h = (int)(bh % a.H);
-  const int64_t t_begin = task.mode == kWhole ? 0 : (int64_t)seg * task.seg_len;
-  const int64_t t_end = task.mode == kWhole ? a.N : min(a.N, t_begin + task.seg_len);
+  const CtaWork wk = cta_work(a, task);
+  const int b = wk.b, h = wk.h;
+  const int64_t t_begin = wk.t_begin, t_end = wk.t_end;
   const int64_t N = t_end;
-  const int nchunks = (int)((t_end - t_begin + kC - 1) / kC);
-  const bool zero_v = task.mode == kSegmentMaps && which == 1;
-  const bool write_out = task.mode != kSegmentMaps;
-  const float* s_entry = task.mode == kWhole ? (a.S_in ? a.S_in + bh * kStateElems : nullptr)
-                         : task.mode == kSegmentOutputs ? task.states + (bh * task.G + seg) * kStateElems
-                                                        : nullptr;
-  float* s_exit = task.mode == kWhole ? a.S_out + bh * kStateElems
-                  : task.mode == kSegmentMaps
-                      ? task.maps + ((bh * (task.G - 1) + seg) * 2 + which) * kStateElems
-                      : (seg == task.G - 1 ? a.S_out + bh * kStateElems : nullptr);
+  const int nchunks = wk.nchunks;
+  const bool zero_v = wk.zero_v, write_out = wk.write_out;
+  const float* s_entry = wk.s_entry;
+  float* s_exit = wk.s_exit;
   float* Lsm = reinterpret_cast<float*>(sm + kOffL);
   float* Tsm = reinterpret_cast<float*>(sm + kOffW);
   float* Zsm = reinterpret_cast<float*>(sm + kOffZ);
@@ -154,7 +103,6 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   const float* be_p = a.beta + b * a.b_sb + h * a.b_sh;
   // per-chunk gate tables, double-buffered by chunk parity
   auto gsm = [&](int c) { return reinterpret_cast<float*>(sm + kOffGate + (c & 1) * 1024); };  // g_r
-  auto bsm = [&](int c) { return gsm(c) + kC; };      // beta_r
   auto gam = [&](int c) { return gsm(c) + 2 * kC; };  // gamma_r = e^{g_r}
   auto gin = [&](int c) { return gsm(c) + 3 * kC; };  // 1 / gamma_r
   auto stage = [&](int c) { return sbase + (uint32_t)(c & 1) * kStageBytes; };
@@ -242,23 +190,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   auto phase_gates = [&](int cc) {
     const float lg = lg_next, bt = bt_next;
     load_gates(cc + 1, lg_next, bt_next);
-    float gx = lg;
-    if (tid < kC) {
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float y = __shfl_up_sync(kFullMask, gx, off);
-        if (lane >= off) gx += y;
-      }
-      if (tid == 31) warp0_total = gx;
-    }
-    __syncthreads();
-    if (tid < kC) {
-      if (warp == 1) gx += warp0_total;
-      gsm(cc)[tid] = gx;
-      bsm(cc)[tid] = bt;
-      gam(cc)[tid] = __expf(gx);
-      gin(cc)[tid] = __expf(-gx);
-    }
+    gate_tables(tid, lg, bt, gsm(cc), &warp0_total);
   };
   auto wait_tma = [&](int cc) {
     ok = ok && mbar_wait(smem_u32(&bar_tma[cc & 1]), (uint32_t)((cc >> 1) & 1), status);
@@ -269,144 +201,14 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
     mma_phase ^= 1;
     mma_pending = !ok;
   };
-  auto mma_kq = [&](int cc) {  // [K;Q] K^T of chunk cc -> KQ
-    const uint32_t st = stage(cc);
-    const uint32_t id = idesc_bf16(128, 64, 0, 0);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-      mma_bf16(tmem + kColKQ, kmaj(st + kOffKQ + koff), kmaj(st + kOffKQ + koff), id, ks > 0);
-    }
-  };
+  auto mma_kq_of = [&](int cc) { mma_kq(tmem + kColKQ, stage(cc) + kOffKQ); };  // [K;Q] K^T of chunk cc -> KQ
   // L (into the S0-tile scratch) and P_o of chunk cc from KQ
-  auto phase_L_Po = [&](int cc) {
-    float v[32];
-    ld32(tlane + kColKQ + 32 * half, v);
-    const int j0 = 32 * half;
-    const float* gm = gam(cc);
-    const float* gi = gin(cc);
-    if (row < kC) {
-      const int r = row;
-      const float f = bsm(cc)[r] * gm[r];
-      float* Lrow = Lsm + r * kLStride + j0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) Lrow[j] = (j0 + j < r) ? f * gi[j0 + j] * v[j] : 0.f;
-    } else {
-      const int r = row - kC;
-      const float f = gm[r];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = (j0 + j <= r) ? f * gi[j0 + j] * v[j] : 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<uint4*>(sm + po(cc) + sw128_off(r, j0 + 8 * q, 64)) = pack8_bf16(v + 8 * q);
-    }
-  };
-  // T = (I + L)^{-1} of chunk cc by doubling, then the bf16 tiles T diag(beta gamma), T diag(beta)
-  auto phase_T = [&](int cc) {
-    if (tid < kC) {
-      // 16x16 diagonal blocks, right-looking substitution: one thread per block column
-      const int base = (tid >> 4) * 16, col = tid & 15;
-      float x[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) x[r] = (r == col) ? 1.f : 0.f;
-#pragma unroll
-      for (int j = 0; j < 15; ++j) {
-        const float* Lc = Lsm + (base + j + 1) * kLStride + base + j;
-#pragma unroll
-        for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-Lc[(r - j - 1) * kLStride], x[j], x[r]);
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) Tsm[(base + r) * kTStride + base + col] = x[r];
-    } else {
-      // zero the six 16x16 blocks above the block diagonal
-      for (int e = tid - kC; e < 6 * 256; e += kThreads - kC) {
-        const int pr = e >> 8, w = e & 255;
-        const int bi = pr < 3 ? 0 : (pr < 5 ? 1 : 2);
-        const int bj = pr < 3 ? pr + 1 : (pr < 5 ? pr - 1 : 3);
-        Tsm[(bi * 16 + (w >> 4)) * kTStride + bj * 16 + (w & 15)] = 0.f;
-      }
-    }
-    __syncthreads();
-    {
-      // level 32: [[A,0],[C,B]]^-1 lower-left block = -B^-1 (C A^-1); blocks k = 0, 1
-      const int k = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
-      const int R = 32 * k + 16, Cb = 32 * k;
-      float z0 = 0.f, z1 = 0.f;
-#pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        const float l = Lsm[(R + r) * kLStride + Cb + m];
-        z0 = fmaf(l, Tsm[(Cb + m) * kTStride + Cb + c0], z0);
-        z1 = fmaf(l, Tsm[(Cb + m) * kTStride + Cb + c0 + 1], z1);
-      }
-      Zsm[k * 256 + r * 16 + c0] = z0;
-      Zsm[k * 256 + r * 16 + c0 + 1] = z1;
-      __syncthreads();
-      float t0v = 0.f, t1v = 0.f;
-#pragma unroll
-      for (int p2 = 0; p2 < 16; ++p2) {
-        const float tv = Tsm[(R + r) * kTStride + R + p2];
-        t0v = fmaf(tv, Zsm[k * 256 + p2 * 16 + c0], t0v);
-        t1v = fmaf(tv, Zsm[k * 256 + p2 * 16 + c0 + 1], t1v);
-      }
-      Tsm[(R + r) * kTStride + Cb + c0] = -t0v;
-      Tsm[(R + r) * kTStride + Cb + c0 + 1] = -t1v;
-    }
-    __syncthreads();
-    {
-      // level 64: rows 32.., columns 0..31; thread: 4 columns of one row
-      const int r = tid >> 3, c0 = (tid & 7) * 4;
-      float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-      for (int m = 0; m < 32; ++m) {
-        const float l = Lsm[(32 + r) * kLStride + m];
-        const float4 tv = *reinterpret_cast<const float4*>(Tsm + m * kTStride + c0);
-        z.x = fmaf(l, tv.x, z.x); z.y = fmaf(l, tv.y, z.y); z.z = fmaf(l, tv.z, z.z); z.w = fmaf(l, tv.w, z.w);
-      }
-      *reinterpret_cast<float4*>(Zsm + r * 32 + c0) = z;
-      __syncthreads();
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-      for (int p2 = 0; p2 < 32; ++p2) {
-        const float tv = Tsm[(32 + r) * kTStride + 32 + p2];
-        const float4 zz = *reinterpret_cast<const float4*>(Zsm + p2 * 32 + c0);
-        o.x = fmaf(tv, zz.x, o.x); o.y = fmaf(tv, zz.y, o.y); o.z = fmaf(tv, zz.z, o.z); o.w = fmaf(tv, zz.w, o.w);
-      }
-      *reinterpret_cast<float4*>(Tsm + (32 + r) * kTStride + c0) = make_float4(-o.x, -o.y, -o.z, -o.w);
-    }
-    __syncthreads();
-    {
-      const int r = tid >> 2, c0 = (tid & 3) * 16;
-      const float* bt = bsm(cc);
-      const float* gm = gam(cc);
-      float t1[16], t2[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float tv = Tsm[r * kTStride + c0 + j];
-        t2[j] = tv * bt[c0 + j];
-        t1[j] = t2[j] * gm[c0 + j];
-      }
-      if (zero_v) {  // V taken as zero: U~ = T diag(beta) V = 0
-#pragma unroll
-        for (int j = 0; j < 16; ++j) t2[j] = 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        *reinterpret_cast<uint4*>(sm + kOffT1 + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t1 + 8 * q);
-        *reinterpret_cast<uint4*>(sm + kOffT2 + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t2 + 8 * q);
-      }
-    }
-  };
-  auto mma_wu = [&](int cc) {  // W^T = K^T (T diag(beta gamma))^T, U~^T = V^T (T diag(beta))^T
-    const uint32_t st = stage(cc);
-    const uint32_t id = idesc_bf16(128, 64, 1, 0);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      mma_bf16(tmem + kColW, sw128_desc(st + kOffKQ + ks * 2048, 16384, 1024), kmaj(sbase + kOffT1 + ks * 32), id,
-               ks > 0);
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
-      mma_bf16(tmem + kColUt, sw128_desc(st + kOffV + ks * 2048, 8192, 1024), kmaj(sbase + kOffT2 + ks * 32), id,
-               ks > 0);
+  auto phase_L_Po_of = [&](int cc) { phase_L_Po(tlane + kColKQ + 32 * half, row, half, gsm(cc), Lsm, sm + po(cc), 1.f); };
+  // T = (I + L)^{-1} of chunk cc, then the bf16 tiles T diag(beta gamma), T diag(beta)
+  auto phase_T_of = [&](int cc) { phase_T(tid, Lsm, Tsm, Zsm, gsm(cc), zero_v, sm + kOffT1, sm + kOffT2); };
+  // W^T = K^T (T diag(beta gamma))^T, U~^T = V^T (T diag(beta))^T of chunk cc
+  auto mma_wu_of = [&](int cc) {
+    mma_wu(tmem + kColW, tmem + kColUt, stage(cc) + kOffKQ, stage(cc) + kOffV, sbase + kOffT1, sbase + kOffT2);
   };
   auto phase_Wtile = [&]() {  // lane k, rows r in [32 half, 32 half + 32)
     float w[32];
@@ -427,19 +229,19 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   if (__syncthreads_or(!ok)) goto done;
   if (tid == 0) {
     tc_fence_after();
-    mma_kq(0);
+    mma_kq_of(0);
     mma_commit(smem_u32(&bar_mma));
   }
   mma_pending = true;
   wait_mma();
   if (__syncthreads_or(!ok)) goto done;
   tc_fence_after();
-  phase_L_Po(0);
+  phase_L_Po_of(0);
   __syncthreads();
-  phase_T(0);
+  phase_T_of(0);
   sync_for_mma();
   if (tid == 0) {
-    mma_wu(0);
+    mma_wu_of(0);
     mma_commit(smem_u32(&bar_mma));
   }
   mma_pending = true;
@@ -484,7 +286,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         const uint32_t koff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
         mma_bf16(tmem + kColY, kmaj(sbase + kOffS0 + koff), kmaj(st + kOffKQ + 8192 + koff), id, ks > 0);
       }
-      if (has_next) mma_kq(c + 1);
+      if (has_next) mma_kq_of(c + 1);
       mma_commit(smem_u32(&bar_mma));
     }
     mma_pending = true;
@@ -529,7 +331,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
         *reinterpret_cast<uint4*>(sm + kOffUD + sw128_off(row, j0 + 8 * q, 128)) = pack8_bf16(ud + 8 * q);
       }
     }
-    if (has_next) phase_L_Po(c + 1);
+    if (has_next) phase_L_Po_of(c + 1);
     sync_for_mma();
 
     // ---- MMA 4: (P_o U)^T = U^T P_o^T ; S += U^T diag(gamma_C/gamma) K  (chunk c)
@@ -547,7 +349,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
       mma_commit(smem_u32(&bar_mma));
     }
     mma_pending = true;
-    if (has_next) phase_T(c + 1);  // overlaps MMA 4; its tiles are not operands of MMA 4
+    if (has_next) phase_T_of(c + 1);  // overlaps MMA 4; its tiles are not operands of MMA 4
     sync_for_mma();
     wait_mma();
     if (__syncthreads_or(!ok)) break;
@@ -555,7 +357,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
 
     // ---- MMA 2 of chunk c+1 (W^T, U~^T), overlapped with chunk c's outputs and the next S0 tile
     if (tid == 0 && has_next) {
-      mma_wu(c + 1);
+      mma_wu_of(c + 1);
       mma_commit(smem_u32(&bar_mma));
     }
     if (has_next) mma_pending = true;
@@ -674,6 +476,45 @@ gdn_segment_combine_kernel(const float* S_in, const float* maps, float* states, 
 
 // ----------------------------------------------------------------------------- host side
 
+template <typename TOut>
+cudaError_t launch_typed(const GdnPrefillLaunch& a, void* ws, unsigned* status, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  // strides of 0 (broadcast views) or not multiples of 16 bytes cannot be described
+  if (!gdn_make_map(&mq, a.q, a.B, a.H, a.N) || !gdn_make_map(&mk, a.k, a.B, a.H, a.N) ||
+      !gdn_make_map(&mv, a.v, a.B, a.H, a.N))
+    return cudaErrorInvalidValue;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(gdn_chunked_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemAlloc);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const GdnSegPlan plan = gdn_segment_plan(a.B, a.H, a.N);
+  const int64_t BH = a.B * a.H;
+  if (plan.G == 1) {
+    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr};
+    gdn_chunked_kernel<TOut><<<(unsigned)BH, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, task, status);
+    return cudaGetLastError();
+  }
+  float* maps = static_cast<float*>(ws);
+  float* states = maps + BH * (plan.G - 1) * 2 * kStateElems;
+  const GdnTask t1{kSegmentMaps, plan.G, plan.seg_len, maps, nullptr};
+  gdn_chunked_kernel<TOut><<<(unsigned)(BH * (plan.G - 1) * 2), kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, t1,
+                                                                                               status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_gdn_segment_combine(a.S_in, maps, states, plan.G, BH, stream);
+  if (e != cudaSuccess) return e;
+  const GdnTask t2{kSegmentOutputs, plan.G, plan.seg_len, nullptr, states};
+  gdn_chunked_kernel<TOut><<<(unsigned)(BH * plan.G), kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, t2, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+namespace {
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -691,8 +532,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
 // bf16 [B, H, N, 128] view -> 4-D tensor map with a (64 features x 64 tokens) box, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const View4& x, int64_t B, int64_t H, int64_t N) {
+bool gdn_make_map(CUtensorMap* m, const View4& x, int64_t B, int64_t H, int64_t N) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
@@ -704,45 +547,18 @@ bool make_map(CUtensorMap* m, const View4& x, int64_t B, int64_t H, int64_t N) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename TOut>
-cudaError_t launch_typed(const GdnPrefillLaunch& a, void* ws, unsigned* status, cudaStream_t stream) {
-  CUtensorMap mq, mk, mv;
-  // strides of 0 (broadcast views) or not multiples of 16 bytes cannot be described
-  if (!make_map(&mq, a.q, a.B, a.H, a.N) || !make_map(&mk, a.k, a.B, a.H, a.N) || !make_map(&mv, a.v, a.B, a.H, a.N))
-    return cudaErrorInvalidValue;
+cudaError_t launch_gdn_segment_combine(const float* S_in, const float* maps, float* states, int G, int64_t BH,
+                                       cudaStream_t stream) {
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(gdn_chunked_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSmemAlloc);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(gdn_segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)kCombineSmem);
+    attr_err = cudaFuncSetAttribute(gdn_segment_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kCombineSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const GdnSegPlan plan = gdn_segment_plan(a.B, a.H, a.N);
-  const int64_t BH = a.B * a.H;
-  if (plan.G == 1) {
-    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr};
-    gdn_chunked_kernel<TOut><<<(unsigned)BH, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, task, status);
-    return cudaGetLastError();
-  }
-  float* maps = static_cast<float*>(ws);
-  float* states = maps + BH * (plan.G - 1) * 2 * kStateElems;
-  const GdnTask t1{kSegmentMaps, plan.G, plan.seg_len, maps, nullptr};
-  gdn_chunked_kernel<TOut><<<(unsigned)(BH * (plan.G - 1) * 2), kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, t1,
-                                                                                               status);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  gdn_segment_combine_kernel<<<(unsigned)BH, kCombineThreads, kCombineSmem, stream>>>(a.S_in, maps, states, plan.G);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const GdnTask t2{kSegmentOutputs, plan.G, plan.seg_len, nullptr, states};
-  gdn_chunked_kernel<TOut><<<(unsigned)(BH * plan.G), kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, t2, status);
+  gdn_segment_combine_kernel<<<(unsigned)BH, kCombineThreads, kCombineSmem, stream>>>(S_in, maps, states, G);
   return cudaGetLastError();
 }
-
-}  // namespace
 
 // Number of sequence segments per (b,h).  With one CTA per SM, the three
 // launches cost about ceil(2 (G-1) BH / P) + ceil(G BH / P) waves of a

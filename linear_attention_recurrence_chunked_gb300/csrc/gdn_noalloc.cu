@@ -6,9 +6,10 @@
 // allocate, an inference engine that reserved its whole memory budget up front,
 // or a latency-critical loop that must not pay the implicit device-wide
 // synchronisation of cudaMalloc/cudaFree.  la_gdn_prefill_noalloc serves them:
-// its scratch (the segment maps and entry states of long sequences) lives in
-// a fixed array in this library's device memory, so the call allocates
-// nothing -- no cudaMalloc, no cudaFree, no allocating library routine.
+// its scratch (the per-chunk records of the two-kernel schedule, or the
+// segment maps and entry states of long sequences) lives in a fixed array in
+// this library's device memory, so the call allocates nothing -- no
+// cudaMalloc, no cudaFree, no allocating library routine.
 //
 // Cost: every GPU that loads the library holds kNoallocScratchBytes of device
 // memory for the array until the process exits.
@@ -23,8 +24,10 @@ namespace {
 
 // Upper bound of the scratch this entry point can use: 16 MiB, i.e. 256 of the
 // 64 KiB fp32 128x128 blocks the segment scan keeps per segment map or entry
-// state.  Problems that need more (a 16-head, 1M-token prefill needs 25.6 MiB)
-// are refused; they go through la_gdn_prefill with a caller workspace.
+// state, or the chunk records of about 290 (b,h,64-token chunk) triples.
+// Problems whose minimum scratch is larger (a 16-head, 1M-token prefill needs
+// 25.6 MiB) are refused; they go through la_gdn_prefill with a caller
+// workspace.
 constexpr size_t kNoallocScratchBytes = size_t(16) << 20;
 
 // The scratch array.  In host code `g_noalloc_scratch` is only a host-side
@@ -55,16 +58,18 @@ la_status scratch_address(void** out) {
 
 extern "C" la_status la_gdn_prefill_noalloc(const la_gdn_prefill_args* args, void* stream) {
   if (!args) return LA_ERR_INVALID_ARGUMENT;
-  // Problems whose scratch would not fit the fixed array are refused before
-  // anything else happens (la_gdn_prefill_workspace_size reports the need).
+  // Problems whose minimum scratch would not fit the fixed array are refused
+  // before anything else happens (la_gdn_prefill_workspace_size_min reports
+  // it).  Problems whose fastest schedule fits the array run that schedule;
+  // the others run the single-kernel scan, whose scratch fits.
+  const size_t need_min = la_gdn_prefill_workspace_size_min(args);
+  if (need_min > kNoallocScratchBytes) return LA_ERR_WORKSPACE;
   const size_t need = la_gdn_prefill_workspace_size(args);
-  if (need > kNoallocScratchBytes) return LA_ERR_WORKSPACE;
+  if (need == 0) return la_gdn_prefill(args, nullptr, 0, stream);
   void* scratch = nullptr;
-  if (need > 0) {
-    const la_status st = scratch_address(&scratch);
-    if (st != LA_OK) return st;
-  }
-  // The segment scan writes every scratch byte it reads within the call, so
+  const la_status st = scratch_address(&scratch);
+  if (st != LA_OK) return st;
+  // Both schedules write every scratch byte they read within the call, so
   // nothing in the array has to start at zero.
-  return la_gdn_prefill(args, scratch, need > 0 ? kNoallocScratchBytes : 0, stream);
+  return la_gdn_prefill(args, scratch, kNoallocScratchBytes, stream);
 }

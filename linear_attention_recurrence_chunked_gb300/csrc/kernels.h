@@ -65,9 +65,14 @@ cudaError_t launch_taylor_decode(const DecodeLaunch& a, cudaStream_t stream);
 // fp32 inputs: token-serial CUDA-core kernels (fp32 arithmetic throughout).
 cudaError_t launch_taylor_prefill_recurrent(const TaylorPrefillLaunch& a, cudaStream_t stream);
 cudaError_t launch_gdn_prefill_recurrent(const GdnPrefillLaunch& a, cudaStream_t stream);
-// bf16 inputs: chunked tcgen05 kernels.
+// bf16 inputs: chunked tcgen05 kernels.  The single-kernel scan needs the
+// segment scratch of gdn_segment_plan only; the two-kernel split (chunk-local
+// records, then the state chain) needs gdn_split_workspace_bytes.
 cudaError_t launch_gdn_prefill_chunked(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* dev_status,
                                        cudaStream_t stream);
+size_t gdn_split_workspace_bytes(int64_t B, int64_t H, int64_t N);
+cudaError_t launch_gdn_prefill_split(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* dev_status,
+                                     cudaStream_t stream);
 cudaError_t launch_taylor_prefill_chunked(const TaylorPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(int arrive, uint64_t limit_ns, unsigned* dev_status, cudaStream_t stream);
 

@@ -141,14 +141,24 @@ def test_decode_rejections(lib):
     assert call(mk(S=0)) == la.LA_OK
 
 
-def test_gdn_segment_workspace_query_and_rejection(lib):
+def test_gdn_workspace_queries_and_rejection(lib):
+    rec = 74240  # two-kernel schedule: record bytes per 64-token chunk of one (b,h)
+    big = gdn_args(B=1, H=16, N=1 << 20)
+    need_min = lib.la_gdn_prefill_workspace_size_min(ctypes.byref(big))
+    need = lib.la_gdn_prefill_workspace_size(ctypes.byref(big))
     # few heads and a long sequence plan sequence segments, which need scratch
-    a = gdn_args(B=1, H=16, N=1 << 20)
-    need = lib.la_gdn_prefill_workspace_size(ctypes.byref(a))
-    assert need > 0
-    # short sequences or many heads need none
-    assert lib.la_gdn_prefill_workspace_size(ctypes.byref(gdn_args(B=4, H=16, N=16384))) == 0
-    assert lib.la_gdn_prefill_workspace_size(ctypes.byref(gdn_args(B=1, H=2, N=64))) == 0
-    # a missing or short workspace is rejected on the host, before any launch
-    assert lib.la_gdn_prefill(ctypes.byref(a), None, 0, None) == la.LA_ERR_WORKSPACE
-    assert lib.la_gdn_prefill(ctypes.byref(a), ctypes.c_void_p(0x100000), need - 16, None) == la.LA_ERR_WORKSPACE
+    assert need_min > 0
+    assert need == 16 * (1 << 14) * rec + need_min
+    # short sequences or many heads need no segment scratch, only the records
+    for B, H, N in ((4, 16, 16384), (1, 2, 64), (1, 1, 65)):
+        a = gdn_args(B=B, H=H, N=N)
+        assert lib.la_gdn_prefill_workspace_size_min(ctypes.byref(a)) == 0
+        assert lib.la_gdn_prefill_workspace_size(ctypes.byref(a)) == B * H * ((N + 63) // 64) * rec
+    # fp32 inputs run token-serial kernels without scratch
+    f32 = gdn_args(set={"in_dtype": la.LA_DTYPE_F32})
+    assert lib.la_gdn_prefill_workspace_size(ctypes.byref(f32)) == 0
+    assert lib.la_gdn_prefill_workspace_size_min(ctypes.byref(f32)) == 0
+    # a missing, short or misaligned workspace is rejected on the host, before any launch
+    assert lib.la_gdn_prefill(ctypes.byref(big), None, 0, None) == la.LA_ERR_WORKSPACE
+    assert lib.la_gdn_prefill(ctypes.byref(big), ctypes.c_void_p(0x100000), need_min - 16, None) == la.LA_ERR_WORKSPACE
+    assert lib.la_gdn_prefill(ctypes.byref(big), ctypes.c_void_p(0x100008), need, None) == la.LA_ERR_WORKSPACE

@@ -161,7 +161,7 @@ def test_gdn_sequence_segments_match_oracle(N, inplace):
     dev = cuda_device()
     inp = _slow_decay(synthetic.gdn_inputs(1, 2, N, dtype=torch.bfloat16, seed=300 + N), seed=N)
     x = {n: inp[n].to(dev) for n in NAMES}
-    assert la.la_gdn_prefill_workspace_size(*(x[n] for n in NAMES)) > 0, "expected the segment path"
+    assert la.la_gdn_prefill_workspace_size_min(*(x[n] for n in NAMES)) > 0, "expected the segment path"
     S_in = (torch.randn((1, 2, 128, 128), generator=torch.Generator().manual_seed(9)) * 0.1)
     S_dev = S_in.to(dev).contiguous()
     o, S = la.la_gdn_prefill(*(x[n] for n in NAMES), S_in=S_dev, S_out=S_dev if inplace else None)
@@ -170,4 +170,54 @@ def test_gdn_sequence_segments_match_oracle(N, inplace):
     tol = TOL[torch.bfloat16]
     assert rel_err(to_np(o), ref["o"]) < tol
     assert rel_err(to_np(S), ref["S"]) < tol
+    assert la.la_device_status() == la.LA_OK
+
+
+@pytest.mark.parametrize("B,H,N,seg", [(1, 3, 1000, False), (2, 2, 257, False), (1, 2, 6144, True)])
+def test_gdn_two_schedules_agree(B, H, N, seg):
+    """The two-kernel schedule (chunk-local records, then the state chain) and
+    the one-kernel scan compute the same chunk form; they differ only in
+    where roundings fall (the chain keeps S / sigma with a running decay
+    sigma, and rounds q_scale diag(gamma) Q to bf16), so they must agree far
+    inside the bf16 tolerance -- with an incoming state, fp32 outputs, and on
+    the segment path too.  Both are also checked against the oracle."""
+    dev = cuda_device()
+    inp = synthetic.gdn_inputs(B, H, N, dtype=torch.bfloat16, seed=600 + N)
+    if seg:
+        inp = _slow_decay(inp, seed=N)
+    x = {n: inp[n].to(dev) for n in NAMES}
+    need = la.la_gdn_prefill_workspace_size(*(x[n] for n in NAMES))
+    need_min = la.la_gdn_prefill_workspace_size_min(*(x[n] for n in NAMES))
+    assert need > need_min and (need_min > 0) == seg
+    S_in = torch.randn((B, H, 128, 128), generator=torch.Generator().manual_seed(N)) * 0.1
+    outs = []
+    for ws_bytes in (need, need_min):
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        o, S = la.la_gdn_prefill(*(x[n] for n in NAMES), S_in=S_in.to(dev), out_dtype=torch.float32, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((o.cpu(), S.cpu()))
+    ref = oracle_ref(inp, S_in=S_in)
+    tol = TOL[torch.bfloat16]
+    for o, S in outs:
+        assert rel_err(o.numpy(), ref["o"]) < tol
+        assert rel_err(S.numpy(), ref["S"]) < tol
+    assert rel_err(outs[0][0].numpy(), outs[1][0].numpy().astype(np.float64)) < 5e-3
+    assert rel_err(outs[0][1].numpy(), outs[1][1].numpy().astype(np.float64)) < 5e-3
+    assert la.la_device_status() == la.LA_OK
+
+
+def test_gdn_workspace_between_min_and_full_runs_one_kernel_schedule():
+    """A workspace one byte short of the two-kernel need still runs (one-kernel
+    schedule); a misaligned one is refused without a launch."""
+    dev = cuda_device()
+    inp = synthetic.gdn_inputs(1, 2, 300, dtype=torch.bfloat16, seed=71)
+    x = {n: inp[n].to(dev) for n in NAMES}
+    need = la.la_gdn_prefill_workspace_size(*(x[n] for n in NAMES))
+    ws = torch.empty(need + 16, dtype=torch.uint8, device=dev)
+    o1, S1 = la.la_gdn_prefill(*(x[n] for n in NAMES), workspace=ws[: need - 1])
+    o2, S2 = la.la_gdn_prefill(*(x[n] for n in NAMES), workspace=ws[:need])
+    torch.cuda.synchronize()
+    assert rel_err(to_np(o1), to_np(o2)) < 5e-3 and rel_err(to_np(S1), to_np(S2)) < 5e-3
+    with pytest.raises(la.LAError):
+        la.la_gdn_prefill(*(x[n] for n in NAMES), workspace=ws[1:need + 1])
     assert la.la_device_status() == la.LA_OK
