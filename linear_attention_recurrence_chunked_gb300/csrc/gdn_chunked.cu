@@ -205,7 +205,9 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   // L (into the S0-tile scratch) and P_o of chunk cc from KQ
   auto phase_L_Po_of = [&](int cc) { phase_L_Po(tlane + kColKQ + 32 * half, row, half, gsm(cc), Lsm, sm + po(cc), 1.f); };
   // T = (I + L)^{-1} of chunk cc, then the bf16 tiles T diag(beta gamma), T diag(beta)
-  auto phase_T_of = [&](int cc) { phase_T(tid, Lsm, Tsm, Zsm, gsm(cc), zero_v, sm + kOffT1, sm + kOffT2); };
+  auto phase_T_of = [&](int cc) {
+    phase_T(tid, Lsm, [&](int r) { return Tsm + r * kTStride; }, Zsm, gsm(cc), zero_v, sm + kOffT1, sm + kOffT2);
+  };
   // W^T = K^T (T diag(beta gamma))^T, U~^T = V^T (T diag(beta))^T of chunk cc
   auto mma_wu_of = [&](int cc) {
     mma_wu(tmem + kColW, tmem + kColUt, stage(cc) + kOffKQ, stage(cc) + kOffV, sbase + kOffT1, sbase + kOffT2);

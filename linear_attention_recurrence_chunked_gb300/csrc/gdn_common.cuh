@@ -179,10 +179,13 @@ __device__ __forceinline__ void phase_L_Po(uint32_t kq_taddr, int row, int half,
 // T = (I + L)^{-1} by doubling (16x16 diagonal blocks by forward
 // substitution, then 32x32 and 64x64 blocks from
 // [[A,0],[C,B]]^-1 = [[A^-1,0],[-B^-1 C A^-1, B^-1]]), then the bf16 tiles
-// T diag(beta gamma) and T diag(beta) (zero when zero_v).  Tsm: fp32
-// [64][kTStride]; Zsm: 1024 fp32 of block products.  Every thread of the
-// block calls it; it contains block-wide barriers.
-__device__ __forceinline__ void phase_T(int tid, const float* Lsm, float* Tsm, float* Zsm, const float* gate,
+// T diag(beta gamma) and T diag(beta) (zero when zero_v).  T is fp32 with 64
+// floats per row; Trow(r) gives row r (16-byte aligned).  Zsm: 1024 fp32 of
+// block products.  Every thread of the block calls it; it contains
+// block-wide barriers, and L is no longer read once the last one has passed
+// (the bf16 tiles may overlay it).
+template <typename TRow>
+__device__ __forceinline__ void phase_T(int tid, const float* Lsm, TRow Trow, float* Zsm, const float* gate,
                                         bool zero_v, uint8_t* t1_tile, uint8_t* t2_tile) {
   if (tid < kC) {
     // 16x16 diagonal blocks, right-looking substitution: one thread per block column
@@ -197,14 +200,14 @@ __device__ __forceinline__ void phase_T(int tid, const float* Lsm, float* Tsm, f
       for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-Lc[(r - j - 1) * kLStride], x[j], x[r]);
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) Tsm[(base + r) * kTStride + base + col] = x[r];
+    for (int r = 0; r < 16; ++r) Trow(base + r)[base + col] = x[r];
   } else {
     // zero the six 16x16 blocks above the block diagonal
     for (int e = tid - kC; e < 6 * 256; e += kThreads - kC) {
       const int pr = e >> 8, w = e & 255;
       const int bi = pr < 3 ? 0 : (pr < 5 ? 1 : 2);
       const int bj = pr < 3 ? pr + 1 : (pr < 5 ? pr - 1 : 3);
-      Tsm[(bi * 16 + (w >> 4)) * kTStride + bj * 16 + (w & 15)] = 0.f;
+      Trow(bi * 16 + (w >> 4))[bj * 16 + (w & 15)] = 0.f;
     }
   }
   __syncthreads();
@@ -216,21 +219,23 @@ __device__ __forceinline__ void phase_T(int tid, const float* Lsm, float* Tsm, f
 #pragma unroll
     for (int m = 0; m < 16; ++m) {
       const float l = Lsm[(R + r) * kLStride + Cb + m];
-      z0 = fmaf(l, Tsm[(Cb + m) * kTStride + Cb + c0], z0);
-      z1 = fmaf(l, Tsm[(Cb + m) * kTStride + Cb + c0 + 1], z1);
+      const float* tm = Trow(Cb + m);
+      z0 = fmaf(l, tm[Cb + c0], z0);
+      z1 = fmaf(l, tm[Cb + c0 + 1], z1);
     }
     Zsm[k * 256 + r * 16 + c0] = z0;
     Zsm[k * 256 + r * 16 + c0 + 1] = z1;
     __syncthreads();
     float t0v = 0.f, t1v = 0.f;
+    const float* tr = Trow(R + r);
 #pragma unroll
     for (int p2 = 0; p2 < 16; ++p2) {
-      const float tv = Tsm[(R + r) * kTStride + R + p2];
+      const float tv = tr[R + p2];
       t0v = fmaf(tv, Zsm[k * 256 + p2 * 16 + c0], t0v);
       t1v = fmaf(tv, Zsm[k * 256 + p2 * 16 + c0 + 1], t1v);
     }
-    Tsm[(R + r) * kTStride + Cb + c0] = -t0v;
-    Tsm[(R + r) * kTStride + Cb + c0 + 1] = -t1v;
+    Trow(R + r)[Cb + c0] = -t0v;
+    Trow(R + r)[Cb + c0 + 1] = -t1v;
   }
   __syncthreads();
   {
@@ -240,29 +245,31 @@ __device__ __forceinline__ void phase_T(int tid, const float* Lsm, float* Tsm, f
 #pragma unroll 8
     for (int m = 0; m < 32; ++m) {
       const float l = Lsm[(32 + r) * kLStride + m];
-      const float4 tv = *reinterpret_cast<const float4*>(Tsm + m * kTStride + c0);
+      const float4 tv = *reinterpret_cast<const float4*>(Trow(m) + c0);
       z.x = fmaf(l, tv.x, z.x); z.y = fmaf(l, tv.y, z.y); z.z = fmaf(l, tv.z, z.z); z.w = fmaf(l, tv.w, z.w);
     }
     *reinterpret_cast<float4*>(Zsm + r * 32 + c0) = z;
     __syncthreads();
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* tr = Trow(32 + r);
 #pragma unroll 8
     for (int p2 = 0; p2 < 32; ++p2) {
-      const float tv = Tsm[(32 + r) * kTStride + 32 + p2];
+      const float tv = tr[32 + p2];
       const float4 zz = *reinterpret_cast<const float4*>(Zsm + p2 * 32 + c0);
       o.x = fmaf(tv, zz.x, o.x); o.y = fmaf(tv, zz.y, o.y); o.z = fmaf(tv, zz.z, o.z); o.w = fmaf(tv, zz.w, o.w);
     }
-    *reinterpret_cast<float4*>(Tsm + (32 + r) * kTStride + c0) = make_float4(-o.x, -o.y, -o.z, -o.w);
+    *reinterpret_cast<float4*>(Trow(32 + r) + c0) = make_float4(-o.x, -o.y, -o.z, -o.w);
   }
   __syncthreads();
   {
     const int r = tid >> 2, c0 = (tid & 3) * 16;
     const float* bt = gate + kC;
     const float* gm = gate + 2 * kC;
+    const float* tr = Trow(r);
     float t1[16], t2[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const float tv = Tsm[r * kTStride + c0 + j];
+      const float tv = tr[c0 + j];
       t2[j] = tv * bt[c0 + j];
       t1[j] = t2[j] * gm[c0 + j];
     }

@@ -51,23 +51,31 @@ constexpr uint32_t kRecU = 32768;      // fp32 U~^T [128 i][64 r], chunk-swizzle
 static_assert(kRecA % 16 == 0 && kRecU % 16 == 0, "bulk copies move multiples of 16 bytes");
 
 // ---------------------------------------------------------------- chunk-local kernel
-// shared memory (offsets from a 1024-byte aligned base)
-constexpr uint32_t kLOffKQ = 0;                     // [K;Q] [128][128] bf16
+// Shared memory (offsets from a 1024-byte aligned base), about 70 KB so that
+// three CTAs share an SM: tiles die early and their space is reused.
+constexpr uint32_t kLOffKQ = 0;                     // [K;Q] [128][128] bf16, two [128][64] blocks
 constexpr uint32_t kLOffV = 32768;                  // V [64][128] bf16
-constexpr uint32_t kLOffT1 = 49152;                 // bf16 T diag(beta gamma) [64][64]
-constexpr uint32_t kLOffT2 = 57344;                 // bf16 T diag(beta) [64][64]
-constexpr uint32_t kLOffPo = 65536;                 // bf16 P_o' [64][64]
-constexpr uint32_t kLOffL = 73728;                  // fp32 L [64][65]
+constexpr uint32_t kLOffL = 49152;                  // fp32 L [64][65]
 constexpr uint32_t kLOffZ = kLOffL + 64 * 65 * 4;   // fp32 block products (4 KB)
-constexpr uint32_t kLOffT = kLOffZ + 4096;          // fp32 T [64][64]
-constexpr uint32_t kLOffGate = kLOffT + 16384;      // fp32 gate tables [4][64]
+constexpr uint32_t kLOffGate = kLOffZ + 4096;       // fp32 gate tables [4][64]
 constexpr uint32_t kLSmemUsed = kLOffGate + 1024;
 constexpr uint32_t kLSmemAlloc = kLSmemUsed + 1024;
-static_assert(2 * (kLSmemAlloc + 1024) <= 233472, "two chunk-local CTAs per SM");
-// tensor-memory columns
-constexpr uint32_t kLColKQ = 0, kLColW = 64, kLColUt = 128, kLTmemCols = 256;
+// T (fp32, 64 floats per row) in the Q rows of the [K;Q] tile once [K;Q] K^T
+// and Q' are done: rows 0..31 in block 0, rows 32..63 in block 1
+constexpr uint32_t kLOffT0 = kLOffKQ + 8192, kLOffT1Rows = kLOffKQ + 16384 + 8192;
+// bf16 T diag(beta gamma) and T diag(beta) [64][64] over L once the inversion is done
+constexpr uint32_t kLOffT1 = kLOffL, kLOffT2 = kLOffL + 8192;
+// staging of the record parts written with one bulk copy each: Q' over L
+// before L exists; W over the K rows of block 0 and U~^T over block 1 and V
+// once the W/U~ MMAs are done
+constexpr uint32_t kLOffQimg = kLOffL, kLOffWimg = kLOffKQ, kLOffUimg = kLOffKQ + 16384;
+static_assert(kLOffL % 1024 == 0 && 16384 <= 64 * 65 * 4, "bf16 T tiles and the Q' image overlay L");
+static_assert(kLOffUimg + kRecU <= kLOffV + 16384, "U~^T staging fits [K;Q] block 1 and V");
+static_assert(3 * (kLSmemAlloc + 1024) <= 233472, "three chunk-local CTAs per SM");
+// tensor memory: [K;Q] K^T in columns 0..63, then W^T over it and U~^T in 64..127
+constexpr uint32_t kLColKQ = 0, kLColW = 0, kLColUt = 64, kLTmemCols = 128;
 
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
 gdn_local_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                  const __grid_constant__ CUtensorMap tmap_v, const GdnPrefillLaunch a, int nch, uint8_t* recA,
                  uint8_t* recU, unsigned* status) {
@@ -89,7 +97,6 @@ gdn_local_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
   float* gate = reinterpret_cast<float*>(sm + kLOffGate);
   float* Lsm = reinterpret_cast<float*>(sm + kLOffL);
   float* Zsm = reinterpret_cast<float*>(sm + kLOffZ);
-  float* Tsm = reinterpret_cast<float*>(sm + kLOffT);
   uint8_t* ra = recA + rec * kRecA;
 
   // this chunk's alpha and beta first: their latency overlaps the setup below
@@ -152,14 +159,29 @@ gdn_local_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       float y[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) y[j] = f * __bfloat162float(x[j]);
-      *reinterpret_cast<uint4*>(ra + kRecAQ + bk * 8192 + r * 128 + ch * 16) = pack8_bf16(y);
+      *reinterpret_cast<uint4*>(sm + kLOffQimg + bk * 8192 + r * 128 + ch * 16) = pack8_bf16(y);
+    }
+    if (tid < 32)  // gamma and 1/gamma
+      reinterpret_cast<uint4*>(ra + kRecAGate)[tid] = reinterpret_cast<const uint4*>(gate + 2 * kC)[tid];
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(ra + kRecAQ, sbase + kLOffQimg, 16384);
+      bulk_commit();
     }
     wait_mma();
-    if (__syncthreads_or(!ok)) break;
+    if (tid == 0) bulk_wait_read();  // the L region is written next
+    if (__syncthreads_or(!ok)) break;  // also: every thread is done reading Q
     tc_fence_after();
-    phase_L_Po(tlane + kLColKQ + 32 * half, row, half, gate, Lsm, sm + kLOffPo, a.q_scale);
+    // L into shared memory, P_o' straight into record A
+    phase_L_Po(tlane + kLColKQ + 32 * half, row, half, gate, Lsm, ra + kRecAPo, a.q_scale);
+    tc_fence_before();
     __syncthreads();
-    phase_T(tid, Lsm, Tsm, Zsm, gate, false, sm + kLOffT1, sm + kLOffT2);
+    phase_T(tid, Lsm,
+            [&](int r) {
+              return reinterpret_cast<float*>(sm + (r < 32 ? kLOffT0 + r * 256 : kLOffT1Rows + (r - 32) * 256));
+            },
+            Zsm, gate, false, sm + kLOffT1, sm + kLOffT2);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -169,35 +191,33 @@ gdn_local_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
       mma_commit(smem_u32(&bar_mma));
     }
     mma_pending = true;
-    // while the MMAs run: the P_o' image and the gamma tables to record A
-    {
-      const uint4* po_src = reinterpret_cast<const uint4*>(sm + kLOffPo);
-      uint4* po_dst = reinterpret_cast<uint4*>(ra + kRecAPo);
-      po_dst[tid] = po_src[tid];
-      po_dst[tid + kThreads] = po_src[tid + kThreads];
-      if (tid < 32)
-        reinterpret_cast<uint4*>(ra + kRecAGate)[tid] = reinterpret_cast<const uint4*>(gate + 2 * kC)[tid];
-    }
     wait_mma();
     if (__syncthreads_or(!ok)) break;
     tc_fence_after();
     {
-      // W image, straight from tensor memory: lane k holds W^T[k][r] for r in [32 half, 32 half + 32);
-      // for a fixed r the 32 lanes of a warp write 64 contiguous bytes
+      // W image: lane k holds W^T[k][r] for r in [32 half, 32 half + 32)
       float w[32];
       ld32(tlane + kLColW + 32 * half, w);
 #pragma unroll
-      for (int r = 0; r < 32; ++r) st_bf16(ra + kRecAW + sw128_off(32 * half + r, row, 64), w[r]);
+      for (int r = 0; r < 32; ++r) st_bf16(sm + kLOffWimg + sw128_off(32 * half + r, row, 64), w[r]);
       // U~^T row `row`, columns [32 half, 32 half + 32): eight 16-byte chunks, swizzled by row % 16
       float u[32];
       ld32(tlane + kLColUt + 32 * half, u);
-      uint8_t* ru = recU + rec * kRecU + (int64_t)row * 256;
+      uint8_t* ru = sm + kLOffUimg + row * 256;
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const int ch = 8 * half + q;
         *reinterpret_cast<float4*>(ru + ((ch ^ (row & 15)) << 4)) =
             make_float4(u[4 * q], u[4 * q + 1], u[4 * q + 2], u[4 * q + 3]);
       }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(ra + kRecAW, sbase + kLOffWimg, 16384);
+      bulk_store(recU + rec * kRecU, sbase + kLOffUimg, kRecU);
+      bulk_commit();
+      bulk_wait_read();  // shared memory stays valid until the copies have read it
     }
   } while (false);
 
