@@ -575,11 +575,12 @@ GdnSegPlan gdn_segment_plan(int64_t B, int64_t H, int64_t N) {
   if (BH <= 0 || N <= 0) return p;
   constexpr int64_t P = 148, kMinSegChunks = 32, kMaxG = 16;
   auto waves = [&](int64_t ctas) { return (ctas + P - 1) / P; };
-  double best = (double)waves(BH);
+  const double whole = (double)waves(BH);
+  double best = whole;
   int64_t bestG = 1;
   for (int64_t G = 2; G <= kMaxG && G * kMinSegChunks <= nchunks; ++G) {
     const double cost = (double)(waves(2 * (G - 1) * BH) + waves(G * BH)) / (double)G;
-    if (cost < 0.8 * best && (bestG == 1 || cost < best)) {
+    if (cost < 0.8 * whole && cost < best) {
       best = cost;
       bestG = G;
     }

@@ -24,9 +24,9 @@ namespace {
 
 // Upper bound of the scratch this entry point can use: 16 MiB, i.e. 256 of the
 // 64 KiB fp32 128x128 blocks the segment scan keeps per segment map or entry
-// state, or the chunk records of about 290 (b,h,64-token chunk) triples.
+// state, or the chunk records of 225 (b,h,64-token chunk) triples.
 // Problems whose minimum scratch is larger (a 16-head, 1M-token prefill needs
-// 25.6 MiB) are refused; they go through la_gdn_prefill with a caller
+// 25 MiB) are refused; they go through la_gdn_prefill with a caller
 // workspace.
 constexpr size_t kNoallocScratchBytes = size_t(16) << 20;
 

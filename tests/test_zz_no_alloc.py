@@ -56,7 +56,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
 def test_noalloc_refuses_problems_beyond_its_scratch():
     cuda_device()
     lib = la.load_library()
-    # 16 heads x 1M tokens needs 25.6 MiB of scratch: refused before any launch
+    # 16 heads x 1M tokens needs 25 MiB of segment scratch: refused before any launch
     # (placeholder pointers: nothing is dereferenced when the call is refused)
     B, H, N = 1, 16, 1 << 20
     t = lambda off: la.LATensor(0x100000 + off, H * N * 128, N * 128, 128)
