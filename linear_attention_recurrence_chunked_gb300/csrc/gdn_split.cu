@@ -20,13 +20,13 @@
 //   record U (32768 B): U~^T in fp32, [128 i][64 r], the 16-byte chunks of
 //       row i XOR-swizzled by i % 16 so that a warp reads 32 rows without
 //       bank conflicts.
-// The chain kernel has three roles.  One thread of warp 8 issues every copy
-// (k by TMA, the records with the bulk-copy engine) and every MMA; warps 0-3
+// The chain kernel has three roles.  One thread of warp 12 issues every copy
+// (k by TMA, the records with the bulk-copy engine) and every MMA; warps 0-7
 // run the CUDA-core passes of the critical path of each chunk,
 //   X = S0 W^T -> U, U diag(1/(sigma gamma)) -> S update -> bf16 S0,
-// each thread owning one row, and hand over to the issuer through mbarriers;
+// two threads per state row, and hand over to the issuer through mbarriers;
 // O^T = S0 Q'^T + U^T P_o'^T accumulates beside that path in one of two
-// tensor-memory buffers, which warps 4-7 drain to global memory.  The
+// tensor-memory buffers, which warps 8-11 drain to global memory.  The
 // decay gamma_C is never applied to the tensor-memory state: it holds
 // S / sigma with sigma the running product of gamma_C, which enters through
 // U diag(1 / (sigma gamma)) and the bf16 S0 copy, and is folded back into the
@@ -249,9 +249,9 @@ constexpr uint32_t kCColS = 0;     // S / sigma [i][k], 128 columns
 constexpr uint32_t kCColX = 128;   // (W S0^T)^T [i][r]
 constexpr uint32_t kCColO = 192;   // 2 x O^T [i][r], by chunk parity
 constexpr uint32_t kCTmemCols = 512;
-constexpr int kChainThreads = 128;   // warps 0-3: the chain's CUDA-core passes
-constexpr int kOutThreads = 128;     // warps 4-7: outputs
-constexpr int kIssuerWarp = 8;       // warp 8: copies and MMAs
+constexpr int kChainThreads = 256;   // warps 0-7: the chain's CUDA-core passes, two threads per state row
+constexpr int kOutThreads = 128;     // warps 8-11: outputs
+constexpr int kIssuerWarp = 12;      // warp 12: copies and MMAs
 constexpr int kChainBlock = kChainThreads + kOutThreads + 32;
 constexpr float kFoldBelow = 2.3283064e-10f;  // 2^-32: sigma is folded into the state below this
 
@@ -273,7 +273,8 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
   __shared__ uint32_t tmem_base_sh;
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int row = tid & 127;
+  const int row = tid & 127;   // state row / value index of this thread's TMEM lane
+  const int half = (tid >> 7) & 1;  // chain warps: which half of the row's columns
   const CtaWork wk = cta_work(a, task);
   const int b = wk.b, h = wk.h;
   const int nchunks = wk.nchunks;
@@ -413,10 +414,12 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
       }
     }
   } else if (tid < kChainThreads) {
-    // ================================================================ chain warps (lane i = row i of S)
+    // ================================================================ chain warps (lane i = row i of S;
+    // this thread: columns [64 half, 64 half + 64) of the state, [32 half, 32 half + 32) of U)
     bool ok = true;
-    // Initial state (sigma = 1), all 128 columns of this row, and its bf16 S0 copy.
-    for (int hf = 0; hf < 2; ++hf) {
+    // Initial state (sigma = 1) and its bf16 S0 copy.
+    {
+      const int hf = half;
       const float* src = wk.s_entry ? wk.s_entry + (int64_t)row * kD + 64 * hf : nullptr;
       float v[64];
 #pragma unroll
@@ -448,13 +451,13 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
            (wk.zero_v || wait(&bar_ut, par));
       if (!ok) break;
       tc_fence_after();
-      // ---- U^T = U~^T - X and U^T diag(1 / (sigma gamma)), this row, all 64 columns
+      // ---- U^T = U~^T - X and U^T diag(1 / (sigma gamma)), this row, columns [32 half, 32 half + 32)
       {
         const float* gi = gate(c) + kC;
         const float inv_sigma = 1.f / sigma;
         const uint8_t* ur = sm + kCOffUt + row * 256;
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        {
+          const int hf = half;
           float u[32], x[32];
           tmem_ld16(tlane + kCColX + 32 * hf, *reinterpret_cast<float(*)[16]>(x));
           tmem_ld16(tlane + kCColX + 32 * hf + 16, *reinterpret_cast<float(*)[16]>(x + 16));
@@ -493,8 +496,8 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
       const float sigma_new = sigma * gate(c)[kC - 1];
       const bool fold = sigma_new < kFoldBelow;
       if (has_next || fold) {
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
+        {
+          const int hf = half;
           float v[64];
 #pragma unroll
           for (int c0 = 0; c0 < 64; c0 += 16)
@@ -524,10 +527,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
     }
 
     if (ok && wk.s_exit) {
-      // final state S = sigma S~: lane i row i
+      // final state S = sigma S~: lane i row i, this thread's half of the columns
       float* dst = wk.s_exit + (int64_t)row * kD;
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
+      {
+        const int hf = half;
         float v[64];
 #pragma unroll
         for (int c0 = 0; c0 < 64; c0 += 16)
