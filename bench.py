@@ -6,6 +6,7 @@ B=8, H=16, N=4096, d'=16, d_v=64, bf16 in / fp32 state, in tokens/s (B*N per
 step).  The same run also times, under ``paths``:
   gdn_prefill       Gated DeltaNet prefill B=4, H=16, N=16384, d=128
   gdn_prefill_long  Gated DeltaNet prefill B=1, H=16, N=1,048,576, d=128
+  gated_prefill     scalar-gate (A_t = alpha_t I) prefill on the gdn_prefill inputs
   decode_gdn        1000 decode steps, 256 seqs x 16 heads, 128x128 state
   decode_taylor     1000 decode steps, 256 seqs x 16 heads, 273x64 state + z
 each with its own tokens/s and roofline.
@@ -310,27 +311,28 @@ def gpu_arm(args, ws, rank, local):
 KERNELS_PER_CALL = {"based_prefill": 1, "gdn_prefill": 2, "decode": 1}
 
 
-PATH_NAMES = ("gdn_prefill", "gdn_prefill_long", "decode_gdn", "decode_taylor")
+PATH_NAMES = ("gdn_prefill", "gdn_prefill_long", "gated_prefill", "decode_gdn", "decode_taylor")
 
 
 def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
     out = {}
     launches = 0
     steps = max(1, args.steps)
-    for name in ("gdn_prefill", "gdn_prefill_long"):
+    for name in ("gdn_prefill", "gdn_prefill_long", "gated_prefill"):
         if only is not None and name != only:
             continue
-        w = synthetic.WORKLOADS[name]
-        reps = steps if name == "gdn_prefill" else max(1, min(steps, args.long_steps))
-        x = synthetic.workload_inputs(name, device=dev, seed=w.seed + seed_off)
+        # the scalar gate (A_t = alpha_t I) runs on the GDN workload's inputs
+        w = synthetic.WORKLOADS["gdn_prefill" if name == "gated_prefill" else name]
+        prefill = la.la_gated_prefill if name == "gated_prefill" else la.la_gdn_prefill
+        reps = max(1, min(steps, args.long_steps)) if name == "gdn_prefill_long" else steps
+        x = synthetic.workload_inputs(w.name, device=dev, seed=w.seed + seed_off)
         o = torch.empty((w.B, w.H, w.N, 128), dtype=torch.bfloat16, device=dev)
         S = torch.empty((w.B, w.H, 128, 128), dtype=torch.float32, device=dev)
         ws_t = torch.empty(max(1, la.la_gdn_prefill_workspace_size(x["q"], x["k"], x["v"], x["alpha"], x["beta"])),
                            dtype=torch.uint8, device=dev)
 
         def step():
-            la.la_gdn_prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], o=o, S_out=S, workspace=ws_t,
-                              stream=stream)
+            prefill(x["q"], x["k"], x["v"], x["alpha"], x["beta"], o=o, S_out=S, workspace=ws_t, stream=stream)
 
         t = Timer(stream, flush)
         for _ in range(min(args.warmup, 3) if name == "gdn_prefill_long" else args.warmup):
@@ -347,7 +349,8 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         launches += reps * per_call
         byts = BYTES_PER_TOKEN_HEAD["gdn_prefill"] * w.B * w.H * w.N + STATE_BYTES["gdn"] * w.B * w.H
         r = roofline(byts, ms, pk["hbm_gbs"], ncu_traffic(name))
-        out[name] = {"workload": w.description, "tokens_per_s": round(whole_job_rate(w.B * w.N, ws, ms * 1e-3), 1),
+        desc = w.description.replace("Gated DeltaNet", "Scalar-gate") if name == "gated_prefill" else w.description
+        out[name] = {"workload": desc, "tokens_per_s": round(whole_job_rate(w.B * w.N, ws, ms * 1e-3), 1),
                      "ms": round(ms, 4), "roofline": r}
         del x, o, S, ws_t
         torch.cuda.empty_cache()

@@ -22,7 +22,12 @@
  *                    per-token cost J(7 d_k d_v + d_k + 2 d_v) in App. C.6,
  *                    Eq. (11) counts exactly this update).
  *
- * Both run as a chunked prefill that returns the final state (the state is
+ *   Scalar gate      A_t = alpha_t I, i.e. S_t = alpha_t S_{t-1} + beta_t v_t k_t^T
+ *                    (the "gated" family NoteBank Sec. 2 names next to the
+ *                    delta rule; alpha = beta = 1 is standard additive linear
+ *                    attention, A_t = I); same arguments as Gated DeltaNet.
+ *
+ * All run as a chunked prefill that returns the final state (the state is
  * carried across chunk boundaries, NoteBank Sec. 3.2) and as a one-token
  * decode step that updates the state in place.  Outputs are read after the
  * token's own write (o_t = S_t q_t with S_t already holding token t).
@@ -65,7 +70,7 @@ typedef enum la_status {
 
 typedef enum la_dtype { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
 
-typedef enum la_variant { LA_VARIANT_TAYLOR = 0, LA_VARIANT_GDN = 1 } la_variant;
+typedef enum la_variant { LA_VARIANT_TAYLOR = 0, LA_VARIANT_GDN = 1, LA_VARIANT_GATED = 2 } la_variant;
 
 /* A strided [B, H, N, d] view; strides in ELEMENTS; the d axis is contiguous. */
 typedef struct la_tensor {
@@ -113,13 +118,15 @@ typedef struct la_gdn_prefill_args {
 } la_gdn_prefill_args;
 
 /* One decode step for S sequences x H heads, state updated in place.
+ *   variant : LA_VARIANT_TAYLOR, LA_VARIANT_GDN or LA_VARIANT_GATED (the
+ *          scalar gate; layouts as GDN)
  *   q, k : [S, H, d_k] contiguous in_dtype (Taylor: d_k means d' = 16)
  *   v    : [S, H, d_v] contiguous in_dtype
- *   alpha, beta : [S, H] fp32 contiguous (GDN only; ignored for Taylor)
+ *   alpha, beta : [S, H] fp32 contiguous (GDN and scalar gate; ignored for Taylor)
  *   out  : [S, H, d_v] contiguous out_dtype
- *   state: GDN [S, H, d_v, d_k] fp32; Taylor [S, H, D, d_v] fp32 (s)
- *   z    : Taylor [S, H, D] fp32 (ignored for GDN)
- *   eps  : Taylor denominator term; q_scale: GDN query scale. */
+ *   state: GDN / scalar gate [S, H, d_v, d_k] fp32; Taylor [S, H, D, d_v] fp32 (s)
+ *   z    : Taylor [S, H, D] fp32 (ignored otherwise)
+ *   eps  : Taylor denominator term; q_scale: GDN / scalar-gate query scale. */
 typedef struct la_decode_args {
   la_variant variant;
   int64_t S, H, d_k, d_v;
@@ -171,6 +178,14 @@ la_status la_based_prefill(const la_based_prefill_args* args, void* workspace,
  * the state across boundaries as in NoteBank Sec. 3.2). */
 la_status la_gdn_prefill(const la_gdn_prefill_args* args, void* workspace,
                          size_t workspace_bytes, void* stream);
+
+/* Chunked scalar-gate prefill, A_t = alpha_t I (NoteBank Sec. 2 Eq. (1) with
+ * the gated family's retention): S_t = alpha_t S_{t-1} + beta_t v_t k_t^T,
+ * o_t = S_t (q_scale q_t).  Arguments, layouts, workspace (query it with the
+ * la_gdn_prefill_workspace_size functions), schedules and errors exactly as
+ * la_gdn_prefill; the chunk form is the same with L = 0, so T = I. */
+la_status la_gated_prefill(const la_gdn_prefill_args* args, void* workspace,
+                           size_t workspace_bytes, void* stream);
 
 /* la_gdn_prefill for callers that cannot allocate device memory (the pages
  * have no counterpart; this is an interface convenience).  Some callers have

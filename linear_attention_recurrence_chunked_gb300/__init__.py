@@ -28,6 +28,7 @@ LA_DTYPE_F32 = 0
 LA_DTYPE_BF16 = 1
 LA_VARIANT_TAYLOR = 0
 LA_VARIANT_GDN = 1
+LA_VARIANT_GATED = 2
 
 TAYLOR_DFEAT = 16
 TAYLOR_DV = 64
@@ -68,7 +69,7 @@ class DecodeArgs(ctypes.Structure):
                 ("eps", ctypes.c_float), ("q_scale", ctypes.c_float)]
 
 
-EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_decode_step", "la_based_prefill_workspace_size",
+EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_gated_prefill", "la_decode_step", "la_based_prefill_workspace_size",
             "la_gdn_prefill_workspace_size", "la_gdn_prefill_workspace_size_min", "la_gdn_prefill_noalloc", "la_device_status",
             "la_selftest_bounded_wait", "la_status_string", "la_abi_version")
 
@@ -100,6 +101,8 @@ def load_library(path: str | None = None):
     lib.la_based_prefill.argtypes = [ctypes.POINTER(BasedPrefillArgs), vp, ctypes.c_size_t, vp]
     lib.la_gdn_prefill.restype = ctypes.c_int
     lib.la_gdn_prefill.argtypes = [ctypes.POINTER(GdnPrefillArgs), vp, ctypes.c_size_t, vp]
+    lib.la_gated_prefill.restype = ctypes.c_int
+    lib.la_gated_prefill.argtypes = [ctypes.POINTER(GdnPrefillArgs), vp, ctypes.c_size_t, vp]
     lib.la_gdn_prefill_noalloc.restype = ctypes.c_int
     lib.la_gdn_prefill_noalloc.argtypes = [ctypes.POINTER(GdnPrefillArgs), vp]
     lib.la_decode_step.restype = ctypes.c_int
@@ -250,15 +253,7 @@ def la_gdn_prefill_workspace_size_min(q, k, v, alpha, beta, o=None) -> int:
     return int(load_library().la_gdn_prefill_workspace_size_min(ctypes.byref(a)))
 
 
-def la_gdn_prefill(q, k, v, alpha, beta, o=None, S_in=None, S_out=None, q_scale: float = 1.0,
-                   out_dtype=None, workspace=None, stream=None):
-    """Chunked gated-delta-rule prefill.  Returns (o, S_out).
-
-    q, k, v: [B,H,N,128] (fp32 or bf16); alpha, beta: fp32 [B,H,N];
-    S: fp32 [B,H,128,128] (row = value index).  workspace: optional uint8
-    device tensor; by default la_gdn_prefill_workspace_size bytes are
-    allocated (two-kernel schedule); a smaller one of at least
-    la_gdn_prefill_workspace_size_min bytes selects the one-kernel schedule."""
+def _gdn_family_prefill(fn_name, q, k, v, alpha, beta, o, S_in, S_out, q_scale, out_dtype, workspace, stream):
     lib = load_library()
     _check_cuda(q, k, v, alpha, beta, o, S_in, S_out)
     B, H, N, _ = q.shape
@@ -273,11 +268,32 @@ def la_gdn_prefill(q, k, v, alpha, beta, o=None, S_in=None, S_out=None, q_scale:
     a = _gdn_args(q, k, v, o, alpha, beta, S_in, S_out, q_scale)
     need = int(lib.la_gdn_prefill_workspace_size(ctypes.byref(a)))
     ws, ws_bytes = _workspace(need, workspace, q.device)
-    st = lib.la_gdn_prefill(ctypes.byref(a), _ptr(ws) if isinstance(ws, torch.Tensor) else ws, ws_bytes,
-                            _stream_handle(stream))
+    st = getattr(lib, fn_name)(ctypes.byref(a), _ptr(ws) if isinstance(ws, torch.Tensor) else ws, ws_bytes,
+                               _stream_handle(stream))
     if st != LA_OK:
-        raise LAError(st, "la_gdn_prefill")
+        raise LAError(st, fn_name)
     return o, S_out
+
+
+def la_gdn_prefill(q, k, v, alpha, beta, o=None, S_in=None, S_out=None, q_scale: float = 1.0,
+                   out_dtype=None, workspace=None, stream=None):
+    """Chunked gated-delta-rule prefill.  Returns (o, S_out).
+
+    q, k, v: [B,H,N,128] (fp32 or bf16); alpha, beta: fp32 [B,H,N];
+    S: fp32 [B,H,128,128] (row = value index).  workspace: optional uint8
+    device tensor; by default la_gdn_prefill_workspace_size bytes are
+    allocated (two-kernel schedule); a smaller one of at least
+    la_gdn_prefill_workspace_size_min bytes selects the one-kernel schedule."""
+    return _gdn_family_prefill("la_gdn_prefill", q, k, v, alpha, beta, o, S_in, S_out, q_scale, out_dtype,
+                               workspace, stream)
+
+
+def la_gated_prefill(q, k, v, alpha, beta, o=None, S_in=None, S_out=None, q_scale: float = 1.0,
+                     out_dtype=None, workspace=None, stream=None):
+    """Chunked scalar-gate prefill, S_t = alpha_t S_{t-1} + beta_t v_t k_t^T,
+    o_t = S_t (q_scale q_t).  Arguments, workspace and result as la_gdn_prefill."""
+    return _gdn_family_prefill("la_gated_prefill", q, k, v, alpha, beta, o, S_in, S_out, q_scale, out_dtype,
+                               workspace, stream)
 
 
 def la_gdn_prefill_noalloc(q, k, v, alpha, beta, o, S_out, S_in=None, q_scale: float = 1.0, stream=None):
@@ -298,7 +314,8 @@ def la_decode_step(variant: int, q, k, v, state, z=None, alpha=None, beta=None, 
                    eps: float = 0.0, q_scale: float = 1.0, out_dtype=None, stream=None):
     """One decode step, state (and z) updated in place.  Returns out [S,H,d_v].
 
-    GDN: q, k, v [S,H,128], alpha, beta fp32 [S,H], state fp32 [S,H,128,128].
+    GDN and the scalar gate (LA_VARIANT_GATED): q, k, v [S,H,128], alpha, beta
+    fp32 [S,H], state fp32 [S,H,128,128].
     Taylor: q, k [S,H,16], v [S,H,64], state fp32 [S,H,273,64], z fp32 [S,H,273]."""
     lib = load_library()
     _check_cuda(q, k, v, state, z, alpha, beta, out)

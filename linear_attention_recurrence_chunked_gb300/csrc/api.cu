@@ -103,6 +103,49 @@ la_status check_gdn(const la_gdn_prefill_args* a) {
 
 }  // namespace
 
+namespace {
+
+// The GDN-family prefill: delta = 1 is the gated delta rule, delta = 0 the
+// scalar gate A_t = alpha_t I; both share validation, workspace and kernels.
+la_status gdn_family_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes, void* stream, float delta) {
+  const la_status st = check_gdn(a);
+  if (st != LA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t BH = a->B * a->H;
+  if (BH == 0) return LA_OK;
+  if (a->N == 0) return pass_state(a->S_out, a->S_in, (size_t)(BH * kGdnD * kGdnD), s);
+  // bf16: the two-kernel split when the workspace holds its chunk records,
+  // else the single-kernel scan, which needs the segment scratch only
+  bool split = false;
+  if (a->in_dtype == LA_DTYPE_BF16) {
+    if (ws != nullptr && !aligned16(ws)) return LA_ERR_WORKSPACE;
+    const int64_t nch = (a->N + 63) / 64;
+    split = ws != nullptr && ws_bytes >= la::gdn_split_workspace_bytes(a->B, a->H, a->N) && BH * nch <= INT32_MAX;
+    const size_t need_min = la::gdn_segment_plan(a->B, a->H, a->N).ws_bytes;
+    if (!split && need_min > 0 && (ws == nullptr || ws_bytes < need_min)) return LA_ERR_WORKSPACE;
+  }
+  la::GdnPrefillLaunch L{};
+  L.B = a->B; L.H = a->H; L.N = a->N;
+  L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
+  L.out_bf16 = a->out_dtype == LA_DTYPE_BF16;
+  L.q = view(a->q); L.k = view(a->k); L.v = view(a->v);
+  L.o = a->o.ptr; L.o_sb = a->o.stride_b; L.o_sh = a->o.stride_h; L.o_st = a->o.stride_t;
+  L.alpha = static_cast<const float*>(a->alpha.ptr); L.a_sb = a->alpha.stride_b; L.a_sh = a->alpha.stride_h;
+  L.beta = static_cast<const float*>(a->beta.ptr); L.b_sb = a->beta.stride_b; L.b_sh = a->beta.stride_h;
+  L.q_scale = a->q_scale;
+  L.S_in = a->S_in; L.S_out = a->S_out;
+  L.delta = delta;
+  if (!L.in_bf16) return from_cuda(la::launch_gdn_prefill_recurrent(L, s));
+  unsigned* status = device_status_ptr();
+  if (!status) return LA_ERR_CUDA;
+  const cudaError_t e = split ? la::launch_gdn_prefill_split(L, ws, ws_bytes, status, s)
+                              : la::launch_gdn_prefill_chunked(L, ws, ws_bytes, status, s);
+  if (e == cudaErrorInvalidValue) return LA_ERR_UNSUPPORTED;  // strides TMA cannot describe
+  return from_cuda(e);
+}
+
+}  // namespace
+
 extern "C" {
 
 int la_abi_version(void) { return LA_ABI_VERSION; }
@@ -169,48 +212,23 @@ la_status la_based_prefill(const la_based_prefill_args* a, void* ws, size_t ws_b
   return from_cuda(e);
 }
 
+
 la_status la_gdn_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes, void* stream) {
-  const la_status st = check_gdn(a);
-  if (st != LA_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int64_t BH = a->B * a->H;
-  if (BH == 0) return LA_OK;
-  if (a->N == 0) return pass_state(a->S_out, a->S_in, (size_t)(BH * kGdnD * kGdnD), s);
-  // bf16: the two-kernel split when the workspace holds its chunk records,
-  // else the single-kernel scan, which needs the segment scratch only
-  bool split = false;
-  if (a->in_dtype == LA_DTYPE_BF16) {
-    if (ws != nullptr && !aligned16(ws)) return LA_ERR_WORKSPACE;
-    const int64_t nch = (a->N + 63) / 64;
-    split = ws != nullptr && ws_bytes >= la::gdn_split_workspace_bytes(a->B, a->H, a->N) && BH * nch <= INT32_MAX;
-    const size_t need_min = la::gdn_segment_plan(a->B, a->H, a->N).ws_bytes;
-    if (!split && need_min > 0 && (ws == nullptr || ws_bytes < need_min)) return LA_ERR_WORKSPACE;
-  }
-  la::GdnPrefillLaunch L{};
-  L.B = a->B; L.H = a->H; L.N = a->N;
-  L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
-  L.out_bf16 = a->out_dtype == LA_DTYPE_BF16;
-  L.q = view(a->q); L.k = view(a->k); L.v = view(a->v);
-  L.o = a->o.ptr; L.o_sb = a->o.stride_b; L.o_sh = a->o.stride_h; L.o_st = a->o.stride_t;
-  L.alpha = static_cast<const float*>(a->alpha.ptr); L.a_sb = a->alpha.stride_b; L.a_sh = a->alpha.stride_h;
-  L.beta = static_cast<const float*>(a->beta.ptr); L.b_sb = a->beta.stride_b; L.b_sh = a->beta.stride_h;
-  L.q_scale = a->q_scale;
-  L.S_in = a->S_in; L.S_out = a->S_out;
-  if (!L.in_bf16) return from_cuda(la::launch_gdn_prefill_recurrent(L, s));
-  unsigned* status = device_status_ptr();
-  if (!status) return LA_ERR_CUDA;
-  const cudaError_t e = split ? la::launch_gdn_prefill_split(L, ws, ws_bytes, status, s)
-                              : la::launch_gdn_prefill_chunked(L, ws, ws_bytes, status, s);
-  if (e == cudaErrorInvalidValue) return LA_ERR_UNSUPPORTED;  // strides TMA cannot describe
-  return from_cuda(e);
+  return gdn_family_prefill(a, ws, ws_bytes, stream, 1.f);
+}
+
+la_status la_gated_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_bytes, void* stream) {
+  return gdn_family_prefill(a, ws, ws_bytes, stream, 0.f);
 }
 
 la_status la_decode_step(const la_decode_args* a, void* stream) {
   if (!a) return LA_ERR_INVALID_ARGUMENT;
   if (a->S < 0 || a->H < 0 || a->S > kMaxDim || a->H > kMaxDim) return LA_ERR_INVALID_ARGUMENT;
   if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return LA_ERR_INVALID_ARGUMENT;
-  if (a->variant != LA_VARIANT_TAYLOR && a->variant != LA_VARIANT_GDN) return LA_ERR_INVALID_ARGUMENT;
-  if (a->variant == LA_VARIANT_GDN && (a->d_k != kGdnD || a->d_v != kGdnD)) return LA_ERR_UNSUPPORTED;
+  if (a->variant != LA_VARIANT_TAYLOR && a->variant != LA_VARIANT_GDN && a->variant != LA_VARIANT_GATED)
+    return LA_ERR_INVALID_ARGUMENT;
+  const bool gdn_family = a->variant != LA_VARIANT_TAYLOR;
+  if (gdn_family && (a->d_k != kGdnD || a->d_v != kGdnD)) return LA_ERR_UNSUPPORTED;
   if (a->variant == LA_VARIANT_TAYLOR && (a->d_k != kTaylorF || a->d_v != kTaylorDv)) return LA_ERR_UNSUPPORTED;
   const int64_t SH = a->S * a->H;
   if (SH == 0) return LA_OK;
@@ -220,7 +238,7 @@ la_status la_decode_step(const la_decode_args* a, void* stream) {
   if ((reinterpret_cast<uintptr_t>(a->q) % in_align) || (reinterpret_cast<uintptr_t>(a->k) % in_align) ||
       (reinterpret_cast<uintptr_t>(a->v) % in_align) || !aligned16(a->state))
     return LA_ERR_INVALID_ARGUMENT;
-  if (a->variant == LA_VARIANT_GDN && (!a->alpha || !a->beta)) return LA_ERR_INVALID_ARGUMENT;
+  if (gdn_family && (!a->alpha || !a->beta)) return LA_ERR_INVALID_ARGUMENT;
   if (a->variant == LA_VARIANT_TAYLOR && (!a->z || (reinterpret_cast<uintptr_t>(a->z) & 3u)))
     return LA_ERR_INVALID_ARGUMENT;
   la::DecodeLaunch L{};
@@ -229,8 +247,9 @@ la_status la_decode_step(const la_decode_args* a, void* stream) {
   L.out_bf16 = a->out_dtype == LA_DTYPE_BF16;
   L.q = a->q; L.k = a->k; L.v = a->v; L.alpha = a->alpha; L.beta = a->beta;
   L.out = a->out; L.state = a->state; L.z = a->z; L.eps = a->eps; L.q_scale = a->q_scale;
+  L.delta = a->variant == LA_VARIANT_GDN ? 1.f : 0.f;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return from_cuda(a->variant == LA_VARIANT_GDN ? la::launch_gdn_decode(L, s) : la::launch_taylor_decode(L, s));
+  return from_cuda(gdn_family ? la::launch_gdn_decode(L, s) : la::launch_taylor_decode(L, s));
 }
 
 la_status la_selftest_bounded_wait(int arrive, int64_t limit_ns, void* stream) {

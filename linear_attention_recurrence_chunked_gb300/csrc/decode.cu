@@ -15,6 +15,8 @@ namespace {
 // Gated DeltaNet decode (NoteBank Sec. 2 Eq. (1), A = alpha (I - beta k k^T)):
 //   a_i = S_i . k,  u_i = beta (v_i - alpha a_i),  S_i <- alpha S_i + u_i k^T,
 //   o_i = S_i(new) . q = alpha (S_i . q) + u_i (k . q).
+// With delta = 0 the same kernel runs the scalar gate A = alpha I
+// (u_i = beta v_i).
 // One CTA per (sequence, head); 8 warps x 16 rows; a lane holds 4 of the 128
 // columns of each of its warp's rows.
 constexpr int kGdnD = 128;
@@ -25,7 +27,7 @@ template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(kGdnThreads)
 gdn_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* __restrict__ v,
                   const float* __restrict__ alpha, const float* __restrict__ beta,
-                  TOut* __restrict__ out, float* __restrict__ state, float q_scale) {
+                  TOut* __restrict__ out, float* __restrict__ state, float q_scale, float delta) {
   const int64_t sh = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row0 = warp * kGdnRowsPerWarp;
@@ -51,7 +53,7 @@ gdn_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
     part[kGdnRowsPerWarp + r] = dot4(s[r], qq);
   }
   const float red = warp_reduce_scatter<2 * kGdnRowsPerWarp>(part);
-  const float u = be * (vv - al * red);                        // valid on lanes 0..15
+  const float u = be * (vv - delta * (al * red));              // valid on lanes 0..15
   const float u_mate = __shfl_xor_sync(kFullMask, u, 16);      // lanes 16..31 get u_{lane-16}
   if (lane >= kGdnRowsPerWarp)
     store1(out + sh * kGdnD + row0 + (lane - kGdnRowsPerWarp), al * red + u_mate * kq);
@@ -168,7 +170,7 @@ cudaError_t launch_gdn_decode(const DecodeLaunch& a, cudaStream_t stream) {
   if (grid == 0) return cudaSuccess;
 #define LA_GDN_DECODE(TI, TO)                                                                    \
   gdn_decode_kernel<TI, TO><<<grid, kGdnThreads, 0, stream>>>(                                  \
-      (const TI*)a.q, (const TI*)a.k, (const TI*)a.v, a.alpha, a.beta, (TO*)a.out, a.state, a.q_scale)
+      (const TI*)a.q, (const TI*)a.k, (const TI*)a.v, a.alpha, a.beta, (TO*)a.out, a.state, a.q_scale, a.delta)
   if (a.in_bf16 && a.out_bf16) LA_GDN_DECODE(__nv_bfloat16, __nv_bfloat16);
   else if (a.in_bf16) LA_GDN_DECODE(__nv_bfloat16, float);
   else if (a.out_bf16) LA_GDN_DECODE(float, __nv_bfloat16);

@@ -203,10 +203,11 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   };
   auto mma_kq_of = [&](int cc) { mma_kq(tmem + kColKQ, stage(cc) + kOffKQ); };  // [K;Q] K^T of chunk cc -> KQ
   // L (into the S0-tile scratch) and P_o of chunk cc from KQ
-  auto phase_L_Po_of = [&](int cc) { phase_L_Po(tlane + kColKQ + 32 * half, row, half, gsm(cc), Lsm, sm + po(cc), 1.f); };
+  auto phase_L_Po_of = [&](int cc) { phase_L_Po(tlane + kColKQ + 32 * half, row, half, gsm(cc), Lsm, sm + po(cc), 1.f, a.delta); };
   // T = (I + L)^{-1} of chunk cc, then the bf16 tiles T diag(beta gamma), T diag(beta)
   auto phase_T_of = [&](int cc) {
-    phase_T(tid, Lsm, [&](int r) { return Tsm + r * kTStride; }, Zsm, gsm(cc), zero_v, sm + kOffT1, sm + kOffT2);
+    phase_T(tid, Lsm, [&](int r) { return Tsm + r * kTStride; }, Zsm, gsm(cc), zero_v, a.delta, sm + kOffT1,
+            sm + kOffT2);
   };
   // W^T = K^T (T diag(beta gamma))^T, U~^T = V^T (T diag(beta))^T of chunk cc
   auto mma_wu_of = [&](int cc) {

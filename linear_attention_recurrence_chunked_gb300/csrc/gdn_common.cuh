@@ -148,11 +148,13 @@ __device__ __forceinline__ void mma_wu(uint32_t d_w, uint32_t d_ut, uint32_t kq_
     mma_bf16(d_ut, sw128_desc(v_tile + ks * 2048, 8192, 1024), kmaj(t2 + ks * 32), id, ks > 0);
 }
 
-// L (fp32 [64][kLStride]) and the bf16 tile po_scale * P_o [64][64] of one
-// chunk from [K;Q] K^T in TMEM.  kq_taddr: this thread's lane at the first of
+// delta * L (fp32 [64][kLStride]) and the bf16 tile po_scale * P_o [64][64]
+// of one chunk from [K;Q] K^T in TMEM.  delta = 0 is the scalar gate
+// (A_t = alpha_t I): nothing is erased, so L = 0 (T = I, U~ = diag(beta) V)
+// here and W = 0 in phase_T.  kq_taddr: this thread's lane at the first of
 // its 32 columns; gate: the chunk's gate tables.
 __device__ __forceinline__ void phase_L_Po(uint32_t kq_taddr, int row, int half, const float* gate, float* Lsm,
-                                           uint8_t* po_tile, float po_scale) {
+                                           uint8_t* po_tile, float po_scale, float delta) {
   float v[32];
   ld32(kq_taddr, v);
   const int j0 = 32 * half;
@@ -161,7 +163,7 @@ __device__ __forceinline__ void phase_L_Po(uint32_t kq_taddr, int row, int half,
   const float* gi = gate + 3 * kC;
   if (row < kC) {
     const int r = row;
-    const float f = bt[r] * gm[r];
+    const float f = bt[r] * gm[r] * delta;
     float* Lrow = Lsm + r * kLStride + j0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) Lrow[j] = (j0 + j < r) ? f * gi[j0 + j] * v[j] : 0.f;
@@ -179,14 +181,15 @@ __device__ __forceinline__ void phase_L_Po(uint32_t kq_taddr, int row, int half,
 // T = (I + L)^{-1} by doubling (16x16 diagonal blocks by forward
 // substitution, then 32x32 and 64x64 blocks from
 // [[A,0],[C,B]]^-1 = [[A^-1,0],[-B^-1 C A^-1, B^-1]]), then the bf16 tiles
-// T diag(beta gamma) and T diag(beta) (zero when zero_v).  T is fp32 with 64
+// delta T diag(beta gamma) (the erase of the incoming state; zero for the
+// scalar gate) and T diag(beta) (zero when zero_v).  T is fp32 with 64
 // floats per row; Trow(r) gives row r (16-byte aligned).  Zsm: 1024 fp32 of
 // block products.  Every thread of the block calls it; it contains
 // block-wide barriers, and L is no longer read once the last one has passed
 // (the bf16 tiles may overlay it).
 template <typename TRow>
 __device__ __forceinline__ void phase_T(int tid, const float* Lsm, TRow Trow, float* Zsm, const float* gate,
-                                        bool zero_v, uint8_t* t1_tile, uint8_t* t2_tile) {
+                                        bool zero_v, float delta, uint8_t* t1_tile, uint8_t* t2_tile) {
   if (tid < kC) {
     // 16x16 diagonal blocks, right-looking substitution: one thread per block column
     const int base = (tid >> 4) * 16, col = tid & 15;
@@ -271,7 +274,7 @@ __device__ __forceinline__ void phase_T(int tid, const float* Lsm, TRow Trow, fl
     for (int j = 0; j < 16; ++j) {
       const float tv = tr[c0 + j];
       t2[j] = tv * bt[c0 + j];
-      t1[j] = t2[j] * gm[c0 + j];
+      t1[j] = t2[j] * gm[c0 + j] * delta;
     }
     if (zero_v) {  // V taken as zero: U~ = T diag(beta) V = 0
 #pragma unroll

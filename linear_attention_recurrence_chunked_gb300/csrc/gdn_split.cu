@@ -174,14 +174,14 @@ gdn_local_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_consta
     if (__syncthreads_or(!ok)) break;  // also: every thread is done reading Q
     tc_fence_after();
     // L into shared memory, P_o' straight into record A
-    phase_L_Po(tlane + kLColKQ + 32 * half, row, half, gate, Lsm, ra + kRecAPo, a.q_scale);
+    phase_L_Po(tlane + kLColKQ + 32 * half, row, half, gate, Lsm, ra + kRecAPo, a.q_scale, a.delta);
     tc_fence_before();
     __syncthreads();
     phase_T(tid, Lsm,
             [&](int r) {
               return reinterpret_cast<float*>(sm + (r < 32 ? kLOffT0 + r * 256 : kLOffT1Rows + (r - 32) * 256));
             },
-            Zsm, gate, false, sm + kLOffT1, sm + kLOffT2);
+            Zsm, gate, false, a.delta, sm + kLOffT1, sm + kLOffT2);
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();

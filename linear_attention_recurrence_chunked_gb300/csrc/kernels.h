@@ -21,6 +21,7 @@ struct DecodeLaunch {
   float* state;
   float* z;
   float eps, q_scale;
+  float delta;  // GDN-family decode: 1 = gated delta rule, 0 = scalar gate (A_t = alpha_t I)
 };
 
 struct TaylorPrefillLaunch {
@@ -49,6 +50,7 @@ struct GdnPrefillLaunch {
   float q_scale;
   const float* S_in;
   float* S_out;
+  float delta;  // 1 = gated delta rule, A_t = alpha_t (I - beta_t k_t k_t^T); 0 = scalar gate, A_t = alpha_t I
 };
 
 // Sequence-segment plan of the gated-delta-rule prefill (see gdn_chunked.cu):

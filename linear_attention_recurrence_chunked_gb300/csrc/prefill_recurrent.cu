@@ -70,7 +70,7 @@ gdn_prefill_recurrent_kernel(GdnPrefillLaunch a) {
     }
     // lane l: index l>>1 -> lanes 0..15 hold a_{l>>1}, lanes 16..31 hold c_{(l-16)>>1}
     const float red = warp_reduce_scatter<2 * kRowsPerWarp>(part);
-    const float u = be * (vv - al * red);
+    const float u = be * (vv - a.delta * (al * red));  // delta = 0: the scalar gate writes beta v
     const float u_mate = __shfl_xor_sync(kFullMask, u, 16);
     if (lane >= 16 && (lane & 1) == 0)
       store1(o_base + t * a.o_st + row0 + ((lane - 16) >> 1), al * red + u_mate * kq);

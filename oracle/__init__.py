@@ -70,6 +70,9 @@ def _declare(lib) -> None:
     lib.oracle_gdn.restype = ctypes.c_int
     lib.oracle_gdn.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int, vp, vp, vp,
                                vp, vp, dp, vp, vp, i64, vp, vp, ctypes.c_int]
+    lib.oracle_gated.restype = ctypes.c_int
+    lib.oracle_gated.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int, vp, vp, vp,
+                                 vp, vp, dp, vp, vp, i64, vp, vp, ctypes.c_int]
 
 
 def load_library(path: str):
@@ -168,13 +171,8 @@ def taylor(q, k, v, s_in=None, z_in=None, eps: float = 0.0, t_samples=None,
     return out
 
 
-def gdn(q, k, v, alpha, beta, S_in=None, q_scale: float = 1.0, t_samples=None,
-        nthreads: int | None = None):
-    """Token-by-token gated delta rule.
-
-    q, k: [B,H,N,d_k], v: [B,H,N,d_v] (float32 or bf16 bits), alpha, beta: [B,H,N] float32.
-    Returns dict(o=[B,H,rows,d_v], S=[B,H,d_v,d_k]).
-    """
+def _gdn_family(fn_name, q, k, v, alpha, beta, S_in=None, q_scale: float = 1.0, t_samples=None,
+                nthreads: int | None = None):
     q, kind = _as_input(q)
     k, kind_k = _as_input(k)
     v, kind_v = _as_input(v)
@@ -191,10 +189,29 @@ def gdn(q, k, v, alpha, beta, S_in=None, q_scale: float = 1.0, t_samples=None,
     t, rows = _samples(t_samples, N)
     o = np.zeros((B, H, rows, dv), dtype=np.float64)
     S = np.zeros((B, H, dv, dk), dtype=np.float64)
-    rc = _load().oracle_gdn(B, H, N, dk, dv, kind, _ptr(q), _ptr(k), _ptr(v),
-                            _ptr(alpha), _ptr(beta), float(q_scale), _ptr(S_in),
-                            _ptr(t), rows if t is not None else 0, _ptr(o), _ptr(S),
-                            nthreads or default_threads())
+    rc = getattr(_load(), fn_name)(B, H, N, dk, dv, kind, _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(alpha), _ptr(beta), float(q_scale), _ptr(S_in),
+                                   _ptr(t), rows if t is not None else 0, _ptr(o), _ptr(S),
+                                   nthreads or default_threads())
     if rc != 0:
-        raise ValueError(f"oracle_gdn rejected its arguments (rc={rc})")
+        raise ValueError(f"{fn_name} rejected its arguments (rc={rc})")
     return {"o": o, "S": S}
+
+
+def gdn(q, k, v, alpha, beta, S_in=None, q_scale: float = 1.0, t_samples=None,
+        nthreads: int | None = None):
+    """Token-by-token gated delta rule (NoteBank Sec. 2 Eq. (1),
+    A_t = alpha_t (I - beta_t k_t k_t^T)).
+
+    q, k: [B,H,N,d_k], v: [B,H,N,d_v] (float32 or bf16 bits), alpha, beta: [B,H,N] float32.
+    Returns dict(o=[B,H,rows,d_v], S=[B,H,d_v,d_k]).
+    """
+    return _gdn_family("oracle_gdn", q, k, v, alpha, beta, S_in, q_scale, t_samples, nthreads)
+
+
+def gated(q, k, v, alpha, beta, S_in=None, q_scale: float = 1.0, t_samples=None,
+          nthreads: int | None = None):
+    """Token-by-token scalar gate (NoteBank Sec. 2 Eq. (1) with A_t = alpha_t I):
+    S_t = alpha_t S_{t-1} + beta_t v_t k_t^T, o_t = S_t (q_scale q_t).
+    Arguments and result as gdn()."""
+    return _gdn_family("oracle_gated", q, k, v, alpha, beta, S_in, q_scale, t_samples, nthreads)

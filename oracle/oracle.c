@@ -17,6 +17,9 @@
  *         structure of the gated delta rule
  *             A_t = alpha_t (I - beta_t k_t k_t^T)
  *         used by the Gated DeltaNet backbone that the page wraps.
+ *   [NB-G] same page, Sec. 2: besides the delta rule it names the "gated"
+ *         family, whose retention is a scalar decay of the whole state:
+ *             A_t = alpha_t I   (alpha = beta = 1: additive linear attention)
  *   [BN]  "BASED：简单线性注意力如何平衡召回能力与生成吞吐" (reading notes of
  *         "Simple linear attention language models balance the
  *         recall-throughput tradeoff"), Sec. 2.2 (the paper's Eqs. (1)-(3)):
@@ -199,6 +202,50 @@ static void* gdn_worker(void* arg) {
   return NULL;
 }
 
+/* ---------------------------------------------------------------------- */
+/* Scalar gate ([NB-G]: Eq. (1) with A_t = alpha_t I)                      */
+
+static void* gated_worker(void* arg) {
+  const job_t* j = (const job_t*)arg;
+  const int64_t dk = j->dk, dv = j->dv, N = j->N;
+  double* S = (double*)malloc(sizeof(double) * dv * dk);
+  double* kt = (double*)malloc(sizeof(double) * dk);
+  double* qt = (double*)malloc(sizeof(double) * dk);
+  double* vt = (double*)malloc(sizeof(double) * dv);
+  const int64_t rows = n_out_rows(j);
+  for (int64_t bh = j->worker; bh < j->B * j->H; bh += j->nthreads) {
+    for (int64_t i = 0; i < dv * dk; ++i) S[i] = j->s_in ? j->s_in[bh * dv * dk + i] : 0.0;
+    int64_t next = 0;
+    for (int64_t t = 0; t < N; ++t) {
+      const int64_t qk_off = (bh * N + t) * dk, v_off = (bh * N + t) * dv;
+      for (int64_t a = 0; a < dk; ++a) {
+        kt[a] = in_at(j->in_kind, j->k, qk_off + a);
+        qt[a] = j->q_scale * in_at(j->in_kind, j->q, qk_off + a);
+      }
+      for (int64_t c = 0; c < dv; ++c) vt[c] = in_at(j->in_kind, j->v, v_off + c);
+      const double al = (double)j->alpha[bh * N + t];
+      const double be = (double)j->beta[bh * N + t];
+      /* S_t = S_{t-1} (alpha I) + beta v k^T */
+      for (int64_t i = 0; i < dv; ++i)
+        for (int64_t a = 0; a < dk; ++a) S[i * dk + a] = al * S[i * dk + a] + be * vt[i] * kt[a];
+      int record = j->t_samples ? (next < j->n_samples && j->t_samples[next] == t) : 1;
+      if (!record) continue;
+      /* o_t = S_t q_t */
+      const int64_t slot = j->t_samples ? next : t;
+      double* o = j->out + (bh * rows + slot) * dv;
+      for (int64_t i = 0; i < dv; ++i) {
+        double acc = 0.0;
+        for (int64_t a = 0; a < dk; ++a) acc += S[i * dk + a] * qt[a];
+        o[i] = acc;
+      }
+      if (j->t_samples) ++next;
+    }
+    if (j->s_out) memcpy(j->s_out + bh * dv * dk, S, sizeof(double) * dv * dk);
+  }
+  free(S); free(kt); free(qt); free(vt);
+  return NULL;
+}
+
 static int run_jobs(const job_t* proto, void* (*fn)(void*), int nthreads) {
   if (nthreads < 1) nthreads = 1;
   if ((int64_t)nthreads > proto->B * proto->H) nthreads = (int)(proto->B * proto->H);
@@ -276,4 +323,24 @@ int oracle_gdn(int64_t B, int64_t H, int64_t N, int64_t dk, int64_t dv,
   j.out = o; j.s_out = S_out;
   if (B * H == 0) return 0;
   return run_jobs(&j, gdn_worker, nthreads);
+}
+
+/* Scalar gate, token by token; arguments as oracle_gdn. */
+int oracle_gated(int64_t B, int64_t H, int64_t N, int64_t dk, int64_t dv,
+                 int in_kind, const void* q, const void* k, const void* v,
+                 const float* alpha, const float* beta, double q_scale,
+                 const double* S_in, const int64_t* t_samples, int64_t n_samples,
+                 double* o, double* S_out, int nthreads) {
+  if (B < 0 || H < 0 || N < 0 || dk < 1 || dv < 1) return -1;
+  if (in_kind != ORACLE_IN_F32 && in_kind != ORACLE_IN_BF16) return -1;
+  if (t_samples && check_samples(t_samples, n_samples, N)) return -1;
+  job_t j;
+  memset(&j, 0, sizeof j);
+  j.B = B; j.H = H; j.N = N; j.dk = dk; j.dv = dv; j.in_kind = in_kind;
+  j.q = q; j.k = k; j.v = v; j.alpha = alpha; j.beta = beta;
+  j.q_scale = q_scale; j.s_in = S_in;
+  j.t_samples = t_samples; j.n_samples = n_samples;
+  j.out = o; j.s_out = S_out;
+  if (B * H == 0) return 0;
+  return run_jobs(&j, gated_worker, nthreads);
 }

@@ -162,3 +162,22 @@ def test_gdn_workspace_queries_and_rejection(lib):
     assert lib.la_gdn_prefill(ctypes.byref(big), None, 0, None) == la.LA_ERR_WORKSPACE
     assert lib.la_gdn_prefill(ctypes.byref(big), ctypes.c_void_p(0x100000), need_min - 16, None) == la.LA_ERR_WORKSPACE
     assert lib.la_gdn_prefill(ctypes.byref(big), ctypes.c_void_p(0x100008), need, None) == la.LA_ERR_WORKSPACE
+
+
+def test_gated_prefill_and_decode_rejections(lib):
+    # the scalar gate shares the gated delta rule's arguments and validation
+    call = lambda a, ws=None, n=0: lib.la_gated_prefill(ctypes.byref(a), ws, n, None)
+    assert lib.la_gated_prefill(None, None, 0, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert call(gdn_args(dk=64, dv=64)) == la.LA_ERR_UNSUPPORTED
+    assert call(gdn_args(set={"S_out": None})) == la.LA_ERR_INVALID_ARGUMENT
+    a = gdn_args()
+    a.alpha = _tensor(0x20000, 64, 64, 2)
+    assert call(a) == la.LA_ERR_INVALID_ARGUMENT
+    big = gdn_args(B=1, H=16, N=1 << 20)
+    assert call(big) == la.LA_ERR_WORKSPACE
+    assert call(gdn_args(B=0)) == la.LA_OK
+    mk = lambda **kw: la.DecodeArgs(la.LA_VARIANT_GATED, 2, 2, kw.get("dk", 128), 128, la.LA_DTYPE_BF16,
+                                    la.LA_DTYPE_BF16, 0x10000, 0x20000, 0x30000, kw.get("alpha", 0x40000), 0x50000,
+                                    0x60000, 0x70000, None, 0.0, 1.0)
+    assert lib.la_decode_step(ctypes.byref(mk(dk=64)), None) == la.LA_ERR_UNSUPPORTED
+    assert lib.la_decode_step(ctypes.byref(mk(alpha=None)), None) == la.LA_ERR_INVALID_ARGUMENT

@@ -27,6 +27,12 @@ MUTANTS = [
     ("beta dropped from erase", "al * (S[i * dk + a] - be * Sk[i] * kt[a])", "al * (S[i * dk + a] - Sk[i] * kt[a])"),
     ("query read with the key", "acc += S[i * dk + a] * qt[a];", "acc += S[i * dk + a] * kt[a];"),
     ("state_in ignored", "S[i] = j->s_in ? j->s_in[bh * dv * dk + i] : 0.0;", "S[i] = 0.0;"),
+    ("scalar gate: decay dropped", "S[i * dk + a] = al * S[i * dk + a] + be * vt[i] * kt[a];",
+     "S[i * dk + a] = S[i * dk + a] + be * vt[i] * kt[a];"),
+    ("scalar gate: write decayed", "S[i * dk + a] = al * S[i * dk + a] + be * vt[i] * kt[a];",
+     "S[i * dk + a] = al * (S[i * dk + a] + be * vt[i] * kt[a]);"),
+    ("scalar gate: beta dropped", "S[i * dk + a] = al * S[i * dk + a] + be * vt[i] * kt[a];",
+     "S[i * dk + a] = al * S[i * dk + a] + vt[i] * kt[a];"),
 ]
 
 PIN_FUNCS = [
@@ -40,6 +46,9 @@ PIN_FUNCS = [
     pins.test_gdn_beta_zero_pure_decay,
     pins.test_gdn_overwrite_property_unit_keys,
     pins.test_gdn_q_scale_split_and_samples,
+    lambda: pins.test_gated_equals_closed_form(6, 5, 17),
+    pins.test_gated_equals_delta_rule_for_orthogonal_keys,
+    pins.test_gated_additive_special_case,
 ]
 
 

@@ -319,6 +319,85 @@ def test_gdn_q_scale_split_and_samples():
     assert np.array_equal(smp["o"], full["o"][:, :, t])
 
 
+# --------------------------------------------------------------------------
+# Scalar gate, A_t = alpha_t I (the gated family of NoteBank Sec. 2)
+
+
+def gated_closed_form(q, k, v, alpha, beta, S0, q_scale=1.0):
+    """Unrolled scalar-gate recurrence, written as explicit sums:
+    S_t = (prod_{m<=t} alpha_m) S_0 + sum_{j<=t} (prod_{j<m<=t} alpha_m) beta_j v_j k_j^T,
+    o_t = S_t (q_scale q_t)."""
+    B, H, N, dk = q.shape
+    dv = v.shape[-1]
+    o = np.zeros((B, H, N, dv))
+    S_out = np.zeros((B, H, dv, dk))
+    for b in range(B):
+        for h in range(H):
+            a = alpha[b, h].astype(np.float64)
+            for t in range(N):
+                S = np.prod(a[: t + 1]) * S0[b, h]
+                for j in range(t + 1):
+                    S = S + np.prod(a[j + 1: t + 1]) * float(beta[b, h, j]) * np.outer(
+                        v[b, h, j].astype(np.float64), k[b, h, j].astype(np.float64))
+                o[b, h, t] = S @ (q_scale * q[b, h, t].astype(np.float64))
+                if t == N - 1:
+                    S_out[b, h] = S
+    return o, S_out
+
+
+@pytest.mark.parametrize("dk,dv,N", [(6, 5, 17), (8, 8, 25)])
+def test_gated_equals_closed_form(dk, dv, N):
+    q, k, v, alpha, beta = gdn_rand(2, 2, N, dk, dv)
+    S0 = rng.standard_normal((2, 2, dv, dk))
+    out = oracle.gated(q, k, v, alpha, beta, S_in=S0, q_scale=0.75)
+    o_ref, S_ref = gated_closed_form(q, k, v, alpha, beta, S0, q_scale=0.75)
+    assert rel_err(out["o"], o_ref) < 1e-12
+    assert rel_err(out["S"], S_ref) < 1e-12
+
+
+def test_gated_equals_delta_rule_for_orthogonal_keys():
+    """Each key orthogonal to every earlier key and S_0 = 0: S_{t-1} k_t = 0,
+    so the delta rule's erase term vanishes and the gated delta rule (pinned
+    above against the dense Eq. (1)) equals the scalar gate, for any alpha, beta."""
+    dk, dv, N = 16, 6, 14
+    had = np.array([[1.0]])
+    while had.shape[0] < dk:
+        had = np.block([[had, had], [had, -had]])
+    rows = rng.permutation(dk)[:N]
+    k = (had[rows] * rng.choice([-1.0, 1.0], N)[:, None] / 4.0).astype(np.float32)[None, None]
+    q = f32((1, 1, N, dk))
+    v = f32((1, 1, N, dv))
+    alpha = np.exp(-rng.uniform(0.001, 0.1, (1, 1, N))).astype(np.float32)
+    beta = (1 / (1 + np.exp(-rng.standard_normal((1, 1, N))))).astype(np.float32)
+    a = oracle.gated(q, k, v, alpha, beta)
+    b = oracle.gdn(q, k, v, alpha, beta)
+    assert rel_err(a["o"], b["o"]) < 1e-12
+    assert rel_err(a["S"], b["S"]) < 1e-12
+
+
+def test_gated_additive_special_case():
+    """alpha = beta = 1 is standard additive linear attention (NoteBank Sec. 2):
+    o_t = sum_{j<=t} (k_j . q_t) v_j."""
+    dk, dv, N = 5, 4, 19
+    q, k, v, _, _ = gdn_rand(1, 1, N, dk, dv)
+    ones = np.ones((1, 1, N), np.float32)
+    out = oracle.gated(q, k, v, ones, ones)
+    kd, vd, qd = k[0, 0].astype(np.float64), v[0, 0].astype(np.float64), q[0, 0].astype(np.float64)
+    for t in range(N):
+        ref = sum((kd[j] @ qd[t]) * vd[j] for j in range(t + 1))
+        assert np.allclose(out["o"][0, 0, t], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gated_split_resume():
+    dk, dv, N = 8, 6, 33
+    q, k, v, alpha, beta = gdn_rand(1, 2, N, dk, dv)
+    full = oracle.gated(q, k, v, alpha, beta)
+    a = oracle.gated(q[:, :, :10], k[:, :, :10], v[:, :, :10], alpha[:, :, :10], beta[:, :, :10])
+    b = oracle.gated(q[:, :, 10:], k[:, :, 10:], v[:, :, 10:], alpha[:, :, 10:], beta[:, :, 10:], S_in=a["S"])
+    assert rel_err(np.concatenate([a["o"], b["o"]], axis=2), full["o"]) < 1e-13
+    assert rel_err(b["S"], full["S"]) < 1e-13
+
+
 def test_gdn_state_size_arithmetic():
     g = json.load(open(os.path.join(GOLDEN, "state_size.json")))
     q, k, v, alpha, beta = gdn_rand(1, 1, 2, 4, 3)
