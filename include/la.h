@@ -217,9 +217,33 @@ la_status la_gdn_prefill_noalloc(const la_gdn_prefill_args* args, void* stream);
  * readout and still reads and writes the whole persistent state). */
 la_status la_decode_step(const la_decode_args* args, void* stream);
 
+/* Readout-boundary state rescaling (NoteBank App. D.1: S <- lambda S with
+ * lambda in [0, 1]; lambda = 1 keeps the state, lambda = 0 resets it).
+ *   states : n_states consecutive fp32 states of elems_per_state elements
+ *            each (any state of this library: GDN / scalar-gate S, Taylor s
+ *            or z), device memory, 4-byte aligned (16 bytes runs faster)
+ *   lambda : device array of n_states factors, or NULL to use lambda_all
+ * A factor of 0 writes zeros whatever the state held.  Asynchronous on
+ * stream; the states are updated in place. */
+la_status la_state_rescale(float* states, int64_t n_states, int64_t elems_per_state,
+                           const float* lambda, float lambda_all, void* stream);
+
+/* State copy and branch (NoteBank App. B, Alg. 1: the question is processed
+ * on a copy of the state): destination state i becomes a copy of source
+ * state index[i], for i < n_dst (one source may feed several destinations).
+ *   dst : n_dst states, src : n_src states (fp32, elems_per_state each,
+ *         device memory, 4-byte aligned); dst and src must not overlap
+ *         (LA_ERR_INVALID_ARGUMENT otherwise, nothing launched)
+ *   index : device int64 array of n_dst source indices
+ * An index outside [0, n_src) leaves that destination untouched and sets the
+ * device status word: la_device_status then reports LA_ERR_INVALID_ARGUMENT. */
+la_status la_state_gather(float* dst, const float* src, const int64_t* index, int64_t n_dst,
+                          int64_t n_src, int64_t elems_per_state, void* stream);
+
 /* Synchronises `stream`, then reports (and clears when `clear` != 0) the
- * device-side status word that bounded waits set on expiry:
- * LA_OK or LA_ERR_TIMEOUT; LA_ERR_CUDA if the synchronisation failed. */
+ * device-side status word: LA_ERR_TIMEOUT when a bounded wait expired,
+ * LA_ERR_INVALID_ARGUMENT when la_state_gather skipped an out-of-range
+ * index, else LA_OK; LA_ERR_CUDA if the synchronisation failed. */
 la_status la_device_status(void* stream, int clear);
 
 /* Self-test of the bounded-wait error path (infrastructure; the pages have no

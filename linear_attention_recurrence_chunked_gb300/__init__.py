@@ -71,7 +71,8 @@ class DecodeArgs(ctypes.Structure):
 
 EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_gated_prefill", "la_decode_step", "la_based_prefill_workspace_size",
             "la_gdn_prefill_workspace_size", "la_gdn_prefill_workspace_size_min", "la_gdn_prefill_noalloc", "la_device_status",
-            "la_selftest_bounded_wait", "la_status_string", "la_abi_version")
+            "la_state_rescale", "la_state_gather", "la_selftest_bounded_wait", "la_status_string",
+            "la_abi_version")
 
 
 class LAError(RuntimeError):
@@ -113,6 +114,10 @@ def load_library(path: str | None = None):
     lib.la_gdn_prefill_workspace_size.argtypes = [ctypes.POINTER(GdnPrefillArgs)]
     lib.la_gdn_prefill_workspace_size_min.restype = ctypes.c_size_t
     lib.la_gdn_prefill_workspace_size_min.argtypes = [ctypes.POINTER(GdnPrefillArgs)]
+    lib.la_state_rescale.restype = ctypes.c_int
+    lib.la_state_rescale.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_float, vp]
+    lib.la_state_gather.restype = ctypes.c_int
+    lib.la_state_gather.argtypes = [vp, vp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp]
     lib.la_device_status.restype = ctypes.c_int
     lib.la_device_status.argtypes = [vp, ctypes.c_int]
     lib.la_selftest_bounded_wait.restype = ctypes.c_int
@@ -334,6 +339,58 @@ def la_decode_step(variant: int, q, k, v, state, z=None, alpha=None, beta=None, 
     if st != LA_OK:
         raise LAError(st, "la_decode_step")
     return out
+
+
+def _state_split(t, state_dims: int):
+    if t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError("states must be contiguous float32 tensors")
+    if not 0 <= state_dims <= t.dim():
+        raise ValueError("state_dims out of range")
+    per = 1
+    for d in t.shape[t.dim() - state_dims:]:
+        per *= int(d)
+    n = t.numel() // per if per else 0
+    return n, per
+
+
+def la_state_rescale(states, lam, state_dims: int = 2, stream=None):
+    """S <- lambda S for every state in `states` (its last `state_dims` dims
+    form one state: 2 for GDN S or Taylor s, 1 for Taylor z), in place.
+    lam: a float, or a float32 device tensor with one factor per state.
+    A factor of 0 resets the state to zeros.  Returns `states`."""
+    lib = load_library()
+    _check_cuda(states, lam if isinstance(lam, torch.Tensor) else None)
+    n, per = _state_split(states, state_dims)
+    lam_t = lam if isinstance(lam, torch.Tensor) else None
+    if lam_t is not None and (lam_t.dtype != torch.float32 or not lam_t.is_contiguous() or lam_t.numel() != n):
+        raise ValueError("lam must be a contiguous float32 tensor with one factor per state")
+    st = lib.la_state_rescale(_ptr(states), n, per, _ptr(lam_t), 0.0 if lam_t is not None else float(lam),
+                              _stream_handle(stream))
+    if st != LA_OK:
+        raise LAError(st, "la_state_rescale")
+    return states
+
+
+def la_state_gather(src, index, state_dims: int = 2, dst=None, stream=None):
+    """dst[i] = src[index[i]] over states (the last `state_dims` dims of src
+    form one state); index: int64 device tensor.  Copies one state to
+    several destinations, reorders, or keeps a branch point.  Returns dst,
+    shaped [len(index), *state_shape]."""
+    lib = load_library()
+    _check_cuda(src, index, dst)
+    n_src, per = _state_split(src, state_dims)
+    if index.dtype != torch.int64 or not index.is_contiguous():
+        raise ValueError("index must be a contiguous int64 tensor")
+    shape = tuple(src.shape[src.dim() - state_dims:])
+    if dst is None:
+        dst = torch.empty((index.numel(), *shape), dtype=torch.float32, device=src.device)
+    n_dst, per_d = _state_split(dst, state_dims)
+    if per_d != per or n_dst != index.numel():
+        raise ValueError("dst must hold len(index) states of the source's shape")
+    st = lib.la_state_gather(_ptr(dst), _ptr(src), _ptr(index), n_dst, n_src, per, _stream_handle(stream))
+    if st != LA_OK:
+        raise LAError(st, "la_state_gather")
+    return dst
 
 
 def la_device_status(stream=None, clear: bool = True) -> int:

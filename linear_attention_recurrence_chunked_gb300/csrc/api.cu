@@ -60,6 +60,7 @@ la_status pass_state(float* out, const float* in, size_t n_floats, cudaStream_t 
 constexpr int64_t kTaylorF = 16, kTaylorDv = 64, kTaylorD = 1 + 16 + 16 * 16;
 constexpr int64_t kGdnD = 128;
 constexpr int64_t kMaxDim = int64_t(1) << 40;
+constexpr int64_t kMaxElems = int64_t(1) << 44;  // elements of one state array (64 TiB of fp32)
 
 la_status check_based(const la_based_prefill_args* a) {
   if (!a) return LA_ERR_INVALID_ARGUMENT;
@@ -252,6 +253,38 @@ la_status la_decode_step(const la_decode_args* a, void* stream) {
   return from_cuda(gdn_family ? la::launch_gdn_decode(L, s) : la::launch_taylor_decode(L, s));
 }
 
+la_status la_state_rescale(float* states, int64_t n_states, int64_t elems_per_state, const float* lambda,
+                           float lambda_all, void* stream) {
+  if (n_states < 0 || elems_per_state < 0 || n_states > kMaxDim || elems_per_state > kMaxDim ||
+      (elems_per_state > 0 && n_states > kMaxElems / elems_per_state))
+    return LA_ERR_INVALID_ARGUMENT;
+  if (n_states == 0 || elems_per_state == 0) return LA_OK;
+  if (!states || (reinterpret_cast<uintptr_t>(states) & 3u)) return LA_ERR_INVALID_ARGUMENT;
+  if (lambda && (reinterpret_cast<uintptr_t>(lambda) & 3u)) return LA_ERR_INVALID_ARGUMENT;
+  return from_cuda(la::launch_state_rescale(states, n_states, elems_per_state, lambda, lambda_all,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_state_gather(float* dst, const float* src, const int64_t* index, int64_t n_dst, int64_t n_src,
+                          int64_t elems_per_state, void* stream) {
+  if (n_dst < 0 || n_src < 0 || elems_per_state < 0 || n_dst > kMaxDim || n_src > kMaxDim ||
+      elems_per_state > kMaxDim ||
+      (elems_per_state > 0 && (n_dst > kMaxElems / elems_per_state || n_src > kMaxElems / elems_per_state)))
+    return LA_ERR_INVALID_ARGUMENT;
+  if (n_dst == 0 || elems_per_state == 0) return LA_OK;
+  if (!dst || !src || !index) return LA_ERR_INVALID_ARGUMENT;
+  if ((reinterpret_cast<uintptr_t>(dst) & 3u) || (reinterpret_cast<uintptr_t>(src) & 3u) ||
+      (reinterpret_cast<uintptr_t>(index) & 7u))
+    return LA_ERR_INVALID_ARGUMENT;
+  const uintptr_t d0 = reinterpret_cast<uintptr_t>(dst), d1 = d0 + (uintptr_t)(n_dst * elems_per_state) * 4u;
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(src), s1 = s0 + (uintptr_t)(n_src * elems_per_state) * 4u;
+  if (d0 < s1 && s0 < d1) return LA_ERR_INVALID_ARGUMENT;  // overlapping arrays
+  unsigned* status = device_status_ptr();
+  if (!status) return LA_ERR_CUDA;
+  return from_cuda(la::launch_state_gather(dst, src, index, n_dst, n_src, elems_per_state, status,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
 la_status la_selftest_bounded_wait(int arrive, int64_t limit_ns, void* stream) {
   if (limit_ns < 1000000 || limit_ns > 2000000000) return LA_ERR_INVALID_ARGUMENT;
   unsigned* status = device_status_ptr();
@@ -267,7 +300,8 @@ la_status la_device_status(void* stream, int clear) {
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_la_device_status, &zero, sizeof zero) != cudaSuccess) return LA_ERR_CUDA;
   }
-  return v ? LA_ERR_TIMEOUT : LA_OK;
+  if (v & la::kStatusTimeout) return LA_ERR_TIMEOUT;
+  return v ? LA_ERR_INVALID_ARGUMENT : LA_OK;  // kStatusBadIndex
 }
 
 }  // extern "C"

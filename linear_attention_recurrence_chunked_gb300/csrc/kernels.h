@@ -7,6 +7,10 @@
 
 namespace la {
 
+// Bits of the device status word (read back by la_device_status).
+constexpr unsigned kStatusTimeout = 1u;   // a bounded wait expired
+constexpr unsigned kStatusBadIndex = 2u;  // a state index outside its array was skipped
+
 struct View4 {        // strided [B, H, N, d] view, element strides
   const void* ptr;
   int64_t sb, sh, st;
@@ -76,6 +80,11 @@ size_t gdn_split_workspace_bytes(int64_t B, int64_t H, int64_t N);
 cudaError_t launch_gdn_prefill_split(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* dev_status,
                                      cudaStream_t stream);
 cudaError_t launch_taylor_prefill_chunked(const TaylorPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
+// State operations between calls (state_ops.cu).  per = fp32 elements per state.
+cudaError_t launch_state_rescale(float* states, int64_t n_states, int64_t per, const float* lambda, float lambda_all,
+                                 cudaStream_t stream);
+cudaError_t launch_state_gather(float* dst, const float* src, const int64_t* index, int64_t n_dst, int64_t n_src,
+                                int64_t per, unsigned* dev_status, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(int arrive, uint64_t limit_ns, unsigned* dev_status, cudaStream_t stream);
 
 }  // namespace la

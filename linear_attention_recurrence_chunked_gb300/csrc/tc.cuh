@@ -9,12 +9,14 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "kernels.h"
+
 namespace la {
 namespace tc {
 
-// Status bits written by an expired bounded wait (OR-ed into the device
+// Status bit written by an expired bounded wait (OR-ed into the device
 // status word the host reads back as LA_ERR_TIMEOUT).
-constexpr unsigned kStatusTimeout = 1u;
+using ::la::kStatusTimeout;
 // A bounded wait gives up after this many nanoseconds of spinning.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 

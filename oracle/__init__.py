@@ -215,3 +215,28 @@ def gated(q, k, v, alpha, beta, S_in=None, q_scale: float = 1.0, t_samples=None,
     S_t = alpha_t S_{t-1} + beta_t v_t k_t^T, o_t = S_t (q_scale q_t).
     Arguments and result as gdn()."""
     return _gdn_family("oracle_gated", q, k, v, alpha, beta, S_in, q_scale, t_samples, nthreads)
+
+
+# ---------------------------------------------------------------------------
+# State operations between calls.  Each is its plain definition in numpy
+# (float32 in, float32 out, one rounding per element exactly as stated).
+
+
+def state_rescale(states, lam, state_dims: int = 2):
+    """NoteBank App. D.1: S <- lambda S per state, lambda in [0, 1]; lambda = 0
+    resets (zeros, whatever the state held).  lam: scalar or one per state."""
+    x = np.array(states, dtype=np.float32, copy=True)
+    lead = x.shape[: x.ndim - state_dims]
+    lam = np.broadcast_to(np.asarray(lam, dtype=np.float32), lead)
+    for idx in np.ndindex(*lead):
+        x[idx] = np.zeros_like(x[idx]) if lam[idx] == 0 else (lam[idx] * x[idx]).astype(np.float32)
+    return x
+
+
+def state_gather(src, index, state_dims: int = 2):
+    """NoteBank App. B Alg. 1 (copy(S)): destination i is a copy of source
+    state index[i]; src is flattened to [n_states, *state_shape]."""
+    src = np.asarray(src, dtype=np.float32)
+    shape = src.shape[src.ndim - state_dims:]
+    flat = src.reshape((-1,) + shape)
+    return np.stack([flat[int(i)].copy() for i in index]) if len(index) else np.zeros((0,) + shape, np.float32)

@@ -181,3 +181,18 @@ def test_gated_prefill_and_decode_rejections(lib):
                                     0x60000, 0x70000, None, 0.0, 1.0)
     assert lib.la_decode_step(ctypes.byref(mk(dk=64)), None) == la.LA_ERR_UNSUPPORTED
     assert lib.la_decode_step(ctypes.byref(mk(alpha=None)), None) == la.LA_ERR_INVALID_ARGUMENT
+
+
+def test_state_op_rejections(lib):
+    vp = ctypes.c_void_p
+    # nothing to do: no pointer is looked at
+    assert lib.la_state_rescale(None, 0, 16, None, 0.5, None) == la.LA_OK
+    assert lib.la_state_gather(None, None, None, 0, 4, 16, None) == la.LA_OK
+    assert lib.la_state_rescale(None, 2, 16, None, 0.5, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert lib.la_state_rescale(vp(0x10002), 2, 16, None, 0.5, None) == la.LA_ERR_INVALID_ARGUMENT  # misaligned
+    assert lib.la_state_rescale(vp(0x10000), -1, 16, None, 0.5, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert lib.la_state_rescale(vp(0x10000), 1 << 30, 1 << 30, None, 0.5, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert lib.la_state_gather(vp(0x10000), None, vp(0x30000), 2, 2, 16, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert lib.la_state_gather(vp(0x10000), vp(0x20000), vp(0x30004), 2, 2, 16, None) == la.LA_ERR_INVALID_ARGUMENT
+    # overlapping destination and source
+    assert lib.la_state_gather(vp(0x10000), vp(0x10040), vp(0x30000), 2, 2, 16, None) == la.LA_ERR_INVALID_ARGUMENT

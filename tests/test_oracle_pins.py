@@ -398,6 +398,52 @@ def test_gated_split_resume():
     assert rel_err(b["S"], full["S"]) < 1e-13
 
 
+# --------------------------------------------------------------------------
+# State operations (NoteBank App. D.1 rescale/reset; App. B Alg. 1 copy)
+
+
+def test_state_rescale_definition_and_reset():
+    S = rng.standard_normal((3, 2, 5, 4)).astype(np.float32)
+    assert np.array_equal(oracle.state_rescale(S, 1.0), S)
+    bad = S.copy()
+    bad[0, 1, 2, 3] = np.nan
+    bad[2, 0, 0, 0] = np.inf
+    assert np.array_equal(oracle.state_rescale(bad, 0.0), np.zeros_like(S))  # a reset, whatever was stored
+    lam = np.array([[0.5, 0.25], [1.0, 0.0], [0.75, 0.125]], np.float32)
+    out = oracle.state_rescale(S, lam)
+    for b in range(3):
+        for h in range(2):
+            assert np.array_equal(out[b, h], S[b, h] * lam[b, h])
+    # powers of two compose exactly
+    assert np.array_equal(oracle.state_rescale(oracle.state_rescale(S, 0.5), 0.25), oracle.state_rescale(S, 0.125))
+
+
+def test_state_rescale_feeds_the_recurrence_linearly():
+    """The recurrence is affine in its entry state, so replaying from
+    lambda S_0 gives o(0) + lambda (o(S_0) - o(0)) for both the gated delta
+    rule and the scalar gate (each pinned above to its definition)."""
+    dk, dv, N = 8, 6, 21
+    q, k, v, alpha, beta = gdn_rand(1, 2, N, dk, dv)
+    S0 = rng.standard_normal((1, 2, dv, dk)).astype(np.float32)
+    lam = 0.25  # a power of two: lambda S_0 is exact in float32
+    for fn in (oracle.gdn, oracle.gated):
+        base = fn(q, k, v, alpha, beta)
+        full = fn(q, k, v, alpha, beta, S_in=S0)
+        resc = fn(q, k, v, alpha, beta, S_in=oracle.state_rescale(S0, lam))
+        assert rel_err(resc["o"], base["o"] + lam * (full["o"] - base["o"])) < 1e-12
+        assert rel_err(resc["S"], base["S"] + lam * (full["S"] - base["S"])) < 1e-12
+
+
+def test_state_gather_copies_and_branches():
+    src = rng.standard_normal((4, 3, 7)).astype(np.float32)
+    idx = [2, 0, 2, 3, 2]
+    out = oracle.state_gather(src, idx, state_dims=1)
+    flat = src.reshape(-1, 7)
+    for i, j in enumerate(idx):
+        assert np.array_equal(out[i], flat[j])
+    assert oracle.state_gather(src, [], state_dims=1).shape == (0, 7)
+
+
 def test_gdn_state_size_arithmetic():
     g = json.load(open(os.path.join(GOLDEN, "state_size.json")))
     q, k, v, alpha, beta = gdn_rand(1, 1, 2, 4, 3)
