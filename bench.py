@@ -9,6 +9,7 @@ step).  The same run also times, under ``paths``:
   gated_prefill     scalar-gate (A_t = alpha_t I) prefill on the gdn_prefill inputs
   decode_gdn        1000 decode steps, 256 seqs x 16 heads, 128x128 state
   decode_taylor     1000 decode steps, 256 seqs x 16 heads, 273x64 state + z
+  decode_swa        1000 sliding-window softmax decode steps, 256 seqs x 16 heads, window 64
 each with its own tokens/s and roofline.
 
 Timing: W untimed warm-up steps, then K steps; each launch is bracketed by
@@ -50,7 +51,11 @@ METRIC = "prefill & decode tokens/s on 1 GB300; % of tensor-core / HBM roofline 
 # plus, for prefill, the final fp32 state written once per (b,h).
 BYTES_PER_TOKEN_HEAD = {"taylor_prefill": 320, "gdn_prefill": 1032,
                         "gdn_decode": 2 * 128 * 128 * 4 + 4 * 128 * 2 + 8,
-                        "taylor_decode": 2 * (273 * 64 + 273) * 4 + 2 * 16 * 2 + 2 * 64 * 2}
+                        "taylor_decode": 2 * (273 * 64 + 273) * 4 + 2 * 16 * 2 + 2 * 64 * 2,
+                        # window 64, d 64, bf16: the full window's keys and values read, the new
+                        # token's k, v written into the ring, q, k, v read, o written
+                        "swa_decode": 2 * 64 * 64 * 2 + 2 * 64 * 2 + 3 * 64 * 2 + 64 * 2}
+SWA_WINDOW, SWA_D = 64, 64
 STATE_BYTES = {"taylor": (273 * 64 + 273) * 4, "gdn": 128 * 128 * 4}
 
 
@@ -311,7 +316,7 @@ def gpu_arm(args, ws, rank, local):
 KERNELS_PER_CALL = {"based_prefill": 1, "gdn_prefill": 2, "decode": 1}
 
 
-PATH_NAMES = ("gdn_prefill", "gdn_prefill_long", "gated_prefill", "decode_gdn", "decode_taylor")
+PATH_NAMES = ("gdn_prefill", "gdn_prefill_long", "gated_prefill", "decode_gdn", "decode_taylor", "decode_swa")
 
 
 def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
@@ -398,6 +403,43 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
                                     "tokens_per_s": round(whole_job_rate(S_, ws, per_step * 1e-3), 1),
                                     "ms_per_step": round(per_step, 5), "roofline": r}
         del xs, state, z, outb
+        torch.cuda.empty_cache()
+    if only is None or only == "decode_swa":
+        # sliding-window softmax decode (the window layers of BASED), window 64, head dim 64;
+        # every sequence starts with a full window, positions precomputed per step
+        S_, H_ = w.B, w.H
+        n_steps = w.N if only is None else max(1, args.steps)
+        g = torch.Generator(device="cpu").manual_seed(w.seed + 7 + seed_off)
+        n_inputs = 16
+        xs = [tuple((torch.randn((S_, H_, SWA_D), generator=g) * SWA_D ** -0.25).to(torch.bfloat16).to(dev)
+                    for _ in range(3)) for _ in range(n_inputs)]
+        kc = (torch.randn((S_, H_, SWA_WINDOW, SWA_D), generator=g) * SWA_D ** -0.25).to(torch.bfloat16).to(dev)
+        vc = torch.randn((S_, H_, SWA_WINDOW, SWA_D), generator=g).to(torch.bfloat16).to(dev)
+        total = n_steps + 64
+        pos = (SWA_WINDOW + torch.arange(total, dtype=torch.int64)).view(total, 1).repeat(1, S_).to(dev)
+        outb = torch.empty((S_, H_, SWA_D), dtype=torch.bfloat16, device=dev)
+
+        def run_swa(count, first):
+            for i in range(count):
+                qx, kx, vx = xs[i % n_inputs]
+                la.la_swa_decode_step(qx, kx, vx, kc, vc, pos[first + i], out=outb, stream=stream)
+
+        t = Timer(stream, flush)
+        t.run(lambda: run_swa(min(n_steps, 50) if only is None else max(1, args.warmup), 0))  # warm-up
+        t.reset()
+        barrier(ws)
+        t.run(lambda: run_swa(n_steps, 0))
+        ms = max_over_ranks(t.total_ms(), ws)
+        launches += n_steps
+        per_step = ms / n_steps
+        byts = BYTES_PER_TOKEN_HEAD["swa_decode"] * S_ * H_
+        r = roofline(byts, per_step, pk["hbm_gbs"], ncu_traffic("swa_decode"))
+        out["decode_swa"] = {"workload": f"sliding-window softmax decode {S_} seqs x {H_} heads, window "
+                                         f"{SWA_WINDOW}, d {SWA_D}, {n_steps} steps (ring caches "
+                                         f"{2 * S_ * H_ * SWA_WINDOW * SWA_D * 2 >> 20} MiB, L2-resident)",
+                             "tokens_per_s": round(whole_job_rate(S_, ws, per_step * 1e-3), 1),
+                             "ms_per_step": round(per_step, 5), "roofline": r}
+        del xs, kc, vc, pos, outb
         torch.cuda.empty_cache()
     return out, launches
 

@@ -212,6 +212,38 @@ la_status la_gated_prefill(const la_gdn_prefill_args* args, void* workspace,
  * Arguments, validation and other errors as for la_gdn_prefill. */
 la_status la_gdn_prefill_noalloc(const la_gdn_prefill_args* args, void* stream);
 
+/* One decode step of sliding-window softmax attention, the window layers of
+ * BASED (BASED notes Sec. 2.4: standard softmax over the last `window`
+ * tokens, whose KV the layer keeps; Sec. 2.5: the step fuses dot products,
+ * softmax and weighted sum).  S sequences x H heads, head dim d.
+ *   q, k, v : [S, H, d] contiguous in_dtype (any rotary embedding applied)
+ *   k_cache, v_cache : [S, H, window, d] contiguous in_dtype ring buffers;
+ *          token p lives in slot p % window; the step writes k, v of token
+ *          pos into slot pos % window (updated in place)
+ *   pos  : [S] int64 device array, tokens already seen per sequence (read
+ *          only: the caller advances it); slots 0..min(pos, window-1) must
+ *          hold tokens pos - min(pos, window - 1) .. pos - 1
+ *   out  : [S, H, d] out_dtype, o = sum_j softmax_j(scale q . k_j) v_j over
+ *          tokens max(0, pos - window + 1) .. pos
+ *   scale: multiplies q . k (1/sqrt(d) for standard softmax attention)
+ * d: a multiple of 8 in [8, 128]; window in [1, 256]; pointers 16-byte
+ * aligned.  A negative pos skips that sequence and sets the device status
+ * word (la_device_status reports LA_ERR_INVALID_ARGUMENT). */
+typedef struct la_swa_decode_args {
+  int64_t S, H, d, window;
+  la_dtype in_dtype, out_dtype;
+  const void* q;
+  const void* k;
+  const void* v;
+  void* k_cache;
+  void* v_cache;
+  const int64_t* pos;
+  void* out;
+  float scale;
+} la_swa_decode_args;
+
+la_status la_swa_decode_step(const la_swa_decode_args* args, void* stream);
+
 /* One recurrent decode step (NoteBank Eq. (1) for one token; BASED notes
  * Sec. 2.5: the decode step fuses the outer-product write with the query
  * readout and still reads and writes the whole persistent state). */
@@ -243,7 +275,8 @@ la_status la_state_gather(float* dst, const float* src, const int64_t* index, in
 /* Synchronises `stream`, then reports (and clears when `clear` != 0) the
  * device-side status word: LA_ERR_TIMEOUT when a bounded wait expired,
  * LA_ERR_INVALID_ARGUMENT when la_state_gather skipped an out-of-range
- * index, else LA_OK; LA_ERR_CUDA if the synchronisation failed. */
+ * index or la_swa_decode_step a negative position, else LA_OK; LA_ERR_CUDA
+ * if the synchronisation failed. */
 la_status la_device_status(void* stream, int clear);
 
 /* Self-test of the bounded-wait error path (infrastructure; the pages have no

@@ -71,8 +71,17 @@ class DecodeArgs(ctypes.Structure):
 
 EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_gated_prefill", "la_decode_step", "la_based_prefill_workspace_size",
             "la_gdn_prefill_workspace_size", "la_gdn_prefill_workspace_size_min", "la_gdn_prefill_noalloc", "la_device_status",
-            "la_state_rescale", "la_state_gather", "la_selftest_bounded_wait", "la_status_string",
+            "la_state_rescale", "la_state_gather", "la_swa_decode_step", "la_selftest_bounded_wait",
+            "la_status_string",
             "la_abi_version")
+
+
+class SwaDecodeArgs(ctypes.Structure):
+    _fields_ = [("S", _i64), ("H", _i64), ("d", _i64), ("window", _i64),
+                ("in_dtype", ctypes.c_int), ("out_dtype", ctypes.c_int),
+                ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("scale", ctypes.c_float)]
 
 
 class LAError(RuntimeError):
@@ -114,6 +123,8 @@ def load_library(path: str | None = None):
     lib.la_gdn_prefill_workspace_size.argtypes = [ctypes.POINTER(GdnPrefillArgs)]
     lib.la_gdn_prefill_workspace_size_min.restype = ctypes.c_size_t
     lib.la_gdn_prefill_workspace_size_min.argtypes = [ctypes.POINTER(GdnPrefillArgs)]
+    lib.la_swa_decode_step.restype = ctypes.c_int
+    lib.la_swa_decode_step.argtypes = [ctypes.POINTER(SwaDecodeArgs), vp]
     lib.la_state_rescale.restype = ctypes.c_int
     lib.la_state_rescale.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_float, vp]
     lib.la_state_gather.restype = ctypes.c_int
@@ -391,6 +402,34 @@ def la_state_gather(src, index, state_dims: int = 2, dst=None, stream=None):
     if st != LA_OK:
         raise LAError(st, "la_state_gather")
     return dst
+
+
+def la_swa_decode_step(q, k, v, k_cache, v_cache, pos, out=None, scale: float | None = None, out_dtype=None,
+                       stream=None):
+    """One sliding-window softmax-attention decode step (the window layers of
+    BASED).  q, k, v: [S,H,d]; k_cache, v_cache: [S,H,window,d] ring buffers
+    (token p in slot p % window), updated in place; pos: int64 [S] tokens
+    already seen per sequence (not advanced here).  scale defaults to
+    1/sqrt(d).  Returns out [S,H,d]."""
+    lib = load_library()
+    _check_cuda(q, k, v, k_cache, v_cache, pos, out)
+    for name, t in (("q", q), ("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache), ("pos", pos),
+                    ("out", out)):
+        if t is not None and not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if pos.dtype != torch.int64:
+        raise ValueError("pos must be int64")
+    S, H, d = q.shape
+    window = k_cache.shape[2]
+    if out is None:
+        out = torch.empty((S, H, d), dtype=out_dtype or q.dtype, device=q.device)
+    a = SwaDecodeArgs(S, H, d, window, _dtype_code(q.dtype), _dtype_code(out.dtype), _ptr(q), _ptr(k), _ptr(v),
+                      _ptr(k_cache), _ptr(v_cache), _ptr(pos), _ptr(out),
+                      float(scale if scale is not None else d ** -0.5))
+    st = lib.la_swa_decode_step(ctypes.byref(a), _stream_handle(stream))
+    if st != LA_OK:
+        raise LAError(st, "la_swa_decode_step")
+    return out
 
 
 def la_device_status(stream=None, clear: bool = True) -> int:

@@ -285,6 +285,29 @@ la_status la_state_gather(float* dst, const float* src, const int64_t* index, in
                                            static_cast<cudaStream_t>(stream)));
 }
 
+la_status la_swa_decode_step(const la_swa_decode_args* a, void* stream) {
+  if (!a) return LA_ERR_INVALID_ARGUMENT;
+  if (a->S < 0 || a->H < 0 || a->S > kMaxDim || a->H > kMaxDim) return LA_ERR_INVALID_ARGUMENT;
+  if (!valid_dtype(a->in_dtype) || !valid_dtype(a->out_dtype)) return LA_ERR_INVALID_ARGUMENT;
+  if (a->d < 8 || a->d > 128 || a->d % 8 != 0 || a->window < 1 || a->window > 256) return LA_ERR_UNSUPPORTED;
+  const int64_t SH = a->S * a->H;
+  if (SH == 0) return LA_OK;
+  if (SH > (int64_t(1) << 31) - 1) return LA_ERR_UNSUPPORTED;
+  if (!a->q || !a->k || !a->v || !a->k_cache || !a->v_cache || !a->pos || !a->out) return LA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(a->q) || !aligned16(a->k) || !aligned16(a->v) || !aligned16(a->k_cache) ||
+      !aligned16(a->v_cache) || !aligned16(a->out) || (reinterpret_cast<uintptr_t>(a->pos) & 7u))
+    return LA_ERR_INVALID_ARGUMENT;
+  unsigned* status = device_status_ptr();
+  if (!status) return LA_ERR_CUDA;
+  la::SwaDecodeLaunch L{};
+  L.S = a->S; L.H = a->H; L.d = (int)a->d; L.window = (int)a->window;
+  L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
+  L.out_bf16 = a->out_dtype == LA_DTYPE_BF16;
+  L.q = a->q; L.k = a->k; L.v = a->v; L.k_cache = a->k_cache; L.v_cache = a->v_cache;
+  L.pos = a->pos; L.out = a->out; L.scale = a->scale; L.status = status;
+  return from_cuda(la::launch_swa_decode(L, static_cast<cudaStream_t>(stream)));
+}
+
 la_status la_selftest_bounded_wait(int arrive, int64_t limit_ns, void* stream) {
   if (limit_ns < 1000000 || limit_ns > 2000000000) return LA_ERR_INVALID_ARGUMENT;
   unsigned* status = device_status_ptr();

@@ -80,6 +80,19 @@ size_t gdn_split_workspace_bytes(int64_t B, int64_t H, int64_t N);
 cudaError_t launch_gdn_prefill_split(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* dev_status,
                                      cudaStream_t stream);
 cudaError_t launch_taylor_prefill_chunked(const TaylorPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
+struct SwaDecodeLaunch {
+  int64_t S, H;
+  int d, window;
+  bool in_bf16, out_bf16;
+  const void *q, *k, *v;
+  void *k_cache, *v_cache;
+  const int64_t* pos;
+  void* out;
+  float scale;
+  unsigned* status;  // device status word (a negative position sets kStatusBadIndex)
+};
+cudaError_t launch_swa_decode(const SwaDecodeLaunch& a, cudaStream_t stream);
+
 // State operations between calls (state_ops.cu).  per = fp32 elements per state.
 cudaError_t launch_state_rescale(float* states, int64_t n_states, int64_t per, const float* lambda, float lambda_all,
                                  cudaStream_t stream);

@@ -240,3 +240,36 @@ def state_gather(src, index, state_dims: int = 2):
     shape = src.shape[src.ndim - state_dims:]
     flat = src.reshape((-1,) + shape)
     return np.stack([flat[int(i)].copy() for i in index]) if len(index) else np.zeros((0,) + shape, np.float32)
+
+
+# ---------------------------------------------------------------------------
+# Sliding-window softmax attention (the window layers of BASED: standard
+# softmax over the last `window` tokens, BASED notes Sec. 2.4), token by
+# token in float64.  Small cases only (plain loops).
+
+
+def swa(q, k, v, window: int, scale: float, t_samples=None):
+    """q, k: [B,H,N,d] (float32 or bf16 bits), v: [B,H,N,d_v].  Returns
+    o [B,H,rows,d_v] with o_i = sum_{j=max(0,i-window+1)}^{i}
+    softmax_j(scale q_i . k_j) v_j."""
+    q = _widen(q)
+    k = _widen(k)
+    v = _widen(v)
+    B, H, N, _ = q.shape
+    ts = range(N) if t_samples is None else [int(t) for t in t_samples]
+    o = np.zeros((B, H, len(ts), v.shape[-1]))
+    for b in range(B):
+        for h in range(H):
+            for r, i in enumerate(ts):
+                lo = max(0, i - window + 1)
+                s = np.array([scale * float(np.dot(q[b, h, i], k[b, h, j])) for j in range(lo, i + 1)])
+                e = np.exp(s - s.max())
+                o[b, h, r] = sum(e[j - lo] * v[b, h, j] for j in range(lo, i + 1)) / e.sum()
+    return o
+
+
+def _widen(x):
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.uint16:
+        return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return x.astype(np.float64)

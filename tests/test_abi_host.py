@@ -196,3 +196,19 @@ def test_state_op_rejections(lib):
     assert lib.la_state_gather(vp(0x10000), vp(0x20000), vp(0x30004), 2, 2, 16, None) == la.LA_ERR_INVALID_ARGUMENT
     # overlapping destination and source
     assert lib.la_state_gather(vp(0x10000), vp(0x10040), vp(0x30000), 2, 2, 16, None) == la.LA_ERR_INVALID_ARGUMENT
+
+
+def test_swa_decode_rejections(lib):
+    mk = lambda **kw: la.SwaDecodeArgs(kw.get("S", 2), 2, kw.get("d", 64), kw.get("window", 64), la.LA_DTYPE_BF16,
+                                       la.LA_DTYPE_BF16, kw.get("q", 0x10000), 0x20000, 0x30000, 0x40000, 0x50000,
+                                       kw.get("pos", 0x60000), 0x70000, 0.125)
+    call = lambda a: lib.la_swa_decode_step(ctypes.byref(a), None)
+    assert lib.la_swa_decode_step(None, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert call(mk(d=60)) == la.LA_ERR_UNSUPPORTED      # not a multiple of 8
+    assert call(mk(d=256)) == la.LA_ERR_UNSUPPORTED
+    assert call(mk(window=0)) == la.LA_ERR_UNSUPPORTED
+    assert call(mk(window=512)) == la.LA_ERR_UNSUPPORTED
+    assert call(mk(q=None)) == la.LA_ERR_INVALID_ARGUMENT
+    assert call(mk(q=0x10008)) == la.LA_ERR_INVALID_ARGUMENT  # misaligned
+    assert call(mk(pos=0x60004)) == la.LA_ERR_INVALID_ARGUMENT
+    assert call(mk(S=0)) == la.LA_OK

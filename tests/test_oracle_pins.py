@@ -444,6 +444,46 @@ def test_state_gather_copies_and_branches():
     assert oracle.state_gather(src, [], state_dims=1).shape == (0, 7)
 
 
+# --------------------------------------------------------------------------
+# Sliding-window softmax attention (BASED notes Sec. 2.4)
+
+
+def masked_softmax_attention(q, k, v, scale, mask):
+    """Row-wise softmax of the masked score matrix, then times V (the matrix
+    form of attention; mask[i, j] True keeps key j for query i)."""
+    sc = scale * np.einsum("bhid,bhjd->bhij", q.astype(np.float64), k.astype(np.float64))
+    sc = np.where(mask, sc, -np.inf)
+    sc = sc - sc.max(axis=-1, keepdims=True)
+    p = np.exp(sc)
+    p /= p.sum(axis=-1, keepdims=True)
+    return np.einsum("bhij,bhjd->bhid", p, v.astype(np.float64))
+
+
+@pytest.mark.parametrize("window", [1, 2, 5, 16])
+def test_swa_equals_banded_matrix_softmax(window):
+    N, d = 23, 6
+    q, k, v = f32((2, 2, N, d)), f32((2, 2, N, d)), f32((2, 2, N, 5))
+    i, j = np.arange(N)[:, None], np.arange(N)[None, :]
+    band = (j <= i) & (j > i - window)
+    ref = masked_softmax_attention(q, k, v, 0.4, band)
+    assert rel_err(oracle.swa(q, k, v, window, 0.4), ref) < 1e-12
+
+
+def test_swa_special_cases():
+    N, d = 17, 4
+    q, k, v = f32((1, 1, N, d)), f32((1, 1, N, d)), f32((1, 1, N, 3))
+    # a window at least N long is plain causal softmax attention
+    i, j = np.arange(N)[:, None], np.arange(N)[None, :]
+    assert rel_err(oracle.swa(q, k, v, N + 3, 0.5), masked_softmax_attention(q, k, v, 0.5, j <= i)) < 1e-12
+    # window 1: each token reads its own value
+    assert np.allclose(oracle.swa(q, k, v, 1, 0.5), v.astype(np.float64), rtol=0, atol=0)
+    # equal keys: the mean of the window's values
+    ke = np.repeat(k[:, :, :1], N, axis=2)
+    o = oracle.swa(q, ke, v, 4, 0.5)
+    for t in range(N):
+        assert np.allclose(o[0, 0, t], v[0, 0, max(0, t - 3): t + 1].astype(np.float64).mean(axis=0), atol=1e-14)
+
+
 def test_gdn_state_size_arithmetic():
     g = json.load(open(os.path.join(GOLDEN, "state_size.json")))
     q, k, v, alpha, beta = gdn_rand(1, 1, 2, 4, 3)
