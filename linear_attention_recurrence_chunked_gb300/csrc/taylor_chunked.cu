@@ -46,7 +46,9 @@ constexpr int kDv = 64;      // d_v
 constexpr int kDc = 160;     // compact features, padded (153 used)
 constexpr int kDcUsed = 1 + kF + kF + kF * (kF - 1) / 2;  // 153
 constexpr int kDfull = 1 + kF + kF * kF;                  // 273
-constexpr int kThreads = 256;  // two threads per token row of the chunk
+constexpr int kWorkers = 256;  // warps 0-7: two threads per token row of the chunk
+constexpr int kBlock = kWorkers + 32;  // + warp 8: one thread issues the copies and MMAs
+constexpr uint32_t kBarWorkers = 1;    // named barrier of the worker warps
 constexpr float kInvSqrt2 = 0.70710678118654752f;
 
 // shared memory (offsets from a 1024-byte aligned base)
@@ -152,17 +154,23 @@ __device__ __forceinline__ void store_row32<float>(float* dst, const float* v) {
 }
 
 template <typename TOut>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBlock, 1)
 taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPrefillLaunch a, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_tma[2];
-  __shared__ uint64_t bar_mma;
+  __shared__ uint64_t bar_tma[2];  // V tile of the chunk landed, by stage
+  __shared__ uint64_t bar_qk;      // Q K^T computed
+  __shared__ uint64_t bar_pv;      // readout, state update and P [V | 1] computed
+  __shared__ uint64_t bar_qkin;    // workers: this chunk's q, k rows are in the QK tile
+  __shared__ uint64_t bar_feat;    // workers: Phi_Q, Phi_K written and the c / z tiles refreshed
+  __shared__ uint64_t bar_p;       // workers: P written
+  __shared__ uint64_t bar_fin;     // drain after an expired wait
   __shared__ uint32_t tmem_base_sh;
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  const bool worker = tid < kWorkers;
   const int row = tid & (kC - 1);   // token row of the chunk == TMEM lane
-  const int half = tid >> 7;        // which half of a row's columns this thread takes
+  const int half = (tid >> 7) & 1;  // which half of a row's columns this worker takes
   const int64_t bh = blockIdx.x;
   const int b = (int)(bh / a.H), h = (int)(bh % a.H);
   const int64_t N = a.N;
@@ -173,11 +181,17 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   const int f1 = feature_of_lane(row);  // feature of this lane in the M = 64 accumulator
   const int my_feature = half == 0 ? row : f1;
   const uint32_t my_colc = half == 0 ? kColC0 : kColC1;
+  auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(smem_u32(bar), parity, status); };
 
   if (tid == 0) {
     mbar_init(smem_u32(&bar_tma[0]), 1);
     mbar_init(smem_u32(&bar_tma[1]), 1);
-    mbar_init(smem_u32(&bar_mma), 1);
+    mbar_init(smem_u32(&bar_qk), 1);
+    mbar_init(smem_u32(&bar_pv), 1);
+    mbar_init(smem_u32(&bar_qkin), kWorkers);
+    mbar_init(smem_u32(&bar_feat), kWorkers);
+    mbar_init(smem_u32(&bar_p), kWorkers);
+    mbar_init(smem_u32(&bar_fin), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmap_v);
   }
@@ -185,267 +199,325 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     tmem_alloc(smem_u32(&tmem_base_sh), kTmemCols);
     tmem_relinquish();
   }
+  // ---- constant tiles: [.. | 1] block (column 0 = 1) and the z tile, zeroed first
+  for (int i = tid; i < 16384 / 16; i += kBlock) reinterpret_cast<uint4*>(sm + kOffOnes)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < 6144 / 16; i += kBlock) reinterpret_cast<uint4*>(sm + kOffZt)[i] = make_uint4(0, 0, 0, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 
-  auto issue_tma = [&](int c) {
-    const uint32_t bar = smem_u32(&bar_tma[c & 1]);
-    mbar_arrive_expect_tx(bar, 16384);
-    tma_load_4d(sbase + kOffV + (uint32_t)(c & 1) * 16384u, &tmap_v, 0, c * kC, h, b, bar);
-  };
-  int tma_issued = 0;
-  if (tid == 0) {
-    issue_tma(0);
-    tma_issued = 1;
-    if (nchunks > 1) {
-      issue_tma(1);
-      tma_issued = 2;
+  if (!worker) {
+    // ================================================================ issuer warp: copies and MMAs.
+    // The whole warp walks the loop and waits (it stays converged for the
+    // block-wide barrier at the end); lane 0 issues.
+    const bool leader = (tid & 31) == 0;
+    auto issue_tma = [&](int c) {
+      const uint32_t bar = smem_u32(&bar_tma[c & 1]);
+      mbar_arrive_expect_tx(bar, 16384);
+      tma_load_4d(sbase + kOffV + (uint32_t)(c & 1) * 16384u, &tmap_v, 0, c * kC, h, b, bar);
+    };
+    int tma_issued = 0, tma_done = 0;
+    bool ok = true, mma_issued = false;
+    if (leader) {
+      issue_tma(0);
+      if (nchunks > 1) issue_tma(1);
     }
-  }
-  // q (half 0) or k (half 1) row of chunk c into the QK tile, asynchronously
-  auto fetch_qk = [&](int cc) {
-    const int64_t t = (int64_t)cc * kC + row;
-    const bool in = cc < nchunks && t < N;
-    const __nv_bfloat16* src = half == 0 ? qp + (in ? t : 0) * a.q.st : kp + (in ? t : 0) * a.k.st;
-    cp_async16(sbase + kOffQK + sw128_off(row, 16 * half, kC), src, in ? 16u : 0u);
-    cp_async16(sbase + kOffQK + sw128_off(row, 16 * half + 8, kC), src + 8, in ? 16u : 0u);
-    cp_async_commit();
-  };
-  fetch_qk(0);
-
-  // ---- constant tiles: [.. | 1] block (column 0 = 1) and the z tile, zeroed first
-  for (int i = tid; i < 16384 / 16; i += kThreads) reinterpret_cast<uint4*>(sm + kOffOnes)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = tid; i < 6144 / 16; i += kThreads) reinterpret_cast<uint4*>(sm + kOffZt)[i] = make_uint4(0, 0, 0, 0);
-  __syncthreads();
-  if (tid < kC) *reinterpret_cast<__nv_bfloat16*>(sm + kOffOnes + sw128_off(tid, 0, kC)) = __float2bfloat16_rn(1.f);
-
-  // ---- initial compact state c_in (fp32 in TMEM, bf16 tile) and z_in
-  const float* s_in = a.s_in ? a.s_in + bh * kDfull * kDv : nullptr;
-  const float* z_in = a.z_in ? a.z_in + bh * kDfull : nullptr;
-  auto compact_row = [&](int j, float* out /*64*/) {
-    if (!s_in || j < 0 || j >= kDcUsed) {
-#pragma unroll
-      for (int c = 0; c < kDv; ++c) out[c] = 0.f;
-      return;
-    }
-    int r0, r1;
-    float sc;
-    const int n = full_rows_of(j, r0, r1, sc);
-#pragma unroll
-    for (int c = 0; c < kDv; c += 4) {
-      float4 x = *reinterpret_cast<const float4*>(s_in + r0 * kDv + c);
-      if (n == 2) {
-        const float4 y = *reinterpret_cast<const float4*>(s_in + r1 * kDv + c);
-        x.x = (x.x + y.x) * sc; x.y = (x.y + y.y) * sc; x.z = (x.z + y.z) * sc; x.w = (x.w + y.w) * sc;
+    tma_issued = nchunks > 1 ? 2 : 1;
+    __syncwarp();
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const uint32_t par = (uint32_t)(c & 1);
+      // Q K^T as soon as the q, k rows are in
+      ok = wait(&bar_qkin, par);
+      if (!ok) break;
+      tc_fence_after();
+      if (leader) {
+        mma_bf16(tmem + kColQK, kmaj(sbase + kOffQK), kmaj(sbase + kOffQK + 32), idesc_bf16(128, 128, 0, 0), 0u);
+        mma_commit(smem_u32(&bar_qk));
       }
-      out[c] = x.x; out[c + 1] = x.y; out[c + 2] = x.z; out[c + 3] = x.w;
+      __syncwarp();
+      mma_issued = true;
+      // readout Phi_Q [c | z]_{<b} -> Acc and state update [c | z] += Phi_K^T [V | 1]
+      ok = wait(&bar_feat, par) && wait(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1));
+      if (!ok) break;
+      tma_done = c + 1;
+      tc_fence_after();
+      const uint32_t vt = sbase + kOffV + (uint32_t)(c & 1) * 16384u;
+      const uint32_t lbo = sbase + kOffOnes - vt;  // distance from the V block to the [.. | 1] block
+      if (leader) {
+        const uint32_t id = idesc_bf16(128, 64, 0, 1);
+        const uint32_t idz = idesc_bf16(128, 16, 0, 0);
+#pragma unroll
+        for (int ks = 0; ks < kDc / 16; ++ks) {
+          const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+          const uint32_t zoff = (uint32_t)(ks >> 2) * 2048u + (uint32_t)(ks & 3) * 32u;
+          mma_bf16(tmem + kColAcc, kmaj(sbase + kOffPhiQ + aoff), sw128_desc(sbase + kOffCt + ks * 2048, 0, 1024), id,
+                   ks > 0);
+          mma_bf16(tmem + kColAcc + 64, kmaj(sbase + kOffPhiQ + aoff), kmaj(sbase + kOffZt + zoff), idz, ks > 0);
+        }
+        const uint32_t id0 = idesc_bf16(128, 80, 1, 1), id1 = idesc_bf16(64, 80, 1, 1);
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks) {
+          const uint64_t bv = sw128_desc(vt + ks * 2048, lbo, 1024);
+          mma_bf16(tmem + kColC0, sw128_desc(sbase + kOffPhiK + ks * 2048, 16384, 1024), bv, id0, 1u);
+          mma_bf16(tmem + kColC1, sw128_desc(sbase + kOffPhiK + 2 * 16384 + ks * 2048, 16384, 1024), bv, id1, 1u);
+        }
+      }
+      __syncwarp();
+      // P [V | 1] -> Acc once P is written
+      ok = wait(&bar_p, par);
+      if (!ok) break;
+      tc_fence_after();
+      if (leader) {
+        const uint32_t id = idesc_bf16(128, 80, 0, 1);
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks) {
+          const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
+          mma_bf16(tmem + kColAcc, kmaj(sbase + kOffP + aoff), sw128_desc(vt + ks * 2048, lbo, 1024), id, 1u);
+        }
+        mma_commit(smem_u32(&bar_pv));
+      }
+      __syncwarp();
+      // the V stage of chunk c is free once its MMAs completed: load chunk c+2 into it
+      if (c + 2 < nchunks) {
+        ok = wait(&bar_pv, par);
+        if (!ok) break;
+        if (leader) issue_tma(c + 2);
+        __syncwarp();
+        tma_issued = c + 3;
+      }
     }
-  };
-  auto compact_z = [&](int j) -> float {
-    if (!z_in || j < 0 || j >= kDcUsed) return 0.f;
-    int r0, r1;
-    float sc;
-    const int n = full_rows_of(j, r0, r1, sc);
-    return n == 2 ? (z_in[r0] + z_in[r1]) * sc : z_in[r0];
-  };
-  {
-    float v[kDv + 16];
-    compact_row(my_feature, v);
-    v[kDv] = compact_z(my_feature);
-#pragma unroll
-    for (int i = 1; i < 16; ++i) v[kDv + i] = 0.f;
-#pragma unroll
-    for (int c = 0; c < kDv + 16; c += 16) tmem_st16(tlane + my_colc + c, *reinterpret_cast<float(*)[16]>(v + c));
-    if (my_feature >= 0) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(my_feature, 8 * q, 192)) = pack8_bf16(v + 8 * q);
-      *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(v[kDv]);
+    if (!ok) {
+      // a wait expired: let this CTA's own copies and MMAs drain (bounded) before TMEM is freed
+      for (int k = tma_done; k < tma_issued; ++k) wait(&bar_tma[k & 1], (uint32_t)((k >> 1) & 1));
+      if (mma_issued) {
+        if (leader) mma_commit(smem_u32(&bar_fin));
+        __syncwarp();
+        wait(&bar_fin, 0);
+      }
     }
-    tmem_st_wait();
-  }
+    __syncwarp();
+  } else {
+    // ================================================================ workers: two threads per token row
+    if (tid < kC) *reinterpret_cast<__nv_bfloat16*>(sm + kOffOnes + sw128_off(tid, 0, kC)) = __float2bfloat16_rn(1.f);
+    // q (half 0) or k (half 1) row of chunk cc into the QK tile, asynchronously
+    auto fetch_qk = [&](int cc) {
+      const int64_t t = (int64_t)cc * kC + row;
+      const bool in = cc < nchunks && t < N;
+      const __nv_bfloat16* src = half == 0 ? qp + (in ? t : 0) * a.q.st : kp + (in ? t : 0) * a.k.st;
+      cp_async16(sbase + kOffQK + sw128_off(row, 16 * half, kC), src, in ? 16u : 0u);
+      cp_async16(sbase + kOffQK + sw128_off(row, 16 * half + 8, kC), src + 8, in ? 16u : 0u);
+      cp_async_commit();
+    };
+    fetch_qk(0);
 
-  uint32_t mma_phase = 0;
-  bool ok = true;
-  bool mma_pending = false;
-  int c = 0;
-  for (; c < nchunks; ++c) {
-    const int64_t t = (int64_t)c * kC + row;
-    const bool valid = t < N;
-    cp_async_wait_all();
-    __syncthreads();
-    // ---- compact features of this row's q and k; this thread writes features [80 half, 80 half + 80)
+    // ---- initial compact state c_in (fp32 in TMEM, bf16 tile) and z_in
+    const float* s_in = a.s_in ? a.s_in + bh * kDfull * kDv : nullptr;
+    const float* z_in = a.z_in ? a.z_in + bh * kDfull : nullptr;
+    auto compact_row = [&](int j, float* out /*64*/) {
+      if (!s_in || j < 0 || j >= kDcUsed) {
+#pragma unroll
+        for (int c = 0; c < kDv; ++c) out[c] = 0.f;
+        return;
+      }
+      int r0, r1;
+      float sc;
+      const int n = full_rows_of(j, r0, r1, sc);
+#pragma unroll
+      for (int c = 0; c < kDv; c += 4) {
+        float4 x = *reinterpret_cast<const float4*>(s_in + r0 * kDv + c);
+        if (n == 2) {
+          const float4 y = *reinterpret_cast<const float4*>(s_in + r1 * kDv + c);
+          x.x = (x.x + y.x) * sc; x.y = (x.y + y.y) * sc; x.z = (x.z + y.z) * sc; x.w = (x.w + y.w) * sc;
+        }
+        out[c] = x.x; out[c + 1] = x.y; out[c + 2] = x.z; out[c + 3] = x.w;
+      }
+    };
+    auto compact_z = [&](int j) -> float {
+      if (!z_in || j < 0 || j >= kDcUsed) return 0.f;
+      int r0, r1;
+      float sc;
+      const int n = full_rows_of(j, r0, r1, sc);
+      return n == 2 ? (z_in[r0] + z_in[r1]) * sc : z_in[r0];
+    };
     {
-      float xq[kF], xk[kF];
-      const __nv_bfloat16* hq = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 0, kC));
-      const __nv_bfloat16* hq2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 8, kC));
-      const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 16, kC));
-      const __nv_bfloat16* hk2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 24, kC));
+      float v[kDv + 16];
+      compact_row(my_feature, v);
+      v[kDv] = compact_z(my_feature);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        xq[i] = __bfloat162float(hq[i]);
-        xq[8 + i] = __bfloat162float(hq2[i]);
-        xk[i] = __bfloat162float(hk[i]);
-        xk[8 + i] = __bfloat162float(hk2[i]);
-      }
-      if (half == 0) {
-        store_features80<0>(sm + kOffPhiQ, row, xq);
-        store_features80<0>(sm + kOffPhiK, row, xk);
-        // a padded token must not add its constant feature to the state
-        if (!valid) *reinterpret_cast<__nv_bfloat16*>(sm + kOffPhiK + sw128_off(row, 0, kC)) = __float2bfloat16_rn(0.f);
-      } else {
-        store_features80<80>(sm + kOffPhiQ, row, xq);
-        store_features80<80>(sm + kOffPhiK, row, xk);
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- MMA 1: Q K^T -> QK ; Phi_Q c_{<b} -> Acc[0:64) ; Phi_Q z_{<b} -> Acc[64:80)
-    if (tid == 0) {
-      mma_bf16(tmem + kColQK, kmaj(sbase + kOffQK), kmaj(sbase + kOffQK + 32), idesc_bf16(128, 128, 0, 0), 0u);
-      const uint32_t id = idesc_bf16(128, 64, 0, 1);
-      const uint32_t idz = idesc_bf16(128, 16, 0, 0);
+      for (int i = 1; i < 16; ++i) v[kDv + i] = 0.f;
 #pragma unroll
-      for (int ks = 0; ks < kDc / 16; ++ks) {
-        const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-        const uint32_t zoff = (uint32_t)(ks >> 2) * 2048u + (uint32_t)(ks & 3) * 32u;
-        mma_bf16(tmem + kColAcc, kmaj(sbase + kOffPhiQ + aoff), sw128_desc(sbase + kOffCt + ks * 2048, 0, 1024), id,
-                 ks > 0);
-        mma_bf16(tmem + kColAcc + 64, kmaj(sbase + kOffPhiQ + aoff), kmaj(sbase + kOffZt + zoff), idz, ks > 0);
-      }
-      mma_commit(smem_u32(&bar_mma));
-    }
-    mma_pending = true;
-    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
-    mma_phase ^= 1;
-    mma_pending = !ok;
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-    fetch_qk(c + 1);  // the QK tile is free again: next chunk's rows load behind this one
-
-    // ---- P = tril(1 + A + A^2/2) for row `row`, columns [64 half, 64 half + 64)
-    {
-      float p[64];
-#pragma unroll
-      for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tlane + kColQK + 64 * half + c0, *reinterpret_cast<float(*)[16]>(p + c0));
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float x = p[j];
-        p[j] = (64 * half + j <= row && valid) ? fmaf(0.5f * x, x, 1.f + x) : 0.f;
-      }
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<uint4*>(sm + kOffP + sw128_off(row, 64 * half + 8 * q, kC)) = pack8_bf16(p + 8 * q);
-    }
-    ok = ok && mbar_wait(smem_u32(&bar_tma[c & 1]), (uint32_t)((c >> 1) & 1), status);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-
-    // ---- MMA 2: Acc += P [V | 1] ; [c | z] += Phi_K^T [V | 1]
-    const uint32_t vt = sbase + kOffV + (uint32_t)(c & 1) * 16384u;
-    const uint32_t lbo = sbase + kOffOnes - vt;  // distance from the V block to the [.. | 1] block
-    if (tid == 0) {
-      const uint32_t id = idesc_bf16(128, 80, 0, 1);
-      const uint32_t id0 = idesc_bf16(128, 80, 1, 1), id1 = idesc_bf16(64, 80, 1, 1);
-#pragma unroll
-      for (int ks = 0; ks < kC / 16; ++ks) {
-        const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-        const uint64_t bv = sw128_desc(vt + ks * 2048, lbo, 1024);
-        mma_bf16(tmem + kColAcc, kmaj(sbase + kOffP + aoff), bv, id, 1u);
-        mma_bf16(tmem + kColC0, sw128_desc(sbase + kOffPhiK + ks * 2048, 16384, 1024), bv, id0, 1u);
-        mma_bf16(tmem + kColC1, sw128_desc(sbase + kOffPhiK + 2 * 16384 + ks * 2048, 16384, 1024), bv, id1, 1u);
-      }
-      mma_commit(smem_u32(&bar_mma));
-    }
-    mma_pending = true;
-    ok = ok && mbar_wait(smem_u32(&bar_mma), mma_phase, status);
-    mma_phase ^= 1;
-    mma_pending = !ok;
-    if (__syncthreads_or(!ok)) break;
-    tc_fence_after();
-
-    // ---- outputs y = Acc / (Acc[64] + eps) (this thread: 32 columns); refresh the bf16 c and z tiles
-    {
-      float d[16], y[32], v[kDv], zz[16];
-      tmem_ld16(tlane + kColAcc + 64, d);
-      tmem_ld16(tlane + kColAcc + 32 * half, *reinterpret_cast<float(*)[16]>(y));
-      tmem_ld16(tlane + kColAcc + 32 * half + 16, *reinterpret_cast<float(*)[16]>(y + 16));
-#pragma unroll
-      for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + my_colc + c0, *reinterpret_cast<float(*)[16]>(v + c0));
-      tmem_ld16(tlane + my_colc + kDv, zz);
-      tmem_ld_wait();
-      if (valid) {
-        const float inv = 1.f / (d[0] + a.eps);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) y[j] *= inv;
-        TOut* yrow = reinterpret_cast<TOut*>(a.y) + b * a.y_sb + h * a.y_sh + t * a.y_st + 32 * half;
-        store_row32<TOut>(yrow, y);
-      }
+      for (int c = 0; c < kDv + 16; c += 16) tmem_st16(tlane + my_colc + c, *reinterpret_cast<float(*)[16]>(v + c));
       if (my_feature >= 0) {
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(my_feature, 8 * q, 192)) = pack8_bf16(v + 8 * q);
-        *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(zz[0]);
+        *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(v[kDv]);
       }
+      tmem_st_wait();
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0 && c + 2 < nchunks) {
-      issue_tma(c + 2);
-      tma_issued = c + 3;
-    }
-  }
-  cp_async_wait_all();
 
-  if (ok) {
-    // ---- final state in the 273-row basis: s_out = s_in + expand(c - c_in).
-    // Every 273-basis row belongs to exactly one compact feature, and a row of
-    // s_in / z_in is read before the same row of s_out / z_out is written, so
-    // the update may run in place (s_out == s_in).
-    float* s_out = a.s_out + bh * kDfull * kDv;
-    float* z_out = a.z_out + bh * kDfull;
-    const int j = my_feature;
-    float cur[kDv], zz[16];
+    bool ok = true;
+    for (int c = 0; c < nchunks; ++c) {
+      const uint32_t par = (uint32_t)(c & 1);
+      const int64_t t = (int64_t)c * kC + row;
+      const bool valid = t < N;
+      // ---- this chunk's q, k rows are in: the issuer starts Q K^T
+      cp_async_wait_all();
+      named_bar_sync(kBarWorkers, kWorkers);  // every row (and, for c = 0, the constant and state tiles) is in
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_qkin));
+      // ---- compact features of this row's q and k; this thread writes features [80 half, 80 half + 80)
+      {
+        float xq[kF], xk[kF];
+        const __nv_bfloat16* hq = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 0, kC));
+        const __nv_bfloat16* hq2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 8, kC));
+        const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 16, kC));
+        const __nv_bfloat16* hk2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 24, kC));
 #pragma unroll
-    for (int c0 = 0; c0 < kDv; c0 += 16) tmem_ld16(tlane + my_colc + c0, *reinterpret_cast<float(*)[16]>(cur + c0));
-    tmem_ld16(tlane + my_colc + kDv, zz);
-    tmem_ld_wait();
-    if (j >= 0 && j < kDcUsed) {
-      float prev[kDv];
-      compact_row(j, prev);
-      const float zprev = compact_z(j);
-      int r0, r1;
-      float sc;
-      const int n = full_rows_of(j, r0, r1, sc);
-      for (int k = 0; k < n; ++k) {
-        const int r = k == 0 ? r0 : r1;
-#pragma unroll
-        for (int cc = 0; cc < kDv; cc += 4) {
-          float4 base = s_in ? *reinterpret_cast<const float4*>(s_in + r * kDv + cc) : make_float4(0.f, 0.f, 0.f, 0.f);
-          base.x += (cur[cc] - prev[cc]) * sc;
-          base.y += (cur[cc + 1] - prev[cc + 1]) * sc;
-          base.z += (cur[cc + 2] - prev[cc + 2]) * sc;
-          base.w += (cur[cc + 3] - prev[cc + 3]) * sc;
-          *reinterpret_cast<float4*>(s_out + r * kDv + cc) = base;
+        for (int i = 0; i < 8; ++i) {
+          xq[i] = __bfloat162float(hq[i]);
+          xq[8 + i] = __bfloat162float(hq2[i]);
+          xk[i] = __bfloat162float(hk[i]);
+          xk[8 + i] = __bfloat162float(hk2[i]);
         }
-        const float zb = z_in ? z_in[r] : 0.f;
-        z_out[r] = zb + (zz[0] - zprev) * sc;
+        if (half == 0) {
+          store_features80<0>(sm + kOffPhiQ, row, xq);
+          store_features80<0>(sm + kOffPhiK, row, xk);
+          // a padded token must not add its constant feature to the state
+          if (!valid) *reinterpret_cast<__nv_bfloat16*>(sm + kOffPhiK + sw128_off(row, 0, kC)) = __float2bfloat16_rn(0.f);
+        } else {
+          store_features80<80>(sm + kOffPhiQ, row, xq);
+          store_features80<80>(sm + kOffPhiK, row, xk);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&bar_feat));  // with last chunk's refreshed c / z tiles: the readout may start
+
+      // ---- P = tril(1 + A + A^2/2) for row `row`, columns [64 half, 64 half + 64)
+      ok = wait(&bar_qk, par);
+      if (named_bar_or(kBarWorkers, kWorkers, !ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+#pragma unroll
+      for (int hp = 0; hp < 2; ++hp) {
+        float p[32];
+        tmem_ld16(tlane + kColQK + 64 * half + 32 * hp, *reinterpret_cast<float(*)[16]>(p));
+        tmem_ld16(tlane + kColQK + 64 * half + 32 * hp + 16, *reinterpret_cast<float(*)[16]>(p + 16));
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x = p[j];
+          p[j] = (64 * half + 32 * hp + j <= row && valid) ? fmaf(0.5f * x, x, 1.f + x) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(sm + kOffP + sw128_off(row, 64 * half + 32 * hp + 8 * q, kC)) =
+              pack8_bf16(p + 8 * q);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_p));
+      // every worker is past the features (the QK tile) and Q K^T has completed: next chunk's rows load
+      named_bar_sync(kBarWorkers, kWorkers);
+      fetch_qk(c + 1);
+
+      // ---- outputs y = Acc / (Acc[64] + eps) (this thread: 32 columns); refresh the bf16 c and z tiles
+      ok = wait(&bar_pv, par);
+      if (named_bar_or(kBarWorkers, kWorkers, !ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        float d[16], y[32];
+        tmem_ld16(tlane + kColAcc + 64, d);
+        tmem_ld16(tlane + kColAcc + 32 * half, *reinterpret_cast<float(*)[16]>(y));
+        tmem_ld16(tlane + kColAcc + 32 * half + 16, *reinterpret_cast<float(*)[16]>(y + 16));
+        tmem_ld_wait();
+        if (valid) {
+          const float inv = 1.f / (d[0] + a.eps);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) y[j] *= inv;
+          TOut* yrow = reinterpret_cast<TOut*>(a.y) + b * a.y_sb + h * a.y_sh + t * a.y_st + 32 * half;
+          store_row32<TOut>(yrow, y);
+        }
+      }
+      // tensor-memory loads are warp-collective: every lane loads, lanes without a feature do not store
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+        float v[32];
+        tmem_ld16(tlane + my_colc + 32 * hv, *reinterpret_cast<float(*)[16]>(v));
+        tmem_ld16(tlane + my_colc + 32 * hv + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+        tmem_ld_wait();
+        if (my_feature >= 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(my_feature, 32 * hv + 8 * q, 192)) = pack8_bf16(v + 8 * q);
+        }
+      }
+      {
+        float zz[16];
+        tmem_ld16(tlane + my_colc + kDv, zz);
+        tmem_ld_wait();
+        if (my_feature >= 0)
+          *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(zz[0]);
+      }
+      tc_fence_before();  // the tensor-memory reads above precede the next chunk's MMAs
+    }
+    cp_async_wait_all();
+
+    if (ok) {
+      // ---- final state in the 273-row basis: s_out = s_in + expand(c - c_in).
+      // Every 273-basis row belongs to exactly one compact feature, and a row of
+      // s_in / z_in is read before the same row of s_out / z_out is written, so
+      // the update may run in place (s_out == s_in).
+      float* s_out = a.s_out + bh * kDfull * kDv;
+      float* z_out = a.z_out + bh * kDfull;
+      const int j = my_feature;
+      const bool has = j >= 0 && j < kDcUsed;
+      float prev[kDv];
+      compact_row(j, prev);  // zeros when j has no full-basis rows
+      const float zprev = compact_z(j);
+      int r0 = 0, r1 = -1;
+      float sc = 1.f;
+      const int n = has ? full_rows_of(j, r0, r1, sc) : 0;
+      // tensor-memory loads are warp-collective: every lane loads, lanes without a feature write nothing
+      float zz[16];
+      tmem_ld16(tlane + my_colc + kDv, zz);
+      tmem_ld_wait();
+      {
+#pragma unroll
+        for (int hv = 0; hv < 2; ++hv) {
+          float cur[32];
+          tmem_ld16(tlane + my_colc + 32 * hv, *reinterpret_cast<float(*)[16]>(cur));
+          tmem_ld16(tlane + my_colc + 32 * hv + 16, *reinterpret_cast<float(*)[16]>(cur + 16));
+          tmem_ld_wait();
+          for (int k = 0; k < n; ++k) {
+            const int r = k == 0 ? r0 : r1;
+#pragma unroll
+            for (int cc = 0; cc < 32; cc += 4) {
+              const int col = 32 * hv + cc;
+              float4 base = s_in ? *reinterpret_cast<const float4*>(s_in + r * kDv + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+              base.x += (cur[cc] - prev[col]) * sc;
+              base.y += (cur[cc + 1] - prev[col + 1]) * sc;
+              base.z += (cur[cc + 2] - prev[col + 2]) * sc;
+              base.w += (cur[cc + 3] - prev[col + 3]) * sc;
+              *reinterpret_cast<float4*>(s_out + r * kDv + col) = base;
+            }
+          }
+        }
+        for (int k = 0; k < n; ++k) {
+          const int r = k == 0 ? r0 : r1;
+          const float zb = z_in ? z_in[r] : 0.f;
+          z_out[r] = zb + (zz[0] - zprev) * sc;
+        }
       }
     }
-  } else if (tid == 0) {
-    for (int k = c; k < tma_issued; ++k) mbar_wait(smem_u32(&bar_tma[k & 1]), (uint32_t)((k >> 1) & 1), status);
-    if (mma_pending) mbar_wait(smem_u32(&bar_mma), mma_phase, status);
   }
   tc_fence_before();
   __syncthreads();
@@ -489,7 +561,7 @@ cudaError_t launch_typed(const TaylorPrefillLaunch& a, unsigned* status, cudaStr
                                     (int)kSmemAlloc);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  taylor_chunked_kernel<TOut><<<(unsigned)(a.B * a.H), kThreads, kSmemAlloc, stream>>>(mv, a, status);
+  taylor_chunked_kernel<TOut><<<(unsigned)(a.B * a.H), kBlock, kSmemAlloc, stream>>>(mv, a, status);
   return cudaGetLastError();
 }
 
