@@ -54,7 +54,7 @@ constexpr float kInvSqrt2 = 0.70710678118654752f;
 // shared memory (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffV = 0;                      // 2 stages x bf16 V [128 tokens][64] (16 KB each)
 constexpr uint32_t kOffOnes = 32768;               // bf16 [128 tokens][64], column 0 = 1: the "1" of [V | 1]
-constexpr uint32_t kOffQK = kOffOnes + 16384;      // bf16 [128 tokens][64]: cols 0..15 q, 16..31 k
+constexpr uint32_t kOffQK = kOffOnes + 16384;      // bf16 [128 tokens][64]: q, k at cols 32p..32p+15, 32p+16..32p+31 for chunk parity p
 constexpr uint32_t kOffPhiQ = kOffQK + 16384;      // bf16 [128 tokens][192] (3 blocks of 16 KB)
 constexpr uint32_t kOffPhiK = kOffPhiQ + 49152;    // bf16 [128 tokens][192]
 constexpr uint32_t kOffP = kOffPhiK + 49152;       // bf16 [128 r][128 j] (2 blocks of 16 KB)
@@ -67,8 +67,8 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 // tensor memory columns; N = 80 accumulators: columns 0..63 = v, column 64 = the "1" column
 constexpr uint32_t kColC0 = 0;     // [c | z], features 0..127 (M = 128: lane = feature)
 constexpr uint32_t kColC1 = 96;    // [c | z], features 128..191 (M = 64 layout)
-constexpr uint32_t kColAcc = 192;  // [numerator | denominator] per token
-constexpr uint32_t kColQK = 320;   // Q K^T [r][j], 128 cols
+constexpr uint32_t kColAcc = 192;  // 2 x [numerator | denominator] per token (80 columns each), by chunk parity
+constexpr uint32_t kColQK = 384;   // Q K^T [r][j], 128 cols
 constexpr uint32_t kTmemCols = 512;
 
 __device__ __forceinline__ uint64_t kmaj(uint32_t addr) { return sw128_desc(addr, 0, 1024); }
@@ -160,9 +160,10 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_tma[2];  // V tile of the chunk landed, by stage
   __shared__ uint64_t bar_qk;      // Q K^T computed
-  __shared__ uint64_t bar_pv;      // readout, state update and P [V | 1] computed
+  __shared__ uint64_t bar_r1;      // readout and state update computed
+  __shared__ uint64_t bar_pv[2];   // P [V | 1] (and everything before it) computed, by chunk parity
   __shared__ uint64_t bar_qkin;    // workers: this chunk's q, k rows are in the QK tile
-  __shared__ uint64_t bar_feat;    // workers: Phi_Q, Phi_K written and the c / z tiles refreshed
+  __shared__ uint64_t bar_feat;    // workers: Phi_Q, Phi_K written and the c / z tiles refreshed (next readout)
   __shared__ uint64_t bar_p;       // workers: P written
   __shared__ uint64_t bar_fin;     // drain after an expired wait
   __shared__ uint32_t tmem_base_sh;
@@ -187,7 +188,9 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     mbar_init(smem_u32(&bar_tma[0]), 1);
     mbar_init(smem_u32(&bar_tma[1]), 1);
     mbar_init(smem_u32(&bar_qk), 1);
-    mbar_init(smem_u32(&bar_pv), 1);
+    mbar_init(smem_u32(&bar_r1), 1);
+    mbar_init(smem_u32(&bar_pv[0]), 1);
+    mbar_init(smem_u32(&bar_pv[1]), 1);
     mbar_init(smem_u32(&bar_qkin), kWorkers);
     mbar_init(smem_u32(&bar_feat), kWorkers);
     mbar_init(smem_u32(&bar_p), kWorkers);
@@ -233,7 +236,8 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       if (!ok) break;
       tc_fence_after();
       if (leader) {
-        mma_bf16(tmem + kColQK, kmaj(sbase + kOffQK), kmaj(sbase + kOffQK + 32), idesc_bf16(128, 128, 0, 0), 0u);
+        const uint32_t qk = sbase + kOffQK + par * 64u;  // this chunk's half of the QK tile
+        mma_bf16(tmem + kColQK, kmaj(qk), kmaj(qk + 32), idesc_bf16(128, 128, 0, 0), 0u);
         mma_commit(smem_u32(&bar_qk));
       }
       __syncwarp();
@@ -245,6 +249,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       tc_fence_after();
       const uint32_t vt = sbase + kOffV + (uint32_t)(c & 1) * 16384u;
       const uint32_t lbo = sbase + kOffOnes - vt;  // distance from the V block to the [.. | 1] block
+      const uint32_t acc = tmem + kColAcc + par * 80u;
       if (leader) {
         const uint32_t id = idesc_bf16(128, 64, 0, 1);
         const uint32_t idz = idesc_bf16(128, 16, 0, 0);
@@ -252,9 +257,8 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         for (int ks = 0; ks < kDc / 16; ++ks) {
           const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
           const uint32_t zoff = (uint32_t)(ks >> 2) * 2048u + (uint32_t)(ks & 3) * 32u;
-          mma_bf16(tmem + kColAcc, kmaj(sbase + kOffPhiQ + aoff), sw128_desc(sbase + kOffCt + ks * 2048, 0, 1024), id,
-                   ks > 0);
-          mma_bf16(tmem + kColAcc + 64, kmaj(sbase + kOffPhiQ + aoff), kmaj(sbase + kOffZt + zoff), idz, ks > 0);
+          mma_bf16(acc, kmaj(sbase + kOffPhiQ + aoff), sw128_desc(sbase + kOffCt + ks * 2048, 0, 1024), id, ks > 0);
+          mma_bf16(acc + 64, kmaj(sbase + kOffPhiQ + aoff), kmaj(sbase + kOffZt + zoff), idz, ks > 0);
         }
         const uint32_t id0 = idesc_bf16(128, 80, 1, 1), id1 = idesc_bf16(64, 80, 1, 1);
 #pragma unroll
@@ -263,6 +267,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
           mma_bf16(tmem + kColC0, sw128_desc(sbase + kOffPhiK + ks * 2048, 16384, 1024), bv, id0, 1u);
           mma_bf16(tmem + kColC1, sw128_desc(sbase + kOffPhiK + 2 * 16384 + ks * 2048, 16384, 1024), bv, id1, 1u);
         }
+        mma_commit(smem_u32(&bar_r1));
       }
       __syncwarp();
       // P [V | 1] -> Acc once P is written
@@ -274,14 +279,14 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
 #pragma unroll
         for (int ks = 0; ks < kC / 16; ++ks) {
           const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-          mma_bf16(tmem + kColAcc, kmaj(sbase + kOffP + aoff), sw128_desc(vt + ks * 2048, lbo, 1024), id, 1u);
+          mma_bf16(acc, kmaj(sbase + kOffP + aoff), sw128_desc(vt + ks * 2048, lbo, 1024), id, 1u);
         }
-        mma_commit(smem_u32(&bar_pv));
+        mma_commit(smem_u32(&bar_pv[par]));
       }
       __syncwarp();
       // the V stage of chunk c is free once its MMAs completed: load chunk c+2 into it
       if (c + 2 < nchunks) {
-        ok = wait(&bar_pv, par);
+        ok = wait(&bar_pv[par], (uint32_t)((c >> 1) & 1));
         if (!ok) break;
         if (leader) issue_tma(c + 2);
         __syncwarp();
@@ -301,17 +306,18 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   } else {
     // ================================================================ workers: two threads per token row
     if (tid < kC) *reinterpret_cast<__nv_bfloat16*>(sm + kOffOnes + sw128_off(tid, 0, kC)) = __float2bfloat16_rn(1.f);
-    // q (half 0) or k (half 1) row of chunk cc into the QK tile, asynchronously
+    // q (half 0) or k (half 1) row of chunk cc into its half of the QK tile, asynchronously
     auto fetch_qk = [&](int cc) {
       const int64_t t = (int64_t)cc * kC + row;
       const bool in = cc < nchunks && t < N;
       const __nv_bfloat16* src = half == 0 ? qp + (in ? t : 0) * a.q.st : kp + (in ? t : 0) * a.k.st;
-      cp_async16(sbase + kOffQK + sw128_off(row, 16 * half, kC), src, in ? 16u : 0u);
-      cp_async16(sbase + kOffQK + sw128_off(row, 16 * half + 8, kC), src + 8, in ? 16u : 0u);
+      const int col = 32 * (cc & 1) + 16 * half;
+      cp_async16(sbase + kOffQK + sw128_off(row, col, kC), src, in ? 16u : 0u);
+      cp_async16(sbase + kOffQK + sw128_off(row, col + 8, kC), src + 8, in ? 16u : 0u);
       cp_async_commit();
     };
     fetch_qk(0);
-
+    fetch_qk(1);
     // ---- initial compact state c_in (fp32 in TMEM, bf16 tile) and z_in
     const float* s_in = a.s_in ? a.s_in + bh * kDfull * kDv : nullptr;
     const float* z_in = a.z_in ? a.z_in + bh * kDfull : nullptr;
@@ -358,96 +364,63 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       tmem_st_wait();
     }
 
-    bool ok = true;
-    for (int c = 0; c < nchunks; ++c) {
-      const uint32_t par = (uint32_t)(c & 1);
-      const int64_t t = (int64_t)c * kC + row;
-      const bool valid = t < N;
-      // ---- this chunk's q, k rows are in: the issuer starts Q K^T
-      cp_async_wait_all();
-      named_bar_sync(kBarWorkers, kWorkers);  // every row (and, for c = 0, the constant and state tiles) is in
+    // ---- per-chunk worker passes
+    // q, k rows of chunk cc (half cc & 1 of the QK tile) into this thread's 16 floats each
+    auto read_qk = [&](int cc, float* xq, float* xk) {
+      const int c0 = 32 * (cc & 1);
+      const __nv_bfloat16* hq = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, c0, kC));
+      const __nv_bfloat16* hq2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, c0 + 8, kC));
+      const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, c0 + 16, kC));
+      const __nv_bfloat16* hk2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, c0 + 24, kC));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        xq[i] = __bfloat162float(hq[i]);
+        xq[8 + i] = __bfloat162float(hq2[i]);
+        xk[i] = __bfloat162float(hk[i]);
+        xk[8 + i] = __bfloat162float(hk2[i]);
+      }
+    };
+    // compact features of chunk cc's q and k rows; this thread writes features [80 half, 80 half + 80)
+    auto features = [&](int cc) {
+      float xq[kF], xk[kF];
+      read_qk(cc, xq, xk);
+      const bool valid = (int64_t)cc * kC + row < N;
+      if (half == 0) {
+        store_features80<0>(sm + kOffPhiQ, row, xq);
+        store_features80<0>(sm + kOffPhiK, row, xk);
+        // a padded token must not add its constant feature to the state
+        if (!valid) *reinterpret_cast<__nv_bfloat16*>(sm + kOffPhiK + sw128_off(row, 0, kC)) = __float2bfloat16_rn(0.f);
+      } else {
+        store_features80<80>(sm + kOffPhiQ, row, xq);
+        store_features80<80>(sm + kOffPhiK, row, xk);
+      }
+    };
+    // chunk cc's rows are in (this thread's cp.async groups up to cc have landed): the issuer may start Q K^T
+    auto announce_qk = [&]() {
+      named_bar_sync(kBarWorkers, kWorkers);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&bar_qkin));
-      // ---- compact features of this row's q and k; this thread writes features [80 half, 80 half + 80)
-      {
-        float xq[kF], xk[kF];
-        const __nv_bfloat16* hq = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 0, kC));
-        const __nv_bfloat16* hq2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 8, kC));
-        const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 16, kC));
-        const __nv_bfloat16* hk2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, 24, kC));
+    };
+    // outputs of chunk cc: y = Acc / (Acc[64] + eps), this thread 32 columns
+    auto outputs = [&](int cc) {
+      const uint32_t acc = tlane + kColAcc + (uint32_t)(cc & 1) * 80u;
+      float d[16], y[32];
+      tmem_ld16(acc + 64, d);
+      tmem_ld16(acc + 32 * half, *reinterpret_cast<float(*)[16]>(y));
+      tmem_ld16(acc + 32 * half + 16, *reinterpret_cast<float(*)[16]>(y + 16));
+      tmem_ld_wait();
+      const int64_t t = (int64_t)cc * kC + row;
+      if (t < N) {
+        const float inv = 1.f / (d[0] + a.eps);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          xq[i] = __bfloat162float(hq[i]);
-          xq[8 + i] = __bfloat162float(hq2[i]);
-          xk[i] = __bfloat162float(hk[i]);
-          xk[8 + i] = __bfloat162float(hk2[i]);
-        }
-        if (half == 0) {
-          store_features80<0>(sm + kOffPhiQ, row, xq);
-          store_features80<0>(sm + kOffPhiK, row, xk);
-          // a padded token must not add its constant feature to the state
-          if (!valid) *reinterpret_cast<__nv_bfloat16*>(sm + kOffPhiK + sw128_off(row, 0, kC)) = __float2bfloat16_rn(0.f);
-        } else {
-          store_features80<80>(sm + kOffPhiQ, row, xq);
-          store_features80<80>(sm + kOffPhiK, row, xk);
-        }
+        for (int j = 0; j < 32; ++j) y[j] *= inv;
+        TOut* yrow = reinterpret_cast<TOut*>(a.y) + b * a.y_sb + h * a.y_sh + t * a.y_st + 32 * half;
+        store_row32<TOut>(yrow, y);
       }
-      fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&bar_feat));  // with last chunk's refreshed c / z tiles: the readout may start
-
-      // ---- P = tril(1 + A + A^2/2) for row `row`, columns [64 half, 64 half + 64)
-      ok = wait(&bar_qk, par);
-      if (named_bar_or(kBarWorkers, kWorkers, !ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int hp = 0; hp < 2; ++hp) {
-        float p[32];
-        tmem_ld16(tlane + kColQK + 64 * half + 32 * hp, *reinterpret_cast<float(*)[16]>(p));
-        tmem_ld16(tlane + kColQK + 64 * half + 32 * hp + 16, *reinterpret_cast<float(*)[16]>(p + 16));
-        tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float x = p[j];
-          p[j] = (64 * half + 32 * hp + j <= row && valid) ? fmaf(0.5f * x, x, 1.f + x) : 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(sm + kOffP + sw128_off(row, 64 * half + 32 * hp + 8 * q, kC)) =
-              pack8_bf16(p + 8 * q);
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bar_p));
-      // every worker is past the features (the QK tile) and Q K^T has completed: next chunk's rows load
-      named_bar_sync(kBarWorkers, kWorkers);
-      fetch_qk(c + 1);
-
-      // ---- outputs y = Acc / (Acc[64] + eps) (this thread: 32 columns); refresh the bf16 c and z tiles
-      ok = wait(&bar_pv, par);
-      if (named_bar_or(kBarWorkers, kWorkers, !ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      {
-        float d[16], y[32];
-        tmem_ld16(tlane + kColAcc + 64, d);
-        tmem_ld16(tlane + kColAcc + 32 * half, *reinterpret_cast<float(*)[16]>(y));
-        tmem_ld16(tlane + kColAcc + 32 * half + 16, *reinterpret_cast<float(*)[16]>(y + 16));
-        tmem_ld_wait();
-        if (valid) {
-          const float inv = 1.f / (d[0] + a.eps);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) y[j] *= inv;
-          TOut* yrow = reinterpret_cast<TOut*>(a.y) + b * a.y_sb + h * a.y_sh + t * a.y_st + 32 * half;
-          store_row32<TOut>(yrow, y);
-        }
-      }
-      // tensor-memory loads are warp-collective: every lane loads, lanes without a feature do not store
+    };
+    // bf16 c and z tiles for the next readout from the tensor-memory state (warp-collective loads)
+    auto refresh_state_tiles = [&]() {
 #pragma unroll
       for (int hv = 0; hv < 2; ++hv) {
         float v[32];
@@ -460,14 +433,95 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
             *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(my_feature, 32 * hv + 8 * q, 192)) = pack8_bf16(v + 8 * q);
         }
       }
-      {
-        float zz[16];
-        tmem_ld16(tlane + my_colc + kDv, zz);
-        tmem_ld_wait();
-        if (my_feature >= 0)
-          *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(zz[0]);
+      float zz[16];
+      tmem_ld16(tlane + my_colc + kDv, zz);
+      tmem_ld_wait();
+      if (my_feature >= 0)
+        *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(zz[0]);
+    };
+
+    bool ok = true;
+    // prologue: chunk 0's rows and features
+    cp_async_wait_all_but_one();  // chunk 1's rows may still be in flight
+    announce_qk();
+    features(0);
+    fence_proxy_async_smem();
+    mbar_arrive(smem_u32(&bar_feat));
+    for (int c = 0; c < nchunks; ++c) {
+      const uint32_t par = (uint32_t)(c & 1);
+      const bool has_next = c + 1 < nchunks;
+      // ---- P = tril(1 + A + A^2/2) of chunk c, row `row`, columns [64 half, 64 half + 64), while the
+      //      readout and state update of chunk c run
+      ok = wait(&bar_qk, par);
+      if (named_bar_or(kBarWorkers, kWorkers, !ok)) {
+        ok = false;
+        break;
       }
-      tc_fence_before();  // the tensor-memory reads above precede the next chunk's MMAs
+      tc_fence_after();
+      {
+        const bool valid = (int64_t)c * kC + row < N;
+#pragma unroll
+        for (int hp = 0; hp < 2; ++hp) {
+          float p[32];
+          tmem_ld16(tlane + kColQK + 64 * half + 32 * hp, *reinterpret_cast<float(*)[16]>(p));
+          tmem_ld16(tlane + kColQK + 64 * half + 32 * hp + 16, *reinterpret_cast<float(*)[16]>(p + 16));
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float x = p[j];
+            p[j] = (64 * half + 32 * hp + j <= row && valid) ? fmaf(0.5f * x, x, 1.f + x) : 0.f;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(sm + kOffP + sw128_off(row, 64 * half + 32 * hp + 8 * q, kC)) =
+                pack8_bf16(p + 8 * q);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&bar_p));
+      // ---- outputs of the previous chunk (its P [V | 1] completed long ago)
+      if (c > 0) {
+        ok = wait(&bar_pv[par ^ 1u], (uint32_t)(((c - 1) >> 1) & 1));
+        if (named_bar_or(kBarWorkers, kWorkers, !ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        outputs(c - 1);
+      }
+      // ---- next chunk's rows: Q K^T may start (its tensor-memory columns were read above)
+      if (has_next) {
+        cp_async_wait_all();
+        announce_qk();
+        // the QK tile half of chunk c is free (Q K^T of chunk c done, every worker past its features)
+        fetch_qk(c + 2);
+      }
+      // ---- once the readout and state update of chunk c are done: state tiles and next features
+      ok = wait(&bar_r1, par);
+      if (named_bar_or(kBarWorkers, kWorkers, !ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (has_next) {
+        refresh_state_tiles();
+        features(c + 1);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bar_feat));
+      }
+    }
+    if (ok && nchunks > 0) {
+      // outputs of the last chunk
+      const int c = nchunks - 1;
+      ok = wait(&bar_pv[c & 1], (uint32_t)((c >> 1) & 1));
+      if (!named_bar_or(kBarWorkers, kWorkers, !ok)) {
+        tc_fence_after();
+        outputs(c);
+      } else {
+        ok = false;
+      }
     }
     cp_async_wait_all();
 
