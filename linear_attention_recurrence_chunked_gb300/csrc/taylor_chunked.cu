@@ -139,6 +139,24 @@ __device__ __forceinline__ int feature_of_lane(int lane) {
   return w < 16 ? 128 + q * 16 + w : -1;
 }
 
+// Eight bf16 values of a 16-byte vector as floats.
+__device__ __forceinline__ void unpack8_bf16(const uint4 u, float* x) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// One arrival per warp once every lane of it got here: each lane fenced its
+// own shared-memory writes for the async proxy and its tensor-memory accesses
+// before, and __syncwarp orders them before lane 0's release-arrive.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 template <typename T>
 __device__ __forceinline__ void store_row32(T* dst, const float* v);
 template <>
@@ -191,9 +209,9 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     mbar_init(smem_u32(&bar_r1), 1);
     mbar_init(smem_u32(&bar_pv[0]), 1);
     mbar_init(smem_u32(&bar_pv[1]), 1);
-    mbar_init(smem_u32(&bar_qkin), kWorkers);
-    mbar_init(smem_u32(&bar_feat), kWorkers);
-    mbar_init(smem_u32(&bar_p), kWorkers);
+    mbar_init(smem_u32(&bar_qkin), 1);               // one arrival after the workers' named barrier
+    mbar_init(smem_u32(&bar_feat), kWorkers / 32);   // one arrival per worker warp
+    mbar_init(smem_u32(&bar_p), kWorkers / 32);
     mbar_init(smem_u32(&bar_fin), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmap_v);
@@ -229,19 +247,22 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     }
     tma_issued = nchunks > 1 ? 2 : 1;
     __syncwarp();
-    for (int c = 0; c < nchunks && ok; ++c) {
-      const uint32_t par = (uint32_t)(c & 1);
-      // Q K^T as soon as the q, k rows are in
-      ok = wait(&bar_qkin, par);
-      if (!ok) break;
+    // Q K^T of chunk cc as soon as its q, k rows are in
+    auto issue_qk = [&](int cc) -> bool {
+      if (!wait(&bar_qkin, (uint32_t)(cc & 1))) return false;
       tc_fence_after();
       if (leader) {
-        const uint32_t qk = sbase + kOffQK + par * 64u;  // this chunk's half of the QK tile
+        const uint32_t qk = sbase + kOffQK + (uint32_t)(cc & 1) * 64u;  // this chunk's half of the QK tile
         mma_bf16(tmem + kColQK, kmaj(qk), kmaj(qk + 32), idesc_bf16(128, 128, 0, 0), 0u);
         mma_commit(smem_u32(&bar_qk));
       }
       __syncwarp();
       mma_issued = true;
+      return true;
+    };
+    ok = issue_qk(0);
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const uint32_t par = (uint32_t)(c & 1);
       // readout Phi_Q [c | z]_{<b} -> Acc and state update [c | z] += Phi_K^T [V | 1]
       ok = wait(&bar_feat, par) && wait(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1));
       if (!ok) break;
@@ -284,6 +305,11 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         mma_commit(smem_u32(&bar_pv[par]));
       }
       __syncwarp();
+      // Q K^T of the next chunk right behind P [V | 1] (the workers announce its rows after writing P)
+      if (c + 1 < nchunks) {
+        ok = issue_qk(c + 1);
+        if (!ok) break;
+      }
       // the V stage of chunk c is free once its MMAs completed: load chunk c+2 into it
       if (c + 2 < nchunks) {
         ok = wait(&bar_pv[par], (uint32_t)((c >> 1) & 1));
@@ -368,17 +394,10 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     // q, k rows of chunk cc (half cc & 1 of the QK tile) into this thread's 16 floats each
     auto read_qk = [&](int cc, float* xq, float* xk) {
       const int c0 = 32 * (cc & 1);
-      const __nv_bfloat16* hq = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, c0, kC));
-      const __nv_bfloat16* hq2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, c0 + 8, kC));
-      const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, c0 + 16, kC));
-      const __nv_bfloat16* hk2 = reinterpret_cast<const __nv_bfloat16*>(sm + kOffQK + sw128_off(row, c0 + 24, kC));
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        xq[i] = __bfloat162float(hq[i]);
-        xq[8 + i] = __bfloat162float(hq2[i]);
-        xk[i] = __bfloat162float(hk[i]);
-        xk[8 + i] = __bfloat162float(hk2[i]);
-      }
+      for (int i = 0; i < 4; ++i)
+        unpack8_bf16(*reinterpret_cast<const uint4*>(sm + kOffQK + sw128_off(row, c0 + 8 * i, kC)),
+                     i < 2 ? xq + 8 * i : xk + 8 * (i - 2));
     };
     // compact features of chunk cc's q and k rows; this thread writes features [80 half, 80 half + 80)
     auto features = [&](int cc) {
@@ -397,10 +416,10 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     };
     // chunk cc's rows are in (this thread's cp.async groups up to cc have landed): the issuer may start Q K^T
     auto announce_qk = [&]() {
-      named_bar_sync(kBarWorkers, kWorkers);
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_qkin));
+      named_bar_sync(kBarWorkers, kWorkers);
+      if (tid == 0) mbar_arrive(smem_u32(&bar_qkin));
     };
     // outputs of chunk cc: y = Acc / (Acc[64] + eps), this thread 32 columns
     auto outputs = [&](int cc) {
@@ -440,90 +459,94 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(zz[0]);
     };
 
+    // Error path: a wait that expires sets the status word and leaves this thread's `ok` false; the
+    // thread then skips its later waits (so it meets at most one expiry) but still passes every named
+    // barrier and arrival, so no other thread is left waiting on it, and the final state is not written.
+    // The workers need no agreement barrier after their waits.
     bool ok = true;
     // prologue: chunk 0's rows and features
     cp_async_wait_all_but_one();  // chunk 1's rows may still be in flight
     announce_qk();
     features(0);
     fence_proxy_async_smem();
-    mbar_arrive(smem_u32(&bar_feat));
+    tc_fence_before();
+    warp_arrive(smem_u32(&bar_feat));
     for (int c = 0; c < nchunks; ++c) {
       const uint32_t par = (uint32_t)(c & 1);
       const bool has_next = c + 1 < nchunks;
       // ---- P = tril(1 + A + A^2/2) of chunk c, row `row`, columns [64 half, 64 half + 64), while the
       //      readout and state update of chunk c run
-      ok = wait(&bar_qk, par);
-      if (named_bar_or(kBarWorkers, kWorkers, !ok)) {
-        ok = false;
-        break;
-      }
+      ok = ok && wait(&bar_qk, par);
       tc_fence_after();
       {
         const bool valid = (int64_t)c * kC + row < N;
 #pragma unroll
         for (int hp = 0; hp < 2; ++hp) {
-          float p[32];
-          tmem_ld16(tlane + kColQK + 64 * half + 32 * hp, *reinterpret_cast<float(*)[16]>(p));
-          tmem_ld16(tlane + kColQK + 64 * half + 32 * hp + 16, *reinterpret_cast<float(*)[16]>(p + 16));
-          tmem_ld_wait();
+          // columns [base, base + nv) of this row are kept (inclusive causal mask); the branches are
+          // warp-uniform: whole 32-column groups above every row of the warp are zeros without a load
+          const int base = 64 * half + 32 * hp;
+          const int nv = valid ? row - base + 1 : 0;
+          uint8_t* prow = sm + kOffP;
+          if (__all_sync(0xffffffffu, nv <= 0)) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float x = p[j];
-            p[j] = (64 * half + 32 * hp + j <= row && valid) ? fmaf(0.5f * x, x, 1.f + x) : 0.f;
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(prow + sw128_off(row, base + 8 * q, kC)) = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+          }
+          float p[32];
+          tmem_ld16(tlane + kColQK + base, *reinterpret_cast<float(*)[16]>(p));
+          tmem_ld16(tlane + kColQK + base + 16, *reinterpret_cast<float(*)[16]>(p + 16));
+          tmem_ld_wait();
+          // 1 + x + x^2/2 as 1 + x (1 + x/2)
+          if (__all_sync(0xffffffffu, nv >= 32)) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) p[j] = fmaf(p[j], fmaf(0.5f, p[j], 1.f), 1.f);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) p[j] = j < nv ? fmaf(p[j], fmaf(0.5f, p[j], 1.f), 1.f) : 0.f;
           }
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(sm + kOffP + sw128_off(row, 64 * half + 32 * hp + 8 * q, kC)) =
-                pack8_bf16(p + 8 * q);
+            *reinterpret_cast<uint4*>(prow + sw128_off(row, base + 8 * q, kC)) = pack8_bf16(p + 8 * q);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_p));
-      // ---- outputs of the previous chunk (its P [V | 1] completed long ago)
-      if (c > 0) {
-        ok = wait(&bar_pv[par ^ 1u], (uint32_t)(((c - 1) >> 1) & 1));
-        if (named_bar_or(kBarWorkers, kWorkers, !ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        outputs(c - 1);
-      }
-      // ---- next chunk's rows: Q K^T may start (its tensor-memory columns were read above)
+      warp_arrive(smem_u32(&bar_p));
+      // ---- next chunk's rows: Q K^T of chunk c + 1 may start (every worker has read this chunk's Q K^T
+      //      columns above), so it runs while the outputs below are written
       if (has_next) {
         cp_async_wait_all();
         announce_qk();
         // the QK tile half of chunk c is free (Q K^T of chunk c done, every worker past its features)
         fetch_qk(c + 2);
       }
-      // ---- once the readout and state update of chunk c are done: state tiles and next features
-      ok = wait(&bar_r1, par);
-      if (named_bar_or(kBarWorkers, kWorkers, !ok)) {
-        ok = false;
-        break;
+      // ---- outputs of the previous chunk (its P [V | 1] completed long ago)
+      if (c > 0) {
+        ok = ok && wait(&bar_pv[par ^ 1u], (uint32_t)(((c - 1) >> 1) & 1));
+        tc_fence_after();
+        outputs(c - 1);
       }
+      // ---- once the readout and state update of chunk c are done: state tiles and next features
+      ok = ok && wait(&bar_r1, par);
       tc_fence_after();
       if (has_next) {
         refresh_state_tiles();
         features(c + 1);
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(smem_u32(&bar_feat));
+        warp_arrive(smem_u32(&bar_feat));
       }
     }
-    if (ok && nchunks > 0) {
+    if (nchunks > 0) {
       // outputs of the last chunk
       const int c = nchunks - 1;
-      ok = wait(&bar_pv[c & 1], (uint32_t)((c >> 1) & 1));
-      if (!named_bar_or(kBarWorkers, kWorkers, !ok)) {
-        tc_fence_after();
-        outputs(c);
-      } else {
-        ok = false;
-      }
+      ok = ok && wait(&bar_pv[c & 1], (uint32_t)((c >> 1) & 1));
+      tc_fence_after();
+      outputs(c);
     }
     cp_async_wait_all();
+    ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the final-state pass below uses warp-collective loads
 
     if (ok) {
       // ---- final state in the 273-row basis: s_out = s_in + expand(c - c_in).
