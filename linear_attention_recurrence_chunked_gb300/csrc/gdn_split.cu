@@ -294,10 +294,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
     mbar_init(smem_u32(&bar_s), 1);
     mbar_init(smem_u32(&bar_o[0]), 1);
     mbar_init(smem_u32(&bar_o[1]), 1);
-    mbar_init(smem_u32(&bar_ofree[0]), kOutThreads);
-    mbar_init(smem_u32(&bar_ofree[1]), kOutThreads);
-    mbar_init(smem_u32(&bar_s0), kChainThreads);
-    mbar_init(smem_u32(&bar_u), kChainThreads);
+    mbar_init(smem_u32(&bar_ofree[0]), kOutThreads / 32);  // one arrival per warp
+    mbar_init(smem_u32(&bar_ofree[1]), kOutThreads / 32);
+    mbar_init(smem_u32(&bar_s0), kChainThreads / 32);
+    mbar_init(smem_u32(&bar_u), kChainThreads / 32);
     mbar_init(smem_u32(&bar_fin), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmap_k);
@@ -441,15 +441,16 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    mbar_arrive(smem_u32(&bar_s0));
+    warp_arrive(smem_u32(&bar_s0));
     float sigma = 1.f;
+    // An expired wait leaves this thread's `ok` false: it skips its later waits (so it meets at most one
+    // expiry) but still makes every arrival, so no warp waits on it, and the final state is not written.
 
     for (int c = 0; c < nchunks; ++c) {
       const bool has_next = c + 1 < nchunks;
       const uint32_t par = (uint32_t)(c & 1);
-      ok = wait(&bar_stage[c & 1], (uint32_t)((c >> 1) & 1)) && wait(&bar_x, par) &&
+      ok = ok && wait(&bar_stage[c & 1], (uint32_t)((c >> 1) & 1)) && wait(&bar_x, par) &&
            (wk.zero_v || wait(&bar_ut, par));
-      if (!ok) break;
       tc_fence_after();
       // ---- U^T = U~^T - X and U^T diag(1 / (sigma gamma)), this row, columns [32 half, 32 half + 32)
       {
@@ -487,9 +488,8 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_u));
-      ok = wait(&bar_s, par);
-      if (!ok) break;
+      warp_arrive(smem_u32(&bar_u));
+      ok = ok && wait(&bar_s, par);
       tc_fence_after();
 
       // ---- sigma <- sigma gamma_C; bf16 S0 = sigma S~ for chunk c+1, folding sigma into S~ when small
@@ -522,10 +522,11 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
       if (has_next) {
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(smem_u32(&bar_s0));
+        warp_arrive(smem_u32(&bar_s0));
       }
     }
 
+    ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the final-state loads below are warp-collective
     if (ok && wk.s_exit) {
       // final state S = sigma S~: lane i row i, this thread's half of the columns
       float* dst = wk.s_exit + (int64_t)row * kD;
@@ -545,9 +546,10 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
   } else if (wk.write_out) {
     // ================================================================ output warps
     // O^T of chunk c: lane i = value index, columns = the chunk's 64 tokens.
+    bool ok = true;  // as in the chain warps: an expired wait skips the later waits, never an arrival
     for (int c = 0; c < nchunks; ++c) {
       const uint32_t par = (uint32_t)(c & 1);
-      if (!wait(&bar_o[par], (uint32_t)((c >> 1) & 1))) break;
+      ok = ok && wait(&bar_o[par], (uint32_t)((c >> 1) & 1));
       tc_fence_after();
       float o[64];
 #pragma unroll
@@ -555,7 +557,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
         tmem_ld16(tlane + kCColO + 64 * par + c0, *reinterpret_cast<float(*)[16]>(o + c0));
       tmem_ld_wait();
       tc_fence_before();
-      mbar_arrive(smem_u32(&bar_ofree[par]));  // the buffer may be overwritten from here on
+      warp_arrive(smem_u32(&bar_ofree[par]));  // the buffer may be overwritten from here on
       const int64_t t0 = wk.t_begin + (int64_t)c * kC;
       const int nvalid = (wk.t_end - t0 < kC) ? (int)(wk.t_end - t0) : kC;
       TOut* optr = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + t0 * a.o_st + row;

@@ -149,14 +149,6 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 u, float* x) {
   }
 }
 
-// One arrival per warp once every lane of it got here: each lane fenced its
-// own shared-memory writes for the async proxy and its tensor-memory accesses
-// before, and __syncwarp orders them before lane 0's release-arrive.
-__device__ __forceinline__ void warp_arrive(uint32_t bar) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
 template <typename T>
 __device__ __forceinline__ void store_row32(T* dst, const float* v);
 template <>
@@ -234,6 +226,8 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     // The whole warp walks the loop and waits (it stays converged for the
     // block-wide barrier at the end); lane 0 issues.
     const bool leader = (tid & 31) == 0;
+    // every lane waits; the result is made warp-uniform so that the lanes leave the loop together
+    auto iwait = [&](uint64_t* bar, uint32_t parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
     auto issue_tma = [&](int c) {
       const uint32_t bar = smem_u32(&bar_tma[c & 1]);
       mbar_arrive_expect_tx(bar, 16384);
@@ -249,7 +243,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     __syncwarp();
     // Q K^T of chunk cc as soon as its q, k rows are in
     auto issue_qk = [&](int cc) -> bool {
-      if (!wait(&bar_qkin, (uint32_t)(cc & 1))) return false;
+      if (!iwait(&bar_qkin, (uint32_t)(cc & 1))) return false;
       tc_fence_after();
       if (leader) {
         const uint32_t qk = sbase + kOffQK + (uint32_t)(cc & 1) * 64u;  // this chunk's half of the QK tile
@@ -264,7 +258,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     for (int c = 0; c < nchunks && ok; ++c) {
       const uint32_t par = (uint32_t)(c & 1);
       // readout Phi_Q [c | z]_{<b} -> Acc and state update [c | z] += Phi_K^T [V | 1]
-      ok = wait(&bar_feat, par) && wait(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1));
+      ok = iwait(&bar_feat, par) && iwait(&bar_tma[c & 1], (uint32_t)((c >> 1) & 1));
       if (!ok) break;
       tma_done = c + 1;
       tc_fence_after();
@@ -292,7 +286,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       }
       __syncwarp();
       // P [V | 1] -> Acc once P is written
-      ok = wait(&bar_p, par);
+      ok = iwait(&bar_p, par);
       if (!ok) break;
       tc_fence_after();
       if (leader) {
@@ -312,7 +306,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       }
       // the V stage of chunk c is free once its MMAs completed: load chunk c+2 into it
       if (c + 2 < nchunks) {
-        ok = wait(&bar_pv[par], (uint32_t)((c >> 1) & 1));
+        ok = iwait(&bar_pv[par], (uint32_t)((c >> 1) & 1));
         if (!ok) break;
         if (leader) issue_tma(c + 2);
         __syncwarp();
@@ -321,11 +315,11 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     }
     if (!ok) {
       // a wait expired: let this CTA's own copies and MMAs drain (bounded) before TMEM is freed
-      for (int k = tma_done; k < tma_issued; ++k) wait(&bar_tma[k & 1], (uint32_t)((k >> 1) & 1));
+      for (int k = tma_done; k < tma_issued; ++k) iwait(&bar_tma[k & 1], (uint32_t)((k >> 1) & 1));
       if (mma_issued) {
         if (leader) mma_commit(smem_u32(&bar_fin));
         __syncwarp();
-        wait(&bar_fin, 0);
+        iwait(&bar_fin, 0);
       }
     }
     __syncwarp();

@@ -54,6 +54,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// One arrival per warp once every lane of it got here: each lane fenced its
+// own shared-memory writes for the async proxy and its tensor-memory accesses
+// before, and __syncwarp orders them before lane 0's release-arrive.  Every
+// lane of the warp must call it.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 // Waits for phase `parity` of the barrier to complete; gives up after
 // limit_ns, ORs kStatusTimeout into *status and returns false.
 __device__ __forceinline__ bool mbar_wait_ns(uint32_t bar, uint32_t parity, unsigned* status, uint64_t limit_ns) {
