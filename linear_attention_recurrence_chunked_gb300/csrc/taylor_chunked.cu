@@ -97,26 +97,59 @@ __device__ __forceinline__ float feature(const float* x) {
   else if constexpr (kind == 3) return x[feat_a(J)] * x[feat_b(J)];
   else return 0.f;
 }
-// Features [BEGIN, BEGIN + 8) of x as one 16-byte bf16 vector.
+// Elements I and K of a bf16 row held as 8 words (two bf16 each, element 2i
+// in the low half of word i), as one bf16 pair: I low, K high.
+template <int I, int K>
+__device__ __forceinline__ uint32_t bf16_pair(const uint32_t* w) {
+  if constexpr (I / 2 == K / 2 && I % 2 == 0 && K % 2 == 1) {
+    return w[I / 2];
+  } else {
+    constexpr uint32_t sel = (uint32_t)(2 * (I % 2)) | ((uint32_t)(2 * (I % 2) + 1) << 4) |
+                             ((uint32_t)(4 + 2 * (K % 2)) << 8) | ((uint32_t)(5 + 2 * (K % 2)) << 12);
+    return __byte_perm(w[I / 2], w[K / 2], sel);
+  }
+}
+// Two bf16 products rounded to nearest even: the product of two bf16 values
+// is exact in fp32, so this equals the fp32 product rounded to bf16.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  const __nv_bfloat162 r =
+      __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&a), *reinterpret_cast<const __nv_bfloat162*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+// Features J, J + 1 of a row as one bf16 pair.  w: the row as bf16 words; x:
+// the same values as floats.  Cross terms are paired bf16 products, linear
+// terms are the input values themselves; the rest go through fp32.
+template <int J>
+__device__ __forceinline__ uint32_t feature_pair(const uint32_t* w, const float* x) {
+  constexpr int k0 = feat_kind(J), k1 = feat_kind(J + 1);
+  if constexpr (k0 == 3 && k1 == 3) {
+    return bf16x2_mul(bf16_pair<feat_a(J), feat_a(J + 1)>(w), bf16_pair<feat_b(J), feat_b(J + 1)>(w));
+  } else if constexpr (k0 == 1 && k1 == 1) {
+    return bf16_pair<feat_a(J), feat_a(J + 1)>(w);
+  } else {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(feature<J>(x), feature<J + 1>(x));
+    return *reinterpret_cast<const uint32_t*>(&p);
+  }
+}
+// Features [BEGIN, BEGIN + 8) of a row as one 16-byte bf16 vector.
 template <int BEGIN>
-__device__ __forceinline__ uint4 feature8(const float* x) {
-  const float f[8] = {feature<BEGIN>(x), feature<BEGIN + 1>(x), feature<BEGIN + 2>(x), feature<BEGIN + 3>(x),
-                      feature<BEGIN + 4>(x), feature<BEGIN + 5>(x), feature<BEGIN + 6>(x), feature<BEGIN + 7>(x)};
-  return pack8_bf16(f);
+__device__ __forceinline__ uint4 feature8(const uint32_t* w, const float* x) {
+  return make_uint4(feature_pair<BEGIN>(w, x), feature_pair<BEGIN + 2>(w, x), feature_pair<BEGIN + 4>(w, x),
+                    feature_pair<BEGIN + 6>(w, x));
 }
 // Row `row` of a [128][192] feature tile, features [BEGIN, BEGIN + 80).
 template <int BEGIN>
-__device__ __forceinline__ void store_features80(uint8_t* tile, int row, const float* x) {
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 0, kC)) = feature8<BEGIN + 0>(x);
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 8, kC)) = feature8<BEGIN + 8>(x);
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 16, kC)) = feature8<BEGIN + 16>(x);
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 24, kC)) = feature8<BEGIN + 24>(x);
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 32, kC)) = feature8<BEGIN + 32>(x);
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 40, kC)) = feature8<BEGIN + 40>(x);
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 48, kC)) = feature8<BEGIN + 48>(x);
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 56, kC)) = feature8<BEGIN + 56>(x);
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 64, kC)) = feature8<BEGIN + 64>(x);
-  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 72, kC)) = feature8<BEGIN + 72>(x);
+__device__ __forceinline__ void store_features80(uint8_t* tile, int row, const uint32_t* w, const float* x) {
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 0, kC)) = feature8<BEGIN + 0>(w, x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 8, kC)) = feature8<BEGIN + 8>(w, x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 16, kC)) = feature8<BEGIN + 16>(w, x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 24, kC)) = feature8<BEGIN + 24>(w, x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 32, kC)) = feature8<BEGIN + 32>(w, x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 40, kC)) = feature8<BEGIN + 40>(w, x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 48, kC)) = feature8<BEGIN + 48>(w, x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 56, kC)) = feature8<BEGIN + 56>(w, x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 64, kC)) = feature8<BEGIN + 64>(w, x);
+  *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 72, kC)) = feature8<BEGIN + 72>(w, x);
 }
 
 // Full-basis state rows of compact feature j; returns how many (1 or 2).
@@ -386,26 +419,30 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
 
     // ---- per-chunk worker passes
     // q, k rows of chunk cc (half cc & 1 of the QK tile) into this thread's 16 floats each
-    auto read_qk = [&](int cc, float* xq, float* xk) {
+    auto read_qk = [&](int cc, uint32_t* wq, uint32_t* wk, float* xq, float* xk) {
       const int c0 = 32 * (cc & 1);
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-        unpack8_bf16(*reinterpret_cast<const uint4*>(sm + kOffQK + sw128_off(row, c0 + 8 * i, kC)),
-                     i < 2 ? xq + 8 * i : xk + 8 * (i - 2));
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = *reinterpret_cast<const uint4*>(sm + kOffQK + sw128_off(row, c0 + 8 * i, kC));
+        uint32_t* wd = i < 2 ? wq + 4 * i : wk + 4 * (i - 2);
+        wd[0] = u.x; wd[1] = u.y; wd[2] = u.z; wd[3] = u.w;
+        unpack8_bf16(u, i < 2 ? xq + 8 * i : xk + 8 * (i - 2));
+      }
     };
     // compact features of chunk cc's q and k rows; this thread writes features [80 half, 80 half + 80)
     auto features = [&](int cc) {
+      uint32_t wq[kF / 2], wk[kF / 2];
       float xq[kF], xk[kF];
-      read_qk(cc, xq, xk);
+      read_qk(cc, wq, wk, xq, xk);
       const bool valid = (int64_t)cc * kC + row < N;
       if (half == 0) {
-        store_features80<0>(sm + kOffPhiQ, row, xq);
-        store_features80<0>(sm + kOffPhiK, row, xk);
+        store_features80<0>(sm + kOffPhiQ, row, wq, xq);
+        store_features80<0>(sm + kOffPhiK, row, wk, xk);
         // a padded token must not add its constant feature to the state
         if (!valid) *reinterpret_cast<__nv_bfloat16*>(sm + kOffPhiK + sw128_off(row, 0, kC)) = __float2bfloat16_rn(0.f);
       } else {
-        store_features80<80>(sm + kOffPhiQ, row, xq);
-        store_features80<80>(sm + kOffPhiK, row, xk);
+        store_features80<80>(sm + kOffPhiQ, row, wq, xq);
+        store_features80<80>(sm + kOffPhiK, row, wk, xk);
       }
     };
     // chunk cc's rows are in (this thread's cp.async groups up to cc have landed): the issuer may start Q K^T
