@@ -66,7 +66,7 @@ def _declare(lib) -> None:
     lib.oracle_taylor_feature.argtypes = [vp, i64, vp]
     lib.oracle_taylor.restype = ctypes.c_int
     lib.oracle_taylor.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int, vp, vp, vp,
-                                  vp, vp, dp, vp, i64, vp, vp, vp, vp, ctypes.c_int]
+                                  vp, vp, dp, vp, vp, i64, vp, vp, vp, vp, ctypes.c_int]
     lib.oracle_gdn.restype = ctypes.c_int
     lib.oracle_gdn.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int, vp, vp, vp,
                                vp, vp, dp, vp, vp, i64, vp, vp, ctypes.c_int]
@@ -134,10 +134,13 @@ def taylor_feature(x) -> np.ndarray:
 
 
 def taylor(q, k, v, s_in=None, z_in=None, eps: float = 0.0, t_samples=None,
-           want_den: bool = False, nthreads: int | None = None):
+           want_den: bool = False, nthreads: int | None = None, decay=None):
     """Token-by-token Taylor linear attention with the s/z normaliser.
 
     q, k: [B,H,N,d'], v: [B,H,N,d_v] (float32 or bf16 bits as uint16).
+    decay: None, or the per-head retention lambda ([H] or a scalar): the state
+    is scaled by lambda before each write (BASED notes, the decay paragraph
+    after Table 7; reading in oracle.c).
     Returns dict(y=[B,H,rows,d_v], s=[B,H,D,d_v], z=[B,H,D], den=[B,H,rows]?).
     """
     q, kind = _as_input(q)
@@ -155,12 +158,14 @@ def taylor(q, k, v, s_in=None, z_in=None, eps: float = 0.0, t_samples=None,
         assert s_in.shape == (B, H, D, dv)
     if z_in is not None:
         assert z_in.shape == (B, H, D)
+    if decay is not None:
+        decay = np.ascontiguousarray(np.broadcast_to(np.asarray(decay, dtype=np.float64), (H,)))
     y = np.zeros((B, H, rows, dv), dtype=np.float64)
     den = np.zeros((B, H, rows), dtype=np.float64) if want_den else None
     s = np.zeros((B, H, D, dv), dtype=np.float64)
     z = np.zeros((B, H, D), dtype=np.float64)
     rc = _load().oracle_taylor(B, H, N, df, dv, kind, _ptr(q), _ptr(k), _ptr(v),
-                               _ptr(s_in), _ptr(z_in), float(eps), _ptr(t), rows if t is not None else 0,
+                               _ptr(s_in), _ptr(z_in), float(eps), _ptr(decay), _ptr(t), rows if t is not None else 0,
                                _ptr(y), _ptr(den), _ptr(s), _ptr(z),
                                nthreads or default_threads())
     if rc != 0:

@@ -28,6 +28,8 @@
  *             s_0 = 0, z_0 = 0;
  *         Sec. 2.3 (the paper's Eq. (4)): the 2nd-order Taylor map
  *             phi(x) = [1, x, vec(x x^T)/sqrt(2)],  D = 1 + d' + d'^2.
+ *   [BN-D] same page, the paragraph on decay after Table 7: the 10B-token
+ *         runs use a fixed decay rate per head (the 30B/50B runs none).
  *
  * Readings taken where the pages leave a step open:
  *   - o_t / y_i are read AFTER token t's write (inclusive prefix, Eq. (1)
@@ -39,6 +41,12 @@
  *   - The Taylor denominator gets + eps (0 by default); the pages state it
  *     is positive for a non-empty prefix and that implementations add eps.
  *   - The initial state is zero unless one is passed in.
+ *   - [BN-D] gives no formula for the per-head decay; the plain reading is
+ *     a constant scalar retention of the whole state before each write,
+ *         s_i = lambda_h s_{i-1} + phi(k_i) v_i^T,
+ *         z_i = lambda_h z_{i-1} + phi(k_i),
+ *     the A_t = lambda I member of the [NB-G] family; lambda = 1 (the
+ *     default) is the undecayed recurrence above.
  *
  * Everything is computed token by token in double precision, exactly as
  * the definitions above read; the only parallelism is over independent
@@ -85,6 +93,7 @@ typedef struct {
   const float *alpha, *beta;
   double q_scale, eps;
   const double *s_in, *z_in;
+  const double* decay; /* Taylor: per-head lambda [H], or NULL (no decay) */
   const int64_t* t_samples;
   int64_t n_samples;
   double *out, *den, *s_out, *z_out;
@@ -111,7 +120,8 @@ static void* taylor_worker(void* arg) {
   double* vt = (double*)malloc(sizeof(double) * dv);
   const int64_t rows = n_out_rows(j);
   for (int64_t bh = j->worker; bh < j->B * j->H; bh += j->nthreads) {
-    /* s_0, z_0: given state or zero. */
+    /* s_0, z_0: given state or zero; lambda: this head's decay ([BN-D]). */
+    const double lam = j->decay ? j->decay[bh % j->H] : 1.0;
     for (int64_t i = 0; i < D * dv; ++i) s[i] = j->s_in ? j->s_in[bh * D * dv + i] : 0.0;
     for (int64_t i = 0; i < D; ++i) z[i] = j->z_in ? j->z_in[bh * D + i] : 0.0;
     int64_t next = 0; /* next sample slot */
@@ -122,11 +132,11 @@ static void* taylor_worker(void* arg) {
         xq[a] = in_at(j->in_kind, j->q, qk_off + a);
       }
       for (int64_t c = 0; c < dv; ++c) vt[c] = in_at(j->in_kind, j->v, v_off + c);
-      /* s_t = s_{t-1} + phi(k_t) v_t^T ;  z_t = z_{t-1} + phi(k_t) */
+      /* s_t = lambda s_{t-1} + phi(k_t) v_t^T ;  z_t = lambda z_{t-1} + phi(k_t) */
       oracle_taylor_feature(xk, df, phk);
       for (int64_t r = 0; r < D; ++r) {
-        for (int64_t c = 0; c < dv; ++c) s[r * dv + c] += phk[r] * vt[c];
-        z[r] += phk[r];
+        for (int64_t c = 0; c < dv; ++c) s[r * dv + c] = lam * s[r * dv + c] + phk[r] * vt[c];
+        z[r] = lam * z[r] + phk[r];
       }
       int record = j->t_samples ? (next < j->n_samples && j->t_samples[next] == t) : 1;
       if (!record) continue;
@@ -281,12 +291,13 @@ static int check_samples(const int64_t* t, int64_t n, int64_t N) {
 /* Taylor linear attention, token by token.
  * q, k: [B,H,N,dfeat]; v: [B,H,N,dv]; contiguous; float32 or bf16 bits.
  * s_in/z_in: [B,H,D,dv] / [B,H,D] or NULL (zero state).
+ * decay: per-head lambda [H] or NULL (no decay).
  * t_samples: NULL (every token) or n_samples strictly increasing indices.
  * y: [B,H,rows,dv]; den (nullable): [B,H,rows] = z_t^T phi(q_t) (no eps);
  * s_out/z_out: final state (nullable).  Returns 0, or -1 on bad arguments. */
 int oracle_taylor(int64_t B, int64_t H, int64_t N, int64_t dfeat, int64_t dv,
                   int in_kind, const void* q, const void* k, const void* v,
-                  const double* s_in, const double* z_in, double eps,
+                  const double* s_in, const double* z_in, double eps, const double* decay,
                   const int64_t* t_samples, int64_t n_samples,
                   double* y, double* den, double* s_out, double* z_out,
                   int nthreads) {
@@ -296,7 +307,7 @@ int oracle_taylor(int64_t B, int64_t H, int64_t N, int64_t dfeat, int64_t dv,
   job_t j;
   memset(&j, 0, sizeof j);
   j.B = B; j.H = H; j.N = N; j.dk = dfeat; j.dv = dv; j.in_kind = in_kind;
-  j.q = q; j.k = k; j.v = v; j.eps = eps; j.s_in = s_in; j.z_in = z_in;
+  j.q = q; j.k = k; j.v = v; j.eps = eps; j.s_in = s_in; j.z_in = z_in; j.decay = decay;
   j.t_samples = t_samples; j.n_samples = n_samples;
   j.out = y; j.den = den; j.s_out = s_out; j.z_out = z_out;
   if (B * H == 0) return 0;

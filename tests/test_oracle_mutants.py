@@ -20,7 +20,10 @@ MUTANTS = [
     ("dropped 1/sqrt2 in phi", "x[a] * x[b] * inv_sqrt2", "x[a] * x[b]"),
     ("column-major quadratic block", "phi[1 + dfeat + a * dfeat + b] = x[a] * x[b] * inv_sqrt2",
      "phi[1 + dfeat + a * dfeat + b] = x[a] * x[(b + 1) % dfeat] * inv_sqrt2"),
-    ("normaliser not accumulated", "z[r] += phk[r];", "z[r] = phk[r];"),
+    ("normaliser not accumulated", "z[r] = lam * z[r] + phk[r];", "z[r] = phk[r];"),
+    ("decay applied after the write", "s[r * dv + c] = lam * s[r * dv + c] + phk[r] * vt[c];",
+     "s[r * dv + c] = lam * (s[r * dv + c] + phk[r] * vt[c]);"),
+    ("decay skipped on the normaliser", "z[r] = lam * z[r] + phk[r];", "z[r] = z[r] + phk[r];"),
     ("eps forced to one", "y[c] = nm / (dn + j->eps);", "y[c] = nm / (dn + 1.0);"),
     ("delta-rule sign flipped", "al * (S[i * dk + a] - be * Sk[i] * kt[a])", "al * (S[i * dk + a] + be * Sk[i] * kt[a])"),
     ("write decayed by alpha", "+ be * vt[i] * kt[a];", "+ al * be * vt[i] * kt[a];"),
@@ -41,6 +44,8 @@ PIN_FUNCS = [
     lambda: pins.test_taylor_equals_quadratic_form(4, 5, 37),
     pins.test_taylor_state_invariants,
     pins.test_taylor_zero_query_is_running_mean,
+    lambda: pins.test_taylor_decay_equals_weighted_quadratic_form(4, 5, 33),
+    pins.test_taylor_decay_split_resume_with_state,
     lambda: pins.test_gdn_equals_dense_matrix_form(6, 5, 23),
     pins.test_gdn_reduces_to_additive_for_orthogonal_keys,
     pins.test_gdn_beta_zero_pure_decay,

@@ -179,6 +179,75 @@ def test_taylor_split_resume_and_samples():
     assert np.array_equal(smp["y"], full["y"][:, :, t])
 
 
+# --------------------------------------------------------------------------
+# Taylor with a fixed per-head decay (BASED notes, the decay paragraph after
+# Table 7; reading: s_i = lambda s_{i-1} + phi(k_i) v_i^T, z likewise)
+
+
+def decayed_quadratic_form(q, k, v, lam, s0_probe=None):
+    """y_i = sum_{j<=i} lam^(i-j) K(q_i,k_j) v_j / sum_{j<=i} lam^(i-j) K(q_i,k_j), by brute force."""
+    B, H, N, _ = q.shape
+    y = np.zeros(v.shape, dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            for i in range(N):
+                w = np.array([lam[h] ** (i - j) * taylor_kernel(q[b, h, i].astype(np.float64),
+                                                               k[b, h, j].astype(np.float64))
+                              for j in range(i + 1)])
+                y[b, h, i] = w @ v[b, h, : i + 1].astype(np.float64) / w.sum()
+    return y
+
+
+def test_taylor_decay_one_is_undecayed():
+    q, k, v = f32((1, 2, 30, 16), 0.25), f32((1, 2, 30, 16), 0.25), f32((1, 2, 30, 8))
+    a = oracle.taylor(q, k, v)
+    b = oracle.taylor(q, k, v, decay=np.ones(2))
+    assert np.array_equal(a["y"], b["y"]) and np.array_equal(a["s"], b["s"]) and np.array_equal(a["z"], b["z"])
+
+
+@pytest.mark.parametrize("df,dv,N", [(4, 5, 33), (16, 8, 40)])
+def test_taylor_decay_equals_weighted_quadratic_form(df, dv, N):
+    q = f32((1, 3, N, df), 1 / math.sqrt(df))
+    k = f32((1, 3, N, df), 1 / math.sqrt(df))
+    v = f32((1, 3, N, dv))
+    lam = np.array([0.9, 0.5, 0.99])
+    out = oracle.taylor(q, k, v, decay=lam, nthreads=2)
+    assert rel_err(out["y"], decayed_quadratic_form(q, k, v, lam)) < 1e-12
+    # the final state read by a probe x: phi(x)^T s_N = sum_j lam^(N-1-j) K(x, k_j) v_j
+    x = rng.standard_normal(df) / math.sqrt(df)
+    phx = oracle.taylor_feature(x)
+    for h in range(3):
+        w = np.array([lam[h] ** (N - 1 - j) * taylor_kernel(x, k[0, h, j].astype(np.float64)) for j in range(N)])
+        assert rel_err(phx @ out["s"][0, h], w @ v[0, h].astype(np.float64)) < 1e-12
+        assert phx @ out["z"][0, h] == pytest.approx(w.sum(), rel=1e-12)
+
+
+def test_taylor_decay_zero_keeps_only_the_current_token():
+    q, k, v = f32((1, 1, 12, 16), 0.25), f32((1, 1, 12, 16), 0.25), f32((1, 1, 12, 6))
+    s0 = rng.standard_normal((1, 1, 273, 6))
+    z0 = np.abs(rng.standard_normal((1, 1, 273)))
+    y = oracle.taylor(q, k, v, s_in=s0, z_in=z0, decay=0.0)["y"][0, 0]
+    assert rel_err(y, v[0, 0].astype(np.float64)) < 1e-13
+
+
+def test_taylor_decay_split_resume_with_state():
+    df, dv, N = 16, 8, 41
+    q, k, v = f32((1, 2, N, df), 0.25), f32((1, 2, N, df), 0.25), f32((1, 2, N, dv))
+    lam = np.array([0.95, 0.7])
+    s0 = rng.standard_normal((1, 2, 273, dv)) * 0.1
+    z0 = np.abs(rng.standard_normal((1, 2, 273))) * 0.1
+    full = oracle.taylor(q, k, v, s_in=s0, z_in=z0, decay=lam)
+    a = oracle.taylor(q[:, :, :19], k[:, :, :19], v[:, :, :19], s_in=s0, z_in=z0, decay=lam)
+    b = oracle.taylor(q[:, :, 19:], k[:, :, 19:], v[:, :, 19:], s_in=a["s"], z_in=a["z"], decay=lam)
+    assert rel_err(np.concatenate([a["y"], b["y"]], axis=2), full["y"]) < 1e-13
+    assert rel_err(b["s"], full["s"]) < 1e-13 and rel_err(b["z"], full["z"]) < 1e-13
+    # the recurrence is linear in (s0, v): with v = 0 the incoming state's share of s_N is lam^N s0
+    zero_v = oracle.taylor(q, k, np.zeros_like(v), s_in=s0, z_in=z0, decay=lam)
+    no_s0 = oracle.taylor(q, k, np.zeros_like(v), decay=lam)
+    for h in range(2):
+        assert rel_err(zero_v["s"][0, h] - no_s0["s"][0, h], lam[h] ** N * s0[0, h]) < 1e-12
+
+
 def test_bf16_bits_decode_like_float32():
     x = f32((1, 1, 20, 16), 0.25)
     bits = (x.view(np.uint32) >> 16).astype(np.uint16)           # truncate to bf16
