@@ -4,6 +4,7 @@ One step = one pass of every hot-path row on synthetic inputs resident in
 HBM.  The headline line (``value``) is the BASED Taylor prefill,
 B=8, H=16, N=4096, d'=16, d_v=64, bf16 in / fp32 state, in tokens/s (B*N per
 step).  The same run also times, under ``paths``:
+  based_prefill_decay  the headline workload with a fixed per-head decay
   gdn_prefill       Gated DeltaNet prefill B=4, H=16, N=16384, d=128
   gdn_prefill_long  Gated DeltaNet prefill B=1, H=16, N=1,048,576, d=128
   gated_prefill     scalar-gate (A_t = alpha_t I) prefill on the gdn_prefill inputs
@@ -316,13 +317,47 @@ def gpu_arm(args, ws, rank, local):
 KERNELS_PER_CALL = {"based_prefill": 1, "gdn_prefill": 2, "decode": 1}
 
 
-PATH_NAMES = ("gdn_prefill", "gdn_prefill_long", "gated_prefill", "decode_gdn", "decode_taylor", "decode_swa")
+PATH_NAMES = ("based_prefill_decay", "gdn_prefill", "gdn_prefill_long", "gated_prefill", "decode_gdn", "decode_taylor",
+              "decode_swa")
+
+
+def decay_rates(H):
+    """Fixed per-head retention for the decayed BASED path: lambda_h = 1 - 2^-(5 + h mod 8), a spread from a
+    32-token to a 4096-token memory (the pages give no values)."""
+    return torch.tensor([1.0 - 2.0 ** -(5 + h % 8) for h in range(H)], dtype=torch.float32)
 
 
 def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
     out = {}
     launches = 0
     steps = max(1, args.steps)
+    if only is None or only == "based_prefill_decay":
+        # the headline workload with a fixed per-head decay (a separate instantiation of the kernel)
+        w = synthetic.WORKLOADS[HEADLINE]
+        x = synthetic.workload_inputs(HEADLINE, device=dev, seed=w.seed + seed_off)
+        lam = decay_rates(w.H).to(dev)
+        y = torch.empty((w.B, w.H, w.N, 64), dtype=torch.bfloat16, device=dev)
+        s = torch.empty((w.B, w.H, la.TAYLOR_D, 64), dtype=torch.float32, device=dev)
+        z = torch.empty((w.B, w.H, la.TAYLOR_D), dtype=torch.float32, device=dev)
+
+        def dstep():
+            la.la_based_prefill(x["q"], x["k"], x["v"], y=y, s_out=s, z_out=z, stream=stream, decay=lam)
+
+        t = Timer(stream, flush)
+        for _ in range(args.warmup):
+            t.run(dstep)
+        t.reset()
+        barrier(ws)
+        for _ in range(steps):
+            t.run(dstep)
+        ms = max_over_ranks(t.total_ms(), ws) / steps
+        launches += steps * KERNELS_PER_CALL["based_prefill"]
+        byts = BYTES_PER_TOKEN_HEAD["taylor_prefill"] * w.B * w.H * w.N + STATE_BYTES["taylor"] * w.B * w.H
+        out["based_prefill_decay"] = {"workload": w.description + ", per-head decay 1 - 2^-(5 + h mod 8)",
+                                      "tokens_per_s": round(whole_job_rate(w.B * w.N, ws, ms * 1e-3), 1),
+                                      "ms": round(ms, 4), "roofline": roofline(byts, ms, pk["hbm_gbs"], None)}
+        del x, y, s, z
+        torch.cuda.empty_cache()
     for name in ("gdn_prefill", "gdn_prefill_long", "gated_prefill"):
         if only is not None and name != only:
             continue

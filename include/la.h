@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define LA_ABI_VERSION 1
+#define LA_ABI_VERSION 2
 
 typedef enum la_status {
   LA_OK = 0,
@@ -86,7 +86,12 @@ typedef struct la_tensor {
  *          the order [1, x_0..x_{d'-1}, x_a x_b/sqrt2 for a, then b]; NULL = zero.
  *   z_in : [B, H, D] fp32 contiguous; NULL = zero.
  *   s_out, z_out : final state after token N-1 (required; may alias s_in/z_in).
- *   eps  : added to the denominator (0 reproduces the pages' definition). */
+ *   eps  : added to the denominator (0 reproduces the pages' definition).
+ *   decay: NULL, or [H] fp32 on the device: a fixed retention lambda_h per
+ *          head, s_i = lambda_h s_{i-1} + phi(k_i) v_i^T and z_i likewise
+ *          (BASED notes, the paragraph on decay after Table 7: the 10B-token
+ *          runs use a fixed per-head decay rate).  For lambda_h in [0, 1]
+ *          every intermediate stays in range; values are not checked. */
 typedef struct la_based_prefill_args {
   int64_t B, H, N, d_feat, d_v;
   la_dtype in_dtype, out_dtype;
@@ -96,6 +101,7 @@ typedef struct la_based_prefill_args {
   float* s_out;
   float* z_out;
   float eps;
+  const float* decay;
 } la_based_prefill_args;
 
 /* Gated DeltaNet prefill.
@@ -126,7 +132,9 @@ typedef struct la_gdn_prefill_args {
  *   out  : [S, H, d_v] contiguous out_dtype
  *   state: GDN / scalar gate [S, H, d_v, d_k] fp32; Taylor [S, H, D, d_v] fp32 (s)
  *   z    : Taylor [S, H, D] fp32 (ignored otherwise)
- *   eps  : Taylor denominator term; q_scale: GDN / scalar-gate query scale. */
+ *   eps  : Taylor denominator term; q_scale: GDN / scalar-gate query scale.
+ *   decay: Taylor only: NULL or [H] fp32 per-head retention lambda_h, as in
+ *          la_based_prefill_args (ignored otherwise). */
 typedef struct la_decode_args {
   la_variant variant;
   int64_t S, H, d_k, d_v;
@@ -141,6 +149,7 @@ typedef struct la_decode_args {
   float* z;
   float eps;
   float q_scale;
+  const float* decay;
 } la_decode_args;
 
 /* Bytes of device workspace the matching prefill call needs for `args`

@@ -48,7 +48,7 @@ class BasedPrefillArgs(ctypes.Structure):
                 ("q", LATensor), ("k", LATensor), ("v", LATensor), ("y", LATensor),
                 ("s_in", ctypes.c_void_p), ("z_in", ctypes.c_void_p),
                 ("s_out", ctypes.c_void_p), ("z_out", ctypes.c_void_p),
-                ("eps", ctypes.c_float)]
+                ("eps", ctypes.c_float), ("decay", ctypes.c_void_p)]
 
 
 class GdnPrefillArgs(ctypes.Structure):
@@ -66,7 +66,7 @@ class DecodeArgs(ctypes.Structure):
                 ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("alpha", ctypes.c_void_p), ("beta", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("state", ctypes.c_void_p), ("z", ctypes.c_void_p),
-                ("eps", ctypes.c_float), ("q_scale", ctypes.c_float)]
+                ("eps", ctypes.c_float), ("q_scale", ctypes.c_float), ("decay", ctypes.c_void_p)]
 
 
 EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_gated_prefill", "la_decode_step", "la_based_prefill_workspace_size",
@@ -207,11 +207,16 @@ def _workspace(nbytes: int, workspace, device):
 # entry points
 
 
-def _based_args(q, k, v, y, s_in, z_in, s_out, z_out, eps):
+def _based_args(q, k, v, y, s_in, z_in, s_out, z_out, eps, decay=None):
     B, H, N, F = q.shape
     return BasedPrefillArgs(B, H, N, F, v.shape[-1], _dtype_code(q.dtype), _dtype_code(y.dtype),
                             _view4(q), _view4(k), _view4(v), _view4(y),
-                            _ptr(s_in), _ptr(z_in), _ptr(s_out), _ptr(z_out), float(eps))
+                            _ptr(s_in), _ptr(z_in), _ptr(s_out), _ptr(z_out), float(eps), _ptr(decay))
+
+
+def _check_decay(decay, H):
+    if decay is not None and (decay.dtype != torch.float32 or decay.shape != (H,) or not decay.is_contiguous()):
+        raise ValueError("decay must be a contiguous float32 tensor of shape [H]")
 
 
 def la_based_prefill_workspace_size(q, k, v, y=None) -> int:
@@ -221,14 +226,16 @@ def la_based_prefill_workspace_size(q, k, v, y=None) -> int:
 
 
 def la_based_prefill(q, k, v, y=None, s_in=None, z_in=None, s_out=None, z_out=None, eps: float = 0.0,
-                     out_dtype=None, workspace=None, stream=None):
+                     out_dtype=None, workspace=None, stream=None, decay=None):
     """Chunked Taylor (BASED) prefill.  Returns (y, s_out, z_out).
 
     q, k: [B,H,N,16], v: [B,H,N,64] (fp32 or bf16); states fp32
-    s: [B,H,273,64], z: [B,H,273]."""
+    s: [B,H,273,64], z: [B,H,273]; decay: None or fp32 [H], the per-head
+    retention lambda (s_i = lambda s_{i-1} + phi(k_i) v_i^T, z likewise)."""
     lib = load_library()
-    _check_cuda(q, k, v, y, s_in, z_in, s_out, z_out)
+    _check_cuda(q, k, v, y, s_in, z_in, s_out, z_out, decay)
     B, H, N, _ = q.shape
+    _check_decay(decay, H)
     dv = v.shape[-1]
     if y is None:
         y = torch.empty((B, H, N, dv), dtype=out_dtype or q.dtype, device=q.device)
@@ -239,7 +246,7 @@ def la_based_prefill(q, k, v, y=None, s_in=None, z_in=None, s_out=None, z_out=No
     for name, t in (("s_in", s_in), ("z_in", z_in), ("s_out", s_out), ("z_out", z_out)):
         if t is not None and (t.dtype != torch.float32 or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous float32 tensor")
-    a = _based_args(q, k, v, y, s_in, z_in, s_out, z_out, eps)
+    a = _based_args(q, k, v, y, s_in, z_in, s_out, z_out, eps, decay)
     need = int(lib.la_based_prefill_workspace_size(ctypes.byref(a)))
     ws, ws_bytes = _workspace(need, workspace, q.device)
     st = lib.la_based_prefill(ctypes.byref(a), _ptr(ws) if isinstance(ws, torch.Tensor) else ws, ws_bytes,
@@ -327,25 +334,27 @@ def la_gdn_prefill_noalloc(q, k, v, alpha, beta, o, S_out, S_in=None, q_scale: f
 
 
 def la_decode_step(variant: int, q, k, v, state, z=None, alpha=None, beta=None, out=None,
-                   eps: float = 0.0, q_scale: float = 1.0, out_dtype=None, stream=None):
+                   eps: float = 0.0, q_scale: float = 1.0, out_dtype=None, stream=None, decay=None):
     """One decode step, state (and z) updated in place.  Returns out [S,H,d_v].
 
     GDN and the scalar gate (LA_VARIANT_GATED): q, k, v [S,H,128], alpha, beta
     fp32 [S,H], state fp32 [S,H,128,128].
-    Taylor: q, k [S,H,16], v [S,H,64], state fp32 [S,H,273,64], z fp32 [S,H,273]."""
+    Taylor: q, k [S,H,16], v [S,H,64], state fp32 [S,H,273,64], z fp32 [S,H,273];
+    decay: None or fp32 [H] per-head retention, as in la_based_prefill."""
     lib = load_library()
-    _check_cuda(q, k, v, state, z, alpha, beta, out)
+    _check_cuda(q, k, v, state, z, alpha, beta, out, decay)
     for name, t in (("q", q), ("k", k), ("v", v), ("state", state), ("z", z), ("alpha", alpha),
                     ("beta", beta), ("out", out)):
         if t is not None and not t.is_contiguous():
             raise ValueError(f"{name} must be contiguous")
     S, H, dk = q.shape
     dv = v.shape[-1]
+    _check_decay(decay, H)
     if out is None:
         out = torch.empty((S, H, dv), dtype=out_dtype or q.dtype, device=q.device)
     a = DecodeArgs(int(variant), S, H, dk, dv, _dtype_code(q.dtype), _dtype_code(out.dtype),
                    _ptr(q), _ptr(k), _ptr(v), _ptr(alpha), _ptr(beta), _ptr(out), _ptr(state), _ptr(z),
-                   float(eps), float(q_scale))
+                   float(eps), float(q_scale), _ptr(decay))
     st = lib.la_decode_step(ctypes.byref(a), _stream_handle(stream))
     if st != LA_OK:
         raise LAError(st, "la_decode_step")

@@ -77,7 +77,7 @@ la_status check_based(const la_based_prefill_args* a) {
   if (B * H > 0) {
     if (!a->s_out || !a->z_out) return LA_ERR_INVALID_ARGUMENT;
     if (!aligned16(a->s_out) || !aligned16(a->s_in) || (reinterpret_cast<uintptr_t>(a->z_out) & 3u) ||
-        (reinterpret_cast<uintptr_t>(a->z_in) & 3u))
+        (reinterpret_cast<uintptr_t>(a->z_in) & 3u) || (reinterpret_cast<uintptr_t>(a->decay) & 3u))
       return LA_ERR_INVALID_ARGUMENT;
   }
   return LA_OK;
@@ -205,6 +205,7 @@ la_status la_based_prefill(const la_based_prefill_args* a, void* ws, size_t ws_b
   L.y = a->y.ptr; L.y_sb = a->y.stride_b; L.y_sh = a->y.stride_h; L.y_st = a->y.stride_t;
   L.s_in = a->s_in; L.z_in = a->z_in; L.s_out = a->s_out; L.z_out = a->z_out;
   L.eps = a->eps;
+  L.decay = a->decay;
   if (!L.in_bf16) return from_cuda(la::launch_taylor_prefill_recurrent(L, s));
   unsigned* status = device_status_ptr();
   if (!status) return LA_ERR_CUDA;
@@ -240,7 +241,8 @@ la_status la_decode_step(const la_decode_args* a, void* stream) {
       (reinterpret_cast<uintptr_t>(a->v) % in_align) || !aligned16(a->state))
     return LA_ERR_INVALID_ARGUMENT;
   if (gdn_family && (!a->alpha || !a->beta)) return LA_ERR_INVALID_ARGUMENT;
-  if (a->variant == LA_VARIANT_TAYLOR && (!a->z || (reinterpret_cast<uintptr_t>(a->z) & 3u)))
+  if (a->variant == LA_VARIANT_TAYLOR &&
+      (!a->z || (reinterpret_cast<uintptr_t>(a->z) & 3u) || (reinterpret_cast<uintptr_t>(a->decay) & 3u)))
     return LA_ERR_INVALID_ARGUMENT;
   la::DecodeLaunch L{};
   L.S = a->S; L.H = a->H;
@@ -249,6 +251,7 @@ la_status la_decode_step(const la_decode_args* a, void* stream) {
   L.q = a->q; L.k = a->k; L.v = a->v; L.alpha = a->alpha; L.beta = a->beta;
   L.out = a->out; L.state = a->state; L.z = a->z; L.eps = a->eps; L.q_scale = a->q_scale;
   L.delta = a->variant == LA_VARIANT_GDN ? 1.f : 0.f;
+  L.decay = a->variant == LA_VARIANT_TAYLOR ? a->decay : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return from_cuda(gdn_family ? la::launch_gdn_decode(L, s) : la::launch_taylor_decode(L, s));
 }

@@ -95,7 +95,7 @@ template <typename TIn, typename TOut>
 __global__ void __launch_bounds__(kTayThreads)
 taylor_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TIn* __restrict__ v,
                      TOut* __restrict__ out, float* __restrict__ s_state, float* __restrict__ z_state,
-                     float eps) {
+                     float eps, const float* __restrict__ decay, int64_t H) {
   __shared__ float xk[kTayF], xq[kTayF];
   __shared__ float4 red[kTayRowGroups][kTayDv / 4];
   __shared__ float dred[kTayThreads / 32];
@@ -103,6 +103,7 @@ taylor_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const
   const int tid = threadIdx.x, cg = tid & 15, rg = tid >> 4;
   float* s = s_state + sh * (kTayD * kTayDv);
   float* z = z_state + sh * kTayD;
+  const float lam = decay ? decay[sh % H] : 1.f;  // s <- lam s + phi(k) v^T, z <- lam z + phi(k)
 
   float4 sv[kTayRowsPerThread];
 #pragma unroll
@@ -124,10 +125,10 @@ taylor_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const
     if (j < kTayD) {
       const float fk = taylor_phi(xk, j), fq = taylor_phi(xq, j);
       float4 x = sv[i];
-      x.x = fmaf(fk, vv.x, x.x);
-      x.y = fmaf(fk, vv.y, x.y);
-      x.z = fmaf(fk, vv.z, x.z);
-      x.w = fmaf(fk, vv.w, x.w);
+      x.x = fmaf(fk, vv.x, lam * x.x);
+      x.y = fmaf(fk, vv.y, lam * x.y);
+      x.z = fmaf(fk, vv.z, lam * x.z);
+      x.w = fmaf(fk, vv.w, lam * x.w);
       __stcs(reinterpret_cast<float4*>(s + j * kTayDv) + cg, x);
       acc.x = fmaf(fq, x.x, acc.x);
       acc.y = fmaf(fq, x.y, acc.y);
@@ -138,11 +139,11 @@ taylor_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const
   // normaliser rows: thread t owns z_t and z_{t+256}
   float dpart;
   {
-    zv0 += taylor_phi(xk, tid);
+    zv0 = fmaf(lam, zv0, taylor_phi(xk, tid));
     __stcs(z + tid, zv0);
     dpart = taylor_phi(xq, tid) * zv0;
     if (tid + kTayThreads < kTayD) {
-      zv1 += taylor_phi(xk, tid + kTayThreads);
+      zv1 = fmaf(lam, zv1, taylor_phi(xk, tid + kTayThreads));
       __stcs(z + tid + kTayThreads, zv1);
       dpart = fmaf(taylor_phi(xq, tid + kTayThreads), zv1, dpart);
     }
@@ -184,7 +185,7 @@ cudaError_t launch_taylor_decode(const DecodeLaunch& a, cudaStream_t stream) {
   if (grid == 0) return cudaSuccess;
 #define LA_TAY_DECODE(TI, TO)                                                                    \
   taylor_decode_kernel<TI, TO><<<grid, kTayThreads, 0, stream>>>(                               \
-      (const TI*)a.q, (const TI*)a.k, (const TI*)a.v, (TO*)a.out, a.state, a.z, a.eps)
+      (const TI*)a.q, (const TI*)a.k, (const TI*)a.v, (TO*)a.out, a.state, a.z, a.eps, a.decay, a.H)
   if (a.in_bf16 && a.out_bf16) LA_TAY_DECODE(__nv_bfloat16, __nv_bfloat16);
   else if (a.in_bf16) LA_TAY_DECODE(__nv_bfloat16, float);
   else if (a.out_bf16) LA_TAY_DECODE(float, __nv_bfloat16);

@@ -26,6 +26,7 @@ struct DecodeLaunch {
   float* z;
   float eps, q_scale;
   float delta;  // GDN-family decode: 1 = gated delta rule, 0 = scalar gate (A_t = alpha_t I)
+  const float* decay;  // Taylor decode: per-head retention [H] or null
 };
 
 struct TaylorPrefillLaunch {
@@ -39,6 +40,7 @@ struct TaylorPrefillLaunch {
   float* s_out;
   float* z_out;
   float eps;
+  const float* decay;  // per-head retention [H] or null (no decay)
 };
 
 struct GdnPrefillLaunch {

@@ -115,6 +115,7 @@ taylor_prefill_recurrent_kernel(TaylorPrefillLaunch a) {
   const int64_t bh = blockIdx.x;
   const int64_t b = bh / a.H, h = bh % a.H;
   const int tid = threadIdx.x, cg = tid & 15, rg = tid >> 4;
+  const float lam = a.decay ? a.decay[h] : 1.f;  // s <- lam s + phi(k) v^T, z <- lam z + phi(k)
 
   float4 sv[kRowsPerThread];
   const float* s_in = a.s_in ? a.s_in + bh * kDt * kDv : nullptr;
@@ -153,20 +154,20 @@ taylor_prefill_recurrent_kernel(TaylorPrefillLaunch a) {
       const int j = rg + kRG * i;
       if (j < kDt) {
         const float fk = phi_at(xkb, j), fq = phi_at(xqb, j);
-        sv[i].x = fmaf(fk, vv.x, sv[i].x);
-        sv[i].y = fmaf(fk, vv.y, sv[i].y);
-        sv[i].z = fmaf(fk, vv.z, sv[i].z);
-        sv[i].w = fmaf(fk, vv.w, sv[i].w);
+        sv[i].x = fmaf(fk, vv.x, lam * sv[i].x);
+        sv[i].y = fmaf(fk, vv.y, lam * sv[i].y);
+        sv[i].z = fmaf(fk, vv.z, lam * sv[i].z);
+        sv[i].w = fmaf(fk, vv.w, lam * sv[i].w);
         acc.x = fmaf(fq, sv[i].x, acc.x);
         acc.y = fmaf(fq, sv[i].y, acc.y);
         acc.z = fmaf(fq, sv[i].z, acc.z);
         acc.w = fmaf(fq, sv[i].w, acc.w);
       }
     }
-    zv0 += phi_at(xkb, tid);
+    zv0 = fmaf(lam, zv0, phi_at(xkb, tid));
     float dpart = phi_at(xqb, tid) * zv0;
     if (tid + kTThreads < kDt) {
-      zv1 += phi_at(xkb, tid + kTThreads);
+      zv1 = fmaf(lam, zv1, phi_at(xkb, tid + kTThreads));
       dpart = fmaf(phi_at(xqb, tid + kTThreads), zv1, dpart);
     }
     red[buf][rg][cg] = acc;

@@ -11,6 +11,13 @@
 // form kernel 1 + a + a^2/2 (paper Eq. (4)), so the C x D feature product
 // is never formed for it.
 //
+// With a fixed per-head retention lambda (s_i = lambda s_{i-1} + phi(k_i) v_i^T,
+// z likewise; BASED notes, the decay paragraph after Table 7) the chunk of n
+// tokens r = 0..n-1 uses P_rj = lambda^(r-j) (1 + a + a^2/2), readout rows
+// scaled by lambda^(r+1), state-update rows by lambda^(n-1-j), and the state
+// scaled by lambda^n before the update; every factor is at most 1 for lambda
+// in [0, 1].  This is a separate instantiation (DECAY = true).
+//
 // Inside the kernel the state is kept in the compact symmetric feature basis
 // (the pages' 153-wide count, padded to 160): c = [1, x_a, x_a^2/sqrt2,
 // x_a x_b (a<b)] gives the same kernel value as phi with half the width.  The
@@ -137,6 +144,35 @@ __device__ __forceinline__ uint4 feature8(const uint32_t* w, const float* x) {
   return make_uint4(feature_pair<BEGIN>(w, x), feature_pair<BEGIN + 2>(w, x), feature_pair<BEGIN + 4>(w, x),
                     feature_pair<BEGIN + 6>(w, x));
 }
+// Features [BEGIN, BEGIN + 8) of a row times `sc`, rounded once to bf16.
+template <int BEGIN>
+__device__ __forceinline__ uint4 feature8_scaled(const float* x, float sc) {
+  const float f[8] = {feature<BEGIN>(x) * sc,     feature<BEGIN + 1>(x) * sc, feature<BEGIN + 2>(x) * sc,
+                      feature<BEGIN + 3>(x) * sc, feature<BEGIN + 4>(x) * sc, feature<BEGIN + 5>(x) * sc,
+                      feature<BEGIN + 6>(x) * sc, feature<BEGIN + 7>(x) * sc};
+  return pack8_bf16(f);
+}
+template <int BEGIN>
+__device__ __forceinline__ void store_features80_scaled(uint8_t* tile, int row, const float* x, float sc) {
+#pragma unroll
+  for (int g = 0; g < 10; ++g) {
+    // g is a compile-time constant after unrolling; the switch selects the instantiation
+    uint4 u;
+    switch (g) {
+      case 0: u = feature8_scaled<BEGIN + 0>(x, sc); break;
+      case 1: u = feature8_scaled<BEGIN + 8>(x, sc); break;
+      case 2: u = feature8_scaled<BEGIN + 16>(x, sc); break;
+      case 3: u = feature8_scaled<BEGIN + 24>(x, sc); break;
+      case 4: u = feature8_scaled<BEGIN + 32>(x, sc); break;
+      case 5: u = feature8_scaled<BEGIN + 40>(x, sc); break;
+      case 6: u = feature8_scaled<BEGIN + 48>(x, sc); break;
+      case 7: u = feature8_scaled<BEGIN + 56>(x, sc); break;
+      case 8: u = feature8_scaled<BEGIN + 64>(x, sc); break;
+      default: u = feature8_scaled<BEGIN + 72>(x, sc); break;
+    }
+    *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 8 * g, kC)) = u;
+  }
+}
 // Row `row` of a [128][192] feature tile, features [BEGIN, BEGIN + 80).
 template <int BEGIN>
 __device__ __forceinline__ void store_features80(uint8_t* tile, int row, const uint32_t* w, const float* x) {
@@ -196,7 +232,7 @@ __device__ __forceinline__ void store_row32<float>(float* dst, const float* v) {
     reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-template <typename TOut>
+template <typename TOut, bool DECAY>
 __global__ void __launch_bounds__(kBlock, 1)
 taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPrefillLaunch a, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
@@ -226,6 +262,11 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   const int my_feature = half == 0 ? row : f1;
   const uint32_t my_colc = half == 0 ? kColC0 : kColC1;
   auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(smem_u32(bar), parity, status); };
+  // per-head retention: lambda^e for e >= 0 (lambda^0 = 1 also for lambda = 0)
+  const float lam = DECAY ? a.decay[h] : 1.f;
+  const float l2lam = DECAY ? log2f(lam) : 0.f;
+  auto lam_pow = [&](float e) { return (!DECAY || e == 0.f) ? 1.f : exp2f(l2lam * e); };
+  auto chunk_len = [&](int cc) { return (int)min((int64_t)kC, N - (int64_t)cc * kC); };
 
   if (tid == 0) {
     mbar_init(smem_u32(&bar_tma[0]), 1);
@@ -406,14 +447,19 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       v[kDv] = compact_z(my_feature);
 #pragma unroll
       for (int i = 1; i < 16; ++i) v[kDv + i] = 0.f;
-#pragma unroll
-      for (int c = 0; c < kDv + 16; c += 16) tmem_st16(tlane + my_colc + c, *reinterpret_cast<float(*)[16]>(v + c));
       if (my_feature >= 0) {
 #pragma unroll
         for (int q = 0; q < 8; ++q)
           *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(my_feature, 8 * q, 192)) = pack8_bf16(v + 8 * q);
         *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(v[kDv]);
       }
+      if constexpr (DECAY) {  // chunk 0's update adds to lambda^n0 [c_in | z_in]; its readout sees c_in
+        const float sc = lam_pow((float)chunk_len(0));
+#pragma unroll
+        for (int i = 0; i < kDv + 16; ++i) v[i] *= sc;
+      }
+#pragma unroll
+      for (int c = 0; c < kDv + 16; c += 16) tmem_st16(tlane + my_colc + c, *reinterpret_cast<float(*)[16]>(v + c));
       tmem_st_wait();
     }
 
@@ -435,6 +481,20 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       float xq[kF], xk[kF];
       read_qk(cc, wq, wk, xq, xk);
       const bool valid = (int64_t)cc * kC + row < N;
+      if constexpr (DECAY) {
+        // readout rows times lambda^(r+1), update rows times lambda^(n-1-r) (padded rows: 0)
+        const int n = chunk_len(cc);
+        const float sq = lam_pow((float)(row + 1));
+        const float sk = row < n ? lam_pow((float)(n - 1 - row)) : 0.f;
+        if (half == 0) {
+          store_features80_scaled<0>(sm + kOffPhiQ, row, xq, sq);
+          store_features80_scaled<0>(sm + kOffPhiK, row, xk, sk);
+        } else {
+          store_features80_scaled<80>(sm + kOffPhiQ, row, xq, sq);
+          store_features80_scaled<80>(sm + kOffPhiK, row, xk, sk);
+        }
+        return;
+      }
       if (half == 0) {
         store_features80<0>(sm + kOffPhiQ, row, wq, xq);
         store_features80<0>(sm + kOffPhiK, row, wk, xk);
@@ -470,7 +530,9 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       }
     };
     // bf16 c and z tiles for the next readout from the tensor-memory state (warp-collective loads)
-    auto refresh_state_tiles = [&]() {
+    auto refresh_state_tiles = [&](float next_scale) {
+      // (with decay: the fp32 state becomes lambda^n [c | z] for the next chunk's update; the bf16 tiles
+      // keep the unscaled state for its readout)
 #pragma unroll
       for (int hv = 0; hv < 2; ++hv) {
         float v[32];
@@ -482,12 +544,24 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
           for (int q = 0; q < 4; ++q)
             *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(my_feature, 32 * hv + 8 * q, 192)) = pack8_bf16(v + 8 * q);
         }
+        if constexpr (DECAY) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= next_scale;
+          tmem_st16(tlane + my_colc + 32 * hv, *reinterpret_cast<float(*)[16]>(v));
+          tmem_st16(tlane + my_colc + 32 * hv + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+        }
       }
       float zz[16];
       tmem_ld16(tlane + my_colc + kDv, zz);
       tmem_ld_wait();
       if (my_feature >= 0)
         *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(zz[0]);
+      if constexpr (DECAY) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) zz[i] *= next_scale;
+        tmem_st16(tlane + my_colc + kDv, zz);
+        tmem_st_wait();
+      }
     };
 
     // Error path: a wait that expires sets the status word and leaves this thread's `ok` false; the
@@ -536,6 +610,16 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
 #pragma unroll
             for (int j = 0; j < 32; ++j) p[j] = j < nv ? fmaf(p[j], fmaf(0.5f, p[j], 1.f), 1.f) : 0.f;
           }
+          if constexpr (DECAY) {
+            // times lambda^(row - base - j) on the kept columns: from column 31 down the factor starts at
+            // lambda^max(nv - 32, 0) and gains one lambda per kept column
+            float f = lam_pow((float)max(nv - 32, 0));
+#pragma unroll
+            for (int j = 31; j >= 0; --j) {
+              p[j] *= f;
+              if (j < nv) f *= lam;
+            }
+          }
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             *reinterpret_cast<uint4*>(prow + sw128_off(row, base + 8 * q, kC)) = pack8_bf16(p + 8 * q);
@@ -562,7 +646,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       ok = ok && wait(&bar_r1, par);
       tc_fence_after();
       if (has_next) {
-        refresh_state_tiles();
+        refresh_state_tiles(lam_pow((float)chunk_len(c + 1)));
         features(c + 1);
         fence_proxy_async_smem();
         tc_fence_before();
@@ -588,9 +672,17 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       float* z_out = a.z_out + bh * kDfull;
       const int j = my_feature;
       const bool has = j >= 0 && j < kDcUsed;
+      // with decay the incoming state's share is Lambda = lambda^N of it:
+      // s_out = Lambda s_in + expand(c - Lambda c_in)
+      const float Lam = lam_pow((float)N);
       float prev[kDv];
       compact_row(j, prev);  // zeros when j has no full-basis rows
-      const float zprev = compact_z(j);
+      float zprev = compact_z(j);
+      if constexpr (DECAY) {
+#pragma unroll
+        for (int i = 0; i < kDv; ++i) prev[i] *= Lam;
+        zprev *= Lam;
+      }
       int r0 = 0, r1 = -1;
       float sc = 1.f;
       const int n = has ? full_rows_of(j, r0, r1, sc) : 0;
@@ -611,6 +703,9 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
             for (int cc = 0; cc < 32; cc += 4) {
               const int col = 32 * hv + cc;
               float4 base = s_in ? *reinterpret_cast<const float4*>(s_in + r * kDv + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+              if constexpr (DECAY) {
+                base.x *= Lam; base.y *= Lam; base.z *= Lam; base.w *= Lam;
+              }
               base.x += (cur[cc] - prev[col]) * sc;
               base.y += (cur[cc + 1] - prev[col + 1]) * sc;
               base.z += (cur[cc + 2] - prev[col + 2]) * sc;
@@ -621,7 +716,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         }
         for (int k = 0; k < n; ++k) {
           const int r = k == 0 ? r0 : r1;
-          const float zb = z_in ? z_in[r] : 0.f;
+          const float zb = z_in ? Lam * z_in[r] : 0.f;
           z_out[r] = zb + (zz[0] - zprev) * sc;
         }
       }
@@ -649,7 +744,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-template <typename TOut>
+template <typename TOut, bool DECAY>
 cudaError_t launch_typed(const TaylorPrefillLaunch& a, unsigned* status, cudaStream_t stream) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return cudaErrorInvalidValue;
@@ -665,11 +760,11 @@ cudaError_t launch_typed(const TaylorPrefillLaunch& a, unsigned* status, cudaStr
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(taylor_chunked_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(taylor_chunked_kernel<TOut, DECAY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)kSmemAlloc);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  taylor_chunked_kernel<TOut><<<(unsigned)(a.B * a.H), kBlock, kSmemAlloc, stream>>>(mv, a, status);
+  taylor_chunked_kernel<TOut, DECAY><<<(unsigned)(a.B * a.H), kBlock, kSmemAlloc, stream>>>(mv, a, status);
   return cudaGetLastError();
 }
 
@@ -677,7 +772,9 @@ cudaError_t launch_typed(const TaylorPrefillLaunch& a, unsigned* status, cudaStr
 
 cudaError_t launch_taylor_prefill_chunked(const TaylorPrefillLaunch& a, unsigned* status, cudaStream_t stream) {
   if (a.B * a.H == 0 || a.N == 0) return cudaSuccess;
-  return a.out_bf16 ? launch_typed<__nv_bfloat16>(a, status, stream) : launch_typed<float>(a, status, stream);
+  if (a.decay)
+    return a.out_bf16 ? launch_typed<__nv_bfloat16, true>(a, status, stream) : launch_typed<float, true>(a, status, stream);
+  return a.out_bf16 ? launch_typed<__nv_bfloat16, false>(a, status, stream) : launch_typed<float, false>(a, status, stream);
 }
 
 }  // namespace la

@@ -43,7 +43,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert la.la_abi_version() == 1
+    assert la.la_abi_version() == 2
     for code in range(6):
         assert la.la_status_string(code)
     assert la.la_status_string(99) == "unknown status"
@@ -118,6 +118,7 @@ def test_based_rejections(lib):
     assert call_based(lib, based_args(dv=32)) == la.LA_ERR_UNSUPPORTED
     assert call_based(lib, based_args(set={"z_out": None})) == la.LA_ERR_INVALID_ARGUMENT
     assert call_based(lib, based_args(set={"s_out": 0x10004})) == la.LA_ERR_INVALID_ARGUMENT
+    assert call_based(lib, based_args(set={"decay": 0x10002})) == la.LA_ERR_INVALID_ARGUMENT  # not 4-byte aligned
     a = based_args()
     a.q = _tensor(0x10000, 16 * 64, 16 * 64, 12)
     assert call_based(lib, a) == la.LA_ERR_INVALID_ARGUMENT
@@ -128,7 +129,8 @@ def test_decode_rejections(lib):
     mk = lambda **kw: la.DecodeArgs(kw.get("variant", la.LA_VARIANT_GDN), kw.get("S", 2), 2, kw.get("dk", 128),
                                     kw.get("dv", 128), la.LA_DTYPE_BF16, la.LA_DTYPE_BF16,
                                     kw.get("q", 0x10000), 0x20000, 0x30000, kw.get("alpha", 0x40000), 0x50000,
-                                    0x60000, kw.get("state", 0x70000), kw.get("z", None), 0.0, 1.0)
+                                    0x60000, kw.get("state", 0x70000), kw.get("z", None), 0.0, 1.0,
+                                    kw.get("decay", None))
     call = lambda a: lib.la_decode_step(ctypes.byref(a), None)
     assert lib.la_decode_step(None, None) == la.LA_ERR_INVALID_ARGUMENT
     assert call(mk(variant=5)) == la.LA_ERR_INVALID_ARGUMENT
@@ -138,6 +140,7 @@ def test_decode_rejections(lib):
     assert call(mk(q=None)) == la.LA_ERR_INVALID_ARGUMENT
     assert call(mk(alpha=None)) == la.LA_ERR_INVALID_ARGUMENT
     assert call(mk(state=0x70004)) == la.LA_ERR_INVALID_ARGUMENT
+    assert call(mk(variant=la.LA_VARIANT_TAYLOR, dk=16, dv=64, z=0x80000, decay=0x90002)) == la.LA_ERR_INVALID_ARGUMENT
     assert call(mk(S=0)) == la.LA_OK
 
 
