@@ -278,3 +278,95 @@ def _widen(x):
     if x.dtype == np.uint16:
         return (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     return x.astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# NoteBank write side and routing ("History Replays Itself: Unleashing
+# Long-Context Capability in Linear Attention", Sec. 2 Eqs. (3)-(5) and
+# App. B Eqs. (8)-(9)).  Plain numpy definitions: scores and addresses in
+# float64; routing in float32, the precision the pages fix for it (bf16
+# addresses and question features converted to fp32, then normalised).
+# Readings: a zero vector normalises to zero (so a zero key scores 1); the
+# argmaxes take the earliest index on ties; only notes with at least one
+# vote are retrieved.
+
+
+def _unit(x):
+    n = np.linalg.norm(x, axis=-1, keepdims=True)
+    return np.where(n > 0, x / np.where(n > 0, n, 1.0), 0.0)
+
+
+def notebank_scores(k, chunk: int, window: int = 48):
+    """Distinctiveness of every token in every channel (Eqs. (3), (8)):
+    mu_C = unit(mean_{t in C} unit(k_t)) per chunk C of `chunk` tokens
+    ([c*chunk, (c+1)*chunk), the last one possibly short) and channel;
+    d_t^{l,h} = 1 - <unit(k_t), mu_C(t)>; d_t = mean over the L*H channels;
+    w_t = sum_{u=t}^{t+window-1} d_u (the sliding window of App. B.2).
+    k: [L, H, N, d] (float32 or bf16 bits).  Returns dict(d_ch [L,H,N],
+    d [N], w [N - window + 1])."""
+    k = _widen(k)
+    L, H, N, _ = k.shape
+    kh = _unit(k)
+    d_ch = np.zeros((L, H, N))
+    for c0 in range(0, N, chunk):
+        c1 = min(c0 + chunk, N)
+        mu = _unit(kh[:, :, c0:c1].mean(axis=2))
+        d_ch[:, :, c0:c1] = 1.0 - np.einsum("lhtd,lhd->lht", kh[:, :, c0:c1], mu)
+    d = d_ch.mean(axis=(0, 1))
+    w = np.array([d[t:t + window].sum() for t in range(max(N - window + 1, 0))])
+    return {"d_ch": d_ch, "d": d, "w": w}
+
+
+def _round_bf16(x):
+    """Round float32 values to bf16 (nearest, ties to even); returned as float64."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = ((b + 0x7FFF + ((b >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def notebank_address(d_ch, q, coords, spans):
+    """Note addresses (Eqs. (4), (9)): for note i with token span I_i and
+    channel (l,h), t* = argmax_{t in I_i} d_t^{l,h} (earliest on ties) and
+    rho_i^{l,h} = P^{l,h} q_{t*}: the query's coordinates coords[l,h, 0..15]
+    at t*, stored as bf16.  d_ch: [L,H,N]; q: [L,H,N,d] (float32 or bf16
+    bits); coords: [L,H,16]; spans: [n,2] (start, length >= 1).  Returns
+    t_star [n,L,H] and rho [n,L,H,16] (the bf16 values as float64)."""
+    d_ch = np.asarray(d_ch, dtype=np.float64)
+    qf = _widen(q).astype(np.float32)
+    L, H, N = d_ch.shape
+    spans = np.asarray(spans, dtype=np.int64).reshape(-1, 2)
+    n = spans.shape[0]
+    t_star = np.zeros((n, L, H), dtype=np.int64)
+    rho = np.zeros((n, L, H, coords.shape[-1]))
+    for i, (s0, ln) in enumerate(spans):
+        for l in range(L):
+            for h in range(H):
+                seg = d_ch[l, h, s0:s0 + ln]
+                t = int(s0 + int(np.argmax(seg)))  # numpy returns the first maximum
+                t_star[i, l, h] = t
+                rho[i, l, h] = _round_bf16(qf[l, h, t, np.asarray(coords[l, h], dtype=np.int64)])
+    return t_star, rho
+
+
+def notebank_route(rho, u, R: int, positions=None):
+    """Routing (Eq. (5)): s_i^{l,h} = max_tau <unit(u_tau^{l,h}), unit(rho_i^{l,h})>
+    in float32; each channel votes for argmax_i s_i^{l,h} (earliest on ties);
+    V_i = number of votes; the at most R notes with V_i >= 1 and the most
+    votes, ties to the earlier-inserted note, returned in text order (by
+    `positions`, else insertion order).  rho: [n, J, 16]; u: [J, nq, 16]
+    (values of bf16 numbers).  Returns dict(s [n,J], winner [J], votes [n],
+    top [<= R])."""
+    rho = np.asarray(rho, dtype=np.float32)
+    u = np.asarray(u, dtype=np.float32)
+    n, J, _ = rho.shape
+    rn = (rho / np.linalg.norm(rho, axis=-1, keepdims=True).astype(np.float32)).astype(np.float32)
+    un = (u / np.linalg.norm(u, axis=-1, keepdims=True).astype(np.float32)).astype(np.float32)
+    s = np.zeros((n, J), dtype=np.float32)
+    for j in range(J):
+        s[:, j] = np.max(rn[:, j, :] @ un[j].T, axis=1)
+    winner = np.array([int(np.argmax(s[:, j])) for j in range(J)], dtype=np.int64)
+    votes = np.bincount(winner, minlength=n).astype(np.int64)
+    order = sorted((i for i in range(n) if votes[i] >= 1), key=lambda i: (-votes[i], i))[:R]
+    pos = np.arange(n) if positions is None else np.asarray(positions)
+    top = np.array(sorted(order, key=lambda i: (pos[i], i)), dtype=np.int64)
+    return {"s": s, "winner": winner, "votes": votes, "top": top}

@@ -83,3 +83,36 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new):
     finally:
         oracle.restore_library(prev)
     assert any(caught), f"no pin caught the planted mistake '{name}'"
+
+
+# Planted mistakes in the numpy definitions (the NoteBank write side and routing): the function is
+# rebuilt from an edited copy of its source and swapped in while the NoteBank pins run.
+PY_SRC = os.path.join(os.path.dirname(SRC), "__init__.py")
+PY_MUTANTS = [
+    ("chunk mean not re-normalised", "mu = _unit(kh[:, :, c0:c1].mean(axis=2))", "mu = kh[:, :, c0:c1].mean(axis=2)"),
+    ("keys not normalised", "kh = _unit(k)", "kh = k"),
+    ("window one token short", "w = np.array([d[t:t + window].sum()", "w = np.array([d[t:t + window - 1].sum()"),
+    ("channel mean over tokens", "d = d_ch.mean(axis=(0, 1))", "d = d_ch.mean(axis=(0, 1)) * 0 + d_ch.mean()"),
+    ("last maximum on ties", "t = int(s0 + int(np.argmax(seg)))",
+     "t = int(s0 + len(seg) - 1 - int(np.argmax(seg[::-1])))"),
+    ("address gathered at the span start", "rho[i, l, h] = _round_bf16(qf[l, h, t,", "rho[i, l, h] = _round_bf16(qf[l, h, s0,"),
+    ("later note wins equal votes", "key=lambda i: (-votes[i], i))[:R]", "key=lambda i: (-votes[i], -i))[:R]"),
+    ("retrieved in vote order", "top = np.array(sorted(order, key=lambda i: (pos[i], i)), dtype=np.int64)",
+     "top = np.array(order, dtype=np.int64)"),
+    ("mean instead of max over the question", "s[:, j] = np.max(rn[:, j, :] @ un[j].T, axis=1)",
+     "s[:, j] = np.mean(rn[:, j, :] @ un[j].T, axis=1)"),
+]
+NB_PINS = [pins.test_notebank_scores_hand_example, pins.test_notebank_scores_identities,
+           pins.test_notebank_address_argmax_and_gather, pins.test_notebank_route_worked_example,
+           pins.test_notebank_route_ties_scaling_and_max_over_question]
+
+
+@pytest.mark.parametrize("name,old,new", PY_MUTANTS, ids=[m[0] for m in PY_MUTANTS])
+def test_notebank_pins_catch_planted_mistake(monkeypatch, name, old, new):
+    text = open(PY_SRC).read()
+    assert old in text, f"mutation anchor for '{name}' not found"
+    ns = {"__name__": "oracle_mutant", "__file__": PY_SRC}
+    exec(compile(text.replace(old, new, 1), "oracle_mutant", "exec"), ns)
+    for fn in ("notebank_scores", "notebank_address", "notebank_route"):
+        monkeypatch.setattr(oracle, fn, ns[fn])
+    assert any(_caught(f) for f in NB_PINS), f"no pin caught the planted mistake '{name}'"

@@ -579,3 +579,106 @@ def test_empty_sequence_passes_state_through():
     S0 = rng.standard_normal((1, 2, 8, 16))
     out = oracle.gdn(q, q, v, np.zeros((1, 2, 0), np.float32), np.zeros((1, 2, 0), np.float32), S_in=S0)
     assert np.array_equal(out["S"], S0)
+
+
+# --------------------------------------------------------------------------
+# NoteBank write side and routing (NoteBank Sec. 2 Eqs. (3)-(5), App. B
+# Eqs. (8)-(9))
+
+
+def test_notebank_scores_hand_example():
+    # keys (1,0), (0,1), (1,1): unit keys e1, e2, (e1+e2)/sqrt2; their mean points along (1,1),
+    # so mu = (1,1)/sqrt2 and d = 1 - 1/sqrt2, 1 - 1/sqrt2, 0
+    k = np.array([[[[1, 0], [0, 1], [1, 1]]]], dtype=np.float32)
+    r = oracle.notebank_scores(k, chunk=3, window=2)
+    a = 1 - 1 / math.sqrt(2)
+    assert np.allclose(r["d_ch"][0, 0], [a, a, 0.0], rtol=0, atol=1e-15)
+    assert np.allclose(r["w"], [2 * a, a], rtol=0, atol=1e-15)
+
+
+def test_notebank_scores_identities():
+    L, H, N, d, C = 2, 3, 70, 8, 32
+    k = f32((L, H, N, d))
+    r = oracle.notebank_scores(k, chunk=C, window=5)
+    # per chunk and channel: mean_t (1 - d_t) = <mean_t unit(k_t), mu> = |mean_t unit(k_t)|
+    kh = k / np.linalg.norm(k.astype(np.float64), axis=-1, keepdims=True)
+    for c0 in range(0, N, C):
+        c1 = min(c0 + C, N)
+        m = np.linalg.norm(kh[:, :, c0:c1].mean(axis=2), axis=-1)
+        assert np.allclose((1 - r["d_ch"][:, :, c0:c1]).mean(axis=2), m, rtol=1e-12, atol=1e-12)
+    assert np.all(r["d_ch"] >= -1e-12) and np.all(r["d_ch"] <= 2 + 1e-12)
+    assert np.allclose(r["d"], r["d_ch"].mean(axis=(0, 1)), rtol=0, atol=0)
+    cs = np.concatenate([[0.0], np.cumsum(r["d"])])
+    assert np.allclose(r["w"], cs[5:] - cs[:-5], rtol=1e-12, atol=1e-12)
+    # positive rescaling of any key changes nothing; parallel keys are not distinctive
+    k2 = k * (0.5 + rng.random((L, H, N, 1))).astype(np.float32)
+    assert np.allclose(oracle.notebank_scores(k2, chunk=C, window=5)["d_ch"], r["d_ch"], atol=1e-6)
+    par = np.broadcast_to(k[:, :, :1], k.shape) * (1 + rng.random((L, H, N, 1))).astype(np.float32)
+    assert np.allclose(oracle.notebank_scores(par, chunk=C)["d_ch"], 0.0, atol=1e-7)
+
+
+def test_notebank_address_argmax_and_gather():
+    L, H, N, d = 1, 2, 40, 32
+    d_ch = rng.random((L, H, N))
+    d_ch[0, 0, 12] = d_ch[0, 0, 17] = 5.0      # tie inside the span: the earlier token wins
+    d_ch[0, 1, 30] = 9.0                       # outside the span: ignored
+    q = f32((L, H, N, d))
+    coords = np.stack([rng.permutation(d)[:16] for _ in range(L * H)]).reshape(L, H, 16)
+    t_star, rho = oracle.notebank_address(d_ch, q, coords, [(10, 15)])
+    assert t_star[0, 0, 0] == 12
+    assert t_star[0, 0, 1] == 10 + int(np.argmax(d_ch[0, 1, 10:25]))
+    for h in range(H):
+        vals = q[0, h, t_star[0, 0, h], coords[0, h]]
+        assert np.all(np.abs(rho[0, 0, h] - vals) <= np.abs(vals) * 2.0 ** -8)   # one bf16 rounding
+        assert np.array_equal(rho[0, 0, h], oracle._round_bf16(vals))
+
+
+def test_notebank_route_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "notebank_vote_example.json")))
+    names = g["notes"]
+    J = len(g["channel_winners"])
+    # note i's address in channel j is e_j if note i should win channel j, else e_(j+1); the question
+    # feature of channel j is e_j: the winner has cosine 1, the other note 0
+    rho = np.zeros((len(names), J, 16), np.float32)
+    for j, w in enumerate(g["channel_winners"]):
+        for i, nm in enumerate(names):
+            rho[i, j, j if nm == w else j + 1] = 1.0
+    u = np.zeros((J, 1, 16), np.float32)
+    for j in range(J):
+        u[j, 0, j] = 1.0
+    # A was written after B in the text: the replay order must follow the text, not the votes
+    r = oracle.notebank_route(rho, u, R=g["R"], positions=[500, 100])
+    assert [names[i] for i in r["winner"]] == g["channel_winners"]
+    assert {names[i]: int(r["votes"][i]) for i in range(len(names))} == g["votes"]
+    assert sorted(names[i] for i in r["top"]) == sorted(g["retrieved"])
+    assert [names[i] for i in r["top"]] == ["B", "A"]
+    assert [names[i] for i in oracle.notebank_route(rho, u, R=1, positions=[500, 100])["top"]] == ["A"]
+
+
+def test_notebank_route_ties_scaling_and_max_over_question():
+    n, J, nq = 6, 4, 5
+    rho = f32((n, J, 16))
+    u = f32((J, nq, 16))
+    r = oracle.notebank_route(rho, u, R=3)
+    # cosine: positive rescaling of addresses or question features changes nothing
+    r2 = oracle.notebank_route(rho * 3.0, u * 0.25, R=3)
+    assert np.allclose(r2["s"], r["s"], atol=1e-6) and np.array_equal(r2["winner"], r["winner"])
+    # max over question tokens: each s equals the best single-token cosine
+    for i in range(n):
+        for j in range(J):
+            best = max(float(np.dot(rho[i, j], u[j, t]) / np.linalg.norm(rho[i, j]) / np.linalg.norm(u[j, t]))
+                       for t in range(nq))
+            assert r["s"][i, j] == pytest.approx(best, abs=1e-6)
+    assert r["votes"].sum() == J
+    # a duplicate of the winning note inserted later never takes its vote (ties go to the earlier note)
+    w0 = int(r["winner"][0])
+    dup = np.concatenate([rho, rho[w0:w0 + 1]], axis=0)
+    assert oracle.notebank_route(dup, u, R=3)["winner"][0] == w0
+    # equal votes: the earlier-inserted note is retrieved first
+    rho2 = np.zeros((3, 2, 16), np.float32)
+    u2 = np.zeros((2, 1, 16), np.float32)
+    rho2[0, 0, 0] = rho2[2, 1, 1] = 1.0
+    rho2[1, :, 5] = rho2[0, 1, 5] = rho2[2, 0, 5] = 1.0
+    u2[0, 0, 0] = u2[1, 0, 1] = 1.0
+    r3 = oracle.notebank_route(rho2, u2, R=1)
+    assert list(r3["votes"]) == [1, 0, 1] and list(r3["top"]) == [0]
