@@ -11,7 +11,9 @@ step).  The same run also times, under ``paths``:
   decode_gdn        1000 decode steps, 256 seqs x 16 heads, 128x128 state
   decode_taylor     1000 decode steps, 256 seqs x 16 heads, 273x64 state + z
   decode_swa        1000 sliding-window softmax decode steps, 256 seqs x 16 heads, window 64
-each with its own tokens/s and roofline.
+  notebank_write    NoteBank write side: scores of 192 channels (d_k 256) over 16K tokens + note addresses
+  notebank_route    NoteBank routing of one 64-token question over 4092 notes x 192 channels
+each with its own rate and roofline.
 
 Timing: W untimed warm-up steps, then K steps; each launch is bracketed by
 CUDA events on its own stream and an L2 flush (a 512 MiB write, outside the
@@ -318,7 +320,12 @@ KERNELS_PER_CALL = {"based_prefill": 1, "gdn_prefill": 2, "decode": 1}
 
 
 PATH_NAMES = ("based_prefill_decay", "gdn_prefill", "gdn_prefill_long", "gated_prefill", "decode_gdn", "decode_taylor",
-              "decode_swa")
+              "decode_swa", "notebank_write", "notebank_route")
+
+# NoteBank sizes (NoteBank App. C: GDN backbone with J = 192 layer-head channels of d_k = 256, write chunks of
+# 512 tokens, 16-dimensional addresses, about 4092 stored notes; the question length is a synthetic choice)
+NB_L, NB_H, NB_D, NB_N, NB_CHUNK, NB_WINDOW = 24, 8, 256, 16384, 512, 48
+NB_NOTES, NB_NOTE_LEN, NB_Q, NB_R = 4092, 64, 64, 2
 
 
 def decay_rates(H):
@@ -475,6 +482,78 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
                              "tokens_per_s": round(whole_job_rate(S_, ws, per_step * 1e-3), 1),
                              "ms_per_step": round(per_step, 5), "roofline": r}
         del xs, kc, vc, pos, outb
+        torch.cuda.empty_cache()
+    if only is None or only in ("notebank_write", "notebank_route"):
+        nb, nb_launches = notebank_paths(args, la, dev, stream, flush, pk, seed_off, ws, only)
+        out.update(nb)
+        launches += nb_launches
+    return out, launches
+
+
+def notebank_paths(args, la, dev, stream, flush, pk, seed_off, ws, only):
+    """NoteBank's write side on one 16K-token document (scores of all 192 channels, then the addresses of
+    two notes per 512-token chunk) and its routing of one question over 4092 stored notes."""
+    out, launches = {}, 0
+    steps = max(1, args.steps)
+    g = torch.Generator(device="cpu").manual_seed(11 + seed_off)
+    J = NB_L * NB_H
+    if only is None or only == "notebank_write":
+        k = torch.randn((NB_L, NB_H, NB_N, NB_D), generator=g).to(torch.bfloat16).to(dev)
+        q = torch.randn((NB_L, NB_H, NB_N, NB_D), generator=g).to(torch.bfloat16).to(dev)
+        coords = torch.stack([torch.randperm(NB_D, generator=g)[:16] for _ in range(J)]).view(NB_L, NB_H, 16)
+        coords = coords.to(torch.int32).to(dev)
+        n_notes = 2 * (NB_N // NB_CHUNK)
+        starts = torch.arange(n_notes, dtype=torch.int64) * (NB_CHUNK // 2)
+        spans = torch.stack([starts, torch.full_like(starts, NB_NOTE_LEN)], dim=1).to(dev)
+
+        def wstep():
+            d_ch, _, _ = la.la_notebank_scores(k, chunk=NB_CHUNK, window=NB_WINDOW, stream=stream)
+            la.la_notebank_address(d_ch, q, coords, spans, stream=stream)
+
+        t = Timer(stream, flush)
+        for _ in range(args.warmup):
+            t.run(wstep)
+        t.reset()
+        barrier(ws)
+        for _ in range(steps):
+            t.run(wstep)
+        ms = max_over_ranks(t.total_ms(), ws) / steps
+        launches += 3 * steps  # chunk scores, token scores, addresses
+        # algorithmic bytes: every key read once, d_ch written and read once, d_mean and w written,
+        # and per (note, channel) the span's scores and 16 query coordinates
+        byts = J * NB_N * (NB_D * 2 + 4 + 4) + NB_N * 8 + n_notes * J * (NB_NOTE_LEN * 4 + 16 * 2 * 2 + 4)
+        out["notebank_write"] = {"workload": f"NoteBank write side: {J} channels ({NB_L} layers x {NB_H} heads), "
+                                             f"d_k {NB_D}, {NB_N} tokens, chunks of {NB_CHUNK}, "
+                                             f"{n_notes} note addresses",
+                                 "tokens_per_s": round(whole_job_rate(NB_N, ws, ms * 1e-3), 1),
+                                 "ms": round(ms, 4), "roofline": roofline(byts, ms, pk["hbm_gbs"], None)}
+        del k, q
+        torch.cuda.empty_cache()
+    if only is None or only == "notebank_route":
+        rho = torch.randn((NB_NOTES, J, 16), generator=g).to(torch.bfloat16).to(dev)
+        u = torch.randn((J, NB_Q, 16), generator=g).to(torch.bfloat16).to(dev)
+        positions = (torch.arange(NB_NOTES, dtype=torch.int64) * 32).to(dev)
+
+        def rstep():
+            la.la_notebank_route(rho, u, NB_R, positions=positions, stream=stream)
+
+        t = Timer(stream, flush)
+        for _ in range(args.warmup):
+            t.run(rstep)
+        t.reset()
+        barrier(ws)
+        for _ in range(steps):
+            t.run(rstep)
+        ms = max_over_ranks(t.total_ms(), ws) / steps
+        launches += 2 * steps
+        flops = 2.0 * NB_NOTES * J * NB_Q * 16
+        out["notebank_route"] = {"workload": f"NoteBank routing: {NB_NOTES} notes x {J} channels x 16-dim addresses, "
+                                             f"{NB_Q}-token question, R = {NB_R}",
+                                 "questions_per_s": round(whole_job_rate(1, ws, ms * 1e-3), 1),
+                                 "ms": round(ms, 4),
+                                 "roofline": {"bound": "alu", "achieved": round(flops / (ms * 1e-3) / 1e12, 3),
+                                              "unit": "TFLOP/s fp32 (cosines)"}}
+        del rho, u
         torch.cuda.empty_cache()
     return out, launches
 

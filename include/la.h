@@ -281,11 +281,93 @@ la_status la_state_rescale(float* states, int64_t n_states, int64_t elems_per_st
 la_status la_state_gather(float* dst, const float* src, const int64_t* index, int64_t n_dst,
                           int64_t n_src, int64_t elems_per_state, void* stream);
 
+/* ---- NoteBank write side and routing ("History Replays Itself: Unleashing
+ * Long-Context Capability in Linear Attention" (NoteBank), Sec. 2 Eqs. (3)-(5),
+ * App. B Eqs. (8)-(9)).  A channel is one (layer, head) of the backbone:
+ * the L x H channels of one document are passed as [L, H, N, d] views. */
+
+/* Per-token distinctiveness (Eqs. (3), (8)).  For every chunk of `chunk`
+ * tokens ([c*chunk, (c+1)*chunk), the last one possibly short) and channel:
+ *   mu = unit(mean of the chunk's unit keys),  d_ch[l,h,t] = 1 - <unit(k_t), mu>;
+ * d_mean[t] = mean of d_ch over the channels; w[t] = d_mean[t] + ... +
+ * d_mean[t + window - 1] for t <= N - window (the sliding window whose
+ * maximum picks a note's first window, App. B.2: window = 48).  A zero key
+ * normalises to zero (it scores 1).
+ *   k      : [L, H, N, d] in_dtype view (stride_b = layer, stride_h = head,
+ *            stride_t = token; the feature axis contiguous), d a multiple of
+ *            32 up to 256
+ *   chunk  : 1..1024 (the pages' write chunk is 512 for GDN)
+ *   window : 1..4096
+ *   d_ch   : [L, H, N] fp32, d_mean : [N] fp32, w : [N - window + 1] fp32 or
+ *            NULL; device memory, contiguous.
+ * fp32 arithmetic; the channel mean and window sums add in a fixed order. */
+typedef struct la_notebank_scores_args {
+  int64_t L, H, N, d;
+  la_dtype in_dtype;
+  la_tensor k;
+  int64_t chunk, window;
+  float* d_ch;
+  float* d_mean;
+  float* w;
+} la_notebank_scores_args;
+la_status la_notebank_scores(const la_notebank_scores_args* args, void* stream);
+
+/* Note addresses (Eqs. (4), (9)): for note i with token span
+ * [spans[2i], spans[2i] + spans[2i+1]) and channel (l,h),
+ *   t_star[i,l,h] = argmax over the span of d_ch[l,h,t] (the earliest token
+ *                   on ties),
+ *   rho[i,l,h,:]  = q[l,h,t_star, coords[l,h,0..15]] rounded to bf16 (the
+ *                   query, not the key, at the chosen position; coords is the
+ *                   fixed coordinate selection P^{l,h}).
+ *   q      : [L, H, N, d] in_dtype view;  d_ch : [L, H, N] fp32 (la_notebank_scores)
+ *   coords : [L, H, 16] int32, each in [0, d);  spans : [n_notes, 2] int64
+ *   t_star : [n_notes, L, H] int32;  rho : [n_notes, L, H, 16] bf16
+ * All device memory.  A span outside [0, N) or of length < 1, or a coordinate
+ * outside [0, d), writes t_star = -1 and a zero address for that (note,
+ * channel) and sets the device status word (la_device_status reports
+ * LA_ERR_INVALID_ARGUMENT). */
+typedef struct la_notebank_address_args {
+  int64_t L, H, N, d, n_notes;
+  la_dtype in_dtype;
+  la_tensor q;
+  const float* d_ch;
+  const int32_t* coords;
+  const int64_t* spans;
+  int32_t* t_star;
+  void* rho;
+} la_notebank_address_args;
+la_status la_notebank_address(const la_notebank_address_args* args, void* stream);
+
+/* Routing (Eq. (5)).  For channel j and note i:
+ *   s[i,j] = max over question tokens tau of <unit(u[j,tau]), unit(rho[i,j])>
+ * in fp32 (bf16 inputs converted, then normalised); winner[j] = the first
+ * note with the largest s[., j]; votes[i] = number of channels won; top =
+ * the at most R notes with votes >= 1 and the most votes (ties to the
+ * earlier-inserted note), sorted by positions[] (text order; insertion order
+ * when positions is NULL), padded with -1.  n_notes = 0 gives winner = -1.
+ *   rho : [n_notes, J, 16] bf16 (notes in insertion order, 16-byte aligned)
+ *   u   : [J, n_q, 16] bf16 question features (16-byte aligned), n_q 1..512
+ *   positions : [n_notes] int64 or NULL;  s : [n_notes, J] fp32 or NULL
+ *   winner : [J] int32;  votes : [n_notes] int32;  top : [R] int32 (R 1..64)
+ * All device memory. */
+typedef struct la_notebank_route_args {
+  int64_t n_notes, J, n_q, R;
+  const void* rho;
+  const void* u;
+  const int64_t* positions;
+  float* s;
+  int32_t* winner;
+  int32_t* votes;
+  int32_t* top;
+} la_notebank_route_args;
+la_status la_notebank_route(const la_notebank_route_args* args, void* stream);
+
 /* Synchronises `stream`, then reports (and clears when `clear` != 0) the
  * device-side status word: LA_ERR_TIMEOUT when a bounded wait expired,
  * LA_ERR_INVALID_ARGUMENT when la_state_gather skipped an out-of-range
- * index or la_swa_decode_step a negative position, else LA_OK; LA_ERR_CUDA
- * if the synchronisation failed. */
+ * index, la_swa_decode_step met a negative position or la_notebank_address
+ * a bad span or coordinate, else LA_OK; LA_ERR_CUDA if the synchronisation
+ * failed. */
 la_status la_device_status(void* stream, int clear);
 
 /* Self-test of the bounded-wait error path (infrastructure; the pages have no

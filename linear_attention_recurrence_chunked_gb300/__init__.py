@@ -71,9 +71,27 @@ class DecodeArgs(ctypes.Structure):
 
 EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_gated_prefill", "la_decode_step", "la_based_prefill_workspace_size",
             "la_gdn_prefill_workspace_size", "la_gdn_prefill_workspace_size_min", "la_gdn_prefill_noalloc", "la_device_status",
-            "la_state_rescale", "la_state_gather", "la_swa_decode_step", "la_selftest_bounded_wait",
-            "la_status_string",
-            "la_abi_version")
+            "la_state_rescale", "la_state_gather", "la_swa_decode_step", "la_notebank_scores", "la_notebank_address",
+            "la_notebank_route", "la_selftest_bounded_wait", "la_status_string", "la_abi_version")
+
+
+class NotebankScoresArgs(ctypes.Structure):
+    _fields_ = [("L", _i64), ("H", _i64), ("N", _i64), ("d", _i64), ("in_dtype", ctypes.c_int),
+                ("k", LATensor), ("chunk", _i64), ("window", _i64),
+                ("d_ch", ctypes.c_void_p), ("d_mean", ctypes.c_void_p), ("w", ctypes.c_void_p)]
+
+
+class NotebankAddressArgs(ctypes.Structure):
+    _fields_ = [("L", _i64), ("H", _i64), ("N", _i64), ("d", _i64), ("n_notes", _i64), ("in_dtype", ctypes.c_int),
+                ("q", LATensor), ("d_ch", ctypes.c_void_p), ("coords", ctypes.c_void_p), ("spans", ctypes.c_void_p),
+                ("t_star", ctypes.c_void_p), ("rho", ctypes.c_void_p)]
+
+
+class NotebankRouteArgs(ctypes.Structure):
+    _fields_ = [("n_notes", _i64), ("J", _i64), ("n_q", _i64), ("R", _i64),
+                ("rho", ctypes.c_void_p), ("u", ctypes.c_void_p), ("positions", ctypes.c_void_p),
+                ("s", ctypes.c_void_p), ("winner", ctypes.c_void_p), ("votes", ctypes.c_void_p),
+                ("top", ctypes.c_void_p)]
 
 
 class SwaDecodeArgs(ctypes.Structure):
@@ -125,6 +143,12 @@ def load_library(path: str | None = None):
     lib.la_gdn_prefill_workspace_size_min.argtypes = [ctypes.POINTER(GdnPrefillArgs)]
     lib.la_swa_decode_step.restype = ctypes.c_int
     lib.la_swa_decode_step.argtypes = [ctypes.POINTER(SwaDecodeArgs), vp]
+    lib.la_notebank_scores.restype = ctypes.c_int
+    lib.la_notebank_scores.argtypes = [ctypes.POINTER(NotebankScoresArgs), vp]
+    lib.la_notebank_address.restype = ctypes.c_int
+    lib.la_notebank_address.argtypes = [ctypes.POINTER(NotebankAddressArgs), vp]
+    lib.la_notebank_route.restype = ctypes.c_int
+    lib.la_notebank_route.argtypes = [ctypes.POINTER(NotebankRouteArgs), vp]
     lib.la_state_rescale.restype = ctypes.c_int
     lib.la_state_rescale.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_float, vp]
     lib.la_state_gather.restype = ctypes.c_int
@@ -439,6 +463,73 @@ def la_swa_decode_step(q, k, v, k_cache, v_cache, pos, out=None, scale: float | 
     if st != LA_OK:
         raise LAError(st, "la_swa_decode_step")
     return out
+
+
+NOTE_ADDR_DIMS = 16  # d_rho
+
+
+def la_notebank_scores(k, chunk: int = 512, window: int = 48, stream=None):
+    """NoteBank write-side scores (NoteBank Sec. 2 Eqs. (3), (8)).  k: [L, H, N, d]
+    (the L x H channels of one document; fp32 or bf16, d a multiple of 32 up
+    to 256).  Returns (d_ch [L,H,N], d_mean [N], w [N - window + 1]) fp32."""
+    lib = load_library()
+    _check_cuda(k)
+    L, H, N, d = k.shape
+    d_ch = torch.empty((L, H, N), dtype=torch.float32, device=k.device)
+    d_mean = torch.empty((N,), dtype=torch.float32, device=k.device)
+    w = torch.empty((max(N - window + 1, 0),), dtype=torch.float32, device=k.device)
+    a = NotebankScoresArgs(L, H, N, d, _dtype_code(k.dtype), _view4(k), int(chunk), int(window),
+                           _ptr(d_ch), _ptr(d_mean), _ptr(w) if w.numel() else None)
+    st = lib.la_notebank_scores(ctypes.byref(a), _stream_handle(stream))
+    if st != LA_OK:
+        raise LAError(st, "la_notebank_scores")
+    return d_ch, d_mean, w
+
+
+def la_notebank_address(d_ch, q, coords, spans, stream=None):
+    """NoteBank note addresses (Eqs. (4), (9)): per note span and channel, the
+    argmax of d_ch over the span and the query's 16 `coords` there as bf16.
+    d_ch [L,H,N] fp32, q [L,H,N,d], coords int32 [L,H,16], spans int64 [n,2]
+    (start, length), all on the device.  Returns (t_star int32 [n,L,H],
+    rho bf16 [n,L,H,16])."""
+    lib = load_library()
+    _check_cuda(d_ch, q, coords, spans)
+    L, H, N, d = q.shape
+    n = spans.shape[0]
+    if coords.dtype != torch.int32 or spans.dtype != torch.int64 or not coords.is_contiguous() or not spans.is_contiguous():
+        raise ValueError("coords must be contiguous int32 and spans contiguous int64")
+    t_star = torch.empty((n, L, H), dtype=torch.int32, device=q.device)
+    rho = torch.empty((n, L, H, NOTE_ADDR_DIMS), dtype=torch.bfloat16, device=q.device)
+    a = NotebankAddressArgs(L, H, N, d, n, _dtype_code(q.dtype), _view4(q), _ptr(d_ch), _ptr(coords), _ptr(spans),
+                            _ptr(t_star), _ptr(rho))
+    st = lib.la_notebank_address(ctypes.byref(a), _stream_handle(stream))
+    if st != LA_OK:
+        raise LAError(st, "la_notebank_address")
+    return t_star, rho
+
+
+def la_notebank_route(rho, u, R: int, positions=None, want_scores: bool = False, stream=None):
+    """NoteBank routing (Eq. (5)).  rho bf16 [n, J, 16] (notes in insertion
+    order), u bf16 [J, n_q, 16] (question features), positions int64 [n] or
+    None.  Returns (top int32 [R] in text order, -1 padded, winner int32 [J],
+    votes int32 [n], s fp32 [n, J] or None)."""
+    lib = load_library()
+    _check_cuda(rho, u, positions)
+    n, J = rho.shape[0], u.shape[0]
+    for name, t in (("rho", rho), ("u", u)):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor")
+    dev = u.device
+    winner = torch.empty((J,), dtype=torch.int32, device=dev)
+    votes = torch.empty((n,), dtype=torch.int32, device=dev)
+    top = torch.empty((R,), dtype=torch.int32, device=dev)
+    s = torch.empty((n, J), dtype=torch.float32, device=dev) if want_scores else None
+    a = NotebankRouteArgs(n, J, u.shape[1], int(R), _ptr(rho), _ptr(u), _ptr(positions), _ptr(s), _ptr(winner),
+                          _ptr(votes), _ptr(top))
+    st = lib.la_notebank_route(ctypes.byref(a), _stream_handle(stream))
+    if st != LA_OK:
+        raise LAError(st, "la_notebank_route")
+    return top, winner, votes, s
 
 
 def la_device_status(stream=None, clear: bool = True) -> int:

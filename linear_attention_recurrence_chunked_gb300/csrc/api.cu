@@ -311,6 +311,74 @@ la_status la_swa_decode_step(const la_swa_decode_args* a, void* stream) {
   return from_cuda(la::launch_swa_decode(L, static_cast<cudaStream_t>(stream)));
 }
 
+la_status la_notebank_scores(const la_notebank_scores_args* a, void* stream) {
+  if (!a) return LA_ERR_INVALID_ARGUMENT;
+  if (a->L < 0 || a->H < 0 || a->N < 0 || a->L > kMaxDim || a->H > kMaxDim || a->N > kMaxDim)
+    return LA_ERR_INVALID_ARGUMENT;
+  if (!valid_dtype(a->in_dtype)) return LA_ERR_INVALID_ARGUMENT;
+  if (a->d < 32 || a->d > 256 || a->d % 32 != 0) return LA_ERR_UNSUPPORTED;
+  if (a->chunk < 1 || a->chunk > 1024 || a->window < 1 || a->window > 4096) return LA_ERR_INVALID_ARGUMENT;
+  const int64_t J = a->L * a->H;
+  if (J == 0 || a->N == 0) return LA_OK;
+  if (J * ((a->N + a->chunk - 1) / a->chunk) > (int64_t(1) << 31) - 1) return LA_ERR_UNSUPPORTED;
+  if (!valid_view(a->k, a->L, a->H, a->N, a->d, a->in_dtype)) return LA_ERR_INVALID_ARGUMENT;
+  if (!a->d_ch || !a->d_mean || (reinterpret_cast<uintptr_t>(a->d_ch) & 3u) ||
+      (reinterpret_cast<uintptr_t>(a->d_mean) & 3u) || (reinterpret_cast<uintptr_t>(a->w) & 3u))
+    return LA_ERR_INVALID_ARGUMENT;
+  la::NotebankScoresLaunch L{};
+  L.L = a->L; L.H = a->H; L.N = a->N; L.d = a->d;
+  L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
+  L.k = view(a->k);
+  L.chunk = a->chunk; L.window = a->window;
+  L.d_ch = a->d_ch; L.d_mean = a->d_mean; L.w = a->N >= a->window ? a->w : nullptr;
+  return from_cuda(la::launch_notebank_scores(L, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_notebank_address(const la_notebank_address_args* a, void* stream) {
+  if (!a) return LA_ERR_INVALID_ARGUMENT;
+  if (a->L < 0 || a->H < 0 || a->N < 0 || a->n_notes < 0 || a->L > kMaxDim || a->H > kMaxDim || a->N > kMaxDim ||
+      a->n_notes > kMaxDim)
+    return LA_ERR_INVALID_ARGUMENT;
+  if (!valid_dtype(a->in_dtype)) return LA_ERR_INVALID_ARGUMENT;
+  if (a->d < la::kNoteAddrDims || a->d > kMaxDim) return LA_ERR_UNSUPPORTED;
+  const int64_t warps = a->n_notes * a->L * a->H;
+  if (warps == 0) return LA_OK;
+  if (warps > (int64_t(1) << 33)) return LA_ERR_UNSUPPORTED;  // grid of warps * 32 / 256 blocks
+  if (a->N == 0) return LA_ERR_INVALID_ARGUMENT;  // no token to point at
+  if (!valid_view(a->q, a->L, a->H, a->N, a->d, a->in_dtype)) return LA_ERR_INVALID_ARGUMENT;
+  if (!a->d_ch || !a->coords || !a->spans || !a->t_star || !a->rho || (reinterpret_cast<uintptr_t>(a->d_ch) & 3u) ||
+      (reinterpret_cast<uintptr_t>(a->coords) & 3u) || (reinterpret_cast<uintptr_t>(a->spans) & 7u) ||
+      (reinterpret_cast<uintptr_t>(a->t_star) & 3u) || (reinterpret_cast<uintptr_t>(a->rho) & 1u))
+    return LA_ERR_INVALID_ARGUMENT;
+  unsigned* status = device_status_ptr();
+  if (!status) return LA_ERR_CUDA;
+  la::NotebankAddressLaunch L{};
+  L.L = a->L; L.H = a->H; L.N = a->N; L.d = a->d; L.n_notes = a->n_notes;
+  L.in_bf16 = a->in_dtype == LA_DTYPE_BF16;
+  L.q = view(a->q);
+  L.d_ch = a->d_ch; L.coords = a->coords; L.spans = a->spans; L.t_star = a->t_star; L.rho = a->rho;
+  return from_cuda(la::launch_notebank_address(L, status, static_cast<cudaStream_t>(stream)));
+}
+
+la_status la_notebank_route(const la_notebank_route_args* a, void* stream) {
+  if (!a) return LA_ERR_INVALID_ARGUMENT;
+  if (a->n_notes < 0 || a->J < 0 || a->n_notes > (int64_t(1) << 31) - 2 || a->J > kMaxDim)
+    return LA_ERR_INVALID_ARGUMENT;
+  if (a->n_q < 1 || a->n_q > 512 || a->R < 1 || a->R > 64) return LA_ERR_UNSUPPORTED;
+  if (a->J == 0) return LA_OK;
+  if (!a->u || !a->winner || !a->top || !aligned16(a->u) || (reinterpret_cast<uintptr_t>(a->winner) & 3u) ||
+      (reinterpret_cast<uintptr_t>(a->top) & 3u))
+    return LA_ERR_INVALID_ARGUMENT;
+  if (a->n_notes > 0 && (!a->rho || !a->votes || !aligned16(a->rho) || (reinterpret_cast<uintptr_t>(a->votes) & 3u) ||
+                         (reinterpret_cast<uintptr_t>(a->s) & 3u) || (reinterpret_cast<uintptr_t>(a->positions) & 7u)))
+    return LA_ERR_INVALID_ARGUMENT;
+  la::NotebankRouteLaunch L{};
+  L.n_notes = a->n_notes; L.J = a->J; L.n_q = a->n_q; L.R = a->R;
+  L.rho = a->rho; L.u = a->u; L.positions = a->positions; L.s = a->s;
+  L.winner = a->winner; L.votes = a->votes; L.top = a->top;
+  return from_cuda(la::launch_notebank_route(L, static_cast<cudaStream_t>(stream)));
+}
+
 la_status la_selftest_bounded_wait(int arrive, int64_t limit_ns, void* stream) {
   if (limit_ns < 1000000 || limit_ns > 2000000000) return LA_ERR_INVALID_ARGUMENT;
   unsigned* status = device_status_ptr();

@@ -102,4 +102,39 @@ cudaError_t launch_state_gather(float* dst, const float* src, const int64_t* ind
                                 int64_t per, unsigned* dev_status, cudaStream_t stream);
 cudaError_t launch_bounded_wait_selftest(int arrive, uint64_t limit_ns, unsigned* dev_status, cudaStream_t stream);
 
+// NoteBank write side and routing (notebank.cu).
+constexpr int kNoteAddrDims = 16;  // d_rho: query coordinates stored per channel and note
+struct NotebankScoresLaunch {
+  int64_t L, H, N, d;   // channels = L x H; key width d (multiple of 32, <= 256)
+  bool in_bf16;
+  View4 k;              // [L, H, N, d]
+  int64_t chunk, window;
+  float* d_ch;          // [L, H, N]
+  float* d_mean;        // [N]
+  float* w;             // [N - window + 1] or null
+};
+struct NotebankAddressLaunch {
+  int64_t L, H, N, d, n_notes;
+  bool in_bf16;
+  View4 q;                // [L, H, N, d]
+  const float* d_ch;      // [L, H, N]
+  const int32_t* coords;  // [L, H, 16]
+  const int64_t* spans;   // [n_notes, 2]: start, length
+  int32_t* t_star;        // [n_notes, L, H]
+  void* rho;              // [n_notes, L, H, 16] bf16
+};
+struct NotebankRouteLaunch {
+  int64_t n_notes, J, n_q, R;
+  const void* rho;           // [n_notes, J, 16] bf16
+  const void* u;             // [J, n_q, 16] bf16
+  const int64_t* positions;  // [n_notes] or null
+  float* s;                  // [n_notes, J] or null
+  int32_t* winner;           // [J]
+  int32_t* votes;            // [n_notes]
+  int32_t* top;              // [R]
+};
+cudaError_t launch_notebank_scores(const NotebankScoresLaunch& a, cudaStream_t stream);
+cudaError_t launch_notebank_address(const NotebankAddressLaunch& a, unsigned* status, cudaStream_t stream);
+cudaError_t launch_notebank_route(const NotebankRouteLaunch& a, cudaStream_t stream);
+
 }  // namespace la

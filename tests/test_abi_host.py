@@ -215,3 +215,40 @@ def test_swa_decode_rejections(lib):
     assert call(mk(q=0x10008)) == la.LA_ERR_INVALID_ARGUMENT  # misaligned
     assert call(mk(pos=0x60004)) == la.LA_ERR_INVALID_ARGUMENT
     assert call(mk(S=0)) == la.LA_OK
+
+
+def test_notebank_rejections(lib):
+    def scores(**kw):
+        L, H, N, d = kw.get("L", 2), kw.get("H", 2), kw.get("N", 100), kw.get("d", 128)
+        a = la.NotebankScoresArgs(L, H, N, d, la.LA_DTYPE_BF16, _tensor(0x100000, H * N * d, N * d, d),
+                                  kw.get("chunk", 64), kw.get("window", 48), kw.get("d_ch", 0x200000), 0x300000,
+                                  0x400000)
+        return lib.la_notebank_scores(ctypes.byref(a), None)
+    assert lib.la_notebank_scores(None, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert scores(d=48) == la.LA_ERR_UNSUPPORTED
+    assert scores(d=512) == la.LA_ERR_UNSUPPORTED
+    assert scores(chunk=0) == la.LA_ERR_INVALID_ARGUMENT and scores(chunk=2048) == la.LA_ERR_INVALID_ARGUMENT
+    assert scores(window=0) == la.LA_ERR_INVALID_ARGUMENT
+    assert scores(d_ch=0x200002) == la.LA_ERR_INVALID_ARGUMENT
+    assert scores(L=0) == la.LA_OK and scores(N=0) == la.LA_OK
+
+    def address(**kw):
+        L, H, N, d = 2, 2, kw.get("N", 100), kw.get("d", 128)
+        a = la.NotebankAddressArgs(L, H, N, d, kw.get("n", 3), la.LA_DTYPE_BF16, _tensor(0x100000, H * N * d, N * d, d),
+                                   0x200000, 0x300000, kw.get("spans", 0x400000), 0x500000, 0x600000)
+        return lib.la_notebank_address(ctypes.byref(a), None)
+    assert lib.la_notebank_address(None, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert address(d=8) == la.LA_ERR_UNSUPPORTED
+    assert address(spans=0x400004) == la.LA_ERR_INVALID_ARGUMENT
+    assert address(N=0) == la.LA_ERR_INVALID_ARGUMENT
+    assert address(n=0) == la.LA_OK
+
+    def route(**kw):
+        a = la.NotebankRouteArgs(kw.get("n", 10), kw.get("J", 4), kw.get("nq", 5), kw.get("R", 2), 0x100000,
+                                 kw.get("u", 0x200000), None, None, 0x300000, 0x400000, 0x500000)
+        return lib.la_notebank_route(ctypes.byref(a), None)
+    assert lib.la_notebank_route(None, None) == la.LA_ERR_INVALID_ARGUMENT
+    assert route(nq=0) == la.LA_ERR_UNSUPPORTED and route(nq=513) == la.LA_ERR_UNSUPPORTED
+    assert route(R=0) == la.LA_ERR_UNSUPPORTED
+    assert route(u=0x200008) == la.LA_ERR_INVALID_ARGUMENT
+    assert route(J=0) == la.LA_OK
