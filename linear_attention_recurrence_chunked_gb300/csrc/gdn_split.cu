@@ -294,10 +294,11 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
     mbar_init(smem_u32(&bar_s), 1);
     mbar_init(smem_u32(&bar_o[0]), 1);
     mbar_init(smem_u32(&bar_o[1]), 1);
-    mbar_init(smem_u32(&bar_ofree[0]), kOutThreads / 32);  // one arrival per warp
-    mbar_init(smem_u32(&bar_ofree[1]), kOutThreads / 32);
-    mbar_init(smem_u32(&bar_s0), kChainThreads / 32);
-    mbar_init(smem_u32(&bar_u), kChainThreads / 32);
+    // one arrival per thread: measured slightly faster here than one per warp after __syncwarp
+    mbar_init(smem_u32(&bar_ofree[0]), kOutThreads);
+    mbar_init(smem_u32(&bar_ofree[1]), kOutThreads);
+    mbar_init(smem_u32(&bar_s0), kChainThreads);
+    mbar_init(smem_u32(&bar_u), kChainThreads);
     mbar_init(smem_u32(&bar_fin), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmap_k);
@@ -441,7 +442,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
     }
     fence_proxy_async_smem();
     tc_fence_before();
-    warp_arrive(smem_u32(&bar_s0));
+    mbar_arrive(smem_u32(&bar_s0));
     float sigma = 1.f;
     // An expired wait leaves this thread's `ok` false: it skips its later waits (so it meets at most one
     // expiry) but still makes every arrival, so no warp waits on it, and the final state is not written.
@@ -488,7 +489,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      warp_arrive(smem_u32(&bar_u));
+      mbar_arrive(smem_u32(&bar_u));
       ok = ok && wait(&bar_s, par);
       tc_fence_after();
 
@@ -522,7 +523,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
       if (has_next) {
         fence_proxy_async_smem();
         tc_fence_before();
-        warp_arrive(smem_u32(&bar_s0));
+        mbar_arrive(smem_u32(&bar_s0));
       }
     }
 
@@ -557,7 +558,7 @@ gdn_chain_kernel(const __grid_constant__ CUtensorMap tmap_k, const GdnPrefillLau
         tmem_ld16(tlane + kCColO + 64 * par + c0, *reinterpret_cast<float(*)[16]>(o + c0));
       tmem_ld_wait();
       tc_fence_before();
-      warp_arrive(smem_u32(&bar_ofree[par]));  // the buffer may be overwritten from here on
+      mbar_arrive(smem_u32(&bar_ofree[par]));  // the buffer may be overwritten from here on
       const int64_t t0 = wk.t_begin + (int64_t)c * kC;
       const int nvalid = (wk.t_end - t0 < kC) ? (int)(wk.t_end - t0) : kC;
       TOut* optr = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + t0 * a.o_st + row;
