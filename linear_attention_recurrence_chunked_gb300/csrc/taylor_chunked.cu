@@ -218,18 +218,41 @@ __device__ __forceinline__ void unpack8_bf16(const uint4 u, float* x) {
   }
 }
 
+// 32 bytes to global memory in one instruction (one full sector); dst 32-byte aligned.
+__device__ __forceinline__ void st_global_32b(void* dst, uint4 a, uint4 b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 as_u4(float x, float y, float z, float w) {
+  return make_uint4(__float_as_uint(x), __float_as_uint(y), __float_as_uint(z), __float_as_uint(w));
+}
+// 32 output values of a row: whole 32-byte sectors when the row segment is 32-byte aligned (each
+// warp-wide store then fills 32 sectors instead of half-filling them), else 16-byte vectors.
 template <typename T>
-__device__ __forceinline__ void store_row32(T* dst, const float* v);
+__device__ __forceinline__ void store_row32(T* dst, const float* v, bool al32);
 template <>
-__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
+__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, const float* v, bool al32) {
+  if (al32) {
+    st_global_32b(dst, pack8_bf16(v), pack8_bf16(v + 8));
+    st_global_32b(dst + 16, pack8_bf16(v + 16), pack8_bf16(v + 24));
+  } else {
 #pragma unroll
-  for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(dst)[q] = pack8_bf16(v + 8 * q);
+    for (int q = 0; q < 4; ++q) reinterpret_cast<uint4*>(dst)[q] = pack8_bf16(v + 8 * q);
+  }
 }
 template <>
-__device__ __forceinline__ void store_row32<float>(float* dst, const float* v) {
+__device__ __forceinline__ void store_row32<float>(float* dst, const float* v, bool al32) {
+  if (al32) {
 #pragma unroll
-  for (int q = 0; q < 8; ++q)
-    reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    for (int q = 0; q < 4; ++q)
+      st_global_32b(dst + 8 * q, as_u4(v[8 * q], v[8 * q + 1], v[8 * q + 2], v[8 * q + 3]),
+                    as_u4(v[8 * q + 4], v[8 * q + 5], v[8 * q + 6], v[8 * q + 7]));
+  } else {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      reinterpret_cast<float4*>(dst)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
 }
 
 template <typename TOut, bool DECAY>
@@ -262,6 +285,8 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   const int my_feature = half == 0 ? row : f1;
   const uint32_t my_colc = half == 0 ? kColC0 : kColC1;
   auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(smem_u32(bar), parity, status); };
+  // every 32-value output segment starts on a 32-byte boundary (base and strides allow it)
+  const bool y_al32 = ((reinterpret_cast<uintptr_t>(a.y) | (uintptr_t)((a.y_sb | a.y_sh | a.y_st) * sizeof(TOut))) & 31u) == 0;
   // per-head retention: lambda^e for e >= 0 (lambda^0 = 1 also for lambda = 0)
   const float lam = DECAY ? a.decay[h] : 1.f;
   const float l2lam = DECAY ? log2f(lam) : 0.f;
@@ -526,7 +551,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
 #pragma unroll
         for (int j = 0; j < 32; ++j) y[j] *= inv;
         TOut* yrow = reinterpret_cast<TOut*>(a.y) + b * a.y_sb + h * a.y_sh + t * a.y_st + 32 * half;
-        store_row32<TOut>(yrow, y);
+        store_row32<TOut>(yrow, y, y_al32);
       }
     };
     // bf16 c and z tiles for the next readout from the tensor-memory state (warp-collective loads)

@@ -128,3 +128,18 @@ def test_based_prefill_full_size():
     assert rel_err(to_np(s), ref["s"]) < tol
     assert rel_err(to_np(z), ref["z"]) < tol
     assert la.la_device_status() == la.LA_OK
+
+
+def test_taylor_output_on_16_byte_boundary():
+    """y starting 16 bytes past a 32-byte boundary (rows of 80 bf16): the
+    kernel falls back from 32-byte to 16-byte stores; results unchanged."""
+    dev = cuda_device()
+    inp = synthetic.taylor_inputs(1, 2, 300, dtype=torch.bfloat16, seed=41)
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    buf = torch.zeros((1, 2, 300, 80), dtype=torch.bfloat16, device=dev)
+    y = buf[..., 8:72]
+    _, s, z = la.la_based_prefill(q, k, v, y=y)
+    y_ref, s_ref, z_ref = la.la_based_prefill(q, k, v)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_ref) and torch.equal(s, s_ref) and torch.equal(z, z_ref)
+    assert torch.count_nonzero(buf[..., :8]).item() == 0 and torch.count_nonzero(buf[..., 72:]).item() == 0
