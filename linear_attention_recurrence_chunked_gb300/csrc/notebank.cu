@@ -22,11 +22,15 @@
 // per channel over all notes plus one CTA for the vote.
 #include <math.h>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace la {
 namespace {
+namespace cg = cooperative_groups;
 
 constexpr int kScoreThreads = 256;
 constexpr int kMaxD = 256;               // key / query width, multiple of 32
@@ -111,6 +115,117 @@ notebank_chunk_scores_kernel(NotebankScoresLaunch a) {
     for (int i = 0; i < PER; ++i) dt = fmaf(x[i], mv[i], dt);
     dt = warp_sum(dt);
     if (lane == 0) out[r] = 1.f - dt * inv_norm[r];
+  }
+}
+
+// The same scores with each chunk split over a cluster of kClusterCtas CTAs
+// that keep their share of the chunk's keys in shared memory: the keys are
+// read from HBM once.  Each CTA sums its unit keys; after a cluster barrier
+// every CTA adds the kClusterCtas partial sums (in rank order, so all get the
+// same bits) through distributed shared memory; a second barrier keeps every
+// CTA's partial alive until all have read it.
+constexpr int kClusterCtas = 4;
+
+template <typename T, int PER>
+__global__ void __cluster_dims__(kClusterCtas, 1, 1) __launch_bounds__(kScoreThreads)
+notebank_chunk_scores_cluster_kernel(NotebankScoresLaunch a, int sub) {
+  extern __shared__ __align__(16) uint8_t nb_smem[];
+  T* rows = reinterpret_cast<T*>(nb_smem);                       // [sub][d]
+  float* inv_norm = reinterpret_cast<float*>(rows + (int64_t)sub * a.d);  // [sub]
+  __shared__ float part[kScoreThreads / 32][kMaxD];
+  __shared__ float cpart[kMaxD];  // this CTA's sum of unit keys, read by the whole cluster
+  __shared__ float mu[kMaxD];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = (int)cluster.block_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kWarps = kScoreThreads / 32;
+  const int d = (int)a.d;
+  const int64_t nchunks = (a.N + a.chunk - 1) / a.chunk;
+  const int64_t item = blockIdx.x / kClusterCtas;
+  const int64_t ch = item / nchunks, c = item % nchunks;
+  const int64_t l = ch / a.H, h = ch % a.H;
+  const int64_t t0 = c * a.chunk;
+  const int n = (int)min((int64_t)a.chunk, a.N - t0);
+  const int r0 = rank * sub, r1 = min(n, r0 + sub);  // this CTA's rows of the chunk
+  const T* base = reinterpret_cast<const T*>(a.k.ptr) + l * a.k.sb + h * a.k.sh;
+
+  // this CTA's rows into shared memory, all requested at once (16-byte copies; the views are
+  // 16-byte aligned with rows of d * sizeof(T), a multiple of 64 bytes)
+  {
+    const int vrow = d * (int)sizeof(T) / 16;
+    const int nv = max(r1 - r0, 0) * vrow;
+    const uint32_t sdst = tc::smem_u32(nb_smem);
+    for (int v = threadIdx.x; v < nv; v += kScoreThreads) {
+      const int rr = v / vrow, cv = v - rr * vrow;
+      tc::cp_async16(sdst + (uint32_t)(rr * vrow + cv) * 16u,
+                     reinterpret_cast<const uint8_t*>(base + (t0 + r0 + rr) * a.k.st) + cv * 16, 16u);
+    }
+    tc::cp_async_commit();
+    tc::cp_async_wait_all();
+    __syncthreads();
+  }
+  // pass 1: inverse norms and the sum of unit keys
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  for (int r = r0 + warp; r < r1; r += kWarps) {
+    const T* src = rows + (int64_t)(r - r0) * d;
+    float x[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) x[i] = to_f(src[lane + 32 * i]);
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) ss = fmaf(x[i], x[i], ss);
+    ss = warp_sum(ss);
+    const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;  // a zero key normalises to zero
+#pragma unroll
+    for (int i = 0; i < PER; ++i) acc[i] = fmaf(x[i], inv, acc[i]);
+    if (lane == 0) inv_norm[r - r0] = inv;
+  }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) part[warp][lane + 32 * i] = acc[i];
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) s += part[w][lane + 32 * i];
+      cpart[lane + 32 * i] = s;
+    }
+  }
+  cluster.sync();
+  // mean direction of the whole chunk, normalised (the 1/|C| of the mean cancels)
+  if (warp == 0) {
+    float m[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) m[i] = 0.f;
+    for (int q = 0; q < kClusterCtas; ++q) {
+      const float* rp = cluster.map_shared_rank(cpart, q);
+#pragma unroll
+      for (int i = 0; i < PER; ++i) m[i] += rp[lane + 32 * i];
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) ss = fmaf(m[i], m[i], ss);
+    ss = warp_sum(ss);
+    const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) mu[lane + 32 * i] = m[i] * inv;
+  }
+  cluster.sync();  // every partial has been read; mu is visible to the whole CTA
+  float mv[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) mv[i] = mu[lane + 32 * i];
+  // pass 2 from shared memory: d_t = 1 - <k_t, mu> / |k_t|
+  float* out = a.d_ch + ch * a.N + t0;
+  for (int r = r0 + warp; r < r1; r += kWarps) {
+    const T* src = rows + (int64_t)(r - r0) * d;
+    float dt = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) dt = fmaf(to_f(src[lane + 32 * i]), mv[i], dt);
+    dt = warp_sum(dt);
+    if (lane == 0) out[r] = 1.f - dt * inv_norm[r - r0];
   }
 }
 
@@ -317,21 +432,38 @@ notebank_vote_kernel(NotebankRouteLaunch a) {
   }
 }
 
-template <typename T>
-cudaError_t launch_scores_typed(const NotebankScoresLaunch& a, cudaStream_t stream) {
+constexpr size_t kClusterSmemMax = 160 * 1024;  // keys of a cluster's share of a chunk, plus norms
+
+template <typename T, int PER>
+cudaError_t launch_scores_pd(const NotebankScoresLaunch& a, cudaStream_t stream) {
   const int64_t nchunks = (a.N + a.chunk - 1) / a.chunk;
-  const unsigned grid = (unsigned)(a.L * a.H * nchunks);
-  switch (a.d / 32) {
-    case 1: notebank_chunk_scores_kernel<T, 1><<<grid, kScoreThreads, 0, stream>>>(a); break;
-    case 2: notebank_chunk_scores_kernel<T, 2><<<grid, kScoreThreads, 0, stream>>>(a); break;
-    case 3: notebank_chunk_scores_kernel<T, 3><<<grid, kScoreThreads, 0, stream>>>(a); break;
-    case 4: notebank_chunk_scores_kernel<T, 4><<<grid, kScoreThreads, 0, stream>>>(a); break;
-    case 5: notebank_chunk_scores_kernel<T, 5><<<grid, kScoreThreads, 0, stream>>>(a); break;
-    case 6: notebank_chunk_scores_kernel<T, 6><<<grid, kScoreThreads, 0, stream>>>(a); break;
-    case 7: notebank_chunk_scores_kernel<T, 7><<<grid, kScoreThreads, 0, stream>>>(a); break;
-    default: notebank_chunk_scores_kernel<T, 8><<<grid, kScoreThreads, 0, stream>>>(a); break;
+  const int64_t items = a.L * a.H * nchunks;
+  const int sub = (int)((a.chunk + kClusterCtas - 1) / kClusterCtas);
+  const size_t smem = (size_t)sub * (size_t)a.d * sizeof(T) + (size_t)sub * sizeof(float);
+  if (smem <= kClusterSmemMax && items * kClusterCtas <= (int64_t)INT32_MAX) {
+    static cudaError_t attr = cudaFuncSetAttribute(notebank_chunk_scores_cluster_kernel<T, PER>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kClusterSmemMax);
+    if (attr != cudaSuccess) return attr;
+    notebank_chunk_scores_cluster_kernel<T, PER>
+        <<<(unsigned)(items * kClusterCtas), kScoreThreads, smem, stream>>>(a, sub);
+  } else {  // the share of a chunk does not fit: two passes over global memory
+    notebank_chunk_scores_kernel<T, PER><<<(unsigned)items, kScoreThreads, 0, stream>>>(a);
   }
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_scores_typed(const NotebankScoresLaunch& a, cudaStream_t stream) {
+  switch (a.d / 32) {
+    case 1: return launch_scores_pd<T, 1>(a, stream);
+    case 2: return launch_scores_pd<T, 2>(a, stream);
+    case 3: return launch_scores_pd<T, 3>(a, stream);
+    case 4: return launch_scores_pd<T, 4>(a, stream);
+    case 5: return launch_scores_pd<T, 5>(a, stream);
+    case 6: return launch_scores_pd<T, 6>(a, stream);
+    case 7: return launch_scores_pd<T, 7>(a, stream);
+    default: return launch_scores_pd<T, 8>(a, stream);
+  }
 }
 
 }  // namespace
