@@ -30,13 +30,14 @@
 // One CTA per (batch, head), two threads per token row of a 128-token chunk
 // (each takes half of the row's columns and features).  V tiles arrive by TMA
 // (two stages); q and k rows by cp.async, issued a chunk ahead, from which the
-// features are formed in registers.  Tensor-memory state: [c | z] for
-// features 0..127 as an M = 128 accumulator and for features 128..191 as an
-// M = 64 accumulator.  The normaliser runs through the tensor cores with the
-// state: the B operand is [V | 1] (a constant block whose first column is
-// ones), so z += Phi_K^T 1 lands in column 64 of the state accumulators and
-// the row sums of P in column 64 of the numerator; a tile whose first row
-// is z supplies Phi_Q z.
+// features are formed in registers.  The state lives transposed in tensor
+// memory as one M = 128 accumulator of 160 feature columns, [c^T ; z^T ; 0]:
+// lanes 0..63 hold c^T (lane = value column), lane 64 holds z.  Its update
+// [c^T ; z^T] += [V | 1]^T Phi_K is 8 MMAs of N = 160 whose A operand is the
+// V tile next to a constant block with a first column of ones (the ones row
+// accumulates z).  The readout Phi_Q [c | z] is 10 MMAs of N = 80 against a
+// bf16 copy of lanes 0..64, K-major with rows 65..79 zero, which puts Phi_Q z
+// in column 64 of the numerator; P [V | 1] adds the row sums of P there.
 #include <mutex>
 
 #include "common.cuh"
@@ -65,15 +66,17 @@ constexpr uint32_t kOffQK = kOffOnes + 16384;      // bf16 [128 tokens][64]: q, 
 constexpr uint32_t kOffPhiQ = kOffQK + 16384;      // bf16 [128 tokens][192] (3 blocks of 16 KB)
 constexpr uint32_t kOffPhiK = kOffPhiQ + 49152;    // bf16 [128 tokens][192]
 constexpr uint32_t kOffP = kOffPhiK + 49152;       // bf16 [128 r][128 j] (2 blocks of 16 KB)
-constexpr uint32_t kOffCt = kOffP + 32768;         // bf16 c [192 features][64 v] (24 KB)
-constexpr uint32_t kOffZt = kOffCt + 24576;        // bf16 [16][192 features], row 0 = z (6 KB)
-constexpr uint32_t kSmemUsed = kOffZt + 6144;
+constexpr uint32_t kOffCt = kOffP + 32768;         // bf16 [c^T ; z^T ; 0] [80 rows][192 features], K-major:
+constexpr uint32_t kCtRows = 80;                   //   3 blocks of [80][64] (10 KB each)
+constexpr uint32_t kCtBlock = kCtRows * 128;
+constexpr uint32_t kSmemUsed = kOffCt + 3 * kCtBlock;
+constexpr int kStageLd = kDv + 1;                  // [160][65] fp32 staging of the state (init, final),
+static_assert(kDc * kStageLd * 4 <= 49152, "");    //   in the Phi_Q tile while that is unused
 constexpr uint32_t kSmemAlloc = kSmemUsed + 1024;
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
-// tensor memory columns; N = 80 accumulators: columns 0..63 = v, column 64 = the "1" column
-constexpr uint32_t kColC0 = 0;     // [c | z], features 0..127 (M = 128: lane = feature)
-constexpr uint32_t kColC1 = 96;    // [c | z], features 128..191 (M = 64 layout)
+// tensor memory columns
+constexpr uint32_t kColS = 0;      // [c^T ; z^T ; 0]: lane = value column (64 = z), column = compact feature (160)
 constexpr uint32_t kColAcc = 192;  // 2 x [numerator | denominator] per token (80 columns each), by chunk parity
 constexpr uint32_t kColQK = 384;   // Q K^T [r][j], 128 cols
 constexpr uint32_t kTmemCols = 512;
@@ -200,14 +203,6 @@ __device__ __forceinline__ int full_rows_of(int j, int& r0, int& r1, float& scal
   return 2;
 }
 
-// Features 0..127 live in the M = 128 accumulator (lane = feature);
-// features 128..191 in the M = 64 accumulator, whose row m sits in lane
-// (m % 16) + 32 (m / 16).  Inverse map for the latter (-1: lane unused).
-__device__ __forceinline__ int feature_of_lane(int lane) {
-  const int q = lane >> 5, w = lane & 31;
-  return w < 16 ? 128 + q * 16 + w : -1;
-}
-
 // Eight bf16 values of a 16-byte vector as floats.
 __device__ __forceinline__ void unpack8_bf16(const uint4 u, float* x) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -267,6 +262,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   __shared__ uint64_t bar_qkin;    // workers: this chunk's q, k rows are in the QK tile
   __shared__ uint64_t bar_feat;    // workers: Phi_Q, Phi_K written and the c / z tiles refreshed (next readout)
   __shared__ uint64_t bar_p;       // workers: P written
+  __shared__ uint64_t bar_accfree[2];  // workers: outputs of the chunk two back read its accumulator, by parity
   __shared__ uint64_t bar_fin;     // drain after an expired wait
   __shared__ uint32_t tmem_base_sh;
 
@@ -281,9 +277,9 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   const uint32_t sbase = smem_u32(sm);
   const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(a.q.ptr) + b * a.q.sb + h * a.q.sh;
   const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(a.k.ptr) + b * a.k.sb + h * a.k.sh;
-  const int f1 = feature_of_lane(row);  // feature of this lane in the M = 64 accumulator
-  const int my_feature = half == 0 ? row : f1;
-  const uint32_t my_colc = half == 0 ? kColC0 : kColC1;
+  // state role: lane `row` of the transposed state (value column `row`, z for row 64), compact features
+  // [80 half, 80 half + 80); warps 3 and 7 hold only lanes above 64
+  const bool state_warp = (warp & 3) <= 2;
   auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(smem_u32(bar), parity, status); };
   // every 32-value output segment starts on a 32-byte boundary (base and strides allow it)
   const bool y_al32 = ((reinterpret_cast<uintptr_t>(a.y) | (uintptr_t)((a.y_sb | a.y_sh | a.y_st) * sizeof(TOut))) & 31u) == 0;
@@ -303,6 +299,8 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     mbar_init(smem_u32(&bar_qkin), 1);               // one arrival after the workers' named barrier
     mbar_init(smem_u32(&bar_feat), kWorkers / 32);   // one arrival per worker warp
     mbar_init(smem_u32(&bar_p), kWorkers / 32);
+    mbar_init(smem_u32(&bar_accfree[0]), kWorkers / 32);
+    mbar_init(smem_u32(&bar_accfree[1]), kWorkers / 32);
     mbar_init(smem_u32(&bar_fin), 1);
     fence_mbar_init();
     tma_prefetch_desc(&tmap_v);
@@ -313,7 +311,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   }
   // ---- constant tiles: [.. | 1] block (column 0 = 1) and the z tile, zeroed first
   for (int i = tid; i < 16384 / 16; i += kBlock) reinterpret_cast<uint4*>(sm + kOffOnes)[i] = make_uint4(0, 0, 0, 0);
-  for (int i = tid; i < 6144 / 16; i += kBlock) reinterpret_cast<uint4*>(sm + kOffZt)[i] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < (int)(3 * kCtBlock / 16); i += kBlock) reinterpret_cast<uint4*>(sm + kOffCt)[i] = make_uint4(0, 0, 0, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -365,21 +363,29 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       const uint32_t lbo = sbase + kOffOnes - vt;  // distance from the V block to the [.. | 1] block
       const uint32_t acc = tmem + kColAcc + par * 80u;
       if (leader) {
-        const uint32_t id = idesc_bf16(128, 64, 0, 1);
-        const uint32_t idz = idesc_bf16(128, 16, 0, 0);
+        // state update: [c^T ; z^T] += [V | 1]^T Phi_K (A: the V block and the [.. | 1] block, value-major;
+        // B: Phi_K, feature-major, N = 160)
+        const uint32_t idu = idesc_bf16(128, kDc, 1, 1);
+#pragma unroll
+        for (int ks = 0; ks < kC / 16; ++ks)
+          mma_bf16(tmem + kColS, sw128_desc(vt + ks * 2048, lbo, 1024),
+                   sw128_desc(sbase + kOffPhiK + ks * 2048, 16384, 1024), idu, 1u);
+      }
+      __syncwarp();
+      // the readout accumulates into this parity's numerator, which the outputs of chunk c - 2 read
+      if (c >= 2) {
+        ok = iwait(&bar_accfree[par], (uint32_t)(((c - 2) >> 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+      }
+      if (leader) {
+        // readout: Acc = Phi_Q [c | z] (both operands K-major; the readout tile holds c^T and z as rows)
+        const uint32_t id = idesc_bf16(128, 80, 0, 0);
 #pragma unroll
         for (int ks = 0; ks < kDc / 16; ++ks) {
           const uint32_t aoff = (uint32_t)(ks >> 2) * 16384u + (uint32_t)(ks & 3) * 32u;
-          const uint32_t zoff = (uint32_t)(ks >> 2) * 2048u + (uint32_t)(ks & 3) * 32u;
-          mma_bf16(acc, kmaj(sbase + kOffPhiQ + aoff), sw128_desc(sbase + kOffCt + ks * 2048, 0, 1024), id, ks > 0);
-          mma_bf16(acc + 64, kmaj(sbase + kOffPhiQ + aoff), kmaj(sbase + kOffZt + zoff), idz, ks > 0);
-        }
-        const uint32_t id0 = idesc_bf16(128, 80, 1, 1), id1 = idesc_bf16(64, 80, 1, 1);
-#pragma unroll
-        for (int ks = 0; ks < kC / 16; ++ks) {
-          const uint64_t bv = sw128_desc(vt + ks * 2048, lbo, 1024);
-          mma_bf16(tmem + kColC0, sw128_desc(sbase + kOffPhiK + ks * 2048, 16384, 1024), bv, id0, 1u);
-          mma_bf16(tmem + kColC1, sw128_desc(sbase + kOffPhiK + 2 * 16384 + ks * 2048, 16384, 1024), bv, id1, 1u);
+          const uint32_t boff = (uint32_t)(ks >> 2) * kCtBlock + (uint32_t)(ks & 3) * 32u;
+          mma_bf16(acc, kmaj(sbase + kOffPhiQ + aoff), kmaj(sbase + kOffCt + boff), id, ks > 0);
         }
         mma_commit(smem_u32(&bar_r1));
       }
@@ -466,26 +472,40 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       const int n = full_rows_of(j, r0, r1, sc);
       return n == 2 ? (z_in[r0] + z_in[r1]) * sc : z_in[r0];
     };
+    // row `row` of the bf16 readout tile, features [f0, f0 + 16) (never across a 64-feature block)
+    auto store_ct16 = [&](int f0, const float* v) {
+      uint8_t* blk = sm + kOffCt + (uint32_t)(f0 >> 6) * kCtBlock;
+      *reinterpret_cast<uint4*>(blk + sw128_off(row, f0 & 63, kCtRows)) = pack8_bf16(v);
+      *reinterpret_cast<uint4*>(blk + sw128_off(row, (f0 & 63) + 8, kCtRows)) = pack8_bf16(v + 8);
+    };
     {
-      float v[kDv + 16];
-      compact_row(my_feature, v);
-      v[kDv] = compact_z(my_feature);
+      // incoming state, transposed through shared memory: thread j < 160 forms the compact row
+      // [c_in | z_in] of feature j; lane `row` of the transposed state then takes its 80 features
+      float* stage = reinterpret_cast<float*>(sm + kOffPhiQ);  // [160][65] fp32 until features(0)
+      if (tid < kDc) {
+        float v[kDv];
+        compact_row(tid, v);
 #pragma unroll
-      for (int i = 1; i < 16; ++i) v[kDv + i] = 0.f;
-      if (my_feature >= 0) {
+        for (int c = 0; c < kDv; ++c) stage[tid * kStageLd + c] = v[c];
+        stage[tid * kStageLd + kDv] = compact_z(tid);
+      }
+      named_bar_sync(kBarWorkers, kWorkers);
+      float v[80];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(my_feature, 8 * q, 192)) = pack8_bf16(v + 8 * q);
-        *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(v[kDv]);
+      for (int i = 0; i < 80; ++i) v[i] = row <= kDv ? stage[(80 * half + i) * kStageLd + row] : 0.f;
+      if (row <= kDv) {
+#pragma unroll
+        for (int g = 0; g < 5; ++g) store_ct16(80 * half + 16 * g, v + 16 * g);
       }
       if constexpr (DECAY) {  // chunk 0's update adds to lambda^n0 [c_in | z_in]; its readout sees c_in
         const float sc = lam_pow((float)chunk_len(0));
 #pragma unroll
-        for (int i = 0; i < kDv + 16; ++i) v[i] *= sc;
+        for (int i = 0; i < 80; ++i) v[i] *= sc;
       }
 #pragma unroll
-      for (int c = 0; c < kDv + 16; c += 16) tmem_st16(tlane + my_colc + c, *reinterpret_cast<float(*)[16]>(v + c));
+      for (int g = 0; g < 5; ++g) tmem_st16(tlane + kColS + 80 * half + 16 * g, *reinterpret_cast<float(*)[16]>(v + 16 * g));
       tmem_st_wait();
+      named_bar_sync(kBarWorkers, kWorkers);  // the staging area is Phi_Q's, written by features(0)
     }
 
     // ---- per-chunk worker passes
@@ -556,35 +576,22 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     };
     // bf16 c and z tiles for the next readout from the tensor-memory state (warp-collective loads)
     auto refresh_state_tiles = [&](float next_scale) {
-      // (with decay: the fp32 state becomes lambda^n [c | z] for the next chunk's update; the bf16 tiles
-      // keep the unscaled state for its readout)
+      // (with decay: the fp32 state becomes lambda^n [c | z] for the next chunk's update; the bf16 tile
+      // keeps the unscaled state for its readout)
+      if (!state_warp) return;
+      float v[80];
 #pragma unroll
-      for (int hv = 0; hv < 2; ++hv) {
-        float v[32];
-        tmem_ld16(tlane + my_colc + 32 * hv, *reinterpret_cast<float(*)[16]>(v));
-        tmem_ld16(tlane + my_colc + 32 * hv + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-        tmem_ld_wait();
-        if (my_feature >= 0) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<uint4*>(sm + kOffCt + sw128_off(my_feature, 32 * hv + 8 * q, 192)) = pack8_bf16(v + 8 * q);
-        }
-        if constexpr (DECAY) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= next_scale;
-          tmem_st16(tlane + my_colc + 32 * hv, *reinterpret_cast<float(*)[16]>(v));
-          tmem_st16(tlane + my_colc + 32 * hv + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-        }
-      }
-      float zz[16];
-      tmem_ld16(tlane + my_colc + kDv, zz);
+      for (int g = 0; g < 5; ++g) tmem_ld16(tlane + kColS + 80 * half + 16 * g, *reinterpret_cast<float(*)[16]>(v + 16 * g));
       tmem_ld_wait();
-      if (my_feature >= 0)
-        *reinterpret_cast<__nv_bfloat16*>(sm + kOffZt + sw128_off(0, my_feature, 16)) = __float2bfloat16_rn(zz[0]);
+      if (row <= kDv) {
+#pragma unroll
+        for (int g = 0; g < 5; ++g) store_ct16(80 * half + 16 * g, v + 16 * g);
+      }
       if constexpr (DECAY) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) zz[i] *= next_scale;
-        tmem_st16(tlane + my_colc + kDv, zz);
+        for (int i = 0; i < 80; ++i) v[i] *= next_scale;
+#pragma unroll
+        for (int g = 0; g < 5; ++g) tmem_st16(tlane + kColS + 80 * half + 16 * g, *reinterpret_cast<float(*)[16]>(v + 16 * g));
         tmem_st_wait();
       }
     };
@@ -661,12 +668,6 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         // the QK tile half of chunk c is free (Q K^T of chunk c done, every worker past its features)
         fetch_qk(c + 2);
       }
-      // ---- outputs of the previous chunk (its P [V | 1] completed long ago)
-      if (c > 0) {
-        ok = ok && wait(&bar_pv[par ^ 1u], (uint32_t)(((c - 1) >> 1) & 1));
-        tc_fence_after();
-        outputs(c - 1);
-      }
       // ---- once the readout and state update of chunk c are done: state tiles and next features
       ok = ok && wait(&bar_r1, par);
       tc_fence_after();
@@ -676,6 +677,15 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(smem_u32(&bar_feat));
+      }
+      // ---- outputs of the previous chunk, off the chain refresh -> features -> readout; then the
+      //      readout of chunk c + 1 may overwrite its accumulator
+      if (c > 0) {
+        ok = ok && wait(&bar_pv[par ^ 1u], (uint32_t)(((c - 1) >> 1) & 1));
+        tc_fence_after();
+        outputs(c - 1);
+        tc_fence_before();
+        warp_arrive(smem_u32(&bar_accfree[par ^ 1u]));
       }
     }
     if (nchunks > 0) {
@@ -688,61 +698,59 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
     cp_async_wait_all();
     ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the final-state pass below uses warp-collective loads
 
-    if (ok) {
-      // ---- final state in the 273-row basis: s_out = s_in + expand(c - c_in).
-      // Every 273-basis row belongs to exactly one compact feature, and a row of
-      // s_in / z_in is read before the same row of s_out / z_out is written, so
-      // the update may run in place (s_out == s_in).
-      float* s_out = a.s_out + bh * kDfull * kDv;
-      float* z_out = a.z_out + bh * kDfull;
-      const int j = my_feature;
-      const bool has = j >= 0 && j < kDcUsed;
-      // with decay the incoming state's share is Lambda = lambda^N of it:
-      // s_out = Lambda s_in + expand(c - Lambda c_in)
-      const float Lam = lam_pow((float)N);
-      float prev[kDv];
-      compact_row(j, prev);  // zeros when j has no full-basis rows
-      float zprev = compact_z(j);
-      if constexpr (DECAY) {
+    // all workers agree before the block-wide staging below (each thread's `ok` may differ)
+    if (!named_bar_or(kBarWorkers, kWorkers, !ok)) {
+      // ---- final state in the 273-row basis: s_out = s_in + expand(c - c_in), the state transposed back
+      // through shared memory (stage[j][v] = c[j][v], stage[j][64] = z_j).  Every 273-basis row belongs to
+      // exactly one compact feature, and a row of s_in / z_in is read before the same row of s_out / z_out
+      // is written, so the update may run in place (s_out == s_in).
+      float* stage = reinterpret_cast<float*>(sm + kOffPhiQ);
+      if (state_warp) {
+        float cur[80];
 #pragma unroll
-        for (int i = 0; i < kDv; ++i) prev[i] *= Lam;
-        zprev *= Lam;
-      }
-      int r0 = 0, r1 = -1;
-      float sc = 1.f;
-      const int n = has ? full_rows_of(j, r0, r1, sc) : 0;
-      // tensor-memory loads are warp-collective: every lane loads, lanes without a feature write nothing
-      float zz[16];
-      tmem_ld16(tlane + my_colc + kDv, zz);
-      tmem_ld_wait();
-      {
+        for (int g = 0; g < 5; ++g) tmem_ld16(tlane + kColS + 80 * half + 16 * g, *reinterpret_cast<float(*)[16]>(cur + 16 * g));
+        tmem_ld_wait();
+        if (row <= kDv) {
 #pragma unroll
-        for (int hv = 0; hv < 2; ++hv) {
-          float cur[32];
-          tmem_ld16(tlane + my_colc + 32 * hv, *reinterpret_cast<float(*)[16]>(cur));
-          tmem_ld16(tlane + my_colc + 32 * hv + 16, *reinterpret_cast<float(*)[16]>(cur + 16));
-          tmem_ld_wait();
-          for (int k = 0; k < n; ++k) {
-            const int r = k == 0 ? r0 : r1;
-#pragma unroll
-            for (int cc = 0; cc < 32; cc += 4) {
-              const int col = 32 * hv + cc;
-              float4 base = s_in ? *reinterpret_cast<const float4*>(s_in + r * kDv + col) : make_float4(0.f, 0.f, 0.f, 0.f);
-              if constexpr (DECAY) {
-                base.x *= Lam; base.y *= Lam; base.z *= Lam; base.w *= Lam;
-              }
-              base.x += (cur[cc] - prev[col]) * sc;
-              base.y += (cur[cc + 1] - prev[col + 1]) * sc;
-              base.z += (cur[cc + 2] - prev[col + 2]) * sc;
-              base.w += (cur[cc + 3] - prev[col + 3]) * sc;
-              *reinterpret_cast<float4*>(s_out + r * kDv + col) = base;
-            }
-          }
+          for (int i = 0; i < 80; ++i) stage[(80 * half + i) * kStageLd + row] = cur[i];
         }
+      }
+      named_bar_sync(kBarWorkers, kWorkers);
+      if (tid < kDcUsed) {
+        float* s_out = a.s_out + bh * kDfull * kDv;
+        float* z_out = a.z_out + bh * kDfull;
+        const int j = tid;
+        const float* cur = stage + j * kStageLd;
+        // with decay the incoming state's share is Lambda = lambda^N of it:
+        // s_out = Lambda s_in + expand(c - Lambda c_in)
+        const float Lam = lam_pow((float)N);
+        float prev[kDv];
+        compact_row(j, prev);
+        float zprev = compact_z(j);
+        if constexpr (DECAY) {
+#pragma unroll
+          for (int i = 0; i < kDv; ++i) prev[i] *= Lam;
+          zprev *= Lam;
+        }
+        int r0 = 0, r1 = -1;
+        float sc = 1.f;
+        const int n = full_rows_of(j, r0, r1, sc);
         for (int k = 0; k < n; ++k) {
           const int r = k == 0 ? r0 : r1;
+#pragma unroll
+          for (int col = 0; col < kDv; col += 4) {
+            float4 base = s_in ? *reinterpret_cast<const float4*>(s_in + r * kDv + col) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (DECAY) {
+              base.x *= Lam; base.y *= Lam; base.z *= Lam; base.w *= Lam;
+            }
+            base.x += (cur[col] - prev[col]) * sc;
+            base.y += (cur[col + 1] - prev[col + 1]) * sc;
+            base.z += (cur[col + 2] - prev[col + 2]) * sc;
+            base.w += (cur[col + 3] - prev[col + 3]) * sc;
+            *reinterpret_cast<float4*>(s_out + r * kDv + col) = base;
+          }
           const float zb = z_in ? Lam * z_in[r] : 0.f;
-          z_out[r] = zb + (zz[0] - zprev) * sc;
+          z_out[r] = zb + (cur[kDv] - zprev) * sc;
         }
       }
     }
