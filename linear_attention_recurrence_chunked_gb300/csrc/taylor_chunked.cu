@@ -147,31 +147,46 @@ __device__ __forceinline__ uint4 feature8(const uint32_t* w, const float* x) {
   return make_uint4(feature_pair<BEGIN>(w, x), feature_pair<BEGIN + 2>(w, x), feature_pair<BEGIN + 4>(w, x),
                     feature_pair<BEGIN + 6>(w, x));
 }
-// Features [BEGIN, BEGIN + 8) of a row times `sc`, rounded once to bf16.
+// Feature J of a row times `sc`, with xs = sc x precomputed: one multiply per
+// product term (x_a x_b sc as (sc x_a) x_b).
+template <int J>
+__device__ __forceinline__ float feature_scaled(const float* x, const float* xs, float sc) {
+  constexpr int kind = feat_kind(J);
+  if constexpr (kind == 0) return sc;
+  else if constexpr (kind == 1) return xs[feat_a(J)];
+  else if constexpr (kind == 2) return xs[feat_a(J)] * kInvSqrt2 * x[feat_a(J)];
+  else if constexpr (kind == 3) return xs[feat_a(J)] * x[feat_b(J)];
+  else return 0.f;
+}
+// Features [BEGIN, BEGIN + 8) of a row times `sc`, rounded to bf16.
 template <int BEGIN>
-__device__ __forceinline__ uint4 feature8_scaled(const float* x, float sc) {
-  const float f[8] = {feature<BEGIN>(x) * sc,     feature<BEGIN + 1>(x) * sc, feature<BEGIN + 2>(x) * sc,
-                      feature<BEGIN + 3>(x) * sc, feature<BEGIN + 4>(x) * sc, feature<BEGIN + 5>(x) * sc,
-                      feature<BEGIN + 6>(x) * sc, feature<BEGIN + 7>(x) * sc};
+__device__ __forceinline__ uint4 feature8_scaled(const float* x, const float* xs, float sc) {
+  const float f[8] = {feature_scaled<BEGIN>(x, xs, sc),     feature_scaled<BEGIN + 1>(x, xs, sc),
+                      feature_scaled<BEGIN + 2>(x, xs, sc), feature_scaled<BEGIN + 3>(x, xs, sc),
+                      feature_scaled<BEGIN + 4>(x, xs, sc), feature_scaled<BEGIN + 5>(x, xs, sc),
+                      feature_scaled<BEGIN + 6>(x, xs, sc), feature_scaled<BEGIN + 7>(x, xs, sc)};
   return pack8_bf16(f);
 }
 template <int BEGIN>
 __device__ __forceinline__ void store_features80_scaled(uint8_t* tile, int row, const float* x, float sc) {
+  float xs[kF];
+#pragma unroll
+  for (int i = 0; i < kF; ++i) xs[i] = sc * x[i];
 #pragma unroll
   for (int g = 0; g < 10; ++g) {
     // g is a compile-time constant after unrolling; the switch selects the instantiation
     uint4 u;
     switch (g) {
-      case 0: u = feature8_scaled<BEGIN + 0>(x, sc); break;
-      case 1: u = feature8_scaled<BEGIN + 8>(x, sc); break;
-      case 2: u = feature8_scaled<BEGIN + 16>(x, sc); break;
-      case 3: u = feature8_scaled<BEGIN + 24>(x, sc); break;
-      case 4: u = feature8_scaled<BEGIN + 32>(x, sc); break;
-      case 5: u = feature8_scaled<BEGIN + 40>(x, sc); break;
-      case 6: u = feature8_scaled<BEGIN + 48>(x, sc); break;
-      case 7: u = feature8_scaled<BEGIN + 56>(x, sc); break;
-      case 8: u = feature8_scaled<BEGIN + 64>(x, sc); break;
-      default: u = feature8_scaled<BEGIN + 72>(x, sc); break;
+      case 0: u = feature8_scaled<BEGIN + 0>(x, xs, sc); break;
+      case 1: u = feature8_scaled<BEGIN + 8>(x, xs, sc); break;
+      case 2: u = feature8_scaled<BEGIN + 16>(x, xs, sc); break;
+      case 3: u = feature8_scaled<BEGIN + 24>(x, xs, sc); break;
+      case 4: u = feature8_scaled<BEGIN + 32>(x, xs, sc); break;
+      case 5: u = feature8_scaled<BEGIN + 40>(x, xs, sc); break;
+      case 6: u = feature8_scaled<BEGIN + 48>(x, xs, sc); break;
+      case 7: u = feature8_scaled<BEGIN + 56>(x, xs, sc); break;
+      case 8: u = feature8_scaled<BEGIN + 64>(x, xs, sc); break;
+      default: u = feature8_scaled<BEGIN + 72>(x, xs, sc); break;
     }
     *reinterpret_cast<uint4*>(tile + sw128_off(row, BEGIN + 8 * g, kC)) = u;
   }
@@ -265,6 +280,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   __shared__ uint64_t bar_accfree[2];  // workers: outputs of the chunk two back read its accumulator, by parity
   __shared__ uint64_t bar_fin;     // drain after an expired wait
   __shared__ uint32_t tmem_base_sh;
+  __shared__ float lam_tab[64];    // with decay: zeros at [0, 32), lambda^0..lambda^31 at [32, 64)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const bool worker = tid < kWorkers;
@@ -312,6 +328,9 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
   // ---- constant tiles: [.. | 1] block (column 0 = 1) and the z tile, zeroed first
   for (int i = tid; i < 16384 / 16; i += kBlock) reinterpret_cast<uint4*>(sm + kOffOnes)[i] = make_uint4(0, 0, 0, 0);
   for (int i = tid; i < (int)(3 * kCtBlock / 16); i += kBlock) reinterpret_cast<uint4*>(sm + kOffCt)[i] = make_uint4(0, 0, 0, 0);
+  if constexpr (DECAY) {
+    if (tid < 64) lam_tab[tid] = tid < 32 ? 0.f : lam_pow((float)(tid - 32));
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -592,7 +611,8 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         for (int i = 0; i < 80; ++i) v[i] *= next_scale;
 #pragma unroll
         for (int g = 0; g < 5; ++g) tmem_st16(tlane + kColS + 80 * half + 16 * g, *reinterpret_cast<float(*)[16]>(v + 16 * g));
-        tmem_st_wait();
+        // (their completion is awaited at the feature hand-off: only the tensor-memory write is
+        // asynchronous, the source registers are free once the store is issued)
       }
     };
 
@@ -643,14 +663,13 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
             for (int j = 0; j < 32; ++j) p[j] = j < nv ? fmaf(p[j], fmaf(0.5f, p[j], 1.f), 1.f) : 0.f;
           }
           if constexpr (DECAY) {
-            // times lambda^(row - base - j) on the kept columns: from column 31 down the factor starts at
-            // lambda^max(nv - 32, 0) and gains one lambda per kept column
-            float f = lam_pow((float)max(nv - 32, 0));
+            // times lambda^(row - base - j) = lambda^(nv - 1 - j) on the kept columns, as
+            // lambda^max(nv - 32, 0) times a table entry: lambda^(31 - j) for a full group, lambda^(nv - 1 - j)
+            // on the diagonal, and 0 from the table's lower half for the columns past it (already 0)
+            const float f = lam_pow((float)max(nv - 32, 0));
+            const float* tb = lam_tab + 31 + min(nv, 32);
 #pragma unroll
-            for (int j = 31; j >= 0; --j) {
-              p[j] *= f;
-              if (j < nv) f *= lam;
-            }
+            for (int j = 0; j < 32; ++j) p[j] *= f * tb[-j];
           }
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -674,6 +693,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       if (has_next) {
         refresh_state_tiles(lam_pow((float)chunk_len(c + 1)));
         features(c + 1);
+        if constexpr (DECAY) tmem_st_wait();  // the rescaled state is in tensor memory before the next update
         fence_proxy_async_smem();
         tc_fence_before();
         warp_arrive(smem_u32(&bar_feat));
