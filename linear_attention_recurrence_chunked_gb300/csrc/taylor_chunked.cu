@@ -577,13 +577,19 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       if (tid == 0) mbar_arrive(smem_u32(&bar_qkin));
     };
     // outputs of chunk cc: y = Acc / (Acc[64] + eps), this thread 32 columns
-    auto outputs = [&](int cc) {
+    auto outputs = [&](int cc, bool release_acc) {
       const uint32_t acc = tlane + kColAcc + (uint32_t)(cc & 1) * 80u;
       float d[16], y[32];
       tmem_ld16(acc + 64, d);
       tmem_ld16(acc + 32 * half, *reinterpret_cast<float(*)[16]>(y));
       tmem_ld16(acc + 32 * half + 16, *reinterpret_cast<float(*)[16]>(y + 16));
       tmem_ld_wait();
+      if (release_acc) {
+        // the accumulator is in registers: the readout of chunk cc + 2 may overwrite it (arriving before
+        // the y stores keeps the arrival from waiting for them)
+        tc_fence_before();
+        warp_arrive(smem_u32(&bar_accfree[cc & 1]));
+      }
       const int64_t t = (int64_t)cc * kC + row;
       if (t < N) {
         const float inv = 1.f / (d[0] + a.eps);
@@ -698,14 +704,12 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
         tc_fence_before();
         warp_arrive(smem_u32(&bar_feat));
       }
-      // ---- outputs of the previous chunk, off the chain refresh -> features -> readout; then the
-      //      readout of chunk c + 1 may overwrite its accumulator
+      // ---- outputs of the previous chunk, off the chain refresh -> features -> readout; once its
+      //      accumulator is in registers the readout of chunk c + 1 may overwrite it
       if (c > 0) {
         ok = ok && wait(&bar_pv[par ^ 1u], (uint32_t)(((c - 1) >> 1) & 1));
         tc_fence_after();
-        outputs(c - 1);
-        tc_fence_before();
-        warp_arrive(smem_u32(&bar_accfree[par ^ 1u]));
+        outputs(c - 1, true);
       }
     }
     if (nchunks > 0) {
@@ -713,7 +717,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       const int c = nchunks - 1;
       ok = ok && wait(&bar_pv[c & 1], (uint32_t)((c >> 1) & 1));
       tc_fence_after();
-      outputs(c);
+      outputs(c, false);
     }
     cp_async_wait_all();
     ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the final-state pass below uses warp-collective loads
