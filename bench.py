@@ -362,7 +362,8 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         byts = BYTES_PER_TOKEN_HEAD["taylor_prefill"] * w.B * w.H * w.N + STATE_BYTES["taylor"] * w.B * w.H
         out["based_prefill_decay"] = {"workload": w.description + ", per-head decay 1 - 2^-(5 + h mod 8)",
                                       "tokens_per_s": round(whole_job_rate(w.B * w.N, ws, ms * 1e-3), 1),
-                                      "ms": round(ms, 4), "roofline": roofline(byts, ms, pk["hbm_gbs"], None)}
+                                      "ms": round(ms, 4),
+                                      "roofline": roofline(byts, ms, pk["hbm_gbs"], ncu_traffic("based_prefill_decay"))}
         del x, y, s, z
         torch.cuda.empty_cache()
     for name in ("gdn_prefill", "gdn_prefill_long", "gated_prefill"):
@@ -526,7 +527,8 @@ def notebank_paths(args, la, dev, stream, flush, pk, seed_off, ws, only):
                                              f"d_k {NB_D}, {NB_N} tokens, chunks of {NB_CHUNK}, "
                                              f"{n_notes} note addresses",
                                  "tokens_per_s": round(whole_job_rate(NB_N, ws, ms * 1e-3), 1),
-                                 "ms": round(ms, 4), "roofline": roofline(byts, ms, pk["hbm_gbs"], None)}
+                                 "ms": round(ms, 4),
+                                 "roofline": roofline(byts, ms, pk["hbm_gbs"], ncu_traffic("notebank_write"))}
         del k, q
         torch.cuda.empty_cache()
     if only is None or only == "notebank_route":

@@ -118,12 +118,40 @@ notebank_chunk_scores_kernel(NotebankScoresLaunch a) {
   }
 }
 
+// Elements [PER lane, PER lane + PER) of a 16-byte aligned shared-memory row, as floats: one vector
+// load per 16 bytes (a warp reads the whole row in d * sizeof(T) / 128 wavefronts).
+template <typename T, int PER>
+__device__ __forceinline__ void load_lane_run(const T* row, int lane, float (&x)[PER]) {
+  const T* p = row + PER * lane;
+  constexpr int kBytes = PER * (int)sizeof(T);
+  if constexpr (kBytes % 16 == 0) {
+#pragma unroll
+    for (int v = 0; v < kBytes / 16; ++v) {
+      const uint4 u = reinterpret_cast<const uint4*>(p)[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      if constexpr (sizeof(T) == 2) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          x[8 * v + 2 * j] = __uint_as_float(w[j] << 16);
+          x[8 * v + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) x[4 * v + j] = __uint_as_float(w[j]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) x[i] = to_f(p[i]);
+  }
+}
+
 // The same scores with each chunk split over a cluster of kClusterCtas CTAs
 // that keep their share of the chunk's keys in shared memory: the keys are
 // read from HBM once.  Each CTA sums its unit keys; after a cluster barrier
-// every CTA adds the kClusterCtas partial sums (in rank order, so all get the
-// same bits) through distributed shared memory; a second barrier keeps every
-// CTA's partial alive until all have read it.
+// every warp adds the kClusterCtas partial sums (in rank order, so all get the
+// same bits) through distributed shared memory; a second barrier at the end
+// keeps every CTA's partial alive until all have read it.
 constexpr int kClusterCtas = 4;
 
 template <typename T, int PER>
@@ -164,38 +192,50 @@ notebank_chunk_scores_cluster_kernel(NotebankScoresLaunch a, int sub) {
     tc::cp_async_wait_all();
     __syncthreads();
   }
-  // pass 1: inverse norms and the sum of unit keys
+  // pass 1: inverse norms and the sum of unit keys.  Lane l holds dims [PER l, PER l + PER) of a row;
+  // the partial sums, their cluster-wide total and mu keep dim PER l + i at position 32 i + l, so that
+  // a warp's accesses to them are free of bank conflicts
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-  for (int r = r0 + warp; r < r1; r += kWarps) {
-    const T* src = rows + (int64_t)(r - r0) * d;
-    float x[PER];
+  // kU rows per warp at a time (rows r, r + kWarps, ...): independent load / reduce chains overlap
+  constexpr int kU = 4;
+  for (int rb = r0 + warp; rb < r1; rb += kU * kWarps) {
+    float x[kU][PER], ss[kU];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) x[i] = to_f(src[lane + 32 * i]);
-    float ss = 0.f;
+    for (int u = 0; u < kU; ++u) {
+      const int r = rb + u * kWarps;
+      if (r < r1) load_lane_run<T, PER>(rows + (int64_t)(r - r0) * d, lane, x[u]);
+      else
 #pragma unroll
-    for (int i = 0; i < PER; ++i) ss = fmaf(x[i], x[i], ss);
-    ss = warp_sum(ss);
-    const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;  // a zero key normalises to zero
+        for (int i = 0; i < PER; ++i) x[u][i] = 0.f;
+      ss[u] = 0.f;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = fmaf(x[i], inv, acc[i]);
-    if (lane == 0) inv_norm[r - r0] = inv;
-  }
+      for (int i = 0; i < PER; ++i) ss[u] = fmaf(x[u][i], x[u][i], ss[u]);
+    }
 #pragma unroll
-  for (int i = 0; i < PER; ++i) part[warp][lane + 32 * i] = acc[i];
-  __syncthreads();
-  if (warp == 0) {
+    for (int u = 0; u < kU; ++u) ss[u] = warp_sum(ss[u]);
 #pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      float s = 0.f;
+    for (int u = 0; u < kU; ++u) {
+      const int r = rb + u * kWarps;
+      const float inv = ss[u] > 0.f ? rsqrtf(ss[u]) : 0.f;  // a zero key (or a row past the end) adds nothing
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) s += part[w][lane + 32 * i];
-      cpart[lane + 32 * i] = s;
+      for (int i = 0; i < PER; ++i) acc[i] = fmaf(x[u][i], inv, acc[i]);
+      if (lane == 0 && r < r1) inv_norm[r - r0] = inv;
     }
   }
+#pragma unroll
+  for (int i = 0; i < PER; ++i) part[warp][32 * i + lane] = acc[i];
+  __syncthreads();
+  for (int i = warp; i < PER; i += kWarps) {  // the warps' partial sums, warp by warp in a fixed order
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) s += part[w][32 * i + lane];
+    cpart[32 * i + lane] = s;
+  }
   cluster.sync();
-  // mean direction of the whole chunk, normalised (the 1/|C| of the mean cancels)
+  // mean direction of the whole chunk, normalised (the 1/|C| of the mean cancels), formed by warp 0 from
+  // the kClusterCtas partial sums in rank order (so every CTA gets the same bits)
   if (warp == 0) {
     float m[PER];
 #pragma unroll
@@ -203,7 +243,7 @@ notebank_chunk_scores_cluster_kernel(NotebankScoresLaunch a, int sub) {
     for (int q = 0; q < kClusterCtas; ++q) {
       const float* rp = cluster.map_shared_rank(cpart, q);
 #pragma unroll
-      for (int i = 0; i < PER; ++i) m[i] += rp[lane + 32 * i];
+      for (int i = 0; i < PER; ++i) m[i] += rp[32 * i + lane];
     }
     float ss = 0.f;
 #pragma unroll
@@ -211,22 +251,37 @@ notebank_chunk_scores_cluster_kernel(NotebankScoresLaunch a, int sub) {
     ss = warp_sum(ss);
     const float inv = ss > 0.f ? rsqrtf(ss) : 0.f;
 #pragma unroll
-    for (int i = 0; i < PER; ++i) mu[lane + 32 * i] = m[i] * inv;
+    for (int i = 0; i < PER; ++i) mu[32 * i + lane] = m[i] * inv;
   }
-  cluster.sync();  // every partial has been read; mu is visible to the whole CTA
+  __syncthreads();
   float mv[PER];
 #pragma unroll
-  for (int i = 0; i < PER; ++i) mv[i] = mu[lane + 32 * i];
+  for (int i = 0; i < PER; ++i) mv[i] = mu[32 * i + lane];
   // pass 2 from shared memory: d_t = 1 - <k_t, mu> / |k_t|
   float* out = a.d_ch + ch * a.N + t0;
-  for (int r = r0 + warp; r < r1; r += kWarps) {
-    const T* src = rows + (int64_t)(r - r0) * d;
-    float dt = 0.f;
+  for (int rb = r0 + warp; rb < r1; rb += kU * kWarps) {
+    float dt[kU];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) dt = fmaf(to_f(src[lane + 32 * i]), mv[i], dt);
-    dt = warp_sum(dt);
-    if (lane == 0) out[r] = 1.f - dt * inv_norm[r - r0];
+    for (int u = 0; u < kU; ++u) {
+      const int r = rb + u * kWarps;
+      float x[PER];
+      if (r < r1) load_lane_run<T, PER>(rows + (int64_t)(r - r0) * d, lane, x);
+      else
+#pragma unroll
+        for (int i = 0; i < PER; ++i) x[i] = 0.f;
+      dt[u] = 0.f;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) dt[u] = fmaf(x[i], mv[i], dt[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) dt[u] = warp_sum(dt[u]);
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int r = rb + u * kWarps;
+      if (lane == 0 && r < r1) out[r] = 1.f - dt[u] * inv_norm[r - r0];
+    }
   }
+  cluster.sync();  // this CTA's partial sums stay alive until every CTA of the cluster has read them
 }
 
 // d_t = mean over the channels (fixed order), and the window sums of d.
