@@ -13,9 +13,16 @@
 // shuffles give the softmax, then lane l accumulates its d/32 consecutive
 // output columns over the slots, eight slots in flight (each value row read
 // by the warp in one coalesced piece).  The new token is written into its
-// slot first, so all slots are read alike.
+// slot first, so all slots are read alike.  For d of 64 or 128 a second
+// kernel stages each warp's whole window in shared memory with one round of
+// 16-byte copies instead (a step then waits on memory once, not once per
+// group of rows); larger windows than fit take the first kernel.
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "tc.cuh"
 
 namespace la {
 namespace {
@@ -164,18 +171,186 @@ swa_decode_kernel(SwaDecodeLaunch a) {
   }
 }
 
+// The same step with the window staged in shared memory (d = D of 64 or 128, 16-byte aligned caches):
+// each warp copies its whole key and value window in one round of 16-byte cp.async copies, rows
+// padded by 16 bytes (a lane per row then reads without bank conflicts), replaces the copy of the
+// new token's slot with the new k, v and works from shared memory only.
+template <typename TIn, typename TOut, int D>
+__global__ void __launch_bounds__(32 * kWarps)
+swa_decode_staged_kernel(SwaDecodeLaunch a) {
+  extern __shared__ __align__(16) uint8_t sw_smem[];
+  __shared__ float qs[kWarps][D];
+  __shared__ float ps[kWarps][kMaxWindow];
+  constexpr int kRowBytes = D * (int)sizeof(TIn), kPitch = kRowBytes + 16, kVec = kRowBytes / 16;
+  constexpr int kPerVec = 16 / (int)sizeof(TIn);  // elements per 16-byte vector
+  constexpr int kCpl = D / 32;                     // output columns per lane
+  const int nwarps = blockDim.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t sh = (int64_t)blockIdx.x * nwarps + warp;
+  if (sh >= a.S * a.H) return;  // warp-uniform; the kernel has no block-wide barrier
+  const int64_t s = sh / a.H;
+  const int w = a.window;
+  const int64_t pos = a.pos[s];
+  if (pos < 0) {
+    if (lane == 0) atomicOr(a.status, kStatusBadIndex);
+    return;
+  }
+  const int slot_new = (int)(pos % w);
+  const int n = pos + 1 < w ? (int)(pos + 1) : w;
+  uint8_t* ks = sw_smem + (size_t)warp * 2 * w * kPitch;
+  uint8_t* vs = ks + (size_t)w * kPitch;
+  const uint8_t* kc = reinterpret_cast<const uint8_t*>(a.k_cache) + sh * (int64_t)w * kRowBytes;
+  const uint8_t* vc = reinterpret_cast<const uint8_t*>(a.v_cache) + sh * (int64_t)w * kRowBytes;
+  for (int i = lane; i < n * kVec; i += 32) {
+    const int r = i / kVec, c = i - r * kVec;
+    tc::cp_async16(tc::smem_u32(ks + r * kPitch + c * 16), kc + (int64_t)r * kRowBytes + c * 16, 16u);
+    tc::cp_async16(tc::smem_u32(vs + r * kPitch + c * 16), vc + (int64_t)r * kRowBytes + c * 16, 16u);
+  }
+  tc::cp_async_commit();
+  // meanwhile: q (scaled) and the new token into the ring buffer
+  const TIn* q = reinterpret_cast<const TIn*>(a.q) + sh * D;
+  const TIn* k = reinterpret_cast<const TIn*>(a.k) + sh * D;
+  const TIn* v = reinterpret_cast<const TIn*>(a.v) + sh * D;
+  TIn knew[kCpl], vnew[kCpl];
+#pragma unroll
+  for (int e = 0; e < kCpl; ++e) {
+    const int c = lane * kCpl + e;
+    qs[warp][c] = to_f(q[c]) * a.scale;
+    knew[e] = k[c];
+    vnew[e] = v[c];
+    reinterpret_cast<TIn*>(a.k_cache)[(sh * w + slot_new) * D + c] = knew[e];
+    reinterpret_cast<TIn*>(a.v_cache)[(sh * w + slot_new) * D + c] = vnew[e];
+  }
+  tc::cp_async_wait_all();
+  __syncwarp();
+  // the staged copy of the new token's slot may hold the old token: overwrite it
+#pragma unroll
+  for (int e = 0; e < kCpl; ++e) {
+    reinterpret_cast<TIn*>(ks + slot_new * kPitch)[lane * kCpl + e] = knew[e];
+    reinterpret_cast<TIn*>(vs + slot_new * kPitch)[lane * kCpl + e] = vnew[e];
+  }
+  __syncwarp();
+  // scores of this lane's slots
+  float sc[kSlotsPerLane];
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < kSlotsPerLane; ++i) {
+    const int j = lane + 32 * i;
+    float acc = -INFINITY;
+    if (j < n) {
+      const uint8_t* kr = ks + j * kPitch;
+      float p0 = 0.f, p1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < kVec; ++c) {
+        const uint4 u = *reinterpret_cast<const uint4*>(kr + c * 16);
+        const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+        if constexpr (sizeof(TIn) == 2) {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            p0 = fmaf(qs[warp][c * kPerVec + 2 * t], __uint_as_float(wd[t] << 16), p0);
+            p1 = fmaf(qs[warp][c * kPerVec + 2 * t + 1], __uint_as_float(wd[t] & 0xffff0000u), p1);
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            if (t & 1) p1 = fmaf(qs[warp][c * kPerVec + t], __uint_as_float(wd[t]), p1);
+            else p0 = fmaf(qs[warp][c * kPerVec + t], __uint_as_float(wd[t]), p0);
+          }
+        }
+      }
+      acc = p0 + p1;
+    }
+    sc[i] = acc;
+    m = fmaxf(m, acc);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(kFullMask, m, off));
+  float l = 0.f;
+#pragma unroll
+  for (int i = 0; i < kSlotsPerLane; ++i) {
+    const int j = lane + 32 * i;
+    if (j < n) {
+      const float e = __expf(sc[i] - m);
+      ps[warp][j] = e;
+      l += e;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) l += __shfl_xor_sync(kFullMask, l, off);
+  __syncwarp();
+  // o = sum_j p_j v_j / l, lane l owning columns [kCpl l, kCpl l + kCpl), four slots in flight
+  float acc[4][kCpl];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int e = 0; e < kCpl; ++e) acc[u][e] = 0.f;
+  const uint8_t* vl = vs + lane * kCpl * (int)sizeof(TIn);
+  int j = 0;
+  for (; j + 4 <= n; j += 4) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const TIn* vr = reinterpret_cast<const TIn*>(vl + (j + u) * kPitch);
+      const float pj = ps[warp][j + u];
+#pragma unroll
+      for (int e = 0; e < kCpl; ++e) acc[u][e] = fmaf(pj, to_f(vr[e]), acc[u][e]);
+    }
+  }
+  for (; j < n; ++j) {
+    const TIn* vr = reinterpret_cast<const TIn*>(vl + j * kPitch);
+    const float pj = ps[warp][j];
+#pragma unroll
+    for (int e = 0; e < kCpl; ++e) acc[0][e] = fmaf(pj, to_f(vr[e]), acc[0][e]);
+  }
+  const float inv = 1.f / l;
+  TOut* out = reinterpret_cast<TOut*>(a.out) + sh * D;
+#pragma unroll
+  for (int e = 0; e < kCpl; ++e) store1(out + lane * kCpl + e, ((acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e])) * inv);
+}
+
+// The staged kernel for d = D: warps per CTA so that their windows fit in shared memory, 0 if even one
+// warp's does not (the caller then takes the kernel above).
+template <typename TIn, typename TOut, int D>
+cudaError_t launch_staged(const SwaDecodeLaunch& a, cudaStream_t stream, bool& done) {
+  constexpr int64_t kMaxDynamic = 200 * 1024;
+  const int64_t per_warp = 2 * (int64_t)a.window * (D * (int64_t)sizeof(TIn) + 16);
+  const int wpc = (int)std::min<int64_t>(kWarps, kMaxDynamic / per_warp);
+  done = false;
+  if (wpc == 0) return cudaSuccess;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(swa_decode_staged_kernel<TIn, TOut, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kMaxDynamic);
+  });
+  if (attr != cudaSuccess) return attr;
+  const int64_t grid = (a.S * a.H + wpc - 1) / wpc;
+  swa_decode_staged_kernel<TIn, TOut, D><<<(unsigned)grid, 32 * wpc, (size_t)(wpc * per_warp), stream>>>(a);
+  done = true;
+  return cudaGetLastError();
+}
+
+template <typename TIn, typename TOut>
+cudaError_t launch_typed(const SwaDecodeLaunch& a, cudaStream_t stream) {
+  const bool aligned = ((reinterpret_cast<uintptr_t>(a.k_cache) | reinterpret_cast<uintptr_t>(a.v_cache)) & 15u) == 0;
+  if (aligned && (a.d == 64 || a.d == 128)) {
+    bool done = false;
+    const cudaError_t e = a.d == 64 ? launch_staged<TIn, TOut, 64>(a, stream, done)
+                                    : launch_staged<TIn, TOut, 128>(a, stream, done);
+    if (e != cudaSuccess || done) return e;
+  }
+  const int64_t grid = (a.S * a.H + kWarps - 1) / kWarps;
+  swa_decode_kernel<TIn, TOut><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_swa_decode(const SwaDecodeLaunch& a, cudaStream_t stream) {
-  const int64_t grid = (a.S * a.H + kWarps - 1) / kWarps;
-  if (grid == 0) return cudaSuccess;
-#define LA_SWA(TI, TO) swa_decode_kernel<TI, TO><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(a)
-  if (a.in_bf16 && a.out_bf16) LA_SWA(__nv_bfloat16, __nv_bfloat16);
-  else if (a.in_bf16) LA_SWA(__nv_bfloat16, float);
-  else if (a.out_bf16) LA_SWA(float, __nv_bfloat16);
-  else LA_SWA(float, float);
-#undef LA_SWA
-  return cudaGetLastError();
+  if (a.S * a.H == 0) return cudaSuccess;
+  if (a.in_bf16 && a.out_bf16) return launch_typed<__nv_bfloat16, __nv_bfloat16>(a, stream);
+  if (a.in_bf16) return launch_typed<__nv_bfloat16, float>(a, stream);
+  if (a.out_bf16) return launch_typed<float, __nv_bfloat16>(a, stream);
+  return launch_typed<float, float>(a, stream);
 }
 
 }  // namespace la

@@ -26,8 +26,11 @@ def _draw(S, H, N, d, dtype, seed):
 
 @pytest.mark.parametrize("window,d,dtype", [(64, 64, torch.bfloat16), (16, 64, torch.bfloat16),
                                             (128, 128, torch.bfloat16), (1, 64, torch.float32),
-                                            (64, 64, torch.float32), (256, 32, torch.bfloat16)])
+                                            (64, 64, torch.float32), (256, 32, torch.bfloat16),
+                                            (256, 128, torch.bfloat16), (256, 128, torch.float32)])
 def test_swa_decode_matches_oracle(window, d, dtype):
+    """d of 64 or 128 stages each window in shared memory (four warps per CTA, or fewer for large
+    windows: one for 256 x 128 bf16); d = 32 and 256 x 128 fp32 (too large) take the direct kernel."""
     dev = cuda_device()
     S, H, steps = 5, 3, 40
     offsets = [0, 3, window - 1, window + 5, 3 * window + 2]
