@@ -64,4 +64,29 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[NV]) {
   return r;
 }
 
+// Programmatic dependent launch.  A kernel started by launch_dependent() may begin while the kernel
+// before it in the stream still runs: it calls grid_dependents_trigger() to let the next such kernel
+// be scheduled once all of its own CTAs are resident, and grid_dependency_wait() before its first
+// access to memory that an earlier kernel may have written (the wait ends when that kernel has
+// completed and its writes are visible).  Both are no-ops in a kernel launched the ordinary way.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace la

@@ -32,6 +32,8 @@ gdn_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const TI
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row0 = warp * kGdnRowsPerWarp;
   float* S = state + sh * (kGdnD * kGdnD) + (int64_t)row0 * kGdnD;
+  grid_dependents_trigger();
+  grid_dependency_wait();  // the previous step's state and this step's inputs are in memory
 
   float4 s[kGdnRowsPerWarp];
 #pragma unroll
@@ -103,6 +105,8 @@ taylor_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const
   const int tid = threadIdx.x, cg = tid & 15, rg = tid >> 4;
   float* s = s_state + sh * (kTayD * kTayDv);
   float* z = z_state + sh * kTayD;
+  grid_dependents_trigger();
+  grid_dependency_wait();  // the previous step's state and this step's inputs are in memory
   const float lam = decay ? decay[sh % H] : 1.f;  // s <- lam s + phi(k) v^T, z <- lam z + phi(k)
 
   float4 sv[kTayRowsPerThread];
@@ -169,29 +173,31 @@ taylor_decode_kernel(const TIn* __restrict__ q, const TIn* __restrict__ k, const
 cudaError_t launch_gdn_decode(const DecodeLaunch& a, cudaStream_t stream) {
   const unsigned grid = (unsigned)(a.S * a.H);
   if (grid == 0) return cudaSuccess;
+  cudaError_t e;
 #define LA_GDN_DECODE(TI, TO)                                                                    \
-  gdn_decode_kernel<TI, TO><<<grid, kGdnThreads, 0, stream>>>(                                  \
-      (const TI*)a.q, (const TI*)a.k, (const TI*)a.v, a.alpha, a.beta, (TO*)a.out, a.state, a.q_scale, a.delta)
+  e = launch_dependent(gdn_decode_kernel<TI, TO>, dim3(grid), dim3(kGdnThreads), 0, stream, (const TI*)a.q,   \
+                       (const TI*)a.k, (const TI*)a.v, a.alpha, a.beta, (TO*)a.out, a.state, a.q_scale, a.delta)
   if (a.in_bf16 && a.out_bf16) LA_GDN_DECODE(__nv_bfloat16, __nv_bfloat16);
   else if (a.in_bf16) LA_GDN_DECODE(__nv_bfloat16, float);
   else if (a.out_bf16) LA_GDN_DECODE(float, __nv_bfloat16);
   else LA_GDN_DECODE(float, float);
 #undef LA_GDN_DECODE
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_taylor_decode(const DecodeLaunch& a, cudaStream_t stream) {
   const unsigned grid = (unsigned)(a.S * a.H);
   if (grid == 0) return cudaSuccess;
+  cudaError_t e;
 #define LA_TAY_DECODE(TI, TO)                                                                    \
-  taylor_decode_kernel<TI, TO><<<grid, kTayThreads, 0, stream>>>(                               \
-      (const TI*)a.q, (const TI*)a.k, (const TI*)a.v, (TO*)a.out, a.state, a.z, a.eps, a.decay, a.H)
+  e = launch_dependent(taylor_decode_kernel<TI, TO>, dim3(grid), dim3(kTayThreads), 0, stream, (const TI*)a.q, \
+                       (const TI*)a.k, (const TI*)a.v, (TO*)a.out, a.state, a.z, a.eps, a.decay, a.H)
   if (a.in_bf16 && a.out_bf16) LA_TAY_DECODE(__nv_bfloat16, __nv_bfloat16);
   else if (a.in_bf16) LA_TAY_DECODE(__nv_bfloat16, float);
   else if (a.out_bf16) LA_TAY_DECODE(float, __nv_bfloat16);
   else LA_TAY_DECODE(float, float);
 #undef LA_TAY_DECODE
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace la

@@ -91,7 +91,9 @@ swa_decode_kernel(SwaDecodeLaunch a) {
   __shared__ float ps[kWarps][kMaxWindow];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t sh = (int64_t)blockIdx.x * kWarps + warp;
+  grid_dependents_trigger();
   if (sh >= a.S * a.H) return;
+  grid_dependency_wait();  // the caches, positions and inputs of this step are in memory
   const int64_t s = sh / a.H;
   const int d = a.d, w = a.window;
   const int64_t pos = a.pos[s];
@@ -187,7 +189,9 @@ swa_decode_staged_kernel(SwaDecodeLaunch a) {
   const int nwarps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t sh = (int64_t)blockIdx.x * nwarps + warp;
+  grid_dependents_trigger();
   if (sh >= a.S * a.H) return;  // warp-uniform; the kernel has no block-wide barrier
+  grid_dependency_wait();       // the caches, positions and inputs of this step are in memory
   const int64_t s = sh / a.H;
   const int w = a.window;
   const int64_t pos = a.pos[s];
@@ -324,9 +328,9 @@ cudaError_t launch_staged(const SwaDecodeLaunch& a, cudaStream_t stream, bool& d
   });
   if (attr != cudaSuccess) return attr;
   const int64_t grid = (a.S * a.H + wpc - 1) / wpc;
-  swa_decode_staged_kernel<TIn, TOut, D><<<(unsigned)grid, 32 * wpc, (size_t)(wpc * per_warp), stream>>>(a);
   done = true;
-  return cudaGetLastError();
+  return launch_dependent(swa_decode_staged_kernel<TIn, TOut, D>, dim3((unsigned)grid), dim3(32 * wpc),
+                          (size_t)(wpc * per_warp), stream, a);
 }
 
 template <typename TIn, typename TOut>
@@ -339,8 +343,7 @@ cudaError_t launch_typed(const SwaDecodeLaunch& a, cudaStream_t stream) {
     if (e != cudaSuccess || done) return e;
   }
   const int64_t grid = (a.S * a.H + kWarps - 1) / kWarps;
-  swa_decode_kernel<TIn, TOut><<<(unsigned)grid, 32 * kWarps, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(swa_decode_kernel<TIn, TOut>, dim3((unsigned)grid), dim3(32 * kWarps), 0, stream, a);
 }
 
 }  // namespace
