@@ -271,28 +271,59 @@ def gpu_arm(args, ws, rank, local):
     roof["peak_source"] = pk["source"]
 
     # --- e2e through the C ABI with host buffers ----------------------------
+    # Every step copies its inputs in from pinned host memory and its results (y and the final state)
+    # back out.  Steps are pipelined over two device buffer sets, as a serving loop would run them:
+    # step i's inputs go in on one copy stream while step i-1 computes and step i-2's results go out
+    # on the other; the whole K-step region is timed, L2 still flushed before each kernel.  (More
+    # copy streams per direction do not help: the host link, ~160 GB/s per direction here, is the
+    # limit.)
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
-    hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    hs = torch.empty(s.shape, dtype=s.dtype).pin_memory()
-    hz = torch.empty(z.shape, dtype=z.dtype).pin_memory()
+    hy, hs, hz = (torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (y, s, z))
+    bufs = [(q, k, v, y, s, z), tuple(torch.empty_like(t) for t in (q, k, v, y, s, z))]
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def e2e_step():
-        q.copy_(hq, non_blocking=True)
-        k.copy_(hk, non_blocking=True)
-        v.copy_(hv, non_blocking=True)
-        la.la_based_prefill(q, k, v, y=y, s_out=s, z_out=z, stream=stream)
-        hy.copy_(y, non_blocking=True)
-        hs.copy_(s, non_blocking=True)
-        hz.copy_(z, non_blocking=True)
+    def e2e_run(n):
+        ev_comp, ev_out = [None, None], [None, None]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        for i in range(n):
+            bq, bk, bv, by, bs, bz = bufs[i % 2]
+            with torch.cuda.stream(s_in):
+                if ev_comp[i % 2] is not None:
+                    s_in.wait_event(ev_comp[i % 2])  # step i-2's kernel has read this set's inputs
+                bq.copy_(hq, non_blocking=True)
+                bk.copy_(hk, non_blocking=True)
+                bv.copy_(hv, non_blocking=True)
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_in)
+            with torch.cuda.stream(stream):
+                stream.wait_event(ev_in)
+                if ev_out[i % 2] is not None:
+                    stream.wait_event(ev_out[i % 2])  # step i-2's results are out of this set
+                flush.zero_()
+                la.la_based_prefill(bq, bk, bv, y=by, s_out=bs, z_out=bz, stream=stream)
+                ev_comp[i % 2] = torch.cuda.Event()
+                ev_comp[i % 2].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[i % 2])
+                hy.copy_(by, non_blocking=True)
+                hs.copy_(bs, non_blocking=True)
+                hz.copy_(bz, non_blocking=True)
+                ev_out[i % 2] = torch.cuda.Event()
+                ev_out[i % 2].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+        stop.record(stream)
+        return start, stop
 
-    et = Timer(stream, flush)
-    for _ in range(args.warmup):
-        et.run(e2e_step)
-    et.reset()
+    e2e_run(args.warmup)
+    torch.cuda.synchronize()
     barrier(ws)
-    for _ in range(args.steps):
-        et.run(e2e_step)
-    e2e_ms = max_over_ranks(et.total_ms(), ws)
+    start, stop = e2e_run(args.steps)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(start.elapsed_time(stop), ws)
     barrier(ws)
     launches += args.steps * KERNELS_PER_CALL["based_prefill"]
     e2e = {"value": whole_job_rate(tokens * args.steps, ws, e2e_ms * 1e-3), "unit": "tokens/s",
