@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -78,10 +79,20 @@ def peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def _code_only(text):
+    """C++/CUDA source without comments or trailing blanks: what a compiler sees, so that a change of a
+    comment does not count as a change of the kernel (no kernel here has "//" or "/*" in a literal)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_sources_sha(files):
+    """Hash of the code (comments left out) of a kernel's source files."""
     h = hashlib.sha256()
     for f in files:
-        h.update(open(os.path.join(ROOT, "linear_attention_recurrence_chunked_gb300", "csrc", f), "rb").read())
+        path = os.path.join(ROOT, "linear_attention_recurrence_chunked_gb300", "csrc", f)
+        h.update(_code_only(open(path, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -686,7 +686,7 @@ taylor_chunked_kernel(const __grid_constant__ CUtensorMap tmap_v, const TaylorPr
       tc_fence_before();
       warp_arrive(smem_u32(&bar_p));
       // ---- next chunk's rows: Q K^T of chunk c + 1 may start (every worker has read this chunk's Q K^T
-      //      columns above), so it runs while the outputs below are written
+      //      columns above), so it runs while the state tiles and features below are formed
       if (has_next) {
         cp_async_wait_all();
         announce_qk();
