@@ -165,3 +165,24 @@ def test_route_pages_scale_sampled():
     rho = torch.randn((n, J, 16), generator=g).to(torch.bfloat16)
     u = torch.randn((J, nq, 16), generator=g).to(torch.bfloat16)
     check_route(rho, u, 2)
+
+
+def test_scores_full_size_sampled():
+    """The benchmark's launch: 192 channels (24 layers x 8 heads), 16384 tokens, d_k 256, chunks of 512;
+    three sampled channels against the oracle, and at full size the channel mean and the window sums
+    checked as what they are (the mean of the kernel's channel scores, the sums of 48 of them)."""
+    dev = cuda_device()
+    L, H, N, d = 24, 8, 16384, 256
+    gen = torch.Generator(device=dev).manual_seed(13)
+    k = torch.randn((L, H, N, d), generator=gen, device=dev).to(torch.bfloat16)
+    d_ch, d_mean, w = la.la_notebank_scores(k, chunk=512, window=48)
+    torch.cuda.synchronize()
+    for l, h in ((0, 0), (11, 5), (23, 7)):
+        ref = oracle.notebank_scores(synthetic.to_oracle(k[l:l + 1, h:h + 1].cpu()), chunk=512, window=48)
+        assert np.max(np.abs(to_np(d_ch[l:l + 1, h:h + 1]) - ref["d_ch"])) < 2e-5, (l, h)
+    dm = d_ch.double().mean(dim=(0, 1))
+    assert torch.max(torch.abs(d_mean.double() - dm)).item() < 1e-5
+    c = torch.cat([torch.zeros(1, dtype=torch.float64, device=dev), torch.cumsum(d_mean.double(), 0)])
+    ws = c[48:] - c[:-48]
+    assert w.numel() == ws.numel() and torch.max(torch.abs(w.double() - ws)).item() < 1e-3
+    assert la.la_device_status() == la.LA_OK

@@ -74,3 +74,33 @@ def test_swa_decode_negative_position_is_reported_and_skipped():
     assert torch.all(out[0] == -1.0).item() and torch.all(kc[0] == 3.0).item()  # untouched
     assert torch.allclose(out[1], v[1], atol=1e-6)  # pos 0: the window holds only the new token
     assert torch.equal(kc[1, :, 0], k[1])
+
+
+def test_swa_decode_full_size_sampled():
+    """The benchmark's launch: 256 sequences x 16 heads, window 64, d 64, bf16, every ring full at the
+    first step; 8 steps, 16 sampled (sequence, head) pairs against the oracle at every step."""
+    dev = cuda_device()
+    S, H, window, d, steps = 256, 16, 64, 64, 8
+    # tokens 0..63 are already in the rings (token p in slot p); tokens 64..71 arrive one per step
+    q_all, k_all, v_all = _draw(S, H, window + steps, d, torch.bfloat16, seed=21)
+    kc = k_all[:, :, :window].contiguous().to(dev)
+    vc = v_all[:, :, :window].contiguous().to(dev)
+    scale = d ** -0.5
+    outs = []
+    for t in range(steps):
+        p = window + t
+        pos = torch.full((S,), p, dtype=torch.int64, device=dev)
+        outs.append(la.la_swa_decode_step(*(x[:, :, p].contiguous().to(dev) for x in (q_all, k_all, v_all)),
+                                          kc, vc, pos, scale=scale))
+    got = torch.stack(outs, dim=2)  # [S, H, steps, d]
+    rng = np.random.default_rng(5)
+    pairs = sorted(rng.choice(S * H, 16, replace=False).tolist())
+    si, hi = [p // H for p in pairs], [p % H for p in pairs]
+
+    def sub(x):  # [1, pairs, tokens, d]
+        return torch.stack([x[s, h] for s, h in zip(si, hi)]).unsqueeze(0)
+
+    ref = oracle.swa(*(synthetic.to_oracle(sub(x)) for x in (q_all, k_all, v_all)), window, scale,
+                     t_samples=list(range(window, window + steps)))
+    assert rel_err(to_np(sub(got.cpu())), ref) < TOL[torch.bfloat16]
+    assert la.la_device_status() == la.LA_OK

@@ -104,3 +104,15 @@ def test_decay_zero_head_returns_current_value():
                                   decay=torch.zeros(2, device=dev))
     torch.cuda.synchronize()
     assert rel_err(to_np(y), inp["v"].float().numpy()) < TOL[torch.bfloat16]
+
+
+def test_decay_full_size():
+    """The benchmark's launch: B=8, H=16, N=4096 bf16 with lambda_h = 1 - 2^-(5 + h mod 8), a spread from
+    a 32- to a 4096-token memory; every output and final state against the oracle."""
+    dev = cuda_device()
+    inp = synthetic.workload_inputs("based_prefill", device=dev)
+    H = inp["q"].shape[1]
+    lam = [1.0 - 2.0 ** -(5 + h % 8) for h in range(H)]
+    got, ref = run(inp, dev, lam)
+    check(got, ref, TOL[torch.bfloat16])
+    assert la.la_device_status() == la.LA_OK
