@@ -251,11 +251,19 @@ typedef struct la_swa_decode_args {
   float scale;
 } la_swa_decode_args;
 
+/* Like la_decode_step, the step's kernel is launched as a programmatic
+ * dependent of the kernel before it on the stream: it may be scheduled while
+ * that kernel finishes, but touches memory only once it has completed, so the
+ * usual stream order holds. */
 la_status la_swa_decode_step(const la_swa_decode_args* args, void* stream);
 
 /* One recurrent decode step (NoteBank Eq. (1) for one token; BASED notes
  * Sec. 2.5: the decode step fuses the outer-product write with the query
- * readout and still reads and writes the whole persistent state). */
+ * readout and still reads and writes the whole persistent state).  The step's
+ * kernel is launched as a programmatic dependent of the kernel before it on
+ * the stream: it may be scheduled while that kernel finishes (which hides the
+ * launch gap between consecutive steps) but reads and writes memory only once
+ * it has completed, so the usual stream order holds. */
 la_status la_decode_step(const la_decode_args* args, void* stream);
 
 /* Readout-boundary state rescaling (NoteBank App. D.1: S <- lambda S with
