@@ -116,3 +116,31 @@ def test_notebank_pins_catch_planted_mistake(monkeypatch, name, old, new):
     for fn in ("notebank_scores", "notebank_address", "notebank_route"):
         monkeypatch.setattr(oracle, fn, ns[fn])
     assert any(_caught(f) for f in NB_PINS), f"no pin caught the planted mistake '{name}'"
+
+
+# Planted mistakes in the window-attention and state-operation definitions, against their pins.
+SWA_STATE_MUTANTS = [
+    ("window one token too long", "lo = max(0, i - window + 1)", "lo = max(0, i - window)"),
+    ("window excludes the current token", "for j in range(lo, i + 1)])", "for j in range(lo, i)] + [0.0])"),
+    ("scale dropped", "s = np.array([scale * float(np.dot(q[b, h, i], k[b, h, j]))",
+     "s = np.array([float(np.dot(q[b, h, i], k[b, h, j]))"),
+    ("softmax not normalised", "/ e.sum()", "/ 1.0"),
+    ("reset keeps the state", "np.zeros_like(x[idx]) if lam[idx] == 0 else", "x[idx] if lam[idx] == 0 else"),
+    ("rescale by lambda squared", "(lam[idx] * x[idx]).astype(np.float32)", "(lam[idx] * lam[idx] * x[idx]).astype(np.float32)"),
+    ("gather reads the next state", "np.stack([flat[int(i)].copy() for i in index])",
+     "np.stack([flat[(int(i) + 1) % len(flat)].copy() for i in index])"),
+]
+SWA_STATE_PINS = [lambda: pins.test_swa_equals_banded_matrix_softmax(5), lambda: pins.test_swa_equals_banded_matrix_softmax(1),
+                  pins.test_swa_special_cases, pins.test_state_rescale_definition_and_reset,
+                  pins.test_state_rescale_feeds_the_recurrence_linearly, pins.test_state_gather_copies_and_branches]
+
+
+@pytest.mark.parametrize("name,old,new", SWA_STATE_MUTANTS, ids=[m[0] for m in SWA_STATE_MUTANTS])
+def test_window_and_state_pins_catch_planted_mistake(monkeypatch, name, old, new):
+    text = open(PY_SRC).read()
+    assert old in text, f"mutation anchor for '{name}' not found"
+    ns = {"__name__": "oracle_mutant", "__file__": PY_SRC}
+    exec(compile(text.replace(old, new, 1), "oracle_mutant", "exec"), ns)
+    for fn in ("swa", "state_rescale", "state_gather"):
+        monkeypatch.setattr(oracle, fn, ns[fn])
+    assert any(_caught(f) for f in SWA_STATE_PINS), f"no pin caught the planted mistake '{name}'"
