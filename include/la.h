@@ -161,10 +161,12 @@ typedef struct la_decode_args {
  *
  * Gated-delta-rule prefill (bf16 inputs) has two schedules:
  *   - two kernels (the fastest): a chunk-parallel kernel leaves one record
- *     of 74,240 bytes per 64-token chunk of every (b,h) (W, the decayed
- *     queries, P_o, the decay tables and U~ of the chunk), then a sequential
- *     chain per (b,h) consumes them; la_gdn_prefill_workspace_size returns
- *     what it needs;
+ *     of 16,384 bytes per 64-token chunk of every (b,h) (the bf16 images of
+ *     T diag(beta), T = (I + L)^{-1}, and of the chunk's causal queries
+ *     against its keys), then a warp-specialized scan per (b,h) reads q, k,
+ *     v and the record once and forms everything else;
+ *     la_gdn_prefill_workspace_size returns what it needs (plus the segment
+ *     scratch below when long sequences are split);
  *   - one kernel that walks the chunks of each (b,h) itself; it needs scratch
  *     only when it splits long sequences of few (b,h) pairs into segments
  *     (one 64 KiB fp32 map pair per segment but the last, one 64 KiB entry
@@ -212,9 +214,13 @@ la_status la_gated_prefill(const la_gdn_prefill_args* args, void* workspace,
  *     the one-kernel schedule.
  *   - Every GPU that loads the library holds the 16 MiB array until the
  *     process exits.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *   - The first call in each CUDA context looks up the array's device
+ *     address (cudaGetSymbolAddress, with that context's device current)
+ *     and caches it under the context's id; make that first call before
+ *     any stream capture.  A device reset (cudaDeviceReset, or anything
+ *     else that destroys and recreates the primary context) invalidates the
+ *     cached address: the next call then looks it up again, so the first
+ *     call after a reset must also come before any capture.
  *   - All calls share the one array and it keeps the last call's contents
  *     (nothing in it needs to start at zero).  Calls whose GPU work overlaps,
  *     e.g. on two streams at once, race on it: serialise them.
@@ -394,6 +400,16 @@ const char* la_status_string(la_status status);
 
 /* LA_ABI_VERSION of the built library. */
 int la_abi_version(void);
+
+/* The cudaError_t value (as an int) behind the most recent LA_ERR_CUDA that a
+ * call of this library returned to the calling thread; 0 if there was none.
+ * Thread-local, so calls from other threads do not overwrite it. */
+int la_last_cuda_error(void);
+
+/* The CUDA runtime's name of a cudaError_t value (e.g. from
+ * la_last_cuda_error), for callers that do not link the CUDA runtime
+ * themselves; never NULL. */
+const char* la_cuda_error_name(int code);
 
 #ifdef __cplusplus
 }

@@ -8,6 +8,14 @@
 #include "kernels.h"
 #include "la.h"
 
+namespace la {
+namespace {
+thread_local int t_last_cuda_error = 0;
+}  // namespace
+void note_cuda_error(int code) { t_last_cuda_error = code; }
+int last_cuda_error() { return t_last_cuda_error; }
+}  // namespace la
+
 namespace {
 
 // Device status word set by bounded waits that expire (LA_ERR_TIMEOUT).
@@ -46,7 +54,11 @@ bool valid_gate(const la_tensor& x, int64_t B, int64_t H, int64_t N) {
 
 la::View4 view(const la_tensor& x) { return la::View4{x.ptr, x.stride_b, x.stride_h, x.stride_t}; }
 
-la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+la_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return LA_OK;
+  la::note_cuda_error((int)e);
+  return LA_ERR_CUDA;
+}
 
 // N == 0: the final state is the initial state (or zero).
 la_status pass_state(float* out, const float* in, size_t n_floats, cudaStream_t s) {
@@ -115,13 +127,13 @@ la_status gdn_family_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_b
   const int64_t BH = a->B * a->H;
   if (BH == 0) return LA_OK;
   if (a->N == 0) return pass_state(a->S_out, a->S_in, (size_t)(BH * kGdnD * kGdnD), s);
-  // bf16: the two-kernel split when the workspace holds its chunk records,
-  // else the single-kernel scan, which needs the segment scratch only
+  // bf16: the two-kernel scan when the workspace holds its per-chunk inverse
+  // records, else the single-kernel scan, which needs the segment scratch only
   bool split = false;
   if (a->in_dtype == LA_DTYPE_BF16) {
     if (ws != nullptr && !aligned16(ws)) return LA_ERR_WORKSPACE;
     const int64_t nch = (a->N + 63) / 64;
-    split = ws != nullptr && ws_bytes >= la::gdn_split_workspace_bytes(a->B, a->H, a->N) && BH * nch <= INT32_MAX;
+    split = ws != nullptr && ws_bytes >= la::gdn_scan_workspace_bytes(a->B, a->H, a->N) && BH * nch <= INT32_MAX;
     const size_t need_min = la::gdn_segment_plan(a->B, a->H, a->N).ws_bytes;
     if (!split && need_min > 0 && (ws == nullptr || ws_bytes < need_min)) return LA_ERR_WORKSPACE;
   }
@@ -139,7 +151,7 @@ la_status gdn_family_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_b
   if (!L.in_bf16) return from_cuda(la::launch_gdn_prefill_recurrent(L, s));
   unsigned* status = device_status_ptr();
   if (!status) return LA_ERR_CUDA;
-  const cudaError_t e = split ? la::launch_gdn_prefill_split(L, ws, ws_bytes, status, s)
+  const cudaError_t e = split ? la::launch_gdn_prefill_scan(L, ws, ws_bytes, status, s)
                               : la::launch_gdn_prefill_chunked(L, ws, ws_bytes, status, s);
   if (e == cudaErrorInvalidValue) return LA_ERR_UNSUPPORTED;  // strides TMA cannot describe
   return from_cuda(e);
@@ -150,6 +162,13 @@ la_status gdn_family_prefill(const la_gdn_prefill_args* a, void* ws, size_t ws_b
 extern "C" {
 
 int la_abi_version(void) { return LA_ABI_VERSION; }
+
+int la_last_cuda_error(void) { return la::last_cuda_error(); }
+
+const char* la_cuda_error_name(int code) {
+  const char* n = cudaGetErrorName(static_cast<cudaError_t>(code));
+  return n ? n : "unknown CUDA error";
+}
 
 const char* la_status_string(la_status s) {
   switch (s) {
@@ -177,7 +196,7 @@ static bool gdn_chunked_shape(const la_gdn_prefill_args* a) {
 }
 
 size_t la_gdn_prefill_workspace_size(const la_gdn_prefill_args* a) {
-  return gdn_chunked_shape(a) ? la::gdn_split_workspace_bytes(a->B, a->H, a->N) : 0;
+  return gdn_chunked_shape(a) ? la::gdn_scan_workspace_bytes(a->B, a->H, a->N) : 0;
 }
 
 size_t la_gdn_prefill_workspace_size_min(const la_gdn_prefill_args* a) {

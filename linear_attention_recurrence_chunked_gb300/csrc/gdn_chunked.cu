@@ -565,16 +565,19 @@ cudaError_t launch_gdn_segment_combine(const float* S_in, const float* maps, flo
 
 // Number of sequence segments per (b,h).  With one CTA per SM, the three
 // launches cost about ceil(2 (G-1) BH / P) + ceil(G BH / P) waves of a
-// segment's length (P = 148 SMs assumed, so the plan does not depend on the
-// device), against ceil(BH / P) waves of the whole sequence for G = 1;
-// segments are used when they save at least 20 %, keep at least 32 chunks
-// each, and G stays <= 16 (the combine is sequential in G).
+// segment's length, against ceil(BH / P) waves of the whole sequence for
+// G = 1; segments are used when they save at least 20 %, keep at least 32
+// chunks each, and G stays <= 16 (the combine is sequential in G).  P is the
+// GB300's 152 SMs, a constant rather than a device query so that the
+// workspace queries answer from the problem's sizes alone (also on a host
+// without a GPU); on a part with fewer SMs the plan stays correct and only
+// its wave count is off.
 GdnSegPlan gdn_segment_plan(int64_t B, int64_t H, int64_t N) {
   GdnSegPlan p{1, N, 0};
   const int64_t BH = B * H;
   const int64_t nchunks = (N + kC - 1) / kC;
   if (BH <= 0 || N <= 0) return p;
-  constexpr int64_t P = 148, kMinSegChunks = 32, kMaxG = 16;
+  constexpr int64_t P = 152, kMinSegChunks = 32, kMaxG = 16;
   auto waves = [&](int64_t ctas) { return (ctas + P - 1) / P; };
   const double whole = (double)waves(BH);
   double best = whole;

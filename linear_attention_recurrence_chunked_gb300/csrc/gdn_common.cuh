@@ -1,6 +1,6 @@
 // gdn_common.cuh -- pieces shared by the two schedules of the chunked
 // gated-delta-rule prefill: the single-kernel chunk scan (gdn_chunked.cu) and
-// the two-kernel split (gdn_split.cu).  Sizes, the per-launch task of the
+// the two-kernel scan (gdn_scan.cu).  Sizes, the per-launch task of the
 // sequence-segment scheme, and the chunk-local phases of the chunk form
 // (NoteBank Sec. 2 Eq. (1), A_t = alpha_t (I - beta_t k_t k_t^T)):
 //   g_r = sum_{j<=r} log alpha_j,  gamma_r = e^{g_r},  Gamma_rj = e^{g_r - g_j}
@@ -152,9 +152,11 @@ __device__ __forceinline__ void mma_wu(uint32_t d_w, uint32_t d_ut, uint32_t kq_
 // of one chunk from [K;Q] K^T in TMEM.  delta = 0 is the scalar gate
 // (A_t = alpha_t I): nothing is erased, so L = 0 (T = I, U~ = diag(beta) V)
 // here and W = 0 in phase_T.  kq_taddr: this thread's lane at the first of
-// its 32 columns; gate: the chunk's gate tables.
+// its 32 columns; gate: the chunk's gate tables.  A null po_tile skips P_o
+// (the lanes of the Q rows then do nothing); po_row_gamma = false leaves out
+// the row factor gamma_r (P_rj = po_scale (q_r . k_j) / gamma_j, j <= r).
 __device__ __forceinline__ void phase_L_Po(uint32_t kq_taddr, int row, int half, const float* gate, float* Lsm,
-                                           uint8_t* po_tile, float po_scale, float delta) {
+                                           uint8_t* po_tile, float po_scale, float delta, bool po_row_gamma = true) {
   float v[32];
   ld32(kq_taddr, v);
   const int j0 = 32 * half;
@@ -167,9 +169,9 @@ __device__ __forceinline__ void phase_L_Po(uint32_t kq_taddr, int row, int half,
     float* Lrow = Lsm + r * kLStride + j0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) Lrow[j] = (j0 + j < r) ? f * gi[j0 + j] * v[j] : 0.f;
-  } else {
+  } else if (po_tile != nullptr) {
     const int r = row - kC;
-    const float f = gm[r] * po_scale;
+    const float f = (po_row_gamma ? gm[r] : 1.f) * po_scale;
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = (j0 + j <= r) ? f * gi[j0 + j] * v[j] : 0.f;
 #pragma unroll

@@ -1,0 +1,877 @@
+// gdn_scan.cu -- the chunked gated-delta-rule prefill as a chunk-parallel
+// inversion kernel and a warp-specialized scan that reads q, k, v once.
+//
+// Chunk form (gdn_common.cuh; NoteBank Sec. 2 Eq. (1), the state carried
+// across chunk boundaries as in NoteBank Sec. 3.2), chunk of 64 tokens with
+// incoming state S0:
+//   T  = (I + L)^{-1},  L = strict_lower(diag(beta) (Gamma . K K^T))
+//   W  = T diag(beta gamma) K,  U~ = T diag(beta) V,  U = U~ - W S0^T
+//   O  = q_scale diag(gamma) (Q S0^T + P U),  P_rj = (q_r . k_j) / gamma_j  (j <= r)
+//   S_C = gamma_C S0 + U^T diag(gamma_C / gamma) K
+//
+// Kernel 1 (gdn_tinv_kernel, one CTA per chunk over the whole GPU) forms what
+// needs the inversion or the chunk's queries against its keys, neither of which
+// depends on the state: the bf16 tiles T2 = T diag(beta) and P of every chunk
+// (16 KB, the images the scan's MMAs read), written to the caller's workspace.
+//
+// Kernel 2 (gdn_scan_kernel, one CTA per (b,h) or sequence segment) walks the
+// chunks with the fp32 state in tensor memory and does everything else on
+// the tcgen05 tensor cores, from tiles it loads once:
+//   b:  W^T = K^T (T2 diag gamma)^T,  U~^T = V^T T2^T          (chunk-local)
+//   x:  X = S0 W^T                                             (the state path)
+//   y:  Y = S0 Q^T                                             (outputs)
+//   e:  S~ += (U diag(1 / (sigma gamma)))^T K                  (the state update)
+//   d:  Y += U^T P^T  (the chunk's outputs, O^T = q_scale Y diag(gamma))
+// The state is held as S~ = S / sigma, sigma the running product of the
+// chunk decays gamma_C (folded back into S~ whenever it drops below 2^-32):
+// the decay then enters only through a scale of U's columns, and the update
+// S~ += (U diag(1 / (sigma gamma)))^T K takes the raw K tile.
+//
+// Roles (17 warps): warps 0-7 own the state rows (two threads per row) and
+// run the passes on the sequential path, U = U~ - X and the bf16 copy S0 of
+// the state after each update; warps 8-11 run the chunk-local passes a chunk
+// ahead (gates, T2 diag gamma, W^T from tensor memory); warps 12-15 drain
+// the outputs; warp 16 issues every copy and MMA as soon as its inputs are
+// ready.  Workers report progress through counters the issuer reads with one
+// round of loads; waits on copies and MMAs are mbarriers, and every wait is
+// bounded.
+#include <mutex>
+
+#include "gdn_common.cuh"
+
+namespace la {
+namespace {
+using namespace tc;
+using namespace gdn;
+
+// Per-chunk record written by kernel 1 (bf16 tile images, 128-byte swizzle, exactly as the scan's
+// MMAs read them): T2 = T diag(beta) [64 r][64 j], then P [64 r][64 j], P_rj = (q_r . k_j) / gamma_j
+// for j <= r (0 above the diagonal).
+constexpr uint32_t kRecT2 = 0, kRecP = 8192, kRec = 16384;
+
+// ============================================================================ kernel 1
+// Shared memory: the [K;Q] tile (K rows 0-63, Q rows 64-127) for one M=128 MMA giving K K^T and
+// Q K^T; L, block products and gate tables.  Once the MMA is done the tile is dead: T (fp32, rows
+// padded to 68 floats so that a column read across rows spreads over the banks) takes its first
+// 17 KB and the P image its last 8 KB; the T2 image goes over L.
+constexpr uint32_t kIOffKQ = 0;
+constexpr uint32_t kIOffL = 32768;
+constexpr uint32_t kIOffZ = kIOffL + 64 * 65 * 4;
+constexpr uint32_t kIOffGate = kIOffZ + 4096;
+constexpr uint32_t kISmemUsed = kIOffGate + 1024;
+constexpr uint32_t kISmemAlloc = kISmemUsed + 1024;
+constexpr int kTPad = 68;                             // fp32 T row stride
+constexpr uint32_t kIOffT = kIOffKQ;                  // [64][68] fp32 (17408 B)
+constexpr uint32_t kIOffP = kIOffKQ + 24576;          // P image (8 KB)
+constexpr uint32_t kIOffT2 = kIOffL;                  // T2 image (8 KB) over L
+static_assert(64 * kTPad * 4 <= 24576, "T fits below the P image");
+static_assert(4 * (kISmemAlloc + 1024) <= 233472, "four inversion CTAs per SM");
+
+// T = (I + L)^{-1} by doubling, then the bf16 image T diag(beta).  16x16 diagonal blocks by
+// forward substitution (threads 0..63, one column each); then 32x32 and 64x64 blocks from
+// [[A, 0], [C, B]]^{-1} = [[A^{-1}, 0], [-B^{-1} C A^{-1}, B^{-1}]].  Lsm: fp32 [64][65]
+// strictly lower L; Tsm: fp32 [64][kTPad]; Zsm: 1024 fp32 of block products; bt: beta[64].
+// Every thread of the block calls it; it contains block-wide barriers, and L is no longer read
+// once the last one has passed (the T2 image may overlay it).
+__device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, float* Zsm, const float* bt,
+                                         uint8_t* t2_tile) {
+  if (tid < kC) {
+    const int base = (tid >> 4) * 16, col = tid & 15;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) x[r] = (r == col) ? 1.f : 0.f;
+#pragma unroll
+    for (int j = 0; j < 15; ++j) {
+      const float* Lc = Lsm + (base + j + 1) * kLStride + base + j;
+#pragma unroll
+      for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-Lc[(r - j - 1) * kLStride], x[j], x[r]);
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Tsm[(base + r) * kTPad + base + col] = x[r];
+  } else {
+    // the blocks above the 16x16 block diagonal are zero
+    for (int e = tid - kC; e < kC * kC; e += kThreads - kC) {
+      const int r = e >> 6, c = e & 63;
+      if ((c >> 4) > (r >> 4)) Tsm[r * kTPad + c] = 0.f;
+    }
+  }
+  __syncthreads();
+  {
+    // 32x32 blocks k = 0, 1: rows R = 32k + 16.., columns Cb = 32k..; thread: 2 columns of one row
+    const int k = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
+    const int R = 32 * k + 16, Cb = 32 * k;
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      const float l = Lsm[(R + r) * kLStride + Cb + m];
+      const float2 t = *reinterpret_cast<const float2*>(Tsm + (Cb + m) * kTPad + Cb + c0);
+      z0 = fmaf(l, t.x, z0);
+      z1 = fmaf(l, t.y, z1);
+    }
+    *reinterpret_cast<float2*>(Zsm + k * 256 + r * 16 + c0) = make_float2(z0, z1);
+    __syncthreads();
+    float t0v = 0.f, t1v = 0.f;
+    const float* tr = Tsm + (R + r) * kTPad;
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      const float tv = tr[R + p];
+      const float2 zz = *reinterpret_cast<const float2*>(Zsm + k * 256 + p * 16 + c0);
+      t0v = fmaf(tv, zz.x, t0v);
+      t1v = fmaf(tv, zz.y, t1v);
+    }
+    *reinterpret_cast<float2*>(Tsm + (R + r) * kTPad + Cb + c0) = make_float2(-t0v, -t1v);
+  }
+  __syncthreads();
+  {
+    // 64x64: rows 32.., columns 0..31; thread: 4 columns of one row
+    const int r = tid >> 3, c0 = (tid & 7) * 4;
+    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int m = 0; m < 32; ++m) {
+      const float l = Lsm[(32 + r) * kLStride + m];
+      const float4 tv = *reinterpret_cast<const float4*>(Tsm + m * kTPad + c0);
+      z.x = fmaf(l, tv.x, z.x); z.y = fmaf(l, tv.y, z.y); z.z = fmaf(l, tv.z, z.z); z.w = fmaf(l, tv.w, z.w);
+    }
+    *reinterpret_cast<float4*>(Zsm + r * 32 + c0) = z;
+    __syncthreads();
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* tr = Tsm + (32 + r) * kTPad;
+#pragma unroll 8
+    for (int p = 0; p < 32; ++p) {
+      const float tv = tr[32 + p];
+      const float4 zz = *reinterpret_cast<const float4*>(Zsm + p * 32 + c0);
+      o.x = fmaf(tv, zz.x, o.x); o.y = fmaf(tv, zz.y, o.y); o.z = fmaf(tv, zz.z, o.z); o.w = fmaf(tv, zz.w, o.w);
+    }
+    *reinterpret_cast<float4*>(Tsm + (32 + r) * kTPad + c0) = make_float4(-o.x, -o.y, -o.z, -o.w);
+  }
+  __syncthreads();
+  {
+    // T2 = T diag(beta): thread r = tid / 4, 16 columns from c0
+    const int r = tid >> 2, c0 = (tid & 3) * 16;
+    const float* tr = Tsm + r * kTPad + c0;
+    float t2[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 tv = *reinterpret_cast<const float4*>(tr + 4 * q);
+      t2[4 * q] = tv.x * bt[c0 + 4 * q];
+      t2[4 * q + 1] = tv.y * bt[c0 + 4 * q + 1];
+      t2[4 * q + 2] = tv.z * bt[c0 + 4 * q + 2];
+      t2[4 * q + 3] = tv.w * bt[c0 + 4 * q + 3];
+    }
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      *reinterpret_cast<uint4*>(t2_tile + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t2 + 8 * q);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 4)
+gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                const GdnPrefillLaunch a, int nch, uint8_t* rec_out, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_tma;
+  __shared__ uint64_t bar_mma;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ float carry;
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int row = tid & 127, half = tid >> 7;
+  const int64_t rec = blockIdx.x;
+  const int64_t bh = rec / nch;
+  const int c = (int)(rec % nch);
+  const int b = (int)(bh / a.H), h = (int)(bh % a.H);
+  const int64_t t0 = (int64_t)c * kC;
+  const uint32_t sbase = smem_u32(sm);
+  float* gate = reinterpret_cast<float*>(sm + kIOffGate);
+  float* Lsm = reinterpret_cast<float*>(sm + kIOffL);
+  float* Zsm = reinterpret_cast<float*>(sm + kIOffZ);
+  float* Tsm = reinterpret_cast<float*>(sm + kIOffT);
+  uint8_t* rp = rec_out + rec * kRec;
+
+  float al = 1.f, bt = 0.f;
+  if (tid < kC && t0 + tid < a.N) {
+    al = a.alpha[b * a.a_sb + h * a.a_sh + t0 + tid];
+    bt = a.beta[b * a.b_sb + h * a.b_sh + t0 + tid];
+  }
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar_tma), 1);
+    mbar_init(smem_u32(&bar_mma), 1);
+    fence_mbar_init();
+    const uint32_t bar = smem_u32(&bar_tma);
+    mbar_arrive_expect_tx(bar, 32768);
+    tma_load_4d(sbase + kIOffKQ + 0, &tmap_k, 0, (int)t0, h, b, bar);
+    tma_load_4d(sbase + kIOffKQ + 16384, &tmap_k, 64, (int)t0, h, b, bar);
+    tma_load_4d(sbase + kIOffKQ + 8192, &tmap_q, 0, (int)t0, h, b, bar);
+    tma_load_4d(sbase + kIOffKQ + 24576, &tmap_q, 64, (int)t0, h, b, bar);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base_sh), 64);
+    tmem_relinquish();
+  }
+  gate_tables(tid, logf(al), bt, gate, &carry);  // padded tokens: alpha = 1, beta = 0
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+
+  // Every thread waits on the barriers itself (sleeping in hardware).
+  bool ok = true, tma_waited = false, mma_pending = false;
+  do {
+    ok = mbar_wait(smem_u32(&bar_tma), 0, status);
+    tma_waited = ok;
+    if (__syncthreads_or(!ok)) break;
+    if (tid == 0) {
+      tc_fence_after();
+      mma_kq(tmem, sbase + kIOffKQ);
+      mma_commit(smem_u32(&bar_mma));
+    }
+    mma_pending = true;
+    ok = mbar_wait(smem_u32(&bar_mma), 0, status);
+    if (__syncthreads_or(!ok)) break;
+    mma_pending = false;
+    tc_fence_after();
+    // L (rows of K K^T) into shared memory, P (rows of Q K^T) into its image
+    phase_L_Po(tlane + 32 * half, row, half, gate, Lsm, sm + kIOffP, 1.f, a.delta, false);
+    tc_fence_before();
+    __syncthreads();
+    invert_T(tid, Lsm, Tsm, Zsm, gate + kC, sm + kIOffT2);
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(rp + kRecT2, sbase + kIOffT2, 8192);
+      bulk_store(rp + kRecP, sbase + kIOffP, 8192);
+      bulk_commit();
+      bulk_wait_read();
+    }
+  } while (false);
+
+  if (!ok && tid == 0) {
+    if (!tma_waited) mbar_wait(smem_u32(&bar_tma), 0, status);
+    if (mma_pending) mbar_wait(smem_u32(&bar_mma), 0, status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+// ============================================================================ kernel 2
+// Shared memory (offsets from a 1024-byte aligned base), two rings of two
+// slots by chunk parity:
+//   early slot (free once the chunk's state update is done): K [64 r][128 k],
+//       V [64][128], the T2 image;
+//   late slot (free once the chunk's state update and outputs are done):
+//       W^T [128 k][64 r] (rows k, the r contiguous: an MN-major operand),
+//       Q [64 r][128 k], the P image.
+// The bf16 copy S0 of the state is the A operand of x and y straight from
+// tensor memory.
+constexpr uint32_t kEarly = 40960;                    // one early slot
+constexpr uint32_t kEOffK = 0, kEOffV = 16384, kEOffT2 = 32768;
+constexpr uint32_t kLate = 40960;                     // one late slot
+constexpr uint32_t kLOffWT = 0, kLOffQ = 16384, kLOffP = 32768;
+constexpr uint32_t kSOffEarly = 0;
+constexpr uint32_t kSOffLate = 2 * kEarly;            // 81920
+constexpr uint32_t kSOffT1 = kSOffLate + 2 * kLate;   // T2 diag(gamma), one buffer
+constexpr uint32_t kSOffU = kSOffT1 + 8192;           // U^T [128 i][64 r]
+constexpr uint32_t kSOffUD = kSOffU + 16384;          // U^T diag(1 / (sigma gamma)) [128 i][64 r]
+constexpr uint32_t kSOffGate = kSOffUD + 16384;       // gate slots
+constexpr int kGateSlots = 8;
+constexpr uint32_t kGateSlot = 576;                   // gamma[64], 1/(sigma gamma)[64], scalars
+constexpr uint32_t kSSmemUsed = kSOffGate + kGateSlots * kGateSlot;
+constexpr uint32_t kSSmemAlloc = kSSmemUsed + 1024;
+static_assert(kEarly % 1024 == 0 && kLate % 1024 == 0 && kSOffLate % 1024 == 0 && kSOffT1 % 1024 == 0 &&
+                  kSOffU % 1024 == 0 && kSOffUD % 1024 == 0,
+              "MMA operand tiles sit on 1024-byte boundaries");
+static_assert(kSSmemAlloc + 512 <= 232448, "shared memory budget");
+// gate slot layout (floats)
+constexpr int kGGam = 0, kGKds = 64, kGSig = 128, kGSigAfter = 129, kGFold = 130;
+
+// tensor-memory columns
+constexpr uint32_t kTS = 0;     // S~ [i][k], fp32
+constexpr uint32_t kTS0 = 128;  // S0 = bf16(sigma S~) [i][k], two per column (64 columns)
+constexpr uint32_t kTX = 192;   // X [i][r]
+constexpr uint32_t kTY = 256;   // Y [i][r]
+constexpr uint32_t kTU = 320;   // U~^T [i][r], two buffers (320..383, 384..447)
+constexpr uint32_t kTW = 448;   // W^T [k][r]
+constexpr uint32_t kTCols = 512;
+
+constexpr int kStateWarps = 8, kLocalWarps = 4, kOutWarps = 4;
+constexpr int kLocal0 = kStateWarps * 32;            // first local thread
+constexpr int kOut0 = kLocal0 + kLocalWarps * 32;    // first output thread
+constexpr int kIssuer0 = kOut0 + kOutWarps * 32;     // the MMA issuer warp
+constexpr int kLoader0 = kIssuer0 + 32;              // the copy issuer warp
+constexpr int kScanThreads = kLoader0 + 32;
+constexpr int kLocalBar = 1;                         // named barrier of the local warps
+constexpr int kSigT1 = 0, kSigWK = 1, kSigU = 2, kSigS0 = 3, kSigOfree = 4;
+constexpr float kFoldBelow = 2.3283064e-10f;         // 2^-32
+
+// One CTA per SM (shared memory and all 512 tensor-memory columns).  Warps
+// take registers in groups of four, so the 18 warps are budgeted as 20: at
+// most 96 registers a thread; the wide passes work on 32 columns at a time.
+template <typename TOut>
+__global__ void __launch_bounds__(kScanThreads, 1)
+gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                const __grid_constant__ CUtensorMap tmap_v, const GdnPrefillLaunch a, const GdnTask task,
+                int nch_total, const uint8_t* rec, unsigned* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_kv[2];     // early slot landed: K, V, the T2 image
+  __shared__ uint64_t bar_q[2];      // Q and the P image landed in the late slot
+  __shared__ uint64_t bar_b;         // W^T, U~^T computed
+  __shared__ uint64_t bar_x;         // X computed
+  __shared__ uint64_t bar_e;         // state update done
+  __shared__ uint64_t bar_o;         // Y += U^T P^T done: the chunk's outputs are complete
+  __shared__ uint64_t bar_gate[kGateSlots];
+  __shared__ uint64_t bar_fin;
+  // Worker -> issuer hand-offs, one count per warp per chunk: T2 diag(gamma) written (kSigT1), W^T
+  // written with Q and P landed (kSigWK), by the local warps; U^T written (kSigU), S0 written
+  // (kSigS0), by the state warps; Y read (kSigOfree), by the output warps.
+  __shared__ uint32_t sig[8];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ float lshare[2];        // local warps: scan carry, gamma_C
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const CtaWork wk = cta_work(a, task);
+  const int b = wk.b, h = wk.h;
+  const int n = wk.nchunks;
+  const bool WOUT = wk.write_out, ZV = wk.zero_v;
+  const int64_t rec0 = wk.bh * nch_total + wk.t_begin / kC;
+  const uint32_t sb = smem_u32(sm);
+  auto slot = [&](int c) { return reinterpret_cast<float*>(sm + kSOffGate + (uint32_t)(c % kGateSlots) * kGateSlot); };
+  auto gate_par = [&](int c) { return (uint32_t)((c / kGateSlots) & 1); };
+  auto early = [&](int c) { return kSOffEarly + (uint32_t)(c & 1) * kEarly; };
+  auto late = [&](int c) { return kSOffLate + (uint32_t)(c & 1) * kLate; };
+  auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(smem_u32(bar), parity, status); };
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_kv[i]), 1);
+      mbar_init(smem_u32(&bar_q[i]), 1);
+    }
+    mbar_init(smem_u32(&bar_b), 1);
+    mbar_init(smem_u32(&bar_x), 1);
+    mbar_init(smem_u32(&bar_e), 1);
+    mbar_init(smem_u32(&bar_o), 1);
+    for (int i = 0; i < kGateSlots; ++i) mbar_init(smem_u32(&bar_gate[i]), kLocalWarps);
+    mbar_init(smem_u32(&bar_fin), 1);
+    for (int i = 0; i < 8; ++i) sig[i] = 0u;
+    fence_mbar_init();
+    tma_prefetch_desc(&tmap_k);
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_v);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&tmem_base_sh), kTCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lane quarter
+
+  if (warp == kIssuer0 / 32) {
+    // ======================================================================= MMA issuer
+    // One warp issues every MMA as soon as its inputs are ready: each round it reads the workers'
+    // progress counters (independent loads, one round trip), then issues in the order x, y, e, b, d.  An MMA for chunk m is issued only after every MMA that must precede it
+    // in the tensor pipe (which runs them in issue order).  All 32 lanes walk the loop together;
+    // lane 0 alone issues.
+    const bool leader = (tid & 31) == 0;
+    int nb = 0, nx = 0, ny = 0, ne = 0, nd = 0;
+    const uint32_t id64 = idesc_bf16(128, 64, 0, 0);
+    const uint32_t id64t = idesc_bf16(128, 64, 1, 0);    // A MN-major
+    const uint32_t id64n = idesc_bf16(128, 64, 0, 1);    // B MN-major
+    const uint32_t id128n = idesc_bf16(128, 128, 0, 1);  // B MN-major
+    bool ok = true, mma_issued = false;
+    uint64_t t_idle = 0;
+    uint32_t idle = 0;  // rounds without progress since the last issue
+    while (ok && (ne < n || (WOUT && nd < n))) {
+      bool prog = false;
+      // Progress counters (chunks every warp of a group has finished), read afresh right before the
+      // check that uses them.
+      auto prog_t1 = [&]() { return (int)(sig_load(smem_u32(&sig[kSigT1])) / kLocalWarps); };  // also: early slot landed
+      auto prog_wk = [&]() { return (int)(sig_load(smem_u32(&sig[kSigWK])) / kLocalWarps); };  // also: Q and P landed
+      auto prog_u = [&]() { return (int)(sig_load(smem_u32(&sig[kSigU])) / kStateWarps); };
+      auto prog_s0 = [&]() { return (int)(sig_load(smem_u32(&sig[kSigS0])) / kStateWarps); };
+      auto prog_of = [&]() { return (int)(sig_load(smem_u32(&sig[kSigOfree])) / kOutWarps); };
+      // ---- x: X = S0 W^T (the state path); U of the chunk before is no longer read after it
+      if (nx < n && nx < nb && (!WOUT || nd >= nx) && prog_s0() >= nx + 1 && prog_wk() >= nx + 1) {
+        if (leader) {
+          tc_fence_after();
+          const uint32_t wt = sb + late(nx) + kLOffWT;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_bf16_ts(tmem + kTX, tmem + kTS0 + 8u * (uint32_t)ks, sw128_desc(wt + ks * 2048, 0, 1024), id64n,
+                        ks > 0);
+          mma_commit(smem_u32(&bar_x));
+        }
+        __syncwarp();
+        mma_issued = true;
+        ++nx;
+        prog = true;
+      }
+      // ---- y: Y = S0 Q^T, once the outputs of the chunk before are drained
+      if (WOUT && ny < nx && (ny == 0 || prog_of() >= ny)) {
+        if (leader) {
+          tc_fence_after();
+          const uint32_t qt = sb + late(ny) + kLOffQ;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u;
+            mma_bf16_ts(tmem + kTY, tmem + kTS0 + 8u * (uint32_t)ks, kmaj(qt + off), id64, ks > 0);
+          }
+        }
+        __syncwarp();
+        ++ny;
+        prog = true;
+      }
+      // ---- e: S~ += UD^T K (the state path); after y, which reads the S0 the update replaces
+      if (ne < nx && (!WOUT || ny > ne) && prog_u() >= ne + 1) {
+        if (leader) {
+          tc_fence_after();
+          const uint32_t kt = sb + early(ne) + kEOffK;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + kTS, kmaj(sb + kSOffUD + ks * 32), sw128_desc(kt + ks * 2048, 8192, 1024), id128n, 1u);
+          mma_commit(smem_u32(&bar_e));
+        }
+        __syncwarp();
+        ++ne;
+        prog = true;
+      }
+      // ---- b: W^T = K^T T1^T, U~^T = V^T T2^T (chunk-local).  Needs T1 (so the early slot landed),
+      // W^T of the chunk before read, its U~ buffer read (U of chunk m-2) and the late slot free,
+      // since W^T is written there next.
+      if (nb < n && prog_t1() >= nb + 1 && (nb == 0 || prog_wk() >= nb) &&
+          (nb < 2 || (prog_u() >= nb - 1 && prog_s0() >= nb && (!WOUT || prog_of() >= nb - 1)))) {
+        if (leader) {
+          tc_fence_after();
+          const uint32_t es = sb + early(nb);
+          const uint32_t t1 = sb + kSOffT1;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + kTW, sw128_desc(es + kEOffK + ks * 2048, 8192, 1024), kmaj(t1 + ks * 32), id64t, ks > 0);
+          if (!ZV) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16(tmem + kTU + 64u * (uint32_t)(nb & 1), sw128_desc(es + kEOffV + ks * 2048, 8192, 1024),
+                       kmaj(es + kEOffT2 + ks * 32), id64t, ks > 0);
+          }
+          mma_commit(smem_u32(&bar_b));
+        }
+        __syncwarp();
+        mma_issued = true;
+        ++nb;
+        prog = true;
+      }
+      // ---- d: Y += U^T P^T
+      if (WOUT && nd < ne) {
+        if (leader) {
+          tc_fence_after();
+          const uint32_t pp = sb + late(nd) + kLOffP;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + kTY, kmaj(sb + kSOffU + ks * 32), kmaj(pp + ks * 32), id64, 1u);
+          mma_commit(smem_u32(&bar_o));
+        }
+        __syncwarp();
+        ++nd;
+        prog = true;
+      }
+      // idle-time limit, measured on the global timer every 4096 rounds without progress
+      if (prog) {
+        idle = 0;
+      } else if ((++idle & 4095u) == 0) {
+        const uint64_t now = __shfl_sync(kFullMask, globaltimer_ns(), 0);
+        if (idle == 4096u) {
+          t_idle = now;
+        } else if (now - t_idle > kWaitLimitNs) {
+          if (leader) atomicOr(status, kStatusTimeout);
+          ok = false;
+        }
+      }
+    }
+    if (!ok) {
+      // let this CTA's own MMAs finish (bounded) before tensor memory is freed
+      if (mma_issued) {
+        if (leader) mma_commit(smem_u32(&bar_fin));
+        __syncwarp();
+        mbar_wait(smem_u32(&bar_fin), 0, status);
+      }
+    }
+  } else if (warp == kLoader0 / 32) {
+    // ======================================================================= copy issuer
+    // One warp issues the copies of every chunk into its ring slot as soon as the slot is free
+    // (read from the same progress counters); lane 0 alone issues.
+    const bool leader = (tid & 31) == 0;
+    int nkv = 0, nq = 0;
+    bool ok = true;
+    uint64_t t_idle = 0;
+    uint32_t idle = 0;
+    while (ok && (nkv < n || (WOUT && nq < n))) {
+      bool prog = false;
+      const int o_s0 = (int)(sig_load(smem_u32(&sig[kSigS0])) / kStateWarps);
+      const int o_of = (int)(sig_load(smem_u32(&sig[kSigOfree])) / kOutWarps);
+      // ---- copies.  Early slot of chunk m: the update of chunk m-2 is done (S0 of chunk m-1 written
+      // after it).  Late slot: that and the outputs (Y drained) of chunk m-2.
+      if (nkv < n && (nkv < 2 || o_s0 >= nkv)) {
+        if (leader) {
+          const uint32_t es = sb + early(nkv);
+          const uint32_t bar = smem_u32(&bar_kv[nkv & 1]);
+          const int t0 = (int)(wk.t_begin + (int64_t)nkv * kC);
+          mbar_arrive_expect_tx(bar, 16384u + (ZV ? 0u : 16384u) + 8192u);
+          tma_load_4d(es + kEOffK + 0, &tmap_k, 0, t0, h, b, bar);
+          tma_load_4d(es + kEOffK + 8192, &tmap_k, 64, t0, h, b, bar);
+          if (!ZV) {
+            tma_load_4d(es + kEOffV + 0, &tmap_v, 0, t0, h, b, bar);
+            tma_load_4d(es + kEOffV + 8192, &tmap_v, 64, t0, h, b, bar);
+          }
+          bulk_load(es + kEOffT2, rec + (rec0 + nkv) * kRec + kRecT2, 8192, bar);
+        }
+        __syncwarp();
+        ++nkv;
+        prog = true;
+      }
+      if (WOUT && nq < n && (nq < 2 || (o_s0 >= nq && o_of >= nq - 1))) {
+        if (leader) {
+          const uint32_t ls = sb + late(nq);
+          const uint32_t bar = smem_u32(&bar_q[nq & 1]);
+          const int t0 = (int)(wk.t_begin + (int64_t)nq * kC);
+          mbar_arrive_expect_tx(bar, 16384u + 8192u);
+          tma_load_4d(ls + kLOffQ + 0, &tmap_q, 0, t0, h, b, bar);
+          tma_load_4d(ls + kLOffQ + 8192, &tmap_q, 64, t0, h, b, bar);
+          bulk_load(ls + kLOffP, rec + (rec0 + nq) * kRec + kRecP, 8192, bar);
+        }
+        __syncwarp();
+        ++nq;
+        prog = true;
+      }
+      if (prog) {
+        idle = 0;
+      } else if ((++idle & 4095u) == 0) {
+        const uint64_t now = __shfl_sync(kFullMask, globaltimer_ns(), 0);
+        if (idle == 4096u) {
+          t_idle = now;
+        } else if (now - t_idle > kWaitLimitNs) {
+          if (leader) atomicOr(status, kStatusTimeout);
+          ok = false;
+        }
+      }
+    }
+    // let this CTA's own copies land (bounded) before the CTA exits; a buffer's phases complete in
+    // order, so waiting for its last issued load covers the earlier ones
+    for (int m = nkv - 2; m < nkv; ++m)
+      if (m >= 0) mbar_wait(smem_u32(&bar_kv[m & 1]), (uint32_t)((m >> 1) & 1), status);
+    for (int m = nq - 2; m < nq; ++m)
+      if (m >= 0) mbar_wait(smem_u32(&bar_q[m & 1]), (uint32_t)((m >> 1) & 1), status);
+  } else if (tid < kLocal0) {
+    // ======================================================================= state warps
+    // lane i = state row i; this thread: state columns [64 half, +64), U columns [32 half, +32)
+    const int row = tid & 127, half = tid >> 7;
+    bool ok = true;  // an expired wait skips this thread's later waits; every arrival is still made
+    // S0 = bf16(v) for this thread's 64 state columns: packed columns [32 half, +32) of kTS0
+    auto store_s0 = [&](const float* v) {
+#pragma unroll
+      for (int c0 = 0; c0 < 32; c0 += 16) {
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j] = pack2_bf16(v[2 * (c0 + j)], v[2 * (c0 + j) + 1]);
+        tmem_st16u(tlane + kTS0 + 32 * half + c0, w);
+      }
+    };
+    {
+      const float* src = wk.s_entry ? wk.s_entry + (int64_t)row * kD + 64 * half : nullptr;
+      float v[64];
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        const float4 x = src ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[j] = x.x; v[j + 1] = x.y; v[j + 2] = x.z; v[j + 3] = x.w;
+      }
+      if (ZV) {  // identity entry state: the run then yields the segment's linear map
+#pragma unroll
+        for (int j = 0; j < 64; ++j) v[j] = (64 * half + j == row) ? 1.f : 0.f;
+      }
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 16)
+        tmem_st16(tlane + kTS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+      store_s0(v);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    warp_signal(smem_u32(&sig[kSigS0]));
+    ok = wait(&bar_gate[0], 0);  // the gates of a chunk are waited for a chunk ahead, off the sequential path
+    float sigma = 1.f;  // S = sigma S~ after the latest update
+    for (int c = 0; c < n; ++c) {
+      const uint32_t par = (uint32_t)(c & 1);
+      // ---- U^T = U~^T - X and U^T diag(1 / (sigma gamma)), this row, columns [32 half, +32)
+      ok = ok && wait(&bar_x, par);
+      tc_fence_after();
+      {
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {  // 16 columns at a time
+          const int c0 = 32 * half + 16 * part;
+          float kd[16];  // 1/(sigma gamma_r) of these columns, loaded ahead of the tensor memory
+          const float4* kds = reinterpret_cast<const float4*>(slot(c) + kGKds + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 f = kds[q];
+            kd[4 * q] = f.x; kd[4 * q + 1] = f.y; kd[4 * q + 2] = f.z; kd[4 * q + 3] = f.w;
+          }
+          float x[16], u[16];
+          tmem_ld16(tlane + kTX + c0, x);
+          if (!ZV) tmem_ld16(tlane + kTU + 64 * par + c0, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) u[j] = (ZV ? 0.f : u[j]) - x[j];
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            *reinterpret_cast<uint4*>(sm + kSOffU + sw128_off(row, c0 + 8 * q, 128)) = pack8_bf16(u + 8 * q);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) u[j] *= kd[j];
+#pragma unroll
+          for (int q = 0; q < 2; ++q)
+            *reinterpret_cast<uint4*>(sm + kSOffUD + sw128_off(row, c0 + 8 * q, 128)) = pack8_bf16(u + 8 * q);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      warp_signal(smem_u32(&sig[kSigU]));
+      // ---- after the update: S0 of chunk c+1 = sigma' S~, folding sigma' into S~ when small
+      ok = ok && wait(&bar_e, par);
+      tc_fence_after();
+      const float* gs = slot(c);
+      const float sig_after = gs[kGSigAfter];
+      const bool fold = gs[kGFold] != 0.f;
+      const bool has_next = c + 1 < n;
+      if (has_next || fold) {
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {  // 32 state columns at a time
+          const uint32_t col = 64 * half + 32 * part;
+          float v[32];
+          tmem_ld16(tlane + kTS + col, *reinterpret_cast<float(*)[16]>(v));
+          tmem_ld16(tlane + kTS + col + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= sig_after;
+          if (has_next) {
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = pack2_bf16(v[2 * j], v[2 * j + 1]);
+            tmem_st16u(tlane + kTS0 + col / 2, w);
+          }
+          if (fold) {
+            tmem_st16(tlane + kTS + col, *reinterpret_cast<float(*)[16]>(v));
+            tmem_st16(tlane + kTS + col + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+          }
+        }
+        tmem_st_wait();
+      }
+      sigma = fold ? 1.f : sig_after;
+      if (has_next) {
+        tc_fence_before();
+        warp_signal(smem_u32(&sig[kSigS0]));
+        ok = ok && wait(&bar_gate[(c + 1) % kGateSlots], gate_par(c + 1));
+      }
+    }
+    ok = __all_sync(kFullMask, ok);  // warp-uniform: the loads below are warp-collective
+    if (ok && wk.s_exit) {
+      float* dst = wk.s_exit + (int64_t)row * kD + 64 * half;
+      float v[64];
+#pragma unroll
+      for (int c0 = 0; c0 < 64; c0 += 16)
+        tmem_ld16(tlane + kTS + 64 * half + c0, *reinterpret_cast<float(*)[16]>(v + c0));
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 64; j += 4)
+        *reinterpret_cast<float4*>(dst + j) =
+            make_float4(sigma * v[j], sigma * v[j + 1], sigma * v[j + 2], sigma * v[j + 3]);
+    }
+  } else if (tid < kOut0) {
+    // ======================================================================= local warps
+    const int ltid = tid - kLocal0;  // 0..127 = this thread's tensor-memory lane
+    bool ok = true;
+    float sig_run = 1.f;  // sigma before the next chunk whose gates are formed
+    const float* al_p = a.alpha + b * a.a_sb + h * a.a_sh;
+    // gates of chunk c: g = cumsum log alpha, gamma = e^g, 1/(sigma gamma), sigma bookkeeping
+    auto gates = [&](int c) {
+      float* gs = slot(c);
+      const int64_t t = wk.t_begin + (int64_t)c * kC + ltid;
+      float g = (ltid < kC && t < wk.t_end) ? logf(al_p[t]) : 0.f;
+      if (ltid < kC) {
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float y = __shfl_up_sync(kFullMask, g, off);
+          if ((ltid & 31) >= off) g += y;
+        }
+        if (ltid == 31) lshare[0] = g;
+      }
+      named_bar_sync(kLocalBar, kLocalWarps * 32);
+      float gam = 0.f;
+      if (ltid < kC) {
+        if (ltid >= 32) g += lshare[0];
+        gam = __expf(g);
+        gs[kGGam + ltid] = gam;
+        if (ltid == kC - 1) lshare[1] = gam;
+      }
+      named_bar_sync(kLocalBar, kLocalWarps * 32);
+      const float gC = lshare[1];
+      const float s_c = sig_run, s_after = s_c * gC;
+      const bool fold = s_after < kFoldBelow;
+      sig_run = fold ? 1.f : s_after;
+      if (ltid < kC) gs[kGKds + ltid] = 1.f / (s_c * gam);
+      if (ltid == 0) {
+        gs[kGSig] = s_c;
+        gs[kGSigAfter] = s_after;
+        gs[kGFold] = fold ? 1.f : 0.f;
+      }
+      named_bar_sync(kLocalBar, kLocalWarps * 32);  // gates complete; lshare free again
+      warp_arrive(smem_u32(&bar_gate[c % kGateSlots]));
+    };
+    // T1 = delta T2 diag(gamma) of chunk c (into the single T1 buffer; b of chunk c-1 has completed)
+    auto t1_pass = [&](int c) {
+      ok = ok && wait(&bar_kv[c & 1], (uint32_t)((c >> 1) & 1));
+      const float* gam = slot(c) + kGGam;
+      const uint8_t* t2 = sm + early(c) + kEOffT2;
+      const int r = ltid >> 1, j0 = (ltid & 1) * 32;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t off = sw128_off(r, j0 + 8 * q, 64);
+        const uint4 raw = *reinterpret_cast<const uint4*>(t2 + off);
+        const __nv_bfloat16* x = reinterpret_cast<const __nv_bfloat16*>(&raw);
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = __bfloat162float(x[e]) * gam[j0 + 8 * q + e] * a.delta;
+        *reinterpret_cast<uint4*>(sm + kSOffT1 + off) = pack8_bf16(y);
+      }
+      fence_proxy_async_smem();
+      warp_signal(smem_u32(&sig[kSigT1]));
+    };
+    gates(0);
+    if (n > 1) gates(1);
+    if (n > 2) gates(2);
+    t1_pass(0);
+    for (int c = 0; c < n; ++c) {
+      const uint32_t par = (uint32_t)(c & 1);
+      // ---- W^T (lane k of tensor memory holds row k) into its tile
+      ok = ok && wait(&bar_b, par);
+      tc_fence_after();
+      {
+        uint8_t* wt = sm + late(c) + kLOffWT;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {  // columns r, 32 at a time
+          float w[32];
+          tmem_ld16(tlane + kTW + 32 * part, *reinterpret_cast<float(*)[16]>(w));
+          tmem_ld16(tlane + kTW + 32 * part + 16, *reinterpret_cast<float(*)[16]>(w + 16));
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(wt + sw128_off(ltid, 32 * part + 8 * q, 128)) = pack8_bf16(w + 8 * q);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      if (WOUT) ok = ok && wait(&bar_q[c & 1], (uint32_t)((c >> 1) & 1));  // Q and P of the chunk landed
+      warp_signal(smem_u32(&sig[kSigWK]));
+      if (c + 1 < n) t1_pass(c + 1);
+      if (c + 3 < n) gates(c + 3);
+    }
+  } else if (tid < kIssuer0) {
+    // ======================================================================= output warps
+    if (WOUT) {
+      const int i = tid - kOut0;  // value index = tensor-memory lane
+      bool ok = true;
+      for (int c = 0; c < n; ++c) {
+        ok = ok && wait(&bar_o, (uint32_t)(c & 1)) && wait(&bar_gate[c % kGateSlots], gate_par(c));
+        tc_fence_after();
+        float y[64];
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) tmem_ld16(tlane + kTY + c0, *reinterpret_cast<float(*)[16]>(y + c0));
+        tmem_ld_wait();
+        const float* gam = slot(c) + kGGam;
+#pragma unroll
+        for (int r = 0; r < 64; ++r) y[r] *= a.q_scale * gam[r];
+        tc_fence_before();
+        warp_signal(smem_u32(&sig[kSigOfree]));  // Y may be overwritten from here on
+        const int64_t t0 = wk.t_begin + (int64_t)c * kC;
+        const int nvalid = (wk.t_end - t0 < kC) ? (int)(wk.t_end - t0) : kC;
+        TOut* optr = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + t0 * a.o_st + i;
+#pragma unroll
+        for (int r = 0; r < 64; ++r) {
+          if (r < nvalid) store1(optr, y[r]);
+          optr += a.o_st;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTCols);
+}
+
+size_t records_bytes(int64_t BH, int64_t nch) { return (size_t)(BH * nch) * kRec; }
+
+template <typename TOut>
+cudaError_t launch_scan_typed(const GdnPrefillLaunch& a, void* ws, unsigned* status, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv;
+  if (!gdn_make_map(&mq, a.q, a.B, a.H, a.N) || !gdn_make_map(&mk, a.k, a.B, a.H, a.N) ||
+      !gdn_make_map(&mv, a.v, a.B, a.H, a.N))
+    return cudaErrorInvalidValue;
+  static std::once_flag attr_once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once, [] {
+    attr_err = cudaFuncSetAttribute(gdn_tinv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kISmemAlloc);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(gdn_scan_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kSSmemAlloc);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  const int64_t BH = a.B * a.H;
+  const int64_t nch = (a.N + kC - 1) / kC;
+  uint8_t* recT = static_cast<uint8_t*>(ws);
+  float* seg = reinterpret_cast<float*>(recT + records_bytes(BH, nch));
+  gdn_tinv_kernel<<<(unsigned)(BH * nch), kThreads, kISmemAlloc, stream>>>(mq, mk, a, (int)nch, recT, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const GdnSegPlan plan = gdn_segment_plan(a.B, a.H, a.N);
+  if (plan.G == 1) {
+    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr};
+    gdn_scan_kernel<TOut><<<(unsigned)BH, kScanThreads, kSSmemAlloc, stream>>>(mq, mk, mv, a, task, (int)nch, recT,
+                                                                            status);
+    return cudaGetLastError();
+  }
+  float* maps = seg;
+  float* states = maps + BH * (plan.G - 1) * 2 * kStateElems;
+  const GdnTask t1{kSegmentMaps, plan.G, plan.seg_len, maps, nullptr};
+  gdn_scan_kernel<TOut><<<(unsigned)(BH * (plan.G - 1) * 2), kScanThreads, kSSmemAlloc, stream>>>(
+      mq, mk, mv, a, t1, (int)nch, recT, status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_gdn_segment_combine(a.S_in, maps, states, plan.G, BH, stream);
+  if (e != cudaSuccess) return e;
+  const GdnTask t2{kSegmentOutputs, plan.G, plan.seg_len, nullptr, states};
+  gdn_scan_kernel<TOut><<<(unsigned)(BH * plan.G), kScanThreads, kSSmemAlloc, stream>>>(mq, mk, mv, a, t2, (int)nch,
+                                                                                     recT, status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gdn_scan_workspace_bytes(int64_t B, int64_t H, int64_t N) {
+  const int64_t BH = B * H;
+  if (BH <= 0 || N <= 0) return 0;
+  const int64_t nch = (N + kC - 1) / kC;
+  return records_bytes(BH, nch) + gdn_segment_plan(B, H, N).ws_bytes;
+}
+
+cudaError_t launch_gdn_prefill_scan(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* status,
+                                    cudaStream_t stream) {
+  const int64_t BH = a.B * a.H;
+  if (BH == 0 || a.N == 0) return cudaSuccess;
+  const int64_t nch = (a.N + kC - 1) / kC;
+  if (BH * nch > (int64_t)INT32_MAX) return cudaErrorInvalidValue;  // one inversion CTA per chunk
+  if (ws == nullptr || ws_bytes < gdn_scan_workspace_bytes(a.B, a.H, a.N)) return cudaErrorInvalidValue;
+  return a.out_bf16 ? launch_scan_typed<__nv_bfloat16>(a, ws, status, stream)
+                    : launch_scan_typed<float>(a, ws, status, stream);
+}
+
+}  // namespace la

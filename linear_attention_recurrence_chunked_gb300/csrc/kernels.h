@@ -11,6 +11,11 @@ namespace la {
 constexpr unsigned kStatusTimeout = 1u;   // a bounded wait expired
 constexpr unsigned kStatusBadIndex = 2u;  // a state index outside its array was skipped
 
+// The cudaError_t behind the latest LA_ERR_CUDA returned to the calling
+// thread (api.cu); noted by every path that maps a CUDA failure to it.
+void note_cuda_error(int code);
+int last_cuda_error();
+
 struct View4 {        // strided [B, H, N, d] view, element strides
   const void* ptr;
   int64_t sb, sh, st;
@@ -74,13 +79,14 @@ cudaError_t launch_taylor_decode(const DecodeLaunch& a, cudaStream_t stream);
 cudaError_t launch_taylor_prefill_recurrent(const TaylorPrefillLaunch& a, cudaStream_t stream);
 cudaError_t launch_gdn_prefill_recurrent(const GdnPrefillLaunch& a, cudaStream_t stream);
 // bf16 inputs: chunked tcgen05 kernels.  The single-kernel scan needs the
-// segment scratch of gdn_segment_plan only; the two-kernel split (chunk-local
-// records, then the state chain) needs gdn_split_workspace_bytes.
+// segment scratch of gdn_segment_plan only; the two-kernel scan (per-chunk
+// inverse records, then the warp-specialized state scan) needs
+// gdn_scan_workspace_bytes.
 cudaError_t launch_gdn_prefill_chunked(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* dev_status,
                                        cudaStream_t stream);
-size_t gdn_split_workspace_bytes(int64_t B, int64_t H, int64_t N);
-cudaError_t launch_gdn_prefill_split(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* dev_status,
-                                     cudaStream_t stream);
+size_t gdn_scan_workspace_bytes(int64_t B, int64_t H, int64_t N);
+cudaError_t launch_gdn_prefill_scan(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* dev_status,
+                                    cudaStream_t stream);
 cudaError_t launch_taylor_prefill_chunked(const TaylorPrefillLaunch& a, unsigned* dev_status, cudaStream_t stream);
 struct SwaDecodeLaunch {
   int64_t S, H;

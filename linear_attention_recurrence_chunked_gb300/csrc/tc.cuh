@@ -54,6 +54,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// As mbar_try_wait, but the thread may sleep in hardware until the phase
+// completes or `hint_ns` nanoseconds pass (a plain try_wait returns at once,
+// so many waiting warps spinning on it would starve the warps doing work).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+// Non-blocking test of phase `parity` (never suspends the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
 // One arrival per warp once every lane of it got here: each lane fenced its
 // own shared-memory writes for the async proxy and its tensor-memory accesses
 // before, and __syncwarp orders them before lane 0's release-arrive.  Every
@@ -62,14 +88,34 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
+// Progress counters in shared memory: a worker warp adds 1 after finishing a
+// hand-off (release: its earlier writes, and those of the lanes ordered before
+// it by __syncwarp, become visible first); a polling thread reads them with
+// acquire loads.  Independent loads pipeline, unlike mbarrier tests.
+__device__ __forceinline__ void sig_add(uint32_t addr) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;" ::"r"(addr) : "memory");
+}
+__device__ __forceinline__ uint32_t sig_load(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+// One count per warp once every lane got here (see warp_arrive).
+__device__ __forceinline__ void warp_signal(uint32_t addr) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) sig_add(addr);
+}
 // Waits for phase `parity` of the barrier to complete; gives up after
-// limit_ns, ORs kStatusTimeout into *status and returns false.
+// limit_ns, ORs kStatusTimeout into *status and returns false.  The thread
+// sleeps in hardware between polls (up to kWaitSleepNs each), so waiting warps
+// leave the issue slots and the barrier unit to the warps that work.
+constexpr uint32_t kWaitSleepNs = 20000;
 __device__ __forceinline__ bool mbar_wait_ns(uint32_t bar, uint32_t parity, unsigned* status, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) {
       atomicOr(status, kStatusTimeout);
       return false;
     }
@@ -208,6 +254,19 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T with A read from tensor memory: lane m
+// holds row m of A (M = 128), each 32-bit column two consecutive bf16 of
+// its K elements (the lower-addressed one in the low half), so one 16-deep
+// K step spans 8 columns.  Issued by one thread.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrives on `bar` once every MMA this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -242,6 +301,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+// Two floats as one bf16x2 word (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
 
 // Pack 8 floats as bf16 (round to nearest even) into one 16-byte vector.
 __device__ __forceinline__ uint4 pack8_bf16(const float* x) {

@@ -145,7 +145,7 @@ def test_decode_rejections(lib):
 
 
 def test_gdn_workspace_queries_and_rejection(lib):
-    rec = 74240  # two-kernel schedule: record bytes per 64-token chunk of one (b,h)
+    rec = 16384  # two-kernel scan: bytes of the per-chunk record (T diag(beta) and P images) of one (b,h)
     big = gdn_args(B=1, H=16, N=1 << 20)
     need_min = lib.la_gdn_prefill_workspace_size_min(ctypes.byref(big))
     need = lib.la_gdn_prefill_workspace_size(ctypes.byref(big))
@@ -252,3 +252,10 @@ def test_notebank_rejections(lib):
     assert route(R=0) == la.LA_ERR_UNSUPPORTED
     assert route(u=0x200008) == la.LA_ERR_INVALID_ARGUMENT
     assert route(J=0) == la.LA_OK
+
+
+def test_cuda_error_reporting_without_a_gpu(lib):
+    # nothing has failed on this thread yet; names come from the CUDA runtime's table
+    assert lib.la_last_cuda_error() == 0
+    assert lib.la_cuda_error_name(0) == b"cudaSuccess"
+    assert lib.la_cuda_error_name(701) == b"cudaErrorLaunchOutOfResources"
