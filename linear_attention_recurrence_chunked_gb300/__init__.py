@@ -72,7 +72,8 @@ class DecodeArgs(ctypes.Structure):
 EXPORTED = ("la_based_prefill", "la_gdn_prefill", "la_gated_prefill", "la_decode_step", "la_based_prefill_workspace_size",
             "la_gdn_prefill_workspace_size", "la_gdn_prefill_workspace_size_min", "la_gdn_prefill_noalloc", "la_device_status",
             "la_state_rescale", "la_state_gather", "la_swa_decode_step", "la_notebank_scores", "la_notebank_address",
-            "la_notebank_route", "la_selftest_bounded_wait", "la_status_string", "la_abi_version")
+            "la_notebank_route", "la_selftest_bounded_wait", "la_status_string", "la_abi_version",
+            "la_last_cuda_error", "la_cuda_error_name")
 
 
 class NotebankScoresArgs(ctypes.Structure):
@@ -105,7 +106,12 @@ class SwaDecodeArgs(ctypes.Structure):
 class LAError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {la_status_string(status)} (status {status})")
+        msg = f"{where}: {la_status_string(status)} (status {status})"
+        if status == LA_ERR_CUDA:
+            lib = load_library()
+            code = int(lib.la_last_cuda_error())
+            msg += f"; CUDA error {code} ({lib.la_cuda_error_name(code).decode()})"
+        super().__init__(msg)
 
 
 _lib = None
@@ -159,6 +165,10 @@ def load_library(path: str | None = None):
     lib.la_selftest_bounded_wait.argtypes = [ctypes.c_int, ctypes.c_int64, vp]
     lib.la_status_string.restype = ctypes.c_char_p
     lib.la_status_string.argtypes = [ctypes.c_int]
+    lib.la_last_cuda_error.restype = ctypes.c_int
+    lib.la_last_cuda_error.argtypes = []
+    lib.la_cuda_error_name.restype = ctypes.c_char_p
+    lib.la_cuda_error_name.argtypes = [ctypes.c_int]
     lib.la_abi_version.restype = ctypes.c_int
     lib.la_abi_version.argtypes = []
     if path is None:
