@@ -5,6 +5,7 @@ HBM.  The headline line (``value``) is the BASED Taylor prefill,
 B=8, H=16, N=4096, d'=16, d_v=64, bf16 in / fp32 state, in tokens/s (B*N per
 step).  The same run also times, under ``paths``:
   based_prefill_decay  the headline workload with a fixed per-head decay
+  taylor_fp32_small    Taylor linear attention fp32, B=1, H=2, N=256 (latency)
   gdn_prefill       Gated DeltaNet prefill B=4, H=16, N=16384, d=128
   gdn_prefill_long  Gated DeltaNet prefill B=1, H=16, N=1,048,576, d=128
   gated_prefill     scalar-gate (A_t = alpha_t I) prefill on the gdn_prefill inputs
@@ -94,6 +95,42 @@ def kernel_sources_sha(files):
         path = os.path.join(ROOT, "linear_attention_recurrence_chunked_gb300", "csrc", f)
         h.update(_code_only(open(path, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
+
+
+# Dense contractions per chunk and head that the chunked form of each method needs (multiply-adds x 2),
+# the "intra-chunk GEMM" work the tensor cores run:
+#  GDN (C = 64, d_k = d_v = 128): [K;Q] K^T, W = T diag(beta gamma) K, U~ = T diag(beta) V, P U (5 of
+#      2*64*64*128) and W S0^T, Q S0^T, the state update U^T K (3 of 2*64*128*128); the triangular inverse
+#      T runs on the CUDA cores and is not counted.
+#  scalar gate (same chunk): Q K^T, P (beta V) and Q S0^T, the update (no W, no U~, no inverse).
+#  BASED (C = 128, d' = 16, the 153-wide compact feature basis, d_v = 64 plus the normaliser column):
+#      Q K^T 2*128*128*16, readout phi(Q) [S | z] 2*128*153*65, intra-chunk P [V | 1] 2*128*128*65,
+#      update phi(K)^T [V | 1] 2*153*128*65.
+_SMALL, _BIG = 2 * 64 * 64 * 128, 2 * 64 * 128 * 128
+GDN_CHUNK_FLOPS = {"gdn": 5 * _SMALL + 3 * _BIG, "gated": 2 * _SMALL + 2 * _BIG}
+TAYLOR_CHUNK_FLOPS = 2 * 128 * 128 * 16 + 2 * 128 * 153 * 65 + 2 * 128 * 128 * 65 + 2 * 153 * 128 * 65
+
+
+def ncu_entry(key):
+    """The committed ncu summary of a kernel, if its sources are unchanged since it was taken; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(key)
+    if not d or d.get("source_sha") != kernel_sources_sha(d.get("sources", [])):
+        return None
+    return d
+
+
+def tensor_fraction(flops_per_launch, ms_per_launch, pk, key):
+    """Intra-chunk GEMM FLOPs per launch / event time, against the measured sustained dense bf16 rate; the
+    tensor-pipe activity ncu measured for the same kernel (percent of elapsed cycles) beside it."""
+    ach = flops_per_launch / (ms_per_launch * 1e-3) / 1e12
+    peak = pk.get("bf16_tflops_sustained") or pk["bf16_tflops"]
+    e = ncu_entry(key) or {}
+    return {"bound": "tensor", "flops_per_launch": int(flops_per_launch), "achieved": round(ach, 1),
+            "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+            "ncu_tensor_pipe_pct": e.get("tensor_pipe_pct")}
 
 
 def ncu_traffic(key):
@@ -280,6 +317,7 @@ def gpu_arm(args, ws, rank, local):
     bytes_launch = BYTES_PER_TOKEN_HEAD["taylor_prefill"] * w.B * w.H * w.N + STATE_BYTES["taylor"] * w.B * w.H
     roof = roofline(bytes_launch, ms_step, pk["hbm_gbs"], ncu_traffic("taylor_prefill"))
     roof["peak_source"] = pk["source"]
+    tensor = tensor_fraction(TAYLOR_CHUNK_FLOPS * w.B * w.H * ((w.N + 127) // 128), ms_step, pk, "taylor_prefill")
 
     # --- e2e through the C ABI with host buffers ----------------------------
     # Every step copies its inputs in from pinned host memory and its results (y and the final state)
@@ -354,14 +392,15 @@ def gpu_arm(args, ws, rank, local):
             "config": {"workload": w.description, "B": w.B, "H": w.H, "N": w.N, "d_feat": 16, "d_v": 64,
                        "tokens_per_step": tokens, "seed": w.seed, "l2": "flushed between timed steps (512 MiB write)",
                        "parallelism": f"replicas{ws}" if ws > 1 else "single"},
-            "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clk, "paths": paths}
+            "roofline": roof, "tensor": tensor, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+            "paths": paths}
     return line
 
 
 KERNELS_PER_CALL = {"based_prefill": 1, "gdn_prefill": 2, "decode": 1}
 
 
-PATH_NAMES = ("based_prefill_decay", "gdn_prefill", "gdn_prefill_long", "gated_prefill", "decode_gdn", "decode_taylor",
+PATH_NAMES = ("based_prefill_decay", "taylor_fp32_small", "gdn_prefill", "gdn_prefill_long", "gated_prefill", "decode_gdn", "decode_taylor",
               "decode_swa", "notebank_write", "notebank_route")
 
 # NoteBank sizes (NoteBank App. C: GDN backbone with J = 192 layer-head channels of d_k = 256, write chunks of
@@ -405,9 +444,38 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         out["based_prefill_decay"] = {"workload": w.description + ", per-head decay 1 - 2^-(5 + h mod 8)",
                                       "tokens_per_s": round(whole_job_rate(w.B * w.N, ws, ms * 1e-3), 1),
                                       "ms": round(ms, 4),
-                                      "roofline": roofline(byts, ms, pk["hbm_gbs"], ncu_traffic("based_prefill_decay"))}
+                                      "roofline": roofline(byts, ms, pk["hbm_gbs"], ncu_traffic("based_prefill_decay")),
+                                      "tensor": tensor_fraction(TAYLOR_CHUNK_FLOPS * w.B * w.H * ((w.N + 127) // 128),
+                                                                ms, pk, "based_prefill_decay")}
         del x, y, s, z
         torch.cuda.empty_cache()
+    if only is None or only == "taylor_fp32_small":
+        # the small fp32 configuration (B=1, H=2, N=256): two CTAs, so a latency figure, not a roofline one
+        w = synthetic.WORKLOADS["taylor_fp32_small"]
+        x = synthetic.workload_inputs(w.name, device=dev, seed=w.seed + seed_off)
+        y = torch.empty((w.B, w.H, w.N, 64), dtype=torch.float32, device=dev)
+        s = torch.empty((w.B, w.H, la.TAYLOR_D, 64), dtype=torch.float32, device=dev)
+        z = torch.empty((w.B, w.H, la.TAYLOR_D), dtype=torch.float32, device=dev)
+        wsf = torch.empty(max(1, la.la_based_prefill_workspace_size(x["q"], x["k"], x["v"], y)), dtype=torch.uint8,
+                          device=dev)
+
+        def fstep():
+            la.la_based_prefill(x["q"], x["k"], x["v"], y=y, s_out=s, z_out=z, workspace=wsf, stream=stream)
+
+        t = Timer(stream, flush)
+        for _ in range(args.warmup):
+            t.run(fstep)
+        t.reset()
+        barrier(ws)
+        for _ in range(steps):
+            t.run(fstep)
+        ms = max_over_ranks(t.total_ms(), ws) / steps
+        launches += steps * KERNELS_PER_CALL["based_prefill"]
+        byts = sum(a.numel() * a.element_size() for a in (x["q"], x["k"], x["v"], y, s, z))
+        out["taylor_fp32_small"] = {"workload": w.description, "tokens_per_s": round(whole_job_rate(w.B * w.N, ws,
+                                                                                                 ms * 1e-3), 1),
+                                    "ms": round(ms, 4), "roofline": roofline(byts, ms, pk["hbm_gbs"], None)}
+        del x, y, s, z, wsf
     for name in ("gdn_prefill", "gdn_prefill_long", "gated_prefill"):
         if only is not None and name != only:
             continue
@@ -415,8 +483,9 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         w = synthetic.WORKLOADS["gdn_prefill" if name == "gated_prefill" else name]
         prefill = la.la_gated_prefill if name == "gated_prefill" else la.la_gdn_prefill
         reps = max(1, min(steps, args.long_steps)) if name == "gdn_prefill_long" else steps
-        x = synthetic.workload_inputs(w.name, device=dev, seed=w.seed + seed_off)
-        o = torch.empty((w.B, w.H, w.N, 128), dtype=torch.bfloat16, device=dev)
+        N = getattr(args, "tokens", None) if only == name and getattr(args, "tokens", None) else w.N
+        x = synthetic.workload_inputs(w.name, device=dev, seed=w.seed + seed_off, N=N)
+        o = torch.empty((w.B, w.H, N, 128), dtype=torch.bfloat16, device=dev)
         S = torch.empty((w.B, w.H, 128, 128), dtype=torch.float32, device=dev)
         ws_t = torch.empty(max(1, la.la_gdn_prefill_workspace_size(x["q"], x["k"], x["v"], x["alpha"], x["beta"])),
                            dtype=torch.uint8, device=dev)
@@ -437,11 +506,16 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         segments = la.la_gdn_prefill_workspace_size_min(x["q"], x["k"], x["v"], x["alpha"], x["beta"]) > 0
         per_call = 4 if segments else KERNELS_PER_CALL["gdn_prefill"]
         launches += reps * per_call
-        byts = BYTES_PER_TOKEN_HEAD["gdn_prefill"] * w.B * w.H * w.N + STATE_BYTES["gdn"] * w.B * w.H
-        r = roofline(byts, ms, pk["hbm_gbs"], ncu_traffic(name))
+        byts = BYTES_PER_TOKEN_HEAD["gdn_prefill"] * w.B * w.H * N + STATE_BYTES["gdn"] * w.B * w.H
+        r = roofline(byts, ms, pk["hbm_gbs"], ncu_traffic(name) if N == w.N else None)
         desc = w.description.replace("Gated DeltaNet", "Scalar-gate") if name == "gated_prefill" else w.description
-        out[name] = {"workload": desc, "tokens_per_s": round(whole_job_rate(w.B * w.N, ws, ms * 1e-3), 1),
-                     "ms": round(ms, 4), "roofline": r}
+        if N != w.N:
+            desc = desc.replace(f"N={w.N}", f"N={N}")
+        nch = w.B * w.H * ((N + 63) // 64)
+        out[name] = {"workload": desc, "tokens_per_s": round(whole_job_rate(w.B * N, ws, ms * 1e-3), 1),
+                     "ms": round(ms, 4), "roofline": r,
+                     "tensor": tensor_fraction(GDN_CHUNK_FLOPS["gated" if name == "gated_prefill" else "gdn"] * nch,
+                                               ms, pk, name)}
         del x, o, S, ws_t
         torch.cuda.empty_cache()
 
@@ -632,6 +706,91 @@ def cpu_baseline():
                       f"CPU-seeded inputs); {dt:.2f} s wall"}
 
 
+def _timed(fn):
+    t0 = time.perf_counter()
+    fn()
+    return time.perf_counter() - t0
+
+
+def path_cpu_baselines(paths):
+    """The oracle, as it stands, timed on a bounded sample of each secondary path's workload (a few
+    heads, channels or sequences of it; about a second to a few seconds each), in the path's own
+    unit: a token counts once for all of its heads, so a sample of h of H heads over n tokens is
+    n * h / H tokens.  Adds "cpu_baseline" to every path present in `paths`."""
+    import oracle
+    oracle.build()
+    cores = oracle.default_threads()
+    wb, wg, wl, wd = (synthetic.WORKLOADS[n] for n in ("based_prefill", "gdn_prefill", "gdn_prefill_long", "decode"))
+
+    def put(name, units, dt, unit, sample):
+        if name in paths:
+            paths[name]["cpu_baseline"] = {"value": round(units / dt, 2), "unit": unit, "cores": cores,
+                                           "kind": "oracle", "sample": f"{sample}; {dt:.2f} s wall"}
+
+    if "taylor_fp32_small" in paths:
+        w = synthetic.WORKLOADS["taylor_fp32_small"]
+        x = synthetic.workload_inputs(w.name)
+        dt = _timed(lambda: oracle.taylor(*(synthetic.to_oracle(x[n]) for n in ("q", "k", "v"))))
+        put("taylor_fp32_small", w.B * w.N, dt, "tokens/s", "fp64 C oracle on the whole workload")
+    if "based_prefill_decay" in paths:
+        x = synthetic.taylor_inputs(1, wb.H, wb.N, dtype=wb.dtype, seed=wb.seed)
+        lam = decay_rates(wb.H).double().numpy()
+        dt = _timed(lambda: oracle.taylor(*(synthetic.to_oracle(x[n]) for n in ("q", "k", "v")), decay=lam))
+        put("based_prefill_decay", wb.N, dt, "tokens/s", f"fp64 C oracle, 1 sequence x {wb.H} heads x {wb.N} tokens")
+    for name, w, heads, n in (("gdn_prefill", wg, 2, wg.N), ("gated_prefill", wg, 2, wg.N),
+                              ("gdn_prefill_long", wl, 1, 65536)):
+        if name not in paths:
+            continue
+        x = synthetic.gdn_inputs(1, heads, n, dtype=w.dtype, seed=w.seed)
+        fn = oracle.gated if name == "gated_prefill" else oracle.gdn
+        dt = _timed(lambda: fn(*(synthetic.to_oracle(x[m]) for m in ("q", "k", "v")), x["alpha"].numpy(),
+                               x["beta"].numpy()))
+        put(name, n * heads / w.H, dt, "tokens/s", f"fp64 C oracle, {heads} of the {w.H} heads x {n} tokens")
+    seqs, steps = 128, 16  # decode: 128 of the 256 sequences (all 16 heads), 16 consecutive steps
+    if "decode_gdn" in paths:
+        x = synthetic.gdn_inputs(seqs, wd.H, steps, dtype=torch.bfloat16, seed=wd.seed)
+        dt = _timed(lambda: oracle.gdn(*(synthetic.to_oracle(x[m]) for m in ("q", "k", "v")), x["alpha"].numpy(),
+                                       x["beta"].numpy()))
+        put("decode_gdn", seqs * steps, dt, "tokens/s", f"fp64 C oracle, {seqs} sequences x {wd.H} heads x {steps} steps")
+    if "decode_taylor" in paths:
+        x = synthetic.taylor_inputs(seqs, wd.H, steps, dtype=torch.bfloat16, seed=wd.seed)
+        dt = _timed(lambda: oracle.taylor(*(synthetic.to_oracle(x[m]) for m in ("q", "k", "v"))))
+        put("decode_taylor", seqs * steps, dt, "tokens/s",
+            f"fp64 C oracle, {seqs} sequences x {wd.H} heads x {steps} steps")
+    if "decode_swa" in paths:
+        g = torch.Generator().manual_seed(wd.seed)
+        n_seq, heads = 64, wd.H  # 64 sequences x 16 heads, one step at position 64 with a full window
+        qh, kh = ((torch.randn((n_seq, heads, SWA_WINDOW + 1, SWA_D), generator=g) * SWA_D ** -0.25)
+                  .to(torch.bfloat16) for _ in range(2))
+        vh = torch.randn((n_seq, heads, SWA_WINDOW + 1, SWA_D), generator=g).to(torch.bfloat16)
+        dt = _timed(lambda: oracle.swa(*(synthetic.to_oracle(t) for t in (qh, kh, vh)), SWA_WINDOW,
+                                       SWA_D ** -0.5, t_samples=[SWA_WINDOW]))
+        put("decode_swa", n_seq, dt, "tokens/s", f"numpy oracle, {n_seq} sequences x {heads} heads, one step")
+    if "notebank_write" in paths:
+        g = torch.Generator().manual_seed(11)
+        k = torch.randn((1, NB_H, NB_N, NB_D), generator=g).to(torch.bfloat16)
+        q = torch.randn((1, NB_H, NB_N, NB_D), generator=g).to(torch.bfloat16)
+        coords = np.stack([np.random.default_rng(h).permutation(NB_D)[:16] for h in range(NB_H)]).reshape(1, NB_H, 16)
+        n_notes = 2 * (NB_N // NB_CHUNK)
+        spans = np.stack([np.arange(n_notes) * (NB_CHUNK // 2), np.full(n_notes, NB_NOTE_LEN)], axis=1)
+
+        def nb_write():
+            r = oracle.notebank_scores(synthetic.to_oracle(k), chunk=NB_CHUNK, window=NB_WINDOW)
+            oracle.notebank_address(r["d_ch"], synthetic.to_oracle(q), coords, spans)
+
+        dt = _timed(nb_write)
+        put("notebank_write", NB_N / NB_L, dt, "tokens/s",
+            f"numpy oracle, 1 of the {NB_L} layers ({NB_H} channels) x {NB_N} tokens, {n_notes} note addresses")
+    if "notebank_route" in paths:
+        g = torch.Generator().manual_seed(12)
+        J = NB_L * NB_H
+        rho = torch.randn((NB_NOTES, J, 16), generator=g).to(torch.bfloat16).float().numpy()
+        u = torch.randn((J, NB_Q, 16), generator=g).to(torch.bfloat16).float().numpy()
+        dt = _timed(lambda: oracle.notebank_route(rho, u, NB_R))
+        put("notebank_route", 1, dt, "questions/s",
+            f"numpy oracle, all {NB_NOTES} notes x {J} channels, one {NB_Q}-token question")
+
+
 def reference_arm(args, ws, rank):
     import oracle
     if rank != 0:
@@ -666,6 +825,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", choices=PATH_NAMES, default=None,
                     help="time one secondary path alone (K timed launches or decode steps), for profiling")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="with --only and a GDN prefill path: N tokens per sequence instead of the workload's "
+                         "(smaller profiling captures of the same launch configuration)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -697,6 +859,7 @@ def main():
     if rank == 0:
         if not args.no_cpu_baseline and ws == 1:
             line["cpu_baseline"] = cpu_baseline()
+            path_cpu_baselines(line["paths"])
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist

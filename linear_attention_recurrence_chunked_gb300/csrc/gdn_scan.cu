@@ -17,7 +17,8 @@
 // Kernel 2 (gdn_scan_kernel, one CTA per (b,h) or sequence segment) walks the
 // chunks with the fp32 state in tensor memory and does everything else on
 // the tcgen05 tensor cores, from tiles it loads once:
-//   b:  W^T = K^T (T2 diag gamma)^T,  U~^T = V^T T2^T          (chunk-local)
+//   w:  W^T = K^T (T2 diag gamma)^T                            (chunk-local)
+//   u:  U~^T = V^T T2^T                                        (chunk-local)
 //   x:  X = S0 W^T                                             (the state path)
 //   y:  Y = S0 Q^T                                             (outputs)
 //   e:  S~ += (U diag(1 / (sigma gamma)))^T K                  (the state update)
@@ -27,14 +28,14 @@
 // the decay then enters only through a scale of U's columns, and the update
 // S~ += (U diag(1 / (sigma gamma)))^T K takes the raw K tile.
 //
-// Roles (17 warps): warps 0-7 own the state rows (two threads per row) and
+// Roles (18 warps): warps 0-7 own the state rows (two threads per row) and
 // run the passes on the sequential path, U = U~ - X and the bf16 copy S0 of
 // the state after each update; warps 8-11 run the chunk-local passes a chunk
 // ahead (gates, T2 diag gamma, W^T from tensor memory); warps 12-15 drain
-// the outputs; warp 16 issues every copy and MMA as soon as its inputs are
-// ready.  Workers report progress through counters the issuer reads with one
-// round of loads; waits on copies and MMAs are mbarriers, and every wait is
-// bounded.
+// the outputs; warp 16 issues every MMA and warp 17 every copy, each as soon
+// as its inputs are ready.  Workers report progress through counters the
+// issuers read with one round of loads; waits on copies and MMAs are
+// mbarriers, and every wait is bounded.
 #include <mutex>
 
 #include "gdn_common.cuh"
@@ -256,22 +257,30 @@ gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 }
 
 // ============================================================================ kernel 2
-// Shared memory (offsets from a 1024-byte aligned base), two rings of two
-// slots by chunk parity:
-//   early slot (free once the chunk's state update is done): K [64 r][128 k],
-//       V [64][128], the T2 image;
-//   late slot (free once the chunk's state update and outputs are done):
-//       W^T [128 k][64 r] (rows k, the r contiguous: an MN-major operand),
-//       Q [64 r][128 k], the P image.
+// Shared memory (offsets from a 1024-byte aligned base), three rings of copy
+// slots and the tiles the workers write:
+//   K ring, three slots (free once the chunk's state update is done): K
+//       [64 r][128 k], the T2 image.  Three deep so that the copies of chunk
+//       c+1 are in flight a whole chunk before W^T of it is wanted.
+//   V ring, two slots (free once U~ of the chunk is computed): V [64][128].
+//   Q ring, two slots (free once the chunk's outputs are done): Q [64 r][128 k],
+//       the P image.
+//   W^T [128 k][64 r] (rows k, the r contiguous: an MN-major operand), one
+//       tile: W^T of chunk c+1 is computed after x(c) is issued, and copied
+//       into the tile only once it is done.
 // The bf16 copy S0 of the state is the A operand of x and y straight from
 // tensor memory.
-constexpr uint32_t kEarly = 40960;                    // one early slot
-constexpr uint32_t kEOffK = 0, kEOffV = 16384, kEOffT2 = 32768;
-constexpr uint32_t kLate = 40960;                     // one late slot
-constexpr uint32_t kLOffWT = 0, kLOffQ = 16384, kLOffP = 32768;
-constexpr uint32_t kSOffEarly = 0;
-constexpr uint32_t kSOffLate = 2 * kEarly;            // 81920
-constexpr uint32_t kSOffT1 = kSOffLate + 2 * kLate;   // T2 diag(gamma), one buffer
+constexpr int kKSlots = 3;
+constexpr uint32_t kKSlot = 24576;                    // one K slot
+constexpr uint32_t kKOffK = 0, kKOffT2 = 16384;
+constexpr uint32_t kVSlot = 16384;
+constexpr uint32_t kQSlot = 24576;                    // one Q slot
+constexpr uint32_t kQOffQ = 0, kQOffP = 16384;
+constexpr uint32_t kSOffK = 0;
+constexpr uint32_t kSOffV = kSOffK + kKSlots * kKSlot;  // 73728
+constexpr uint32_t kSOffQ = kSOffV + 2 * kVSlot;        // 106496
+constexpr uint32_t kSOffWT = kSOffQ + 2 * kQSlot;       // 155648
+constexpr uint32_t kSOffT1 = kSOffWT + 16384;           // T2 diag(gamma), one buffer
 constexpr uint32_t kSOffU = kSOffT1 + 8192;           // U^T [128 i][64 r]
 constexpr uint32_t kSOffUD = kSOffU + 16384;          // U^T diag(1 / (sigma gamma)) [128 i][64 r]
 constexpr uint32_t kSOffGate = kSOffUD + 16384;       // gate slots
@@ -279,7 +288,8 @@ constexpr int kGateSlots = 8;
 constexpr uint32_t kGateSlot = 576;                   // gamma[64], 1/(sigma gamma)[64], scalars
 constexpr uint32_t kSSmemUsed = kSOffGate + kGateSlots * kGateSlot;
 constexpr uint32_t kSSmemAlloc = kSSmemUsed + 1024;
-static_assert(kEarly % 1024 == 0 && kLate % 1024 == 0 && kSOffLate % 1024 == 0 && kSOffT1 % 1024 == 0 &&
+static_assert(kKSlot % 1024 == 0 && kQSlot % 1024 == 0 && kSOffV % 1024 == 0 && kSOffQ % 1024 == 0 &&
+                  kSOffWT % 1024 == 0 && kSOffT1 % 1024 == 0 &&
                   kSOffU % 1024 == 0 && kSOffUD % 1024 == 0,
               "MMA operand tiles sit on 1024-byte boundaries");
 static_assert(kSSmemAlloc + 512 <= 232448, "shared memory budget");
@@ -302,7 +312,6 @@ constexpr int kIssuer0 = kOut0 + kOutWarps * 32;     // the MMA issuer warp
 constexpr int kLoader0 = kIssuer0 + 32;              // the copy issuer warp
 constexpr int kScanThreads = kLoader0 + 32;
 constexpr int kLocalBar = 1;                         // named barrier of the local warps
-constexpr int kSigT1 = 0, kSigWK = 1, kSigU = 2, kSigS0 = 3, kSigOfree = 4;
 constexpr float kFoldBelow = 2.3283064e-10f;         // 2^-32
 
 // One CTA per SM (shared memory and all 512 tensor-memory columns).  Warps
@@ -315,18 +324,27 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 int nch_total, const uint8_t* rec, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_kv[2];     // early slot landed: K, V, the T2 image
-  __shared__ uint64_t bar_q[2];      // Q and the P image landed in the late slot
+  __shared__ uint64_t bar_k[kKSlots];  // K and the T2 image landed in their slot
+  __shared__ uint64_t bar_v[2];        // V landed
+  __shared__ uint64_t bar_q[2];        // Q and the P image landed
   __shared__ uint64_t bar_b;         // W^T, U~^T computed
   __shared__ uint64_t bar_x;         // X computed
   __shared__ uint64_t bar_e;         // state update done
   __shared__ uint64_t bar_o;         // Y += U^T P^T done: the chunk's outputs are complete
   __shared__ uint64_t bar_gate[kGateSlots];
   __shared__ uint64_t bar_fin;
-  // Worker -> issuer hand-offs, one count per warp per chunk: T2 diag(gamma) written (kSigT1), W^T
-  // written with Q and P landed (kSigWK), by the local warps; U^T written (kSigU), S0 written
-  // (kSigS0), by the state warps; Y read (kSigOfree), by the output warps.
-  __shared__ uint32_t sig[8];
+  // Worker -> MMA issuer hand-offs, one arrival per warp, one phase per chunk: T1 written (bar_t1),
+  // W^T written with Q and P landed (bar_wk), by the local warps; U written (bar_u) and S0 written
+  // (bar_s0, phase 0 = the entry state), by the state warps; Y read (bar_of), by the output warps.
+  // No group gets two phases ahead of the issuer's wait (each next hand-off needs an MMA issued after
+  // that wait), so parities stay unambiguous.
+  __shared__ uint64_t bar_t1, bar_wk, bar_u, bar_s0, bar_of;
+  // Ring slots freed for the copy issuer, one arrival per warp, one phase per use of the slot: the
+  // update (the last MMA to read K and T2) done (bar_kfree) and x issued after U~ done (bar_vfree),
+  // by the state warps; Y read, so that the MMAs reading Q and P are done, by the output warps
+  // (bar_qfree).  A slot's next phase needs the copy the issuer waits to make, so no phase is
+  // passed unseen.
+  __shared__ uint64_t bar_kfree[kKSlots], bar_vfree[2], bar_qfree[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ float lshare[2];        // local warps: scan carry, gamma_C
 
@@ -339,14 +357,22 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   const uint32_t sb = smem_u32(sm);
   auto slot = [&](int c) { return reinterpret_cast<float*>(sm + kSOffGate + (uint32_t)(c % kGateSlots) * kGateSlot); };
   auto gate_par = [&](int c) { return (uint32_t)((c / kGateSlots) & 1); };
-  auto early = [&](int c) { return kSOffEarly + (uint32_t)(c & 1) * kEarly; };
-  auto late = [&](int c) { return kSOffLate + (uint32_t)(c & 1) * kLate; };
+  auto kslot = [&](int c) { return kSOffK + (uint32_t)(c % kKSlots) * kKSlot; };
+  auto kpar = [&](int c) { return (uint32_t)((c / kKSlots) & 1); };
+  auto vslot = [&](int c) { return kSOffV + (uint32_t)(c & 1) * kVSlot; };
+  auto qslot = [&](int c) { return kSOffQ + (uint32_t)(c & 1) * kQSlot; };
   auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(smem_u32(bar), parity, status); };
 
   if (tid == 0) {
+    for (int i = 0; i < kKSlots; ++i) {
+      mbar_init(smem_u32(&bar_k[i]), 1);
+      mbar_init(smem_u32(&bar_kfree[i]), kStateWarps);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bar_kv[i]), 1);
+      mbar_init(smem_u32(&bar_v[i]), 1);
       mbar_init(smem_u32(&bar_q[i]), 1);
+      mbar_init(smem_u32(&bar_vfree[i]), kStateWarps);
+      mbar_init(smem_u32(&bar_qfree[i]), kOutWarps);
     }
     mbar_init(smem_u32(&bar_b), 1);
     mbar_init(smem_u32(&bar_x), 1);
@@ -354,7 +380,12 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     mbar_init(smem_u32(&bar_o), 1);
     for (int i = 0; i < kGateSlots; ++i) mbar_init(smem_u32(&bar_gate[i]), kLocalWarps);
     mbar_init(smem_u32(&bar_fin), 1);
-    for (int i = 0; i < 8; ++i) sig[i] = 0u;
+    mbar_init(smem_u32(&bar_t1), kLocalWarps);
+    mbar_init(smem_u32(&bar_wk), kLocalWarps);
+    mbar_init(smem_u32(&bar_u), kStateWarps);
+    mbar_init(smem_u32(&bar_s0), kStateWarps);
+    mbar_init(smem_u32(&bar_of), kOutWarps);
+
     fence_mbar_init();
     tma_prefetch_desc(&tmap_k);
     tma_prefetch_desc(&tmap_q);
@@ -372,196 +403,180 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 
   if (warp == kIssuer0 / 32) {
     // ======================================================================= MMA issuer
-    // One warp issues every MMA as soon as its inputs are ready: each round it reads the workers'
-    // progress counters (independent loads, one round trip), then issues in the order x, y, e, b, d.  An MMA for chunk m is issued only after every MMA that must precede it
-    // in the tensor pipe (which runs them in issue order).  All 32 lanes walk the loop together;
-    // lane 0 alone issues.
-    const bool leader = (tid & 31) == 0;
-    int nb = 0, nx = 0, ny = 0, ne = 0, nd = 0;
-    const uint32_t id64 = idesc_bf16(128, 64, 0, 0);
-    const uint32_t id64t = idesc_bf16(128, 64, 1, 0);    // A MN-major
-    const uint32_t id64n = idesc_bf16(128, 64, 0, 1);    // B MN-major
-    const uint32_t id128n = idesc_bf16(128, 128, 0, 1);  // B MN-major
-    bool ok = true, mma_issued = false;
-    uint64_t t_idle = 0;
-    uint32_t idle = 0;  // rounds without progress since the last issue
-    while (ok && (ne < n || (WOUT && nd < n))) {
-      bool prog = false;
-      // Progress counters (chunks every warp of a group has finished), read afresh right before the
-      // check that uses them.
-      auto prog_t1 = [&]() { return (int)(sig_load(smem_u32(&sig[kSigT1])) / kLocalWarps); };  // also: early slot landed
-      auto prog_wk = [&]() { return (int)(sig_load(smem_u32(&sig[kSigWK])) / kLocalWarps); };  // also: Q and P landed
-      auto prog_u = [&]() { return (int)(sig_load(smem_u32(&sig[kSigU])) / kStateWarps); };
-      auto prog_s0 = [&]() { return (int)(sig_load(smem_u32(&sig[kSigS0])) / kStateWarps); };
-      auto prog_of = [&]() { return (int)(sig_load(smem_u32(&sig[kSigOfree])) / kOutWarps); };
-      // ---- x: X = S0 W^T (the state path); U of the chunk before is no longer read after it
-      if (nx < n && nx < nb && (!WOUT || nd >= nx) && prog_s0() >= nx + 1 && prog_wk() >= nx + 1) {
-        if (leader) {
-          tc_fence_after();
-          const uint32_t wt = sb + late(nx) + kLOffWT;
+    // Lane 0 issues every MMA in a fixed order, waiting before each for the hand-offs it needs.  The
+    // tensor pipe runs MMAs in issue order, so the order decides the period: the state path
+    // x(c) -> U pass -> e(c) -> S0 pass -> x(c+1) is sequential.  y(c) follows x(c) and runs during
+    // the U pass; W^T of chunk c+1 goes in during the U pass too when its T1 is ready (else right
+    // after e(c)), so that the local warps have copied it out by the time S0 of chunk c+1 is ready;
+    // d(c) and U~^T of chunk c+1 follow e(c) and run during the S0 pass.  x(c+1) follows U~^T of
+    // chunk c+1, so the U pass's wait on x also covers U~.
+    if ((tid & 31) == 0) {
+      const uint32_t id64 = idesc_bf16(128, 64, 0, 0);
+      const uint32_t id64t = idesc_bf16(128, 64, 1, 0);    // A MN-major
+      const uint32_t id64n = idesc_bf16(128, 64, 0, 1);    // B MN-major
+      const uint32_t id128n = idesc_bf16(128, 128, 0, 1);  // B MN-major
+      bool ok = true, mma_issued = false;
+      auto ph = [](int m) { return (uint32_t)(m & 1); };
+      // w: W^T = K^T T1^T (chunk-local) into its tensor-memory tile, from the K slot and T1
+      auto issue_w = [&](int m) {
+        tc_fence_after();
+        const uint32_t kt = sb + kslot(m) + kKOffK;
+        const uint32_t t1 = sb + kSOffT1;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + kTW, sw128_desc(kt + ks * 2048, 8192, 1024), kmaj(t1 + ks * 32), id64t, ks > 0);
+        mma_commit(smem_u32(&bar_b));
+        mma_issued = true;
+      };
+      // u: U~^T = V^T T2^T (chunk-local) into the buffer of chunk m-2, whose U pass is done, once V
+      // of the chunk has landed (T2 came with K, before T1)
+      auto issue_u = [&](int m) -> bool {
+        if (!wait(&bar_v[m & 1], (uint32_t)((m >> 1) & 1))) return false;
+        tc_fence_after();
+        const uint32_t vt = sb + vslot(m);
+        const uint32_t t2 = sb + kslot(m) + kKOffT2;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tmem + kTU + 64u * (uint32_t)(m & 1), sw128_desc(vt + ks * 2048, 8192, 1024),
+                   kmaj(t2 + ks * 32), id64t, ks > 0);
+        mma_issued = true;
+        return true;
+      };
+      // prologue: the chunk-local products of chunk 0
+      if (n > 0) {
+        ok = wait(&bar_t1, 0);
+        if (ok) {
+          issue_w(0);
+          if (!ZV) ok = issue_u(0);
+        }
+      }
+      for (int c = 0; ok && c < n; ++c) {
+        const bool next = c + 1 < n;
+        // ---- x: X = S0 W^T, once S0 of the chunk is in tensor memory and W^T in its tile
+        ok = wait(&bar_s0, ph(c)) && wait(&bar_wk, ph(c));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint32_t wt = sb + kSOffWT;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             mma_bf16_ts(tmem + kTX, tmem + kTS0 + 8u * (uint32_t)ks, sw128_desc(wt + ks * 2048, 0, 1024), id64n,
                         ks > 0);
           mma_commit(smem_u32(&bar_x));
         }
-        __syncwarp();
-        mma_issued = true;
-        ++nx;
-        prog = true;
-      }
-      // ---- y: Y = S0 Q^T, once the outputs of the chunk before are drained
-      if (WOUT && ny < nx && (ny == 0 || prog_of() >= ny)) {
-        if (leader) {
+        // ---- y: Y = S0 Q^T, once the outputs of the chunk before are drained
+        if (WOUT) {
+          ok = c == 0 || wait(&bar_of, ph(c - 1));
+          if (!ok) break;
           tc_fence_after();
-          const uint32_t qt = sb + late(ny) + kLOffQ;
+          const uint32_t qt = sb + qslot(c) + kQOffQ;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t off = (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u;
             mma_bf16_ts(tmem + kTY, tmem + kTS0 + 8u * (uint32_t)ks, kmaj(qt + off), id64, ks > 0);
           }
         }
-        __syncwarp();
-        ++ny;
-        prog = true;
-      }
-      // ---- e: S~ += UD^T K (the state path); after y, which reads the S0 the update replaces
-      if (ne < nx && (!WOUT || ny > ne) && prog_u() >= ne + 1) {
-        if (leader) {
-          tc_fence_after();
-          const uint32_t kt = sb + early(ne) + kEOffK;
+        // ---- w of chunk c+1 now if T1 of it is ready (W^T of chunk c was copied out before x)
+        bool w_done = false;
+        if (next && mbar_test_wait(smem_u32(&bar_t1), ph(c + 1))) {
+          issue_w(c + 1);
+          w_done = true;
+        }
+        // ---- e: S~ += UD^T K, once the U pass is done
+        ok = wait(&bar_u, ph(c));
+        if (!ok) break;
+        tc_fence_after();
+        {
+          const uint32_t kt = sb + kslot(c) + kKOffK;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             mma_bf16(tmem + kTS, kmaj(sb + kSOffUD + ks * 32), sw128_desc(kt + ks * 2048, 8192, 1024), id128n, 1u);
           mma_commit(smem_u32(&bar_e));
         }
-        __syncwarp();
-        ++ne;
-        prog = true;
-      }
-      // ---- b: W^T = K^T T1^T, U~^T = V^T T2^T (chunk-local).  Needs T1 (so the early slot landed),
-      // W^T of the chunk before read, its U~ buffer read (U of chunk m-2) and the late slot free,
-      // since W^T is written there next.
-      if (nb < n && prog_t1() >= nb + 1 && (nb == 0 || prog_wk() >= nb) &&
-          (nb < 2 || (prog_u() >= nb - 1 && prog_s0() >= nb && (!WOUT || prog_of() >= nb - 1)))) {
-        if (leader) {
-          tc_fence_after();
-          const uint32_t es = sb + early(nb);
-          const uint32_t t1 = sb + kSOffT1;
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + kTW, sw128_desc(es + kEOffK + ks * 2048, 8192, 1024), kmaj(t1 + ks * 32), id64t, ks > 0);
-          if (!ZV) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_bf16(tmem + kTU + 64u * (uint32_t)(nb & 1), sw128_desc(es + kEOffV + ks * 2048, 8192, 1024),
-                       kmaj(es + kEOffT2 + ks * 32), id64t, ks > 0);
-          }
-          mma_commit(smem_u32(&bar_b));
+        if (next && !w_done && mbar_test_wait(smem_u32(&bar_t1), ph(c + 1))) {
+          issue_w(c + 1);
+          w_done = true;
         }
-        __syncwarp();
-        mma_issued = true;
-        ++nb;
-        prog = true;
-      }
-      // ---- d: Y += U^T P^T
-      if (WOUT && nd < ne) {
-        if (leader) {
+        // ---- d: Y += U^T P^T
+        if (WOUT) {
           tc_fence_after();
-          const uint32_t pp = sb + late(nd) + kLOffP;
+          const uint32_t pp = sb + qslot(c) + kQOffP;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             mma_bf16(tmem + kTY, kmaj(sb + kSOffU + ks * 32), kmaj(pp + ks * 32), id64, 1u);
           mma_commit(smem_u32(&bar_o));
         }
-        __syncwarp();
-        ++nd;
-        prog = true;
-      }
-      // idle-time limit, measured on the global timer every 4096 rounds without progress
-      if (prog) {
-        idle = 0;
-      } else if ((++idle & 4095u) == 0) {
-        const uint64_t now = __shfl_sync(kFullMask, globaltimer_ns(), 0);
-        if (idle == 4096u) {
-          t_idle = now;
-        } else if (now - t_idle > kWaitLimitNs) {
-          if (leader) atomicOr(status, kStatusTimeout);
-          ok = false;
+        if (next && !w_done) {
+          ok = wait(&bar_t1, ph(c + 1));
+          if (!ok) break;
+          issue_w(c + 1);
+        }
+        if (next && !ZV) {
+          ok = issue_u(c + 1);
+          if (!ok) break;
         }
       }
-    }
-    if (!ok) {
-      // let this CTA's own MMAs finish (bounded) before tensor memory is freed
-      if (mma_issued) {
-        if (leader) mma_commit(smem_u32(&bar_fin));
-        __syncwarp();
+      if (!ok && mma_issued) {
+        // let this CTA's own MMAs finish (bounded) before tensor memory is freed
+        mma_commit(smem_u32(&bar_fin));
         mbar_wait(smem_u32(&bar_fin), 0, status);
       }
     }
+    __syncwarp();
   } else if (warp == kLoader0 / 32) {
     // ======================================================================= copy issuer
-    // One warp issues the copies of every chunk into its ring slot as soon as the slot is free
-    // (read from the same progress counters); lane 0 alone issues.
+    // Lane 0 issues the copies of every chunk in order, each into its ring slot once the slot's
+    // earlier contents are no longer read: K and T2 of chunk m after the update of chunk m-3, V after
+    // U~ of chunk m-2, Q and P after the outputs of chunk m-2.
     const bool leader = (tid & 31) == 0;
-    int nkv = 0, nq = 0;
-    bool ok = true;
-    uint64_t t_idle = 0;
-    uint32_t idle = 0;
-    while (ok && (nkv < n || (WOUT && nq < n))) {
-      bool prog = false;
-      const int o_s0 = (int)(sig_load(smem_u32(&sig[kSigS0])) / kStateWarps);
-      const int o_of = (int)(sig_load(smem_u32(&sig[kSigOfree])) / kOutWarps);
-      // ---- copies.  Early slot of chunk m: the update of chunk m-2 is done (S0 of chunk m-1 written
-      // after it).  Late slot: that and the outputs (Y drained) of chunk m-2.
-      if (nkv < n && (nkv < 2 || o_s0 >= nkv)) {
-        if (leader) {
-          const uint32_t es = sb + early(nkv);
-          const uint32_t bar = smem_u32(&bar_kv[nkv & 1]);
-          const int t0 = (int)(wk.t_begin + (int64_t)nkv * kC);
-          mbar_arrive_expect_tx(bar, 16384u + (ZV ? 0u : 16384u) + 8192u);
-          tma_load_4d(es + kEOffK + 0, &tmap_k, 0, t0, h, b, bar);
-          tma_load_4d(es + kEOffK + 8192, &tmap_k, 64, t0, h, b, bar);
-          if (!ZV) {
-            tma_load_4d(es + kEOffV + 0, &tmap_v, 0, t0, h, b, bar);
-            tma_load_4d(es + kEOffV + 8192, &tmap_v, 64, t0, h, b, bar);
-          }
-          bulk_load(es + kEOffT2, rec + (rec0 + nkv) * kRec + kRecT2, 8192, bar);
-        }
-        __syncwarp();
-        ++nkv;
-        prog = true;
-      }
-      if (WOUT && nq < n && (nq < 2 || (o_s0 >= nq && o_of >= nq - 1))) {
-        if (leader) {
-          const uint32_t ls = sb + late(nq);
-          const uint32_t bar = smem_u32(&bar_q[nq & 1]);
-          const int t0 = (int)(wk.t_begin + (int64_t)nq * kC);
+    int nk = 0, nv = 0, nq = 0;
+    if (leader) {
+      bool ok = true;
+      for (int m = 0; ok && m < n; ++m) {
+        const int t0 = (int)(wk.t_begin + (int64_t)m * kC);
+        if (m >= kKSlots) ok = wait(&bar_kfree[m % kKSlots], kpar(m - kKSlots));
+        if (!ok) break;
+        {
+          const uint32_t kt = sb + kslot(m);
+          const uint32_t bar = smem_u32(&bar_k[m % kKSlots]);
           mbar_arrive_expect_tx(bar, 16384u + 8192u);
-          tma_load_4d(ls + kLOffQ + 0, &tmap_q, 0, t0, h, b, bar);
-          tma_load_4d(ls + kLOffQ + 8192, &tmap_q, 64, t0, h, b, bar);
-          bulk_load(ls + kLOffP, rec + (rec0 + nq) * kRec + kRecP, 8192, bar);
+          tma_load_4d(kt + kKOffK + 0, &tmap_k, 0, t0, h, b, bar);
+          tma_load_4d(kt + kKOffK + 8192, &tmap_k, 64, t0, h, b, bar);
+          bulk_load(kt + kKOffT2, rec + (rec0 + m) * kRec + kRecT2, 8192, bar);
+          ++nk;
         }
-        __syncwarp();
-        ++nq;
-        prog = true;
-      }
-      if (prog) {
-        idle = 0;
-      } else if ((++idle & 4095u) == 0) {
-        const uint64_t now = __shfl_sync(kFullMask, globaltimer_ns(), 0);
-        if (idle == 4096u) {
-          t_idle = now;
-        } else if (now - t_idle > kWaitLimitNs) {
-          if (leader) atomicOr(status, kStatusTimeout);
-          ok = false;
+        if (!ZV) {
+          if (m >= 2) ok = wait(&bar_vfree[m & 1], (uint32_t)(((m - 2) >> 1) & 1));
+          if (!ok) break;
+          const uint32_t vt = sb + vslot(m);
+          const uint32_t bar = smem_u32(&bar_v[m & 1]);
+          mbar_arrive_expect_tx(bar, 16384u);
+          tma_load_4d(vt + 0, &tmap_v, 0, t0, h, b, bar);
+          tma_load_4d(vt + 8192, &tmap_v, 64, t0, h, b, bar);
+          ++nv;
+        }
+        if (WOUT) {
+          if (m >= 2) ok = wait(&bar_qfree[m & 1], (uint32_t)(((m - 2) >> 1) & 1));
+          if (!ok) break;
+          const uint32_t qt = sb + qslot(m);
+          const uint32_t bar = smem_u32(&bar_q[m & 1]);
+          mbar_arrive_expect_tx(bar, 16384u + 8192u);
+          tma_load_4d(qt + kQOffQ + 0, &tmap_q, 0, t0, h, b, bar);
+          tma_load_4d(qt + kQOffQ + 8192, &tmap_q, 64, t0, h, b, bar);
+          bulk_load(qt + kQOffP, rec + (rec0 + m) * kRec + kRecP, 8192, bar);
+          ++nq;
         }
       }
     }
-    // let this CTA's own copies land (bounded) before the CTA exits; a buffer's phases complete in
+    nk = __shfl_sync(kFullMask, nk, 0);
+    nv = __shfl_sync(kFullMask, nv, 0);
+    nq = __shfl_sync(kFullMask, nq, 0);
+    // let this CTA's own copies land (bounded) before the CTA exits; a slot's phases complete in
     // order, so waiting for its last issued load covers the earlier ones
-    for (int m = nkv - 2; m < nkv; ++m)
-      if (m >= 0) mbar_wait(smem_u32(&bar_kv[m & 1]), (uint32_t)((m >> 1) & 1), status);
+    for (int m = nk - kKSlots; m < nk; ++m)
+      if (m >= 0) mbar_wait(smem_u32(&bar_k[m % kKSlots]), kpar(m), status);
+    for (int m = nv - 2; m < nv; ++m)
+      if (m >= 0) mbar_wait(smem_u32(&bar_v[m & 1]), (uint32_t)((m >> 1) & 1), status);
     for (int m = nq - 2; m < nq; ++m)
       if (m >= 0) mbar_wait(smem_u32(&bar_q[m & 1]), (uint32_t)((m >> 1) & 1), status);
   } else if (tid < kLocal0) {
@@ -598,7 +613,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       tmem_st_wait();
     }
     tc_fence_before();
-    warp_signal(smem_u32(&sig[kSigS0]));
+    warp_arrive(smem_u32(&bar_s0));
     ok = wait(&bar_gate[0], 0);  // the gates of a chunk are waited for a chunk ahead, off the sequential path
     float sigma = 1.f;  // S = sigma S~ after the latest update
     for (int c = 0; c < n; ++c) {
@@ -606,46 +621,63 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       // ---- U^T = U~^T - X and U^T diag(1 / (sigma gamma)), this row, columns [32 half, +32)
       ok = ok && wait(&bar_x, par);
       tc_fence_after();
+      warp_arrive(smem_u32(&bar_vfree[c & 1]));  // U~ of chunk c was done before x: V may be refilled
       {
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {  // 16 columns at a time
-          const int c0 = 32 * half + 16 * part;
-          float kd[16];  // 1/(sigma gamma_r) of these columns, loaded ahead of the tensor memory
-          const float4* kds = reinterpret_cast<const float4*>(slot(c) + kGKds + c0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 f = kds[q];
-            kd[4 * q] = f.x; kd[4 * q + 1] = f.y; kd[4 * q + 2] = f.z; kd[4 * q + 3] = f.w;
-          }
-          float x[16], u[16];
-          tmem_ld16(tlane + kTX + c0, x);
-          if (!ZV) tmem_ld16(tlane + kTU + 64 * par + c0, u);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; ++j) u[j] = (ZV ? 0.f : u[j]) - x[j];
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            *reinterpret_cast<uint4*>(sm + kSOffU + sw128_off(row, c0 + 8 * q, 128)) = pack8_bf16(u + 8 * q);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) u[j] *= kd[j];
-#pragma unroll
-          for (int q = 0; q < 2; ++q)
-            *reinterpret_cast<uint4*>(sm + kSOffUD + sw128_off(row, c0 + 8 * q, 128)) = pack8_bf16(u + 8 * q);
+        // all 32 columns [32 half, +32) of X and U~ in one round trip to tensor memory
+        const int c0 = 32 * half;
+        float x[32], u[32];
+        tmem_ld16(tlane + kTX + c0, *reinterpret_cast<float(*)[16]>(x));
+        tmem_ld16(tlane + kTX + c0 + 16, *reinterpret_cast<float(*)[16]>(x + 16));
+        if (!ZV) {
+          tmem_ld16(tlane + kTU + 64 * par + c0, *reinterpret_cast<float(*)[16]>(u));
+          tmem_ld16(tlane + kTU + 64 * par + c0 + 16, *reinterpret_cast<float(*)[16]>(u + 16));
         }
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) u[j] = (ZV ? 0.f : u[j]) - x[j];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(sm + kSOffU + sw128_off(row, c0 + 8 * q, 128)) = pack8_bf16(u + 8 * q);
+        const float4* kds = reinterpret_cast<const float4*>(slot(c) + kGKds + c0);  // 1/(sigma gamma_r)
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float4 f = kds[q];
+          u[4 * q] *= f.x; u[4 * q + 1] *= f.y; u[4 * q + 2] *= f.z; u[4 * q + 3] *= f.w;
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<uint4*>(sm + kSOffUD + sw128_off(row, c0 + 8 * q, 128)) = pack8_bf16(u + 8 * q);
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      warp_signal(smem_u32(&sig[kSigU]));
+      warp_arrive(smem_u32(&bar_u));
       // ---- after the update: S0 of chunk c+1 = sigma' S~, folding sigma' into S~ when small
       ok = ok && wait(&bar_e, par);
       tc_fence_after();
+      warp_arrive(smem_u32(&bar_kfree[c % kKSlots]));  // K and T2 of chunk c may be refilled
       const float* gs = slot(c);
       const float sig_after = gs[kGSigAfter];
       const bool fold = gs[kGFold] != 0.f;
       const bool has_next = c + 1 < n;
-      if (has_next || fold) {
+      if (!fold && has_next) {
+        // this thread's 64 state columns, 32 at a time
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {  // 32 state columns at a time
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t col = 64 * half + 32 * part;
+          float v[32];
+          tmem_ld16(tlane + kTS + col, *reinterpret_cast<float(*)[16]>(v));
+          tmem_ld16(tlane + kTS + col + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+          tmem_ld_wait();
+          uint32_t w[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) w[j] = pack2_bf16(v[2 * j] * sig_after, v[2 * j + 1] * sig_after);
+          tmem_st16u(tlane + kTS0 + col / 2, w);
+        }
+        tmem_st_wait();
+      } else if (fold) {
+        // sigma' folded into S~ (and S0 = S~ written if a chunk follows), 32 columns at a time
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
           const uint32_t col = 64 * half + 32 * part;
           float v[32];
           tmem_ld16(tlane + kTS + col, *reinterpret_cast<float(*)[16]>(v));
@@ -659,17 +691,15 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             for (int j = 0; j < 16; ++j) w[j] = pack2_bf16(v[2 * j], v[2 * j + 1]);
             tmem_st16u(tlane + kTS0 + col / 2, w);
           }
-          if (fold) {
-            tmem_st16(tlane + kTS + col, *reinterpret_cast<float(*)[16]>(v));
-            tmem_st16(tlane + kTS + col + 16, *reinterpret_cast<float(*)[16]>(v + 16));
-          }
+          tmem_st16(tlane + kTS + col, *reinterpret_cast<float(*)[16]>(v));
+          tmem_st16(tlane + kTS + col + 16, *reinterpret_cast<float(*)[16]>(v + 16));
         }
         tmem_st_wait();
       }
       sigma = fold ? 1.f : sig_after;
       if (has_next) {
         tc_fence_before();
-        warp_signal(smem_u32(&sig[kSigS0]));
+        warp_arrive(smem_u32(&bar_s0));
         ok = ok && wait(&bar_gate[(c + 1) % kGateSlots], gate_par(c + 1));
       }
     }
@@ -692,11 +722,17 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     bool ok = true;
     float sig_run = 1.f;  // sigma before the next chunk whose gates are formed
     const float* al_p = a.alpha + b * a.a_sb + h * a.a_sh;
-    // gates of chunk c: g = cumsum log alpha, gamma = e^g, 1/(sigma gamma), sigma bookkeeping
-    auto gates = [&](int c) {
-      float* gs = slot(c);
+    // alpha of chunk c for this thread's token (1 past the end), loaded a chunk before its gates are
+    // formed so that the load's latency is not on the local warps' path
+    auto load_alpha = [&](int c) {
       const int64_t t = wk.t_begin + (int64_t)c * kC + ltid;
-      float g = (ltid < kC && t < wk.t_end) ? logf(al_p[t]) : 0.f;
+      return (ltid < kC && c < n && t < wk.t_end) ? al_p[t] : 1.f;
+    };
+    // gates of chunk c from its alpha: g = cumsum log alpha, gamma = e^g, 1/(sigma gamma), sigma
+    // bookkeeping
+    auto gates = [&](int c, float al) {
+      float* gs = slot(c);
+      float g = ltid < kC ? logf(al) : 0.f;
       if (ltid < kC) {
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -729,9 +765,9 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     };
     // T1 = delta T2 diag(gamma) of chunk c (into the single T1 buffer; b of chunk c-1 has completed)
     auto t1_pass = [&](int c) {
-      ok = ok && wait(&bar_kv[c & 1], (uint32_t)((c >> 1) & 1));
+      ok = ok && wait(&bar_k[c % kKSlots], kpar(c));
       const float* gam = slot(c) + kGGam;
-      const uint8_t* t2 = sm + early(c) + kEOffT2;
+      const uint8_t* t2 = sm + kslot(c) + kKOffT2;
       const int r = ltid >> 1, j0 = (ltid & 1) * 32;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -744,11 +780,12 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         *reinterpret_cast<uint4*>(sm + kSOffT1 + off) = pack8_bf16(y);
       }
       fence_proxy_async_smem();
-      warp_signal(smem_u32(&sig[kSigT1]));
+      warp_arrive(smem_u32(&bar_t1));
     };
-    gates(0);
-    if (n > 1) gates(1);
-    if (n > 2) gates(2);
+    gates(0, load_alpha(0));
+    if (n > 1) gates(1, load_alpha(1));
+    if (n > 2) gates(2, load_alpha(2));
+    float al_next = load_alpha(3);
     t1_pass(0);
     for (int c = 0; c < n; ++c) {
       const uint32_t par = (uint32_t)(c & 1);
@@ -756,7 +793,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       ok = ok && wait(&bar_b, par);
       tc_fence_after();
       {
-        uint8_t* wt = sm + late(c) + kLOffWT;
+        uint8_t* wt = sm + kSOffWT;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {  // columns r, 32 at a time
           float w[32];
@@ -771,9 +808,13 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       fence_proxy_async_smem();
       tc_fence_before();
       if (WOUT) ok = ok && wait(&bar_q[c & 1], (uint32_t)((c >> 1) & 1));  // Q and P of the chunk landed
-      warp_signal(smem_u32(&sig[kSigWK]));
+      warp_arrive(smem_u32(&bar_wk));
       if (c + 1 < n) t1_pass(c + 1);
-      if (c + 3 < n) gates(c + 3);
+      if (c + 3 < n) {
+        const float al = al_next;
+        al_next = load_alpha(c + 4);
+        gates(c + 3, al);
+      }
     }
   } else if (tid < kIssuer0) {
     // ======================================================================= output warps
@@ -791,7 +832,8 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 #pragma unroll
         for (int r = 0; r < 64; ++r) y[r] *= a.q_scale * gam[r];
         tc_fence_before();
-        warp_signal(smem_u32(&sig[kSigOfree]));  // Y may be overwritten from here on
+        warp_arrive(smem_u32(&bar_of));  // Y may be overwritten from here on
+        warp_arrive(smem_u32(&bar_qfree[c & 1]));  // and Q, P of the chunk reloaded
         const int64_t t0 = wk.t_begin + (int64_t)c * kC;
         const int nvalid = (wk.t_end - t0 < kC) ? (int)(wk.t_end - t0) : kC;
         TOut* optr = reinterpret_cast<TOut*>(a.o) + b * a.o_sb + h * a.o_sh + t0 * a.o_st + i;

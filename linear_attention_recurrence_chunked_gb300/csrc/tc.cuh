@@ -100,6 +100,13 @@ __device__ __forceinline__ uint32_t sig_load(uint32_t addr) {
   asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
+// Relaxed read of a progress counter, for spinning; an acquire load of the
+// same counter once the spin has seen enough orders what follows.
+__device__ __forceinline__ uint32_t sig_load_relaxed(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.relaxed.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 // One count per warp once every lane got here (see warp_arrive).
 __device__ __forceinline__ void warp_signal(uint32_t addr) {
   __syncwarp();

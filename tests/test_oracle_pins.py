@@ -682,3 +682,22 @@ def test_notebank_route_ties_scaling_and_max_over_question():
     u2[0, 0, 0] = u2[1, 0, 1] = 1.0
     r3 = oracle.notebank_route(rho2, u2, R=1)
     assert list(r3["votes"]) == [1, 0, 1] and list(r3["top"]) == [0]
+
+
+def test_round_bf16_ties_to_even():
+    """Exact halfway cases of float32 -> bf16 go to the even mantissa (the rounding the GPU's
+    conversions use); values just off the halfway point go to the nearer neighbour."""
+    ulp = 2.0 ** -7  # bf16 spacing in [1, 2)
+    cases = [
+        (1.0 + ulp / 2, 1.0),                  # halfway between 1 and 1 + ulp: even is 1
+        (1.0 + 3 * ulp / 2, 1.0 + 2 * ulp),    # halfway between 1 + ulp and 1 + 2 ulp: even is 1 + 2 ulp
+        (-(1.0 + ulp / 2), -1.0),
+        (-(1.0 + 3 * ulp / 2), -(1.0 + 2 * ulp)),
+        (1.0 + ulp / 2 + 2.0 ** -23, 1.0 + ulp),  # one float32 ulp above halfway: up
+        (1.0 + ulp / 2 - 2.0 ** -23, 1.0),        # one below: down
+        (3.0 + 2.0 ** -7, 3.0),                # spacing 2^-6 in [2, 4): halfway to 3 + 2^-6, 3 is even
+        (0.0, 0.0),
+    ]
+    x = np.array([c[0] for c in cases], dtype=np.float32)
+    assert np.array_equal(x.astype(np.float64), np.array([c[0] for c in cases]))  # exact in float32
+    assert np.array_equal(oracle._round_bf16(x), np.array([c[1] for c in cases]))
