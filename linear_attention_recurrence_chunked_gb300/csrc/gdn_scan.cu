@@ -281,16 +281,13 @@ constexpr uint32_t kSOffV = kSOffK + kKSlots * kKSlot;  // 73728
 constexpr uint32_t kSOffQ = kSOffV + 2 * kVSlot;        // 106496
 constexpr uint32_t kSOffWT = kSOffQ + 2 * kQSlot;       // 155648
 constexpr uint32_t kSOffT1 = kSOffWT + 16384;           // T2 diag(gamma), one buffer
-constexpr uint32_t kSOffU = kSOffT1 + 8192;           // U^T [128 i][64 r]
-constexpr uint32_t kSOffUD = kSOffU + 16384;          // U^T diag(1 / (sigma gamma)) [128 i][64 r]
-constexpr uint32_t kSOffGate = kSOffUD + 16384;       // gate slots
+constexpr uint32_t kSOffGate = kSOffT1 + 8192;        // gate slots
 constexpr int kGateSlots = 8;
 constexpr uint32_t kGateSlot = 576;                   // gamma[64], 1/(sigma gamma)[64], scalars
 constexpr uint32_t kSSmemUsed = kSOffGate + kGateSlots * kGateSlot;
 constexpr uint32_t kSSmemAlloc = kSSmemUsed + 1024;
 static_assert(kKSlot % 1024 == 0 && kQSlot % 1024 == 0 && kSOffV % 1024 == 0 && kSOffQ % 1024 == 0 &&
-                  kSOffWT % 1024 == 0 && kSOffT1 % 1024 == 0 &&
-                  kSOffU % 1024 == 0 && kSOffUD % 1024 == 0,
+                  kSOffWT % 1024 == 0 && kSOffT1 % 1024 == 0,
               "MMA operand tiles sit on 1024-byte boundaries");
 static_assert(kSSmemAlloc + 512 <= 232448, "shared memory budget");
 // gate slot layout (floats)
@@ -302,6 +299,10 @@ constexpr uint32_t kTS0 = 128;  // S0 = bf16(sigma S~) [i][k], two per column (6
 constexpr uint32_t kTX = 192;   // X [i][r]
 constexpr uint32_t kTY = 256;   // Y [i][r]
 constexpr uint32_t kTU = 320;   // U~^T [i][r], two buffers (320..383, 384..447)
+// The U pass writes U (bf16, two per column) over the X columns it has read and U diag(1/(sigma gamma))
+// over the U~ columns it has read: tokens [32 h, +32) of row i go to columns [32 h, +16) of either
+// tile, so an MMA step over tokens [16 s, +16) reads A at column offset ua_off(s).
+__host__ __device__ constexpr uint32_t ua_off(int s) { return 32u * (uint32_t)(s >> 1) + 8u * (uint32_t)(s & 1); }
 constexpr uint32_t kTW = 448;   // W^T [k][r]
 constexpr uint32_t kTCols = 512;
 
@@ -417,6 +418,10 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       const uint32_t id128n = idesc_bf16(128, 128, 0, 1);  // B MN-major
       bool ok = true, mma_issued = false;
       auto ph = [](int m) { return (uint32_t)(m & 1); };
+      // a hand-off that has already happened costs one non-suspending test
+      auto wait_i = [&](uint64_t* bar, uint32_t parity) {
+        return mbar_test_wait(smem_u32(bar), parity) || wait(bar, parity);
+      };
       // w: W^T = K^T T1^T (chunk-local) into its tensor-memory tile, from the K slot and T1
       auto issue_w = [&](int m) {
         tc_fence_after();
@@ -431,7 +436,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       // u: U~^T = V^T T2^T (chunk-local) into the buffer of chunk m-2, whose U pass is done, once V
       // of the chunk has landed (T2 came with K, before T1)
       auto issue_u = [&](int m) -> bool {
-        if (!wait(&bar_v[m & 1], (uint32_t)((m >> 1) & 1))) return false;
+        if (!wait_i(&bar_v[m & 1], (uint32_t)((m >> 1) & 1))) return false;
         tc_fence_after();
         const uint32_t vt = sb + vslot(m);
         const uint32_t t2 = sb + kslot(m) + kKOffT2;
@@ -444,7 +449,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       };
       // prologue: the chunk-local products of chunk 0
       if (n > 0) {
-        ok = wait(&bar_t1, 0);
+        ok = wait_i(&bar_t1, 0);
         if (ok) {
           issue_w(0);
           if (!ZV) ok = issue_u(0);
@@ -453,7 +458,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       for (int c = 0; ok && c < n; ++c) {
         const bool next = c + 1 < n;
         // ---- x: X = S0 W^T, once S0 of the chunk is in tensor memory and W^T in its tile
-        ok = wait(&bar_s0, ph(c)) && wait(&bar_wk, ph(c));
+        ok = wait_i(&bar_s0, ph(c)) && wait_i(&bar_wk, ph(c));
         if (!ok) break;
         tc_fence_after();
         {
@@ -466,7 +471,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         }
         // ---- y: Y = S0 Q^T, once the outputs of the chunk before are drained
         if (WOUT) {
-          ok = c == 0 || wait(&bar_of, ph(c - 1));
+          ok = c == 0 || wait_i(&bar_of, ph(c - 1));
           if (!ok) break;
           tc_fence_after();
           const uint32_t qt = sb + qslot(c) + kQOffQ;
@@ -482,15 +487,16 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           issue_w(c + 1);
           w_done = true;
         }
-        // ---- e: S~ += UD^T K, once the U pass is done
-        ok = wait(&bar_u, ph(c));
+        // ---- e: S~ += UD^T K, once the U pass is done (UD from tensor memory)
+        ok = wait_i(&bar_u, ph(c));
         if (!ok) break;
         tc_fence_after();
         {
           const uint32_t kt = sb + kslot(c) + kKOffK;
+          const uint32_t ud = tmem + kTU + 64u * (uint32_t)(c & 1);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + kTS, kmaj(sb + kSOffUD + ks * 32), sw128_desc(kt + ks * 2048, 8192, 1024), id128n, 1u);
+            mma_bf16_ts(tmem + kTS, ud + ua_off(ks), sw128_desc(kt + ks * 2048, 8192, 1024), id128n, 1u);
           mma_commit(smem_u32(&bar_e));
         }
         if (next && !w_done && mbar_test_wait(smem_u32(&bar_t1), ph(c + 1))) {
@@ -503,11 +509,11 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           const uint32_t pp = sb + qslot(c) + kQOffP;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            mma_bf16(tmem + kTY, kmaj(sb + kSOffU + ks * 32), kmaj(pp + ks * 32), id64, 1u);
+            mma_bf16_ts(tmem + kTY, tmem + kTX + ua_off(ks), kmaj(pp + ks * 32), id64, 1u);
           mma_commit(smem_u32(&bar_o));
         }
         if (next && !w_done) {
-          ok = wait(&bar_t1, ph(c + 1));
+          ok = wait_i(&bar_t1, ph(c + 1));
           if (!ok) break;
           issue_w(c + 1);
         }
@@ -618,37 +624,35 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     float sigma = 1.f;  // S = sigma S~ after the latest update
     for (int c = 0; c < n; ++c) {
       const uint32_t par = (uint32_t)(c & 1);
-      // ---- U^T = U~^T - X and U^T diag(1 / (sigma gamma)), this row, columns [32 half, +32)
+      // ---- U^T = U~^T - X and U^T diag(1 / (sigma gamma)), this row, columns [32 half, +32), both bf16
+      // into tensor memory over the X and U~ columns this thread has just read
       ok = ok && wait(&bar_x, par);
       tc_fence_after();
       warp_arrive(smem_u32(&bar_vfree[c & 1]));  // U~ of chunk c was done before x: V may be refilled
-      {
-        // all 32 columns [32 half, +32) of X and U~ in one round trip to tensor memory
-        const int c0 = 32 * half;
-        float x[32], u[32];
-        tmem_ld16(tlane + kTX + c0, *reinterpret_cast<float(*)[16]>(x));
-        tmem_ld16(tlane + kTX + c0 + 16, *reinterpret_cast<float(*)[16]>(x + 16));
-        if (!ZV) {
-          tmem_ld16(tlane + kTU + 64 * par + c0, *reinterpret_cast<float(*)[16]>(u));
-          tmem_ld16(tlane + kTU + 64 * par + c0 + 16, *reinterpret_cast<float(*)[16]>(u + 16));
-        }
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {  // tokens [32 half + 16 part, +16)
+        const int c0 = 32 * half + 16 * part;
+        float x[16], u[16];
+        tmem_ld16(tlane + kTX + c0, x);
+        if (!ZV) tmem_ld16(tlane + kTU + 64 * par + c0, u);
         tmem_ld_wait();
+        uint32_t w[8];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) u[j] = (ZV ? 0.f : u[j]) - x[j];
+        for (int j = 0; j < 16; ++j) u[j] = (ZV ? 0.f : u[j]) - x[j];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(sm + kSOffU + sw128_off(row, c0 + 8 * q, 128)) = pack8_bf16(u + 8 * q);
+        for (int j = 0; j < 8; ++j) w[j] = pack2_bf16(u[2 * j], u[2 * j + 1]);
+        tmem_st8u(tlane + kTX + 32 * half + 8 * part, w);
         const float4* kds = reinterpret_cast<const float4*>(slot(c) + kGKds + c0);  // 1/(sigma gamma_r)
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 4; ++q) {
           const float4 f = kds[q];
           u[4 * q] *= f.x; u[4 * q + 1] *= f.y; u[4 * q + 2] *= f.z; u[4 * q + 3] *= f.w;
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          *reinterpret_cast<uint4*>(sm + kSOffUD + sw128_off(row, c0 + 8 * q, 128)) = pack8_bf16(u + 8 * q);
+        for (int j = 0; j < 8; ++j) w[j] = pack2_bf16(u[2 * j], u[2 * j + 1]);
+        tmem_st8u(tlane + kTU + 64 * par + 32 * half + 8 * part, w);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       warp_arrive(smem_u32(&bar_u));
       // ---- after the update: S0 of chunk c+1 = sigma' S~, folding sigma' into S~ when small
