@@ -433,6 +433,8 @@ constexpr size_t kCombineSmem = (size_t)kD * kEStride * 4 + (size_t)kD * kD * 4;
 __global__ void __launch_bounds__(kCombineThreads)
 gdn_segment_combine_kernel(const float* S_in, const float* maps, float* states, int G) {
   extern __shared__ float cs[];
+  grid_dependency_wait();  // the maps come from the kernel before (launched as its dependent)
+  grid_dependents_trigger();
   float* E = cs;                    // [128][129]
   float* M = cs + kD * kEStride;    // [128][128]
   const int64_t bh = blockIdx.x;
@@ -559,8 +561,8 @@ cudaError_t launch_gdn_segment_combine(const float* S_in, const float* maps, flo
                                     (int)kCombineSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  gdn_segment_combine_kernel<<<(unsigned)BH, kCombineThreads, kCombineSmem, stream>>>(S_in, maps, states, G);
-  return cudaGetLastError();
+  return launch_dependent(gdn_segment_combine_kernel, dim3((unsigned)BH), dim3(kCombineThreads), kCombineSmem, stream,
+                          S_in, maps, states, G);
 }
 
 // Number of sequence segments per (b,h).  With one CTA per SM, the three

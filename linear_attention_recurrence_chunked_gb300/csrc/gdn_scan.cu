@@ -401,6 +401,10 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);  // this warp's lane quarter
+  // launched as a dependent of the kernel before it: everything above overlapped its end; what
+  // follows reads the records, maps or entry states it wrote
+  grid_dependency_wait();
+  grid_dependents_trigger();
 
   if (warp == kIssuer0 / 32) {
     // ======================================================================= MMA issuer
@@ -881,23 +885,20 @@ cudaError_t launch_scan_typed(const GdnPrefillLaunch& a, void* ws, unsigned* sta
   const GdnSegPlan plan = gdn_segment_plan(a.B, a.H, a.N);
   if (plan.G == 1) {
     const GdnTask task{kWhole, 1, a.N, nullptr, nullptr};
-    gdn_scan_kernel<TOut><<<(unsigned)BH, kScanThreads, kSSmemAlloc, stream>>>(mq, mk, mv, a, task, (int)nch, recT,
-                                                                            status);
-    return cudaGetLastError();
+    return launch_dependent(gdn_scan_kernel<TOut>, dim3((unsigned)BH), dim3(kScanThreads), kSSmemAlloc, stream, mq,
+                            mk, mv, a, task, (int)nch, (const uint8_t*)recT, status);
   }
   float* maps = seg;
   float* states = maps + BH * (plan.G - 1) * 2 * kStateElems;
   const GdnTask t1{kSegmentMaps, plan.G, plan.seg_len, maps, nullptr};
-  gdn_scan_kernel<TOut><<<(unsigned)(BH * (plan.G - 1) * 2), kScanThreads, kSSmemAlloc, stream>>>(
-      mq, mk, mv, a, t1, (int)nch, recT, status);
-  e = cudaGetLastError();
+  e = launch_dependent(gdn_scan_kernel<TOut>, dim3((unsigned)(BH * (plan.G - 1) * 2)), dim3(kScanThreads), kSSmemAlloc,
+                       stream, mq, mk, mv, a, t1, (int)nch, (const uint8_t*)recT, status);
   if (e != cudaSuccess) return e;
   e = launch_gdn_segment_combine(a.S_in, maps, states, plan.G, BH, stream);
   if (e != cudaSuccess) return e;
   const GdnTask t2{kSegmentOutputs, plan.G, plan.seg_len, nullptr, states};
-  gdn_scan_kernel<TOut><<<(unsigned)(BH * plan.G), kScanThreads, kSSmemAlloc, stream>>>(mq, mk, mv, a, t2, (int)nch,
-                                                                                     recT, status);
-  return cudaGetLastError();
+  return launch_dependent(gdn_scan_kernel<TOut>, dim3((unsigned)(BH * plan.G)), dim3(kScanThreads), kSSmemAlloc, stream,
+                          mq, mk, mv, a, t2, (int)nch, (const uint8_t*)recT, status);
 }
 
 }  // namespace

@@ -53,6 +53,7 @@ __device__ __forceinline__ void load_row(const T* row, float (&x)[PER]) {
 template <typename T, int PER>
 __global__ void __launch_bounds__(kScoreThreads)
 notebank_chunk_scores_kernel(NotebankScoresLaunch a) {
+  grid_dependents_trigger();  // the channel-mean kernel may be scheduled once every CTA is resident
   __shared__ float part[kScoreThreads / 32][kMaxD];
   __shared__ float mu[kMaxD];
   __shared__ float inv_norm[1024];  // per token of the chunk (chunk <= 1024)
@@ -163,6 +164,7 @@ notebank_chunk_scores_cluster_kernel(NotebankScoresLaunch a, int sub) {
   __shared__ float part[kScoreThreads / 32][kMaxD];
   __shared__ float cpart[kMaxD];  // this CTA's sum of unit keys, read by the whole cluster
   __shared__ float mu[kMaxD];
+  grid_dependents_trigger();  // the channel-mean kernel may be scheduled once every CTA is resident
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = (int)cluster.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -289,6 +291,8 @@ notebank_chunk_scores_cluster_kernel(NotebankScoresLaunch a, int sub) {
 __global__ void __launch_bounds__(kScoreThreads)
 notebank_token_scores_kernel(NotebankScoresLaunch a) {
   extern __shared__ float dsm[];  // kScoreThreads + window - 1 token means
+  grid_dependency_wait();  // the channel scores come from the kernel before (launched as its dependent)
+  grid_dependents_trigger();
   const int64_t t0 = (int64_t)blockIdx.x * kScoreThreads;
   const int64_t J = a.L * a.H;
   const float invJ = 1.f / (float)J;
@@ -314,6 +318,7 @@ notebank_token_scores_kernel(NotebankScoresLaunch a) {
 template <typename T>
 __global__ void __launch_bounds__(256)
 notebank_address_kernel(NotebankAddressLaunch a, unsigned* status) {
+  grid_dependency_wait();  // the channel scores may come from the kernels just before
   const int64_t J = a.L * a.H;
   const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;  // (note, channel)
   const int lane = threadIdx.x & 31;
@@ -529,17 +534,15 @@ cudaError_t launch_notebank_scores(const NotebankScoresLaunch& a, cudaStream_t s
   if (e != cudaSuccess) return e;
   const unsigned grid = (unsigned)((a.N + kScoreThreads - 1) / kScoreThreads);
   const size_t smem = (size_t)(kScoreThreads + a.window - 1) * sizeof(float);
-  notebank_token_scores_kernel<<<grid, kScoreThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_dependent(notebank_token_scores_kernel, dim3(grid), dim3(kScoreThreads), smem, stream, a);
 }
 
 cudaError_t launch_notebank_address(const NotebankAddressLaunch& a, unsigned* status, cudaStream_t stream) {
   const int64_t warps = a.n_notes * a.L * a.H;
   if (warps == 0) return cudaSuccess;
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
-  if (a.in_bf16) notebank_address_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(a, status);
-  else notebank_address_kernel<float><<<grid, 256, 0, stream>>>(a, status);
-  return cudaGetLastError();
+  if (a.in_bf16) return launch_dependent(notebank_address_kernel<__nv_bfloat16>, dim3(grid), dim3(256), 0, stream, a, status);
+  return launch_dependent(notebank_address_kernel<float>, dim3(grid), dim3(256), 0, stream, a, status);
 }
 
 cudaError_t launch_notebank_route(const NotebankRouteLaunch& a, cudaStream_t stream) {
