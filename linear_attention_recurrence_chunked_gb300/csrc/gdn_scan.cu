@@ -165,6 +165,17 @@ __device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, 
   }
 }
 
+// T2 = diag(beta), the image for delta = 0 (L = 0, so T = I): thread r = tid / 4, 16 columns from c0.
+__device__ __forceinline__ void t2_identity(int tid, const float* bt, uint8_t* t2_tile) {
+  const int r = tid >> 2, c0 = (tid & 3) * 16;
+  float t2[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t2[j] = (c0 + j == r) ? bt[r] : 0.f;
+#pragma unroll
+  for (int q = 0; q < 2; ++q)
+    *reinterpret_cast<uint4*>(t2_tile + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t2 + 8 * q);
+}
+
 __global__ void __launch_bounds__(kThreads, 4)
 gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const GdnPrefillLaunch a, int nch, uint8_t* rec_out, unsigned* status) {
@@ -236,7 +247,8 @@ gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     phase_L_Po(tlane + 32 * half, row, half, gate, Lsm, sm + kIOffP, 1.f, a.delta, false);
     tc_fence_before();
     __syncthreads();
-    invert_T(tid, Lsm, Tsm, Zsm, gate + kC, sm + kIOffT2);
+    if (a.delta != 0.f) invert_T(tid, Lsm, Tsm, Zsm, gate + kC, sm + kIOffT2);
+    else t2_identity(tid, gate + kC, sm + kIOffT2);  // the scalar gate: no inverse to form
     fence_proxy_async_smem();
     __syncthreads();
     if (tid == 0) {
@@ -318,7 +330,10 @@ constexpr float kFoldBelow = 2.3283064e-10f;         // 2^-32
 // One CTA per SM (shared memory and all 512 tensor-memory columns).  Warps
 // take registers in groups of four, so the 18 warps are budgeted as 20: at
 // most 96 registers a thread; the wide passes work on 32 columns at a time.
-template <typename TOut>
+// GATED: the scalar gate (delta = 0), where W = 0 and X = 0, so U = U~ needs nothing from the state:
+// the sequential path shrinks to e(c) -> S0 pass -> e(c+1), with y and d off it, S0 double-buffered in
+// tensor memory (the X columns, unused then, hold the copy of odd chunks) and U in the W^T columns.
+template <typename TOut, bool GATED>
 __global__ void __launch_bounds__(kScanThreads, 1)
 gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const GdnPrefillLaunch a, const GdnTask task,
@@ -363,6 +378,9 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   auto vslot = [&](int c) { return kSOffV + (uint32_t)(c & 1) * kVSlot; };
   auto qslot = [&](int c) { return kSOffQ + (uint32_t)(c & 1) * kQSlot; };
   auto wait = [&](uint64_t* bar, uint32_t parity) { return mbar_wait(smem_u32(bar), parity, status); };
+  // tensor-memory columns of the bf16 state copy S0 of chunk c, and of U
+  auto s0col = [&](int c) { return (GATED && (c & 1)) ? kTX : kTS0; };
+  constexpr uint32_t kTUb = GATED ? kTW : kTX;
 
   if (tid == 0) {
     for (int i = 0; i < kKSlots; ++i) {
@@ -405,6 +423,37 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   // follows reads the records, maps or entry states it wrote
   grid_dependency_wait();
   grid_dependents_trigger();
+  // U pass of chunk c for this thread's row (its warp's lane quarter), tokens [32 h, +32):
+  // U^T = U~^T - X and U^T diag(1 / (sigma gamma)), both bf16, into tensor memory over the X (the W^T
+  // columns for the scalar gate) and U~ columns this thread has just read
+  auto u_pass = [&](int c, int h) {
+    const uint32_t par = (uint32_t)(c & 1);
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {  // tokens [32 h + 16 part, +16)
+      const int c0 = 32 * h + 16 * part;
+      float x[16], u[16];
+      if constexpr (!GATED) tmem_ld16(tlane + kTX + c0, x);  // the scalar gate has X = 0
+      if (!ZV) tmem_ld16(tlane + kTU + 64 * par + c0, u);
+      tmem_ld_wait();
+      uint32_t w[8];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) u[j] = (ZV ? 0.f : u[j]) - (GATED ? 0.f : x[j]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = pack2_bf16(u[2 * j], u[2 * j + 1]);
+      tmem_st8u(tlane + kTUb + 32 * h + 8 * part, w);
+      const float4* kds = reinterpret_cast<const float4*>(slot(c) + kGKds + c0);  // 1/(sigma gamma_r)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 f = kds[q];
+        u[4 * q] *= f.x; u[4 * q + 1] *= f.y; u[4 * q + 2] *= f.z; u[4 * q + 3] *= f.w;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) w[j] = pack2_bf16(u[2 * j], u[2 * j + 1]);
+      tmem_st8u(tlane + kTU + 64 * par + 32 * h + 8 * part, w);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+  };
 
   if (warp == kIssuer0 / 32) {
     // ======================================================================= MMA issuer
@@ -451,6 +500,51 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         mma_issued = true;
         return true;
       };
+      if constexpr (GATED) {
+        // u of chunk m once K with T2 (its slot) and V have landed, then the commit the U pass waits on
+        auto issue_ug = [&](int m) -> bool {
+          if (!wait_i(&bar_k[m % kKSlots], kpar(m))) return false;
+          if (!ZV && !issue_u(m)) return false;
+          mma_commit(smem_u32(&bar_x));
+          mma_issued = true;
+          return true;
+        };
+        if (n > 0) ok = issue_ug(0);
+        for (int c = 0; ok && c < n; ++c) {
+          // ---- e: S~ += UD^T K, once U of the chunk is written and the S0 pass of the chunk before has
+          // read the S~ this update changes
+          ok = wait_i(&bar_u, ph(c)) && wait_i(&bar_s0, ph(c));
+          if (!ok) break;
+          tc_fence_after();
+          {
+            const uint32_t kt = sb + kslot(c) + kKOffK;
+            const uint32_t ud = tmem + kTU + 64u * (uint32_t)(c & 1);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16_ts(tmem + kTS, ud + ua_off(ks), sw128_desc(kt + ks * 2048, 8192, 1024), id128n, 1u);
+            mma_commit(smem_u32(&bar_e));
+          }
+          if (WOUT) {
+            // ---- y: Y = S0 Q^T from the chunk's own S0 buffer, once Q and P have landed and the outputs
+            // of the chunk before are drained; d: Y += U^T P^T
+            ok = (c == 0 || wait_i(&bar_of, ph(c - 1))) && wait_i(&bar_q[c & 1], (uint32_t)((c >> 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t qt = sb + qslot(c) + kQOffQ;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+              const uint32_t off = (uint32_t)(ks >> 2) * 8192u + (uint32_t)(ks & 3) * 32u;
+              mma_bf16_ts(tmem + kTY, tmem + s0col(c) + 8u * (uint32_t)ks, kmaj(qt + off), id64, ks > 0);
+            }
+            const uint32_t pp = sb + qslot(c) + kQOffP;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16_ts(tmem + kTY, tmem + kTUb + ua_off(ks), kmaj(pp + ks * 32), id64, 1u);
+            mma_commit(smem_u32(&bar_o));
+          }
+          if (c + 1 < n) ok = issue_ug(c + 1);
+        }
+      } else {
       // prologue: the chunk-local products of chunk 0
       if (n > 0) {
         ok = wait_i(&bar_t1, 0);
@@ -525,6 +619,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           ok = issue_u(c + 1);
           if (!ok) break;
         }
+      }
       }
       if (!ok && mma_issued) {
         // let this CTA's own MMAs finish (bounded) before tensor memory is freed
@@ -628,36 +723,11 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     float sigma = 1.f;  // S = sigma S~ after the latest update
     for (int c = 0; c < n; ++c) {
       const uint32_t par = (uint32_t)(c & 1);
-      // ---- U^T = U~^T - X and U^T diag(1 / (sigma gamma)), this row, columns [32 half, +32), both bf16
-      // into tensor memory over the X and U~ columns this thread has just read
+      // ---- U of chunk c, this row, tokens [32 half, +32)
       ok = ok && wait(&bar_x, par);
       tc_fence_after();
-      warp_arrive(smem_u32(&bar_vfree[c & 1]));  // U~ of chunk c was done before x: V may be refilled
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {  // tokens [32 half + 16 part, +16)
-        const int c0 = 32 * half + 16 * part;
-        float x[16], u[16];
-        tmem_ld16(tlane + kTX + c0, x);
-        if (!ZV) tmem_ld16(tlane + kTU + 64 * par + c0, u);
-        tmem_ld_wait();
-        uint32_t w[8];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) u[j] = (ZV ? 0.f : u[j]) - x[j];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = pack2_bf16(u[2 * j], u[2 * j + 1]);
-        tmem_st8u(tlane + kTX + 32 * half + 8 * part, w);
-        const float4* kds = reinterpret_cast<const float4*>(slot(c) + kGKds + c0);  // 1/(sigma gamma_r)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 f = kds[q];
-          u[4 * q] *= f.x; u[4 * q + 1] *= f.y; u[4 * q + 2] *= f.z; u[4 * q + 3] *= f.w;
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = pack2_bf16(u[2 * j], u[2 * j + 1]);
-        tmem_st8u(tlane + kTU + 64 * par + 32 * half + 8 * part, w);
-      }
-      tmem_st_wait();
-      tc_fence_before();
+      warp_arrive(smem_u32(&bar_vfree[c & 1]));  // U~ of chunk c was done (before x): V may be refilled
+      u_pass(c, half);
       warp_arrive(smem_u32(&bar_u));
       // ---- after the update: S0 of chunk c+1 = sigma' S~, folding sigma' into S~ when small
       ok = ok && wait(&bar_e, par);
@@ -679,7 +749,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           uint32_t w[16];
 #pragma unroll
           for (int j = 0; j < 16; ++j) w[j] = pack2_bf16(v[2 * j] * sig_after, v[2 * j + 1] * sig_after);
-          tmem_st16u(tlane + kTS0 + col / 2, w);
+          tmem_st16u(tlane + s0col(c + 1) + col / 2, w);
         }
         tmem_st_wait();
       } else if (fold) {
@@ -697,7 +767,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
             uint32_t w[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) w[j] = pack2_bf16(v[2 * j], v[2 * j + 1]);
-            tmem_st16u(tlane + kTS0 + col / 2, w);
+            tmem_st16u(tlane + s0col(c + 1) + col / 2, w);
           }
           tmem_st16(tlane + kTS + col, *reinterpret_cast<float(*)[16]>(v));
           tmem_st16(tlane + kTS + col + 16, *reinterpret_cast<float(*)[16]>(v + 16));
@@ -794,6 +864,17 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     if (n > 1) gates(1, load_alpha(1));
     if (n > 2) gates(2, load_alpha(2));
     float al_next = load_alpha(3);
+    if constexpr (GATED) {
+      // no T1 and no W^T: only the gates, three chunks ahead, paced by the updates (the gate slot of
+      // chunk c+3 last served chunk c-5, whose S0 pass and outputs were done before the update of
+      // chunk c)
+      for (int c = 0; c + 3 < n; ++c) {
+        ok = ok && wait(&bar_e, (uint32_t)(c & 1));
+        const float al = al_next;
+        al_next = load_alpha(c + 4);
+        gates(c + 3, al);
+      }
+    } else {
     t1_pass(0);
     for (int c = 0; c < n; ++c) {
       const uint32_t par = (uint32_t)(c & 1);
@@ -823,6 +904,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
         al_next = load_alpha(c + 4);
         gates(c + 3, al);
       }
+    }
     }
   } else if (tid < kIssuer0) {
     // ======================================================================= output warps
@@ -871,9 +953,13 @@ cudaError_t launch_scan_typed(const GdnPrefillLaunch& a, void* ws, unsigned* sta
   std::call_once(attr_once, [] {
     attr_err = cudaFuncSetAttribute(gdn_tinv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kISmemAlloc);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(gdn_scan_kernel<TOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      attr_err = cudaFuncSetAttribute(gdn_scan_kernel<TOut, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kSSmemAlloc);
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(gdn_scan_kernel<TOut, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kSSmemAlloc);
   });
+  auto scan = a.delta == 0.f ? gdn_scan_kernel<TOut, true> : gdn_scan_kernel<TOut, false>;
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t BH = a.B * a.H;
   const int64_t nch = (a.N + kC - 1) / kC;
@@ -885,19 +971,19 @@ cudaError_t launch_scan_typed(const GdnPrefillLaunch& a, void* ws, unsigned* sta
   const GdnSegPlan plan = gdn_segment_plan(a.B, a.H, a.N);
   if (plan.G == 1) {
     const GdnTask task{kWhole, 1, a.N, nullptr, nullptr};
-    return launch_dependent(gdn_scan_kernel<TOut>, dim3((unsigned)BH), dim3(kScanThreads), kSSmemAlloc, stream, mq,
+    return launch_dependent(scan, dim3((unsigned)BH), dim3(kScanThreads), kSSmemAlloc, stream, mq,
                             mk, mv, a, task, (int)nch, (const uint8_t*)recT, status);
   }
   float* maps = seg;
   float* states = maps + BH * (plan.G - 1) * 2 * kStateElems;
   const GdnTask t1{kSegmentMaps, plan.G, plan.seg_len, maps, nullptr};
-  e = launch_dependent(gdn_scan_kernel<TOut>, dim3((unsigned)(BH * (plan.G - 1) * 2)), dim3(kScanThreads), kSSmemAlloc,
+  e = launch_dependent(scan, dim3((unsigned)(BH * (plan.G - 1) * 2)), dim3(kScanThreads), kSSmemAlloc,
                        stream, mq, mk, mv, a, t1, (int)nch, (const uint8_t*)recT, status);
   if (e != cudaSuccess) return e;
   e = launch_gdn_segment_combine(a.S_in, maps, states, plan.G, BH, stream);
   if (e != cudaSuccess) return e;
   const GdnTask t2{kSegmentOutputs, plan.G, plan.seg_len, nullptr, states};
-  return launch_dependent(gdn_scan_kernel<TOut>, dim3((unsigned)(BH * plan.G)), dim3(kScanThreads), kSSmemAlloc, stream,
+  return launch_dependent(scan, dim3((unsigned)(BH * plan.G)), dim3(kScanThreads), kSSmemAlloc, stream,
                           mq, mk, mv, a, t2, (int)nch, (const uint8_t*)recT, status);
 }
 
