@@ -173,10 +173,12 @@ swa_decode_kernel(SwaDecodeLaunch a) {
   }
 }
 
-// The same step with the window staged in shared memory (d = D of 64 or 128, 16-byte aligned caches):
-// each warp copies its whole key and value window in one round of 16-byte cp.async copies, rows
-// padded by 16 bytes (a lane per row then reads without bank conflicts), replaces the copy of the
-// new token's slot with the new k, v and works from shared memory only.
+// The same step with the key window staged in shared memory (d = D of 64 or 128, 16-byte aligned
+// caches): each warp copies its whole key window in one round of 16-byte cp.async copies, rows padded
+// by 16 bytes (a lane per row then reads without bank conflicts), and replaces the copy of the new
+// token's slot with the new k.  The values are read straight from the cache (one coalesced row per
+// warp load, eight rows in flight), so a warp's shared memory is half what staging both would take
+// and twice as many warps fit on an SM.
 template <typename TIn, typename TOut, int D>
 __global__ void __launch_bounds__(32 * kWarps)
 swa_decode_staged_kernel(SwaDecodeLaunch a) {
@@ -201,14 +203,12 @@ swa_decode_staged_kernel(SwaDecodeLaunch a) {
   }
   const int slot_new = (int)(pos % w);
   const int n = pos + 1 < w ? (int)(pos + 1) : w;
-  uint8_t* ks = sw_smem + (size_t)warp * 2 * w * kPitch;
-  uint8_t* vs = ks + (size_t)w * kPitch;
+  uint8_t* ks = sw_smem + (size_t)warp * w * kPitch;
   const uint8_t* kc = reinterpret_cast<const uint8_t*>(a.k_cache) + sh * (int64_t)w * kRowBytes;
-  const uint8_t* vc = reinterpret_cast<const uint8_t*>(a.v_cache) + sh * (int64_t)w * kRowBytes;
+  const TIn* vcache = reinterpret_cast<const TIn*>(a.v_cache) + sh * (int64_t)w * D;
   for (int i = lane; i < n * kVec; i += 32) {
     const int r = i / kVec, c = i - r * kVec;
     tc::cp_async16(tc::smem_u32(ks + r * kPitch + c * 16), kc + (int64_t)r * kRowBytes + c * 16, 16u);
-    tc::cp_async16(tc::smem_u32(vs + r * kPitch + c * 16), vc + (int64_t)r * kRowBytes + c * 16, 16u);
   }
   tc::cp_async_commit();
   // meanwhile: q (scaled) and the new token into the ring buffer
@@ -227,12 +227,10 @@ swa_decode_staged_kernel(SwaDecodeLaunch a) {
   }
   tc::cp_async_wait_all();
   __syncwarp();
-  // the staged copy of the new token's slot may hold the old token: overwrite it
+  // the staged copy of the new token's slot may hold the old token: overwrite it (the value cache
+  // itself already holds the new v: this warp's own stores, ordered by the __syncwarp)
 #pragma unroll
-  for (int e = 0; e < kCpl; ++e) {
-    reinterpret_cast<TIn*>(ks + slot_new * kPitch)[lane * kCpl + e] = knew[e];
-    reinterpret_cast<TIn*>(vs + slot_new * kPitch)[lane * kCpl + e] = vnew[e];
-  }
+  for (int e = 0; e < kCpl; ++e) reinterpret_cast<TIn*>(ks + slot_new * kPitch)[lane * kCpl + e] = knew[e];
   __syncwarp();
   // scores of this lane's slots
   float sc[kSlotsPerLane];
@@ -282,33 +280,13 @@ swa_decode_staged_kernel(SwaDecodeLaunch a) {
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) l += __shfl_xor_sync(kFullMask, l, off);
   __syncwarp();
-  // o = sum_j p_j v_j / l, lane l owning columns [kCpl l, kCpl l + kCpl), four slots in flight
-  float acc[4][kCpl];
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
-#pragma unroll
-    for (int e = 0; e < kCpl; ++e) acc[u][e] = 0.f;
-  const uint8_t* vl = vs + lane * kCpl * (int)sizeof(TIn);
-  int j = 0;
-  for (; j + 4 <= n; j += 4) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const TIn* vr = reinterpret_cast<const TIn*>(vl + (j + u) * kPitch);
-      const float pj = ps[warp][j + u];
-#pragma unroll
-      for (int e = 0; e < kCpl; ++e) acc[u][e] = fmaf(pj, to_f(vr[e]), acc[u][e]);
-    }
-  }
-  for (; j < n; ++j) {
-    const TIn* vr = reinterpret_cast<const TIn*>(vl + j * kPitch);
-    const float pj = ps[warp][j];
-#pragma unroll
-    for (int e = 0; e < kCpl; ++e) acc[0][e] = fmaf(pj, to_f(vr[e]), acc[0][e]);
-  }
+  // o = sum_j p_j v_j / l from the value cache, lane l owning columns [kCpl l, kCpl l + kCpl)
+  float o[4];
+  weighted_sum<kCpl>(vcache, D, n, ps[warp], lane, o);
   const float inv = 1.f / l;
   TOut* out = reinterpret_cast<TOut*>(a.out) + sh * D;
 #pragma unroll
-  for (int e = 0; e < kCpl; ++e) store1(out + lane * kCpl + e, ((acc[0][e] + acc[1][e]) + (acc[2][e] + acc[3][e])) * inv);
+  for (int e = 0; e < kCpl; ++e) store1(out + lane * kCpl + e, o[e] * inv);
 }
 
 // The staged kernel for d = D: warps per CTA so that their windows fit in shared memory, 0 if even one
@@ -316,7 +294,7 @@ swa_decode_staged_kernel(SwaDecodeLaunch a) {
 template <typename TIn, typename TOut, int D>
 cudaError_t launch_staged(const SwaDecodeLaunch& a, cudaStream_t stream, bool& done) {
   constexpr int64_t kMaxDynamic = 200 * 1024;
-  const int64_t per_warp = 2 * (int64_t)a.window * (D * (int64_t)sizeof(TIn) + 16);
+  const int64_t per_warp = (int64_t)a.window * (D * (int64_t)sizeof(TIn) + 16);
   const int wpc = (int)std::min<int64_t>(kWarps, kMaxDynamic / per_warp);
   done = false;
   if (wpc == 0) return cudaSuccess;
