@@ -89,12 +89,13 @@ __device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, 
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) Tsm[(base + r) * kTPad + base + col] = x[r];
-  } else {
-    // the blocks above the 16x16 block diagonal are zero
-    for (int e = tid - kC; e < kC * kC; e += kThreads - kC) {
-      const int r = e >> 6, c = e & 63;
-      if ((c >> 4) > (r >> 4)) Tsm[r * kTPad + c] = 0.f;
-    }
+  } else if (tid < kC + 128) {
+    // zero the two 16x16 blocks above the diagonal that the 64x64 step reads as part of its 32x32
+    // diagonal blocks (rows 0-15 x columns 16-31, rows 32-47 x columns 48-63), a float4 per thread;
+    // the T2 pass masks everything else above the diagonal
+    const int e = tid - kC, blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4;
+    const int r0 = blk * 32, c0 = blk * 32 + 16;
+    *reinterpret_cast<float4*>(Tsm + (r0 + r) * kTPad + c0 + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   __syncthreads();
   {
@@ -154,10 +155,11 @@ __device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, 
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const float4 tv = *reinterpret_cast<const float4*>(tr + 4 * q);
-      t2[4 * q] = tv.x * bt[c0 + 4 * q];
-      t2[4 * q + 1] = tv.y * bt[c0 + 4 * q + 1];
-      t2[4 * q + 2] = tv.z * bt[c0 + 4 * q + 2];
-      t2[4 * q + 3] = tv.w * bt[c0 + 4 * q + 3];
+      const int c = c0 + 4 * q;  // T is lower triangular: entries above the diagonal were not formed
+      t2[4 * q] = c <= r ? tv.x * bt[c] : 0.f;
+      t2[4 * q + 1] = c + 1 <= r ? tv.y * bt[c + 1] : 0.f;
+      t2[4 * q + 2] = c + 2 <= r ? tv.z * bt[c + 2] : 0.f;
+      t2[4 * q + 3] = c + 3 <= r ? tv.w * bt[c + 3] : 0.f;
     }
 #pragma unroll
     for (int q = 0; q < 2; ++q)
