@@ -61,6 +61,9 @@ BYTES_PER_TOKEN_HEAD = {"taylor_prefill": 320, "gdn_prefill": 1032,
                         # token's k, v written into the ring, q, k, v read, o written
                         "swa_decode": 2 * 64 * 64 * 2 + 2 * 64 * 2 + 3 * 64 * 2 + 64 * 2}
 SWA_WINDOW, SWA_D = 64, 64
+# fp32 FMA rate of the CUDA cores (no tensor cores): 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (the maximum SM
+# clock); the peak the routing kernel's cosines are measured against
+FP32_ALU_TFLOPS = round(152 * 128 * 2 * 2.07e9 / 1e12, 1)
 STATE_BYTES = {"taylor": (273 * 64 + 273) * 4, "gdn": 128 * 128 * 4}
 
 
@@ -474,7 +477,8 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         byts = sum(a.numel() * a.element_size() for a in (x["q"], x["k"], x["v"], y, s, z))
         out["taylor_fp32_small"] = {"workload": w.description, "tokens_per_s": round(whole_job_rate(w.B * w.N, ws,
                                                                                                  ms * 1e-3), 1),
-                                    "ms": round(ms, 4), "roofline": roofline(byts, ms, pk["hbm_gbs"], None)}
+                                    "ms": round(ms, 4),
+                                    "roofline": roofline(byts, ms, pk["hbm_gbs"], ncu_traffic("taylor_fp32_small"))}
         del x, y, s, z, wsf
     for name in ("gdn_prefill", "gdn_prefill_long", "gated_prefill"):
         if only is not None and name != only:
@@ -670,7 +674,10 @@ def notebank_paths(args, la, dev, stream, flush, pk, seed_off, ws, only):
                                  "questions_per_s": round(whole_job_rate(1, ws, ms * 1e-3), 1),
                                  "ms": round(ms, 4),
                                  "roofline": {"bound": "alu", "achieved": round(flops / (ms * 1e-3) / 1e12, 3),
-                                              "unit": "TFLOP/s fp32 (cosines)"}}
+                                              "peak": FP32_ALU_TFLOPS,
+                                              "frac": round(flops / (ms * 1e-3) / 1e12 / FP32_ALU_TFLOPS, 4),
+                                              "unit": "TFLOP/s fp32 (cosines)", "traffic": ncu_traffic("notebank_route"),
+                                              "peak_source": "152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz"}}
         del rho, u
         torch.cuda.empty_cache()
     return out, launches

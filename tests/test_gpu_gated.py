@@ -123,21 +123,19 @@ def test_gated_decode_steps_and_prefill_continuation(dtype):
     assert rel_err(to_np(st), ref["S"]) < tol
 
 
-def test_gated_full_size_sampled():
-    """The benchmark's scalar-gate launch: B=4, H=16, N=16384 bf16 / fp32 state; 8 sampled heads checked
-    on every token and on the final state."""
+def test_gated_full_size():
+    """The benchmark's scalar-gate launch: B=4, H=16, N=16384 bf16 / fp32
+    state, run through the scan's scalar-gate order; every head checked
+    against the oracle on every token and every state entry."""
     dev = cuda_device()
     w = synthetic.WORKLOADS["gdn_prefill"]
     inp = synthetic.workload_inputs("gdn_prefill", device=dev)
     o, S = la.la_gated_prefill(*(inp[n] for n in NAMES))
     torch.cuda.synchronize()
-    rng = np.random.default_rng(11)
-    heads = sorted(rng.choice(w.B * w.H, 8, replace=False).tolist())
-    bi = torch.tensor([h // w.H for h in heads], device=dev)
-    hi = torch.tensor([h % w.H for h in heads], device=dev)
-    sub = {n: inp[n][bi, hi].unsqueeze(0).cpu() for n in NAMES}
-    ref = oracle_ref(sub)
-    tol = TOL[torch.bfloat16]
-    assert rel_err(to_np(o[bi, hi]), ref["o"][0]) < tol
-    assert rel_err(to_np(S[bi, hi]), ref["S"][0]) < tol
     assert la.la_device_status() == la.LA_OK
+    tol = TOL[torch.bfloat16]
+    for b in range(w.B):  # one batch row (16 heads) of oracle work at a time
+        sub = {n: inp[n][b:b + 1].cpu() for n in NAMES}
+        ref = oracle_ref(sub)
+        assert rel_err(to_np(o[b:b + 1]), ref["o"]) < tol, b
+        assert rel_err(to_np(S[b:b + 1]), ref["S"]) < tol, b
