@@ -498,20 +498,20 @@ cudaError_t launch_typed(const GdnPrefillLaunch& a, void* ws, unsigned* status, 
   const GdnSegPlan plan = gdn_segment_plan(a.B, a.H, a.N);
   const int64_t BH = a.B * a.H;
   if (plan.G == 1) {
-    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr};
+    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr, 0, nullptr};
     gdn_chunked_kernel<TOut><<<(unsigned)BH, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, task, status);
     return cudaGetLastError();
   }
   float* maps = static_cast<float*>(ws);
   float* states = maps + BH * (plan.G - 1) * 2 * kStateElems;
-  const GdnTask t1{kSegmentMaps, plan.G, plan.seg_len, maps, nullptr};
+  const GdnTask t1{kSegmentMaps, plan.G, plan.seg_len, maps, nullptr, 0, nullptr};
   gdn_chunked_kernel<TOut><<<(unsigned)(BH * (plan.G - 1) * 2), kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, t1,
                                                                                                status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   e = launch_gdn_segment_combine(a.S_in, maps, states, plan.G, BH, stream);
   if (e != cudaSuccess) return e;
-  const GdnTask t2{kSegmentOutputs, plan.G, plan.seg_len, nullptr, states};
+  const GdnTask t2{kSegmentOutputs, plan.G, plan.seg_len, nullptr, states, 0, nullptr};
   gdn_chunked_kernel<TOut><<<(unsigned)(BH * plan.G), kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a, t2, status);
   return cudaGetLastError();
 }

@@ -39,6 +39,10 @@ struct GdnTask {
   int64_t seg_len;      // tokens per segment (a multiple of the chunk)
   float* maps;          // kSegmentMaps: [BH][G-1][2][128][128]  (B_g, then M_g)
   const float* states;  // kSegmentOutputs: [BH][G][128][128] entry states
+  // kWhole with the chunk records formed in the same launch: CTAs n_scan.. run the inversion and
+  // set ready[record] = 1 once a record is written (null: the records are complete at launch)
+  int n_scan;
+  unsigned* ready;
 };
 
 // The (b,h), segment, token range and entry/exit states of one CTA of `task`.
@@ -101,7 +105,8 @@ __device__ __forceinline__ void st_bf16(uint8_t* p, float x) {
 // 0..63 hold token tid of the chunk): inclusive scan of log alpha, then
 // g, beta, gamma = e^g and 1/gamma into gate[0..63], [64..127], [128..191],
 // [192..255].  Contains a block-wide barrier; `carry` is one shared float.
-__device__ __forceinline__ void gate_tables(int tid, float lg, float bt, float* gate, float* carry) {
+template <typename Sync>
+__device__ __forceinline__ void gate_tables(int tid, float lg, float bt, float* gate, float* carry, Sync sync) {
   const int lane = tid & 31, warp = tid >> 5;
   float gx = lg;
   if (tid < kC) {
@@ -112,7 +117,7 @@ __device__ __forceinline__ void gate_tables(int tid, float lg, float bt, float* 
     }
     if (tid == 31) *carry = gx;
   }
-  __syncthreads();
+  sync();
   if (tid < kC) {
     if (warp == 1) gx += *carry;
     gate[tid] = gx;
@@ -120,6 +125,9 @@ __device__ __forceinline__ void gate_tables(int tid, float lg, float bt, float* 
     gate[2 * kC + tid] = __expf(gx);
     gate[3 * kC + tid] = __expf(-gx);
   }
+}
+__device__ __forceinline__ void gate_tables(int tid, float lg, float bt, float* gate, float* carry) {
+  gate_tables(tid, lg, bt, gate, carry, [] { __syncthreads(); });
 }
 
 // [K;Q] K^T of one chunk into 64 TMEM columns (lanes 0..63: K K^T, lanes

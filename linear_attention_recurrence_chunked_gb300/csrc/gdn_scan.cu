@@ -72,10 +72,11 @@ static_assert(4 * (kISmemAlloc + 1024) <= 233472, "four inversion CTAs per SM");
 // forward substitution (threads 0..63, one column each); then 32x32 and 64x64 blocks from
 // [[A, 0], [C, B]]^{-1} = [[A^{-1}, 0], [-B^{-1} C A^{-1}, B^{-1}]].  Lsm: fp32 [64][65]
 // strictly lower L; Tsm: fp32 [64][kTPad]; Zsm: 1024 fp32 of block products; bt: beta[64].
-// Every thread of the block calls it; it contains block-wide barriers, and L is no longer read
-// once the last one has passed (the T2 image may overlay it).
+// Every thread of the 256 calls it; it contains their barriers (`sync`), and L is no longer read
+// once the last one has passed (the T2 image may overlay it).  t2_tile may be shared or global.
+template <typename Sync>
 __device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, float* Zsm, const float* bt,
-                                         uint8_t* t2_tile) {
+                                         uint8_t* t2_tile, Sync sync) {
   if (tid < kC) {
     const int base = (tid >> 4) * 16, col = tid & 15;
     float x[16];
@@ -97,7 +98,7 @@ __device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, 
     const int r0 = blk * 32, c0 = blk * 32 + 16;
     *reinterpret_cast<float4*>(Tsm + (r0 + r) * kTPad + c0 + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  __syncthreads();
+  sync();
   {
     // 32x32 blocks k = 0, 1: rows R = 32k + 16.., columns Cb = 32k..; thread: 2 columns of one row
     const int k = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
@@ -111,7 +112,7 @@ __device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, 
       z1 = fmaf(l, t.y, z1);
     }
     *reinterpret_cast<float2*>(Zsm + k * 256 + r * 16 + c0) = make_float2(z0, z1);
-    __syncthreads();
+    sync();
     float t0v = 0.f, t1v = 0.f;
     const float* tr = Tsm + (R + r) * kTPad;
 #pragma unroll
@@ -123,7 +124,7 @@ __device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, 
     }
     *reinterpret_cast<float2*>(Tsm + (R + r) * kTPad + Cb + c0) = make_float2(-t0v, -t1v);
   }
-  __syncthreads();
+  sync();
   {
     // 64x64: rows 32.., columns 0..31; thread: 4 columns of one row
     const int r = tid >> 3, c0 = (tid & 7) * 4;
@@ -135,7 +136,7 @@ __device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, 
       z.x = fmaf(l, tv.x, z.x); z.y = fmaf(l, tv.y, z.y); z.z = fmaf(l, tv.z, z.z); z.w = fmaf(l, tv.w, z.w);
     }
     *reinterpret_cast<float4*>(Zsm + r * 32 + c0) = z;
-    __syncthreads();
+    sync();
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
     const float* tr = Tsm + (32 + r) * kTPad;
 #pragma unroll 8
@@ -146,7 +147,7 @@ __device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, 
     }
     *reinterpret_cast<float4*>(Tsm + (32 + r) * kTPad + c0) = make_float4(-o.x, -o.y, -o.z, -o.w);
   }
-  __syncthreads();
+  sync();
   {
     // T2 = T diag(beta): thread r = tid / 4, 16 columns from c0
     const int r = tid >> 2, c0 = (tid & 3) * 16;
@@ -249,7 +250,7 @@ gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     phase_L_Po(tlane + 32 * half, row, half, gate, Lsm, sm + kIOffP, 1.f, a.delta, false);
     tc_fence_before();
     __syncthreads();
-    if (a.delta != 0.f) invert_T(tid, Lsm, Tsm, Zsm, gate + kC, sm + kIOffT2);
+    if (a.delta != 0.f) invert_T(tid, Lsm, Tsm, Zsm, gate + kC, sm + kIOffT2, [] { __syncthreads(); });
     else t2_identity(tid, gate + kC, sm + kIOffT2);  // the scalar gate: no inverse to form
     fence_proxy_async_smem();
     __syncthreads();
@@ -268,6 +269,142 @@ gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, 64);
+}
+
+// ============================================================================ inversion role
+// The CTAs of a scan launch past its scan CTAs (GdnTask::ready set) form the records themselves, so
+// that the inversion runs on the SMs the scan leaves idle, beside it.  Each such CTA runs two
+// independent pipelines of 8 warps (warps 0-7 and 8-15; warps 16-17 only allocate and free) over
+// the records in chunk-major order (record i: chunk i / BH of pair i % BH), so that every (b,h)
+// gets its early chunks first, as its scan CTA wants them.  Per record the steps of
+// gdn_tinv_kernel, with the [K;Q] tile in two stages (the copy of the record after next goes in
+// once T, formed over the current stage, is dead) and the two images stored straight from
+// registers to the record.  A record's flag is released one record later, at a point where the
+// pipeline waits anyway, and the last one after the loop; the scan's copy issuer acquires it
+// before it copies the record.
+constexpr uint32_t kIGrp = 88064;                     // one pipeline: [K;Q] x 2, L, Z, gate tables
+constexpr uint32_t kIGOffL = 65536;                   // the two [K;Q] stages below (T over one)
+constexpr uint32_t kIGOffZ = kIGOffL + 64 * 65 * 4;
+constexpr uint32_t kIGOffGate = kIGOffZ + 4096;
+static_assert(kIGOffGate + 1024 <= kIGrp && kIGrp % 1024 == 0, "one inversion pipeline's shared memory");
+
+__device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
+                                               const GdnPrefillLaunch& a, int nch, int n_ctas, int cta,
+                                               uint8_t* sm, uint8_t* rec_out, unsigned* ready, unsigned* status) {
+  __shared__ uint64_t ibar[2][3];  // per pipeline: [K;Q] landed in stage 0, in stage 1; MMA done
+  __shared__ uint32_t itmem_sh;
+  __shared__ float icarry[2];
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int g = warp >> 3;  // pipeline; 2 for the two spare warps
+  const int lt = tid & 255, row = lt & 127, half = lt >> 7;
+  const int64_t BH = a.B * a.H, nrec = BH * nch;
+  const int64_t stride = 2 * (int64_t)n_ctas;
+  const int64_t first = 2 * (int64_t)cta + g;
+  uint8_t* gsm = sm + (uint32_t)(g & 1) * kIGrp;
+  const uint32_t gbase = smem_u32(gsm);
+  float* Lsm = reinterpret_cast<float*>(gsm + kIGOffL);
+  float* Zsm = reinterpret_cast<float*>(gsm + kIGOffZ);
+  float* gate = reinterpret_cast<float*>(gsm + kIGOffGate);
+
+  if (tid == 0) {
+    for (int p = 0; p < 2; ++p)
+      for (int j = 0; j < 3; ++j) mbar_init(smem_u32(&ibar[p][j]), 1);
+    fence_mbar_init();
+    tma_prefetch_desc(tmap_k);
+    tma_prefetch_desc(tmap_q);
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&itmem_sh), 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = itmem_sh + 64u * (uint32_t)(g & 1);
+  const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+
+  if (g < 2) {
+    auto sync = [g] { named_bar_sync(1 + g, 256); };
+    const uint32_t bar_mma = smem_u32(&ibar[g][2]);
+    int issued[2] = {0, 0};  // the leader's loads per stage
+    // the [K;Q] tile of record i into stage st (leader only)
+    auto load = [&](int64_t i, int st) {
+      const int64_t bh = i % BH;
+      const int t0 = (int)((i / BH) * kC), b = (int)(bh / a.H), h = (int)(bh % a.H);
+      const uint32_t bar = smem_u32(&ibar[g][st]), dst = gbase + (uint32_t)st * 32768u;
+      mbar_arrive_expect_tx(bar, 32768);
+      tma_load_4d(dst + 0, tmap_k, 0, t0, h, b, bar);
+      tma_load_4d(dst + 16384, tmap_k, 64, t0, h, b, bar);
+      tma_load_4d(dst + 8192, tmap_q, 0, t0, h, b, bar);
+      tma_load_4d(dst + 24576, tmap_q, 64, t0, h, b, bar);
+      ++issued[st];
+    };
+    // log alpha and beta of token lt of record i (threads 0..63; padded tokens: alpha = 1, beta = 0)
+    auto gates_of = [&](int64_t i, float& lg, float& bt) {
+      lg = 0.f;
+      bt = 0.f;
+      if (lt < kC && i < nrec) {
+        const int64_t bh = i % BH, t = (i / BH) * kC + lt;
+        const int b = (int)(bh / a.H), h = (int)(bh % a.H);
+        if (t < a.N) {
+          lg = logf(a.alpha[b * a.a_sb + h * a.a_sh + t]);
+          bt = a.beta[b * a.b_sb + h * a.b_sh + t];
+        }
+      }
+    };
+    if (lt == 0) {
+      if (first < nrec) load(first, 0);
+      if (first + stride < nrec) load(first + stride, 1);
+    }
+    float lg_n, bt_n;
+    gates_of(first, lg_n, bt_n);
+    bool ok = true, mma_pending = false;
+    int64_t prev = -1;
+    int k = 0;
+    for (int64_t i = first; i < nrec; i += stride, ++k) {
+      const int st = k & 1;
+      const float lg = lg_n, bt = bt_n;
+      gates_of(i + stride, lg_n, bt_n);  // the next record's gates load during this one
+      gate_tables(lt, lg, bt, gate, &icarry[g], sync);
+      ok = mbar_wait(smem_u32(&ibar[g][st]), (uint32_t)((k >> 1) & 1), status);
+      if (lt == 0 && prev >= 0) flag_release(ready + prev, 1u);
+      if (named_bar_or(1 + g, 256, !ok)) break;
+      if (lt == 0) {
+        tc_fence_after();
+        mma_kq(tmem, gbase + (uint32_t)st * 32768u);
+        mma_commit(bar_mma);
+      }
+      mma_pending = true;
+      ok = mbar_wait(bar_mma, (uint32_t)(k & 1), status);
+      if (named_bar_or(1 + g, 256, !ok)) break;
+      mma_pending = false;
+      tc_fence_after();
+      const int64_t bh = i % BH, r = bh * nch + i / BH;
+      uint8_t* rp = rec_out + r * kRec;
+      phase_L_Po(tlane + 32 * half, row, half, gate, Lsm, rp + kRecP, 1.f, a.delta, false);
+      tc_fence_before();
+      sync();
+      float* Tsm = reinterpret_cast<float*>(gsm + (uint32_t)st * 32768u);  // over the dead [K;Q] tile
+      if (a.delta != 0.f) invert_T(lt, Lsm, Tsm, Zsm, gate + kC, rp + kRecT2, sync);
+      else t2_identity(lt, gate + kC, rp + kRecT2);
+      fence_proxy_async_smem();  // T's writes before the copy that overwrites the stage
+      sync();
+      if (lt == 0 && i + 2 * stride < nrec) load(i + 2 * stride, st);
+      prev = r;
+    }
+    if (lt == 0) {
+      if (ok && prev >= 0) flag_release(ready + prev, 1u);
+      if (!ok) {
+        // let this pipeline's own copies and MMA finish (bounded) before the CTA exits
+        for (int st = 0; st < 2; ++st)
+          if (issued[st] > 0) mbar_wait(smem_u32(&ibar[g][st]), (uint32_t)((issued[st] - 1) & 1), status);
+        if (mma_pending) mbar_wait(bar_mma, (uint32_t)(k & 1), status);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(itmem_sh, 128);
 }
 
 // ============================================================================ kernel 2
@@ -339,9 +476,14 @@ template <typename TOut, bool GATED>
 __global__ void __launch_bounds__(kScanThreads, 1)
 gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                 const __grid_constant__ CUtensorMap tmap_v, const GdnPrefillLaunch a, const GdnTask task,
-                int nch_total, const uint8_t* rec, unsigned* status) {
+                int nch_total, uint8_t* rec, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  if (task.ready != nullptr && (int)blockIdx.x >= task.n_scan) {
+    inversion_role(&tmap_q, &tmap_k, a, nch_total, (int)gridDim.x - task.n_scan, (int)blockIdx.x - task.n_scan,
+                   sm, rec, task.ready, status);
+    return;
+  }
   __shared__ uint64_t bar_k[kKSlots];  // K and the T2 image landed in their slot
   __shared__ uint64_t bar_v[2];        // V landed
   __shared__ uint64_t bar_q[2];        // Q and the P image landed
@@ -642,6 +784,11 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       for (int m = 0; ok && m < n; ++m) {
         const int t0 = (int)(wk.t_begin + (int64_t)m * kC);
         if (m >= kKSlots) ok = wait(&bar_kfree[m % kKSlots], kpar(m - kKSlots));
+        if (ok && task.ready != nullptr) {
+          // the record is formed in this launch: wait for its flag, then copy it
+          ok = flag_wait(task.ready + rec0 + m, 1u, status);
+          fence_proxy_async_global();
+        }
         if (!ok) break;
         {
           const uint32_t kt = sb + kslot(m);
@@ -943,6 +1090,22 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 }
 
 size_t records_bytes(int64_t BH, int64_t nch) { return (size_t)(BH * nch) * kRec; }
+// one ready flag per record, for the launch that forms its records itself
+size_t flags_bytes(int64_t BH, int64_t nch) { return ((size_t)(BH * nch) * sizeof(unsigned) + 255) & ~size_t(255); }
+
+// The fewest inversion CTAs worth a launch that forms its own records.
+constexpr int kMinInversionCtas = 16;
+
+// CTAs of the scan kernel that fit on the current device at once (0 if unknown).
+template <typename K>
+int coresident_ctas(K kernel) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kScanThreads, kSSmemAlloc) != cudaSuccess)
+    return 0;
+  return sms * per_sm;
+}
 
 template <typename TOut>
 cudaError_t launch_scan_typed(const GdnPrefillLaunch& a, void* ws, unsigned* status, cudaStream_t stream) {
@@ -952,6 +1115,7 @@ cudaError_t launch_scan_typed(const GdnPrefillLaunch& a, void* ws, unsigned* sta
     return cudaErrorInvalidValue;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
+  static int coresident[2] = {0, 0};  // per scan instantiation, on the first device used
   std::call_once(attr_once, [] {
     attr_err = cudaFuncSetAttribute(gdn_tinv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kISmemAlloc);
     if (attr_err == cudaSuccess)
@@ -960,33 +1124,48 @@ cudaError_t launch_scan_typed(const GdnPrefillLaunch& a, void* ws, unsigned* sta
     if (attr_err == cudaSuccess)
       attr_err = cudaFuncSetAttribute(gdn_scan_kernel<TOut, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)kSSmemAlloc);
+    if (attr_err == cudaSuccess) {
+      coresident[0] = coresident_ctas(gdn_scan_kernel<TOut, false>);
+      coresident[1] = coresident_ctas(gdn_scan_kernel<TOut, true>);
+    }
   });
-  auto scan = a.delta == 0.f ? gdn_scan_kernel<TOut, true> : gdn_scan_kernel<TOut, false>;
+  const bool gated = a.delta == 0.f;
+  auto scan = gated ? gdn_scan_kernel<TOut, true> : gdn_scan_kernel<TOut, false>;
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t BH = a.B * a.H;
   const int64_t nch = (a.N + kC - 1) / kC;
+  const GdnSegPlan plan = gdn_segment_plan(a.B, a.H, a.N);
   uint8_t* recT = static_cast<uint8_t*>(ws);
   float* seg = reinterpret_cast<float*>(recT + records_bytes(BH, nch));
+  unsigned* ready = reinterpret_cast<unsigned*>(recT + records_bytes(BH, nch) + plan.ws_bytes);
+  const int n_co = coresident[gated ? 1 : 0];
+  if (plan.G == 1 && BH + kMinInversionCtas <= n_co) {
+    // one launch: CTAs 0..BH-1 scan, the rest of the GPU forms the records beside them
+    cudaError_t e = cudaMemsetAsync(ready, 0, (size_t)(BH * nch) * sizeof(unsigned), stream);
+    if (e != cudaSuccess) return e;
+    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr, (int)BH, ready};
+    return launch_cooperative(scan, dim3((unsigned)n_co), dim3(kScanThreads), kSSmemAlloc, stream, mq, mk, mv, a,
+                              task, (int)nch, recT, status);
+  }
   gdn_tinv_kernel<<<(unsigned)(BH * nch), kThreads, kISmemAlloc, stream>>>(mq, mk, a, (int)nch, recT, status);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const GdnSegPlan plan = gdn_segment_plan(a.B, a.H, a.N);
   if (plan.G == 1) {
-    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr};
+    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr, 0, nullptr};
     return launch_dependent(scan, dim3((unsigned)BH), dim3(kScanThreads), kSSmemAlloc, stream, mq,
-                            mk, mv, a, task, (int)nch, (const uint8_t*)recT, status);
+                            mk, mv, a, task, (int)nch, recT, status);
   }
   float* maps = seg;
   float* states = maps + BH * (plan.G - 1) * 2 * kStateElems;
-  const GdnTask t1{kSegmentMaps, plan.G, plan.seg_len, maps, nullptr};
+  const GdnTask t1{kSegmentMaps, plan.G, plan.seg_len, maps, nullptr, 0, nullptr};
   e = launch_dependent(scan, dim3((unsigned)(BH * (plan.G - 1) * 2)), dim3(kScanThreads), kSSmemAlloc,
-                       stream, mq, mk, mv, a, t1, (int)nch, (const uint8_t*)recT, status);
+                       stream, mq, mk, mv, a, t1, (int)nch, recT, status);
   if (e != cudaSuccess) return e;
   e = launch_gdn_segment_combine(a.S_in, maps, states, plan.G, BH, stream);
   if (e != cudaSuccess) return e;
-  const GdnTask t2{kSegmentOutputs, plan.G, plan.seg_len, nullptr, states};
+  const GdnTask t2{kSegmentOutputs, plan.G, plan.seg_len, nullptr, states, 0, nullptr};
   return launch_dependent(scan, dim3((unsigned)(BH * plan.G)), dim3(kScanThreads), kSSmemAlloc, stream,
-                          mq, mk, mv, a, t2, (int)nch, (const uint8_t*)recT, status);
+                          mq, mk, mv, a, t2, (int)nch, recT, status);
 }
 
 }  // namespace
@@ -995,7 +1174,7 @@ size_t gdn_scan_workspace_bytes(int64_t B, int64_t H, int64_t N) {
   const int64_t BH = B * H;
   if (BH <= 0 || N <= 0) return 0;
   const int64_t nch = (N + kC - 1) / kC;
-  return records_bytes(BH, nch) + gdn_segment_plan(B, H, N).ws_bytes;
+  return records_bytes(BH, nch) + gdn_segment_plan(B, H, N).ws_bytes + flags_bytes(BH, nch);
 }
 
 cudaError_t launch_gdn_prefill_scan(const GdnPrefillLaunch& a, void* ws, size_t ws_bytes, unsigned* status,

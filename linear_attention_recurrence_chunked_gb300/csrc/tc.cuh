@@ -155,6 +155,36 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Orders this thread's generic-proxy view of global memory with its async-proxy (bulk copy)
+// accesses: after acquiring a flag, before copying what the flag guards with cp.async.bulk.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- flags between CTAs of one grid
+// Release: every global write this thread has observed (its own, and those of the threads of its
+// CTA ordered before it by a barrier) is visible GPU-wide before the flag reads `v`.
+__device__ __forceinline__ void flag_release(unsigned* flag, unsigned v) {
+  asm volatile("fence.acq_rel.gpu;\n\tst.relaxed.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+// Waits until *flag == v (acquire: what the releasing thread had observed is then visible to this
+// thread); gives up after kWaitLimitNs, ORs kStatusTimeout into *status and returns false.  Only
+// for flags set by CTAs of the same grid that are co-resident (a cooperative launch) and never
+// wait on the waiting CTA.
+__device__ __forceinline__ bool flag_wait(const unsigned* flag, unsigned v, unsigned* status) {
+  uint64_t t0 = 0;
+  for (int i = 0;; ++i) {
+    unsigned x;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(flag) : "memory");
+    if (x == v) return true;
+    if (i == 0) t0 = globaltimer_ns();
+    else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+    __nanosleep(128);
+  }
+}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

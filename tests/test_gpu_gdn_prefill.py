@@ -93,6 +93,32 @@ def test_gdn_prefill_then_decode_matches_longer_prefill():
     assert rel_err(to_np(S), ref["S"]) < TOL[torch.bfloat16]
 
 
+@pytest.mark.parametrize("fn", ["la_gdn_prefill", "la_gated_prefill"])
+def test_records_formed_beside_the_scan_match_the_inversion_kernel(fn):
+    """With few enough (b,h) pairs (unsegmented sequences), the chunk records
+    are formed in the scan's own launch, on the SMs its scan CTAs leave free,
+    and handed over through per-record flags; with more pairs a separate
+    inversion kernel forms them first.  Both use the same arithmetic, so the
+    first 64 pairs of a 144-pair call give exactly the bits of a 64-pair call
+    on the same inputs; two heads of the large call are checked against the
+    oracle."""
+    dev = cuda_device()
+    inp = synthetic.gdn_inputs(1, 144, 700, dtype=torch.bfloat16, seed=47)
+    f = getattr(la, fn)
+    x = {n: inp[n].to(dev) for n in NAMES}
+    o_all, S_all = f(*(x[n] for n in NAMES))
+    o_64, S_64 = f(*(x[n][:, :64].contiguous() for n in NAMES))
+    torch.cuda.synchronize()
+    assert la.la_device_status() == la.LA_OK
+    assert torch.equal(o_all[:, :64], o_64) and torch.equal(S_all[:, :64], S_64)
+    heads = [5, 130]
+    sub = {n: inp[n][:, heads] for n in NAMES}
+    ref = (oracle.gdn if fn == "la_gdn_prefill" else oracle.gated)(
+        *(synthetic.to_oracle(sub[n]) for n in ("q", "k", "v")), sub["alpha"].numpy(), sub["beta"].numpy())
+    assert rel_err(to_np(o_all[:, heads]), ref["o"]) < TOL[torch.bfloat16]
+    assert rel_err(to_np(S_all[:, heads]), ref["S"]) < TOL[torch.bfloat16]
+
+
 def test_gdn_empty_sequence_passes_state():
     dev = cuda_device()
     z = torch.zeros((1, 2, 0, 128), dtype=torch.bfloat16, device=dev)
