@@ -87,7 +87,7 @@ gdn_chunked_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5;
   const int row = tid & 127;   // tensor-memory lane owned with the partner thread
   const int half = tid >> 7;   // which half of the lane's columns
-  const CtaWork wk = cta_work(a, task);
+  const CtaWork wk = cta_work(a, task, (int)blockIdx.x);
   const int b = wk.b, h = wk.h;
   const int64_t t_begin = wk.t_begin, t_end = wk.t_end;
   const int64_t N = t_end;

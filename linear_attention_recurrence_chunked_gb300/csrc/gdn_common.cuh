@@ -39,10 +39,13 @@ struct GdnTask {
   int64_t seg_len;      // tokens per segment (a multiple of the chunk)
   float* maps;          // kSegmentMaps: [BH][G-1][2][128][128]  (B_g, then M_g)
   const float* states;  // kSegmentOutputs: [BH][G][128][128] entry states
-  // kWhole with the chunk records formed in the same launch: CTAs n_scan.. run the inversion and
-  // set ready[record] = 1 once a record is written (null: the records are complete at launch)
+  // kWhole with the chunk records formed in the same launch: CTAs n_scan.. (by placement rank) run
+  // the inversion and set ready[record] = 1 once a record is written (null: the records are complete
+  // at launch); place: the launch's zeroed placement scratch (an arrival counter, then one word per
+  // SM id)
   int n_scan;
   unsigned* ready;
+  unsigned* place;
 };
 
 // The (b,h), segment, token range and entry/exit states of one CTA of `task`.
@@ -57,19 +60,20 @@ struct CtaWork {
   float* s_exit;
 };
 
-__device__ __forceinline__ CtaWork cta_work(const GdnPrefillLaunch& a, const GdnTask& task) {
+// `cta`: this CTA's index in the task (its blockIdx.x unless the launch places its CTAs itself).
+__device__ __forceinline__ CtaWork cta_work(const GdnPrefillLaunch& a, const GdnTask& task, int cta) {
   CtaWork w{};
   int which = 0;
   if (task.mode == kWhole) {
-    w.bh = blockIdx.x;
+    w.bh = cta;
   } else if (task.mode == kSegmentMaps) {
     const int per = 2 * (task.G - 1);
-    w.bh = blockIdx.x / per;
-    w.seg = (int)(blockIdx.x % per) >> 1;
-    which = (int)(blockIdx.x % per) & 1;  // 0: B_g (zero entry state), 1: M_g (identity entry, V taken as 0)
+    w.bh = cta / per;
+    w.seg = (int)(cta % per) >> 1;
+    which = (int)(cta % per) & 1;  // 0: B_g (zero entry state), 1: M_g (identity entry, V taken as 0)
   } else {
-    w.bh = blockIdx.x / task.G;
-    w.seg = (int)(blockIdx.x % task.G);
+    w.bh = cta / task.G;
+    w.seg = (int)(cta % task.G);
   }
   w.b = (int)(w.bh / a.H);
   w.h = (int)(w.bh % a.H);

@@ -51,112 +51,207 @@ using namespace gdn;
 constexpr uint32_t kRecT2 = 0, kRecP = 8192, kRec = 16384;
 
 // ============================================================================ kernel 1
-// Shared memory: the [K;Q] tile (K rows 0-63, Q rows 64-127) for one M=128 MMA giving K K^T and
-// Q K^T; L, block products and gate tables.  Once the MMA is done the tile is dead: T (fp32, rows
-// padded to 68 floats so that a column read across rows spreads over the banks) takes its first
-// 17 KB and the P image its last 8 KB; the T2 image goes over L.
-constexpr uint32_t kIOffKQ = 0;
-constexpr uint32_t kIOffL = 32768;
-constexpr uint32_t kIOffZ = kIOffL + 64 * 65 * 4;
-constexpr uint32_t kIOffGate = kIOffZ + 4096;
-constexpr uint32_t kISmemUsed = kIOffGate + 1024;
-constexpr uint32_t kISmemAlloc = kISmemUsed + 1024;
-constexpr int kTPad = 68;                             // fp32 T row stride
-constexpr uint32_t kIOffT = kIOffKQ;                  // [64][68] fp32 (17408 B)
-constexpr uint32_t kIOffP = kIOffKQ + 24576;          // P image (8 KB)
-constexpr uint32_t kIOffT2 = kIOffL;                  // T2 image (8 KB) over L
-static_assert(64 * kTPad * 4 <= 24576, "T fits below the P image");
-static_assert(4 * (kISmemAlloc + 1024) <= 233472, "four inversion CTAs per SM");
+// T = (I + L)^{-1} of a 64-token chunk by doubling, [[A, 0], [C, B]]^{-1} = [[A^{-1}, 0],
+// [-B^{-1} C A^{-1}, B^{-1}]]: the four 16x16 diagonal blocks by forward substitution on the CUDA
+// cores, the 32- and 64-level off-diagonal blocks as tcgen05 MMAs (kind::tf32: fp32 operands at tf32
+// precision, fp32 accumulation).  Every operand is an fp32 K-major tile with the 128-byte swizzle
+// (panels of [64 rows][32 columns], 8 KB):
+//   LT  L, strictly lower (16 KB);      TA  T, row-major (16 KB);      TB  T^T (16 KB);
+//   SMt the small B operands: X_10^T and X_32^T ([16][32] each, 2 KB), later Z^T ([32][32], 4 KB).
+// The MMAs run at M = 128 with the chunk's 64 rows in lanes 0..63 (the accumulator layout of every
+// other MMA here); A rows 64..127 run over the 8 KB that follow each A tile, which must be shared
+// memory of this CTA, and give accumulator rows that are never read.
+//   X_10 = L_10 T_00, X_32 = L_32 T_22          (rows 16-31, 48-63)       N = 16, K = 16
+//   T_10 = -T_11 X_10, T_32 = -T_33 X_32          (the 32-level blocks)     N = 16, K = 16
+//   Z    = L_[32:64][0:32] T_[0:32][0:32]        (rows 32-63)             N = 32, K = 32
+//   T_[32:64][0:32] = -T_[32:64][32:64] Z                                  N = 32, K = 32
+constexpr uint32_t kPanel = 8192;  // one [64][32] fp32 panel
 
-// T = (I + L)^{-1} by doubling, then the bf16 image T diag(beta).  16x16 diagonal blocks by
-// forward substitution (threads 0..63, one column each); then 32x32 and 64x64 blocks from
-// [[A, 0], [C, B]]^{-1} = [[A^{-1}, 0], [-B^{-1} C A^{-1}, B^{-1}]].  Lsm: fp32 [64][65]
-// strictly lower L; Tsm: fp32 [64][kTPad]; Zsm: 1024 fp32 of block products; bt: beta[64].
-// Every thread of the 256 calls it; it contains their barriers (`sync`), and L is no longer read
-// once the last one has passed (the T2 image may overlay it).  t2_tile may be shared or global.
+__device__ __forceinline__ float* f32_at(uint8_t* tile, int row, int col) {
+  return reinterpret_cast<float*>(tile + sw128_off_f32((uint32_t)row, (uint32_t)col, 64));
+}
+
+// L = strict_lower(diag(beta gamma) [K K^T] diag(1/gamma)) times delta into LT, and the bf16 image of
+// P_rj = (q_r . k_j) / gamma_j (j <= r) into po_tile, from [K;Q] K^T in TMEM (lanes 0..63: K K^T,
+// 64..127: Q K^T).  kq_taddr: this thread's lane at the first of its 32 columns (half = column half).
+__device__ __forceinline__ void phase_LT_Po(uint32_t kq_taddr, int row, int half, const float* gate, uint8_t* LT,
+                                            uint8_t* po_tile, float delta) {
+  float v[32];
+  ld32(kq_taddr, v);
+  const int j0 = 32 * half;
+  const float* bt = gate + kC;
+  const float* gm = gate + 2 * kC;
+  const float* gi = gate + 3 * kC;
+  if (row < kC) {
+    const int r = row;
+    const float f = bt[r] * gm[r] * delta;
+    uint8_t* rowp = LT + (uint32_t)half * kPanel + (uint32_t)r * 128u;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float4 g4 = *reinterpret_cast<const float4*>(gi + j0 + 4 * c);
+      const int j = j0 + 4 * c;
+      float4 o;
+      o.x = j < r ? f * g4.x * v[4 * c] : 0.f;
+      o.y = j + 1 < r ? f * g4.y * v[4 * c + 1] : 0.f;
+      o.z = j + 2 < r ? f * g4.z * v[4 * c + 2] : 0.f;
+      o.w = j + 3 < r ? f * g4.w * v[4 * c + 3] : 0.f;
+      *reinterpret_cast<float4*>(rowp + ((c ^ (r & 7)) << 4)) = o;
+    }
+  } else {
+    const int r = row - kC;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = (j0 + j <= r) ? gi[j0 + j] * v[j] : 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<uint4*>(po_tile + sw128_off(r, j0 + 8 * q, 64)) = pack8_bf16(v + 8 * q);
+  }
+}
+
+// T from L (both as above), then the bf16 image T2 = T diag(beta) into t2_tile (shared or global).
+// lt: thread 0..255 of the 256 that call it (warp lt / 32 must sit at a multiple of four warps in
+// the CTA, so that it reads TMEM lanes 32 (lt / 32 % 4)..); tm: 64 TMEM columns of this group, free;
+// bar: an mbarrier that takes one arrival per commit, *mph its next phase parity (the same in every
+// thread).  Thread lt == 0 issues the MMAs.  `sync` is a barrier of the 256.  An expired wait is
+// recorded in *status and makes it return false; the steps still run, so that every barrier is met.
 template <typename Sync>
-__device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, float* Zsm, const float* bt,
-                                         uint8_t* t2_tile, Sync sync) {
-  if (tid < kC) {
-    const int base = (tid >> 4) * 16, col = tid & 15;
+__device__ __forceinline__ bool invert_T_tc(int lt, uint8_t* LT, uint8_t* TA, uint8_t* TB, uint8_t* SMt, uint32_t tm,
+                                            uint32_t bar, uint32_t& mph, const float* bt, uint8_t* t2_tile,
+                                            unsigned* status, Sync sync) {
+  const int w = lt >> 5, lane = lt & 31;
+  bool ok = true;
+  auto mma_done = [&] {
+    ok = mbar_wait(bar, mph, status) && ok;
+    mph ^= 1u;
+    tc_fence_after();
+  };
+  // diagonal blocks: thread (block lt / 16, column lt % 16) by forward substitution; TA gets the
+  // column, TB the same values as a row
+  if (lt < kC) {
+    const int base = (lt >> 4) * 16, col = lt & 15;
     float x[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) x[r] = (r == col) ? 1.f : 0.f;
 #pragma unroll
     for (int j = 0; j < 15; ++j) {
-      const float* Lc = Lsm + (base + j + 1) * kLStride + base + j;
 #pragma unroll
-      for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-Lc[(r - j - 1) * kLStride], x[j], x[r]);
+      for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-*f32_at(LT, base + r, base + j), x[j], x[r]);
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) Tsm[(base + r) * kTPad + base + col] = x[r];
-  } else if (tid < kC + 128) {
-    // zero the two 16x16 blocks above the diagonal that the 64x64 step reads as part of its 32x32
-    // diagonal blocks (rows 0-15 x columns 16-31, rows 32-47 x columns 48-63), a float4 per thread;
-    // the T2 pass masks everything else above the diagonal
-    const int e = tid - kC, blk = e >> 6, r = (e >> 2) & 15, c4 = (e & 3) * 4;
-    const int r0 = blk * 32, c0 = blk * 32 + 16;
-    *reinterpret_cast<float4*>(Tsm + (r0 + r) * kTPad + c0 + c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0; r < 16; ++r) *f32_at(TA, base + r, base + col) = x[r];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<float4*>(f32_at(TB, base + col, base + 4 * q)) =
+          make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+  } else if (lt < 2 * kC) {
+    // the two upper blocks an MMA reads: TB rows 16-31 x columns 0-15 (T_01^T... zero) and TA rows
+    // 32-47 x columns 48-63 (T_23, zero)
+    const int e = lt - kC, r = e >> 2, c = 4 * (e & 3);
+    *reinterpret_cast<float4*>(f32_at(TB, 16 + r, c)) = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(f32_at(TA, 32 + r, 48 + c)) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  fence_proxy_async_smem();
+  sync();
+  const uint32_t la = smem_u32(LT), ta = smem_u32(TA), tb = smem_u32(TB), sa = smem_u32(SMt);
+  const uint32_t id16 = idesc_tf32(128, 16), id32 = idesc_tf32(128, 32);
+  if (lt == 0) {
+    tc_fence_after();
+#pragma unroll
+    for (int s = 0; s < 2; ++s) mma_tf32(tm + 0, kmaj(la + 32 * s), kmaj(tb + 32 * s), id16, s > 0);
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+      mma_tf32(tm + 16, kmaj(la + kPanel + 32 * s), kmaj(tb + kPanel + 32 * 128 + 32 * s), id16, s > 0);
+    mma_commit(bar);
+  }
+  mma_done();
+  // X_10 (warp 0, lanes 16-31 = rows 16-31) and X_32 (warp 1, rows 48-63), transposed into SMt
+  if (w < 2) {
+    float v[16];
+    tmem_ld16(tm + ((uint32_t)(32 * w) << 16) + 16u * (uint32_t)w, v);
+    tmem_ld_wait();
+    if (lane >= 16) {
+      uint8_t* xt = SMt + 2048 * w;
+#pragma unroll
+      for (int n = 0; n < 16; ++n) *reinterpret_cast<float*>(xt + sw128_off_f32(n, lane - 16, 16)) = v[n];
+    }
+  }
+  tc_fence_before();
+  fence_proxy_async_smem();
+  sync();
+  if (lt == 0) {
+    tc_fence_after();
+#pragma unroll
+    for (int s = 0; s < 2; ++s) mma_tf32(tm + 32, kmaj(ta + 64 + 32 * s), kmaj(sa + 32 * s), id16, s > 0);
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+      mma_tf32(tm + 48, kmaj(ta + kPanel + 64 + 32 * s), kmaj(sa + 2048 + 32 * s), id16, s > 0);
+    mma_commit(bar);
+  }
+  mma_done();
+  // T_10 = -T_11 X_10 (warp 0) and T_32 = -T_33 X_32 (warp 1): into TA, and transposed into TB
+  if (w < 2) {
+    float v[16];
+    tmem_ld16(tm + ((uint32_t)(32 * w) << 16) + 32u + 16u * (uint32_t)w, v);
+    tmem_ld_wait();
+    if (lane >= 16) {
+      const int R = 16 + 32 * w + (lane - 16), C0 = 32 * w;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4*>(f32_at(TA, R, C0 + 4 * q)) =
+            make_float4(-v[4 * q], -v[4 * q + 1], -v[4 * q + 2], -v[4 * q + 3]);
+#pragma unroll
+      for (int n = 0; n < 16; ++n) *f32_at(TB, C0 + n, R) = -v[n];
+    }
+  }
+  tc_fence_before();
+  fence_proxy_async_smem();
+  sync();
+  if (lt == 0) {
+    tc_fence_after();
+#pragma unroll
+    for (int s = 0; s < 4; ++s) mma_tf32(tm + 0, kmaj(la + 32 * s), kmaj(tb + 32 * s), id32, s > 0);
+    mma_commit(bar);
+  }
+  mma_done();
+  // Z (rows 32-63: warps 1 and 5, 16 columns each), transposed into SMt
+  if (w == 1 || w == 5) {
+    const int c0 = w == 1 ? 0 : 16;
+    float v[16];
+    tmem_ld16(tm + (32u << 16) + (uint32_t)c0, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int n = 0; n < 16; ++n) *reinterpret_cast<float*>(SMt + sw128_off_f32(c0 + n, lane, 32)) = v[n];
+  }
+  tc_fence_before();
+  fence_proxy_async_smem();
+  sync();
+  if (lt == 0) {
+    tc_fence_after();
+#pragma unroll
+    for (int s = 0; s < 4; ++s) mma_tf32(tm + 32, kmaj(ta + kPanel + 32 * s), kmaj(sa + 32 * s), id32, s > 0);
+    mma_commit(bar);
+  }
+  mma_done();
+  // T_[32:64][0:32] = -(T_[32:64][32:64] Z) into TA (warps 1 and 5, 16 columns each)
+  if (w == 1 || w == 5) {
+    const int c0 = w == 1 ? 0 : 16;
+    float v[16];
+    tmem_ld16(tm + (32u << 16) + 32u + (uint32_t)c0, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<float4*>(f32_at(TA, 32 + lane, c0 + 4 * q)) =
+          make_float4(-v[4 * q], -v[4 * q + 1], -v[4 * q + 2], -v[4 * q + 3]);
+  }
+  tc_fence_before();
   sync();
   {
-    // 32x32 blocks k = 0, 1: rows R = 32k + 16.., columns Cb = 32k..; thread: 2 columns of one row
-    const int k = tid >> 7, r = (tid >> 3) & 15, c0 = (tid & 7) * 2;
-    const int R = 32 * k + 16, Cb = 32 * k;
-    float z0 = 0.f, z1 = 0.f;
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-      const float l = Lsm[(R + r) * kLStride + Cb + m];
-      const float2 t = *reinterpret_cast<const float2*>(Tsm + (Cb + m) * kTPad + Cb + c0);
-      z0 = fmaf(l, t.x, z0);
-      z1 = fmaf(l, t.y, z1);
-    }
-    *reinterpret_cast<float2*>(Zsm + k * 256 + r * 16 + c0) = make_float2(z0, z1);
-    sync();
-    float t0v = 0.f, t1v = 0.f;
-    const float* tr = Tsm + (R + r) * kTPad;
-#pragma unroll
-    for (int p = 0; p < 16; ++p) {
-      const float tv = tr[R + p];
-      const float2 zz = *reinterpret_cast<const float2*>(Zsm + k * 256 + p * 16 + c0);
-      t0v = fmaf(tv, zz.x, t0v);
-      t1v = fmaf(tv, zz.y, t1v);
-    }
-    *reinterpret_cast<float2*>(Tsm + (R + r) * kTPad + Cb + c0) = make_float2(-t0v, -t1v);
-  }
-  sync();
-  {
-    // 64x64: rows 32.., columns 0..31; thread: 4 columns of one row
-    const int r = tid >> 3, c0 = (tid & 7) * 4;
-    float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int m = 0; m < 32; ++m) {
-      const float l = Lsm[(32 + r) * kLStride + m];
-      const float4 tv = *reinterpret_cast<const float4*>(Tsm + m * kTPad + c0);
-      z.x = fmaf(l, tv.x, z.x); z.y = fmaf(l, tv.y, z.y); z.z = fmaf(l, tv.z, z.z); z.w = fmaf(l, tv.w, z.w);
-    }
-    *reinterpret_cast<float4*>(Zsm + r * 32 + c0) = z;
-    sync();
-    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float* tr = Tsm + (32 + r) * kTPad;
-#pragma unroll 8
-    for (int p = 0; p < 32; ++p) {
-      const float tv = tr[32 + p];
-      const float4 zz = *reinterpret_cast<const float4*>(Zsm + p * 32 + c0);
-      o.x = fmaf(tv, zz.x, o.x); o.y = fmaf(tv, zz.y, o.y); o.z = fmaf(tv, zz.z, o.z); o.w = fmaf(tv, zz.w, o.w);
-    }
-    *reinterpret_cast<float4*>(Tsm + (32 + r) * kTPad + c0) = make_float4(-o.x, -o.y, -o.z, -o.w);
-  }
-  sync();
-  {
-    // T2 = T diag(beta): thread r = tid / 4, 16 columns from c0
-    const int r = tid >> 2, c0 = (tid & 3) * 16;
-    const float* tr = Tsm + r * kTPad + c0;
+    // T2 = T diag(beta): thread r = lt / 4, 16 columns from c0; entries above the diagonal are 0
+    const int r = lt >> 2, c0 = (lt & 3) * 16;
     float t2[16];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float4 tv = *reinterpret_cast<const float4*>(tr + 4 * q);
-      const int c = c0 + 4 * q;  // T is lower triangular: entries above the diagonal were not formed
+      const float4 tv = *reinterpret_cast<const float4*>(f32_at(TA, r, c0 + 4 * q));
+      const int c = c0 + 4 * q;
       t2[4 * q] = c <= r ? tv.x * bt[c] : 0.f;
       t2[4 * q + 1] = c + 1 <= r ? tv.y * bt[c + 1] : 0.f;
       t2[4 * q + 2] = c + 2 <= r ? tv.z * bt[c + 2] : 0.f;
@@ -166,6 +261,7 @@ __device__ __forceinline__ void invert_T(int tid, const float* Lsm, float* Tsm, 
     for (int q = 0; q < 2; ++q)
       *reinterpret_cast<uint4*>(t2_tile + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t2 + 8 * q);
   }
+  return ok;
 }
 
 // T2 = diag(beta), the image for delta = 0 (L = 0, so T = I): thread r = tid / 4, 16 columns from c0.
@@ -178,6 +274,22 @@ __device__ __forceinline__ void t2_identity(int tid, const float* bt, uint8_t* t
   for (int q = 0; q < 2; ++q)
     *reinterpret_cast<uint4*>(t2_tile + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t2 + 8 * q);
 }
+
+// Kernel 1, one CTA per chunk (record): shared memory (offsets from a 1024-byte aligned base) LT,
+// then the [K;Q] tile (K rows 0-63, Q rows 64-127) for one M=128 MMA giving K K^T and Q K^T, which
+// TA and TB overlay once it is done, then SMt and the gate tables.  Each A operand of the inversion
+// has 8 KB of this CTA's shared memory after it.  Both images go to the record straight from
+// registers.
+constexpr uint32_t kIOffLT = 0;
+constexpr uint32_t kIOffKQ = 16384;
+constexpr uint32_t kIOffTA = kIOffKQ, kIOffTB = kIOffKQ + 16384;
+constexpr uint32_t kIOffSM = kIOffKQ + 32768;
+constexpr uint32_t kIOffGate = kIOffSM + 4096;
+constexpr uint32_t kISmemUsed = kIOffGate + 1024;
+constexpr uint32_t kISmemAlloc = kISmemUsed + 1024;
+static_assert(4 * (kISmemAlloc + 1024) <= 233472, "four inversion CTAs per SM");
+static_assert(kIOffLT + 2 * kPanel + 8192 <= kISmemUsed && kIOffTA + 2 * kPanel + 8192 <= kISmemUsed,
+              "every inversion A operand has 8 KB of shared memory after it");
 
 __global__ void __launch_bounds__(kThreads, 4)
 gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -198,9 +310,6 @@ gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   const int64_t t0 = (int64_t)c * kC;
   const uint32_t sbase = smem_u32(sm);
   float* gate = reinterpret_cast<float*>(sm + kIOffGate);
-  float* Lsm = reinterpret_cast<float*>(sm + kIOffL);
-  float* Zsm = reinterpret_cast<float*>(sm + kIOffZ);
-  float* Tsm = reinterpret_cast<float*>(sm + kIOffT);
   uint8_t* rp = rec_out + rec * kRec;
 
   float al = 1.f, bt = 0.f;
@@ -232,6 +341,7 @@ gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 
   // Every thread waits on the barriers itself (sleeping in hardware).
   bool ok = true, tma_waited = false, mma_pending = false;
+  uint32_t mph = 0;
   do {
     ok = mbar_wait(smem_u32(&bar_tma), 0, status);
     tma_waited = ok;
@@ -242,29 +352,26 @@ gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
       mma_commit(smem_u32(&bar_mma));
     }
     mma_pending = true;
-    ok = mbar_wait(smem_u32(&bar_mma), 0, status);
+    ok = mbar_wait(smem_u32(&bar_mma), mph, status);
+    mph ^= 1u;
     if (__syncthreads_or(!ok)) break;
     mma_pending = false;
     tc_fence_after();
-    // L (rows of K K^T) into shared memory, P (rows of Q K^T) into its image
-    phase_L_Po(tlane + 32 * half, row, half, gate, Lsm, sm + kIOffP, 1.f, a.delta, false);
+    // L (rows of K K^T) into LT, P (rows of Q K^T) into its image in the record
+    phase_LT_Po(tlane + 32 * half, row, half, gate, sm + kIOffLT, rp + kRecP, a.delta);
     tc_fence_before();
     __syncthreads();
-    if (a.delta != 0.f) invert_T(tid, Lsm, Tsm, Zsm, gate + kC, sm + kIOffT2, [] { __syncthreads(); });
-    else t2_identity(tid, gate + kC, sm + kIOffT2);  // the scalar gate: no inverse to form
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      bulk_store(rp + kRecT2, sbase + kIOffT2, 8192);
-      bulk_store(rp + kRecP, sbase + kIOffP, 8192);
-      bulk_commit();
-      bulk_wait_read();
+    if (a.delta != 0.f) {
+      ok = invert_T_tc(tid, sm + kIOffLT, sm + kIOffTA, sm + kIOffTB, sm + kIOffSM, tmem, smem_u32(&bar_mma), mph,
+                       gate + kC, rp + kRecT2, status, [] { __syncthreads(); });
+    } else {
+      t2_identity(tid, gate + kC, rp + kRecT2);  // the scalar gate: no inverse to form
     }
   } while (false);
 
   if (!ok && tid == 0) {
     if (!tma_waited) mbar_wait(smem_u32(&bar_tma), 0, status);
-    if (mma_pending) mbar_wait(smem_u32(&bar_mma), 0, status);
+    if (mma_pending) mbar_wait(smem_u32(&bar_mma), mph ^ 1u, status);
   }
   tc_fence_before();
   __syncthreads();
@@ -274,41 +381,52 @@ gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 // ============================================================================ inversion role
 // The CTAs of a scan launch past its scan CTAs (GdnTask::ready set) form the records themselves, so
 // that the inversion runs on the SMs the scan leaves idle, beside it.  Each such CTA runs two
-// independent pipelines of 8 warps (warps 0-7 and 8-15; warps 16-17 only allocate and free) over
-// the records in chunk-major order (record i: chunk i / BH of pair i % BH), so that every (b,h)
-// gets its early chunks first, as its scan CTA wants them.  Per record the steps of
-// gdn_tinv_kernel, with the [K;Q] tile in two stages (the copy of the record after next goes in
-// once T, formed over the current stage, is dead) and the two images stored straight from
-// registers to the record.  A record's flag is released one record later, at a point where the
-// pipeline waits anyway, and the last one after the loop; the scan's copy issuer acquires it
-// before it copies the record.
-constexpr uint32_t kIGrp = 88064;                     // one pipeline: [K;Q] x 2, L, Z, gate tables
-constexpr uint32_t kIGOffL = 65536;                   // the two [K;Q] stages below (T over one)
-constexpr uint32_t kIGOffZ = kIGOffL + 64 * 65 * 4;
-constexpr uint32_t kIGOffGate = kIGOffZ + 4096;
-static_assert(kIGOffGate + 1024 <= kIGrp && kIGrp % 1024 == 0, "one inversion pipeline's shared memory");
+// independent pipelines of 8 worker warps (warps 0-7 and 8-15) over the records in chunk-major
+// order (record i: chunk i / BH of pair i % BH), so that every (b,h) gets its early chunks first, as
+// its scan CTA wants them.  Per record the steps of gdn_tinv_kernel, with the [K;Q] tile in two
+// stages (the copy of the record after next goes in once T, formed over the current stage, is dead)
+// and the two images stored straight from registers to the record.  Lane 0 of warp 16 + g serves
+// pipeline g off its critical path: it issues the pipeline's copies and, once the workers report a
+// record written, releases the record's flag (the GPU-scope fence that release needs waits for the
+// record's stores, so no worker waits on it); the scan's copy issuer acquires the flag before it
+// copies the record.
+// One pipeline's shared memory: the two [K;Q] stages (TA and TB of a record over its dead stage), LT,
+// SMt and the gate tables.  The A operands of the inversion (LT, TA) have 8 KB of shared memory of
+// the CTA after them (pipeline 1's LT: its SMt, gate tables and the unused end of the allocation).
+constexpr uint32_t kIGOffLT = 65536;
+constexpr uint32_t kIGOffSM = kIGOffLT + 2 * kPanel;
+constexpr uint32_t kIGOffGate = kIGOffSM + 4096;
+constexpr uint32_t kIGrp = kIGOffGate + 1024;
+static_assert(kIGrp % 1024 == 0, "one inversion pipeline's shared memory");
 
 __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                                                const GdnPrefillLaunch& a, int nch, int n_ctas, int cta,
                                                uint8_t* sm, uint8_t* rec_out, unsigned* ready, unsigned* status) {
-  __shared__ uint64_t ibar[2][3];  // per pipeline: [K;Q] landed in stage 0, in stage 1; MMA done
+  // per pipeline: [K;Q] landed in stage 0, in stage 1; MMA done; record written (one arrival per
+  // worker warp); record released (the serving lane)
+  __shared__ uint64_t ibar[2][5];
   __shared__ uint32_t itmem_sh;
   __shared__ float icarry[2];
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int g = warp >> 3;  // pipeline; 2 for the two spare warps
+  const bool worker = warp < 16;
+  const int g = worker ? warp >> 3 : warp - 16;  // the pipeline this warp works in or serves
   const int lt = tid & 255, row = lt & 127, half = lt >> 7;
   const int64_t BH = a.B * a.H, nrec = BH * nch;
   const int64_t stride = 2 * (int64_t)n_ctas;
   const int64_t first = 2 * (int64_t)cta + g;
-  uint8_t* gsm = sm + (uint32_t)(g & 1) * kIGrp;
+  uint8_t* gsm = sm + (uint32_t)g * kIGrp;
   const uint32_t gbase = smem_u32(gsm);
-  float* Lsm = reinterpret_cast<float*>(gsm + kIGOffL);
-  float* Zsm = reinterpret_cast<float*>(gsm + kIGOffZ);
+  uint8_t* LT = gsm + kIGOffLT;
+  uint8_t* SMt = gsm + kIGOffSM;
   float* gate = reinterpret_cast<float*>(gsm + kIGOffGate);
+  const uint32_t bar_done = smem_u32(&ibar[g][3]), bar_rel = smem_u32(&ibar[g][4]);
 
   if (tid == 0) {
-    for (int p = 0; p < 2; ++p)
+    for (int p = 0; p < 2; ++p) {
       for (int j = 0; j < 3; ++j) mbar_init(smem_u32(&ibar[p][j]), 1);
+      mbar_init(smem_u32(&ibar[p][3]), 8);
+      mbar_init(smem_u32(&ibar[p][4]), 1);
+    }
     fence_mbar_init();
     tma_prefetch_desc(tmap_k);
     tma_prefetch_desc(tmap_q);
@@ -320,14 +438,75 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = itmem_sh + 64u * (uint32_t)(g & 1);
+  const uint32_t tmem = itmem_sh + 64u * (uint32_t)g;
   const uint32_t tlane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 
-  if (g < 2) {
+  if (worker) {
     auto sync = [g] { named_bar_sync(1 + g, 256); };
     const uint32_t bar_mma = smem_u32(&ibar[g][2]);
-    int issued[2] = {0, 0};  // the leader's loads per stage
-    // the [K;Q] tile of record i into stage st (leader only)
+    // alpha and beta of token lt of record i as stored (threads 0..63; padded tokens: alpha = 1,
+    // beta = 0); loaded a record ahead and taken apart only when that record starts
+    auto gates_raw = [&](int64_t i, float& al, float& bt) {
+      al = 1.f;
+      bt = 0.f;
+      if (lt < kC && i < nrec) {
+        const int64_t bh = i % BH, t = (i / BH) * kC + lt;
+        const int b = (int)(bh / a.H), h = (int)(bh % a.H);
+        if (t < a.N) {
+          al = a.alpha[b * a.a_sb + h * a.a_sh + t];
+          bt = a.beta[b * a.b_sb + h * a.b_sh + t];
+        }
+      }
+    };
+    float al_n, bt_n;
+    gates_raw(first, al_n, bt_n);
+    bool ok = true, mma_pending = false;
+    uint32_t mph = 0;  // next phase parity of bar_mma (five commits a record with the inversion)
+    int k = 0;
+    for (int64_t i = first; i < nrec; i += stride, ++k) {
+      const int st = k & 1;
+      const float lg = logf(al_n), bt = bt_n;
+      gates_raw(i + stride, al_n, bt_n);  // the next record's gates load during this one
+      gate_tables(lt, lg, bt, gate, &icarry[g], sync);
+      ok = mbar_wait(smem_u32(&ibar[g][st]), (uint32_t)((k >> 1) & 1), status);
+      if (named_bar_or(1 + g, 256, !ok)) break;
+      if (lt == 0) {
+        tc_fence_after();
+        mma_kq(tmem, gbase + (uint32_t)st * 32768u);
+        mma_commit(bar_mma);
+      }
+      mma_pending = true;
+      ok = mbar_wait(bar_mma, mph, status);
+      mph ^= 1u;
+      if (named_bar_or(1 + g, 256, !ok)) break;
+      mma_pending = false;
+      tc_fence_after();
+      const int64_t bh = i % BH, r = bh * nch + i / BH;
+      uint8_t* rp = rec_out + r * kRec;
+      phase_LT_Po(tlane + 32 * half, row, half, gate, LT, rp + kRecP, a.delta);
+      tc_fence_before();
+      sync();
+      uint8_t* stage = gsm + (uint32_t)st * 32768u;  // TA and TB over the dead [K;Q] tile
+      if (a.delta != 0.f) {
+        if (!invert_T_tc(lt, LT, stage, stage + 16384, SMt, tmem, bar_mma, mph, gate + kC, rp + kRecT2, status, sync))
+          ok = false;
+      } else {
+        t2_identity(lt, gate + kC, rp + kRecT2);
+      }
+      fence_proxy_async_smem();  // T's writes before the copy that overwrites the stage
+      // record written: one arrival per warp, once the serving lane has released the record before
+      // (so that this arrival opens the next phase only after that one was seen)
+      __syncwarp();
+      if ((tid & 31) == 0) {
+        if (k > 0 && !mbar_wait(bar_rel, (uint32_t)((k - 1) & 1), status)) ok = false;
+        mbar_arrive(bar_done);
+      }
+      sync();  // gate tables and T are rewritten by the next record
+    }
+    if (lt == 0 && !ok && mma_pending) mbar_wait(bar_mma, mph ^ 1u, status);
+  } else if ((tid & 31) == 0) {
+    // the serving lane of pipeline g: copies and flag releases
+    int issued[2] = {0, 0};
     auto load = [&](int64_t i, int st) {
       const int64_t bh = i % BH;
       const int t0 = (int)((i / BH) * kC), b = (int)(bh / a.H), h = (int)(bh % a.H);
@@ -339,72 +518,67 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
       tma_load_4d(dst + 24576, tmap_q, 64, t0, h, b, bar);
       ++issued[st];
     };
-    // log alpha and beta of token lt of record i (threads 0..63; padded tokens: alpha = 1, beta = 0)
-    auto gates_of = [&](int64_t i, float& lg, float& bt) {
-      lg = 0.f;
-      bt = 0.f;
-      if (lt < kC && i < nrec) {
-        const int64_t bh = i % BH, t = (i / BH) * kC + lt;
-        const int b = (int)(bh / a.H), h = (int)(bh % a.H);
-        if (t < a.N) {
-          lg = logf(a.alpha[b * a.a_sb + h * a.a_sh + t]);
-          bt = a.beta[b * a.b_sb + h * a.b_sh + t];
-        }
-      }
-    };
-    if (lt == 0) {
-      if (first < nrec) load(first, 0);
-      if (first + stride < nrec) load(first + stride, 1);
-    }
-    float lg_n, bt_n;
-    gates_of(first, lg_n, bt_n);
-    bool ok = true, mma_pending = false;
-    int64_t prev = -1;
+    if (first < nrec) load(first, 0);
+    if (first + stride < nrec) load(first + stride, 1);
+    bool ok = true;
     int k = 0;
     for (int64_t i = first; i < nrec; i += stride, ++k) {
-      const int st = k & 1;
-      const float lg = lg_n, bt = bt_n;
-      gates_of(i + stride, lg_n, bt_n);  // the next record's gates load during this one
-      gate_tables(lt, lg, bt, gate, &icarry[g], sync);
-      ok = mbar_wait(smem_u32(&ibar[g][st]), (uint32_t)((k >> 1) & 1), status);
-      if (lt == 0 && prev >= 0) flag_release(ready + prev, 1u);
-      if (named_bar_or(1 + g, 256, !ok)) break;
-      if (lt == 0) {
-        tc_fence_after();
-        mma_kq(tmem, gbase + (uint32_t)st * 32768u);
-        mma_commit(bar_mma);
-      }
-      mma_pending = true;
-      ok = mbar_wait(bar_mma, (uint32_t)(k & 1), status);
-      if (named_bar_or(1 + g, 256, !ok)) break;
-      mma_pending = false;
-      tc_fence_after();
+      ok = mbar_wait(bar_done, (uint32_t)(k & 1), status);
+      if (!ok) break;
+      if (i + 2 * stride < nrec) load(i + 2 * stride, k & 1);  // the workers are done with T there
       const int64_t bh = i % BH, r = bh * nch + i / BH;
-      uint8_t* rp = rec_out + r * kRec;
-      phase_L_Po(tlane + 32 * half, row, half, gate, Lsm, rp + kRecP, 1.f, a.delta, false);
-      tc_fence_before();
-      sync();
-      float* Tsm = reinterpret_cast<float*>(gsm + (uint32_t)st * 32768u);  // over the dead [K;Q] tile
-      if (a.delta != 0.f) invert_T(lt, Lsm, Tsm, Zsm, gate + kC, rp + kRecT2, sync);
-      else t2_identity(lt, gate + kC, rp + kRecT2);
-      fence_proxy_async_smem();  // T's writes before the copy that overwrites the stage
-      sync();
-      if (lt == 0 && i + 2 * stride < nrec) load(i + 2 * stride, st);
-      prev = r;
+      flag_release(ready + r, 1u);
+      mbar_arrive(bar_rel);
     }
-    if (lt == 0) {
-      if (ok && prev >= 0) flag_release(ready + prev, 1u);
-      if (!ok) {
-        // let this pipeline's own copies and MMA finish (bounded) before the CTA exits
-        for (int st = 0; st < 2; ++st)
-          if (issued[st] > 0) mbar_wait(smem_u32(&ibar[g][st]), (uint32_t)((issued[st] - 1) & 1), status);
-        if (mma_pending) mbar_wait(bar_mma, (uint32_t)(k & 1), status);
-      }
+    if (!ok) {
+      // let this pipeline's own copies finish (bounded) before the CTA exits
+      for (int st = 0; st < 2; ++st)
+        if (issued[st] > 0) mbar_wait(smem_u32(&ibar[g][st]), (uint32_t)((issued[st] - 1) & 1), status);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(itmem_sh, 128);
+}
+
+// ============================================================================ placement
+// Where a launch's CTAs sit matters for the scan: measured on GB300, 64 scan CTAs on the lowest SM
+// ids (as a 64-CTA launch is placed) take ~540 us at 16K tokens, while the same CTAs spread eight to
+// each group of 16 SM ids (as the full-GPU launch places its first 64 CTAs) take 660-750 us, with the
+// other SMs idle or not.  So a launch that forms its own records gives its roles by placement: every
+// CTA marks its SM id, all meet at one grid barrier (the launch is cooperative, so all CTAs are
+// resident), and a CTA's rank among the marked ids is its index: the lowest n_scan scan.  Every CTA
+// falls back to blockIdx.x, consistently, if the SM ids are out of range or shared, or the barrier
+// expires (the status then reports it).
+constexpr unsigned kMaxSmIds = 1024;
+constexpr size_t kPlaceBytes = ((1 + kMaxSmIds) * sizeof(unsigned) + 255) & ~size_t(255);
+
+__device__ __forceinline__ int placement_rank(unsigned* place, unsigned* status) {
+  __shared__ int rank_sh;
+  __shared__ int bad_sh;
+  unsigned smid, nsmid;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+  asm volatile("mov.u32 %0, %%nsmid;" : "=r"(nsmid));
+  if (nsmid > kMaxSmIds) return (int)blockIdx.x;  // the same for every CTA of the launch
+  if (threadIdx.x == 0) {
+    rank_sh = 0;
+    bad_sh = 0;
+    atomicAdd(place + 1 + smid, 1u);
+    asm volatile("fence.acq_rel.gpu;\n\tred.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(place) : "memory");
+    if (!flag_wait(place, gridDim.x, status)) bad_sh = 1;
+  }
+  __syncthreads();
+  int below = 0, shared_id = 0;
+  for (unsigned s = threadIdx.x; s < nsmid; s += blockDim.x) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(place + 1 + s) : "memory");
+    if (s < smid) below += (int)v;
+    shared_id |= v > 1u;
+  }
+  if (below) atomicAdd(&rank_sh, below);
+  if (shared_id) bad_sh = 1;
+  __syncthreads();
+  return bad_sh ? (int)blockIdx.x : rank_sh;
 }
 
 // ============================================================================ kernel 2
@@ -441,6 +615,8 @@ static_assert(kKSlot % 1024 == 0 && kQSlot % 1024 == 0 && kSOffV % 1024 == 0 && 
                   kSOffWT % 1024 == 0 && kSOffT1 % 1024 == 0,
               "MMA operand tiles sit on 1024-byte boundaries");
 static_assert(kSSmemAlloc + 512 <= 232448, "shared memory budget");
+static_assert(kIGrp + kIGOffLT + 2 * kPanel + 8192 <= kSSmemUsed && 2 * kIGrp <= kSSmemUsed,
+              "the inversion role's two pipelines, and the 8 KB after pipeline 1's LT, fit the scan's shared memory");
 // gate slot layout (floats)
 constexpr int kGGam = 0, kGKds = 64, kGSig = 128, kGSigAfter = 129, kGFold = 130;
 
@@ -479,9 +655,10 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
                 int nch_total, uint8_t* rec, unsigned* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  if (task.ready != nullptr && (int)blockIdx.x >= task.n_scan) {
-    inversion_role(&tmap_q, &tmap_k, a, nch_total, (int)gridDim.x - task.n_scan, (int)blockIdx.x - task.n_scan,
-                   sm, rec, task.ready, status);
+  const int cta = task.ready != nullptr ? placement_rank(task.place, status) : (int)blockIdx.x;
+  if (task.ready != nullptr && cta >= task.n_scan) {
+    inversion_role(&tmap_q, &tmap_k, a, nch_total, (int)gridDim.x - task.n_scan, cta - task.n_scan, sm, rec,
+                   task.ready, status);
     return;
   }
   __shared__ uint64_t bar_k[kKSlots];  // K and the T2 image landed in their slot
@@ -509,7 +686,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   __shared__ float lshare[2];        // local warps: scan carry, gamma_C
 
   const int tid = threadIdx.x, warp = tid >> 5;
-  const CtaWork wk = cta_work(a, task);
+  const CtaWork wk = cta_work(a, task, cta);
   const int b = wk.b, h = wk.h;
   const int n = wk.nchunks;
   const bool WOUT = wk.write_out, ZV = wk.zero_v;
@@ -776,18 +953,24 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
     // ======================================================================= copy issuer
     // Lane 0 issues the copies of every chunk in order, each into its ring slot once the slot's
     // earlier contents are no longer read: K and T2 of chunk m after the update of chunk m-3, V after
-    // U~ of chunk m-2, Q and P after the outputs of chunk m-2.
+    // U~ of chunk m-2, Q and P after the outputs of chunk m-2.  When this launch forms the records
+    // itself, the flag of chunk m+1's record is read early (relaxed, while the issuer waits for the
+    // slots of chunk m) and, if already set, turned into an acquire with a fence where the copy is
+    // issued; otherwise the issuer waits on it there.
     const bool leader = (tid & 31) == 0;
     int nk = 0, nv = 0, nq = 0;
     if (leader) {
+      const unsigned* flags = task.ready != nullptr ? task.ready + rec0 : nullptr;
+      unsigned seen = (flags != nullptr && n > 0) ? flag_peek(flags) : 0u;
       bool ok = true;
       for (int m = 0; ok && m < n; ++m) {
         const int t0 = (int)(wk.t_begin + (int64_t)m * kC);
         if (m >= kKSlots) ok = wait(&bar_kfree[m % kKSlots], kpar(m - kKSlots));
-        if (ok && task.ready != nullptr) {
-          // the record is formed in this launch: wait for its flag, then copy it
-          ok = flag_wait(task.ready + rec0 + m, 1u, status);
+        if (ok && flags != nullptr) {
+          if (seen == 1u) fence_acq_rel_gpu();  // the early read saw the flag: acquire
+          else ok = flag_wait(flags + m, 1u, status);
           fence_proxy_async_global();
+          seen = m + 1 < n ? flag_peek(flags + m + 1) : 0u;
         }
         if (!ok) break;
         {
@@ -1091,7 +1274,10 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 
 size_t records_bytes(int64_t BH, int64_t nch) { return (size_t)(BH * nch) * kRec; }
 // one ready flag per record, for the launch that forms its records itself
-size_t flags_bytes(int64_t BH, int64_t nch) { return ((size_t)(BH * nch) * sizeof(unsigned) + 255) & ~size_t(255); }
+// plus the placement scratch of that launch
+size_t flags_bytes(int64_t BH, int64_t nch) {
+  return (((size_t)(BH * nch) * sizeof(unsigned) + 255) & ~size_t(255)) + kPlaceBytes;
+}
 
 // The fewest inversion CTAs worth a launch that forms its own records.
 constexpr int kMinInversionCtas = 16;
@@ -1141,9 +1327,10 @@ cudaError_t launch_scan_typed(const GdnPrefillLaunch& a, void* ws, unsigned* sta
   const int n_co = coresident[gated ? 1 : 0];
   if (plan.G == 1 && BH + kMinInversionCtas <= n_co) {
     // one launch: CTAs 0..BH-1 scan, the rest of the GPU forms the records beside them
-    cudaError_t e = cudaMemsetAsync(ready, 0, (size_t)(BH * nch) * sizeof(unsigned), stream);
+    cudaError_t e = cudaMemsetAsync(ready, 0, flags_bytes(BH, nch), stream);
     if (e != cudaSuccess) return e;
-    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr, (int)BH, ready};
+    unsigned* place = ready + (flags_bytes(BH, nch) - kPlaceBytes) / sizeof(unsigned);
+    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr, (int)BH, ready, place};
     return launch_cooperative(scan, dim3((unsigned)n_co), dim3(kScanThreads), kSSmemAlloc, stream, mq, mk, mv, a,
                               task, (int)nch, recT, status);
   }

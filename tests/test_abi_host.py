@@ -146,7 +146,9 @@ def test_decode_rejections(lib):
 
 def test_gdn_workspace_queries_and_rejection(lib):
     rec = 16384  # two-kernel scan: bytes of the per-chunk record (T diag(beta) and P images) of one (b,h)
-    flags = lambda n: (4 * n + 255) // 256 * 256  # a 4-byte ready flag per record, rounded up to 256 bytes
+    # a 4-byte ready flag per record, rounded up to 256 bytes, and the launch's placement scratch (an
+    # arrival counter and a word per SM id up to 1024, rounded up to 256 bytes)
+    flags = lambda n: (4 * n + 255) // 256 * 256 + 4352
     big = gdn_args(B=1, H=16, N=1 << 20)
     need_min = lib.la_gdn_prefill_workspace_size_min(ctypes.byref(big))
     need = lib.la_gdn_prefill_workspace_size(ctypes.byref(big))
