@@ -52,18 +52,16 @@ constexpr uint32_t kRecT2 = 0, kRecP = 8192, kRec = 16384;
 
 // ============================================================================ kernel 1
 // T = (I + L)^{-1} of a 64-token chunk by doubling, [[A, 0], [C, B]]^{-1} = [[A^{-1}, 0],
-// [-B^{-1} C A^{-1}, B^{-1}]]: the four 16x16 diagonal blocks by forward substitution on the CUDA
-// cores, the 32- and 64-level off-diagonal blocks as tcgen05 MMAs (kind::tf32: fp32 operands at tf32
-// precision, fp32 accumulation).  Every operand is an fp32 K-major tile with the 128-byte swizzle
-// (panels of [64 rows][32 columns], 8 KB):
+// [-B^{-1} C A^{-1}, B^{-1}]]: the four 16x16 diagonal blocks by forward substitution and the
+// 32-level blocks on the CUDA cores, the two 64-level products (32x32x32) as tcgen05 MMAs (kind::tf32:
+// fp32 operands at tf32 precision, fp32 accumulation).  Every MMA operand is an fp32 K-major tile
+// with the 128-byte swizzle (panels of [64 rows][32 columns], 8 KB):
 //   LT  L, strictly lower (16 KB);      TA  T, row-major (16 KB);      TB  T^T (16 KB);
-//   SMt the small B operands: X_10^T and X_32^T ([16][32] each, 2 KB), later Z^T ([32][32], 4 KB).
+//   SMt 4 KB: the 32-level's products, then Z^T ([32][32]).
 // The MMAs run at M = 128 with the chunk's 64 rows in lanes 0..63 (the accumulator layout of every
 // other MMA here); A rows 64..127 run over the 8 KB that follow each A tile, which must be shared
 // memory of this CTA, and give accumulator rows that are never read.
-//   X_10 = L_10 T_00, X_32 = L_32 T_22          (rows 16-31, 48-63)       N = 16, K = 16
-//   T_10 = -T_11 X_10, T_32 = -T_33 X_32          (the 32-level blocks)     N = 16, K = 16
-//   Z    = L_[32:64][0:32] T_[0:32][0:32]        (rows 32-63)             N = 32, K = 32
+//   Z               = L_[32:64][0:32] T_[0:32][0:32]      (rows 32-63)   N = 32, K = 32
 //   T_[32:64][0:32] = -T_[32:64][32:64] Z                                  N = 32, K = 32
 constexpr uint32_t kPanel = 8192;  // one [64][32] fp32 panel
 
@@ -110,9 +108,16 @@ __device__ __forceinline__ void phase_LT_Po(uint32_t kq_taddr, int row, int half
 // T from L (both as above), then the bf16 image T2 = T diag(beta) into t2_tile (shared or global).
 // lt: thread 0..255 of the 256 that call it (warp lt / 32 must sit at a multiple of four warps in
 // the CTA, so that it reads TMEM lanes 32 (lt / 32 % 4)..); tm: 64 TMEM columns of this group, free;
-// bar: an mbarrier that takes one arrival per commit, *mph its next phase parity (the same in every
+// bar: an mbarrier that takes one arrival per commit, mph its next phase parity (the same in every
 // thread).  Thread lt == 0 issues the MMAs.  `sync` is a barrier of the 256.  An expired wait is
 // recorded in *status and makes it return false; the steps still run, so that every barrier is met.
+//   1. the 16x16 diagonal blocks by forward substitution (threads 0..63, one column each, rows of L
+//      read 16 bytes at a time); TA gets the column, TB the same values as a row;
+//   2. the 32-level blocks T_10 = -T_11 (L_10 T_00) and T_32 = -T_33 (L_32 T_22) on the CUDA cores
+//      (16x16 products, two outputs a thread, through SMt);
+//   3. Z = L_[32:64][0:32] T_[0:32][0:32] as an MMA; meanwhile the T2 image of everything already
+//      final (rows 0-31, and rows 32-63 columns 32-63);
+//   4. T_[32:64][0:32] = -T_[32:64][32:64] Z as an MMA, its T2 image stored from the registers.
 template <typename Sync>
 __device__ __forceinline__ bool invert_T_tc(int lt, uint8_t* LT, uint8_t* TA, uint8_t* TB, uint8_t* SMt, uint32_t tm,
                                             uint32_t bar, uint32_t& mph, const float* bt, uint8_t* t2_tile,
@@ -124,93 +129,119 @@ __device__ __forceinline__ bool invert_T_tc(int lt, uint8_t* LT, uint8_t* TA, ui
     mph ^= 1u;
     tc_fence_after();
   };
-  // diagonal blocks: thread (block lt / 16, column lt % 16) by forward substitution; TA gets the
-  // column, TB the same values as a row
-  if (lt < kC) {
-    const int base = (lt >> 4) * 16, col = lt & 15;
-    float x[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) x[r] = (r == col) ? 1.f : 0.f;
-#pragma unroll
-    for (int j = 0; j < 15; ++j) {
-#pragma unroll
-      for (int r = j + 1; r < 16; ++r) x[r] = fmaf(-*f32_at(LT, base + r, base + j), x[j], x[r]);
-    }
-#pragma unroll
-    for (int r = 0; r < 16; ++r) *f32_at(TA, base + r, base + col) = x[r];
+  // 16 consecutive fp32 of row `row` of a [64][64] tile from column c0 (c0 % 16 == 0) as 4 float4
+  auto row16 = [](const uint8_t* tile, int row, int c0, float4 (&o)[4]) {
+    const uint8_t* rp = tile + (uint32_t)(c0 >> 5) * kPanel + (uint32_t)row * 128u;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
-      *reinterpret_cast<float4*>(f32_at(TB, base + col, base + 4 * q)) =
+      o[q] = *reinterpret_cast<const float4*>(rp + ((((uint32_t)((c0 & 31) >> 2) + q) ^ (uint32_t)(row & 7)) << 4));
+  };
+  if (lt < kC) {
+    // x[r] = delta_rc - sum_{j<r} L[base+r][base+j] x[j]: column c of the block's inverse
+    const int base = (lt >> 4) * 16, c = lt & 15;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = (r == c) ? 1.f : 0.f;
+      if (r > 0) {
+        float4 l4[4];
+        row16(LT, base + r, base, l4);
+        const float* l = reinterpret_cast<const float*>(l4);
+        float acc2 = 0.f;
+#pragma unroll
+        for (int j = 0; j < r; ++j) {
+          if (j & 1) acc2 = fmaf(-l[j], x[j], acc2);
+          else acc = fmaf(-l[j], x[j], acc);
+        }
+        acc += acc2;
+      }
+      x[r] = acc;
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) *f32_at(TA, base + r, base + c) = x[r];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      *reinterpret_cast<float4*>(f32_at(TB, base + c, base + 4 * q)) =
           make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
   } else if (lt < 2 * kC) {
-    // the two upper blocks an MMA reads: TB rows 16-31 x columns 0-15 (T_01^T... zero) and TA rows
-    // 32-47 x columns 48-63 (T_23, zero)
+    // the two upper blocks an MMA reads: TB rows 16-31 x columns 0-15 (T_01 transposed) and TA rows
+    // 32-47 x columns 48-63 (T_23): zero
     const int e = lt - kC, r = e >> 2, c = 4 * (e & 3);
     *reinterpret_cast<float4*>(f32_at(TB, 16 + r, c)) = make_float4(0.f, 0.f, 0.f, 0.f);
     *reinterpret_cast<float4*>(f32_at(TA, 32 + r, 48 + c)) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  sync();
+  // 32-level, pair k (blocks (1,0) for k = 0, (3,2) for k = 1): this thread's row r and columns c, c+1
+  const int k2 = lt >> 7, r16 = (lt >> 3) & 15, cp = (lt & 7) * 2;
+  float* Zt = reinterpret_cast<float*>(SMt) + k2 * 16 * 20;  // Z_k^T [16][20]
+  {
+    float4 lr[4], t0[4], t1[4];
+    row16(LT, 32 * k2 + 16 + r16, 32 * k2, lr);      // L_(2k+1)(2k) row r
+    row16(TB, 32 * k2 + cp, 32 * k2, t0);            // column cp of T_(2k)(2k)
+    row16(TB, 32 * k2 + cp + 1, 32 * k2, t1);        // column cp+1
+    const float* l = reinterpret_cast<const float*>(lr);
+    const float* a0 = reinterpret_cast<const float*>(t0);
+    const float* a1 = reinterpret_cast<const float*>(t1);
+    float z0 = 0.f, z1 = 0.f;
+#pragma unroll
+    for (int m = 0; m < 16; ++m) {
+      z0 = fmaf(l[m], a0[m], z0);
+      z1 = fmaf(l[m], a1[m], z1);
+    }
+    Zt[cp * 20 + r16] = z0;
+    Zt[(cp + 1) * 20 + r16] = z1;
+  }
+  sync();
+  {
+    float4 tr[4], z0[4], z1[4];
+    const int R = 32 * k2 + 16 + r16;
+    row16(TA, R, 32 * k2 + 16, tr);                  // T_(2k+1)(2k+1) row r
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      z0[q] = *reinterpret_cast<const float4*>(Zt + cp * 20 + 4 * q);
+      z1[q] = *reinterpret_cast<const float4*>(Zt + (cp + 1) * 20 + 4 * q);
+    }
+    const float* t = reinterpret_cast<const float*>(tr);
+    const float* b0 = reinterpret_cast<const float*>(z0);
+    const float* b1 = reinterpret_cast<const float*>(z1);
+    float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      o0 = fmaf(t[p], b0[p], o0);
+      o1 = fmaf(t[p], b1[p], o1);
+    }
+    const int C = 32 * k2 + cp;
+    *f32_at(TA, R, C) = -o0;
+    *f32_at(TA, R, C + 1) = -o1;
+    *f32_at(TB, C, R) = -o0;
+    *f32_at(TB, C + 1, R) = -o1;
+  }
   fence_proxy_async_smem();
   sync();
   const uint32_t la = smem_u32(LT), ta = smem_u32(TA), tb = smem_u32(TB), sa = smem_u32(SMt);
-  const uint32_t id16 = idesc_tf32(128, 16), id32 = idesc_tf32(128, 32);
-  if (lt == 0) {
-    tc_fence_after();
-#pragma unroll
-    for (int s = 0; s < 2; ++s) mma_tf32(tm + 0, kmaj(la + 32 * s), kmaj(tb + 32 * s), id16, s > 0);
-#pragma unroll
-    for (int s = 0; s < 2; ++s)
-      mma_tf32(tm + 16, kmaj(la + kPanel + 32 * s), kmaj(tb + kPanel + 32 * 128 + 32 * s), id16, s > 0);
-    mma_commit(bar);
-  }
-  mma_done();
-  // X_10 (warp 0, lanes 16-31 = rows 16-31) and X_32 (warp 1, rows 48-63), transposed into SMt
-  if (w < 2) {
-    float v[16];
-    tmem_ld16(tm + ((uint32_t)(32 * w) << 16) + 16u * (uint32_t)w, v);
-    tmem_ld_wait();
-    if (lane >= 16) {
-      uint8_t* xt = SMt + 2048 * w;
-#pragma unroll
-      for (int n = 0; n < 16; ++n) *reinterpret_cast<float*>(xt + sw128_off_f32(n, lane - 16, 16)) = v[n];
-    }
-  }
-  tc_fence_before();
-  fence_proxy_async_smem();
-  sync();
-  if (lt == 0) {
-    tc_fence_after();
-#pragma unroll
-    for (int s = 0; s < 2; ++s) mma_tf32(tm + 32, kmaj(ta + 64 + 32 * s), kmaj(sa + 32 * s), id16, s > 0);
-#pragma unroll
-    for (int s = 0; s < 2; ++s)
-      mma_tf32(tm + 48, kmaj(ta + kPanel + 64 + 32 * s), kmaj(sa + 2048 + 32 * s), id16, s > 0);
-    mma_commit(bar);
-  }
-  mma_done();
-  // T_10 = -T_11 X_10 (warp 0) and T_32 = -T_33 X_32 (warp 1): into TA, and transposed into TB
-  if (w < 2) {
-    float v[16];
-    tmem_ld16(tm + ((uint32_t)(32 * w) << 16) + 32u + 16u * (uint32_t)w, v);
-    tmem_ld_wait();
-    if (lane >= 16) {
-      const int R = 16 + 32 * w + (lane - 16), C0 = 32 * w;
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<float4*>(f32_at(TA, R, C0 + 4 * q)) =
-            make_float4(-v[4 * q], -v[4 * q + 1], -v[4 * q + 2], -v[4 * q + 3]);
-#pragma unroll
-      for (int n = 0; n < 16; ++n) *f32_at(TB, C0 + n, R) = -v[n];
-    }
-  }
-  tc_fence_before();
-  fence_proxy_async_smem();
-  sync();
+  const uint32_t id32 = idesc_tf32(128, 32);
   if (lt == 0) {
     tc_fence_after();
 #pragma unroll
     for (int s = 0; s < 4; ++s) mma_tf32(tm + 0, kmaj(la + 32 * s), kmaj(tb + 32 * s), id32, s > 0);
     mma_commit(bar);
   }
+  // T2 = T diag(beta) of what is final: rows 0-31 (thread: row lt / 8, 8 columns), and rows 32-63
+  // columns 32-63 (threads 0..127: row 32 + lt / 4, 8 columns from 32); 0 above the diagonal
+  auto t2_chunk = [&](int r, int c0) {
+    float4 a4[2];
+    const uint8_t* rp = TA + (uint32_t)(c0 >> 5) * kPanel + (uint32_t)r * 128u;
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+      a4[q] = *reinterpret_cast<const float4*>(rp + ((((uint32_t)((c0 & 31) >> 2) + q) ^ (uint32_t)(r & 7)) << 4));
+    const float* tv = reinterpret_cast<const float*>(a4);
+    float t2[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t2[j] = c0 + j <= r ? tv[j] * bt[c0 + j] : 0.f;
+    *reinterpret_cast<uint4*>(t2_tile + sw128_off(r, c0, 64)) = pack8_bf16(t2);
+  };
+  t2_chunk(lt >> 3, (lt & 7) * 8);
+  if (lt < 128) t2_chunk(32 + (lt >> 2), 32 + (lt & 3) * 8);
   mma_done();
   // Z (rows 32-63: warps 1 and 5, 16 columns each), transposed into SMt
   if (w == 1 || w == 5) {
@@ -231,36 +262,20 @@ __device__ __forceinline__ bool invert_T_tc(int lt, uint8_t* LT, uint8_t* TA, ui
     mma_commit(bar);
   }
   mma_done();
-  // T_[32:64][0:32] = -(T_[32:64][32:64] Z) into TA (warps 1 and 5, 16 columns each)
+  // T_[32:64][0:32] = -(T_[32:64][32:64] Z): its T2 image straight from the registers (warps 1 and
+  // 5: row 32 + lane, 16 columns each; all below the diagonal)
   if (w == 1 || w == 5) {
     const int c0 = w == 1 ? 0 : 16;
     float v[16];
     tmem_ld16(tm + (32u << 16) + 32u + (uint32_t)c0, v);
     tmem_ld_wait();
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      *reinterpret_cast<float4*>(f32_at(TA, 32 + lane, c0 + 4 * q)) =
-          make_float4(-v[4 * q], -v[4 * q + 1], -v[4 * q + 2], -v[4 * q + 3]);
-  }
-  tc_fence_before();
-  sync();
-  {
-    // T2 = T diag(beta): thread r = lt / 4, 16 columns from c0; entries above the diagonal are 0
-    const int r = lt >> 2, c0 = (lt & 3) * 16;
-    float t2[16];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 tv = *reinterpret_cast<const float4*>(f32_at(TA, r, c0 + 4 * q));
-      const int c = c0 + 4 * q;
-      t2[4 * q] = c <= r ? tv.x * bt[c] : 0.f;
-      t2[4 * q + 1] = c + 1 <= r ? tv.y * bt[c + 1] : 0.f;
-      t2[4 * q + 2] = c + 2 <= r ? tv.z * bt[c + 2] : 0.f;
-      t2[4 * q + 3] = c + 3 <= r ? tv.w * bt[c + 3] : 0.f;
-    }
+    for (int j = 0; j < 16; ++j) v[j] = -v[j] * bt[c0 + j];
 #pragma unroll
     for (int q = 0; q < 2; ++q)
-      *reinterpret_cast<uint4*>(t2_tile + sw128_off(r, c0 + 8 * q, 64)) = pack8_bf16(t2 + 8 * q);
+      *reinterpret_cast<uint4*>(t2_tile + sw128_off(32 + lane, c0 + 8 * q, 64)) = pack8_bf16(v + 8 * q);
   }
+  tc_fence_before();
   return ok;
 }
 
