@@ -459,14 +459,19 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
   if (worker) {
     auto sync = [g] { named_bar_sync(1 + g, 256); };
     const uint32_t bar_mma = smem_u32(&ibar[g][2]);
-    // alpha and beta of token lt of record i as stored (threads 0..63; padded tokens: alpha = 1,
+    // record i's (b,h) pair and chunk, advanced by stride without divisions; *_n: record i + stride
+    const int64_t dbh = stride % BH, dch = stride / BH;
+    int64_t bh_c = first % BH, ch_c = first / BH;
+    int64_t bh_n = bh_c + dbh, ch_n = ch_c + dch;
+    if (bh_n >= BH) bh_n -= BH, ++ch_n;
+    // alpha and beta of token lt of a record as stored (threads 0..63; padded tokens: alpha = 1,
     // beta = 0); loaded a record ahead and taken apart only when that record starts
-    auto gates_raw = [&](int64_t i, float& al, float& bt) {
+    auto gates_raw = [&](int64_t i, int64_t bh, int64_t ch, float& al, float& bt) {
       al = 1.f;
       bt = 0.f;
       if (lt < kC && i < nrec) {
-        const int64_t bh = i % BH, t = (i / BH) * kC + lt;
-        const int b = (int)(bh / a.H), h = (int)(bh % a.H);
+        const int64_t t = ch * kC + lt;
+        const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
         if (t < a.N) {
           al = a.alpha[b * a.a_sb + h * a.a_sh + t];
           bt = a.beta[b * a.b_sb + h * a.b_sh + t];
@@ -474,14 +479,14 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
       }
     };
     float al_n, bt_n;
-    gates_raw(first, al_n, bt_n);
+    gates_raw(first, bh_c, ch_c, al_n, bt_n);
     bool ok = true, mma_pending = false;
     uint32_t mph = 0;  // next phase parity of bar_mma (five commits a record with the inversion)
     int k = 0;
     for (int64_t i = first; i < nrec; i += stride, ++k) {
       const int st = k & 1;
       const float lg = logf(al_n), bt = bt_n;
-      gates_raw(i + stride, al_n, bt_n);  // the next record's gates load during this one
+      gates_raw(i + stride, bh_n, ch_n, al_n, bt_n);  // the next record's gates load during this one
       gate_tables(lt, lg, bt, gate, &icarry[g], sync);
       ok = mbar_wait(smem_u32(&ibar[g][st]), (uint32_t)((k >> 1) & 1), status);
       if (named_bar_or(1 + g, 256, !ok)) break;
@@ -496,8 +501,7 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
       if (named_bar_or(1 + g, 256, !ok)) break;
       mma_pending = false;
       tc_fence_after();
-      const int64_t bh = i % BH, r = bh * nch + i / BH;
-      uint8_t* rp = rec_out + r * kRec;
+      uint8_t* rp = rec_out + (bh_c * nch + ch_c) * kRec;
       phase_LT_Po(tlane + 32 * half, row, half, gate, LT, rp + kRecP, a.delta);
       tc_fence_before();
       sync();
@@ -517,6 +521,9 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
         mbar_arrive(bar_done);
       }
       sync();  // gate tables and T are rewritten by the next record
+      bh_c = bh_n, ch_c = ch_n;
+      bh_n += dbh, ch_n += dch;
+      if (bh_n >= BH) bh_n -= BH, ++ch_n;
     }
     if (lt == 0 && !ok && mma_pending) mbar_wait(bar_mma, mph ^ 1u, status);
   } else if ((tid & 31) == 0) {
