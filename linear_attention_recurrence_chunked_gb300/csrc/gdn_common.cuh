@@ -17,6 +17,90 @@ namespace la {
 namespace gdn {
 using namespace tc;
 
+// ---------------------------------------------------------------- helpers only these kernels use
+// Orders this thread's generic-proxy view of global memory with its async-proxy (bulk copy)
+// accesses: after acquiring a flag, before copying what the flag guards with cp.async.bulk.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- flags between CTAs of one grid
+// Release: every global write this thread has observed (its own, and those of the threads of its
+// CTA ordered before it by a barrier) is visible GPU-wide before the flag reads `v`.
+__device__ __forceinline__ void flag_release(unsigned* flag, unsigned v) {
+  asm volatile("fence.acq_rel.gpu;\n\tst.relaxed.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+// Waits until *flag == v (acquire: what the releasing thread had observed is then visible to this
+// thread); gives up after kWaitLimitNs, ORs kStatusTimeout into *status and returns false.  Only
+// for flags set by CTAs of the same grid that are co-resident (a cooperative launch) and never
+// wait on the waiting CTA.
+__device__ __forceinline__ bool flag_wait(const unsigned* flag, unsigned v, unsigned* status) {
+  uint64_t t0 = 0;
+  for (int i = 0;; ++i) {
+    unsigned x;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(flag) : "memory");
+    if (x == v) return true;
+    if (i == 0) t0 = globaltimer_ns();
+    else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, kStatusTimeout);
+      return false;
+    }
+    __nanosleep(128);
+  }
+}
+
+// Cooperative launch: every CTA of the grid is resident at once (the launch fails otherwise), so
+// CTAs may wait on flags other CTAs of the grid set.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cooperative(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                               Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// A relaxed GPU-scope read of a flag, issued early; if it already shows the value, fence_acq_rel_gpu
+// where the guarded data is used makes the pair an acquire.
+__device__ __forceinline__ unsigned flag_peek(const unsigned* flag) {
+  unsigned x;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(flag) : "memory");
+  return x;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// Instruction descriptor, kind::tf32: fp32 A/B read from shared memory at tf32 precision, both
+// K-major, fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4)                       // D format: f32
+         | (2u << 7)                     // A format: tf32
+         | (2u << 10)                    // B format: tf32
+         | ((uint32_t)(N >> 3) << 17)    // N / 8
+         | ((uint32_t)(M >> 4) << 24);   // M / 16
+}
+// D[tmem] (+)= A[smem] * B[smem]^T, fp32 operands at tf32 precision (one 8-deep K step: 32 bytes of
+// each operand row), issued by one thread.
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Byte offset of fp32 element (row, col) in a K-major 128-byte-swizzled fp32 tile: panels of 32
+// columns (128-byte rows), `rows` rows per panel; 16-byte chunks of a row permuted by row & 7.
+__host__ __device__ __forceinline__ uint32_t sw128_off_f32(uint32_t row, uint32_t col, uint32_t rows) {
+  return (col >> 5) * rows * 128u + row * 128u + ((((col & 31u) >> 2) ^ (row & 7u)) << 4) + ((col & 3u) << 2);
+}
+
 constexpr int kC = 64;         // tokens per chunk
 constexpr int kD = 128;        // d_k = d_v
 constexpr int kThreads = 256;  // two threads per tensor-memory lane, splitting its columns

@@ -155,44 +155,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Orders this thread's generic-proxy view of global memory with its async-proxy (bulk copy)
-// accesses: after acquiring a flag, before copying what the flag guards with cp.async.bulk.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// ---------------------------------------------------------------- flags between CTAs of one grid
-// Release: every global write this thread has observed (its own, and those of the threads of its
-// CTA ordered before it by a barrier) is visible GPU-wide before the flag reads `v`.
-__device__ __forceinline__ void flag_release(unsigned* flag, unsigned v) {
-  asm volatile("fence.acq_rel.gpu;\n\tst.relaxed.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
-}
-// A relaxed GPU-scope read of a flag, issued early; if it already shows the value, fence_acq_rel_gpu
-// where the guarded data is used makes the pair an acquire.
-__device__ __forceinline__ unsigned flag_peek(const unsigned* flag) {
-  unsigned x;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(flag) : "memory");
-  return x;
-}
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-// Waits until *flag == v (acquire: what the releasing thread had observed is then visible to this
-// thread); gives up after kWaitLimitNs, ORs kStatusTimeout into *status and returns false.  Only
-// for flags set by CTAs of the same grid that are co-resident (a cooperative launch) and never
-// wait on the waiting CTA.
-__device__ __forceinline__ bool flag_wait(const unsigned* flag, unsigned v, unsigned* status) {
-  uint64_t t0 = 0;
-  for (int i = 0;; ++i) {
-    unsigned x;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(flag) : "memory");
-    if (x == v) return true;
-    if (i == 0) t0 = globaltimer_ns();
-    else if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      atomicOr(status, kStatusTimeout);
-      return false;
-    }
-    __nanosleep(128);
-  }
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -289,26 +251,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
          | ((uint32_t)(M >> 4) << 24);   // M / 16
 }
 
-// Instruction descriptor, kind::tf32: fp32 A/B read from shared memory at tf32 precision, both
-// K-major, fp32 accumulation.
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
-  return (1u << 4)                       // D format: f32
-         | (2u << 7)                     // A format: tf32
-         | (2u << 10)                    // B format: tf32
-         | ((uint32_t)(N >> 3) << 17)    // N / 8
-         | ((uint32_t)(M >> 4) << 24);   // M / 16
-}
-// D[tmem] (+)= A[smem] * B[smem]^T, fp32 operands at tf32 precision (one 8-deep K step: 32 bytes of
-// each operand row), issued by one thread.
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // D[tmem] (+)= A[smem] * B[smem]^T  (one 16-deep K step), issued by one thread.
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
@@ -407,11 +349,6 @@ __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint
 // Byte offset of element (row, col) of a bf16 tile stored as 64-column
 // blocks of [rows][64] with the 128-byte swizzle (16-byte chunk index XOR row%8);
 // a block is rows*128 bytes, and the tile base must be 1024-byte aligned.
-// Byte offset of fp32 element (row, col) in a K-major 128-byte-swizzled fp32 tile: panels of 32
-// columns (128-byte rows), `rows` rows per panel; 16-byte chunks of a row permuted by row & 7.
-__host__ __device__ __forceinline__ uint32_t sw128_off_f32(uint32_t row, uint32_t col, uint32_t rows) {
-  return (col >> 5) * rows * 128u + row * 128u + ((((col & 31u) >> 2) ^ (row & 7u)) << 4) + ((col & 3u) << 2);
-}
 __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t col, uint32_t rows) {
   return (col >> 6) * rows * 128u + row * 128u + ((((col & 63u) >> 3) ^ (row & 7u)) << 4) + ((col & 7u) << 1);
 }
