@@ -160,19 +160,24 @@ typedef struct la_decode_args {
  * the stream has finished.
  *
  * Gated-delta-rule prefill (bf16 inputs) has two schedules:
- *   - two kernels (the fastest): a chunk-parallel kernel leaves one record
- *     of 16,384 bytes per 64-token chunk of every (b,h) (the bf16 images of
- *     T diag(beta), T = (I + L)^{-1}, and of the chunk's causal queries
- *     against its keys), then a warp-specialized scan per (b,h) reads q, k,
- *     v and the record once and forms everything else;
- *     la_gdn_prefill_workspace_size returns what it needs (plus the segment
- *     scratch below when long sequences are split);
+ *   - records (the fastest): one record of 16,384 bytes per 64-token chunk
+ *     of every (b,h) (the bf16 images of T diag(beta), T = (I + L)^{-1}, and
+ *     of the chunk's causal queries against its keys), read once by a
+ *     warp-specialized scan per (b,h) that also reads q, k, v once and forms
+ *     everything else.  When the (b,h) pairs leave at least 16 SMs free and
+ *     sequences are not split, the records are formed in the scan's own
+ *     launch (a cooperative launch over every SM) by CTAs beside the scan
+ *     and handed over through one 4-byte flag per record; otherwise a
+ *     chunk-parallel kernel forms them first.  la_gdn_prefill_workspace_size
+ *     returns what it needs: the records, the flags (rounded up to 256
+ *     bytes), 4,352 bytes of launch scratch, plus the segment scratch below
+ *     when long sequences are split;
  *   - one kernel that walks the chunks of each (b,h) itself; it needs scratch
  *     only when it splits long sequences of few (b,h) pairs into segments
  *     (one 64 KiB fp32 map pair per segment but the last, one 64 KiB entry
  *     state per segment); la_gdn_prefill_workspace_size_min returns that
  *     (often 0).
- * la_gdn_prefill runs the two-kernel schedule when the workspace holds at
+ * la_gdn_prefill runs the records schedule when the workspace holds at
  * least la_gdn_prefill_workspace_size bytes, else the one-kernel schedule
  * when it holds at least la_gdn_prefill_workspace_size_min bytes, else fails
  * with LA_ERR_WORKSPACE.  Both compute the same result up to rounding. */
@@ -210,7 +215,7 @@ la_status la_gated_prefill(const la_gdn_prefill_args* args, void* workspace,
  *   - Limit: problems whose la_gdn_prefill_workspace_size_min exceeds
  *     16 MiB (16777216 bytes) are refused with LA_ERR_WORKSPACE before
  *     anything is launched; problems that need no scratch always run.  The
- *     two-kernel schedule runs when its records fit the array, otherwise
+ *     records schedule runs when its records fit the array, otherwise
  *     the one-kernel schedule.
  *   - Every GPU that loads the library holds the 16 MiB array until the
  *     process exits.

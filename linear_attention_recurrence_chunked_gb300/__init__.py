@@ -339,7 +339,7 @@ def la_gdn_prefill(q, k, v, alpha, beta, o=None, S_in=None, S_out=None, q_scale:
     q, k, v: [B,H,N,128] (fp32 or bf16); alpha, beta: fp32 [B,H,N];
     S: fp32 [B,H,128,128] (row = value index).  workspace: optional uint8
     device tensor; by default la_gdn_prefill_workspace_size bytes are
-    allocated (two-kernel schedule); a smaller one of at least
+    allocated (the records schedule); a smaller one of at least
     la_gdn_prefill_workspace_size_min bytes selects the one-kernel schedule."""
     return _gdn_family_prefill("la_gdn_prefill", q, k, v, alpha, beta, o, S_in, S_out, q_scale, out_dtype,
                                workspace, stream)

@@ -145,7 +145,7 @@ def test_decode_rejections(lib):
 
 
 def test_gdn_workspace_queries_and_rejection(lib):
-    rec = 16384  # two-kernel scan: bytes of the per-chunk record (T diag(beta) and P images) of one (b,h)
+    rec = 16384  # records schedule: bytes of the per-chunk record (T diag(beta) and P images) of one (b,h)
     # a 4-byte ready flag per record, rounded up to 256 bytes, and the launch's placement scratch (an
     # arrival counter and a word per SM id up to 1024, rounded up to 256 bytes)
     flags = lambda n: (4 * n + 255) // 256 * 256 + 4352

@@ -68,7 +68,7 @@ def test_gated_differs_from_delta_rule():
 def test_gated_segments_and_both_schedules(N):
     """Few heads and a long sequence: sequence segments (the segment maps of
     a scalar gate are pure decays); the one-kernel schedule (minimum
-    workspace) must agree with the two-kernel one and both with the oracle."""
+    workspace) must agree with the records schedule and both with the oracle."""
     dev = cuda_device()
     inp = synthetic.gdn_inputs(1, 2, N, dtype=torch.bfloat16, seed=830 + N)
     g = torch.Generator().manual_seed(N)

@@ -199,7 +199,7 @@ def test_gdn_sequence_segments_match_oracle(N, inplace):
 
 @pytest.mark.parametrize("B,H,N,seg", [(1, 3, 1000, False), (2, 2, 257, False), (1, 2, 6144, True)])
 def test_gdn_two_schedules_agree(B, H, N, seg):
-    """The two-kernel schedule (chunk-local records, then the state chain) and
+    """The records schedule (chunk records, then the state chain) and
     the one-kernel scan compute the same chunk form; they differ only in
     where roundings fall (the chain keeps S / sigma with a running decay
     sigma, and rounds q_scale diag(gamma) Q to bf16), so they must agree far
@@ -231,7 +231,7 @@ def test_gdn_two_schedules_agree(B, H, N, seg):
 
 
 def test_gdn_workspace_between_min_and_full_runs_one_kernel_schedule():
-    """A workspace one byte short of the two-kernel need still runs (one-kernel
+    """A workspace one byte short of the records schedule's need still runs (one-kernel
     schedule); a misaligned one is refused without a launch."""
     dev = cuda_device()
     inp = synthetic.gdn_inputs(1, 2, 300, dtype=torch.bfloat16, seed=71)

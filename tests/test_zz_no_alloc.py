@@ -57,7 +57,7 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
         need_min = la.la_gdn_prefill_workspace_size_min(*args)
         need = la.la_gdn_prefill_workspace_size(*args)
         # segment scratch and per-chunk records both fit the fixed array, so both entry
-        # points run the same two-kernel schedule with segments
+        # points run the same records schedule with segments
         assert 0 < need_min <= need <= 16 << 20
         refs.append(la.la_gdn_prefill(*args))  # existing entry point, caller workspace
     outs = [(torch.empty_like(o), torch.empty_like(S)) for o, S in refs]
