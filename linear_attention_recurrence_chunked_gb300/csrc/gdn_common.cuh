@@ -126,10 +126,11 @@ struct GdnTask {
   // kWhole with the chunk records formed in the same launch: CTAs n_scan.. (by placement rank) run
   // the inversion and set ready[record] = 1 once a record is written (null: the records are complete
   // at launch); place: the launch's zeroed placement scratch (an arrival counter, then one word per
-  // SM id)
+  // SM id); progress: zeroed, one word
   int n_scan;
   unsigned* ready;
   unsigned* place;
+  unsigned* progress;  // chunks whose copies all scans together have issued (a pacing hint)
 };
 
 // The (b,h), segment, token range and entry/exit states of one CTA of `task`.

@@ -400,28 +400,39 @@ gdn_tinv_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 // order (record i: chunk i / BH of pair i % BH), so that every (b,h) gets its early chunks first, as
 // its scan CTA wants them.  Per record the steps of gdn_tinv_kernel, with the [K;Q] tile in two
 // stages (the copy of the record after next goes in once T, formed over the current stage, is dead)
-// and the two images stored straight from registers to the record.  Lane 0 of warp 16 + g serves
-// pipeline g off its critical path: it issues the pipeline's copies and, once the workers report a
+// and the two images stored straight from registers to the record.  Warp 16 + g serves pipeline g
+// off its critical path: its lane 0 issues the pipeline's copies and, once the workers report a
 // record written, releases the record's flag (the GPU-scope fence that release needs waits for the
-// record's stores, so no worker waits on it); the scan's copy issuer acquires the flag before it
-// copies the record.
+// record's stores, so no worker waits on it); the whole warp forms the gate tables two records
+// ahead, into the buffer of the record just written.  The scan's copy issuer acquires a flag before
+// it copies the record.
 // One pipeline's shared memory: the two [K;Q] stages (TA and TB of a record over its dead stage), LT,
-// SMt and the gate tables.  The A operands of the inversion (LT, TA) have 8 KB of shared memory of
+// SMt and two gate-table buffers.  The A operands of the inversion (LT, TA) have 8 KB of shared memory of
 // the CTA after them (pipeline 1's LT: its SMt, gate tables and the unused end of the allocation).
 constexpr uint32_t kIGOffLT = 65536;
 constexpr uint32_t kIGOffSM = kIGOffLT + 2 * kPanel;
-constexpr uint32_t kIGOffGate = kIGOffSM + 4096;
-constexpr uint32_t kIGrp = kIGOffGate + 1024;
+constexpr uint32_t kIGOffGate = kIGOffSM + 4096;  // two gate-table buffers (records k, k+1 by parity)
+constexpr uint32_t kIGrp = kIGOffGate + 2048;
 static_assert(kIGrp % 1024 == 0, "one inversion pipeline's shared memory");
+
+// Pacing: the scan re-reads the [K;Q] tiles the formers have just loaded and the records they have
+// just written, from L2 while the formers are at most a few chunks ahead of it.  Measured at
+// B=4 H=16 N=16384, formers alone 0.514 ms and the scan alone 0.568 ms gave 0.637 ms together
+// without pacing (slower formers gave 0.611).  So the serving lane holds the copy of a record of
+// chunk m while the scans together have issued the copies of fewer than (m - kPaceChunks) BH
+// chunks (one counter for all scans: a wait on the scan of one pair would hold the other pairs'
+// records behind it), for at most kPaceLimitNs: a hint, which no result depends on.
+constexpr unsigned kPaceChunks = 8;
+constexpr uint64_t kPaceLimitNs = 100000;
 
 __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
                                                const GdnPrefillLaunch& a, int nch, int n_ctas, int cta,
-                                               uint8_t* sm, uint8_t* rec_out, unsigned* ready, unsigned* status) {
+                                               uint8_t* sm, uint8_t* rec_out, unsigned* ready, const unsigned* progress,
+                                               unsigned* status) {
   // per pipeline: [K;Q] landed in stage 0, in stage 1; MMA done; record written (one arrival per
-  // worker warp); record released (the serving lane)
-  __shared__ uint64_t ibar[2][5];
+  // worker warp); record released (the serving lane); gate tables in buffer 0, in buffer 1 written
+  __shared__ uint64_t ibar[2][7];
   __shared__ uint32_t itmem_sh;
-  __shared__ float icarry[2];
   const int tid = threadIdx.x, warp = tid >> 5;
   const bool worker = warp < 16;
   const int g = worker ? warp >> 3 : warp - 16;  // the pipeline this warp works in or serves
@@ -433,7 +444,7 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
   const uint32_t gbase = smem_u32(gsm);
   uint8_t* LT = gsm + kIGOffLT;
   uint8_t* SMt = gsm + kIGOffSM;
-  float* gate = reinterpret_cast<float*>(gsm + kIGOffGate);
+  float* gates = reinterpret_cast<float*>(gsm + kIGOffGate);  // buffer p at gates + 256 p
   const uint32_t bar_done = smem_u32(&ibar[g][3]), bar_rel = smem_u32(&ibar[g][4]);
 
   if (tid == 0) {
@@ -441,6 +452,8 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
       for (int j = 0; j < 3; ++j) mbar_init(smem_u32(&ibar[p][j]), 1);
       mbar_init(smem_u32(&ibar[p][3]), 8);
       mbar_init(smem_u32(&ibar[p][4]), 1);
+      mbar_init(smem_u32(&ibar[p][5]), 1);
+      mbar_init(smem_u32(&ibar[p][6]), 1);
     }
     fence_mbar_init();
     tma_prefetch_desc(tmap_k);
@@ -464,30 +477,12 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
     int64_t bh_c = first % BH, ch_c = first / BH;
     int64_t bh_n = bh_c + dbh, ch_n = ch_c + dch;
     if (bh_n >= BH) bh_n -= BH, ++ch_n;
-    // alpha and beta of token lt of a record as stored (threads 0..63; padded tokens: alpha = 1,
-    // beta = 0); loaded a record ahead and taken apart only when that record starts
-    auto gates_raw = [&](int64_t i, int64_t bh, int64_t ch, float& al, float& bt) {
-      al = 1.f;
-      bt = 0.f;
-      if (lt < kC && i < nrec) {
-        const int64_t t = ch * kC + lt;
-        const int b = (int)(bh / a.H), h = (int)(bh - (int64_t)b * a.H);
-        if (t < a.N) {
-          al = a.alpha[b * a.a_sb + h * a.a_sh + t];
-          bt = a.beta[b * a.b_sb + h * a.b_sh + t];
-        }
-      }
-    };
-    float al_n, bt_n;
-    gates_raw(first, bh_c, ch_c, al_n, bt_n);
     bool ok = true, mma_pending = false;
-    uint32_t mph = 0;  // next phase parity of bar_mma (five commits a record with the inversion)
+    uint32_t mph = 0;  // next phase parity of bar_mma (three commits a record with the inversion)
     int k = 0;
     for (int64_t i = first; i < nrec; i += stride, ++k) {
       const int st = k & 1;
-      const float lg = logf(al_n), bt = bt_n;
-      gates_raw(i + stride, bh_n, ch_n, al_n, bt_n);  // the next record's gates load during this one
-      gate_tables(lt, lg, bt, gate, &icarry[g], sync);
+      const float* gate = gates + 256 * st;
       ok = mbar_wait(smem_u32(&ibar[g][st]), (uint32_t)((k >> 1) & 1), status);
       if (named_bar_or(1 + g, 256, !ok)) break;
       if (lt == 0) {
@@ -498,6 +493,8 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
       mma_pending = true;
       ok = mbar_wait(bar_mma, mph, status);
       mph ^= 1u;
+      // the gate tables of this record, formed by the serving warp
+      ok = mbar_wait(smem_u32(&ibar[g][5 + st]), (uint32_t)((k >> 1) & 1), status) && ok;
       if (named_bar_or(1 + g, 256, !ok)) break;
       mma_pending = false;
       tc_fence_after();
@@ -520,14 +517,15 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
         if (k > 0 && !mbar_wait(bar_rel, (uint32_t)((k - 1) & 1), status)) ok = false;
         mbar_arrive(bar_done);
       }
-      sync();  // gate tables and T are rewritten by the next record
+      sync();  // T and the TMEM columns are rewritten by the next record
       bh_c = bh_n, ch_c = ch_n;
       bh_n += dbh, ch_n += dch;
       if (bh_n >= BH) bh_n -= BH, ++ch_n;
     }
     if (lt == 0 && !ok && mma_pending) mbar_wait(bar_mma, mph ^ 1u, status);
-  } else if ((tid & 31) == 0) {
-    // the serving lane of pipeline g: copies and flag releases
+  } else {
+    // the serving warp of pipeline g: copies and flag releases (lane 0), gate tables (the warp)
+    const int lane = tid & 31;
     int issued[2] = {0, 0};
     auto load = [&](int64_t i, int st) {
       const int64_t bh = i % BH;
@@ -540,23 +538,82 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
       tma_load_4d(dst + 24576, tmap_q, 64, t0, h, b, bar);
       ++issued[st];
     };
-    if (first < nrec) load(first, 0);
-    if (first + stride < nrec) load(first + stride, 1);
+    // gate tables of record i into buffer p, then its arrival: lane l takes tokens l and 32 + l and
+    // runs the same two 32-lane scans, carry and exponentials as gate_tables (the same bits)
+    auto gates_of = [&](int64_t i, int p) {
+      const int64_t bh = i % BH, t0 = (i / BH) * kC;
+      const int b = (int)(bh / a.H), h = (int)(bh % a.H);
+      float lg[2], bt[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int64_t t = t0 + lane + 32 * e;
+        float al = 1.f;
+        bt[e] = 0.f;
+        if (t < a.N) {
+          al = a.alpha[b * a.a_sb + h * a.a_sh + t];
+          bt[e] = a.beta[b * a.b_sb + h * a.b_sh + t];
+        }
+        lg[e] = logf(al);
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const float y = __shfl_up_sync(kFullMask, lg[e], off);
+          if (lane >= off) lg[e] += y;
+        }
+      }
+      lg[1] += __shfl_sync(kFullMask, lg[0], 31);
+      float* gt = gates + 256 * p;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int t = lane + 32 * e;
+        gt[t] = lg[e];
+        gt[kC + t] = bt[e];
+        gt[2 * kC + t] = __expf(lg[e]);
+        gt[3 * kC + t] = __expf(-lg[e]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&ibar[g][5 + p]));
+    };
+    if (lane == 0) {
+      if (first < nrec) load(first, 0);
+      if (first + stride < nrec) load(first + stride, 1);
+    }
+    // lane 0: hold record i while the scans together are more than kPaceChunks chunks behind it
+    auto pace = [&](int64_t i) {
+      const int64_t m = i / BH;
+      if (m <= (int64_t)kPaceChunks) return;
+      const uint64_t need = (uint64_t)(m - kPaceChunks) * (uint64_t)BH;
+      const uint64_t t0 = globaltimer_ns();
+      for (;;) {
+        unsigned v;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(progress) : "memory");
+        if ((uint64_t)v >= need || globaltimer_ns() - t0 > kPaceLimitNs) return;
+        __nanosleep(256);
+      }
+    };
+    if (first < nrec) gates_of(first, 0);
+    if (first + stride < nrec) gates_of(first + stride, 1);
     bool ok = true;
     int k = 0;
     for (int64_t i = first; i < nrec; i += stride, ++k) {
       ok = mbar_wait(bar_done, (uint32_t)(k & 1), status);
       if (!ok) break;
-      if (i + 2 * stride < nrec) load(i + 2 * stride, k & 1);  // the workers are done with T there
-      const int64_t bh = i % BH, r = bh * nch + i / BH;
-      flag_release(ready + r, 1u);
-      mbar_arrive(bar_rel);
+      if (lane == 0) {
+        if (i + 2 * stride < nrec) {
+          pace(i + 2 * stride);
+          load(i + 2 * stride, k & 1);  // the workers are done with T there
+        }
+        const int64_t bh = i % BH, r = bh * nch + i / BH;
+        flag_release(ready + r, 1u);
+        mbar_arrive(bar_rel);
+      }
+      if (i + 2 * stride < nrec) gates_of(i + 2 * stride, k & 1);  // and with this buffer
     }
-    if (!ok) {
+    if (!ok && lane == 0) {
       // let this pipeline's own copies finish (bounded) before the CTA exits
       for (int st = 0; st < 2; ++st)
         if (issued[st] > 0) mbar_wait(smem_u32(&ibar[g][st]), (uint32_t)((issued[st] - 1) & 1), status);
     }
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
@@ -573,7 +630,7 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
 // falls back to blockIdx.x, consistently, if the SM ids are out of range or shared, or the barrier
 // expires (the status then reports it).
 constexpr unsigned kMaxSmIds = 1024;
-constexpr size_t kPlaceBytes = ((1 + kMaxSmIds) * sizeof(unsigned) + 255) & ~size_t(255);
+constexpr size_t kPlaceBytes = ((2 + kMaxSmIds) * sizeof(unsigned) + 255) & ~size_t(255);  // + the pacing counter
 
 __device__ __forceinline__ int placement_rank(unsigned* place, unsigned* status) {
   __shared__ int rank_sh;
@@ -680,7 +737,7 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
   const int cta = task.ready != nullptr ? placement_rank(task.place, status) : (int)blockIdx.x;
   if (task.ready != nullptr && cta >= task.n_scan) {
     inversion_role(&tmap_q, &tmap_k, a, nch_total, (int)gridDim.x - task.n_scan, cta - task.n_scan, sm, rec,
-                   task.ready, status);
+                   task.ready, task.progress, status);
     return;
   }
   __shared__ uint64_t bar_k[kKSlots];  // K and the T2 image landed in their slot
@@ -1003,6 +1060,8 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
           tma_load_4d(kt + kKOffK + 8192, &tmap_k, 64, t0, h, b, bar);
           bulk_load(kt + kKOffT2, rec + (rec0 + m) * kRec + kRecT2, 8192, bar);
           ++nk;
+          if (flags != nullptr)  // for the formers' pacing: one more chunk issued
+            asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(task.progress) : "memory");
         }
         if (!ZV) {
           if (m >= 2) ok = wait(&bar_vfree[m & 1], (uint32_t)(((m - 2) >> 1) & 1));
@@ -1297,9 +1356,10 @@ gdn_scan_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constan
 size_t records_bytes(int64_t BH, int64_t nch) { return (size_t)(BH * nch) * kRec; }
 // one ready flag per record, for the launch that forms its records itself
 // plus the placement scratch of that launch
-size_t flags_bytes(int64_t BH, int64_t nch) {
-  return (((size_t)(BH * nch) * sizeof(unsigned) + 255) & ~size_t(255)) + kPlaceBytes;
-}
+// (whose first word counts the chunks all scans have issued, after the placement words), the flags
+// rounded up to 256 bytes
+size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
+size_t flags_bytes(int64_t BH, int64_t nch) { return round256((size_t)(BH * nch) * sizeof(unsigned)) + kPlaceBytes; }
 
 // The fewest inversion CTAs worth a launch that forms its own records.
 constexpr int kMinInversionCtas = 16;
@@ -1351,8 +1411,9 @@ cudaError_t launch_scan_typed(const GdnPrefillLaunch& a, void* ws, unsigned* sta
     // one launch: CTAs 0..BH-1 scan, the rest of the GPU forms the records beside them
     cudaError_t e = cudaMemsetAsync(ready, 0, flags_bytes(BH, nch), stream);
     if (e != cudaSuccess) return e;
-    unsigned* place = ready + (flags_bytes(BH, nch) - kPlaceBytes) / sizeof(unsigned);
-    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr, (int)BH, ready, place};
+    unsigned* place = ready + round256((size_t)(BH * nch) * sizeof(unsigned)) / sizeof(unsigned);
+    unsigned* progress = place + 1 + kMaxSmIds;
+    const GdnTask task{kWhole, 1, a.N, nullptr, nullptr, (int)BH, ready, place, progress};
     return launch_cooperative(scan, dim3((unsigned)n_co), dim3(kScanThreads), kSSmemAlloc, stream, mq, mk, mv, a,
                               task, (int)nch, recT, status);
   }

@@ -146,21 +146,21 @@ def test_decode_rejections(lib):
 
 def test_gdn_workspace_queries_and_rejection(lib):
     rec = 16384  # records schedule: bytes of the per-chunk record (T diag(beta) and P images) of one (b,h)
-    # a 4-byte ready flag per record, rounded up to 256 bytes, and the launch's placement scratch (an
-    # arrival counter and a word per SM id up to 1024, rounded up to 256 bytes)
-    flags = lambda n: (4 * n + 255) // 256 * 256 + 4352
+    # a 4-byte ready flag per record, rounded up to 256 bytes, and the launch's scratch (an arrival
+    # counter, a word per SM id up to 1024 and a progress counter, rounded up to 256 bytes)
+    flags = lambda n, bh: (4 * n + 255) // 256 * 256 + 4352
     big = gdn_args(B=1, H=16, N=1 << 20)
     need_min = lib.la_gdn_prefill_workspace_size_min(ctypes.byref(big))
     need = lib.la_gdn_prefill_workspace_size(ctypes.byref(big))
     # few heads and a long sequence plan sequence segments, which need scratch
     assert need_min > 0
-    assert need == 16 * (1 << 14) * rec + need_min + flags(16 * (1 << 14))
+    assert need == 16 * (1 << 14) * rec + need_min + flags(16 * (1 << 14), 16)
     # short sequences or many heads need no segment scratch, only the records
     for B, H, N in ((4, 16, 16384), (1, 2, 64), (1, 1, 65)):
         a = gdn_args(B=B, H=H, N=N)
         assert lib.la_gdn_prefill_workspace_size_min(ctypes.byref(a)) == 0
         nrec = B * H * ((N + 63) // 64)
-        assert lib.la_gdn_prefill_workspace_size(ctypes.byref(a)) == nrec * rec + flags(nrec)
+        assert lib.la_gdn_prefill_workspace_size(ctypes.byref(a)) == nrec * rec + flags(nrec, B * H)
     # fp32 inputs run token-serial kernels without scratch
     f32 = gdn_args(set={"in_dtype": la.LA_DTYPE_F32})
     assert lib.la_gdn_prefill_workspace_size(ctypes.byref(f32)) == 0
