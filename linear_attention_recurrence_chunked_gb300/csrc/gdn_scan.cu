@@ -418,11 +418,14 @@ static_assert(kIGrp % 1024 == 0, "one inversion pipeline's shared memory");
 // Pacing: the scan re-reads the [K;Q] tiles the formers have just loaded and the records they have
 // just written, from L2 while the formers are at most a few chunks ahead of it.  Measured at
 // B=4 H=16 N=16384, formers alone 0.514 ms and the scan alone 0.568 ms gave 0.637 ms together
-// without pacing (slower formers gave 0.611).  So the serving lane holds the copy of a record of
-// chunk m while the scans together have issued the copies of fewer than (m - kPaceChunks) BH
-// chunks (one counter for all scans: a wait on the scan of one pair would hold the other pairs'
-// records behind it), for at most kPaceLimitNs: a hint, which no result depends on.
-constexpr unsigned kPaceChunks = 8;
+// without pacing, 0.599 ms with the formers held within 8 chunks of the scans (0.616 within 12).
+// So the serving lane holds the copy of a record of chunk m while the scans together have issued the
+// copies of fewer than (m - lead) BH chunks: one counter for all scans, since a wait on the scan of
+// one pair would hold the other pairs' records behind it.  A pipeline's consecutive records lie
+// stride / BH chunks apart and the lane paces the record two ahead of the one being formed, so a
+// lead under about three such spacings waits on records that are not formed yet (a lead of 2 to 5
+// at that shape took 9 ms); lead = ceil(3 stride / BH) (9 there).  The wait is a hint, which no
+// result depends on, and gives up after kPaceLimitNs.
 constexpr uint64_t kPaceLimitNs = 100000;
 
 __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const CUtensorMap* tmap_k,
@@ -577,11 +580,12 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
       if (first < nrec) load(first, 0);
       if (first + stride < nrec) load(first + stride, 1);
     }
-    // lane 0: hold record i while the scans together are more than kPaceChunks chunks behind it
+    // lane 0: hold record i while the scans together are more than `lead` chunks behind it
+    const int64_t lead = (3 * stride + BH - 1) / BH;
     auto pace = [&](int64_t i) {
       const int64_t m = i / BH;
-      if (m <= (int64_t)kPaceChunks) return;
-      const uint64_t need = (uint64_t)(m - kPaceChunks) * (uint64_t)BH;
+      if (m <= lead) return;
+      const uint64_t need = (uint64_t)(m - lead) * (uint64_t)BH;
       const uint64_t t0 = globaltimer_ns();
       for (;;) {
         unsigned v;
@@ -598,13 +602,14 @@ __device__ __forceinline__ void inversion_role(const CUtensorMap* tmap_q, const 
       ok = mbar_wait(bar_done, (uint32_t)(k & 1), status);
       if (!ok) break;
       if (lane == 0) {
+        // release this record first: the scans may need it before the pacing lets the next copy go
+        const int64_t bh = i % BH, r = bh * nch + i / BH;
+        flag_release(ready + r, 1u);
+        mbar_arrive(bar_rel);
         if (i + 2 * stride < nrec) {
           pace(i + 2 * stride);
           load(i + 2 * stride, k & 1);  // the workers are done with T there
         }
-        const int64_t bh = i % BH, r = bh * nch + i / BH;
-        flag_release(ready + r, 1u);
-        mbar_arrive(bar_rel);
       }
       if (i + 2 * stride < nrec) gates_of(i + 2 * stride, k & 1);  // and with this buffer
     }
