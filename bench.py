@@ -104,7 +104,7 @@ def kernel_sources_sha(files):
 # the "intra-chunk GEMM" work the tensor cores run:
 #  GDN (C = 64, d_k = d_v = 128): [K;Q] K^T, W = T diag(beta gamma) K, U~ = T diag(beta) V, P U (5 of
 #      2*64*64*128) and W S0^T, Q S0^T, the state update U^T K (3 of 2*64*128*128); the triangular inverse
-#      T runs on the CUDA cores and is not counted.
+#      T (its two 64-level products run as tf32 MMAs, the rest on the CUDA cores) is not counted.
 #  scalar gate (same chunk): Q K^T, P (beta V) and Q S0^T, the update (no W, no U~, no inverse).
 #  BASED (C = 128, d' = 16, the 153-wide compact feature basis, d_v = 64 plus the normaliser column):
 #      Q K^T 2*128*128*16, readout phi(Q) [S | z] 2*128*153*65, intra-chunk P [V | 1] 2*128*128*65,
@@ -505,10 +505,12 @@ def other_paths(args, la, dev, stream, flush, pk, seed_off, ws, only=None):
         for _ in range(reps):
             t.run(step)
         ms = max_over_ranks(t.total_ms(), ws) / reps
-        # the chunk-local kernel, then the chain; sequences split into segments run the chain as
-        # three kernels (maps, combine, outputs)
+        # one launch when the (b,h) pairs leave at least 16 SMs for forming the records beside the scan
+        # (one CTA per SM); else the chunk-parallel inversion kernel, then the scan; sequences split
+        # into segments run the scan as three kernels (maps, combine, outputs) after the inversion
         segments = la.la_gdn_prefill_workspace_size_min(x["q"], x["k"], x["v"], x["alpha"], x["beta"]) > 0
-        per_call = 4 if segments else KERNELS_PER_CALL["gdn_prefill"]
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        per_call = 4 if segments else (1 if w.B * w.H + 16 <= sms else KERNELS_PER_CALL["gdn_prefill"])
         launches += reps * per_call
         byts = BYTES_PER_TOKEN_HEAD["gdn_prefill"] * w.B * w.H * N + STATE_BYTES["gdn"] * w.B * w.H
         r = roofline(byts, ms, pk["hbm_gbs"], ncu_traffic(name) if N == w.N else None)
