@@ -1,5 +1,6 @@
-// gdn_scan.cu -- the chunked gated-delta-rule prefill as a chunk-parallel
-// inversion kernel and a warp-specialized scan that reads q, k, v once.
+// gdn_scan.cu -- the chunked gated-delta-rule prefill: per-chunk records that
+// hold what needs the triangular inverse, and a warp-specialized scan that
+// reads q, k, v and the records once.
 //
 // Chunk form (gdn_common.cuh; NoteBank Sec. 2 Eq. (1), the state carried
 // across chunk boundaries as in NoteBank Sec. 3.2), chunk of 64 tokens with
@@ -9,12 +10,16 @@
 //   O  = q_scale diag(gamma) (Q S0^T + P U),  P_rj = (q_r . k_j) / gamma_j  (j <= r)
 //   S_C = gamma_C S0 + U^T diag(gamma_C / gamma) K
 //
-// Kernel 1 (gdn_tinv_kernel, one CTA per chunk over the whole GPU) forms what
-// needs the inversion or the chunk's queries against its keys, neither of which
-// depends on the state: the bf16 tiles T2 = T diag(beta) and P of every chunk
-// (16 KB, the images the scan's MMAs read), written to the caller's workspace.
+// Records: what needs the inversion or the chunk's queries against its keys,
+// neither of which depends on the state: the bf16 tiles T2 = T diag(beta) and P
+// of every chunk (16 KB, the images the scan's MMAs read), in the caller's
+// workspace.  T by doubling, its 64-level block as tcgen05 tf32 MMAs
+// (invert_T_tc).  They are formed either by kernel 1 (gdn_tinv_kernel, one CTA
+// per chunk over the whole GPU) before the scan, or, when the (b,h) pairs leave
+// SMs free and sequences are not split, by CTAs of the scan's own cooperative
+// launch beside it (inversion_role), handed over through per-record flags.
 //
-// Kernel 2 (gdn_scan_kernel, one CTA per (b,h) or sequence segment) walks the
+// The scan (gdn_scan_kernel, one CTA per (b,h) or sequence segment) walks the
 // chunks with the fp32 state in tensor memory and does everything else on
 // the tcgen05 tensor cores, from tiles it loads once:
 //   w:  W^T = K^T (T2 diag gamma)^T                            (chunk-local)
@@ -33,9 +38,8 @@
 // the state after each update; warps 8-11 run the chunk-local passes a chunk
 // ahead (gates, T2 diag gamma, W^T from tensor memory); warps 12-15 drain
 // the outputs; warp 16 issues every MMA and warp 17 every copy, each as soon
-// as its inputs are ready.  Workers report progress through counters the
-// issuers read with one round of loads; waits on copies and MMAs are
-// mbarriers, and every wait is bounded.
+// as its inputs are ready.  Hand-offs between them are mbarriers with one
+// arrival per warp, and every wait is bounded.
 #include <mutex>
 
 #include "gdn_common.cuh"
