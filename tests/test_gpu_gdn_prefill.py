@@ -119,6 +119,30 @@ def test_records_formed_beside_the_scan_match_the_inversion_kernel(fn):
     assert rel_err(to_np(S_all[:, heads]), ref["S"]) < TOL[torch.bfloat16]
 
 
+def test_one_launch_at_its_largest_pair_count():
+    """The one-launch schedule runs while the (b,h) pairs leave at least 16 of the
+    GPU's SMs for forming the records: at that limit only 16 record-forming CTAs
+    serve every pair, and their pacing lead (three times their record spacing)
+    is a single chunk.  Its results are the bits of the same pairs run with the
+    records from the chunk-parallel kernel (one more pair than the limit), and two
+    heads meet the oracle."""
+    dev = cuda_device()
+    limit = torch.cuda.get_device_properties(dev).multi_processor_count - 16
+    inp = synthetic.gdn_inputs(1, limit + 1, 1000, dtype=torch.bfloat16, seed=53)
+    x = {n: inp[n].to(dev) for n in NAMES}
+    o_two, S_two = la.la_gdn_prefill(*(x[n] for n in NAMES))          # limit + 1 pairs: two kernels
+    o_one, S_one = la.la_gdn_prefill(*(x[n][:, :limit].contiguous() for n in NAMES))  # one launch
+    torch.cuda.synchronize()
+    assert la.la_device_status() == la.LA_OK
+    assert torch.equal(o_two[:, :limit], o_one) and torch.equal(S_two[:, :limit], S_one)
+    heads = [0, limit - 1]
+    sub = {n: inp[n][:, heads] for n in NAMES}
+    ref = oracle.gdn(*(synthetic.to_oracle(sub[n]) for n in ("q", "k", "v")), sub["alpha"].numpy(),
+                     sub["beta"].numpy())
+    assert rel_err(to_np(o_one[:, heads]), ref["o"]) < TOL[torch.bfloat16]
+    assert rel_err(to_np(S_one[:, heads]), ref["S"]) < TOL[torch.bfloat16]
+
+
 def test_gdn_empty_sequence_passes_state():
     dev = cuda_device()
     z = torch.zeros((1, 2, 0, 128), dtype=torch.bfloat16, device=dev)
