@@ -191,7 +191,12 @@ la_status la_based_prefill(const la_based_prefill_args* args, void* workspace,
                            size_t workspace_bytes, void* stream);
 
 /* Chunked gated-delta-rule prefill (NoteBank Sec. 2 Eq. (1); chunks carry
- * the state across boundaries as in NoteBank Sec. 3.2). */
+ * the state across boundaries as in NoteBank Sec. 3.2).  When the records
+ * schedule forms its records inside the scan's launch (see the workspace
+ * notes above), that launch is cooperative and places one CTA on every SM of
+ * the device: it starts once all SMs are free and holds them until it ends,
+ * so it does not overlap with the caller's kernels on other streams.  Its
+ * CTAs wait on one another only through bounded waits (LA_ERR_TIMEOUT). */
 la_status la_gdn_prefill(const la_gdn_prefill_args* args, void* workspace,
                          size_t workspace_bytes, void* stream);
 
